@@ -1,0 +1,360 @@
+#!/usr/bin/env python
+"""Throughput of GDN chunked prefill (forward + backward) on GB300.
+
+One step = one pass of the whole path over one batch of seeded synthetic
+input: forward (prep, state walk with output, intra-card sequence-parallel
+maps and scan) and backward (recomputed states, reverse gradient walk,
+chunk-local gradients).  Default workload: the edge / TP8 prefill shape
+(B=1, T=8192, H=8, K=V=128, bf16 q/k/v, fp32 g/beta/state, sequence
+parallelism forced).  Prints one JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+`--impl reference` times the fp64 CPU oracle (the only reference this method
+has here) on a bounded sample of the same workload.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN chunked-prefill tokens/s (fwd; fwd+bwd) on 1 GB300 + % of roofline"
+CHUNK = 64
+L2_BYTES = 129 * 2 ** 20
+
+
+# ------------------------------------------------------------------ algorithmic work
+def flops_per_token_head(K, V, part):
+    """Chunk-form FLOPs per token and head (C = 64, masked triangles at half):
+    fwd = 3CK + 2CV + C^2/3 + 6KV ; bwd = 12KV + 6CK + 4CV + 2C^2/3."""
+    C = CHUNK
+    if part == "fwd":
+        return 3 * C * K + 2 * C * V + C * C / 3 + 6 * K * V
+    return 12 * K * V + 6 * C * K + 4 * C * V + 2 * C * C / 3
+
+
+def bytes_per_token_head(K, V, e, part):
+    """Inputs read once, outputs written once.  fwd: q, k, v, g, beta, o.
+    bwd: q, k, v, g, beta, dO in; dq, dk, dv (fp32), dg, dbeta out."""
+    if part == "fwd":
+        return e * (2 * K + V) + 8 + e * V
+    return e * (2 * K + V) + 8 + e * V + 4 * (2 * K + V) + 8
+
+
+# Per-kernel algorithmic FLOPs per token-head processed (the kernel's share
+# of the chunk form) -- used for the roofline of the dominant kernel.
+def kernel_flops_per_token_head(name, K, V):
+    C = CHUNK
+    table = {
+        "simt_prep": 2 * C * K + C * V + C * C / 3,
+        "simt_walk_out": 6 * K * V + C * K + C * V,
+        "simt_walk_states": 4 * K * V,
+        "simt_walk_map": 4 * K * (K + V),
+        "simt_dwalk_out": 6 * K * V + C * K + C * V,
+        "simt_dwalk_map": 4 * K * (K + V) + C * K + C * V,
+        "simt_local_grad": 6 * K * V + 6 * C * K + 3 * C * V + 2 * C * C / 3,
+    }
+    return table.get(name)
+
+
+FP32_LANES_PER_SM = 128
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id=None):
+        self.rows = []
+        self.proc = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if gpu_id is not None:
+            cmd[1:1] = ["-i", str(gpu_id)]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) == 8:
+                self.rows.append(parts)
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if not self.rows:
+            return None
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in self.rows for n, v in zip(names, r[4:]) if v == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(self.rows)}
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_sample(p, heads, reps_min_s=0.0):
+    """fp64 oracle forward + backward on the given heads of problem p.
+    Returns (seconds per pass, threads used, token-heads per pass)."""
+    import oracle
+    sub = p.heads(heads)
+    threads = min(oracle.max_threads(), len(heads) * sub.N)
+    t0 = time.perf_counter()
+    passes = 0
+    while True:
+        oracle.fwd(sub.q, sub.k, sub.v, sub.g, sub.beta, h0=sub.h0, cu_seqlens=sub.cu_seqlens,
+                   nthreads=threads)
+        oracle.bwd(sub.q, sub.k, sub.v, sub.g, sub.beta, do=sub.do, h0=sub.h0, dht=sub.dht,
+                   cu_seqlens=sub.cu_seqlens, nthreads=threads)
+        passes += 1
+        if time.perf_counter() - t0 >= reps_min_s:
+            break
+    dt = (time.perf_counter() - t0) / passes
+    return dt, threads, sub.B * sub.T * len(heads)
+
+
+# ------------------------------------------------------------------ main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="edge")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_ours(args, rank, world, local)
+
+
+def workload_problem(name):
+    import gdn_synth
+    return gdn_synth.make(name)
+
+
+def config_of(p, name):
+    m = p.meta
+    return {"workload": f"{name}: B={p.B} T={p.T} H={p.H} K={p.K} V={p.V} "
+                        f"{m['dtype']} q/k/v, fp32 g/beta/state, cp={m['cp']}, fwd+bwd",
+            "global_batch": p.B, "seq_len": p.T, "heads": p.H, "parallelism": "replicas",
+            "l2_flush_between_steps": True}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    p = workload_problem(args.workload)
+    heads = list(range(p.H))
+    for _ in range(args.warmup):
+        oracle_sample(p, heads[:1])
+    times = []
+    threads = tokens_heads = None
+    for _ in range(args.steps):
+        dt, threads, tokens_heads = oracle_sample(p, heads)
+        times.append(dt)
+    ms = 1e3 * statistics.mean(times)
+    tok = tokens_heads / p.H
+    value = tok / (ms / 1e3)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_of(p, args.workload),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads,
+                             "kind": "oracle",
+                             "sample": f"fp64 oracle fwd+bwd over all {p.H} heads of the "
+                                       f"{args.workload} workload per step"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    import gated_deltanet_linear_bwd_gb300 as gdn
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except OSError:
+        pass
+
+    p = workload_problem(args.workload)
+    cp = p.meta["cp"]
+    d = p.to(dev)
+    e_in = 2 if p.meta["dtype"] == "bf16" else 4
+    tokens = p.B * p.T
+    stream = torch.cuda.current_stream(dev)
+
+    def step(x):
+        o, fs = gdn.chunk_gated_delta_rule_fwd(x.q, x.k, x.v, x.g, x.beta, initial_state=x.h0,
+                                               output_final_state=True, cu_seqlens=x.cu_seqlens,
+                                               cp=cp)
+        grads = gdn.chunk_gated_delta_rule_bwd(x.q, x.k, x.v, x.g, x.beta, x.do, dht=x.dht,
+                                               initial_state=x.h0, cu_seqlens=x.cu_seqlens, cp=cp)
+        return (o, fs) + tuple(grads)
+
+    def fwd_only(x):
+        return gdn.chunk_gated_delta_rule_fwd(x.q, x.k, x.v, x.g, x.beta, initial_state=x.h0,
+                                              output_final_state=True, cu_seqlens=x.cu_seqlens,
+                                              cp=cp)
+
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def timed(fn, steps, profile=False):
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        torch.cuda.synchronize(dev)
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        if profile:
+            gdn.gdn_profile_begin()
+        for i in range(steps):
+            flush.fill_(float(i))                      # evict the inputs from L2 (untimed)
+            starts[i].record(stream)
+            fn()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        prof = gdn.gdn_profile_end() if profile else None
+        if dist:
+            dist.barrier()
+        ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / steps
+        return ms, prof
+
+    for _ in range(max(args.warmup, 3)):
+        step(d)
+    torch.cuda.synchronize(dev)
+    if gdn.gdn_sync_status(stream.cuda_stream) != 0:
+        raise RuntimeError("device status after warm-up: " + gdn.gdn_last_error())
+
+    gpu_index = torch.cuda.get_device_properties(dev)
+    uuid = getattr(gpu_index, "uuid", None)
+    clocks = ClockSampler(f"GPU-{uuid}" if uuid is not None and not str(uuid).startswith("GPU")
+                          else uuid)
+    ms_step, prof = timed(lambda: step(d), args.steps, profile=True)
+    ms_fwd, _ = timed(lambda: fwd_only(d), args.steps)
+
+    # end to end through the public API: pinned host inputs in, results back out
+    host_in = {k: getattr(p, k) for k in ("q", "k", "v", "g", "beta", "h0", "do", "dht")}
+    host_in = {k: v.pin_memory() for k, v in host_in.items() if v is not None}
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    outs = step(d)
+    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs
+                if o is not None]
+    d2h = sum(o.numel() * o.element_size() for o in host_out)
+
+    def e2e_step():
+        x = {k: v.to(dev, non_blocking=True) for k, v in host_in.items()}
+        xx = type(d)(p.name, x["q"], x["k"], x["v"], x["g"], x["beta"], x.get("h0"),
+                     d.cu_seqlens, x["do"], x.get("dht"), p.meta)
+        res = [o for o in step(xx) if o is not None]
+        for h, r in zip(host_out, res):
+            h.copy_(r, non_blocking=True)
+
+    ms_e2e, _ = timed(e2e_step, args.steps)
+    clk = clocks.stop()
+    status = gdn.gdn_sync_status(stream.cuda_stream)
+    if status != 0:
+        raise RuntimeError("device status after the timed region: " + gdn.gdn_last_error())
+
+    if dist:
+        t = torch.tensor([ms_step, ms_fwd, ms_e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step, ms_fwd, ms_e2e = t.tolist()
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+
+    value = world * tokens / (ms_step / 1e3)
+    th = tokens * p.H
+    step_bytes = th * (bytes_per_token_head(p.K, p.V, e_in, "fwd") +
+                       bytes_per_token_head(p.K, p.V, e_in, "bwd"))
+    step_bytes += p.N * p.H * p.K * p.V * 4 * 5          # h0 (x2), hT, dhT, dh0
+    step_flops = th * (flops_per_token_head(p.K, p.V, "fwd") +
+                       flops_per_token_head(p.K, p.V, "bwd"))
+    hbm = peaks.get("hbm_gbs", 6800.0)
+    bf16 = peaks.get("bf16_tflops", 1900.0)
+    t_roof = max(step_bytes / (hbm * 1e9), step_flops / (bf16 * 1e12))
+    total_launches = sum(s[1] for s in prof)
+    dom = max(prof, key=lambda s: s[2])
+    dom_name, dom_launches, dom_ms = dom
+    avg_s = dom_ms / dom_launches / 1e3
+    per_th = kernel_flops_per_token_head(dom_name, p.K, p.V)
+    sm_max = (clk or {}).get("sm_max_mhz") or peaks.get("sm_max_mhz", 2070.0)
+    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    alu_peak = n_sms * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
+    roof = {"kernel": dom_name, "bound": "alu", "unit": "TFLOP/s",
+            "achieved": None if per_th is None else per_th * th / avg_s / 1e12,
+            "peak": alu_peak, "peak_source": "fp32 FMA: SMs x 128 lanes x 2 x max SM clock",
+            "traffic": None, "avg_launch_ms": avg_s * 1e3, "launches_per_step":
+                dom_launches / args.steps}
+    roof["frac"] = None if roof["achieved"] is None else roof["achieved"] / roof["peak"]
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        dt, threads, th_s = oracle_sample(p, list(range(p.H)), reps_min_s=10.0)
+        cpu = {"value": th_s / p.H / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"fp64 oracle fwd+bwd over all {p.H} heads of the {args.workload} "
+                         f"workload, repeated for >= 10 s"}
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded; see gdn_synth.py)", "config": config_of(p, args.workload),
+            "fwd": {"value": world * tokens / (ms_fwd / 1e3), "unit": "tokens/s",
+                    "ms_per_step": ms_fwd},
+            "step_roofline": {"t_roof_ms": t_roof * 1e3, "frac": t_roof * 1e3 / ms_step,
+                              "bytes": step_bytes, "flops": step_flops,
+                              "peaks": {"hbm_gbs": hbm, "bf16_tflops": bf16,
+                                        "source": "measured" if peaks else "fallback"}},
+            "roofline": roof,
+            "kernels": [{"name": n, "launches": l, "ms": m, "share": m / sum(s[2] for s in prof)}
+                        for n, l, m in prof],
+            "gpu_launches": total_launches,
+            "e2e": {"value": world * tokens / (ms_e2e / 1e3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "clocks": clk, "cpu_baseline": cpu}
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

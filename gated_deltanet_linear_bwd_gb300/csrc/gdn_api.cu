@@ -1,0 +1,418 @@
+// gdn_api.cu -- the C ABI of libgdn.so (declared in include/gdn.h):
+// argument validation, the intra-card sequence-parallel decision, workspace
+// layout and launch sequencing.  All device work goes on the caller's stream;
+// nothing here allocates device memory.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "gdn.h"
+#include "gdn_internal.h"
+
+namespace gdn {
+
+// One sticky status word per device (module memory, not an allocation).
+static __device__ int g_status_word;
+
+static thread_local std::string t_last_error;
+static std::atomic<long long> g_spin_limit{1ll << 26};
+
+static gdn_status fail(gdn_status code, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return code;
+}
+
+static gdn_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(GDN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+struct DeviceInfo {
+    int *status = nullptr;
+    int sms = 0;
+    int major = 0, minor = 0;
+    bool ready = false;
+};
+static DeviceInfo g_dev[64];
+static std::mutex g_dev_mu;
+
+// Per-device set-up on first use: the status word's device address and the
+// SM count.  Runs with the target device current.
+static gdn_status device_info(DeviceInfo **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(GDN_ERR_UNSUPPORTED, "device index %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.ready) {
+        e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        if (d.major != 10 || d.minor != 3)
+            return fail(GDN_ERR_UNSUPPORTED, "libgdn is built for sm_103a; device %d is sm_%d%d",
+                        dev, d.major, d.minor);
+        e = cudaGetSymbolAddress((void **)&d.status, g_status_word);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status word)");
+        d.ready = true;
+    }
+    *out = &d;
+    return GDN_OK;
+}
+
+// Fields the forward and backward share.
+struct Common {
+    const void *q, *k, *v;
+    const float *g, *beta, *h0;
+    const int32_t *cu;
+    int B, T, H, K, V, N, dtype, l2, cp_mode, seg_chunks;
+    float scale;
+};
+
+static constexpr size_t kAlign = 256;
+static constexpr int kScratchCtas = 256;  // CTAs of the CUDA-core local-gradient kernel
+
+static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+static gdn_status validate(const Common &c) {
+    if (!c.q || !c.k || !c.v || !c.g || !c.beta)
+        return fail(GDN_ERR_INVALID_ARG, "q, k, v, g and beta are required");
+    if (c.B < 1 || c.T < 0 || c.H < 1)
+        return fail(GDN_ERR_INVALID_ARG, "bad sizes B=%d T=%d H=%d", c.B, c.T, c.H);
+    if ((c.K != 64 && c.K != 128) || (c.V != 64 && c.V != 128))
+        return fail(GDN_ERR_INVALID_ARG, "K and V must each be 64 or 128 (K=%d V=%d)", c.K, c.V);
+    if (c.dtype != GDN_FP32 && c.dtype != GDN_BF16)
+        return fail(GDN_ERR_UNSUPPORTED, "dtype %d is not GDN_FP32 or GDN_BF16", c.dtype);
+    if (c.cu && (c.B != 1 || c.N < 1))
+        return fail(GDN_ERR_INVALID_ARG, "cu_seqlens needs B == 1 and N >= 1 (B=%d N=%d)", c.B, c.N);
+    if (c.cp_mode < GDN_CP_AUTO || c.cp_mode > GDN_CP_FORCE)
+        return fail(GDN_ERR_INVALID_ARG, "cp_mode %d", c.cp_mode);
+    if (c.seg_chunks < 0) return fail(GDN_ERR_INVALID_ARG, "cp_segment_chunks < 0");
+    if (!aligned16(c.q) || !aligned16(c.k) || !aligned16(c.v) || !aligned16(c.g) ||
+        !aligned16(c.beta) || (c.h0 && !aligned16(c.h0)) || (c.cu && !aligned16(c.cu)))
+        return fail(GDN_ERR_INVALID_ARG, "every tensor must be 16-byte aligned");
+    const long long tokens = (long long)c.B * c.T;
+    if (tokens * c.H * (long long)(c.K > c.V ? c.K : c.V) >= (1ll << 40))
+        return fail(GDN_ERR_INVALID_ARG, "problem too large");
+    return GDN_OK;
+}
+
+// The pages' AutoCP rule (ollai.cn page, "FlashQLA的核心优势", second item):
+// on when batch x heads <= 40, or <= 56 with seq_len >= 8192, tuned on an
+// H200 with 132 SMs.  Rescaled here by this GPU's SM count.
+static bool cp_auto(long long units, long long avg_len, int sms) {
+    return units * 132 <= 40ll * sms || (units * 132 <= 56ll * sms && avg_len >= 8192);
+}
+
+static gdn_status make_plan(const Common &c, bool bwd, int sms, Plan &p) {
+    gdn_status st = validate(c);
+    if (st != GDN_OK) return st;
+    Geo &g = p.g;
+    g = Geo{};
+    g.q = c.q; g.k = c.k; g.v = c.v; g.g = c.g; g.beta = c.beta; g.cu = c.cu;
+    g.B = c.B; g.T = c.T; g.H = c.H; g.K = c.K; g.V = c.V;
+    g.N = c.cu ? c.N : c.B;
+    g.nc_fixed = (c.T + kChunk - 1) / kChunk;
+    g.l2norm = c.l2 ? 1 : 0;
+    g.scale = c.scale > 0.f ? c.scale : 1.0f / sqrtf((float)c.K);
+    g.spin_limit = g_spin_limit.load();
+    p.dtype = c.dtype;
+    p.path = kPathSimt;
+    p.h0 = c.h0;
+    p.max_chunks = c.cu ? (c.T + kChunk - 1) / kChunk + c.N : c.B * g.nc_fixed;
+    const long long units = (long long)g.N * c.H;
+    const long long avg_len = c.cu ? (c.T + c.N - 1) / c.N : c.T;
+    const int nc_avg = (int)((avg_len + kChunk - 1) / kChunk);
+    p.cp = c.cp_mode == GDN_CP_FORCE || (c.cp_mode == GDN_CP_AUTO && sms > 0 &&
+                                         cp_auto(units, avg_len, sms));
+    if (p.cp) {
+        int G = c.seg_chunks;
+        if (G <= 0) {
+            long long P = sms > 0 ? (sms + units - 1) / units : 2;
+            if (P < 2) P = 2;
+            if (P > nc_avg) P = nc_avg > 0 ? nc_avg : 1;
+            G = (int)((nc_avg + P - 1) / P);
+            if (G < 1) G = 1;
+        }
+        g.seg_chunks = G;
+        g.nseg_fixed = g.nc_fixed > 0 ? (g.nc_fixed + G - 1) / G : 1;
+        p.max_segs = c.cu ? p.max_chunks + c.N : c.B * g.nseg_fixed;  // <= seg_capacity
+    } else {
+        g.seg_chunks = 1 << 30;
+        g.nseg_fixed = 1;
+        p.max_segs = 0;
+    }
+    p.scratch_ctas = bwd ? kScratchCtas : 0;
+    p.sms = sms;
+    return GDN_OK;
+}
+
+// Carves the workspace; with base == nullptr only sizes it.
+static size_t layout(Plan &p, bool bwd, char *base) {
+    size_t off = 0;
+    auto take = [&](size_t bytes) -> char * {
+        char *ptr = base ? base + off : nullptr;
+        off += (bytes + kAlign - 1) / kAlign * kAlign;
+        return ptr;
+    };
+    const Geo &g = p.g;
+    const size_t th = (size_t)g.B * g.T * g.H;
+    Ws &w = p.ws;
+    w = Ws{};
+    w.counters = (int32_t *)take(64 * sizeof(int32_t));
+    w.gam = (float *)take(th * sizeof(float));
+    w.w = take(th * g.K * sizeof(float));
+    w.u = take(th * g.V * sizeof(float));
+    if (g.cu) {
+        w.chunk_off = (int32_t *)take((g.N + 1) * sizeof(int32_t));
+        w.seg_off = (int32_t *)take((g.N + 1) * sizeof(int32_t));
+    }
+    if (p.cp) {
+        w.warm = (int32_t *)take((size_t)g.N * g.H * sizeof(int32_t));
+        w.maps = (float *)take((size_t)p.max_segs * g.H * g.K * (g.K + g.V) * sizeof(float));
+        w.seg_state = (float *)take((size_t)p.max_segs * g.H * g.K * g.V * sizeof(float));
+    }
+    if (bwd) {
+        const size_t st = (size_t)p.max_chunks * g.H * g.K * g.V * sizeof(float);
+        w.hc = (float *)take(st);
+        w.dhc = (float *)take(st);
+        w.scratch = (float *)take((size_t)p.scratch_ctas *
+                                  simt::scratch_floats_per_cta(g.K, g.V) * sizeof(float));
+    }
+    return off;
+}
+
+// Upper bound on segments under CP for any segment length: every segment
+// holds at least one chunk, except the single segment of an empty sequence.
+static int seg_capacity(const Common &c, int max_chunks) {
+    return c.cu ? max_chunks + c.N : (max_chunks > c.B ? max_chunks : c.B);
+}
+
+static Common common_of(const gdn_fwd_args *a) {
+    return Common{a->q, a->k, a->v, a->g, a->beta, a->initial_state, a->cu_seqlens,
+                  a->B, a->T, a->H, a->K, a->V, a->N, a->dtype, a->use_qk_l2norm,
+                  a->cp_mode, a->cp_segment_chunks, a->scale};
+}
+static Common common_of(const gdn_bwd_args *a) {
+    return Common{a->q, a->k, a->v, a->g, a->beta, a->initial_state, a->cu_seqlens,
+                  a->B, a->T, a->H, a->K, a->V, a->N, a->dtype, a->use_qk_l2norm,
+                  a->cp_mode, a->cp_segment_chunks, a->scale};
+}
+
+}  // namespace gdn
+
+using namespace gdn;
+
+extern "C" {
+
+int32_t gdn_abi_version(void) { return GDN_ABI_VERSION; }
+
+const char *gdn_last_error(void) { return t_last_error.c_str(); }
+
+void gdn_set_spin_limit(int64_t polls) { g_spin_limit.store(polls < 1 ? (1ll << 26) : polls); }
+
+size_t gdn_fwd_workspace_size(const gdn_fwd_args *a) {
+    if (!a) { fail(GDN_ERR_INVALID_ARG, "null args"); return 0; }
+    Plan p;
+    // sizes are device independent: CP capacities use upper bounds
+    if (make_plan(common_of(a), false, 0, p) != GDN_OK) return 0;
+    if (a->cp_mode != GDN_CP_OFF) {  // room for CP whether or not AUTO picks it
+        p.cp = 1;
+        p.max_segs = seg_capacity(common_of(a), p.max_chunks);
+    }
+    return layout(p, false, nullptr);
+}
+
+size_t gdn_bwd_workspace_size(const gdn_bwd_args *a) {
+    if (!a) { fail(GDN_ERR_INVALID_ARG, "null args"); return 0; }
+    Plan p;
+    if (make_plan(common_of(a), true, 0, p) != GDN_OK) return 0;
+    if (a->cp_mode != GDN_CP_OFF) {
+        p.cp = 1;
+        p.max_segs = seg_capacity(common_of(a), p.max_chunks);
+    }
+    return layout(p, true, nullptr);
+}
+
+static gdn_status prepare(const Common &c, bool bwd, void *ws, size_t ws_bytes, Plan &p) {
+    gdn_status st = validate(c);  // host-side checks first: they need no device
+    if (st != GDN_OK) return st;
+    DeviceInfo *dev = nullptr;
+    st = device_info(&dev);
+    if (st != GDN_OK) return st;
+    st = make_plan(c, bwd, dev->sms, p);
+    if (st != GDN_OK) return st;
+    p.g.status = dev->status;
+    const size_t need = layout(p, bwd, nullptr);
+    if (!ws && need > 0) return fail(GDN_ERR_WORKSPACE, "workspace is NULL (%zu bytes needed)", need);
+    if (ws_bytes < need)
+        return fail(GDN_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", ws_bytes, need);
+    if (((uintptr_t)ws & (kAlign - 1)) != 0)
+        return fail(GDN_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    layout(p, bwd, (char *)ws);
+    p.g.chunk_off = p.ws.chunk_off;
+    p.g.seg_off = p.ws.seg_off;
+    return GDN_OK;
+}
+
+gdn_status gdn_chunk_fwd(const gdn_fwd_args *a, void *ws, size_t ws_bytes, void *stream) {
+    if (!a) return fail(GDN_ERR_INVALID_ARG, "null args");
+    if (!a->o) return fail(GDN_ERR_INVALID_ARG, "o is required");
+    if (!aligned16(a->o) || (a->final_state && !aligned16(a->final_state)))
+        return fail(GDN_ERR_INVALID_ARG, "outputs must be 16-byte aligned");
+    if (a->cp_warmup_chunks < 0 || (a->cp_warmup_chunks > 0 && !(a->cp_warmup_tau > 0.f)))
+        return fail(GDN_ERR_INVALID_ARG, "cp_warmup_chunks < 0 or cp_warmup_tau <= 0");
+    Plan p;
+    gdn_status st = prepare(common_of(a), false, ws, ws_bytes, p);
+    if (st != GDN_OK) return st;
+    p.o = a->o;
+    p.final_state = a->final_state;
+    p.cp_stats = a->cp_stats;
+    p.warm_chunks = p.cp ? a->cp_warmup_chunks : 0;
+    p.warm_tau = a->cp_warmup_tau;
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = simt::forward(p, s);
+    if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+    return GDN_OK;
+}
+
+gdn_status gdn_chunk_bwd(const gdn_bwd_args *a, void *ws, size_t ws_bytes, void *stream) {
+    if (!a) return fail(GDN_ERR_INVALID_ARG, "null args");
+    if (!a->d_o || !a->dq || !a->dk || !a->dv || !a->dg || !a->dbeta)
+        return fail(GDN_ERR_INVALID_ARG, "d_o, dq, dk, dv, dg and dbeta are required");
+    if (a->grad_dtype != GDN_FP32 && a->grad_dtype != GDN_BF16)
+        return fail(GDN_ERR_UNSUPPORTED, "grad_dtype %d", a->grad_dtype);
+    if (!aligned16(a->d_o) || !aligned16(a->dq) || !aligned16(a->dk) || !aligned16(a->dv) ||
+        !aligned16(a->dg) || !aligned16(a->dbeta) ||
+        (a->d_final_state && !aligned16(a->d_final_state)) ||
+        (a->d_initial_state && !aligned16(a->d_initial_state)))
+        return fail(GDN_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+    Plan p;
+    gdn_status st = prepare(common_of(a), true, ws, ws_bytes, p);
+    if (st != GDN_OK) return st;
+    p.d_o = a->d_o;
+    p.dht = a->d_final_state;
+    p.grad_dtype = a->grad_dtype;
+    p.dq = a->dq; p.dk = a->dk; p.dv = a->dv;
+    p.dg = a->dg; p.dbeta = a->dbeta; p.dh0 = a->d_initial_state;
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = simt::backward(p, s);
+    if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+    return GDN_OK;
+}
+
+gdn_status gdn_sync_status(void *stream) {
+    DeviceInfo *dev = nullptr;
+    gdn_status st = device_info(&dev);
+    if (st != GDN_OK) return st;
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    int word = 0;
+    e = cudaMemcpy(&word, dev->status, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the status word");
+    if (word != 0) {
+        const int zero = 0;
+        e = cudaMemcpy(dev->status, &zero, sizeof(int), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
+        if (word == GDN_ERR_BAD_SEQLENS)
+            return fail(GDN_ERR_BAD_SEQLENS, "cu_seqlens is not 0 = c0 <= ... <= cN = T");
+        if (word == GDN_ERR_TIMEOUT)
+            return fail(GDN_ERR_TIMEOUT, "a bounded device-side wait ran out");
+        return fail(word, "device status %d", word);
+    }
+    return GDN_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- tracing
+namespace gdn {
+namespace {
+struct ProfRec {
+    const char *name;
+    cudaEvent_t a, b;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfRec> g_prof;
+std::vector<cudaEvent_t> g_ev_pool;
+size_t g_ev_used = 0;
+ProfRec *g_open = nullptr;
+
+cudaEvent_t next_event() {
+    if (g_ev_used == g_ev_pool.size()) {
+        cudaEvent_t e;
+        if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+        g_ev_pool.push_back(e);
+    }
+    return g_ev_pool[g_ev_used++];
+}
+}  // namespace
+
+void prof_before(const char *name, cudaStream_t s) {
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    if (!g_prof_on) return;
+    cudaEvent_t a = next_event(), b = next_event();
+    if (!a || !b) return;
+    cudaEventRecord(a, s);
+    g_prof.push_back(ProfRec{name, a, b});
+    g_open = &g_prof.back();
+}
+
+void prof_after(cudaStream_t s) {
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    if (!g_prof_on || !g_open) return;
+    cudaEventRecord(g_open->b, s);
+    g_open = nullptr;
+}
+}  // namespace gdn
+
+extern "C" {
+
+gdn_status gdn_profile_begin(void) {
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    g_prof.clear();
+    g_ev_used = 0;
+    g_open = nullptr;
+    g_prof_on = true;
+    return GDN_OK;
+}
+
+int32_t gdn_profile_end(gdn_kernel_stat *out, int32_t max) {
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    g_prof_on = false;
+    std::vector<gdn_kernel_stat> acc;
+    for (const ProfRec &r : g_prof) {
+        if (cudaEventSynchronize(r.b) != cudaSuccess) continue;
+        float ms = 0.f;
+        if (cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) continue;
+        gdn_kernel_stat *st = nullptr;
+        for (auto &x : acc)
+            if (strncmp(x.name, r.name, sizeof x.name - 1) == 0) st = &x;
+        if (!st) {
+            acc.push_back(gdn_kernel_stat{});
+            st = &acc.back();
+            strncpy(st->name, r.name, sizeof st->name - 1);
+        }
+        st->launches += 1;
+        st->total_ms += ms;
+    }
+    g_prof.clear();
+    g_ev_used = 0;
+    for (int32_t i = 0; i < (int32_t)acc.size() && i < max && out; ++i) out[i] = acc[i];
+    return (int32_t)acc.size();
+}
+
+}  // extern "C"

@@ -1,0 +1,68 @@
+// gdn_internal.h -- host-side plan shared by the C-ABI layer (gdn_api.cu)
+// and the kernel launchers.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "gdn_common.cuh"
+
+namespace gdn {
+
+// Device pointers carved out of the caller's workspace.
+struct Ws {
+    float *gam = nullptr;        // [tokens, H] within-chunk cumsum of g
+    void *w = nullptr;           // [tokens, H, K] W rows (fp32 or bf16, per path)
+    void *u = nullptr;           // [tokens, H, V] u rows
+    int32_t *chunk_off = nullptr;  // [N+1] (varlen)
+    int32_t *seg_off = nullptr;    // [N+1] (varlen + CP)
+    int32_t *warm = nullptr;       // [N, H] warmup decision
+    float *maps = nullptr;         // [segs, H, K, K+V] affine maps
+    float *seg_state = nullptr;    // [segs, H, K, V] segment start states / end gradients
+    float *hc = nullptr;           // [chunks, H, K, V] chunk start states (bwd)
+    float *dhc = nullptr;          // [chunks, H, K, V] chunk end gradients (bwd)
+    float *scratch = nullptr;      // per-CTA scratch (bwd, CUDA-core path)
+    int32_t *counters = nullptr;   // small zeroed counters
+};
+
+struct Plan {
+    Geo g;
+    Ws ws;
+    int dtype = GDN_FP32;
+    int path = 0;               // kPathSimt / kPathTc
+    int max_chunks = 0;         // chunk capacity (>= actual)
+    int max_segs = 0;           // segment capacity under CP
+    int cp = 0;
+    int warm_chunks = 0;
+    float warm_tau = 0.f;
+    int sms = 0;
+    int scratch_ctas = 0;
+    // forward
+    const float *h0 = nullptr;
+    void *o = nullptr;
+    float *final_state = nullptr;
+    int32_t *cp_stats = nullptr;
+    // backward
+    const void *d_o = nullptr;
+    const float *dht = nullptr;
+    int grad_dtype = GDN_FP32;
+    void *dq = nullptr, *dk = nullptr, *dv = nullptr;
+    float *dg = nullptr, *dbeta = nullptr, *dh0 = nullptr;
+};
+
+enum { kPathSimt = 0, kPathTc = 1 };
+
+// Tracing hooks around every launch (no-ops unless gdn_profile_begin ran).
+void prof_before(const char *name, cudaStream_t s);
+void prof_after(cudaStream_t s);
+
+namespace simt {
+// Per-CTA scratch floats of the local-gradient kernel.
+size_t scratch_floats_per_cta(int K, int V);
+cudaError_t tables(const Plan &p, cudaStream_t s);
+cudaError_t forward(const Plan &p, cudaStream_t s);
+cudaError_t backward(const Plan &p, cudaStream_t s);
+}  // namespace simt
+
+}  // namespace gdn

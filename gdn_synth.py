@@ -73,6 +73,23 @@ class Problem:
     def tokens(self) -> int:
         return self.B * self.T
 
+    def heads(self, hs, batches=None):
+        """The same problem restricted to heads `hs` (and batch rows `batches`
+        when not packed): the sampled (sequence, head) units of a full-size
+        workload."""
+        hs = list(hs)
+        bs = None if batches is None else list(batches)
+
+        def cut(x, state=False):
+            if x is None:
+                return None
+            if bs is not None and (not state or self.cu_seqlens is None):
+                x = x[bs]
+            return x[:, hs] if state else x[:, :, hs]
+        return Problem(self.name, cut(self.q), cut(self.k), cut(self.v), cut(self.g),
+                       cut(self.beta), cut(self.h0, True), self.cu_seqlens, cut(self.do),
+                       cut(self.dht, True), dict(self.meta))
+
     def to(self, device):
         f = lambda x: None if x is None else x.to(device)
         return Problem(self.name, *(f(getattr(self, n)) for n in

@@ -1,0 +1,181 @@
+/*
+ * gdn.h -- C ABI of libgdn.so: Gated DeltaNet (GDN) chunked prefill,
+ * forward and backward, on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation (the pages name it "GDN Chunked Prefill" -- "FlashQLA是什么"
+ * on ollai.cn, sections "FlashQLA的主要功能" and "如何使用FlashQLA" -- and
+ * describe its call as chunk_gated_delta_rule(q, k, v, g, beta,
+ * initial_state, cu_seqlens) returning O and the final state, with separate
+ * low-level fwd / bwd entry points) is the gated delta rule of Yang, Kautz
+ * and Hatamizadeh ("Gated Delta Networks", ICLR 2025), per (sequence, head):
+ *
+ *     S_t = exp(g_t) S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
+ *     o_t = S_t (scale * q_t)
+ *
+ * evaluated chunk by chunk (64 tokens).  States cross the ABI as H = S^T,
+ * i.e. [K, V] with the key index first.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every tensor pointer is a DEVICE pointer on the current CUDA device,
+ *   contiguous, row-major, in the layout stated for it.  The caller owns
+ *   all memory: the library never allocates or frees device memory and
+ *   never synchronises the stream (except gdn_sync_status).
+ * - `stream` is a cudaStream_t passed as void*; NULL means the legacy
+ *   default stream.  Calls are asynchronous on it.
+ * - `workspace` is caller-allocated device memory of at least the size the
+ *   matching *_workspace_size function returns, 256-byte aligned.  It holds
+ *   per-call intermediates only; nothing persists between calls.
+ * - Errors: host-detectable argument problems return a non-zero gdn_status
+ *   before anything is launched, and gdn_last_error() describes them.
+ *   Problems only the device can see (bad cu_seqlens contents, a bounded
+ *   wait that ran out) are recorded in a per-device status word that
+ *   gdn_sync_status() reads and clears.
+ * - Shapes: B batch, T tokens per batch row, H heads, K key dim, V value
+ *   dim.  K and V must each be 64 or 128.  T may be 0.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GDN_ABI_VERSION 1
+
+typedef int32_t gdn_status;
+enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1,  /* null required pointer, bad sizes, misalignment */
+    GDN_ERR_UNSUPPORTED = 2,  /* dtype / shape / device not supported */
+    GDN_ERR_WORKSPACE = 3,    /* workspace smaller than *_workspace_size */
+    GDN_ERR_CUDA = 4,         /* a CUDA runtime call failed; message has its text */
+    GDN_ERR_TIMEOUT = 5,      /* a bounded device-side wait ran out (gdn_sync_status) */
+    GDN_ERR_BAD_SEQLENS = 6   /* cu_seqlens not 0 = c0 <= c1 <= ... <= cN = T (device check) */
+};
+
+/* Element type of q, k, v, o and d_o (and of dq/dk/dv when chosen). */
+enum { GDN_FP32 = 0, GDN_BF16 = 1 };
+
+/* Intra-card sequence parallelism ("AutoCP", ollai.cn page, sections
+ * "FlashQLA的技术原理" and "FlashQLA的核心优势"): each (sequence, head) is
+ * cut into segments walked on separate SMs.  Exact mode reduces every
+ * segment to an affine state map S -> A S + B and joins the maps with a
+ * prefix scan; results equal the serial walk up to rounding order. */
+enum { GDN_CP_AUTO = 0, GDN_CP_OFF = 1, GDN_CP_FORCE = 2 };
+
+typedef struct gdn_fwd_args {
+    /* inputs */
+    const void *q;              /* [B, T, H, K], dtype                              */
+    const void *k;              /* [B, T, H, K], dtype                              */
+    const void *v;              /* [B, T, H, V], dtype                              */
+    const float *g;             /* [B, T, H] log decay (g <= 0 expected)            */
+    const float *beta;          /* [B, T, H] write strength                         */
+    const float *initial_state; /* [N, H, K, V] fp32, NULL = zeros                  */
+    const int32_t *cu_seqlens;  /* [N + 1] int32, NULL = B separate rows of length T.
+                                   When given, B must be 1 and sequence n covers
+                                   tokens cu_seqlens[n] .. cu_seqlens[n+1]-1.        */
+    int32_t B, T, H, K, V;
+    int32_t N;                  /* number of sequences when cu_seqlens != NULL      */
+    int32_t dtype;              /* GDN_FP32 or GDN_BF16                              */
+    float scale;                /* <= 0 means K^-1/2                                */
+    int32_t use_qk_l2norm;      /* 1: q, k scaled to unit norm, (|x|^2 + 1e-6)^-1/2 */
+    int32_t cp_mode;            /* GDN_CP_*                                          */
+    int32_t cp_segment_chunks;  /* chunks per segment under CP; 0 = chosen here     */
+    int32_t cp_warmup_chunks;   /* 0 = exact CP.  W > 0: a segment whose preceding W
+                                   chunks decay by less than cp_warmup_tau starts
+                                   from a W-chunk walk from zero instead of the
+                                   exact map (approximate; off by default)           */
+    float cp_warmup_tau;        /* threshold on exp(sum of g over the W chunks)      */
+    /* outputs */
+    void *o;                    /* [B, T, H, V], dtype                              */
+    float *final_state;         /* [N, H, K, V] fp32, NULL = not written            */
+    int32_t *cp_stats;          /* NULL, or 2 device int32: heads that took the warmup
+                                   shortcut, heads walked under CP (accumulated)     */
+} gdn_fwd_args;
+
+typedef struct gdn_bwd_args {
+    /* the forward's inputs, same meaning and layout as in gdn_fwd_args */
+    const void *q, *k, *v;
+    const float *g, *beta;
+    const float *initial_state;
+    const int32_t *cu_seqlens;
+    int32_t B, T, H, K, V, N;
+    int32_t dtype;
+    float scale;
+    int32_t use_qk_l2norm;
+    int32_t cp_mode;
+    int32_t cp_segment_chunks;
+    /* incoming gradients */
+    const void *d_o;            /* [B, T, H, V], dtype                              */
+    const float *d_final_state; /* [N, H, K, V] fp32, NULL = zeros                  */
+    /* outputs (every one written in full) */
+    int32_t grad_dtype;         /* element type of dq, dk, dv (GDN_FP32 or GDN_BF16) */
+    void *dq;                   /* [B, T, H, K]                                     */
+    void *dk;                   /* [B, T, H, K]                                     */
+    void *dv;                   /* [B, T, H, V]                                     */
+    float *dg;                  /* [B, T, H]                                        */
+    float *dbeta;               /* [B, T, H]                                        */
+    float *d_initial_state;     /* [N, H, K, V] fp32, NULL = not written            */
+} gdn_bwd_args;
+
+/* GDN_ABI_VERSION of the loaded library. */
+int32_t gdn_abi_version(void);
+
+/* Bytes of workspace gdn_chunk_fwd needs for these arguments (0 when the
+ * arguments are invalid; gdn_last_error then says why). */
+size_t gdn_fwd_workspace_size(const gdn_fwd_args *args);
+
+/* Forward: O and (optionally) the final state, in chunked form: per chunk a UT transform T = (I + strict_lower(diag(beta)
+ * K K^T * decay))^-1 gives w and u, the state walks chunk to chunk, and O is
+ * the inter-chunk term plus the masked intra-chunk term. */
+gdn_status gdn_chunk_fwd(const gdn_fwd_args *args, void *workspace, size_t workspace_bytes,
+                         void *stream);
+
+/* Bytes of workspace gdn_chunk_bwd needs. */
+size_t gdn_bwd_workspace_size(const gdn_bwd_args *args);
+
+/* Backward (which the traeai.com page, announcement text, singles out as the
+ * most difficult piece to make fast): given
+ * dO and d(final_state), writes dq, dk, dv, dg, dbeta and d(initial_state).
+ * The forward's per-chunk states are recomputed, not read from a saved
+ * context; the result does not depend on cp_mode beyond rounding. */
+gdn_status gdn_chunk_bwd(const gdn_bwd_args *args, void *workspace, size_t workspace_bytes,
+                         void *stream);
+
+/* Synchronises `stream`, then reads and clears this device's status word:
+ * GDN_OK, GDN_ERR_BAD_SEQLENS, GDN_ERR_TIMEOUT or GDN_ERR_CUDA. */
+gdn_status gdn_sync_status(void *stream);
+
+/* Message for the last non-OK status returned on this host thread. */
+const char *gdn_last_error(void);
+
+/* Testing hook: iteration limit of every bounded device-side wait
+ * (default 1 << 26 polls; values < 1 restore the default).  A limit of 1
+ * makes a wait give up at once and report GDN_ERR_TIMEOUT; the kernels
+ * then finish without touching their outputs further. */
+void gdn_set_spin_limit(int64_t polls);
+
+/* Per-kernel tracing.  Between gdn_profile_begin() and gdn_profile_end()
+ * every kernel launch of this library (on any stream, any device) is
+ * bracketed by a pair of CUDA events recorded on its launching stream.
+ * gdn_profile_end() waits for those events, then fills up to `max` entries
+ * of `out` (one per kernel name, in first-launch order) and returns the
+ * number of distinct kernels (which may exceed `max`).  Off by default;
+ * when off, launches carry no extra events. */
+typedef struct gdn_kernel_stat {
+    char name[64];
+    int32_t launches;
+    double total_ms;
+} gdn_kernel_stat;
+
+gdn_status gdn_profile_begin(void);
+int32_t gdn_profile_end(gdn_kernel_stat *out, int32_t max);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GDN_H_ */

@@ -1,0 +1,125 @@
+"""The C ABI without a GPU: libgdn.so loads, exports every function that
+include/gdn.h declares, the ctypes structs match the C layout, and host-side
+validation rejects bad arguments before touching a device."""
+import ctypes
+import os
+import re
+import subprocess
+import tempfile
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+
+
+@pytest.fixture(scope="module")
+def abi():
+    import __graft_entry__
+    __graft_entry__.build()
+    from gated_deltanet_linear_bwd_gb300 import _abi
+    _abi.load()
+    return _abi
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_every_declared_function_is_exported(abi):
+    names = declared_functions()
+    assert set(names) == set(abi.EXPORTS), names
+    lib = abi.load()
+    for n in names:
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", abi.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    for n in names:
+        assert re.search(rf"\bT {n}\b", out), n
+
+
+def test_struct_layout_matches_header(abi):
+    probe = r"""
+#include <stdio.h>
+#include <stddef.h>
+#include "gdn.h"
+#define F(S, f) printf(#S " " #f " %zu\n", offsetof(S, f));
+int main(void) {
+  printf("gdn_fwd_args sizeof %zu\n", sizeof(gdn_fwd_args));
+  printf("gdn_bwd_args sizeof %zu\n", sizeof(gdn_bwd_args));
+  printf("gdn_kernel_stat sizeof %zu\n", sizeof(gdn_kernel_stat));
+%s
+  return 0;
+}
+"""
+    lines = []
+    for cls in (abi.gdn_fwd_args, abi.gdn_bwd_args, abi.gdn_kernel_stat):
+        for name, _ in cls._fields_:
+            lines.append(f"  F({cls.__name__}, {name})")
+    src = probe.replace("%s", "\n".join(lines))
+    with tempfile.TemporaryDirectory() as d:
+        c = os.path.join(d, "probe.c")
+        exe = os.path.join(d, "probe")
+        open(c, "w").write(src)
+        subprocess.run(["gcc", "-std=c11", "-I", os.path.dirname(HEADER), c, "-o", exe],
+                       check=True)
+        got = subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split("\n")
+    for line in filter(None, got):
+        sname, field, val = line.split()
+        cls = getattr(abi, sname)
+        if field == "sizeof":
+            assert ctypes.sizeof(cls) == int(val), sname
+        else:
+            assert getattr(cls, field).offset == int(val), (sname, field)
+
+
+def _fwd_args(abi, **kw):
+    a = abi.gdn_fwd_args()
+    a.q = a.k = a.v = a.g = a.beta = a.o = 4096
+    a.B, a.T, a.H, a.K, a.V = 1, 256, 2, 64, 64
+    a.dtype = abi.GDN_FP32
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_abi_version_and_workspace_query_need_no_gpu(abi):
+    assert abi.gdn_abi_version() == 1
+    n_off = abi.gdn_fwd_workspace_size(_fwd_args(abi, cp_mode=abi.GDN_CP_OFF))
+    n_cp = abi.gdn_fwd_workspace_size(_fwd_args(abi, cp_mode=abi.GDN_CP_FORCE))
+    assert 0 < n_off < n_cp
+    b = abi.gdn_bwd_args()
+    b.q = b.k = b.v = b.g = b.beta = 4096
+    b.B, b.T, b.H, b.K, b.V = 2, 100, 3, 128, 64
+    assert abi.gdn_bwd_workspace_size(b) > n_off
+
+
+@pytest.mark.parametrize("bad, msg", [
+    (dict(K=96), "K and V"),
+    (dict(V=32), "K and V"),
+    (dict(q=None), "required"),
+    (dict(B=0), "bad sizes"),
+    (dict(dtype=7), "dtype"),
+    (dict(cp_mode=9), "cp_mode"),
+    (dict(q=4097), "aligned"),
+    (dict(cu_seqlens=4096, B=2, N=2), "cu_seqlens"),
+])
+def test_bad_arguments_are_rejected_on_the_host(abi, bad, msg):
+    a = _fwd_args(abi, **bad)
+    assert abi.load().gdn_fwd_workspace_size(ctypes.byref(a)) == 0
+    assert msg in abi.gdn_last_error()
+    rc = abi.load().gdn_chunk_fwd(ctypes.byref(a), ctypes.c_void_p(4096), 1 << 30, None)
+    assert rc in (abi.GDN_ERR_INVALID_ARG, abi.GDN_ERR_UNSUPPORTED)
+    assert msg in abi.gdn_last_error()
+
+
+def test_missing_outputs_are_rejected(abi):
+    a = _fwd_args(abi, o=None)
+    rc = abi.load().gdn_chunk_fwd(ctypes.byref(a), ctypes.c_void_p(4096), 1 << 30, None)
+    assert rc == abi.GDN_ERR_INVALID_ARG
+    b = abi.gdn_bwd_args()
+    rc = abi.load().gdn_chunk_bwd(ctypes.byref(b), ctypes.c_void_p(4096), 1 << 30, None)
+    assert rc == abi.GDN_ERR_INVALID_ARG
+    assert "required" in abi.gdn_last_error()
