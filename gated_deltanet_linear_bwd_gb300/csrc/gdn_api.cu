@@ -86,8 +86,11 @@ static constexpr int kScratchCtas = 256;  // CTAs of the CUDA-core local-gradien
 
 static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
+static bool has_tokens(const Common &c) { return (long long)c.B * c.T > 0; }
+
 static gdn_status validate(const Common &c) {
-    if (!c.q || !c.k || !c.v || !c.g || !c.beta)
+    // empty inputs (T == 0) may come with null pointers
+    if (has_tokens(c) && (!c.q || !c.k || !c.v || !c.g || !c.beta))
         return fail(GDN_ERR_INVALID_ARG, "q, k, v, g and beta are required");
     if (c.B < 1 || c.T < 0 || c.H < 1)
         return fail(GDN_ERR_INVALID_ARG, "bad sizes B=%d T=%d H=%d", c.B, c.T, c.H);
@@ -269,7 +272,7 @@ static gdn_status prepare(const Common &c, bool bwd, void *ws, size_t ws_bytes, 
 
 gdn_status gdn_chunk_fwd(const gdn_fwd_args *a, void *ws, size_t ws_bytes, void *stream) {
     if (!a) return fail(GDN_ERR_INVALID_ARG, "null args");
-    if (!a->o) return fail(GDN_ERR_INVALID_ARG, "o is required");
+    if (!a->o && (long long)a->B * a->T > 0) return fail(GDN_ERR_INVALID_ARG, "o is required");
     if (!aligned16(a->o) || (a->final_state && !aligned16(a->final_state)))
         return fail(GDN_ERR_INVALID_ARG, "outputs must be 16-byte aligned");
     if (a->cp_warmup_chunks < 0 || (a->cp_warmup_chunks > 0 && !(a->cp_warmup_tau > 0.f)))
@@ -290,7 +293,7 @@ gdn_status gdn_chunk_fwd(const gdn_fwd_args *a, void *ws, size_t ws_bytes, void 
 
 gdn_status gdn_chunk_bwd(const gdn_bwd_args *a, void *ws, size_t ws_bytes, void *stream) {
     if (!a) return fail(GDN_ERR_INVALID_ARG, "null args");
-    if (!a->d_o || !a->dq || !a->dk || !a->dv || !a->dg || !a->dbeta)
+    if ((long long)a->B * a->T > 0 && (!a->d_o || !a->dq || !a->dk || !a->dv || !a->dg || !a->dbeta))
         return fail(GDN_ERR_INVALID_ARG, "d_o, dq, dk, dv, dg and dbeta are required");
     if (a->grad_dtype != GDN_FP32 && a->grad_dtype != GDN_BF16)
         return fail(GDN_ERR_UNSUPPORTED, "grad_dtype %d", a->grad_dtype);

@@ -120,6 +120,7 @@ def test_missing_outputs_are_rejected(abi):
     rc = abi.load().gdn_chunk_fwd(ctypes.byref(a), ctypes.c_void_p(4096), 1 << 30, None)
     assert rc == abi.GDN_ERR_INVALID_ARG
     b = abi.gdn_bwd_args()
+    b.B, b.T = 1, 5
     rc = abi.load().gdn_chunk_bwd(ctypes.byref(b), ctypes.c_void_p(4096), 1 << 30, None)
     assert rc == abi.GDN_ERR_INVALID_ARG
     assert "required" in abi.gdn_last_error()
