@@ -22,7 +22,8 @@ namespace gdn {
 static __device__ int g_status_word;
 
 static thread_local std::string t_last_error;
-static std::atomic<long long> g_spin_limit{1ll << 26};
+static constexpr long long kDefaultSpinLimit = 1ll << 21;
+static std::atomic<long long> g_spin_limit{kDefaultSpinLimit};
 
 static gdn_status fail(gdn_status code, const char *fmt, ...) {
     char buf[512];
@@ -224,7 +225,7 @@ int32_t gdn_abi_version(void) { return GDN_ABI_VERSION; }
 
 const char *gdn_last_error(void) { return t_last_error.c_str(); }
 
-void gdn_set_spin_limit(int64_t polls) { g_spin_limit.store(polls < 1 ? (1ll << 26) : polls); }
+void gdn_set_spin_limit(int64_t polls) { g_spin_limit.store(polls < 0 ? kDefaultSpinLimit : polls); }
 
 size_t gdn_fwd_workspace_size(const gdn_fwd_args *a) {
     if (!a) { fail(GDN_ERR_INVALID_ARG, "null args"); return 0; }
@@ -286,7 +287,7 @@ gdn_status gdn_chunk_fwd(const gdn_fwd_args *a, void *ws, size_t ws_bytes, void 
     p.warm_chunks = p.cp ? a->cp_warmup_chunks : 0;
     p.warm_tau = a->cp_warmup_tau;
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t e = simt::forward(p, s);
+    cudaError_t e = tc::supported(p) ? tc::forward(p, s) : simt::forward(p, s);
     if (e != cudaSuccess) return cuda_fail(e, "forward launch");
     return GDN_OK;
 }

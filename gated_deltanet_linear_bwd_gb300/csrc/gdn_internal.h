@@ -63,6 +63,14 @@ size_t scratch_floats_per_cta(int K, int V);
 cudaError_t tables(const Plan &p, cudaStream_t s);
 cudaError_t forward(const Plan &p, cudaStream_t s);
 cudaError_t backward(const Plan &p, cudaStream_t s);
+cudaError_t warm_decide(const Plan &p, cudaStream_t s);
+cudaError_t cp_scan(const Plan &p, const int32_t *warm, cudaStream_t s);
 }  // namespace simt
+
+namespace tc {
+// bf16 q/k/v with K = V = 128 and at least one token.
+bool supported(const Plan &p);
+cudaError_t forward(const Plan &p, cudaStream_t s);
+}  // namespace tc
 
 }  // namespace gdn

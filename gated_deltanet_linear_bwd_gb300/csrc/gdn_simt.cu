@@ -918,6 +918,22 @@ static cudaError_t forward_t(const Plan &p, cudaStream_t s, bool states_only) {
     return cudaSuccess;
 }
 
+cudaError_t warm_decide(const Plan &p, cudaStream_t s) {
+    prof_before("warm_decide", s);
+    warm_decide_kernel<<<p.g.N, 128, 0, s>>>(p.g, p.warm_chunks, p.warm_tau, p.ws.warm,
+                                             p.cp_stats);
+    prof_after(s);
+    return cudaGetLastError();
+}
+
+cudaError_t cp_scan(const Plan &p, const int32_t *warm, cudaStream_t s) {
+    const Geo &g = p.g;
+    GDN_LAUNCH("simt_cp_scan", cp_scan_kernel, dim3(g.N, g.H, g.V / kBV),
+               sizeof(float) * 2 * g.K * kBV, s, g, (const float *)p.ws.maps, p.h0, warm,
+               p.ws.seg_state);
+    return cudaSuccess;
+}
+
 cudaError_t forward(const Plan &p, cudaStream_t s) {
     cudaError_t e = tables(p, s);
     if (e != cudaSuccess) return e;

@@ -1,0 +1,640 @@
+// gdn_tc_fwd.cu -- tensor-core (tcgen05 + TMA) forward kernels for bf16
+// q/k/v with K = V = 128.
+//
+// Orientation: every product is issued with M = 128 by putting the feature
+// dimension (K or V) on the MMA's M side and the 64 chunk rows on N.  The
+// walking state is held as H^T (V rows x K columns), one row per thread, in
+// fp32 registers; its bf16 copy in shared memory is the A operand of the
+// state products.  TMEM lane t is thread t's row.
+//
+// Prep kernel (chunk-parallel, two chunks per CTA):
+//   [Ka; Kb] [Ka; Kb]^T                -> the two 64x64 K K^T blocks
+//   A = strict_lower(diag(beta) K K^T .* D),  T = (I + A)^-1 (CUDA cores)
+//   W^T = K^T (diag(beta e) T^T),  u^T = V^T (diag(beta) T^T)
+// Walk kernel (per sequence or segment, sequential over chunks):
+//   P   = [Q; K] K^T (rows of Q)        masked, decayed          (64 x 64)
+//   U^T = u^T - H^T W^T                 (state product)
+//   O^T = H^T Q^T (inter) ; O^T += U^T P^T (intra)
+//   dH^T = (U^T diag(f)) K              H <- exp(gam_L) H + dH,  f = exp(gam_L - gam)
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "gdn_common.cuh"
+#include "gdn_internal.h"
+#include "tc_ptx.cuh"
+
+namespace gdn {
+namespace tc {
+
+constexpr int kD = 128;           // K = V = 128 on this path
+constexpr int kTile = 8192;       // one 64-row x 128-byte swizzled box
+constexpr uint32_t kIdescKK = idesc_bf16(128, 128, false, false);
+constexpr uint32_t kIdescPrepMN = idesc_bf16(128, 64, true, true);
+
+// ------------------------------------------------------------------ prep
+struct PrepSmem {
+    uint8_t k[4 * kTile];          // [dk half][rows 0-63 chunk a, 64-127 chunk b][128 B]
+    uint8_t v[4 * kTile];          // same for v
+    float A[2][64][64];            // strict-lower A per chunk; reused for bw/bu below
+    float gam[2][64], bet[2][64], rk[2][64], wsum[4];
+    uint64_t tma_bar, mma_bar;
+    uint32_t tmem_base;
+};
+
+// Inclusive cumsum of 64 values held one per thread by two consecutive warps.
+__device__ __forceinline__ float scan64(float x, float *wsum) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    if (warp & 1) x += wsum[warp - 1];
+    return x;
+}
+
+__global__ void __launch_bounds__(128, 2)
+prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+            Geo g, float *ws_gam, __nv_bfloat16 *ws_w, __nv_bfloat16 *ws_u) {
+    extern __shared__ uint8_t smem_raw[];
+    PrepSmem &s = *reinterpret_cast<PrepSmem *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, h = blockIdx.y, H = g.H;
+    ChunkRef ra, rb;
+    if (!chunk_ref(g, 2 * blockIdx.x, ra)) return;
+    const bool has_b = chunk_ref(g, 2 * blockIdx.x + 1, rb);
+    if (!has_b) rb = ra;
+    const int ch = tid >> 6, r = tid & 63;
+    const ChunkRef &mine = ch ? rb : ra;
+    const int L = (ch && !has_b) ? 0 : mine.len;
+
+    if (tid == 0) {
+        mbar_init(&s.tma_bar, 1);
+        mbar_init(&s.mma_bar, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&s.tmem_base, 256);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = s.tmem_base;
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&s.tma_bar, 8 * kTile);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            tma_load_3d(s.k + half * 2 * kTile, &tm_k, &s.tma_bar, half * 64, h, (int)ra.bos);
+            tma_load_3d(s.k + half * 2 * kTile + kTile, &tm_k, &s.tma_bar, half * 64, h, (int)rb.bos);
+            tma_load_3d(s.v + half * 2 * kTile, &tm_v, &s.tma_bar, half * 64, h, (int)ra.bos);
+            tma_load_3d(s.v + half * 2 * kTile + kTile, &tm_v, &s.tma_bar, half * 64, h, (int)rb.bos);
+        }
+    }
+    // gam = cumsum(g), beta (zero beyond the chunk)
+    const long long tok = mine.bos + r;
+    const float graw = r < L ? g.g[tok * H + h] : 0.f;
+    const float gam = scan64(graw, s.wsum);
+    s.gam[ch][r] = gam;
+    s.bet[ch][r] = r < L ? g.beta[tok * H + h] : 0.f;
+    if (r < L) ws_gam[tok * H + h] = gam;
+
+    int mma_n = 0;              // commits issued (uniform across threads)
+    bool tma_pending = true;
+    bool ok = mbar_wait(&s.tma_bar, 0, g.spin_limit, g.status);
+    if (__syncthreads_or(!ok)) goto bail;
+    tma_pending = false;
+    ++mma_n;
+    if (tid == 0) {
+        tc_fence_after();
+        const uint32_t kb = smem_u32(s.k);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * 2 * kTile + (kk & 3) * 32;
+            const uint64_t d = desc_sw128(kb + off, 16, 1024);
+            mma_bf16(tbase, d, d, kIdescKK, kk > 0);
+        }
+        mma_commit(&s.mma_bar);
+    }
+    ok = mbar_wait(&s.mma_bar, 0, g.spin_limit, g.status);
+    if (__syncthreads_or(!ok)) goto bail;
+    tc_fence_after();
+    {
+        // row r of this chunk's K K^T block
+        float kk[64];
+        tmem_ld32(tmem_addr(tbase, warp, ch * 64), kk);
+        tmem_ld32(tmem_addr(tbase, warp, ch * 64 + 32), kk + 32);
+        float nrm = 0.f;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) nrm = (c == r) ? kk[c] : nrm;
+        const float rk = (r < L) ? (g.l2norm ? rsqrtf(nrm + 1e-6f) : 1.f) : 0.f;
+        s.rk[ch][r] = rk;
+        tc_fence_before();
+        __syncthreads();
+        const float br = s.bet[ch][r], gr = s.gam[ch][r];
+        float4 *arow = reinterpret_cast<float4 *>(s.A[ch][r]);
+#pragma unroll
+        for (int c4 = 0; c4 < 16; ++c4) {
+            float x[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int c = 4 * c4 + j;
+                x[j] = (c < r && r < L) ? br * kk[c] * rk * s.rk[ch][c] * __expf(gr - s.gam[ch][c])
+                                        : 0.f;
+            }
+            arow[c4] = make_float4(x[0], x[1], x[2], x[3]);
+        }
+    }
+    __syncthreads();
+    {
+        // column r of T = (I + A)^-1 by forward substitution (A read by broadcast)
+        float col[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) col[i] = (i == r) ? 1.f : 0.f;
+#pragma unroll
+        for (int i = 1; i < 64; ++i) {
+            const float4 *ar = reinterpret_cast<const float4 *>(s.A[ch][i]);
+            float acc = col[i];
+#pragma unroll
+            for (int c4 = 0; c4 < (i + 3) / 4; ++c4) {
+                const float4 a4 = ar[c4];
+                if (4 * c4 + 0 < i) acc -= a4.x * col[4 * c4 + 0];
+                if (4 * c4 + 1 < i) acc -= a4.y * col[4 * c4 + 1];
+                if (4 * c4 + 2 < i) acc -= a4.z * col[4 * c4 + 2];
+                if (4 * c4 + 3 < i) acc -= a4.w * col[4 * c4 + 3];
+            }
+            col[i] = acc;
+        }
+        __syncthreads();  // every column done: A's space becomes bw / bu
+        // MN-major B operands: row j = r holds T[.][j] scaled by beta_j e_j rk_j (W)
+        // and by beta_j (u).
+        uint8_t *bw = reinterpret_cast<uint8_t *>(&s.A[0][0][0]);
+        uint8_t *bu = bw + 2 * kTile;
+        const float bj = s.bet[ch][r], ej = __expf(s.gam[ch][r]), rkj = s.rk[ch][r];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            float x[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) x[i] = col[32 * q + i] * bj * ej * rkj;
+            st_row32(bw + ch * kTile, r, 32 * q, x);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) x[i] = col[32 * q + i] * bj;
+            st_row32(bu + ch * kTile, r, 32 * q, x);
+        }
+    }
+    fence_proxy_async();
+    __syncthreads();
+    ++mma_n;
+    if (tid == 0) {
+        tc_fence_after();
+        const uint32_t kb = smem_u32(s.k), vb = smem_u32(s.v);
+        const uint32_t bw = smem_u32(&s.A[0][0][0]), bu = bw + 2 * kTile;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t bdw = desc_sw128(bw + c * kTile + kk * 2048, kTile, 1024);
+                const uint64_t bdu = desc_sw128(bu + c * kTile + kk * 2048, kTile, 1024);
+                const uint64_t ak = desc_sw128(kb + c * kTile + kk * 2048, 2 * kTile, 1024);
+                const uint64_t av = desc_sw128(vb + c * kTile + kk * 2048, 2 * kTile, 1024);
+                mma_bf16(tbase + c * 64, ak, bdw, kIdescPrepMN, kk > 0);
+                mma_bf16(tbase + 128 + c * 64, av, bdu, kIdescPrepMN, kk > 0);
+            }
+        }
+        mma_commit(&s.mma_bar);
+    }
+    ok = mbar_wait(&s.mma_bar, 1, g.spin_limit, g.status);
+    if (__syncthreads_or(!ok)) goto bail;
+    tc_fence_after();
+    // thread t = feature index (dk for W, dv for u); columns = chunk rows
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const int c = m & 1;                  // chunk
+        const bool isu = m >= 2;
+        const ChunkRef &cr = c ? rb : ra;
+        const int Lc = (c && !has_b) ? 0 : cr.len;
+        __nv_bfloat16 *dst = isu ? ws_u : ws_w;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            float x[32];
+            tmem_ld32(tmem_addr(tbase, warp, (isu ? 128 : 0) + c * 64 + half * 32), x);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int row = half * 32 + j;
+                if (row < Lc)
+                    dst[((cr.bos + row) * H + h) * (long long)kD + tid] = __float2bfloat16_rn(x[j]);
+            }
+        }
+    }
+    goto done;
+bail:
+    if (tid == 0) {
+        if (tma_pending) mbar_drain(&s.tma_bar, 0);
+        if (mma_n > 0) mbar_drain(&s.mma_bar, (mma_n - 1) & 1);
+    }
+done:
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tbase, 256);
+}
+
+// ------------------------------------------------------------------ walk
+struct WalkSmem {
+    uint8_t qk[2][4 * kTile];      // per stage: [dk half][rows 0-63 Q, 64-127 K][128 B]
+    uint8_t w[2][2 * kTile];       // per stage: [dk half][64 rows][128 B]
+    uint8_t u[2][2 * kTile];       // per stage: [dv half][64 rows][128 B]
+    uint8_t hT[4 * kTile];         // [dk half][128 state rows][128 B]  (A operand)
+    uint8_t uT[2 * kTile];         // [128 state rows][64 chunk rows]   (A operand)
+    uint8_t uTs[2 * kTile];        // U^T diag(f)                        (A operand)
+    uint8_t p[kTile];              // [64 rows r][64 cols s]            (B operand)
+    float gam[2][64];
+    float rq[64], rk[64];
+    uint64_t tma_bar[2], mma_bar;
+    uint32_t tmem_base;
+};
+
+struct TcWalkArgs {
+    const float *ws_gam;
+    const float *h0;          // [N, H, K, V] nullable
+    const float *seg_start;   // [segs, H, K, V] (CP)
+    const int32_t *warm;      // [N, H] (CP warmup)
+    int warm_chunks;
+    __nv_bfloat16 *o;         // [tokens, H, V] (kWalkOut with output) nullable
+    float *final_state;       // nullable
+    float *hc;                // [chunks, H, K, V] chunk start states, nullable
+    float *maps;              // [segs, H, K, K+V] (kWalkMap)
+    int cp;
+};
+
+enum { kWalkOut = 0, kWalkMap = 1 };
+
+constexpr uint32_t kIdesc64 = idesc_bf16(128, 64, false, false);      // K-major A and B
+constexpr uint32_t kIdescDH = idesc_bf16(128, 128, false, true);      // B MN-major
+
+__device__ __forceinline__ void write_state_rows(uint8_t *hT, int row, const float *Hr) {
+    st_row64(hT, row, Hr);
+    st_row64(hT + 2 * kTile, row, Hr + 64);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(128, 1)
+walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+            const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_u,
+            Geo g, TcWalkArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    WalkSmem &s = *reinterpret_cast<WalkSmem *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, h = blockIdx.y, cb = blockIdx.z, H = g.H;
+    int n, j = 0, nseg = 1;
+    if (a.cp) {
+        if (!seg_ref(g, blockIdx.x, n, j)) return;
+        nseg = seq_nsegs(g, n);
+    } else {
+        n = blockIdx.x;
+        if (n >= g.N) return;
+    }
+    if (MODE == kWalkMap && (j == nseg - 1 || (a.warm && a.warm[n * H + h]))) return;
+    const bool a_cols = MODE == kWalkMap && cb == 0;   // A columns: start I, u = 0
+    const bool emit = MODE == kWalkOut && a.o != nullptr;
+    const bool states = MODE == kWalkOut && a.hc != nullptr;
+    const int nc = seq_nchunks(g, n);
+    const int c0 = min(nc, j * g.seg_chunks), c1 = min(nc, (j + 1) * g.seg_chunks);
+    const int cbase = seq_chunk_base(g, n);
+    long long sbos;
+    int slen;
+    seq_range(g, n, sbos, slen);
+    bool warm = false;
+    int cstart = c0;
+    if (MODE == kWalkOut && a.cp && j > 0 && a.warm && a.warm[n * H + h]) {
+        warm = true;
+        cstart = max(0, c0 - a.warm_chunks);
+    }
+
+    if (tid == 0) {
+        mbar_init(&s.tma_bar[0], 1);
+        mbar_init(&s.tma_bar[1], 1);
+        mbar_init(&s.mma_bar, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&s.tmem_base, 512);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    // start state: row tid of H^T = column tid of H
+    float Hr[kD];
+    {
+        const float *src = nullptr;
+        if (MODE == kWalkOut && !warm) {
+            if (a.cp && j > 0)
+                src = a.seg_start + ((long long)(seq_seg_base(g, n) + j) * H + h) * kD * kD;
+            else if (a.h0)
+                src = a.h0 + ((long long)n * H + h) * kD * kD;
+        }
+#pragma unroll
+        for (int i = 0; i < kD; ++i)
+            Hr[i] = src ? src[i * kD + tid] : ((a_cols && i == tid) ? 1.f : 0.f);
+    }
+    write_state_rows(s.hT, tid, Hr);
+    fence_proxy_async();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = s.tmem_base;
+    const uint32_t t_p = tbase, t_u = tbase + 64, t_oi = tbase + 128, t_oa = tbase + 192,
+                   t_dh = tbase + 256;
+
+    auto issue_tma = [&](int st, int c) {
+        const int tok0 = (int)(sbos + (long long)c * kChunk);
+        mbar_arrive_expect_tx(&s.tma_bar[st], 8 * kTile);   // 2 halves x (q, k, w, u)
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            tma_load_3d(s.qk[st] + half * 2 * kTile, &tm_q, &s.tma_bar[st], half * 64, h, tok0);
+            tma_load_3d(s.qk[st] + half * 2 * kTile + kTile, &tm_k, &s.tma_bar[st], half * 64, h, tok0);
+            tma_load_3d(s.w[st] + half * kTile, &tm_w, &s.tma_bar[st], half * 64, h, tok0);
+            tma_load_3d(s.u[st] + half * kTile, &tm_u, &s.tma_bar[st], half * 64, h, tok0);
+        }
+    };
+
+    int it = 0, mma_n = 0, tma_pending = 0;   // uniform bookkeeping for the bail-out path
+    bool bailed = false;
+    if (tid == 0 && cstart < c1) issue_tma(0, cstart);
+    if (cstart < c1) tma_pending |= 1;
+    for (int c = cstart; c < c1; ++c, ++it) {
+        const int st = it & 1;
+        const long long bos = sbos + (long long)c * kChunk;
+        const int L = min(kChunk, slen - c * kChunk);
+        const bool out_now = emit && c >= c0;
+        if (c + 1 < c1) {
+            if (tid == 0) {
+                fence_proxy_async();
+                issue_tma(st ^ 1, c + 1);
+            }
+            tma_pending |= 1 << (st ^ 1);
+        }
+        if (tid < 64) s.gam[st][tid] = tid < L ? a.ws_gam[(bos + tid) * H + h] : 0.f;
+        if (states && c >= c0) {
+            float *dst = a.hc + ((long long)(cbase + c) * H + h) * kD * kD;
+#pragma unroll
+            for (int i = 0; i < kD; ++i) dst[i * kD + tid] = Hr[i];
+        }
+        bool ok = mbar_wait(&s.tma_bar[st], (it >> 1) & 1, g.spin_limit, g.status);
+        if (__syncthreads_or(!ok)) { bailed = true; break; }
+        tma_pending &= ~(1 << st);
+        if (g.l2norm) {
+            // |q_r| from the Q rows (threads 0-63), |k_r| from the K rows (64-127)
+            const int r = tid & 63;
+            const uint8_t *base = s.qk[st] + (tid >= 64 ? kTile : 0);
+            float ss = 0.f;
+#pragma unroll
+            for (int half = 0; half < 2; ++half)
+#pragma unroll 8
+                for (int col = 0; col < 64; ++col) {
+                    const float x = ld_bf16(base + half * 2 * kTile, r, col);
+                    ss += x * x;
+                }
+            (tid >= 64 ? s.rk : s.rq)[r] = rsqrtf(ss + 1e-6f);
+            __syncthreads();
+        }
+        ++mma_n;
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t qk = smem_u32(s.qk[st]), wt = smem_u32(s.w[st]), hT = smem_u32(s.hT);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t half = kk >> 2, sub = (kk & 3) * 32;
+                const uint64_t ah = desc_sw128(hT + half * 2 * kTile + sub, 16, 1024);
+                const uint64_t bw = desc_sw128(wt + half * kTile + sub, 16, 1024);
+                mma_bf16(t_u, ah, bw, kIdesc64, kk > 0);
+                if (out_now) {
+                    const uint64_t aq = desc_sw128(qk + half * 2 * kTile + sub, 16, 1024);
+                    const uint64_t bk = desc_sw128(qk + half * 2 * kTile + kTile + sub, 16, 1024);
+                    mma_bf16(t_p, aq, bk, kIdesc64, kk > 0);   // rows 0-63 of [Q; K] K^T
+                    mma_bf16(t_oi, ah, aq, kIdesc64, kk > 0);  // H^T Q^T
+                }
+            }
+            mma_commit(&s.mma_bar);
+        }
+        ok = mbar_wait(&s.mma_bar, (mma_n - 1) & 1, g.spin_limit, g.status);
+        if (__syncthreads_or(!ok)) { bailed = true; break; }
+        tc_fence_after();
+        const float gl = s.gam[st][L - 1];
+        // U = u - W H (this thread's state column) and U diag(f), 32 rows at a time
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            float acc[32], U[32];
+            tmem_ld32(tmem_addr(t_u, warp, q * 32), acc);
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+                const int r = q * 32 + jj;
+                const float uv = a_cols ? 0.f : ld_bf16(s.u[st] + (tid >> 6) * kTile, r, tid & 63);
+                U[jj] = r < L ? uv - acc[jj] : 0.f;
+            }
+            st_row32(s.uT, tid, q * 32, U);
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+                const int r = q * 32 + jj;
+                const float f = r < L ? __expf(gl - s.gam[st][r]) : 0.f;
+                U[jj] *= f * (g.l2norm ? s.rk[r] : 1.f);
+            }
+            st_row32(s.uTs, tid, q * 32, U);
+        }
+        if (out_now && tid < 64) {
+            // P row r = (Q K^T)[r, :] masked to s <= r < L and decayed
+            const int r = tid;
+            const float gr = s.gam[st][r];
+            const float sr = g.l2norm ? s.rq[r] : 1.f;
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                float qk[32];
+                tmem_ld32(tmem_addr(t_p, warp, q * 32), qk);
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) {
+                    const int c2 = q * 32 + jj;
+                    qk[jj] = (c2 <= r && r < L)
+                                 ? qk[jj] * __expf(gr - s.gam[st][c2]) * sr * (g.l2norm ? s.rk[c2] : 1.f)
+                                 : 0.f;
+                }
+                st_row32(s.p, r, q * 32, qk);
+            }
+        }
+        tc_fence_before();
+        fence_proxy_async();
+        __syncthreads();
+        ++mma_n;
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t uT = smem_u32(s.uT), uTs = smem_u32(s.uTs), pp = smem_u32(s.p);
+            const uint32_t kt = smem_u32(s.qk[st]) + kTile;   // K rows of the stack
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t au = desc_sw128(uTs + kk * 32, 16, 1024);
+                const uint64_t bk = desc_sw128(kt + kk * 2048, 2 * kTile, 1024);
+                mma_bf16(t_dh, au, bk, kIdescDH, kk > 0);
+                if (out_now) {
+                    const uint64_t a2 = desc_sw128(uT + kk * 32, 16, 1024);
+                    const uint64_t b2 = desc_sw128(pp + kk * 32, 16, 1024);
+                    mma_bf16(t_oa, a2, b2, kIdesc64, kk > 0);
+                }
+            }
+            mma_commit(&s.mma_bar);
+        }
+        ok = mbar_wait(&s.mma_bar, (mma_n - 1) & 1, g.spin_limit, g.status);
+        if (__syncthreads_or(!ok)) { bailed = true; break; }
+        tc_fence_after();
+        if (out_now) {
+            __nv_bfloat16 *o = a.o + (bos * H + h) * (long long)kD + tid;
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                float oi[32], oa[32];
+                tmem_ld32(tmem_addr(t_oi, warp, q * 32), oi);
+                tmem_ld32(tmem_addr(t_oa, warp, q * 32), oa);
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) {
+                    const int r = q * 32 + jj;
+                    if (r < L) {
+                        const float inter = oi[jj] * __expf(s.gam[st][r]) * (g.l2norm ? s.rq[r] : 1.f);
+                        o[(long long)r * H * kD] = __float2bfloat16_rn(g.scale * (inter + oa[jj]));
+                    }
+                }
+            }
+        }
+        {
+            const float el = __expf(gl);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float d[32];
+                tmem_ld32(tmem_addr(t_dh, warp, q * 32), d);
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) Hr[q * 32 + jj] = el * Hr[q * 32 + jj] + d[jj];
+            }
+        }
+        write_state_rows(s.hT, tid, Hr);
+        tc_fence_before();
+        fence_proxy_async();
+        __syncthreads();
+    }
+
+    if (bailed) {
+        if (tid == 0) {
+            for (int st = 0; st < 2; ++st)
+                if (tma_pending & (1 << st))
+                    mbar_drain(&s.tma_bar[st], ((it + (st != (it & 1))) >> 1) & 1);
+            if (mma_n > 0) mbar_drain(&s.mma_bar, (mma_n - 1) & 1);
+        }
+    } else if (MODE == kWalkMap) {
+        float *dst = a.maps + ((long long)(seq_seg_base(g, n) + j) * H + h) * kD * (2 * kD);
+#pragma unroll
+        for (int i = 0; i < kD; ++i) dst[i * (2 * kD) + cb * kD + tid] = Hr[i];
+    } else if (a.final_state && j == nseg - 1) {
+        float *dst = a.final_state + ((long long)n * H + h) * kD * kD;
+#pragma unroll
+        for (int i = 0; i < kD; ++i) dst[i * kD + tid] = Hr[i];
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tbase, 512);
+}
+
+// ------------------------------------------------------------------ host side
+namespace {
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+cudaError_t encoder() {
+    if (g_encode) return cudaSuccess;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorSymbolNotFound;
+    g_encode = (EncodeTiledFn)fn;
+    return cudaSuccess;
+}
+
+// [tokens, H, 128] bf16 viewed as 3-D (feature, head, token); 64 x 1 x 64 boxes
+// with the 128-byte swizzle.  Rows past the last token read as zeros.
+cudaError_t make_map(CUtensorMap *m, const void *base, long long tokens, int H) {
+    const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)tokens};
+    const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2};
+    const cuuint32_t box[3] = {64, 1, 64};
+    const cuuint32_t es[3] = {1, 1, 1};
+    const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base),
+                                dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <typename F>
+cudaError_t set_smem(F kernel, size_t bytes) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+}  // namespace
+
+bool supported(const Plan &p) {
+    return p.dtype == GDN_BF16 && p.g.K == kD && p.g.V == kD && (long long)p.g.B * p.g.T > 0;
+}
+
+cudaError_t forward(const Plan &p, cudaStream_t s) {
+    cudaError_t e = simt::tables(p, s);
+    if (e != cudaSuccess) return e;
+    if ((e = encoder()) != cudaSuccess) return e;
+    const Geo &g = p.g;
+    const long long tokens = (long long)g.B * g.T;
+    CUtensorMap mq, mk, mv, mw, mu;
+    if ((e = make_map(&mq, g.q, tokens, g.H)) != cudaSuccess) return e;
+    if ((e = make_map(&mk, g.k, tokens, g.H)) != cudaSuccess) return e;
+    if ((e = make_map(&mv, g.v, tokens, g.H)) != cudaSuccess) return e;
+    if ((e = make_map(&mw, p.ws.w, tokens, g.H)) != cudaSuccess) return e;
+    if ((e = make_map(&mu, p.ws.u, tokens, g.H)) != cudaSuccess) return e;
+
+    const size_t prep_smem = sizeof(PrepSmem) + 1024, walk_smem = sizeof(WalkSmem) + 1024;
+    if ((e = set_smem(prep_kernel, prep_smem)) != cudaSuccess) return e;
+    if ((e = set_smem(walk_kernel<kWalkOut>, walk_smem)) != cudaSuccess) return e;
+    if ((e = set_smem(walk_kernel<kWalkMap>, walk_smem)) != cudaSuccess) return e;
+
+    prof_before("tc_prep", s);
+    prep_kernel<<<dim3((p.max_chunks + 1) / 2, g.H), 128, prep_smem, s>>>(
+        mk, mv, g, p.ws.gam, (__nv_bfloat16 *)p.ws.w, (__nv_bfloat16 *)p.ws.u);
+    prof_after(s);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+    TcWalkArgs a{};
+    a.ws_gam = p.ws.gam;
+    a.h0 = p.h0;
+    a.o = (__nv_bfloat16 *)p.o;
+    a.final_state = p.final_state;
+    if (p.cp) {
+        a.cp = 1;
+        a.maps = p.ws.maps;
+        a.seg_start = p.ws.seg_state;
+        if (p.warm_chunks > 0) {
+            if ((e = simt::warm_decide(p, s)) != cudaSuccess) return e;
+            a.warm = p.ws.warm;
+            a.warm_chunks = p.warm_chunks;
+        }
+        prof_before("tc_walk_map", s);
+        walk_kernel<kWalkMap><<<dim3(p.max_segs, g.H, 2), 128, walk_smem, s>>>(mq, mk, mw, mu, g, a);
+        prof_after(s);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = simt::cp_scan(p, a.warm, s)) != cudaSuccess) return e;
+        prof_before("tc_walk_out", s);
+        walk_kernel<kWalkOut><<<dim3(p.max_segs, g.H, 1), 128, walk_smem, s>>>(mq, mk, mw, mu, g, a);
+        prof_after(s);
+    } else {
+        prof_before("tc_walk_out", s);
+        walk_kernel<kWalkOut><<<dim3(g.N, g.H, 1), 128, walk_smem, s>>>(mq, mk, mw, mu, g, a);
+        prof_after(s);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace tc
+}  // namespace gdn

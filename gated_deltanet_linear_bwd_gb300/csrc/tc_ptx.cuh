@@ -1,0 +1,208 @@
+// tc_ptx.cuh -- thin inline-PTX wrappers for the Blackwell (sm_103a) data
+// path used by the tensor-core kernels: mbarriers, TMA tiled loads,
+// tcgen05 MMA with TMEM accumulators, TMEM loads, and the shared-memory /
+// instruction descriptors those MMAs take.
+//
+// Shared-memory operand tiles are written in the canonical 128-byte-swizzle
+// layout (the layout TMA produces with CU_TENSOR_MAP_SWIZZLE_128B): rows of
+// 128 bytes, 8-row atoms of 1024 bytes, the 16-byte chunk index of a row
+// XORed with (row % 8).  Every tile base is 1024-byte aligned.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "gdn_common.cuh"
+
+namespace gdn {
+namespace tc {
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// ------------------------------------------------------------------ mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait: gives up after `limit` polls, records GDN_ERR_TIMEOUT in the
+// status word and returns false.  Callers then skip the rest of their work.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, long long limit,
+                                          int *status) {
+    for (long long i = 0; i < limit; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    set_status(status, GDN_ERR_TIMEOUT);
+    return false;
+}
+// After a wait gave up: waits (with a fixed limit, independent of the
+// testing hook) for the last phase still in flight on `bar`, so that no
+// asynchronous write lands after the CTA has released its TMEM and exited.
+__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity) {
+    for (long long i = 0; i < (1ll << 22); ++i)
+        if (mbar_try_wait(bar, parity)) return;
+}
+
+// ------------------------------------------------------------------ TMA
+// 3-D tiled load (coordinates innermost first) completing on `bar`.
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ TMEM / tcgen05
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols) {  // one full warp
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {  // same warp
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem], bf16 inputs, fp32 accumulation.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "setp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+        "}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrives on `bar` once every MMA issued so far by this thread has completed.
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+// Loads 32 consecutive fp32 columns of this thread's TMEM lane (32x32b
+// shape: warp w reads lanes 32*(w%4) .. +31) and waits for them in the same
+// asm block, so no use of the registers can be scheduled before the wait.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// TMEM address of (lane base of this warp, column col).
+__device__ __forceinline__ uint32_t tmem_addr(uint32_t base, int warp, int col) {
+    return base + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)col;
+}
+
+// ------------------------------------------------------------------ descriptors
+// Shared-memory matrix descriptor, 128-byte swizzle (sm_100 format:
+// start >> 4 in bits 0-13, leading byte offset >> 4 in 16-29, stride byte
+// offset >> 4 in 32-45, version 1 in bits 46-47, layout SWIZZLE_128B = 2 in
+// bits 61-63).  K-major tiles: sbo = 1024 (8-row groups), lbo unused.
+// MN-major tiles: lbo = stride between 64-element MN blocks, sbo = stride
+// between 8-row groups along K.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor of kind::f16: bf16 A and B, fp32 D; a_mn / b_mn
+// select MN-major (transposed) operands.  N >> 3 in bits 17-22, M >> 4 in
+// bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
+           ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Byte offset of element (row, col) of a bf16 tile with 128-byte rows in the
+// 128-byte swizzle layout (the tile base 1024-byte aligned).
+__device__ __forceinline__ uint32_t sw128_off(int row, int col) {
+    const uint32_t chunk = (uint32_t)(col >> 3) ^ (uint32_t)(row & 7);
+    return (uint32_t)row * 128u + (chunk << 4) + (uint32_t)(col & 7) * 2u;
+}
+
+// Writes 32 bf16 values (columns col0 .. col0+31, col0 in {0, 32}) of a
+// 128-byte swizzled row (4 x 16-byte stores).
+__device__ __forceinline__ void st_row32(uint8_t *tile, int row, int col0, const float *x) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint32_t w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            __nv_bfloat162 b = __floats2bfloat162_rn(x[8 * c + 2 * j], x[8 * c + 2 * j + 1]);
+            w[j] = *reinterpret_cast<uint32_t *>(&b);
+        }
+        const uint32_t chunk = (uint32_t)((col0 >> 3) + c) ^ (uint32_t)(row & 7);
+        *reinterpret_cast<uint4 *>(tile + row * 128 + chunk * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+// Writes 64 bf16 values as one whole 128-byte swizzled row.
+__device__ __forceinline__ void st_row64(uint8_t *tile, int row, const float *x) {
+    st_row32(tile, row, 0, x);
+    st_row32(tile, row, 32, x + 32);
+}
+
+__device__ __forceinline__ float ld_bf16(const uint8_t *tile, int row, int col) {
+    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tile + sw128_off(row, col)));
+}
+
+}  // namespace tc
+}  // namespace gdn

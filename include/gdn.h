@@ -153,10 +153,11 @@ gdn_status gdn_sync_status(void *stream);
 /* Message for the last non-OK status returned on this host thread. */
 const char *gdn_last_error(void);
 
-/* Testing hook: iteration limit of every bounded device-side wait
- * (default 1 << 26 polls; values < 1 restore the default).  A limit of 1
- * makes a wait give up at once and report GDN_ERR_TIMEOUT; the kernels
- * then finish without touching their outputs further. */
+/* Testing hook: iteration limit of every bounded device-side wait (default
+ * 1 << 21 polls; a negative value restores the default).  A limit of 0 makes
+ * every wait give up at once: the kernel records GDN_ERR_TIMEOUT, waits for
+ * its own copies and MMAs still in flight, frees its tensor memory and
+ * returns without finishing its outputs.  Takes effect for later calls. */
 void gdn_set_spin_limit(int64_t polls);
 
 /* Per-kernel tracing.  Between gdn_profile_begin() and gdn_profile_end()

@@ -124,6 +124,26 @@ def test_bad_cu_seqlens_sets_the_status_word():
     assert gdn.gdn_sync_status(torch.cuda.current_stream().cuda_stream) == 0  # cleared
 
 
+def test_bounded_wait_gives_up_and_reports_timeout():
+    """Spin limit 0: every bounded wait of the tensor-core kernels gives up at
+    once; the status word reports GDN_ERR_TIMEOUT and the context stays usable."""
+    gdn = lib()
+    p = gdn_synth.make("training", B=1, T=300, H=2, h0_std=0.1)
+    stream = torch.cuda.current_stream().cuda_stream
+    assert gdn.gdn_sync_status(stream) == 0
+    gdn.gdn_set_spin_limit(0)
+    try:
+        gpu_fwd(p)
+        assert gdn.gdn_sync_status(stream) == 5
+    finally:
+        gdn.gdn_set_spin_limit(-1)
+    o, fs = gpu_fwd(p)
+    ro, rfs = oracle_fwd(p)
+    check("o after timeout", o, ro, TOL["bf16"])
+    check("final_state after timeout", fs, rfs, TOL["bf16"])
+    assert gdn.gdn_sync_status(stream) == 0
+
+
 def test_autograd_wrapper_matches_low_level_backward():
     gdn = lib()
     p = gdn_synth.make("tiny", T=130, h0_std=0.1).to("cuda")
