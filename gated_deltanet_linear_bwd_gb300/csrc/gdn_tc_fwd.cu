@@ -57,7 +57,7 @@ __device__ __forceinline__ float scan64(float x, float *wsum) {
 }
 
 __global__ void __launch_bounds__(128, 2)
-prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
             Geo g, float *ws_gam, __nv_bfloat16 *ws_w, __nv_bfloat16 *ws_u) {
     extern __shared__ uint8_t smem_raw[];
     PrepSmem &s = *reinterpret_cast<PrepSmem *>(
@@ -281,7 +281,7 @@ __device__ __forceinline__ void write_state_rows(uint8_t *hT, int row, const flo
 
 template <int MODE>
 __global__ void __launch_bounds__(128, 1)
-walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_u,
             Geo g, TcWalkArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -596,12 +596,12 @@ cudaError_t forward(const Plan &p, cudaStream_t s) {
     if ((e = make_map(&mu, p.ws.u, tokens, g.H)) != cudaSuccess) return e;
 
     const size_t prep_smem = sizeof(PrepSmem) + 1024, walk_smem = sizeof(WalkSmem) + 1024;
-    if ((e = set_smem(prep_kernel, prep_smem)) != cudaSuccess) return e;
-    if ((e = set_smem(walk_kernel<kWalkOut>, walk_smem)) != cudaSuccess) return e;
-    if ((e = set_smem(walk_kernel<kWalkMap>, walk_smem)) != cudaSuccess) return e;
+    if ((e = set_smem(tc_prep_kernel, prep_smem)) != cudaSuccess) return e;
+    if ((e = set_smem(tc_walk_kernel<kWalkOut>, walk_smem)) != cudaSuccess) return e;
+    if ((e = set_smem(tc_walk_kernel<kWalkMap>, walk_smem)) != cudaSuccess) return e;
 
     prof_before("tc_prep", s);
-    prep_kernel<<<dim3((p.max_chunks + 1) / 2, g.H), 128, prep_smem, s>>>(
+    tc_prep_kernel<<<dim3((p.max_chunks + 1) / 2, g.H), 128, prep_smem, s>>>(
         mk, mv, g, p.ws.gam, (__nv_bfloat16 *)p.ws.w, (__nv_bfloat16 *)p.ws.u);
     prof_after(s);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -621,16 +621,16 @@ cudaError_t forward(const Plan &p, cudaStream_t s) {
             a.warm_chunks = p.warm_chunks;
         }
         prof_before("tc_walk_map", s);
-        walk_kernel<kWalkMap><<<dim3(p.max_segs, g.H, 2), 128, walk_smem, s>>>(mq, mk, mw, mu, g, a);
+        tc_walk_kernel<kWalkMap><<<dim3(p.max_segs, g.H, 2), 128, walk_smem, s>>>(mq, mk, mw, mu, g, a);
         prof_after(s);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if ((e = simt::cp_scan(p, a.warm, s)) != cudaSuccess) return e;
         prof_before("tc_walk_out", s);
-        walk_kernel<kWalkOut><<<dim3(p.max_segs, g.H, 1), 128, walk_smem, s>>>(mq, mk, mw, mu, g, a);
+        tc_walk_kernel<kWalkOut><<<dim3(p.max_segs, g.H, 1), 128, walk_smem, s>>>(mq, mk, mw, mu, g, a);
         prof_after(s);
     } else {
         prof_before("tc_walk_out", s);
-        walk_kernel<kWalkOut><<<dim3(g.N, g.H, 1), 128, walk_smem, s>>>(mq, mk, mw, mu, g, a);
+        tc_walk_kernel<kWalkOut><<<dim3(g.N, g.H, 1), 128, walk_smem, s>>>(mq, mk, mw, mu, g, a);
         prof_after(s);
     }
     return cudaGetLastError();
