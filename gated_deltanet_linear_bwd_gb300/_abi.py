@@ -46,7 +46,8 @@ class gdn_kernel_stat(ctypes.Structure):
 
 EXPORTS = ("gdn_abi_version", "gdn_fwd_workspace_size", "gdn_chunk_fwd", "gdn_bwd_workspace_size",
            "gdn_chunk_bwd", "gdn_sync_status", "gdn_last_error", "gdn_set_spin_limit",
-           "gdn_profile_begin", "gdn_profile_end")
+           "gdn_profile_begin", "gdn_profile_end", "gdn_chunk_fwd_static")
+GDN_STATIC_SCRATCH_BYTES = 64 << 20
 
 _lib = None
 
@@ -76,6 +77,8 @@ def load(path: str = LIB_PATH):
     lib.gdn_last_error.argtypes = []
     lib.gdn_set_spin_limit.restype = None
     lib.gdn_set_spin_limit.argtypes = [ctypes.c_int64]
+    lib.gdn_chunk_fwd_static.restype = _i32
+    lib.gdn_chunk_fwd_static.argtypes = [ctypes.POINTER(gdn_fwd_args), _vp]
     lib.gdn_profile_begin.restype = _i32
     lib.gdn_profile_begin.argtypes = []
     lib.gdn_profile_end.restype = _i32
@@ -143,3 +146,11 @@ def gdn_profile_end(max_kernels: int = 64):
     n = int(load().gdn_profile_end(buf, max_kernels))
     return [(buf[i].name.decode(), int(buf[i].launches), float(buf[i].total_ms))
             for i in range(min(n, max_kernels))]
+
+
+def gdn_chunk_fwd_static(args: gdn_fwd_args, stream: int) -> None:
+    """Forward without a workspace: scratch comes from the library's fixed
+    GDN_STATIC_SCRATCH_BYTES device area (see include/gdn.h)."""
+    rc = load().gdn_chunk_fwd_static(ctypes.byref(args), _vp(stream))
+    if rc != GDN_OK:
+        raise GdnError("gdn_chunk_fwd_static", rc)

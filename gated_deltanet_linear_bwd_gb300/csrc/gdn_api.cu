@@ -420,3 +420,42 @@ int32_t gdn_profile_end(gdn_kernel_stat *out, int32_t max) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- static-scratch forward
+// The allocation-free forward keeps its workspace in this file-scope array.
+// In host code `g_static_scratch` names a host-side stand-in, not device
+// memory, so its device address is looked up once per device with
+// cudaGetSymbolAddress and only that address is handed to the kernels.
+namespace gdn {
+static __device__ __align__(256) unsigned char g_static_scratch[GDN_STATIC_SCRATCH_BYTES];
+static void *g_static_ptr[64];
+static std::mutex g_static_mu;
+}  // namespace gdn
+
+extern "C" gdn_status gdn_chunk_fwd_static(const gdn_fwd_args *a, void *stream) {
+    if (!a) return fail(GDN_ERR_INVALID_ARG, "null args");
+    const size_t need = gdn_fwd_workspace_size(a);
+    if (need == 0) return GDN_ERR_INVALID_ARG;     // gdn_last_error already says why
+    if (need > GDN_STATIC_SCRATCH_BYTES)
+        return fail(GDN_ERR_WORKSPACE,
+                    "gdn_chunk_fwd_static: this problem needs %zu bytes of scratch, more than "
+                    "the %zu-byte static scratch area; call gdn_chunk_fwd with a workspace",
+                    need, (size_t)GDN_STATIC_SCRATCH_BYTES);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(GDN_ERR_UNSUPPORTED, "device index %d out of range", dev);
+    void *scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_static_mu);
+        if (!g_static_ptr[dev]) {
+            e = cudaGetSymbolAddress(&g_static_ptr[dev], g_static_scratch);
+            if (e != cudaSuccess) {
+                g_static_ptr[dev] = nullptr;
+                return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+            }
+        }
+        scratch = g_static_ptr[dev];
+    }
+    return gdn_chunk_fwd(a, scratch, GDN_STATIC_SCRATCH_BYTES, stream);
+}

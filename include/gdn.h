@@ -146,6 +146,31 @@ size_t gdn_bwd_workspace_size(const gdn_bwd_args *args);
 gdn_status gdn_chunk_bwd(const gdn_bwd_args *args, void *workspace, size_t workspace_bytes,
                          void *stream);
 
+/* Forward for callers that cannot allocate device memory.  No counterpart
+ * on the pages: this is a library-usage addition.  Some callers cannot call
+ * cudaMalloc -- for example a plugin running inside a host framework that
+ * owns every device allocation, or a latency-critical server thread that
+ * must never hit cudaMalloc's implicit device synchronisation -- so they
+ * cannot hand gdn_chunk_fwd a workspace.  This entry point takes the same
+ * arguments without a workspace and uses a fixed scratch area built into
+ * the library instead: GDN_STATIC_SCRATCH_BYTES (64 MiB) of device memory
+ * that every GPU which loads the library holds until the process exits.
+ *
+ * - The caller still allocates and passes every input and output.
+ * - Problems whose gdn_fwd_workspace_size exceeds GDN_STATIC_SCRATCH_BYTES
+ *   are rejected with GDN_ERR_WORKSPACE before any work is queued.
+ * - The first call on a device looks up the scratch area's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture on the device.
+ * - Every call on a device shares the one scratch area, which keeps the
+ *   last call's contents; the forward writes every scratch byte it reads,
+ *   so nothing needs clearing between calls.  Calls whose work overlaps on
+ *   the GPU (other streams, other host threads) race on the scratch area:
+ *   order them, for example on one stream.
+ * - Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
+#define GDN_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
+gdn_status gdn_chunk_fwd_static(const gdn_fwd_args *args, void *stream);
+
 /* Synchronises `stream`, then reads and clears this device's status word:
  * GDN_OK, GDN_ERR_BAD_SEQLENS, GDN_ERR_TIMEOUT or GDN_ERR_CUDA. */
 gdn_status gdn_sync_status(void *stream);
