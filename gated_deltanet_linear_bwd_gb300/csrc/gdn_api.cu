@@ -192,6 +192,7 @@ static size_t layout(Plan &p, bool bwd, char *base) {
         const size_t st = (size_t)p.max_chunks * g.H * g.K * g.V * sizeof(float);
         w.hc = (float *)take(st);
         w.dhc = (float *)take(st);
+        w.du = take(th * g.V * 2);
         w.scratch = (float *)take((size_t)p.scratch_ctas *
                                   simt::scratch_floats_per_cta(g.K, g.V) * sizeof(float));
     }
@@ -312,7 +313,7 @@ gdn_status gdn_chunk_bwd(const gdn_bwd_args *a, void *ws, size_t ws_bytes, void 
     p.dq = a->dq; p.dk = a->dk; p.dv = a->dv;
     p.dg = a->dg; p.dbeta = a->dbeta; p.dh0 = a->d_initial_state;
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t e = simt::backward(p, s);
+    cudaError_t e = tc::supported(p) ? tc::backward(p, s) : simt::backward(p, s);
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
     return GDN_OK;
 }

@@ -2,6 +2,7 @@
 // and the kernel launchers.  Not part of the public ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -22,6 +23,7 @@ struct Ws {
     float *seg_state = nullptr;    // [segs, H, K, V] segment start states / end gradients
     float *hc = nullptr;           // [chunks, H, K, V] chunk start states (bwd)
     float *dhc = nullptr;          // [chunks, H, K, V] chunk end gradients (bwd)
+    void *du = nullptr;            // [tokens, H, V] bf16 dU of the reverse walk (bwd, tensor cores)
     float *scratch = nullptr;      // per-CTA scratch (bwd, CUDA-core path)
     int32_t *counters = nullptr;   // small zeroed counters
 };
@@ -65,12 +67,21 @@ cudaError_t forward(const Plan &p, cudaStream_t s);
 cudaError_t backward(const Plan &p, cudaStream_t s);
 cudaError_t warm_decide(const Plan &p, cudaStream_t s);
 cudaError_t cp_scan(const Plan &p, const int32_t *warm, cudaStream_t s);
+cudaError_t cp_rscan(const Plan &p, cudaStream_t s);
+// Chunk-local gradients from p.ws.hc / p.ws.dhc; W and u read as bf16 when ws_bf16.
+cudaError_t local_grads(const Plan &p, cudaStream_t s, bool ws_bf16);
 }  // namespace simt
 
 namespace tc {
 // bf16 q/k/v with K = V = 128 and at least one token.
 bool supported(const Plan &p);
 cudaError_t forward(const Plan &p, cudaStream_t s);
+// Backward pieces: prep + walk storing chunk start states (p.ws.hc).
+cudaError_t recompute_states(const Plan &p, cudaStream_t s);
+cudaError_t backward(const Plan &p, cudaStream_t s);
+// TMA descriptors of [tokens, H, 128] bf16 tensors (64 x 1 x 64 boxes, 128B swizzle).
+cudaError_t encoder();
+cudaError_t make_map(CUtensorMap *m, const void *base, long long tokens, int H);
 }  // namespace tc
 
 }  // namespace gdn

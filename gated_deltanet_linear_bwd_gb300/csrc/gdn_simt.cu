@@ -284,37 +284,57 @@ walk_kernel(Geo g, WalkArgs a) {
     }
 }
 
-// ---------------------------------------------------------------- CP scan
-// Exclusive scan of the segment maps: start[j+1] = A_j start[j] + B_j with
-// start[0] = h0.  One CTA per (sequence, head, block of kBV state columns).
-// Heads on the warmup shortcut skip it.
-__global__ void __launch_bounds__(kThreads)
-cp_scan_kernel(Geo g, const float *maps, const float *h0, const int32_t *warm, float *seg_start) {
-    const int n = blockIdx.x, h = blockIdx.y, col0 = blockIdx.z * kBV, K = g.K, V = g.V,
+// ---------------------------------------------------------------- CP scans
+// Exclusive scan of segment maps S -> A S + B over one (sequence, head,
+// block of kSB state columns).  Forward (reverse = 0): start[0] = h0 and
+// start[j+1] = A_j start[j] + B_j.  Backward (reverse = 1): end[nseg-1] =
+// d(final state) and end[j-1] = A'_j end[j] + B'_j.  Thread t owns row t/2
+// and four of the kSB columns; it streams its map row with 16-byte loads.
+constexpr int kSB = 8;
+
+__global__ void __launch_bounds__(256)
+map_scan_kernel(Geo g, const float *maps, const float *init, const int32_t *warm, float *out,
+                int reverse) {
+    const int n = blockIdx.x, h = blockIdx.y, col0 = blockIdx.z * kSB, K = g.K, V = g.V,
               H = g.H;
     if (n >= g.N || col0 >= V) return;
     if (warm && warm[n * H + h]) return;
     const int nseg = seq_nsegs(g, n), sbase = seq_seg_base(g, n);
-    extern __shared__ float sm[];
-    float *S = sm, *S2 = sm + K * kBV;
-    for (int idx = threadIdx.x; idx < K * kBV; idx += blockDim.x) {
-        const int i = idx / kBV, c = col0 + idx % kBV;
-        S[idx] = h0 ? h0[(((long long)n * H + h) * K + i) * V + c] : 0.f;
+    __shared__ __align__(16) float S[128][kSB];
+    const int t = threadIdx.x, i = t >> 1, jq = (t & 1) * 4;
+    const bool act = i < K;
+    for (int idx = t; idx < K * kSB; idx += blockDim.x) {
+        const int r = idx / kSB, c = col0 + idx % kSB;
+        S[r][idx % kSB] = init ? init[(((long long)n * H + h) * K + r) * V + c] : 0.f;
     }
     __syncthreads();
-    for (int j = 0; j + 1 < nseg; ++j) {
+    for (int step = 0; step + 1 < nseg; ++step) {
+        const int j = reverse ? nseg - 1 - step : step;      // map applied
+        const int jo = reverse ? j - 1 : j + 1;              // segment that receives the state
         const float *M = maps + ((long long)(sbase + j) * H + h) * K * (K + V);
-        for (int idx = threadIdx.x; idx < K * kBV; idx += blockDim.x) {
-            const int i = idx / kBV, jj = idx % kBV;
-            float acc = M[i * (K + V) + K + col0 + jj];
-            for (int l = 0; l < K; ++l) acc += M[i * (K + V) + l] * S[l * kBV + jj];
-            S2[idx] = acc;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (act) {
+            const float *row = M + (long long)i * (K + V);
+            acc = *reinterpret_cast<const float4 *>(row + K + col0 + jq);
+            const float4 *row4 = reinterpret_cast<const float4 *>(row);
+            for (int l4 = 0; l4 < K / 4; ++l4) {
+                const float4 a4 = row4[l4];
+                const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float4 s4 = *reinterpret_cast<const float4 *>(&S[4 * l4 + e][jq]);
+                    acc.x += av[e] * s4.x;
+                    acc.y += av[e] * s4.y;
+                    acc.z += av[e] * s4.z;
+                    acc.w += av[e] * s4.w;
+                }
+            }
         }
         __syncthreads();
-        float *dst = seg_start + ((long long)(sbase + j + 1) * H + h) * K * V;
-        for (int idx = threadIdx.x; idx < K * kBV; idx += blockDim.x) {
-            S[idx] = S2[idx];
-            dst[(idx / kBV) * V + col0 + idx % kBV] = S2[idx];
+        if (act) {
+            *reinterpret_cast<float4 *>(&S[i][jq]) = acc;
+            float *dst = out + (((long long)(sbase + jo) * H + h) * K + i) * V + col0 + jq;
+            *reinterpret_cast<float4 *>(dst) = acc;
         }
         __syncthreads();
     }
@@ -491,39 +511,6 @@ dwalk_kernel(Geo g, DWalkArgs a) {
     }
 }
 
-// Reverse exclusive scan of the backward maps: end[j-1] = A'_j end[j] + B'_j
-// with end[nseg-1] = d(final_state).
-__global__ void __launch_bounds__(kThreads)
-cp_rscan_kernel(Geo g, const float *maps, const float *dht, float *seg_end) {
-    const int n = blockIdx.x, h = blockIdx.y, col0 = blockIdx.z * kBV, K = g.K, V = g.V,
-              H = g.H;
-    if (n >= g.N || col0 >= V) return;
-    const int nseg = seq_nsegs(g, n), sbase = seq_seg_base(g, n);
-    extern __shared__ float sm[];
-    float *S = sm, *S2 = sm + K * kBV;
-    for (int idx = threadIdx.x; idx < K * kBV; idx += blockDim.x) {
-        const int i = idx / kBV, c = col0 + idx % kBV;
-        S[idx] = dht ? dht[(((long long)n * H + h) * K + i) * V + c] : 0.f;
-    }
-    __syncthreads();
-    for (int j = nseg - 1; j >= 1; --j) {
-        const float *M = maps + ((long long)(sbase + j) * H + h) * K * (K + V);
-        for (int idx = threadIdx.x; idx < K * kBV; idx += blockDim.x) {
-            const int i = idx / kBV, jj = idx % kBV;
-            float acc = M[i * (K + V) + K + col0 + jj];
-            for (int l = 0; l < K; ++l) acc += M[i * (K + V) + l] * S[l * kBV + jj];
-            S2[idx] = acc;
-        }
-        __syncthreads();
-        float *dst = seg_end + ((long long)(sbase + j - 1) * H + h) * K * V;
-        for (int idx = threadIdx.x; idx < K * kBV; idx += blockDim.x) {
-            S[idx] = S2[idx];
-            dst[(idx / kBV) * V + col0 + idx % kBV] = S2[idx];
-        }
-        __syncthreads();
-    }
-}
-
 // ---------------------------------------------------------------- local gradients
 // Per (chunk, head), from the chunk's start state H0 (hc) and the gradient
 // at its end dHL (dhc); chain rule through the chunk form above:
@@ -539,7 +526,8 @@ cp_rscan_kernel(Geo g, const float *maps, const float *dht, float *seg_end) {
 //   dgam from every exp(gam ...) factor; dg = reverse cumsum of dgam in the chunk
 // followed by the L2-norm backward when q, k were normalised.
 struct LocalArgs {
-    const float *ws_gam, *ws_w, *ws_u, *hc, *dhc;
+    const float *ws_gam, *hc, *dhc;
+    const void *ws_w, *ws_u;         // fp32 or bf16 (template TW)
     const void *d_o;
     void *dq, *dk, *dv;
     float *dg, *dbeta;
@@ -547,7 +535,7 @@ struct LocalArgs {
     int n_items;             // chunk capacity * H
 };
 
-template <typename TI, typename TG>
+template <typename TI, typename TG, typename TW>
 __global__ void __launch_bounds__(kThreads)
 local_grad_kernel(Geo g, LocalArgs a) {
     const int K = g.K, V = g.V, H = g.H, tid = threadIdx.x;
@@ -621,11 +609,11 @@ local_grad_kernel(Geo g, LocalArgs a) {
         // U = u - W H0 ; dU = scale P^T dO + diag(f) K dHL
         for (int idx = tid; idx < L * V; idx += blockDim.x) {
             const int r = idx / V, j = idx % V;
-            const float *wr = a.ws_w + ((bos + r) * H + h) * (long long)K;
-            float u = a.ws_u[((bos + r) * H + h) * (long long)V + j];
+            const TW *wr = (const TW *)a.ws_w + ((bos + r) * H + h) * (long long)K;
+            float u = to_f(((const TW *)a.ws_u)[((bos + r) * H + h) * (long long)V + j]);
             float kd = 0.f;
             for (int i = 0; i < K; ++i) {
-                u -= wr[i] * H0[i * V + j];
+                u -= to_f(wr[i]) * H0[i * V + j];
                 kd += Ks[r * (K + 1) + i] * dHL[i * V + j];
             }
             float pd = 0.f;
@@ -909,8 +897,8 @@ static cudaError_t forward_t(const Plan &p, cudaStream_t s, bool states_only) {
         }
         GDN_LAUNCH("simt_walk_map", (walk_kernel<TI, kMap>), dim3(p.max_segs, H, (K + V) / kBV), walk_smem(K), s,
                    g, a);
-        GDN_LAUNCH("simt_cp_scan", cp_scan_kernel, dim3(g.N, H, V / kBV), sizeof(float) * 2 * K * kBV, s, g,
-                   (const float *)p.ws.maps, p.h0, (const int32_t *)a.warm, p.ws.seg_state);
+        GDN_LAUNCH("map_scan", map_scan_kernel, dim3(g.N, H, V / kSB), 0, s, g,
+                   (const float *)p.ws.maps, p.h0, (const int32_t *)a.warm, p.ws.seg_state, 0);
         GDN_LAUNCH(states_only ? "simt_walk_states" : "simt_walk_out", (walk_kernel<TI, kOut>), dim3(p.max_segs, H, V / kBV), walk_smem(K), s, g, a);
     } else {
         GDN_LAUNCH(states_only ? "simt_walk_states" : "simt_walk_out", (walk_kernel<TI, kOut>), dim3(g.N, H, V / kBV), walk_smem(K), s, g, a);
@@ -928,9 +916,8 @@ cudaError_t warm_decide(const Plan &p, cudaStream_t s) {
 
 cudaError_t cp_scan(const Plan &p, const int32_t *warm, cudaStream_t s) {
     const Geo &g = p.g;
-    GDN_LAUNCH("simt_cp_scan", cp_scan_kernel, dim3(g.N, g.H, g.V / kBV),
-               sizeof(float) * 2 * g.K * kBV, s, g, (const float *)p.ws.maps, p.h0, warm,
-               p.ws.seg_state);
+    GDN_LAUNCH("map_scan", map_scan_kernel, dim3(g.N, g.H, g.V / kSB), 0, s, g,
+               (const float *)p.ws.maps, p.h0, warm, p.ws.seg_state, 0);
     return cudaSuccess;
 }
 
@@ -939,6 +926,29 @@ cudaError_t forward(const Plan &p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     return p.dtype == GDN_BF16 ? forward_t<__nv_bfloat16>(p, s, false)
                                : forward_t<float>(p, s, false);
+}
+
+template <typename TI, typename TG, typename TW>
+static cudaError_t local_grads_t(const Plan &p, cudaStream_t s) {
+    const Geo &g = p.g;
+    LocalArgs l{};
+    l.ws_gam = p.ws.gam;
+    l.ws_w = p.ws.w;
+    l.ws_u = p.ws.u;
+    l.hc = p.ws.hc;
+    l.dhc = p.ws.dhc;
+    l.d_o = p.d_o;
+    l.dq = p.dq;
+    l.dk = p.dk;
+    l.dv = p.dv;
+    l.dg = p.dg;
+    l.dbeta = p.dbeta;
+    l.scratch = p.ws.scratch;
+    l.n_items = p.max_chunks * g.H;
+    const int grid = l.n_items < p.scratch_ctas ? l.n_items : p.scratch_ctas;
+    GDN_LAUNCH("simt_local_grad", (local_grad_kernel<TI, TG, TW>), dim3(grid, 1, 1),
+               local_smem(g.K), s, g, l);
+    return cudaSuccess;
 }
 
 template <typename TI, typename TG>
@@ -960,29 +970,34 @@ static cudaError_t backward_t(const Plan &p, cudaStream_t s) {
         d.cp = 1;
         GDN_LAUNCH("simt_dwalk_map", (dwalk_kernel<TI, kMap>), dim3(p.max_segs, H, (K + V) / kBV), dwalk_smem(K), s,
                    g, d);
-        GDN_LAUNCH("simt_cp_rscan", cp_rscan_kernel, dim3(g.N, H, V / kBV), sizeof(float) * 2 * K * kBV, s, g,
-                   (const float *)p.ws.maps, p.dht, p.ws.seg_state);
+        GDN_LAUNCH("map_rscan", map_scan_kernel, dim3(g.N, H, V / kSB), 0, s, g,
+                   (const float *)p.ws.maps, p.dht, (const int32_t *)nullptr, p.ws.seg_state, 1);
         GDN_LAUNCH("simt_dwalk_out", (dwalk_kernel<TI, kOut>), dim3(p.max_segs, H, V / kBV), dwalk_smem(K), s, g,
                    d);
     } else {
         GDN_LAUNCH("simt_dwalk_out", (dwalk_kernel<TI, kOut>), dim3(g.N, H, V / kBV), dwalk_smem(K), s, g, d);
     }
-    LocalArgs l{};
-    l.ws_gam = p.ws.gam;
-    l.ws_w = (const float *)p.ws.w;
-    l.ws_u = (const float *)p.ws.u;
-    l.hc = p.ws.hc;
-    l.dhc = p.ws.dhc;
-    l.d_o = p.d_o;
-    l.dq = p.dq;
-    l.dk = p.dk;
-    l.dv = p.dv;
-    l.dg = p.dg;
-    l.dbeta = p.dbeta;
-    l.scratch = p.ws.scratch;
-    l.n_items = p.max_chunks * H;
-    const int grid = l.n_items < p.scratch_ctas ? l.n_items : p.scratch_ctas;
-    GDN_LAUNCH("simt_local_grad", (local_grad_kernel<TI, TG>), dim3(grid, 1, 1), local_smem(K), s, g, l);
+    return local_grads_t<TI, TG, float>(p, s);
+}
+
+cudaError_t local_grads(const Plan &p, cudaStream_t s, bool ws_bf16) {
+    typedef __nv_bfloat16 bf;
+    if (ws_bf16) {   // only the tensor-core recompute (bf16 inputs) leaves W, u in bf16
+        if (p.dtype != GDN_BF16) return cudaErrorInvalidValue;
+        return p.grad_dtype == GDN_BF16 ? local_grads_t<bf, bf, bf>(p, s)
+                                        : local_grads_t<bf, float, bf>(p, s);
+    }
+    if (p.dtype == GDN_BF16)
+        return p.grad_dtype == GDN_BF16 ? local_grads_t<bf, bf, float>(p, s)
+                                        : local_grads_t<bf, float, float>(p, s);
+    return p.grad_dtype == GDN_BF16 ? local_grads_t<float, bf, float>(p, s)
+                                    : local_grads_t<float, float, float>(p, s);
+}
+
+cudaError_t cp_rscan(const Plan &p, cudaStream_t s) {
+    const Geo &g = p.g;
+    GDN_LAUNCH("map_rscan", map_scan_kernel, dim3(g.N, g.H, g.V / kSB), 0, s, g,
+               (const float *)p.ws.maps, p.dht, (const int32_t *)nullptr, p.ws.seg_state, 1);
     return cudaSuccess;
 }
 

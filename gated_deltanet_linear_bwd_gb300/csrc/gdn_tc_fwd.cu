@@ -546,6 +546,12 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
 
+template <typename F>
+cudaError_t set_smem(F kernel, size_t bytes) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+}  // namespace
+
 cudaError_t encoder() {
     if (g_encode) return cudaSuccess;
     void *fn = nullptr;
@@ -572,20 +578,15 @@ cudaError_t make_map(CUtensorMap *m, const void *base, long long tokens, int H) 
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <typename F>
-cudaError_t set_smem(F kernel, size_t bytes) {
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-}
-}  // namespace
-
 bool supported(const Plan &p) {
     return p.dtype == GDN_BF16 && p.g.K == kD && p.g.V == kD && (long long)p.g.B * p.g.T > 0;
 }
 
-cudaError_t forward(const Plan &p, cudaStream_t s) {
-    cudaError_t e = simt::tables(p, s);
+// Prep, then the walk: with output (states_only = false) or storing every
+// chunk's start state into p.ws.hc (states_only = true, for the backward).
+static cudaError_t run_forward(const Plan &p, cudaStream_t s, bool states_only) {
+    cudaError_t e = encoder();
     if (e != cudaSuccess) return e;
-    if ((e = encoder()) != cudaSuccess) return e;
     const Geo &g = p.g;
     const long long tokens = (long long)g.B * g.T;
     CUtensorMap mq, mk, mv, mw, mu;
@@ -609,13 +610,15 @@ cudaError_t forward(const Plan &p, cudaStream_t s) {
     TcWalkArgs a{};
     a.ws_gam = p.ws.gam;
     a.h0 = p.h0;
-    a.o = (__nv_bfloat16 *)p.o;
-    a.final_state = p.final_state;
+    a.o = states_only ? nullptr : (__nv_bfloat16 *)p.o;
+    a.final_state = states_only ? nullptr : p.final_state;
+    a.hc = states_only ? p.ws.hc : nullptr;
+    const char *out_name = states_only ? "tc_walk_states" : "tc_walk_out";
     if (p.cp) {
         a.cp = 1;
         a.maps = p.ws.maps;
         a.seg_start = p.ws.seg_state;
-        if (p.warm_chunks > 0) {
+        if (p.warm_chunks > 0 && !states_only) {
             if ((e = simt::warm_decide(p, s)) != cudaSuccess) return e;
             a.warm = p.ws.warm;
             a.warm_chunks = p.warm_chunks;
@@ -625,16 +628,24 @@ cudaError_t forward(const Plan &p, cudaStream_t s) {
         prof_after(s);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if ((e = simt::cp_scan(p, a.warm, s)) != cudaSuccess) return e;
-        prof_before("tc_walk_out", s);
+        prof_before(out_name, s);
         tc_walk_kernel<kWalkOut><<<dim3(p.max_segs, g.H, 1), 128, walk_smem, s>>>(mq, mk, mw, mu, g, a);
         prof_after(s);
     } else {
-        prof_before("tc_walk_out", s);
+        prof_before(out_name, s);
         tc_walk_kernel<kWalkOut><<<dim3(g.N, g.H, 1), 128, walk_smem, s>>>(mq, mk, mw, mu, g, a);
         prof_after(s);
     }
     return cudaGetLastError();
 }
+
+cudaError_t forward(const Plan &p, cudaStream_t s) {
+    cudaError_t e = simt::tables(p, s);
+    if (e != cudaSuccess) return e;
+    return run_forward(p, s, false);
+}
+
+cudaError_t recompute_states(const Plan &p, cudaStream_t s) { return run_forward(p, s, true); }
 
 }  // namespace tc
 }  // namespace gdn
