@@ -79,6 +79,8 @@ cudaError_t forward(const Plan &p, cudaStream_t s);
 // Backward pieces: prep + walk storing chunk start states (p.ws.hc).
 cudaError_t recompute_states(const Plan &p, cudaStream_t s);
 cudaError_t backward(const Plan &p, cudaStream_t s);
+// Chunk-local gradients on tensor cores (no q/k L2 normalisation).
+cudaError_t local_grads(const Plan &p, cudaStream_t s);
 // TMA descriptors of [tokens, H, 128] bf16 tensors (64 x 1 x 64 boxes, 128B swizzle).
 cudaError_t encoder();
 cudaError_t make_map(CUtensorMap *m, const void *base, long long tokens, int H);

@@ -379,7 +379,7 @@ cudaError_t backward(const Plan &p, cudaStream_t s) {
         prof_after(s);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    return simt::local_grads(p, s, true);
+    return g.l2norm ? simt::local_grads(p, s, true) : local_grads(p, s);
 }
 
 }  // namespace tc
