@@ -193,6 +193,7 @@ static size_t layout(Plan &p, bool bwd, char *base) {
         w.hc = (float *)take(st);
         w.dhc = (float *)take(st);
         w.du = take(th * g.V * 2);
+        w.tmat = (float *)take((size_t)p.max_chunks * g.H * 64 * 64 * sizeof(float));
         w.scratch = (float *)take((size_t)p.scratch_ctas *
                                   simt::scratch_floats_per_cta(g.K, g.V) * sizeof(float));
     }

@@ -24,6 +24,7 @@ struct Ws {
     float *hc = nullptr;           // [chunks, H, K, V] chunk start states (bwd)
     float *dhc = nullptr;          // [chunks, H, K, V] chunk end gradients (bwd)
     void *du = nullptr;            // [tokens, H, V] bf16 dU of the reverse walk (bwd, tensor cores)
+    float *tmat = nullptr;         // [chunks, H, 64, 64] fp32 T = (I + A)^-1 by column (bwd, tensor cores)
     float *scratch = nullptr;      // per-CTA scratch (bwd, CUDA-core path)
     int32_t *counters = nullptr;   // small zeroed counters
 };

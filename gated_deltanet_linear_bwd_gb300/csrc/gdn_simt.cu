@@ -288,9 +288,25 @@ walk_kernel(Geo g, WalkArgs a) {
 // Exclusive scan of segment maps S -> A S + B over one (sequence, head,
 // block of kSB state columns).  Forward (reverse = 0): start[0] = h0 and
 // start[j+1] = A_j start[j] + B_j.  Backward (reverse = 1): end[nseg-1] =
-// d(final state) and end[j-1] = A'_j end[j] + B'_j.  Thread t owns row t/2
-// and four of the kSB columns; it streams its map row with 16-byte loads.
+// d(final state) and end[j-1] = A'_j end[j] + B'_j.  The maps of the next
+// step are copied into shared memory (cp.async, double-buffered, rows padded
+// by 4 floats against bank conflicts) while the current step computes;
+// thread t owns row t/2 and four of the kSB columns.
 constexpr int kSB = 8;
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                     (uint32_t)__cvta_generic_to_shared(smem)),
+                 "l"(gmem)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 __global__ void __launch_bounds__(256)
 map_scan_kernel(Geo g, const float *maps, const float *init, const int32_t *warm, float *out,
@@ -300,29 +316,55 @@ map_scan_kernel(Geo g, const float *maps, const float *init, const int32_t *warm
     if (n >= g.N || col0 >= V) return;
     if (warm && warm[n * H + h]) return;
     const int nseg = seq_nsegs(g, n), sbase = seq_seg_base(g, n);
-    __shared__ __align__(16) float S[128][kSB];
+    extern __shared__ __align__(16) float sm[];
+    const int ld = K + 4;                        // padded row stride of the A buffers
+    float *Abuf = sm;                            // [2][K][ld]
+    float *Bbuf = Abuf + 2 * K * ld;             // [2][K][kSB]
+    float *S = Bbuf + 2 * K * kSB;               // [K][kSB]
     const int t = threadIdx.x, i = t >> 1, jq = (t & 1) * 4;
     const bool act = i < K;
+    auto stage = [&](int step, int buf) {
+        const int j = reverse ? nseg - 1 - step : step;
+        const float *M = maps + ((long long)(sbase + j) * H + h) * K * (K + V);
+        float *A = Abuf + buf * K * ld, *Bm = Bbuf + buf * K * kSB;
+        const int per_row = K / 4;
+        for (int idx = t; idx < K * per_row; idx += blockDim.x) {
+            const int row = idx / per_row, c4 = idx % per_row;
+            cp_async16(A + row * ld + 4 * c4, M + (long long)row * (K + V) + 4 * c4);
+        }
+        for (int idx = t; idx < K * (kSB / 4); idx += blockDim.x) {
+            const int row = idx / (kSB / 4), c4 = idx % (kSB / 4);
+            cp_async16(Bm + row * kSB + 4 * c4, M + (long long)row * (K + V) + K + col0 + 4 * c4);
+        }
+        cp_async_commit();
+    };
     for (int idx = t; idx < K * kSB; idx += blockDim.x) {
         const int r = idx / kSB, c = col0 + idx % kSB;
-        S[r][idx % kSB] = init ? init[(((long long)n * H + h) * K + r) * V + c] : 0.f;
+        S[idx] = init ? init[(((long long)n * H + h) * K + r) * V + c] : 0.f;
     }
-    __syncthreads();
-    for (int step = 0; step + 1 < nseg; ++step) {
+    const int steps = nseg - 1;
+    if (steps > 0) stage(0, 0);
+    for (int step = 0; step < steps; ++step) {
+        const int buf = step & 1;
+        if (step + 1 < steps) {
+            stage(step + 1, buf ^ 1);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();
         const int j = reverse ? nseg - 1 - step : step;      // map applied
         const int jo = reverse ? j - 1 : j + 1;              // segment that receives the state
-        const float *M = maps + ((long long)(sbase + j) * H + h) * K * (K + V);
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         if (act) {
-            const float *row = M + (long long)i * (K + V);
-            acc = *reinterpret_cast<const float4 *>(row + K + col0 + jq);
-            const float4 *row4 = reinterpret_cast<const float4 *>(row);
+            const float *A = Abuf + buf * K * ld + i * ld;
+            acc = *reinterpret_cast<const float4 *>(Bbuf + buf * K * kSB + i * kSB + jq);
             for (int l4 = 0; l4 < K / 4; ++l4) {
-                const float4 a4 = row4[l4];
+                const float4 a4 = *reinterpret_cast<const float4 *>(A + 4 * l4);
                 const float av[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float4 s4 = *reinterpret_cast<const float4 *>(&S[4 * l4 + e][jq]);
+                    const float4 s4 = *reinterpret_cast<const float4 *>(&S[(4 * l4 + e) * kSB + jq]);
                     acc.x += av[e] * s4.x;
                     acc.y += av[e] * s4.y;
                     acc.z += av[e] * s4.z;
@@ -332,12 +374,15 @@ map_scan_kernel(Geo g, const float *maps, const float *init, const int32_t *warm
         }
         __syncthreads();
         if (act) {
-            *reinterpret_cast<float4 *>(&S[i][jq]) = acc;
+            *reinterpret_cast<float4 *>(&S[i * kSB + jq]) = acc;
             float *dst = out + (((long long)(sbase + jo) * H + h) * K + i) * V + col0 + jq;
             *reinterpret_cast<float4 *>(dst) = acc;
         }
-        __syncthreads();
     }
+}
+
+static size_t map_scan_smem(int K) {
+    return sizeof(float) * (2 * K * (K + 4) + 2 * K * kSB + K * kSB);
 }
 
 // Warmup shortcut decision per (sequence, head): every segment j > 0 must
@@ -897,7 +942,7 @@ static cudaError_t forward_t(const Plan &p, cudaStream_t s, bool states_only) {
         }
         GDN_LAUNCH("simt_walk_map", (walk_kernel<TI, kMap>), dim3(p.max_segs, H, (K + V) / kBV), walk_smem(K), s,
                    g, a);
-        GDN_LAUNCH("map_scan", map_scan_kernel, dim3(g.N, H, V / kSB), 0, s, g,
+        GDN_LAUNCH("map_scan", map_scan_kernel, dim3(g.N, H, V / kSB), map_scan_smem(K), s, g,
                    (const float *)p.ws.maps, p.h0, (const int32_t *)a.warm, p.ws.seg_state, 0);
         GDN_LAUNCH(states_only ? "simt_walk_states" : "simt_walk_out", (walk_kernel<TI, kOut>), dim3(p.max_segs, H, V / kBV), walk_smem(K), s, g, a);
     } else {
@@ -916,7 +961,7 @@ cudaError_t warm_decide(const Plan &p, cudaStream_t s) {
 
 cudaError_t cp_scan(const Plan &p, const int32_t *warm, cudaStream_t s) {
     const Geo &g = p.g;
-    GDN_LAUNCH("map_scan", map_scan_kernel, dim3(g.N, g.H, g.V / kSB), 0, s, g,
+    GDN_LAUNCH("map_scan", map_scan_kernel, dim3(g.N, g.H, g.V / kSB), map_scan_smem(g.K), s, g,
                (const float *)p.ws.maps, p.h0, warm, p.ws.seg_state, 0);
     return cudaSuccess;
 }
@@ -970,7 +1015,7 @@ static cudaError_t backward_t(const Plan &p, cudaStream_t s) {
         d.cp = 1;
         GDN_LAUNCH("simt_dwalk_map", (dwalk_kernel<TI, kMap>), dim3(p.max_segs, H, (K + V) / kBV), dwalk_smem(K), s,
                    g, d);
-        GDN_LAUNCH("map_rscan", map_scan_kernel, dim3(g.N, H, V / kSB), 0, s, g,
+        GDN_LAUNCH("map_rscan", map_scan_kernel, dim3(g.N, H, V / kSB), map_scan_smem(K), s, g,
                    (const float *)p.ws.maps, p.dht, (const int32_t *)nullptr, p.ws.seg_state, 1);
         GDN_LAUNCH("simt_dwalk_out", (dwalk_kernel<TI, kOut>), dim3(p.max_segs, H, V / kBV), dwalk_smem(K), s, g,
                    d);
@@ -996,7 +1041,7 @@ cudaError_t local_grads(const Plan &p, cudaStream_t s, bool ws_bf16) {
 
 cudaError_t cp_rscan(const Plan &p, cudaStream_t s) {
     const Geo &g = p.g;
-    GDN_LAUNCH("map_rscan", map_scan_kernel, dim3(g.N, g.H, g.V / kSB), 0, s, g,
+    GDN_LAUNCH("map_rscan", map_scan_kernel, dim3(g.N, g.H, g.V / kSB), map_scan_smem(g.K), s, g,
                (const float *)p.ws.maps, p.dht, (const int32_t *)nullptr, p.ws.seg_state, 1);
     return cudaSuccess;
 }

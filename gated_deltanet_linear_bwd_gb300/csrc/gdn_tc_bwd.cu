@@ -42,6 +42,7 @@ struct DWalkSmem {
     uint8_t duT[2 * kTile];        // [128 rows (v)][64 c]                 K-major A
     uint8_t p[kTile];              // [64 rows r][64 c], includes scale    MN-major B
     float gam[2][64];
+    float fr[64];                  // exp(gam_L - gam_r) (x rk_r), 0 past L
     float rq[64], rk[64];
     uint64_t tma_bar[2], mma_bar;
     uint32_t tmem_base;
@@ -66,8 +67,10 @@ cudaError_t set_smem(F kernel, size_t bytes) {
 }
 }  // namespace
 
+// 256 threads: thread t owns row v = t % 128 of dH^T (TMEM lane v) and the
+// column half hs = t / 128; warps w and w + 4 split each epilogue's columns.
 template <int MODE>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(256, 1)
 tc_dwalk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_do,
                 Geo g, TcDWalkArgs a) {
@@ -75,6 +78,7 @@ tc_dwalk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     DWalkSmem &s = *reinterpret_cast<DWalkSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, h = blockIdx.y, cb = blockIdx.z, H = g.H;
+    const int v = tid & 127, hs = tid >> 7;
     int n, j = 0, nseg = 1;
     if (a.cp) {
         if (!seg_ref(g, blockIdx.x, n, j)) return;
@@ -104,7 +108,7 @@ tc_dwalk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tmem_relinquish();
         tc_fence_before();
     }
-    float dH[kD];     // row tid of dH^T = column tid of dH
+    float dH[64];     // dk half hs of row v of dH^T (= column v of dH)
     {
         const float *src = nullptr;
         if (MODE == kDOut) {
@@ -114,11 +118,16 @@ tc_dwalk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 src = a.dht + ((long long)n * H + h) * kD * kD;
         }
 #pragma unroll
-        for (int i = 0; i < kD; ++i)
-            dH[i] = src ? src[i * kD + tid] : ((a_cols && i == tid) ? 1.f : 0.f);
+        for (int i = 0; i < 64; ++i) {
+            const int k = 64 * hs + i;
+            dH[i] = src ? src[k * kD + v] : ((a_cols && k == v) ? 1.f : 0.f);
+        }
     }
-    st_row64(s.dhT, tid, dH);
-    st_row64(s.dhT + 2 * kTile, tid, dH + 64);
+    st_row64(s.dhT + hs * 2 * kTile, v, dH);
+    if (tid < 64 && c1 > c0) {
+        const int Lf = min(kChunk, slen - (c1 - 1) * kChunk);
+        s.gam[0][tid] = tid < Lf ? a.ws_gam[(sbos + (long long)(c1 - 1) * kChunk + tid) * H + h] : 0.f;
+    }
     fence_proxy_async();
     __syncthreads();
     tc_fence_after();
@@ -147,23 +156,24 @@ tc_dwalk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int st = it & 1;
         const long long bos = sbos + (long long)c * kChunk;
         const int L = min(kChunk, slen - c * kChunk);
+        float gnext = 0.f;                     // gam of chunk c - 1, stored at the end
         if (c - 1 >= c0) {
             if (tid == 0) {
                 fence_proxy_async();
                 issue_tma(st ^ 1, c - 1);
             }
             tma_pending |= 1 << (st ^ 1);
+            if (tid < 64) gnext = a.ws_gam[(bos - kChunk + tid) * H + h];   // a full chunk
         }
-        if (tid < 64) s.gam[st][tid] = tid < L ? a.ws_gam[(bos + tid) * H + h] : 0.f;
         if (MODE == kDOut) {
             float *dst = a.dhc + ((long long)(cbase + c) * H + h) * kD * kD;
 #pragma unroll
-            for (int i = 0; i < kD; ++i) dst[i * kD + tid] = dH[i];
+            for (int i = 0; i < 64; ++i) dst[(64 * hs + i) * kD + v] = dH[i];
         }
         bool ok = mbar_wait(&s.tma_bar[st], (it >> 1) & 1, g.spin_limit, g.status);
         if (__syncthreads_or(!ok)) { bailed = true; break; }
         tma_pending &= ~(1 << st);
-        if (g.l2norm) {
+        if (g.l2norm && tid < 128) {
             const int r = tid & 63;
             const uint8_t *base = s.qk[st] + (tid >= 64 ? kTile : 0);
             float ss = 0.f;
@@ -175,7 +185,6 @@ tc_dwalk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     ss += x * x;
                 }
             (tid >= 64 ? s.rk : s.rq)[r] = rsqrtf(ss + 1e-6f);
-            __syncthreads();
         }
         // group 1: P (rows of [Q; K] K^T) and X^T = dH^T K^T
         ++mma_n;
@@ -195,43 +204,44 @@ tc_dwalk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
             mma_commit(&s.mma_bar);
         }
+        if (g.l2norm) __syncthreads();
+        if (tid < 64) {
+            const float gl = s.gam[st][L - 1];
+            s.fr[tid] = tid < L ? __expf(gl - s.gam[st][tid]) * (g.l2norm ? s.rk[tid] : 1.f) : 0.f;
+        }
+        if (use_do && v >= 64) {
+            // row r of diag(scale e^gam) Q, dk half hs (the Q tile is already in place)
+            const int r = v - 64;
+            const float f = r < L ? g.scale * __expf(s.gam[st][r]) * (g.l2norm ? s.rq[r] : 1.f) : 0.f;
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                float x[32];
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj)
+                    x[jj] = f * ld_bf16(s.qk[st] + hs * 2 * kTile, r, q * 32 + jj);
+                st_row32(s.qs + hs * kTile, r, q * 32, x);
+            }
+        }
         ok = mbar_wait(&s.mma_bar, (mma_n - 1) & 1, g.spin_limit, g.status);
         if (__syncthreads_or(!ok)) { bailed = true; break; }
         tc_fence_after();
-        const float gl = s.gam[st][L - 1];
         if (use_do) {
-            const int r = tid & 63;
-            const float gr = s.gam[st][r];
-            const float sr = g.l2norm ? s.rq[r] : 1.f;
-            if (tid < 64) {
-                // P row r, scale included
+            if (v < 64) {
+                // P row r = v, columns 32*hs .. +31, scale included
+                const int r = v;
+                const float gr = s.gam[st][r];
+                const float sr = g.l2norm ? s.rq[r] : 1.f;
+                float x[32];
+                tmem_ld32(tmem_addr(t_p, warp, 32 * hs), x);
 #pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    float x[32];
-                    tmem_ld32(tmem_addr(t_p, warp, q * 32), x);
-#pragma unroll
-                    for (int jj = 0; jj < 32; ++jj) {
-                        const int c2 = q * 32 + jj;
-                        x[jj] = (c2 <= r && r < L)
-                                    ? g.scale * x[jj] * __expf(gr - s.gam[st][c2]) * sr *
-                                          (g.l2norm ? s.rk[c2] : 1.f)
-                                    : 0.f;
-                    }
-                    st_row32(s.p, r, q * 32, x);
+                for (int jj = 0; jj < 32; ++jj) {
+                    const int c2 = 32 * hs + jj;
+                    x[jj] = (c2 <= r && r < L)
+                                ? g.scale * x[jj] * __expf(gr - s.gam[st][c2]) * sr *
+                                      (g.l2norm ? s.rk[c2] : 1.f)
+                                : 0.f;
                 }
-            } else {
-                // row r of diag(scale e^gam) Q (normalised when asked)
-                const float f = r < L ? g.scale * __expf(gr) * sr : 0.f;
-#pragma unroll
-                for (int half = 0; half < 2; ++half)
-#pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        float x[32];
-#pragma unroll
-                        for (int jj = 0; jj < 32; ++jj)
-                            x[jj] = f * ld_bf16(s.qk[st] + half * 2 * kTile, r, q * 32 + jj);
-                        st_row32(s.qs + half * kTile, r, q * 32, x);
-                    }
+                st_row32(s.p, r, 32 * hs, x);
             }
             tc_fence_before();
             fence_proxy_async();
@@ -252,26 +262,23 @@ tc_dwalk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (__syncthreads_or(!ok)) { bailed = true; break; }
             tc_fence_after();
         }
-        // dU^T row (this thread's v) = Y^T + X^T diag(f)
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
+        {
+            // dU^T row v, chunk rows 32*hs .. +31: Y^T + X^T diag(f)
             float x[32], y[32];
-            tmem_ld32(tmem_addr(t_x, warp, q * 32), x);
-            if (use_do) tmem_ld32(tmem_addr(t_y, warp, q * 32), y);
+            tmem_ld32(tmem_addr(t_x, warp, 32 * hs), x);
+            if (use_do) tmem_ld32(tmem_addr(t_y, warp, 32 * hs), y);
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) {
-                const int r = q * 32 + jj;
-                const float f = r < L ? __expf(gl - s.gam[st][r]) * (g.l2norm ? s.rk[r] : 1.f) : 0.f;
-                x[jj] = (use_do ? y[jj] : 0.f) + f * x[jj];
-                if (r >= L) x[jj] = 0.f;
+                const int r = 32 * hs + jj;
+                x[jj] = r < L ? (use_do ? y[jj] : 0.f) + s.fr[r] * x[jj] : 0.f;
             }
-            st_row32(s.duT, tid, q * 32, x);
+            st_row32(s.duT, v, 32 * hs, x);
             if (MODE == kDOut && a.du) {
-                __nv_bfloat16 *dst = a.du + (bos * H + h) * (long long)kD + tid;
+                __nv_bfloat16 *dst = a.du + (bos * H + h) * (long long)kD + v;
 #pragma unroll
                 for (int jj = 0; jj < 32; ++jj)
-                    if (q * 32 + jj < L)
-                        dst[(long long)(q * 32 + jj) * H * kD] = __float2bfloat16_rn(x[jj]);
+                    if (32 * hs + jj < L)
+                        dst[(long long)(32 * hs + jj) * H * kD] = __float2bfloat16_rn(x[jj]);
             }
         }
         tc_fence_before();
@@ -303,17 +310,17 @@ tc_dwalk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (__syncthreads_or(!ok)) { bailed = true; break; }
         tc_fence_after();
         {
-            const float el = __expf(gl);
+            const float el = __expf(s.gam[st][L - 1]);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < 2; ++q) {
                 float z[32];
-                tmem_ld32(tmem_addr(t_z, warp, q * 32), z);
+                tmem_ld32(tmem_addr(t_z, warp, 64 * hs + 32 * q), z);
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj) dH[q * 32 + jj] = el * dH[q * 32 + jj] + z[jj];
+                for (int jj = 0; jj < 32; ++jj) dH[32 * q + jj] = el * dH[32 * q + jj] + z[jj];
             }
         }
-        st_row64(s.dhT, tid, dH);
-        st_row64(s.dhT + 2 * kTile, tid, dH + 64);
+        st_row64(s.dhT + hs * 2 * kTile, v, dH);
+        if (tid < 64) s.gam[st ^ 1][tid] = gnext;
         tc_fence_before();
         fence_proxy_async();
         __syncthreads();
@@ -329,11 +336,11 @@ tc_dwalk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     } else if (MODE == kDMap) {
         float *dst = a.maps + ((long long)(seq_seg_base(g, n) + j) * H + h) * kD * (2 * kD);
 #pragma unroll
-        for (int i = 0; i < kD; ++i) dst[i * (2 * kD) + cb * kD + tid] = dH[i];
+        for (int i = 0; i < 64; ++i) dst[(64 * hs + i) * (2 * kD) + cb * kD + v] = dH[i];
     } else if (a.dh0 && j == 0) {
         float *dst = a.dh0 + ((long long)n * H + h) * kD * kD;
 #pragma unroll
-        for (int i = 0; i < kD; ++i) dst[i * kD + tid] = dH[i];
+        for (int i = 0; i < 64; ++i) dst[(64 * hs + i) * kD + v] = dH[i];
     }
     tc_fence_before();
     __syncthreads();
@@ -366,16 +373,16 @@ cudaError_t backward(const Plan &p, cudaStream_t s) {
         a.maps = p.ws.maps;
         a.seg_end = p.ws.seg_state;
         prof_before("tc_dwalk_map", s);
-        tc_dwalk_kernel<kDMap><<<dim3(p.max_segs, g.H, 2), 128, smem, s>>>(mq, mk, mw, mdo, g, a);
+        tc_dwalk_kernel<kDMap><<<dim3(p.max_segs, g.H, 2), 256, smem, s>>>(mq, mk, mw, mdo, g, a);
         prof_after(s);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if ((e = simt::cp_rscan(p, s)) != cudaSuccess) return e;
         prof_before("tc_dwalk_out", s);
-        tc_dwalk_kernel<kDOut><<<dim3(p.max_segs, g.H, 1), 128, smem, s>>>(mq, mk, mw, mdo, g, a);
+        tc_dwalk_kernel<kDOut><<<dim3(p.max_segs, g.H, 1), 256, smem, s>>>(mq, mk, mw, mdo, g, a);
         prof_after(s);
     } else {
         prof_before("tc_dwalk_out", s);
-        tc_dwalk_kernel<kDOut><<<dim3(g.N, g.H, 1), 128, smem, s>>>(mq, mk, mw, mdo, g, a);
+        tc_dwalk_kernel<kDOut><<<dim3(g.N, g.H, 1), 256, smem, s>>>(mq, mk, mw, mdo, g, a);
         prof_after(s);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

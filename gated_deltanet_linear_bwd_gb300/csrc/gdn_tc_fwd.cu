@@ -58,7 +58,7 @@ __device__ __forceinline__ float scan64(float x, float *wsum) {
 
 __global__ void __launch_bounds__(128, 2)
 tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-            Geo g, float *ws_gam, __nv_bfloat16 *ws_w, __nv_bfloat16 *ws_u) {
+            Geo g, float *ws_gam, __nv_bfloat16 *ws_w, __nv_bfloat16 *ws_u, float *ws_t) {
     extern __shared__ uint8_t smem_raw[];
     PrepSmem &s = *reinterpret_cast<PrepSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -168,6 +168,14 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             }
             col[i] = acc;
         }
+        if (ws_t && r < L) {
+            // the backward keeps T: column r of this chunk's T, [chunk][h][col][row]
+            float4 *dst = reinterpret_cast<float4 *>(
+                ws_t + (((long long)(2 * blockIdx.x + ch) * H + h) * 64 + r) * 64);
+#pragma unroll
+            for (int i4 = 0; i4 < 16; ++i4)
+                dst[i4] = make_float4(col[4 * i4], col[4 * i4 + 1], col[4 * i4 + 2], col[4 * i4 + 3]);
+        }
         __syncthreads();  // every column done: A's space becomes bw / bu
         // MN-major B operands: row j = r holds T[.][j] scaled by beta_j e_j rk_j (W)
         // and by beta_j (u).
@@ -251,6 +259,7 @@ struct WalkSmem {
     uint8_t uTs[2 * kTile];        // U^T diag(f)                        (A operand)
     uint8_t p[kTile];              // [64 rows r][64 cols s]            (B operand)
     float gam[2][64];
+    float fr[64], er[64];          // exp(gam_L - gam_r) (x rk_r), exp(gam_r) (x rq_r); 0 past L
     float rq[64], rk[64];
     uint64_t tma_bar[2], mma_bar;
     uint32_t tmem_base;
@@ -274,20 +283,19 @@ enum { kWalkOut = 0, kWalkMap = 1 };
 constexpr uint32_t kIdesc64 = idesc_bf16(128, 64, false, false);      // K-major A and B
 constexpr uint32_t kIdescDH = idesc_bf16(128, 128, false, true);      // B MN-major
 
-__device__ __forceinline__ void write_state_rows(uint8_t *hT, int row, const float *Hr) {
-    st_row64(hT, row, Hr);
-    st_row64(hT + 2 * kTile, row, Hr + 64);
-}
-
+// 256 threads: thread t owns state row v = t % 128 (TMEM lane v) and the
+// column half hs = t / 128; warps w and w + 4 share a TMEM lane quarter and
+// split every epilogue's columns between them.
 template <int MODE>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(256, 1)
 tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-            const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_u,
-            Geo g, TcWalkArgs a) {
+               const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_u,
+               Geo g, TcWalkArgs a) {
     extern __shared__ uint8_t smem_raw[];
     WalkSmem &s = *reinterpret_cast<WalkSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, h = blockIdx.y, cb = blockIdx.z, H = g.H;
+    const int v = tid & 127, hs = tid >> 7;
     int n, j = 0, nseg = 1;
     if (a.cp) {
         if (!seg_ref(g, blockIdx.x, n, j)) return;
@@ -324,8 +332,8 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         tmem_relinquish();
         tc_fence_before();
     }
-    // start state: row tid of H^T = column tid of H
-    float Hr[kD];
+    // start state: this thread's half (dk 64*hs ..) of column v of H
+    float Hr[64];
     {
         const float *src = nullptr;
         if (MODE == kWalkOut && !warm) {
@@ -335,10 +343,16 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 src = a.h0 + ((long long)n * H + h) * kD * kD;
         }
 #pragma unroll
-        for (int i = 0; i < kD; ++i)
-            Hr[i] = src ? src[i * kD + tid] : ((a_cols && i == tid) ? 1.f : 0.f);
+        for (int i = 0; i < 64; ++i) {
+            const int k = 64 * hs + i;
+            Hr[i] = src ? src[k * kD + v] : ((a_cols && k == v) ? 1.f : 0.f);
+        }
     }
-    write_state_rows(s.hT, tid, Hr);
+    st_row64(s.hT + hs * 2 * kTile, v, Hr);
+    if (tid < 64 && cstart < c1) {
+        const int L0 = min(kChunk, slen - cstart * kChunk);
+        s.gam[0][tid] = tid < L0 ? a.ws_gam[(sbos + (long long)cstart * kChunk + tid) * H + h] : 0.f;
+    }
     fence_proxy_async();
     __syncthreads();
     tc_fence_after();
@@ -367,23 +381,25 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const long long bos = sbos + (long long)c * kChunk;
         const int L = min(kChunk, slen - c * kChunk);
         const bool out_now = emit && c >= c0;
+        float gnext = 0.f;                     // gam of the next chunk, stored at the end
         if (c + 1 < c1) {
             if (tid == 0) {
                 fence_proxy_async();
                 issue_tma(st ^ 1, c + 1);
             }
             tma_pending |= 1 << (st ^ 1);
+            const int Ln = min(kChunk, slen - (c + 1) * kChunk);
+            if (tid < 64 && tid < Ln) gnext = a.ws_gam[(bos + kChunk + tid) * H + h];
         }
-        if (tid < 64) s.gam[st][tid] = tid < L ? a.ws_gam[(bos + tid) * H + h] : 0.f;
         if (states && c >= c0) {
             float *dst = a.hc + ((long long)(cbase + c) * H + h) * kD * kD;
 #pragma unroll
-            for (int i = 0; i < kD; ++i) dst[i * kD + tid] = Hr[i];
+            for (int i = 0; i < 64; ++i) dst[(64 * hs + i) * kD + v] = Hr[i];
         }
         bool ok = mbar_wait(&s.tma_bar[st], (it >> 1) & 1, g.spin_limit, g.status);
         if (__syncthreads_or(!ok)) { bailed = true; break; }
         tma_pending &= ~(1 << st);
-        if (g.l2norm) {
+        if (g.l2norm && tid < 128) {
             // |q_r| from the Q rows (threads 0-63), |k_r| from the K rows (64-127)
             const int r = tid & 63;
             const uint8_t *base = s.qk[st] + (tid >= 64 ? kTile : 0);
@@ -396,7 +412,6 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     ss += x * x;
                 }
             (tid >= 64 ? s.rk : s.rq)[r] = rsqrtf(ss + 1e-6f);
-            __syncthreads();
         }
         ++mma_n;
         if (tid == 0) {
@@ -417,48 +432,46 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
             mma_commit(&s.mma_bar);
         }
+        if (g.l2norm) __syncthreads();        // rq, rk visible below
+        if (tid < 64) {
+            const float gl = s.gam[st][L - 1], gr = s.gam[st][tid];
+            s.fr[tid] = tid < L ? __expf(gl - gr) * (g.l2norm ? s.rk[tid] : 1.f) : 0.f;
+            s.er[tid] = tid < L ? __expf(gr) * (g.l2norm ? s.rq[tid] : 1.f) : 0.f;
+        }
         ok = mbar_wait(&s.mma_bar, (mma_n - 1) & 1, g.spin_limit, g.status);
         if (__syncthreads_or(!ok)) { bailed = true; break; }
         tc_fence_after();
-        const float gl = s.gam[st][L - 1];
-        // U = u - W H (this thread's state column) and U diag(f), 32 rows at a time
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
+        {
+            // U = u - W H for chunk rows 32*hs .. +31 of this thread's state column
             float acc[32], U[32];
-            tmem_ld32(tmem_addr(t_u, warp, q * 32), acc);
+            tmem_ld32(tmem_addr(t_u, warp, 32 * hs), acc);
+            const uint8_t *ut = s.u[st] + (v >> 6) * kTile;
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) {
-                const int r = q * 32 + jj;
-                const float uv = a_cols ? 0.f : ld_bf16(s.u[st] + (tid >> 6) * kTile, r, tid & 63);
+                const int r = 32 * hs + jj;
+                const float uv = a_cols ? 0.f : ld_bf16(ut, r, v & 63);
                 U[jj] = r < L ? uv - acc[jj] : 0.f;
             }
-            st_row32(s.uT, tid, q * 32, U);
+            st_row32(s.uT, v, 32 * hs, U);
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-                const int r = q * 32 + jj;
-                const float f = r < L ? __expf(gl - s.gam[st][r]) : 0.f;
-                U[jj] *= f * (g.l2norm ? s.rk[r] : 1.f);
-            }
-            st_row32(s.uTs, tid, q * 32, U);
+            for (int jj = 0; jj < 32; ++jj) U[jj] *= s.fr[32 * hs + jj];
+            st_row32(s.uTs, v, 32 * hs, U);
         }
-        if (out_now && tid < 64) {
-            // P row r = (Q K^T)[r, :] masked to s <= r < L and decayed
-            const int r = tid;
+        if (out_now && v < 64) {
+            // P row r = v, columns 32*hs .. +31: masked, decayed Q K^T
+            const int r = v;
             const float gr = s.gam[st][r];
             const float sr = g.l2norm ? s.rq[r] : 1.f;
+            float qk[32];
+            tmem_ld32(tmem_addr(t_p, warp, 32 * hs), qk);
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                float qk[32];
-                tmem_ld32(tmem_addr(t_p, warp, q * 32), qk);
-#pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    const int c2 = q * 32 + jj;
-                    qk[jj] = (c2 <= r && r < L)
-                                 ? qk[jj] * __expf(gr - s.gam[st][c2]) * sr * (g.l2norm ? s.rk[c2] : 1.f)
-                                 : 0.f;
-                }
-                st_row32(s.p, r, q * 32, qk);
+            for (int jj = 0; jj < 32; ++jj) {
+                const int c2 = 32 * hs + jj;
+                qk[jj] = (c2 <= r && r < L)
+                             ? qk[jj] * __expf(gr - s.gam[st][c2]) * sr * (g.l2norm ? s.rk[c2] : 1.f)
+                             : 0.f;
             }
+            st_row32(s.p, r, 32 * hs, qk);
         }
         tc_fence_before();
         fence_proxy_async();
@@ -485,33 +498,29 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (__syncthreads_or(!ok)) { bailed = true; break; }
         tc_fence_after();
         if (out_now) {
-            __nv_bfloat16 *o = a.o + (bos * H + h) * (long long)kD + tid;
+            __nv_bfloat16 *o = a.o + (bos * H + h) * (long long)kD + v;
+            float oi[32], oa[32];
+            tmem_ld32(tmem_addr(t_oi, warp, 32 * hs), oi);
+            tmem_ld32(tmem_addr(t_oa, warp, 32 * hs), oa);
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                float oi[32], oa[32];
-                tmem_ld32(tmem_addr(t_oi, warp, q * 32), oi);
-                tmem_ld32(tmem_addr(t_oa, warp, q * 32), oa);
-#pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    const int r = q * 32 + jj;
-                    if (r < L) {
-                        const float inter = oi[jj] * __expf(s.gam[st][r]) * (g.l2norm ? s.rq[r] : 1.f);
-                        o[(long long)r * H * kD] = __float2bfloat16_rn(g.scale * (inter + oa[jj]));
-                    }
-                }
+            for (int jj = 0; jj < 32; ++jj) {
+                const int r = 32 * hs + jj;
+                if (r < L)
+                    o[(long long)r * H * kD] = __float2bfloat16_rn(g.scale * (oi[jj] * s.er[r] + oa[jj]));
             }
         }
         {
-            const float el = __expf(gl);
+            const float el = __expf(s.gam[st][L - 1]);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < 2; ++q) {
                 float d[32];
-                tmem_ld32(tmem_addr(t_dh, warp, q * 32), d);
+                tmem_ld32(tmem_addr(t_dh, warp, 64 * hs + 32 * q), d);
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj) Hr[q * 32 + jj] = el * Hr[q * 32 + jj] + d[jj];
+                for (int jj = 0; jj < 32; ++jj) Hr[32 * q + jj] = el * Hr[32 * q + jj] + d[jj];
             }
         }
-        write_state_rows(s.hT, tid, Hr);
+        st_row64(s.hT + hs * 2 * kTile, v, Hr);
+        if (tid < 64) s.gam[st ^ 1][tid] = gnext;
         tc_fence_before();
         fence_proxy_async();
         __syncthreads();
@@ -527,11 +536,11 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     } else if (MODE == kWalkMap) {
         float *dst = a.maps + ((long long)(seq_seg_base(g, n) + j) * H + h) * kD * (2 * kD);
 #pragma unroll
-        for (int i = 0; i < kD; ++i) dst[i * (2 * kD) + cb * kD + tid] = Hr[i];
+        for (int i = 0; i < 64; ++i) dst[(64 * hs + i) * (2 * kD) + cb * kD + v] = Hr[i];
     } else if (a.final_state && j == nseg - 1) {
         float *dst = a.final_state + ((long long)n * H + h) * kD * kD;
 #pragma unroll
-        for (int i = 0; i < kD; ++i) dst[i * kD + tid] = Hr[i];
+        for (int i = 0; i < 64; ++i) dst[(64 * hs + i) * kD + v] = Hr[i];
     }
     tc_fence_before();
     __syncthreads();
@@ -603,7 +612,8 @@ static cudaError_t run_forward(const Plan &p, cudaStream_t s, bool states_only) 
 
     prof_before("tc_prep", s);
     tc_prep_kernel<<<dim3((p.max_chunks + 1) / 2, g.H), 128, prep_smem, s>>>(
-        mk, mv, g, p.ws.gam, (__nv_bfloat16 *)p.ws.w, (__nv_bfloat16 *)p.ws.u);
+        mk, mv, g, p.ws.gam, (__nv_bfloat16 *)p.ws.w, (__nv_bfloat16 *)p.ws.u,
+        states_only ? p.ws.tmat : nullptr);
     prof_after(s);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
@@ -624,16 +634,16 @@ static cudaError_t run_forward(const Plan &p, cudaStream_t s, bool states_only) 
             a.warm_chunks = p.warm_chunks;
         }
         prof_before("tc_walk_map", s);
-        tc_walk_kernel<kWalkMap><<<dim3(p.max_segs, g.H, 2), 128, walk_smem, s>>>(mq, mk, mw, mu, g, a);
+        tc_walk_kernel<kWalkMap><<<dim3(p.max_segs, g.H, 2), 256, walk_smem, s>>>(mq, mk, mw, mu, g, a);
         prof_after(s);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if ((e = simt::cp_scan(p, a.warm, s)) != cudaSuccess) return e;
         prof_before(out_name, s);
-        tc_walk_kernel<kWalkOut><<<dim3(p.max_segs, g.H, 1), 128, walk_smem, s>>>(mq, mk, mw, mu, g, a);
+        tc_walk_kernel<kWalkOut><<<dim3(p.max_segs, g.H, 1), 256, walk_smem, s>>>(mq, mk, mw, mu, g, a);
         prof_after(s);
     } else {
         prof_before(out_name, s);
-        tc_walk_kernel<kWalkOut><<<dim3(g.N, g.H, 1), 128, walk_smem, s>>>(mq, mk, mw, mu, g, a);
+        tc_walk_kernel<kWalkOut><<<dim3(g.N, g.H, 1), 256, walk_smem, s>>>(mq, mk, mw, mu, g, a);
         prof_after(s);
     }
     return cudaGetLastError();

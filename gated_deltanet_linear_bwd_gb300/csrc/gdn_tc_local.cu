@@ -5,7 +5,7 @@
 // the workspace), the chunk start state H0 and the gradient at its end dHL
 // (workspace, fp32), gam and beta.  With D = exp(gam_r - gam_s),
 // e = exp(gam), f = exp(gam_L - gam), and T = (I + A)^-1 recomputed:
-//   U    = u - W H0
+//   U    = u - W H0   (T itself is kept by the recompute's prep kernel)
 //   dS   = scale (dO U^T) .* lower_incl .* D
 //   dW   = -dU H0^T,  dYw = T^T dW,  dYu = T^T dU
 //   dT   = dU (diag(beta) V)^T + dW (diag(beta e) K)^T,  dA = -T^T dT T^T
@@ -47,7 +47,7 @@ struct LocalSmem {
     uint8_t ds[kTile];         // dS rows r
     uint8_t tt[kTile];         // row r = column r of T
     uint8_t gs[kTile];         // Gs rows r
-    float fa[64][64];          // A, then X = dT T^T
+    float fa[64][64];          // X = dT T^T
     float tf[64][65];          // T
     float fd[64][65];          // dT, then dA
     float gam[64], bet[64], ee[64], ff[64];
@@ -100,7 +100,7 @@ __device__ __forceinline__ float block_sum(float x, float *scratch4) {
 }
 
 struct TcLocalArgs {
-    const float *ws_gam, *hc, *dhc;
+    const float *ws_gam, *hc, *dhc, *tmat;
     const __nv_bfloat16 *ws_u;
     void *dq, *dk, *dv;
     float *dg, *dbeta;
@@ -240,28 +240,9 @@ tc_local_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             for (int jj = 0; jj < 32; ++jj) x[jj] = (q * 32 + jj) < L ? -x[jj] : 0.f;
             st_row32(dwT, tid, q * 32, x);
         }
-        if (tid >= 64) {
-            // row r of A = strict_lower(diag(beta) K K^T .* D)
-            const float br = s.bet[r], gr = s.gam[r];
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                float kk[32];
-                tmem_ld32(tmem_addr(t_p, warp, q * 32), kk);
-#pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4) {
-                    float x[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int c = q * 32 + 4 * j4 + e;
-                        x[e] = (c < r && r < L) ? br * kk[4 * j4 + e] * __expf(gr - s.gam[c]) : 0.f;
-                    }
-                    *reinterpret_cast<float4 *>(&s.fa[r][q * 32 + 4 * j4]) = make_float4(x[0], x[1], x[2], x[3]);
-                }
-            }
-        }
         tc_fence_before();
         fence_proxy_async();
-        reduce64(p, s.rowA, s.red, false);    // contains the barrier that publishes uT, dwT, A
+        reduce64(p, s.rowA, s.red, false);    // contains the barrier that publishes uT, dwT
     }
 
     // ---------------- wave 2: dP = dO U^T, dW K^T (lanes 0-63), T on CUDA cores
@@ -281,23 +262,17 @@ tc_local_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mma_commit(&s.mma_bar);
     }
     if (tid < 64) {
-        // column r of T = (I + A)^-1 by forward substitution
+        // column r of T = (I + A)^-1, kept by the prep kernel of the recompute
+        const float4 *src = reinterpret_cast<const float4 *>(
+            a.tmat + (((long long)ci * H + h) * 64 + r) * 64);
         float col[64];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) col[i] = (i == r) ? 1.f : 0.f;
-#pragma unroll
-        for (int i = 1; i < 64; ++i) {
-            const float4 *ar = reinterpret_cast<const float4 *>(s.fa[i]);
-            float acc = col[i];
-#pragma unroll
-            for (int c4 = 0; c4 < (i + 3) / 4; ++c4) {
-                const float4 a4 = ar[c4];
-                if (4 * c4 + 0 < i) acc -= a4.x * col[4 * c4 + 0];
-                if (4 * c4 + 1 < i) acc -= a4.y * col[4 * c4 + 1];
-                if (4 * c4 + 2 < i) acc -= a4.z * col[4 * c4 + 2];
-                if (4 * c4 + 3 < i) acc -= a4.w * col[4 * c4 + 3];
-            }
-            col[i] = acc;
+        for (int i4 = 0; i4 < 16; ++i4) {
+            const float4 t4 = r < L ? src[i4] : make_float4(0.f, 0.f, 0.f, 0.f);
+            col[4 * i4] = t4.x;
+            col[4 * i4 + 1] = t4.y;
+            col[4 * i4 + 2] = t4.z;
+            col[4 * i4 + 3] = t4.w;
         }
 #pragma unroll
         for (int i = 0; i < 64; ++i) s.tf[i][r] = col[i];
@@ -549,6 +524,7 @@ cudaError_t local_grads(const Plan &p, cudaStream_t s) {
     a.ws_gam = p.ws.gam;
     a.hc = p.ws.hc;
     a.dhc = p.ws.dhc;
+    a.tmat = p.ws.tmat;
     a.ws_u = (const __nv_bfloat16 *)p.ws.u;
     a.dq = p.dq;
     a.dk = p.dk;
