@@ -40,28 +40,31 @@ constexpr uint32_t kMM = idesc_bf16(128, 64, true, true);     // A MN-major, B M
 struct LocalSmem {
     uint8_t qk[4 * kTile];     // [dk half][Q rows 0-63, K rows 64-127][128 B]
     uint8_t v[2 * kTile];      // [dv half][64 rows][128 B]
-    uint8_t dO[2 * kTile];     // after wave 2: dHL^T half 1
+    uint8_t dO[2 * kTile];     // after wave 2: dHL^T k half 0
     uint8_t du[2 * kTile];
-    uint8_t w[2 * kTile];      // after wave 1: dHL^T half 0
+    uint8_t w[2 * kTile];      // after wave 1: dHL^T k half 1
     uint8_t h0T[4 * kTile];    // [k half][128 rows v][128 B]; after wave 1: uT, dwT
     uint8_t ds[kTile];         // dS rows r
     uint8_t tt[kTile];         // row r = column r of T
     uint8_t gs[kTile];         // Gs rows r
-    float fa[64][64];          // X = dT T^T
-    float tf[64][65];          // T
-    float fd[64][65];          // dT, then dA
+    float xm[64][64];          // X = dT T^T, row-major
+    float tf[64][64];          // T, row-major
+    float tft[64][64];         // T^T
+    float fd[64 * 68];         // dT^T (stride 68), then dA row-major (stride 65)
     float gam[64], bet[64], ee[64], ff[64];
-    float red[4][64];
-    float zrow[64], zprow[64], zcol[64], rowA[64], dbA[64], yw[64], yu[64], zpp[64];
-    float hdot[8];             // [0]: <dHL, H0>; [4..7]: block_sum scratch
+    float red[8][32];
+    float zrow[2][64], zprow[2][64], dbA[2][64];
+    float zcol[64], rowA[64], yw[64], yu[64], zpp[64];
+    float hdot[16];            // [0]: <dHL, H0>; [8..15]: block_sum scratch
     uint64_t tma_bar, mma_bar;
     uint32_t tmem_base;
 };
 
-// Sums 64 per-thread values over all 128 threads: dst[i] (+)= sum_t a_t[i].
-// Warp butterfly (each lane ends with the sums of entries 2*lane and
-// 2*lane + 1), then the four warps combine through shared memory.
-__device__ __forceinline__ void reduce64(float (&a)[64], float *dst, float (&red)[4][64],
+// 256 threads; thread t contributes a[j] to entry 32 * (t / 128) + j.
+// dst[i] (+)= the sum of all contributions to entry i (i < 64).  Warp
+// butterfly (lane l ends with entry l of its warp), then the four warps of
+// each half combine through shared memory.
+__device__ __forceinline__ void reduce32(float (&a)[32], float *dst, float (&red)[8][32],
                                          bool accumulate) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #define GDN_BFLY(MASK, HALF)                                                  \
@@ -73,28 +76,29 @@ __device__ __forceinline__ void reduce64(float (&a)[64], float *dst, float (&red
             a[i] = keep + __shfl_xor_sync(0xffffffffu, send, (MASK));         \
         }                                                                     \
     }
-    GDN_BFLY(16, 32)
-    GDN_BFLY(8, 16)
-    GDN_BFLY(4, 8)
-    GDN_BFLY(2, 4)
-    GDN_BFLY(1, 2)
+    GDN_BFLY(16, 16)
+    GDN_BFLY(8, 8)
+    GDN_BFLY(4, 4)
+    GDN_BFLY(2, 2)
+    GDN_BFLY(1, 1)
 #undef GDN_BFLY
-    red[warp][2 * lane] = a[0];
-    red[warp][2 * lane + 1] = a[1];
+    red[warp][lane] = a[0];
     __syncthreads();
     if (threadIdx.x < 64) {
-        const int i = threadIdx.x;
-        const float sum = red[0][i] + red[1][i] + red[2][i] + red[3][i];
+        const int i = threadIdx.x, w0 = 4 * (i >> 5), l = i & 31;
+        const float sum = red[w0][l] + red[w0 + 1][l] + red[w0 + 2][l] + red[w0 + 3][l];
         dst[i] = accumulate ? dst[i] + sum : sum;
     }
     __syncthreads();
 }
 
-__device__ __forceinline__ float block_sum(float x, float *scratch4) {
+__device__ __forceinline__ float block_sum(float x, float *scratch8) {
     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    if ((threadIdx.x & 31) == 0) scratch4[threadIdx.x >> 5] = x;
+    if ((threadIdx.x & 31) == 0) scratch8[threadIdx.x >> 5] = x;
     __syncthreads();
-    const float s = scratch4[0] + scratch4[1] + scratch4[2] + scratch4[3];
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) s += scratch8[w];
     __syncthreads();
     return s;
 }
@@ -112,8 +116,12 @@ cudaError_t set_smem(F kernel, size_t bytes) {
 }
 }  // namespace
 
+// 256 threads.  Feature-major results: thread t reads TMEM lane v = t % 128
+// (feature v) and the chunk-row half hs = t / 128.  Row-major 64 x 64
+// results sit on lanes 0-63 (warps 0, 1, 4, 5: row r = v, column half hs);
+// lanes 64-127 of the [Q; K] K^T product hold K K^T (warps 2, 3, 6, 7).
 template <typename TG>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(256, 1)
 tc_local_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                 const __grid_constant__ CUtensorMap tm_du, const __grid_constant__ CUtensorMap tm_w,
@@ -122,9 +130,10 @@ tc_local_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     LocalSmem &s = *reinterpret_cast<LocalSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, h = blockIdx.y, H = g.H, ci = blockIdx.x;
+    const int v = tid & 127, hs = tid >> 7, c0 = 32 * hs;
     ChunkRef cr;
     if (!chunk_ref(g, ci, cr)) return;
-    const int L = cr.len, r = tid & 63;
+    const int L = cr.len;
     const long long bos = cr.bos;
     const float scale = g.scale;
     uint8_t *uT = s.h0T, *dwT = s.h0T + 2 * kTile;   // after wave 1
@@ -160,26 +169,23 @@ tc_local_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
     }
     if (tid < 64) {
-        s.gam[r] = r < L ? a.ws_gam[(bos + r) * H + h] : 0.f;
-        s.bet[r] = r < L ? g.beta[(bos + r) * H + h] : 0.f;
+        s.gam[tid] = tid < L ? a.ws_gam[(bos + tid) * H + h] : 0.f;
+        s.bet[tid] = tid < L ? g.beta[(bos + tid) * H + h] : 0.f;
     }
     const float *H0 = a.hc + ((long long)ci * H + h) * kD * kD;
     const float *dHL = a.dhc + ((long long)ci * H + h) * kD * kD;
     {
-        // H0 column tid -> row tid of H0^T (bf16, two k halves)
+        // k half hs of column v of H0 -> row v of H0^T
+        float x[64];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            float x[64];
-#pragma unroll
-            for (int i = 0; i < 64; ++i) x[i] = H0[(half * 64 + i) * kD + tid];
-            st_row64(s.h0T + half * 2 * kTile, tid, x);
-        }
+        for (int i = 0; i < 64; ++i) x[i] = H0[(64 * hs + i) * kD + v];
+        st_row64(s.h0T + hs * 2 * kTile, v, x);
     }
     fence_proxy_async();
     __syncthreads();
     if (tid < 64) {
-        s.ee[r] = r < L ? __expf(s.gam[r]) : 0.f;
-        s.ff[r] = r < L ? __expf(s.gam[L - 1] - s.gam[r]) : 0.f;
+        s.ee[tid] = tid < L ? __expf(s.gam[tid]) : 0.f;
+        s.ff[tid] = tid < L ? __expf(s.gam[L - 1] - s.gam[tid]) : 0.f;
     }
     int mma_n = 0;
     bool tma_pending = true;
@@ -192,22 +198,21 @@ tc_local_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (tid == 0) {
         tc_fence_after();
         const uint32_t qk = smem_u32(s.qk), h0 = smem_u32(s.h0T), w = smem_u32(s.w),
-                       du = smem_u32(s.du), v = smem_u32(s.v), dO = smem_u32(s.dO);
+                       du = smem_u32(s.du), vv = smem_u32(s.v), dO = smem_u32(s.dO);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t hs = kk >> 2, sub = (kk & 3) * 32;
-            const uint64_t aH = desc_sw128(h0 + hs * 2 * kTile + sub, 16, 1024);
-            const uint64_t aQK = desc_sw128(qk + hs * 2 * kTile + sub, 16, 1024);
-            const uint64_t bK = desc_sw128(qk + hs * 2 * kTile + kTile + sub, 16, 1024);
-            const uint64_t bQ = aQK;
-            mma_bf16(t_u, aH, desc_sw128(w + hs * kTile + sub, 16, 1024), kKK, kk > 0);
+            const uint32_t hh = kk >> 2, sub = (kk & 3) * 32;
+            const uint64_t aH = desc_sw128(h0 + hh * 2 * kTile + sub, 16, 1024);
+            const uint64_t aQK = desc_sw128(qk + hh * 2 * kTile + sub, 16, 1024);
+            const uint64_t bK = desc_sw128(qk + hh * 2 * kTile + kTile + sub, 16, 1024);
+            mma_bf16(t_u, aH, desc_sw128(w + hh * kTile + sub, 16, 1024), kKK, kk > 0);
             mma_bf16(t_p, aQK, bK, kKK, kk > 0);
-            mma_bf16(t_qh, aH, bQ, kKK, kk > 0);
-            mma_bf16(t_tu, desc_sw128(du + hs * kTile + sub, 16, 1024),
-                     desc_sw128(v + hs * kTile + sub, 16, 1024), kKK, kk > 0);
+            mma_bf16(t_qh, aH, aQK, kKK, kk > 0);
+            mma_bf16(t_tu, desc_sw128(du + hh * kTile + sub, 16, 1024),
+                     desc_sw128(vv + hh * kTile + sub, 16, 1024), kKK, kk > 0);
             const uint64_t aHm = desc_sw128(h0 + kk * 2048, 2 * kTile, 1024);   // H0, MN-major
-            mma_bf16(t_dw, aHm, desc_sw128(du + hs * kTile + sub, 16, 1024), kMK, kk > 0);
-            mma_bf16(t_q1, aHm, desc_sw128(dO + hs * kTile + sub, 16, 1024), kMK, kk > 0);
+            mma_bf16(t_dw, aHm, desc_sw128(du + hh * kTile + sub, 16, 1024), kMK, kk > 0);
+            mma_bf16(t_q1, aHm, desc_sw128(dO + hh * kTile + sub, 16, 1024), kMK, kk > 0);
         }
         mma_commit(&s.mma_bar);
     }
@@ -215,37 +220,29 @@ tc_local_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (__syncthreads_or(!ok)) goto bail;
     tc_fence_after();
     {
-        // U^T row (thread = v) into uT; partials of sum_v dO[r][v] (Q H0)[r][v]
-        const __nv_bfloat16 *ug = a.ws_u + (bos * H + h) * (long long)kD + tid;
-        float p[64];
+        // U^T (row v, chunk rows c0..c0+31) into uT; -(H0 dU^T) (row k = v) into dwT;
+        // partial sums of dO[r][v] (Q H0)[r][v] over v for rowA
+        const __nv_bfloat16 *ug = a.ws_u + (bos * H + h) * (long long)kD + v;
+        float x[32], y[32];
+        tmem_ld32(tmem_addr(t_u, warp, c0), x);
+        tmem_ld32(tmem_addr(t_qh, warp, c0), y);
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            float acc[32], qh[32];
-            tmem_ld32(tmem_addr(t_u, warp, q * 32), acc);
-            tmem_ld32(tmem_addr(t_qh, warp, q * 32), qh);
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-                const int c = q * 32 + jj;
-                acc[jj] = c < L ? __bfloat162float(ug[(long long)c * H * kD]) - acc[jj] : 0.f;
-                p[c] = c < L ? ld_bf16(s.dO + (tid >> 6) * kTile, c, tid & 63) * qh[jj] : 0.f;
-            }
-            st_row32(uT, tid, q * 32, acc);
+        for (int jj = 0; jj < 32; ++jj) {
+            const int c = c0 + jj;
+            x[jj] = c < L ? __bfloat162float(ug[(long long)c * H * kD]) - x[jj] : 0.f;
+            y[jj] = c < L ? ld_bf16(s.dO + (v >> 6) * kTile, c, v & 63) * y[jj] : 0.f;
         }
-        // dW^T row (thread = k) = -(H0 dU^T)[k][:]
+        st_row32(uT, v, c0, x);
+        tmem_ld32(tmem_addr(t_dw, warp, c0), x);
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            float x[32];
-            tmem_ld32(tmem_addr(t_dw, warp, q * 32), x);
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) x[jj] = (q * 32 + jj) < L ? -x[jj] : 0.f;
-            st_row32(dwT, tid, q * 32, x);
-        }
+        for (int jj = 0; jj < 32; ++jj) x[jj] = (c0 + jj) < L ? -x[jj] : 0.f;
+        st_row32(dwT, v, c0, x);
         tc_fence_before();
         fence_proxy_async();
-        reduce64(p, s.rowA, s.red, false);    // contains the barrier that publishes uT, dwT
+        reduce32(y, s.rowA, s.red, false);    // its barriers publish uT and dwT
     }
 
-    // ---------------- wave 2: dP = dO U^T, dW K^T (lanes 0-63), T on CUDA cores
+    // ---------------- wave 2: dP = dO U^T, dW K^T (lanes 0-63); T from the recompute
     ++mma_n;
     if (tid == 0) {
         tc_fence_after();
@@ -253,16 +250,17 @@ tc_local_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                        dwa = smem_u32(dwT);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t hs = kk >> 2, sub = (kk & 3) * 32;
-            mma_bf16(t_dp, desc_sw128(dO + hs * kTile + sub, 16, 1024),
+            const uint32_t hh = kk >> 2, sub = (kk & 3) * 32;
+            mma_bf16(t_dp, desc_sw128(dO + hh * kTile + sub, 16, 1024),
                      desc_sw128(uTa + kk * 2048, kTile, 1024), kKM, kk > 0);
             mma_bf16(t_tw, desc_sw128(dwa + kk * 2048, 0, 1024),
-                     desc_sw128(qk + hs * 2 * kTile + kTile + sub, 16, 1024), kMK, kk > 0);
+                     desc_sw128(qk + hh * 2 * kTile + kTile + sub, 16, 1024), kMK, kk > 0);
         }
         mma_commit(&s.mma_bar);
     }
     if (tid < 64) {
-        // column r of T = (I + A)^-1, kept by the prep kernel of the recompute
+        // column r of T (kept by the prep kernel of the recompute)
+        const int r = tid;
         const float4 *src = reinterpret_cast<const float4 *>(
             a.tmat + (((long long)ci * H + h) * 64 + r) * 64);
         float col[64];
@@ -273,6 +271,7 @@ tc_local_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             col[4 * i4 + 1] = t4.y;
             col[4 * i4 + 2] = t4.z;
             col[4 * i4 + 3] = t4.w;
+            reinterpret_cast<float4 *>(s.tft[r])[i4] = t4;
         }
 #pragma unroll
         for (int i = 0; i < 64; ++i) s.tf[i][r] = col[i];
@@ -282,112 +281,134 @@ tc_local_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (__syncthreads_or(!ok)) goto bail;
     tc_fence_after();
     {
-        float z[64];
-        if (tid < 64) {
+        float z[32];
+        if (v < 64) {
+            // dS row r = v (columns c0..c0+31), z = dS .* Q K^T, and dT^T (columns r)
+            const int r = v;
             const float gr = s.gam[r];
+            float dp[32], qk[32];
+            tmem_ld32(tmem_addr(t_dp, warp, c0), dp);
+            tmem_ld32(tmem_addr(t_p, warp, c0), qk);
             float zr = 0.f;
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                float dp[32], qk[32];
-                tmem_ld32(tmem_addr(t_dp, warp, q * 32), dp);
-                tmem_ld32(tmem_addr(t_p, warp, q * 32), qk);
-#pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    const int c = q * 32 + jj;
-                    const float ds = (c <= r && r < L) ? scale * dp[jj] * __expf(gr - s.gam[c]) : 0.f;
-                    const float zz = ds * qk[jj];
-                    zr += zz;
-                    z[c] = -zz;
-                    dp[jj] = ds;
-                }
-                st_row32(s.ds, r, q * 32, dp);
+            for (int jj = 0; jj < 32; ++jj) {
+                const int c = c0 + jj;
+                const float ds = (c <= r && r < L) ? scale * dp[jj] * __expf(gr - s.gam[c]) : 0.f;
+                const float zz = ds * qk[jj];
+                zr += zz;
+                z[jj] = -zz;
+                dp[jj] = ds;
             }
-            s.zrow[r] = zr;
+            st_row32(s.ds, r, c0, dp);
+            s.zrow[hs][r] = zr;
+            tmem_ld32(tmem_addr(t_tu, warp, c0), dp);
+            tmem_ld32(tmem_addr(t_tw, warp, c0), qk);
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                float tu[32], tw[32];
-                tmem_ld32(tmem_addr(t_tu, warp, q * 32), tu);
-                tmem_ld32(tmem_addr(t_tw, warp, q * 32), tw);
-#pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    const int c = q * 32 + jj;
-                    s.fd[r][c] = (c < r && r < L) ? s.bet[c] * (tu[jj] + s.ee[c] * tw[jj]) : 0.f;
-                }
+            for (int jj = 0; jj < 32; ++jj) {
+                const int c = c0 + jj;
+                s.fd[c * 68 + r] = (c < r && r < L) ? s.bet[c] * (dp[jj] + s.ee[c] * qk[jj]) : 0.f;
             }
         } else {
 #pragma unroll
-            for (int c = 0; c < 64; ++c) z[c] = 0.f;
+            for (int jj = 0; jj < 32; ++jj) z[jj] = 0.f;
         }
-        // dHL^T rows (thread = v): k half 0 into the dO tile, half 1 into the W tile
+        // dHL^T rows (feature v, k half hs): k half 0 into the dO tile, 1 into the W tile
         float hd = 0.f;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
+        {
             float x[64];
 #pragma unroll
             for (int i = 0; i < 64; ++i) {
-                const int k = half * 64 + i;
-                const float d = dHL[k * kD + tid];
-                hd += d * H0[k * kD + tid];
+                const int k = 64 * hs + i;
+                const float d = dHL[k * kD + v];
+                hd += d * H0[k * kD + v];
                 x[i] = d;
             }
-            st_row64(half ? s.w : s.dO, tid, x);
+            st_row64(hs ? s.w : s.dO, v, x);
         }
-        reduce64(z, s.zcol, s.red, false);
-        hd = block_sum(hd, s.hdot + 4);
+        reduce32(z, s.zcol, s.red, false);
+        hd = block_sum(hd, s.hdot + 8);
         if (tid == 0) s.hdot[0] = hd;
     }
-    // ---------------- X = dT T^T, dA = -T^T X on CUDA cores (fp32)
+    // ---------------- X = dT T^T, then dA = -T^T X (strict lower), fp32, 4 x 4 per thread
     {
-        const int s0 = (tid >> 6) * 32;
-        for (int c = s0; c < s0 + 32; ++c) {
-            float acc = 0.f;
-            const int bmax = min(r, c + 1);
-            for (int b = 0; b < bmax; ++b) acc += s.fd[r][b] * s.tf[c][b];
-            s.fa[r][c] = acc;
+        const int rb = 4 * (tid >> 4), sb = 4 * (tid & 15);
+        float acc[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j2 = 0; j2 < 4; ++j2) acc[i][j2] = 0.f;
+#pragma unroll 4
+        for (int b = 0; b < 64; ++b) {
+            const float4 d4 = *reinterpret_cast<const float4 *>(&s.fd[b * 68 + rb]);
+            const float4 t4 = *reinterpret_cast<const float4 *>(&s.tft[b][sb]);
+            const float dv4[4] = {d4.x, d4.y, d4.z, d4.w}, tv4[4] = {t4.x, t4.y, t4.z, t4.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j2 = 0; j2 < 4; ++j2) acc[i][j2] += dv4[i] * tv4[j2];
         }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<float4 *>(&s.xm[rb + i][sb]) =
+                make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
         __syncthreads();
-        for (int c = s0; c < s0 + 32; ++c) {
-            float acc = 0.f;
-            if (c < r && r < L)
-                for (int q = r; q < 64; ++q) acc += s.tf[q][r] * s.fa[q][c];
-            s.fd[r][c] = -acc;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j2 = 0; j2 < 4; ++j2) acc[i][j2] = 0.f;
+#pragma unroll 4
+        for (int q = 0; q < 64; ++q) {
+            const float4 t4 = *reinterpret_cast<const float4 *>(&s.tf[q][rb]);
+            const float4 x4 = *reinterpret_cast<const float4 *>(&s.xm[q][sb]);
+            const float tv4[4] = {t4.x, t4.y, t4.z, t4.w}, xv4[4] = {x4.x, x4.y, x4.z, x4.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j2 = 0; j2 < 4; ++j2) acc[i][j2] += tv4[i] * xv4[j2];
         }
+        __syncthreads();                       // every read of dT^T is done: fd becomes dA
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j2 = 0; j2 < 4; ++j2) {
+                const int r = rb + i, c = sb + j2;
+                s.fd[r * 65 + c] = (c < r && r < L) ? -acc[i][j2] : 0.f;
+            }
         __syncthreads();
     }
     {
-        // Gs = G + G^T, z' = G .* K K^T, and the dA part of dbeta (threads 64-127, row r)
-        float zp[64];
-        if (tid >= 64) {
+        // Gs = G + G^T, z' = G .* K K^T and the dA part of dbeta: row r = v - 64
+        float zp[32];
+        if (v >= 64) {
+            const int r = v - 64;
             const float gr = s.gam[r], br = s.bet[r];
+            float kk[32], gsv[32];
+            tmem_ld32(tmem_addr(t_p, warp, c0), kk);
             float zpr = 0.f, dba = 0.f;
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                float kk[32], gsv[32];
-                tmem_ld32(tmem_addr(t_p, warp, q * 32), kk);
-#pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    const int c = q * 32 + jj;
-                    const bool low = c < r && r < L, up = c > r && c < L;
-                    const float d_rc = low ? __expf(gr - s.gam[c]) : 0.f;
-                    const float g_rc = low ? s.fd[r][c] * br * d_rc : 0.f;
-                    const float g_cr = up ? s.fd[c][r] * s.bet[c] * __expf(s.gam[c] - gr) : 0.f;
-                    gsv[jj] = g_rc + g_cr;
-                    const float zz = g_rc * kk[jj];
-                    zpr += zz;
-                    zp[c] = -zz;
-                    dba += low ? s.fd[r][c] * kk[jj] * d_rc : 0.f;
-                }
-                st_row32(s.gs, r, q * 32, gsv);
+            for (int jj = 0; jj < 32; ++jj) {
+                const int c = c0 + jj;
+                const bool low = c < r && r < L, up = c > r && c < L;
+                const float d_rc = low ? __expf(gr - s.gam[c]) : 0.f;
+                const float da_rc = s.fd[r * 65 + c];
+                const float g_rc = low ? da_rc * br * d_rc : 0.f;
+                const float g_cr = up ? s.fd[c * 65 + r] * s.bet[c] * __expf(s.gam[c] - gr) : 0.f;
+                gsv[jj] = g_rc + g_cr;
+                const float zz = g_rc * kk[jj];
+                zpr += zz;
+                zp[jj] = -zz;
+                dba += low ? da_rc * kk[jj] * d_rc : 0.f;
             }
-            s.zprow[r] = zpr;
-            s.dbA[r] = dba;
+            st_row32(s.gs, r, c0, gsv);
+            s.zprow[hs][r] = zpr;
+            s.dbA[hs][r] = dba;
         } else {
 #pragma unroll
-            for (int c = 0; c < 64; ++c) zp[c] = 0.f;
+            for (int jj = 0; jj < 32; ++jj) zp[jj] = 0.f;
         }
         tc_fence_before();
         fence_proxy_async();
-        reduce64(zp, s.zcol, s.red, true);
+        reduce32(zp, s.zcol, s.red, true);
     }
 
     // ---------------- wave 3
@@ -420,80 +441,76 @@ tc_local_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (__syncthreads_or(!ok)) goto bail;
     tc_fence_after();
     {
+        // feature v (= k for dq, dk; = v for dv), chunk rows c0 .. c0+31
         const long long rs = (long long)H * kD;
-        TG *dq = (TG *)a.dq + (bos * H + h) * (long long)kD + tid;
-        TG *dk = (TG *)a.dk + (bos * H + h) * (long long)kD + tid;
-        TG *dv = (TG *)a.dv + (bos * H + h) * (long long)kD + tid;
-        const uint8_t *krow = s.qk + (tid >> 6) * 2 * kTile + kTile;
-        const uint8_t *vrow = s.v + (tid >> 6) * kTile;
-        float pz[64];
+        TG *dq = (TG *)a.dq + (bos * H + h) * (long long)kD + v;
+        TG *dk = (TG *)a.dk + (bos * H + h) * (long long)kD + v;
+        TG *dv = (TG *)a.dv + (bos * H + h) * (long long)kD + v;
+        const uint8_t *krow = s.qk + (v >> 6) * 2 * kTile + kTile;
+        const uint8_t *vrow = s.v + (v >> 6) * kTile;
+        float x[32], y[32], pz[32], pw[32];
+        tmem_ld32(tmem_addr(t_q1, warp, c0), x);
+        tmem_ld32(tmem_addr(t_q2, warp, c0), y);
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            float q1[32], q2[32];
-            tmem_ld32(tmem_addr(t_q1, warp, q * 32), q1);
-            tmem_ld32(tmem_addr(t_q2, warp, q * 32), q2);
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-                const int c = q * 32 + jj;
-                if (c < L) from_f(dq + c * rs, scale * s.ee[c] * q1[jj] + q2[jj]);
-            }
-            float d[32], e[32], y[32];
-            tmem_ld32(tmem_addr(t_dk, warp, q * 32), d);
-            tmem_ld32(tmem_addr(t_dkh, warp, q * 32), e);
-            tmem_ld32(tmem_addr(t_yw, warp, q * 32), y);
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-                const int c = q * 32 + jj;
-                const float dkh = s.ff[c] * e[jj];
-                if (c < L) from_f(dk + c * rs, d[jj] + dkh + s.bet[c] * s.ee[c] * y[jj]);
-                pz[c] = c < L ? dkh * ld_bf16(krow, c, tid & 63) : 0.f;
-            }
+        for (int jj = 0; jj < 32; ++jj) {
+            const int c = c0 + jj;
+            if (c < L) from_f(dq + c * rs, scale * s.ee[c] * x[jj] + y[jj]);
         }
-        reduce64(pz, s.zpp, s.red, false);
+        tmem_ld32(tmem_addr(t_dk, warp, c0), x);
+        tmem_ld32(tmem_addr(t_dkh, warp, c0), y);
+        tmem_ld32(tmem_addr(t_yw, warp, c0), pw);
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            float y[32];
-            tmem_ld32(tmem_addr(t_yw, warp, q * 32), y);
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-                const int c = q * 32 + jj;
-                pz[c] = c < L ? y[jj] * ld_bf16(krow, c, tid & 63) : 0.f;
-            }
+        for (int jj = 0; jj < 32; ++jj) {
+            const int c = c0 + jj;
+            const float kv = c < L ? ld_bf16(krow, c, v & 63) : 0.f;
+            const float dkh = s.ff[c] * y[jj];
+            if (c < L) from_f(dk + c * rs, x[jj] + dkh + s.bet[c] * s.ee[c] * pw[jj]);
+            pz[jj] = dkh * kv;
+            pw[jj] *= kv;
         }
-        reduce64(pz, s.yw, s.red, false);
+        reduce32(pz, s.zpp, s.red, false);
+        reduce32(pw, s.yw, s.red, false);
+        tmem_ld32(tmem_addr(t_yu, warp, c0), y);
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            float y[32];
-            tmem_ld32(tmem_addr(t_yu, warp, q * 32), y);
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-                const int c = q * 32 + jj;
-                if (c < L) from_f(dv + c * rs, s.bet[c] * y[jj]);
-                pz[c] = c < L ? y[jj] * ld_bf16(vrow, c, tid & 63) : 0.f;
-            }
+        for (int jj = 0; jj < 32; ++jj) {
+            const int c = c0 + jj;
+            if (c < L) from_f(dv + c * rs, s.bet[c] * y[jj]);
+            pz[jj] = c < L ? y[jj] * ld_bf16(vrow, c, v & 63) : 0.f;
         }
-        reduce64(pz, s.yu, s.red, false);
+        reduce32(pz, s.yu, s.red, false);
     }
     {
-        const float zsum = block_sum(tid < 64 ? s.zpp[tid] : 0.f, s.hdot + 4);
+        const float zsum = block_sum(tid < 64 ? s.zpp[tid] : 0.f, s.hdot + 8);
         if (tid < 64) {
-            float dgam = 0.f, db = 0.f;
+            const int r = tid;
+            float dgam = 0.f;
             if (r < L) {
-                dgam = s.zrow[r] + s.zprow[r] + s.zcol[r] + s.bet[r] * s.ee[r] * s.yw[r] +
-                       scale * s.ee[r] * s.rowA[r] - s.zpp[r];
+                dgam = s.zrow[0][r] + s.zrow[1][r] + s.zprow[0][r] + s.zprow[1][r] + s.zcol[r] +
+                       s.bet[r] * s.ee[r] * s.yw[r] + scale * s.ee[r] * s.rowA[r] - s.zpp[r];
                 if (r == L - 1) dgam += zsum + s.ee[r] * s.hdot[0];
-                db = s.yu[r] + s.ee[r] * s.yw[r] + s.dbA[r];
-                a.dbeta[(bos + r) * H + h] = db;
+                a.dbeta[(bos + r) * H + h] = s.yu[r] + s.ee[r] * s.yw[r] + s.dbA[0][r] + s.dbA[1][r];
             }
-            s.red[0][r] = dgam;
+            s.red[r >> 5][r & 31] = dgam;
         }
         __syncthreads();
-        if (tid == 0) {
-            float acc = 0.f;
-            for (int c = L - 1; c >= 0; --c) {
-                acc += s.red[0][c];
-                a.dg[(bos + c) * H + h] = acc;
+        if (tid < 64) {
+            // dg = reverse cumsum of dgam within the chunk (warp scans over 2 x 32)
+            const int lane = tid & 31, w = tid >> 5;
+            float x = s.red[1 - w][31 - lane];          // reversed order: position p = 63 - r
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float yv = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += yv;
             }
+            s.red[2 + w][lane] = x;
+        }
+        __syncthreads();
+        if (tid < 64) {
+            const int pidx = tid;                        // position in reversed order
+            const int r = 63 - pidx;
+            float x = s.red[2 + (pidx >> 5)][pidx & 31];
+            if (pidx >= 32) x += s.red[2][31];
+            if (r < L) a.dg[(bos + r) * H + h] = x;
         }
     }
     goto done;
@@ -536,10 +553,10 @@ cudaError_t local_grads(const Plan &p, cudaStream_t s) {
     prof_before("tc_local_grad", s);
     if (p.grad_dtype == GDN_BF16) {
         if ((e = set_smem(tc_local_kernel<__nv_bfloat16>, smem)) != cudaSuccess) return e;
-        tc_local_kernel<__nv_bfloat16><<<grid, 128, smem, s>>>(mq, mk, mv, mdo, mdu, mw, g, a);
+        tc_local_kernel<__nv_bfloat16><<<grid, 256, smem, s>>>(mq, mk, mv, mdo, mdu, mw, g, a);
     } else {
         if ((e = set_smem(tc_local_kernel<float>, smem)) != cudaSuccess) return e;
-        tc_local_kernel<float><<<grid, 128, smem, s>>>(mq, mk, mv, mdo, mdu, mw, g, a);
+        tc_local_kernel<float><<<grid, 256, smem, s>>>(mq, mk, mv, mdo, mdu, mw, g, a);
     }
     prof_after(s);
     return cudaGetLastError();
