@@ -163,7 +163,8 @@ def workload_problem(name):
 def config_of(p, name):
     m = p.meta
     return {"workload": f"{name}: B={p.B} T={p.T} H={p.H} K={p.K} V={p.V} "
-                        f"{m['dtype']} q/k/v, fp32 g/beta/state, cp={m['cp']}, fwd+bwd",
+                        f"{m['dtype']} q/k/v, fp32 g/beta/state, cp={m['cp']}, "
+                        f"fwd (keeping its context) + bwd",
             "global_batch": p.B, "seq_len": p.T, "heads": p.H, "parallelism": "replicas",
             "l2_flush_between_steps": True}
 
@@ -221,11 +222,14 @@ def run_ours(args, rank, world, local):
     stream = torch.cuda.current_stream(dev)
 
     def step(x):
-        o, fs = gdn.chunk_gated_delta_rule_fwd(x.q, x.k, x.v, x.g, x.beta, initial_state=x.h0,
-                                               output_final_state=True, cu_seqlens=x.cu_seqlens,
-                                               cp=cp)
+        # a training step: the forward keeps its per-chunk context, the backward reuses it
+        o, fs, saved = gdn.chunk_gated_delta_rule_fwd(x.q, x.k, x.v, x.g, x.beta,
+                                                      initial_state=x.h0, output_final_state=True,
+                                                      cu_seqlens=x.cu_seqlens, cp=cp,
+                                                      save_ctx=True)
         grads = gdn.chunk_gated_delta_rule_bwd(x.q, x.k, x.v, x.g, x.beta, x.do, dht=x.dht,
-                                               initial_state=x.h0, cu_seqlens=x.cu_seqlens, cp=cp)
+                                               initial_state=x.h0, cu_seqlens=x.cu_seqlens, cp=cp,
+                                               ctx=saved)
         return (o, fs) + tuple(grads)
 
     def fwd_only(x):

@@ -26,7 +26,7 @@ class gdn_fwd_args(ctypes.Structure):
                 ("B", _i32), ("T", _i32), ("H", _i32), ("K", _i32), ("V", _i32), ("N", _i32),
                 ("dtype", _i32), ("scale", _f32), ("use_qk_l2norm", _i32), ("cp_mode", _i32),
                 ("cp_segment_chunks", _i32), ("cp_warmup_chunks", _i32), ("cp_warmup_tau", _f32),
-                ("o", _vp), ("final_state", _vp), ("cp_stats", _vp)]
+                ("o", _vp), ("final_state", _vp), ("cp_stats", _vp), ("ctx", _vp)]
 
 
 class gdn_bwd_args(ctypes.Structure):
@@ -37,7 +37,7 @@ class gdn_bwd_args(ctypes.Structure):
                 ("cp_segment_chunks", _i32),
                 ("d_o", _vp), ("d_final_state", _vp),
                 ("grad_dtype", _i32), ("dq", _vp), ("dk", _vp), ("dv", _vp), ("dg", _vp),
-                ("dbeta", _vp), ("d_initial_state", _vp)]
+                ("dbeta", _vp), ("d_initial_state", _vp), ("ctx", _vp)]
 
 
 class gdn_kernel_stat(ctypes.Structure):
@@ -46,7 +46,7 @@ class gdn_kernel_stat(ctypes.Structure):
 
 EXPORTS = ("gdn_abi_version", "gdn_fwd_workspace_size", "gdn_chunk_fwd", "gdn_bwd_workspace_size",
            "gdn_chunk_bwd", "gdn_sync_status", "gdn_last_error", "gdn_set_spin_limit",
-           "gdn_profile_begin", "gdn_profile_end", "gdn_chunk_fwd_static")
+           "gdn_profile_begin", "gdn_profile_end", "gdn_chunk_fwd_static", "gdn_fwd_ctx_size")
 GDN_STATIC_SCRATCH_BYTES = 64 << 20
 
 _lib = None
@@ -77,6 +77,8 @@ def load(path: str = LIB_PATH):
     lib.gdn_last_error.argtypes = []
     lib.gdn_set_spin_limit.restype = None
     lib.gdn_set_spin_limit.argtypes = [ctypes.c_int64]
+    lib.gdn_fwd_ctx_size.restype = ctypes.c_size_t
+    lib.gdn_fwd_ctx_size.argtypes = [ctypes.POINTER(gdn_fwd_args)]
     lib.gdn_chunk_fwd_static.restype = _i32
     lib.gdn_chunk_fwd_static.argtypes = [ctypes.POINTER(gdn_fwd_args), _vp]
     lib.gdn_profile_begin.restype = _i32
@@ -110,6 +112,11 @@ def gdn_fwd_workspace_size(args: gdn_fwd_args) -> int:
     if n == 0:
         raise GdnError("gdn_fwd_workspace_size", GDN_ERR_INVALID_ARG)
     return n
+
+
+def gdn_fwd_ctx_size(args: gdn_fwd_args) -> int:
+    """Bytes of the saved forward context (0: this path keeps none)."""
+    return int(load().gdn_fwd_ctx_size(ctypes.byref(args)))
 
 
 def gdn_bwd_workspace_size(args: gdn_bwd_args) -> int:

@@ -67,8 +67,10 @@ def _common(args, q, k, v, g, beta, initial_state, cu_seqlens, scale, use_qk_l2n
 def chunk_gated_delta_rule_fwd(q, k, v, g, beta, scale=None, initial_state=None,
                                output_final_state=True, cu_seqlens=None, use_qk_l2norm=False,
                                cp="auto", cp_segment_chunks=0, cp_warmup_chunks=0,
-                               cp_warmup_tau=1e-3, cp_stats=None):
-    """Low-level forward: returns (o, final_state or None)."""
+                               cp_warmup_tau=1e-3, cp_stats=None, save_ctx=False):
+    """Low-level forward: returns (o, final_state or None), or
+    (o, final_state, ctx) with save_ctx=True, where ctx is the saved-context
+    buffer for chunk_gated_delta_rule_bwd (None when the path keeps none)."""
     a = _abi.gdn_fwd_args()
     B, T, H, K, V, N, dev = _common(a, q, k, v, g, beta, initial_state, cu_seqlens, scale,
                                     use_qk_l2norm, cp, cp_segment_chunks)
@@ -78,17 +80,24 @@ def chunk_gated_delta_rule_fwd(q, k, v, g, beta, scale=None, initial_state=None,
     a.cp_warmup_chunks = int(cp_warmup_chunks)
     a.cp_warmup_tau = float(cp_warmup_tau)
     a.cp_stats = _ptr(cp_stats)
+    ctx = None
+    if save_ctx:
+        nc = _abi.gdn_fwd_ctx_size(a)
+        if nc > 0:
+            ctx = torch.empty(nc, dtype=torch.uint8, device=dev)
+            a.ctx = ctx.data_ptr()
     n = _abi.gdn_fwd_workspace_size(a)
     ws = torch.empty(n, dtype=torch.uint8, device=dev)
     _abi.gdn_chunk_fwd(a, ws.data_ptr(), n, torch.cuda.current_stream(dev).cuda_stream)
-    return o, fs
+    return (o, fs, ctx) if save_ctx else (o, fs)
 
 
 def chunk_gated_delta_rule_bwd(q, k, v, g, beta, do, dht=None, scale=None, initial_state=None,
                                cu_seqlens=None, use_qk_l2norm=False, cp="auto",
                                cp_segment_chunks=0, grad_dtype=torch.float32,
-                               want_dh0=True):
-    """Low-level backward: returns (dq, dk, dv, dg, dbeta, dh0 or None)."""
+                               want_dh0=True, ctx=None):
+    """Low-level backward: returns (dq, dk, dv, dg, dbeta, dh0 or None).
+    `ctx` (optional) is the buffer a forward with the same inputs saved."""
     a = _abi.gdn_bwd_args()
     B, T, H, K, V, N, dev = _common(a, q, k, v, g, beta, initial_state, cu_seqlens, scale,
                                     use_qk_l2norm, cp, cp_segment_chunks)
@@ -106,6 +115,7 @@ def chunk_gated_delta_rule_bwd(q, k, v, g, beta, do, dht=None, scale=None, initi
     a.grad_dtype = _DT[grad_dtype]
     a.dq, a.dk, a.dv, a.dg, a.dbeta = (t.data_ptr() for t in (dq, dk, dv, dg, db))
     a.d_initial_state = _ptr(dh0)
+    a.ctx = _ptr(ctx)
     n = _abi.gdn_bwd_workspace_size(a)
     ws = torch.empty(n, dtype=torch.uint8, device=dev)
     _abi.gdn_chunk_bwd(a, ws.data_ptr(), n, torch.cuda.current_stream(dev).cuda_stream)
@@ -115,22 +125,24 @@ def chunk_gated_delta_rule_bwd(q, k, v, g, beta, do, dht=None, scale=None, initi
 class _ChunkGatedDeltaRule(torch.autograd.Function):
     @staticmethod
     def forward(ctx, q, k, v, g, beta, initial_state, scale, cu_seqlens, use_qk_l2norm, cp):
-        o, fs = chunk_gated_delta_rule_fwd(q, k, v, g, beta, scale=scale,
-                                           initial_state=initial_state, output_final_state=True,
-                                           cu_seqlens=cu_seqlens, use_qk_l2norm=use_qk_l2norm,
-                                           cp=cp)
-        ctx.save_for_backward(q, k, v, g, beta, initial_state, cu_seqlens)
+        o, fs, saved = chunk_gated_delta_rule_fwd(q, k, v, g, beta, scale=scale,
+                                                  initial_state=initial_state,
+                                                  output_final_state=True,
+                                                  cu_seqlens=cu_seqlens,
+                                                  use_qk_l2norm=use_qk_l2norm, cp=cp,
+                                                  save_ctx=True)
+        ctx.save_for_backward(q, k, v, g, beta, initial_state, cu_seqlens, saved)
         ctx.cfg = (scale, use_qk_l2norm, cp)
         return o, fs
 
     @staticmethod
     def backward(ctx, do, dht):
-        q, k, v, g, beta, h0, cu = ctx.saved_tensors
+        q, k, v, g, beta, h0, cu, saved = ctx.saved_tensors
         scale, l2, cp = ctx.cfg
         dq, dk, dv, dg, db, dh0 = chunk_gated_delta_rule_bwd(
             q, k, v, g, beta, do.contiguous().to(q.dtype),
             dht=None if dht is None else dht.contiguous(), scale=scale, initial_state=h0,
-            cu_seqlens=cu, use_qk_l2norm=l2, cp=cp, want_dh0=h0 is not None)
+            cu_seqlens=cu, use_qk_l2norm=l2, cp=cp, want_dh0=h0 is not None, ctx=saved)
         return (dq.to(q.dtype), dk.to(k.dtype), dv.to(v.dtype), dg, db, dh0, None, None, None,
                 None)
 

@@ -206,6 +206,31 @@ static int seg_capacity(const Common &c, int max_chunks) {
     return c.cu ? max_chunks + c.N : (max_chunks > c.B ? max_chunks : c.B);
 }
 
+// Saved forward context (tensor-core path): gam, W, u, T, chunk start states.
+static size_t ctx_layout(Plan &p, char *base) {
+    size_t off = 0;
+    auto take = [&](size_t bytes) -> char * {
+        char *ptr = base ? base + off : nullptr;
+        off += (bytes + kAlign - 1) / kAlign * kAlign;
+        return ptr;
+    };
+    const Geo &g = p.g;
+    const size_t th = (size_t)g.B * g.T * g.H;
+    float *gam = (float *)take(th * sizeof(float));
+    void *w = take(th * g.K * 2);
+    void *u = take(th * g.V * 2);
+    float *tm = (float *)take((size_t)p.max_chunks * g.H * 64 * 64 * sizeof(float));
+    float *hc = (float *)take((size_t)p.max_chunks * g.H * g.K * g.V * sizeof(float));
+    if (base) {
+        p.ws.gam = gam;
+        p.ws.w = w;
+        p.ws.u = u;
+        p.ws.tmat = tm;
+        p.ws.hc = hc;
+    }
+    return off;
+}
+
 static Common common_of(const gdn_fwd_args *a) {
     return Common{a->q, a->k, a->v, a->g, a->beta, a->initial_state, a->cu_seqlens,
                   a->B, a->T, a->H, a->K, a->V, a->N, a->dtype, a->use_qk_l2norm,
@@ -239,6 +264,14 @@ size_t gdn_fwd_workspace_size(const gdn_fwd_args *a) {
         p.max_segs = seg_capacity(common_of(a), p.max_chunks);
     }
     return layout(p, false, nullptr);
+}
+
+size_t gdn_fwd_ctx_size(const gdn_fwd_args *a) {
+    if (!a) { fail(GDN_ERR_INVALID_ARG, "null args"); return 0; }
+    Plan p;
+    if (make_plan(common_of(a), false, 0, p) != GDN_OK) return 0;
+    if (!tc::supported(p)) return 0;
+    return ctx_layout(p, nullptr);
 }
 
 size_t gdn_bwd_workspace_size(const gdn_bwd_args *a) {
@@ -288,8 +321,17 @@ gdn_status gdn_chunk_fwd(const gdn_fwd_args *a, void *ws, size_t ws_bytes, void 
     p.cp_stats = a->cp_stats;
     p.warm_chunks = p.cp ? a->cp_warmup_chunks : 0;
     p.warm_tau = a->cp_warmup_tau;
+    const bool save = a->ctx && tc::supported(p);
+    if (save && p.warm_chunks > 0)
+        return fail(GDN_ERR_INVALID_ARG,
+                    "ctx cannot be saved under the warmup shortcut (its states are approximate)");
+    if (save) {
+        if (((uintptr_t)a->ctx & (kAlign - 1)) != 0)
+            return fail(GDN_ERR_INVALID_ARG, "ctx must be 256-byte aligned");
+        ctx_layout(p, (char *)a->ctx);
+    }
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t e = tc::supported(p) ? tc::forward(p, s) : simt::forward(p, s);
+    cudaError_t e = tc::supported(p) ? tc::forward(p, s, save) : simt::forward(p, s);
     if (e != cudaSuccess) return cuda_fail(e, "forward launch");
     return GDN_OK;
 }
@@ -313,8 +355,14 @@ gdn_status gdn_chunk_bwd(const gdn_bwd_args *a, void *ws, size_t ws_bytes, void 
     p.grad_dtype = a->grad_dtype;
     p.dq = a->dq; p.dk = a->dk; p.dv = a->dv;
     p.dg = a->dg; p.dbeta = a->dbeta; p.dh0 = a->d_initial_state;
+    const bool have_ctx = a->ctx && tc::supported(p);
+    if (have_ctx) {
+        if (((uintptr_t)a->ctx & (kAlign - 1)) != 0)
+            return fail(GDN_ERR_INVALID_ARG, "ctx must be 256-byte aligned");
+        ctx_layout(p, (char *)const_cast<void *>(a->ctx));
+    }
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t e = tc::supported(p) ? tc::backward(p, s) : simt::backward(p, s);
+    cudaError_t e = tc::supported(p) ? tc::backward(p, s, have_ctx) : simt::backward(p, s);
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
     return GDN_OK;
 }

@@ -76,10 +76,12 @@ cudaError_t local_grads(const Plan &p, cudaStream_t s, bool ws_bf16);
 namespace tc {
 // bf16 q/k/v with K = V = 128 and at least one token.
 bool supported(const Plan &p);
-cudaError_t forward(const Plan &p, cudaStream_t s);
+// save: also keep T (p.ws.tmat) and every chunk's start state (p.ws.hc).
+cudaError_t forward(const Plan &p, cudaStream_t s, bool save);
 // Backward pieces: prep + walk storing chunk start states (p.ws.hc).
 cudaError_t recompute_states(const Plan &p, cudaStream_t s);
-cudaError_t backward(const Plan &p, cudaStream_t s);
+// have_ctx: gam, W, u, T and the chunk start states are already in p.ws.
+cudaError_t backward(const Plan &p, cudaStream_t s, bool have_ctx);
 // Chunk-local gradients on tensor cores (no q/k L2 normalisation).
 cudaError_t local_grads(const Plan &p, cudaStream_t s);
 // TMA descriptors of [tokens, H, 128] bf16 tensors (64 x 1 x 64 boxes, 128B swizzle).

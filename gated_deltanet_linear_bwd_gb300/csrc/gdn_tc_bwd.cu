@@ -348,10 +348,10 @@ tc_dwalk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 }
 
 // ------------------------------------------------------------------ host side
-cudaError_t backward(const Plan &p, cudaStream_t s) {
+cudaError_t backward(const Plan &p, cudaStream_t s, bool have_ctx) {
     cudaError_t e = simt::tables(p, s);
     if (e != cudaSuccess) return e;
-    if ((e = recompute_states(p, s)) != cudaSuccess) return e;
+    if (!have_ctx && (e = recompute_states(p, s)) != cudaSuccess) return e;
     const Geo &g = p.g;
     const long long tokens = (long long)g.B * g.T;
     CUtensorMap mq, mk, mw, mdo;

@@ -593,7 +593,8 @@ bool supported(const Plan &p) {
 
 // Prep, then the walk: with output (states_only = false) or storing every
 // chunk's start state into p.ws.hc (states_only = true, for the backward).
-static cudaError_t run_forward(const Plan &p, cudaStream_t s, bool states_only) {
+// save (with output): also keep T and the chunk start states for the backward.
+static cudaError_t run_forward(const Plan &p, cudaStream_t s, bool states_only, bool save) {
     cudaError_t e = encoder();
     if (e != cudaSuccess) return e;
     const Geo &g = p.g;
@@ -613,7 +614,7 @@ static cudaError_t run_forward(const Plan &p, cudaStream_t s, bool states_only) 
     prof_before("tc_prep", s);
     tc_prep_kernel<<<dim3((p.max_chunks + 1) / 2, g.H), 128, prep_smem, s>>>(
         mk, mv, g, p.ws.gam, (__nv_bfloat16 *)p.ws.w, (__nv_bfloat16 *)p.ws.u,
-        states_only ? p.ws.tmat : nullptr);
+        (states_only || save) ? p.ws.tmat : nullptr);
     prof_after(s);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
@@ -622,7 +623,7 @@ static cudaError_t run_forward(const Plan &p, cudaStream_t s, bool states_only) 
     a.h0 = p.h0;
     a.o = states_only ? nullptr : (__nv_bfloat16 *)p.o;
     a.final_state = states_only ? nullptr : p.final_state;
-    a.hc = states_only ? p.ws.hc : nullptr;
+    a.hc = (states_only || save) ? p.ws.hc : nullptr;
     const char *out_name = states_only ? "tc_walk_states" : "tc_walk_out";
     if (p.cp) {
         a.cp = 1;
@@ -649,13 +650,13 @@ static cudaError_t run_forward(const Plan &p, cudaStream_t s, bool states_only) 
     return cudaGetLastError();
 }
 
-cudaError_t forward(const Plan &p, cudaStream_t s) {
+cudaError_t forward(const Plan &p, cudaStream_t s, bool save) {
     cudaError_t e = simt::tables(p, s);
     if (e != cudaSuccess) return e;
-    return run_forward(p, s, false);
+    return run_forward(p, s, false, save);
 }
 
-cudaError_t recompute_states(const Plan &p, cudaStream_t s) { return run_forward(p, s, true); }
+cudaError_t recompute_states(const Plan &p, cudaStream_t s) { return run_forward(p, s, true, false); }
 
 }  // namespace tc
 }  // namespace gdn

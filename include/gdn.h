@@ -44,7 +44,7 @@
 extern "C" {
 #endif
 
-#define GDN_ABI_VERSION 1
+#define GDN_ABI_VERSION 2
 
 typedef int32_t gdn_status;
 enum {
@@ -95,6 +95,10 @@ typedef struct gdn_fwd_args {
     float *final_state;         /* [N, H, K, V] fp32, NULL = not written            */
     int32_t *cp_stats;          /* NULL, or 2 device int32: heads that took the warmup
                                    shortcut, heads walked under CP (accumulated)     */
+    void *ctx;                  /* NULL, or a saved-context buffer of
+                                   gdn_fwd_ctx_size() bytes (256-byte aligned): the
+                                   forward also keeps what the backward would
+                                   otherwise recompute (see gdn_fwd_ctx_size)        */
 } gdn_fwd_args;
 
 typedef struct gdn_bwd_args {
@@ -120,6 +124,9 @@ typedef struct gdn_bwd_args {
     float *dg;                  /* [B, T, H]                                        */
     float *dbeta;               /* [B, T, H]                                        */
     float *d_initial_state;     /* [N, H, K, V] fp32, NULL = not written            */
+    const void *ctx;            /* NULL, or the buffer a gdn_chunk_fwd call with the same
+                                   inputs and sizes filled: the backward then skips
+                                   recomputing the forward's per-chunk quantities   */
 } gdn_bwd_args;
 
 /* GDN_ABI_VERSION of the loaded library. */
@@ -134,6 +141,15 @@ size_t gdn_fwd_workspace_size(const gdn_fwd_args *args);
  * the inter-chunk term plus the masked intra-chunk term. */
 gdn_status gdn_chunk_fwd(const gdn_fwd_args *args, void *workspace, size_t workspace_bytes,
                          void *stream);
+
+/* Bytes of the saved forward context for these arguments: 0 when the path
+ * keeps none (then gdn_chunk_fwd ignores args->ctx and gdn_chunk_bwd
+ * recomputes).  The tensor-core path (bf16, K = V = 128) keeps the
+ * within-chunk cumsum of g, W, u, each chunk's (I + A)^-1 and each chunk's
+ * start state: about 4 K V / 64 + 2 (K + V) + 260 bytes per token and head.
+ * The contents are only meaningful to a gdn_chunk_bwd call with the same
+ * inputs, sizes and flags; the library cannot check that. */
+size_t gdn_fwd_ctx_size(const gdn_fwd_args *args);
 
 /* Bytes of workspace gdn_chunk_bwd needs. */
 size_t gdn_bwd_workspace_size(const gdn_bwd_args *args);

@@ -100,6 +100,44 @@ def test_cp_result_does_not_depend_on_segmenting():
         assert np.abs(fs - ref_fs).max() <= 1e-3
 
 
+# ------------------------------------------------------------- saved forward context
+@pytest.mark.parametrize("kw,cp", [
+    (dict(B=2, T=300, H=2), "off"),
+    (dict(B=1, T=700, H=2), "force"),
+    (dict(lengths=[130, 0, 64, 257], H=2), "auto"),
+])
+def test_backward_with_saved_context_matches_recompute_and_oracle(kw, cp):
+    gdn = lib()
+    p = gdn_synth.make("training", h0_std=0.1, dht_std=0.01, **kw)
+    d = p.to("cuda")
+    o, fs, saved = gdn.chunk_gated_delta_rule_fwd(d.q, d.k, d.v, d.g, d.beta, initial_state=d.h0,
+                                                  cu_seqlens=d.cu_seqlens, cp=cp, save_ctx=True)
+    assert saved is not None and saved.numel() > 0
+    with_ctx = gdn.chunk_gated_delta_rule_bwd(d.q, d.k, d.v, d.g, d.beta, d.do, dht=d.dht,
+                                              initial_state=d.h0, cu_seqlens=d.cu_seqlens, cp=cp,
+                                              ctx=saved)
+    torch.cuda.synchronize()
+    r = oracle_bwd(p)
+    ro, rfs = oracle_fwd(p)
+    check("o (saving)", to_np(o), ro, TOL["bf16"])
+    check("final_state (saving)", to_np(fs), rfs, TOL["bf16"])
+    g = gpu_bwd(p, cp=cp)
+    for name, x in zip(["dq", "dk", "dv", "dg", "dbeta", "dh0"], with_ctx):
+        check(f"{name} with ctx", to_np(x), r[name], TOL["bf16"])
+        assert np.abs(to_np(x) - g[name]).max() <= 1e-3, name   # same arithmetic either way
+
+
+def test_fp32_path_keeps_no_context_and_warmup_refuses_one():
+    gdn = lib()
+    p = gdn_synth.make("tiny", T=100).to("cuda")
+    o, fs, saved = gdn.chunk_gated_delta_rule_fwd(p.q, p.k, p.v, p.g, p.beta, save_ctx=True)
+    assert saved is None
+    pb = gdn_synth.make("edge", T=1024, H=2).to("cuda")
+    with pytest.raises(gdn.GdnError, match="warmup"):
+        gdn.chunk_gated_delta_rule_fwd(pb.q, pb.k, pb.v, pb.g, pb.beta, cp="force",
+                                       cp_warmup_chunks=4, save_ctx=True)
+
+
 # ------------------------------------------------------------- warmup shortcut (flag)
 def test_warmup_shortcut_error_is_reported_separately():
     # strongly decaying heads: the 6-chunk window forgets all but ~e^-40 of the state
