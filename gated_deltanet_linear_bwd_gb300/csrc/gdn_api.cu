@@ -4,6 +4,7 @@
 // nothing here allocates device memory.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdarg>
@@ -177,8 +178,10 @@ static size_t layout(Plan &p, bool bwd, char *base) {
     w = Ws{};
     w.counters = (int32_t *)take(64 * sizeof(int32_t));
     w.gam = (float *)take(th * sizeof(float));
-    w.w = take(th * g.K * sizeof(float));
-    w.u = take(th * g.V * sizeof(float));
+    // CUDA cores keep fp32 token rows, tensor cores bf16 chunk tiles of 64 rows
+    const size_t tiles = (size_t)p.max_chunks * g.H * 64 * 2;
+    w.w = take(std::max(th * g.K * sizeof(float), tiles * g.K));
+    w.u = take(std::max(th * g.V * sizeof(float), tiles * g.V));
     if (g.cu) {
         w.chunk_off = (int32_t *)take((g.N + 1) * sizeof(int32_t));
         w.seg_off = (int32_t *)take((g.N + 1) * sizeof(int32_t));
@@ -192,7 +195,7 @@ static size_t layout(Plan &p, bool bwd, char *base) {
         const size_t st = (size_t)p.max_chunks * g.H * g.K * g.V * sizeof(float);
         w.hc = (float *)take(st);
         w.dhc = (float *)take(st);
-        w.du = take(th * g.V * 2);
+        w.du = take(tiles * g.V);
         w.tmat = (float *)take((size_t)p.max_chunks * g.H * 64 * 64 * sizeof(float));
         w.scratch = (float *)take((size_t)p.scratch_ctas *
                                   simt::scratch_floats_per_cta(g.K, g.V) * sizeof(float));
@@ -217,8 +220,9 @@ static size_t ctx_layout(Plan &p, char *base) {
     const Geo &g = p.g;
     const size_t th = (size_t)g.B * g.T * g.H;
     float *gam = (float *)take(th * sizeof(float));
-    void *w = take(th * g.K * 2);
-    void *u = take(th * g.V * 2);
+    const size_t tiles = (size_t)p.max_chunks * g.H * 64 * 2;   // bf16 chunk tiles
+    void *w = take(tiles * g.K);
+    void *u = take(tiles * g.V);
     float *tm = (float *)take((size_t)p.max_chunks * g.H * 64 * 64 * sizeof(float));
     float *hc = (float *)take((size_t)p.max_chunks * g.H * g.K * g.V * sizeof(float));
     if (base) {

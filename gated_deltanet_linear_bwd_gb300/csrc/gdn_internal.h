@@ -14,8 +14,9 @@ namespace gdn {
 // Device pointers carved out of the caller's workspace.
 struct Ws {
     float *gam = nullptr;        // [tokens, H] within-chunk cumsum of g
-    void *w = nullptr;           // [tokens, H, K] W rows (fp32 or bf16, per path)
-    void *u = nullptr;           // [tokens, H, V] u rows
+    void *w = nullptr;           // W: fp32 [tokens, H, K] (CUDA cores) or bf16 W^T tiles
+                                 // [chunk][H][K][64] (tensor cores)
+    void *u = nullptr;           // u: likewise ([tokens, H, V] or [chunk][H][V][64])
     int32_t *chunk_off = nullptr;  // [N+1] (varlen)
     int32_t *seg_off = nullptr;    // [N+1] (varlen + CP)
     int32_t *warm = nullptr;       // [N, H] warmup decision
@@ -23,7 +24,7 @@ struct Ws {
     float *seg_state = nullptr;    // [segs, H, K, V] segment start states / end gradients
     float *hc = nullptr;           // [chunks, H, K, V] chunk start states (bwd)
     float *dhc = nullptr;          // [chunks, H, K, V] chunk end gradients (bwd)
-    void *du = nullptr;            // [tokens, H, V] bf16 dU of the reverse walk (bwd, tensor cores)
+    void *du = nullptr;            // [chunk][H][V][64] bf16 dU^T of the reverse walk (bwd, tensor cores)
     float *tmat = nullptr;         // [chunks, H, 64, 64] fp32 T = (I + A)^-1 by column (bwd, tensor cores)
     float *scratch = nullptr;      // per-CTA scratch (bwd, CUDA-core path)
     int32_t *counters = nullptr;   // small zeroed counters
@@ -87,6 +88,8 @@ cudaError_t local_grads(const Plan &p, cudaStream_t s);
 // TMA descriptors of [tokens, H, 128] bf16 tensors (64 x 1 x 64 boxes, 128B swizzle).
 cudaError_t encoder();
 cudaError_t make_map(CUtensorMap *m, const void *base, long long tokens, int H);
+// Chunk-major transposed tiles [chunk][H][128][64] bf16 (W^T, u^T, dU^T): one box per tile.
+cudaError_t make_map_tiles(CUtensorMap *m, const void *base, long long rows_total);
 }  // namespace tc
 
 }  // namespace gdn

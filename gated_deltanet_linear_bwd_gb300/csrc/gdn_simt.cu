@@ -651,14 +651,24 @@ local_grad_kernel(Geo g, LocalArgs a) {
         __syncthreads();
         unit_lower_inverse(Tm, M1, L);
 
+        // W and u: fp32 token rows from the CUDA-core forward, bf16 transposed
+        // chunk tiles [chunk][H][feature][64 rows] from the tensor-core forward
+        const TW *wsw = (const TW *)a.ws_w, *wsu = (const TW *)a.ws_u;
+        auto Wat = [&](int r, int i) {
+            return sizeof(TW) == 4 ? to_f(wsw[((bos + r) * H + h) * (long long)K + i])
+                                   : to_f(wsw[(((long long)ci * H + h) * K + i) * kChunk + r]);
+        };
+        auto uat = [&](int r, int j) {
+            return sizeof(TW) == 4 ? to_f(wsu[((bos + r) * H + h) * (long long)V + j])
+                                   : to_f(wsu[(((long long)ci * H + h) * V + j) * kChunk + r]);
+        };
         // U = u - W H0 ; dU = scale P^T dO + diag(f) K dHL
         for (int idx = tid; idx < L * V; idx += blockDim.x) {
             const int r = idx / V, j = idx % V;
-            const TW *wr = (const TW *)a.ws_w + ((bos + r) * H + h) * (long long)K;
-            float u = to_f(((const TW *)a.ws_u)[((bos + r) * H + h) * (long long)V + j]);
+            float u = uat(r, j);
             float kd = 0.f;
             for (int i = 0; i < K; ++i) {
-                u -= to_f(wr[i]) * H0[i * V + j];
+                u -= Wat(r, i) * H0[i * V + j];
                 kd += Ks[r * (K + 1) + i] * dHL[i * V + j];
             }
             float pd = 0.f;

@@ -31,11 +31,11 @@ constexpr uint32_t idesc_neg_a(uint32_t d) { return d | (1u << 13); }
 constexpr uint32_t kIdKK64 = idesc_bf16(128, 64, false, false);   // K-major A, K-major B
 constexpr uint32_t kIdMM64 = idesc_bf16(128, 64, true, true);     // MN-major A and B, N = 64
 constexpr uint32_t kIdMM128 = idesc_bf16(128, 128, true, true);   // MN-major A and B, N = 128
-constexpr uint32_t kIdKM128Neg = idesc_neg_a(idesc_bf16(128, 128, false, true));
+constexpr uint32_t kIdKK128Neg = idesc_neg_a(idesc_bf16(128, 128, false, false));
 
 struct DWalkSmem {
     uint8_t qk[2][4 * kTile];      // per stage: [dk half][Q rows 0-63, K rows 64-127][128 B]
-    uint8_t w[2][2 * kTile];       // per stage: [dk half][64 rows][128 B]
+    uint8_t w[2][2 * kTile];       // per stage: W^T, [128 rows k][64 chunk rows]  K-major B
     uint8_t dO[2][2 * kTile];      // per stage: [dv half][64 rows][128 B]
     uint8_t dhT[4 * kTile];        // [dk half][128 rows (v)][128 B]      K-major A
     uint8_t qs[2 * kTile];         // diag(scale e^gam) Q: [dk half][64 rows r][128 B], MN-major B
@@ -54,7 +54,7 @@ struct TcDWalkArgs {
     const float *seg_end;     // [segs, H, K, V] (CP): gradient at each segment's end
     float *dh0;               // [N, H, K, V] nullable
     float *dhc;               // [chunks, H, K, V] gradient at every chunk's end (kOut)
-    __nv_bfloat16 *du;        // [tokens, H, V] dU (kOut), nullable
+    __nv_bfloat16 *du;        // [chunk][H][V][64] dU^T tiles (kOut), nullable
     float *maps;              // [segs, H, K, K+V] (kMap)
     int cp;
 };
@@ -141,9 +141,9 @@ tc_dwalk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int half = 0; half < 2; ++half) {
             tma_load_3d(s.qk[st] + half * 2 * kTile, &tm_q, &s.tma_bar[st], half * 64, h, tok0);
             tma_load_3d(s.qk[st] + half * 2 * kTile + kTile, &tm_k, &s.tma_bar[st], half * 64, h, tok0);
-            tma_load_3d(s.w[st] + half * kTile, &tm_w, &s.tma_bar[st], half * 64, h, tok0);
             tma_load_3d(s.dO[st] + half * kTile, &tm_do, &s.tma_bar[st], half * 64, h, tok0);
         }
+        tma_load_2d(s.w[st], &tm_w, &s.tma_bar[st], 0, (int)(((long long)(cbase + c) * H + h) * kD));
     };
 
     int it = 0, mma_n = 0, tma_pending = 0;
@@ -274,11 +274,19 @@ tc_dwalk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
             st_row32(s.duT, v, 32 * hs, x);
             if (MODE == kDOut && a.du) {
-                __nv_bfloat16 *dst = a.du + (bos * H + h) * (long long)kD + v;
+                // 32 chunk rows of dU^T row v: 64 contiguous bytes of the chunk tile
+                uint4 *dst = reinterpret_cast<uint4 *>(
+                    a.du + (((long long)(cbase + c) * H + h) * kD + v) * 64 + 32 * hs);
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj)
-                    if (32 * hs + jj < L)
-                        dst[(long long)(32 * hs + jj) * H * kD] = __float2bfloat16_rn(x[jj]);
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t w4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        __nv_bfloat162 b2 = __floats2bfloat162_rn(x[8 * q + 2 * e], x[8 * q + 2 * e + 1]);
+                        w4[e] = *reinterpret_cast<uint32_t *>(&b2);
+                    }
+                    dst[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                }
             }
         }
         tc_fence_before();
@@ -301,8 +309,8 @@ tc_dwalk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
                 const uint64_t au = desc_sw128(du + kk * 32, 16, 1024);
-                const uint64_t bw = desc_sw128(wt + kk * 2048, kTile, 1024);
-                mma_bf16(t_z, au, bw, kIdKM128Neg, (use_do || kk > 0) ? 1u : 0u);
+                const uint64_t bw = desc_sw128(wt + kk * 32, 16, 1024);   // W^T, K-major
+                mma_bf16(t_z, au, bw, kIdKK128Neg, (use_do || kk > 0) ? 1u : 0u);
             }
             mma_commit(&s.mma_bar);
         }
@@ -357,7 +365,8 @@ cudaError_t backward(const Plan &p, cudaStream_t s, bool have_ctx) {
     CUtensorMap mq, mk, mw, mdo;
     if ((e = make_map(&mq, g.q, tokens, g.H)) != cudaSuccess) return e;
     if ((e = make_map(&mk, g.k, tokens, g.H)) != cudaSuccess) return e;
-    if ((e = make_map(&mw, p.ws.w, tokens, g.H)) != cudaSuccess) return e;
+    if ((e = make_map_tiles(&mw, p.ws.w, (long long)p.max_chunks * g.H * kD)) != cudaSuccess)
+        return e;
     if ((e = make_map(&mdo, p.d_o, tokens, g.H)) != cudaSuccess) return e;
     const size_t smem = sizeof(DWalkSmem) + 1024;
     if ((e = set_smem(tc_dwalk_kernel<kDOut>, smem)) != cudaSuccess) return e;

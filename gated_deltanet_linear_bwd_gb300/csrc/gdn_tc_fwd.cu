@@ -217,23 +217,32 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     ok = mbar_wait(&s.mma_bar, 1, g.spin_limit, g.status);
     if (__syncthreads_or(!ok)) goto bail;
     tc_fence_after();
-    // thread t = feature index (dk for W, dv for u); columns = chunk rows
+    // thread t = feature index (dk for W, dv for u); its 64 chunk rows form one
+    // contiguous 128-byte row of the chunk-major tile [chunk][H][feature][row]
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
         const int c = m & 1;                  // chunk
         const bool isu = m >= 2;
+        if (c && !has_b) continue;
         const ChunkRef &cr = c ? rb : ra;
-        const int Lc = (c && !has_b) ? 0 : cr.len;
-        __nv_bfloat16 *dst = isu ? ws_u : ws_w;
+        const int Lc = cr.len;
+        uint4 *dst = reinterpret_cast<uint4 *>(
+            (isu ? ws_u : ws_w) + (((long long)(2 * blockIdx.x + c) * H + h) * kD + tid) * 64);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             float x[32];
-            tmem_ld32(tmem_addr(tbase, warp, (isu ? 128 : 0) + c * 64 + half * 32), x);
+            tmem_ld32(tmem_addr(tbase, warp, (isu ? 128 : 0) + c * 64 + 32 * half), x);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int row = half * 32 + j;
-                if (row < Lc)
-                    dst[((cr.bos + row) * H + h) * (long long)kD + tid] = __float2bfloat16_rn(x[j]);
+            for (int q = 0; q < 4; ++q) {
+                uint32_t w4[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int j0 = 8 * q + 2 * e, r0 = 32 * half + j0;
+                    __nv_bfloat162 b2 = __floats2bfloat162_rn(r0 < Lc ? x[j0] : 0.f,
+                                                              r0 + 1 < Lc ? x[j0 + 1] : 0.f);
+                    w4[e] = *reinterpret_cast<uint32_t *>(&b2);
+                }
+                dst[4 * half + q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
             }
         }
     }
@@ -252,8 +261,8 @@ done:
 // ------------------------------------------------------------------ walk
 struct WalkSmem {
     uint8_t qk[2][4 * kTile];      // per stage: [dk half][rows 0-63 Q, 64-127 K][128 B]
-    uint8_t w[2][2 * kTile];       // per stage: [dk half][64 rows][128 B]
-    uint8_t u[2][2 * kTile];       // per stage: [dv half][64 rows][128 B]
+    uint8_t w[2][2 * kTile];       // per stage: W^T, [128 rows k][64 chunk rows]
+    uint8_t u[2][2 * kTile];       // per stage: u^T, [128 rows v][64 chunk rows]
     uint8_t hT[4 * kTile];         // [dk half][128 state rows][128 B]  (A operand)
     uint8_t uT[2 * kTile];         // [128 state rows][64 chunk rows]   (A operand)
     uint8_t uTs[2 * kTile];        // U^T diag(f)                        (A operand)
@@ -282,6 +291,7 @@ enum { kWalkOut = 0, kWalkMap = 1 };
 
 constexpr uint32_t kIdesc64 = idesc_bf16(128, 64, false, false);      // K-major A and B
 constexpr uint32_t kIdescDH = idesc_bf16(128, 128, false, true);      // B MN-major
+constexpr uint32_t kIdescKM64 = idesc_bf16(128, 64, false, true);     // B MN-major, N = 64
 
 // 256 threads: thread t owns state row v = t % 128 (TMEM lane v) and the
 // column half hs = t / 128; warps w and w + 4 share a TMEM lane quarter and
@@ -367,9 +377,10 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         for (int half = 0; half < 2; ++half) {
             tma_load_3d(s.qk[st] + half * 2 * kTile, &tm_q, &s.tma_bar[st], half * 64, h, tok0);
             tma_load_3d(s.qk[st] + half * 2 * kTile + kTile, &tm_k, &s.tma_bar[st], half * 64, h, tok0);
-            tma_load_3d(s.w[st] + half * kTile, &tm_w, &s.tma_bar[st], half * 64, h, tok0);
-            tma_load_3d(s.u[st] + half * kTile, &tm_u, &s.tma_bar[st], half * 64, h, tok0);
         }
+        const int trow = (int)(((long long)(cbase + c) * H + h) * kD);
+        tma_load_2d(s.w[st], &tm_w, &s.tma_bar[st], 0, trow);
+        tma_load_2d(s.u[st], &tm_u, &s.tma_bar[st], 0, trow);
     };
 
     int it = 0, mma_n = 0, tma_pending = 0;   // uniform bookkeeping for the bail-out path
@@ -421,8 +432,8 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             for (int kk = 0; kk < 8; ++kk) {
                 const uint32_t half = kk >> 2, sub = (kk & 3) * 32;
                 const uint64_t ah = desc_sw128(hT + half * 2 * kTile + sub, 16, 1024);
-                const uint64_t bw = desc_sw128(wt + half * kTile + sub, 16, 1024);
-                mma_bf16(t_u, ah, bw, kIdesc64, kk > 0);
+                const uint64_t bw = desc_sw128(wt + kk * 2048, 2 * kTile, 1024);   // W^T, MN-major
+                mma_bf16(t_u, ah, bw, kIdescKM64, kk > 0);
                 if (out_now) {
                     const uint64_t aq = desc_sw128(qk + half * 2 * kTile + sub, 16, 1024);
                     const uint64_t bk = desc_sw128(qk + half * 2 * kTile + kTile + sub, 16, 1024);
@@ -445,12 +456,19 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // U = u - W H for chunk rows 32*hs .. +31 of this thread's state column
             float acc[32], U[32];
             tmem_ld32(tmem_addr(t_u, warp, 32 * hs), acc);
-            const uint8_t *ut = s.u[st] + (v >> 6) * kTile;
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-                const int r = 32 * hs + jj;
-                const float uv = a_cols ? 0.f : ld_bf16(ut, r, v & 63);
-                U[jj] = r < L ? uv - acc[jj] : 0.f;
+            for (int q = 0; q < 4; ++q) {
+                // 8 chunk rows of u^T row v: one 16-byte swizzled chunk
+                uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+                if (!a_cols)
+                    raw = *reinterpret_cast<const uint4 *>(
+                        s.u[st] + v * 128 + ((((32 * hs) >> 3) + q) ^ (v & 7)) * 16);
+                const __nv_bfloat16 *bv = reinterpret_cast<const __nv_bfloat16 *>(&raw);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int jj = 8 * q + e, r = 32 * hs + jj;
+                    U[jj] = r < L ? __bfloat162float(bv[e]) - acc[jj] : 0.f;
+                }
             }
             st_row32(s.uT, v, 32 * hs, U);
 #pragma unroll
@@ -587,8 +605,24 @@ cudaError_t make_map(CUtensorMap *m, const void *base, long long tokens, int H) 
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Chunk-major transposed tiles [chunk][H][128 features][64 rows] bf16 viewed as
+// 2-D (64 rows, rows_total features); one 64 x 128 box = one (chunk, head) tile.
+cudaError_t make_map_tiles(CUtensorMap *m, const void *base, long long rows_total) {
+    const cuuint64_t dims[2] = {64, (cuuint64_t)rows_total};
+    const cuuint64_t strides[1] = {64 * 2};
+    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t es[2] = {1, 1};
+    const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base),
+                                dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 bool supported(const Plan &p) {
-    return p.dtype == GDN_BF16 && p.g.K == kD && p.g.V == kD && (long long)p.g.B * p.g.T > 0;
+    // the chunk-tile TMA row coordinate (chunk * H + head) * 128 is a 32-bit int
+    return p.dtype == GDN_BF16 && p.g.K == kD && p.g.V == kD && (long long)p.g.B * p.g.T > 0 &&
+           (long long)p.max_chunks * p.g.H * kD < (1ll << 31);
 }
 
 // Prep, then the walk: with output (states_only = false) or storing every
@@ -603,8 +637,9 @@ static cudaError_t run_forward(const Plan &p, cudaStream_t s, bool states_only, 
     if ((e = make_map(&mq, g.q, tokens, g.H)) != cudaSuccess) return e;
     if ((e = make_map(&mk, g.k, tokens, g.H)) != cudaSuccess) return e;
     if ((e = make_map(&mv, g.v, tokens, g.H)) != cudaSuccess) return e;
-    if ((e = make_map(&mw, p.ws.w, tokens, g.H)) != cudaSuccess) return e;
-    if ((e = make_map(&mu, p.ws.u, tokens, g.H)) != cudaSuccess) return e;
+    const long long tile_rows = (long long)p.max_chunks * g.H * kD;
+    if ((e = make_map_tiles(&mw, p.ws.w, tile_rows)) != cudaSuccess) return e;
+    if ((e = make_map_tiles(&mu, p.ws.u, tile_rows)) != cudaSuccess) return e;
 
     const size_t prep_smem = sizeof(PrepSmem) + 1024, walk_smem = sizeof(WalkSmem) + 1024;
     if ((e = set_smem(tc_prep_kernel, prep_smem)) != cudaSuccess) return e;

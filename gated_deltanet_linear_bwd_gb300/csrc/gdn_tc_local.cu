@@ -1,8 +1,8 @@
 // gdn_tc_local.cu -- tensor-core chunk-local gradients for bf16 q/k/v with
 // K = V = 128 (no q/k L2 normalisation), one (chunk, head) per CTA.
 //
-// Inputs per chunk: q, k, v, dO (TMA), dU and W (workspace, TMA), u (from
-// the workspace), the chunk start state H0 and the gradient at its end dHL
+// Inputs per chunk: q, k, v, dO (TMA), dU^T and W^T (workspace chunk tiles,
+// TMA), u^T (workspace chunk tile), the chunk start state H0 and the gradient at its end dHL
 // (workspace, fp32), gam and beta.  With D = exp(gam_r - gam_s),
 // e = exp(gam), f = exp(gam_L - gam), and T = (I + A)^-1 recomputed:
 //   U    = u - W H0   (T itself is kept by the recompute's prep kernel)
@@ -41,8 +41,8 @@ struct LocalSmem {
     uint8_t qk[4 * kTile];     // [dk half][Q rows 0-63, K rows 64-127][128 B]
     uint8_t v[2 * kTile];      // [dv half][64 rows][128 B]
     uint8_t dO[2 * kTile];     // after wave 2: dHL^T k half 0
-    uint8_t du[2 * kTile];
-    uint8_t w[2 * kTile];      // after wave 1: dHL^T k half 1
+    uint8_t du[2 * kTile];     // dU^T: [128 rows v][64 chunk rows]
+    uint8_t w[2 * kTile];      // W^T: [128 rows k][64 chunk rows]; after wave 1: dHL^T k half 1
     uint8_t h0T[4 * kTile];    // [k half][128 rows v][128 B]; after wave 1: uT, dwT
     uint8_t ds[kTile];         // dS rows r
     uint8_t tt[kTile];         // row r = column r of T
@@ -164,9 +164,10 @@ tc_local_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tma_load_3d(s.qk + half * 2 * kTile + kTile, &tm_k, &s.tma_bar, half * 64, h, tok0);
             tma_load_3d(s.v + half * kTile, &tm_v, &s.tma_bar, half * 64, h, tok0);
             tma_load_3d(s.dO + half * kTile, &tm_do, &s.tma_bar, half * 64, h, tok0);
-            tma_load_3d(s.du + half * kTile, &tm_du, &s.tma_bar, half * 64, h, tok0);
-            tma_load_3d(s.w + half * kTile, &tm_w, &s.tma_bar, half * 64, h, tok0);
         }
+        const int trow = (int)(((long long)ci * H + h) * kD);
+        tma_load_2d(s.du, &tm_du, &s.tma_bar, 0, trow);
+        tma_load_2d(s.w, &tm_w, &s.tma_bar, 0, trow);
     }
     if (tid < 64) {
         s.gam[tid] = tid < L ? a.ws_gam[(bos + tid) * H + h] : 0.f;
@@ -205,13 +206,14 @@ tc_local_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const uint64_t aH = desc_sw128(h0 + hh * 2 * kTile + sub, 16, 1024);
             const uint64_t aQK = desc_sw128(qk + hh * 2 * kTile + sub, 16, 1024);
             const uint64_t bK = desc_sw128(qk + hh * 2 * kTile + kTile + sub, 16, 1024);
-            mma_bf16(t_u, aH, desc_sw128(w + hh * kTile + sub, 16, 1024), kKK, kk > 0);
+            mma_bf16(t_u, aH, desc_sw128(w + kk * 2048, 2 * kTile, 1024), kKM, kk > 0);   // W^T, MN-major
             mma_bf16(t_p, aQK, bK, kKK, kk > 0);
             mma_bf16(t_qh, aH, aQK, kKK, kk > 0);
-            mma_bf16(t_tu, desc_sw128(du + hh * kTile + sub, 16, 1024),
-                     desc_sw128(vv + hh * kTile + sub, 16, 1024), kKK, kk > 0);
+            // dU V^T: A = dU from the dU^T tile (MN-major; lanes 64-127 alias rows 0-63)
+            mma_bf16(t_tu, desc_sw128(du + kk * 2048, 0, 1024),
+                     desc_sw128(vv + hh * kTile + sub, 16, 1024), kMK, kk > 0);
             const uint64_t aHm = desc_sw128(h0 + kk * 2048, 2 * kTile, 1024);   // H0, MN-major
-            mma_bf16(t_dw, aHm, desc_sw128(du + hh * kTile + sub, 16, 1024), kMK, kk > 0);
+            mma_bf16(t_dw, aHm, desc_sw128(du + kk * 2048, 2 * kTile, 1024), kMM, kk > 0);
             mma_bf16(t_q1, aHm, desc_sw128(dO + hh * kTile + sub, 16, 1024), kMK, kk > 0);
         }
         mma_commit(&s.mma_bar);
@@ -222,15 +224,22 @@ tc_local_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     {
         // U^T (row v, chunk rows c0..c0+31) into uT; -(H0 dU^T) (row k = v) into dwT;
         // partial sums of dO[r][v] (Q H0)[r][v] over v for rowA
-        const __nv_bfloat16 *ug = a.ws_u + (bos * H + h) * (long long)kD + v;
+        // u^T tile row v, chunk rows c0 .. c0+31: 64 contiguous bytes
+        const uint4 *ug = reinterpret_cast<const uint4 *>(
+            a.ws_u + (((long long)ci * H + h) * kD + v) * 64 + c0);
         float x[32], y[32];
         tmem_ld32(tmem_addr(t_u, warp, c0), x);
         tmem_ld32(tmem_addr(t_qh, warp, c0), y);
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-            const int c = c0 + jj;
-            x[jj] = c < L ? __bfloat162float(ug[(long long)c * H * kD]) - x[jj] : 0.f;
-            y[jj] = c < L ? ld_bf16(s.dO + (v >> 6) * kTile, c, v & 63) * y[jj] : 0.f;
+        for (int q = 0; q < 4; ++q) {
+            const uint4 raw = ug[q];
+            const __nv_bfloat16 *bv = reinterpret_cast<const __nv_bfloat16 *>(&raw);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int jj = 8 * q + e, c = c0 + jj;
+                x[jj] = c < L ? __bfloat162float(bv[e]) - x[jj] : 0.f;
+                y[jj] = c < L ? ld_bf16(s.dO + (v >> 6) * kTile, c, v & 63) * y[jj] : 0.f;
+            }
         }
         st_row32(uT, v, c0, x);
         tmem_ld32(tmem_addr(t_dw, warp, c0), x);
@@ -428,8 +437,8 @@ tc_local_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             mma_bf16(t_dk, aK, desc_sw128(gs + kk * 32, 16, 1024), kMK, 1);
             mma_bf16(t_yw, desc_sw128(dwa + kk * 32, 16, 1024), desc_sw128(tt + kk * 32, 16, 1024),
                      kKK, kk > 0);
-            mma_bf16(t_yu, desc_sw128(du + kk * 2048, kTile, 1024), desc_sw128(tt + kk * 32, 16, 1024),
-                     kMK, kk > 0);
+            mma_bf16(t_yu, desc_sw128(du + kk * 32, 16, 1024), desc_sw128(tt + kk * 32, 16, 1024),
+                     kKK, kk > 0);   // dU^T, K-major
         }
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
@@ -535,8 +544,9 @@ cudaError_t local_grads(const Plan &p, cudaStream_t s) {
     if ((e = make_map(&mk, g.k, tokens, g.H)) != cudaSuccess) return e;
     if ((e = make_map(&mv, g.v, tokens, g.H)) != cudaSuccess) return e;
     if ((e = make_map(&mdo, p.d_o, tokens, g.H)) != cudaSuccess) return e;
-    if ((e = make_map(&mdu, p.ws.du, tokens, g.H)) != cudaSuccess) return e;
-    if ((e = make_map(&mw, p.ws.w, tokens, g.H)) != cudaSuccess) return e;
+    const long long tile_rows = (long long)p.max_chunks * g.H * kD;
+    if ((e = make_map_tiles(&mdu, p.ws.du, tile_rows)) != cudaSuccess) return e;
+    if ((e = make_map_tiles(&mw, p.ws.w, tile_rows)) != cudaSuccess) return e;
     TcLocalArgs a{};
     a.ws_gam = p.ws.gam;
     a.hc = p.ws.hc;
