@@ -67,6 +67,44 @@ def kernel_flops_per_token_head(name, K, V):
 FP32_LANES_PER_SM = 128
 
 
+# Per-kernel algorithmic HBM bytes per token-head for the tensor-core path
+# (bf16 q/k/v/dO, bf16 gradients, K = V = 128, chunk C = 64): every operand
+# read once, every result written once.  W^T, u^T, dU^T are the bf16 chunk
+# tiles; T is the fp32 64 x 64 inverse and hc / dhc the fp32 chunk states,
+# so per token they cost 64 * 4 and K * V * 4 / C bytes.
+def kernel_bytes_per_token_head(name, K, V, e=2, eg=2):
+    C = CHUNK
+    t_mat = C * 4
+    state = K * V * 4 / C
+    table = {
+        "tc_prep": e * (K + V) + 8 + 4 + 2 * (K + V) + t_mat,
+        "tc_walk_out": 2 * e * K + 2 * (K + V) + 4 + e * V + state,
+        "tc_dwalk_out": 2 * e * K + 2 * K + e * V + 4 + state + 2 * V,
+        "tc_local_grad": (e * (2 * K + 2 * V) + 2 * (K + 2 * V) + 2 * state + t_mat + 8 +
+                          eg * (2 * K + V) + 8),
+    }
+    return table.get(name)
+
+
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
+# ncu capture of the named kernel on the named workload, valid while the
+# kernel's source file still hashes to `sha256` (otherwise reported as null).
+NCU_TRAFFIC = {}
+
+
+def measured_traffic(name, workload):
+    import hashlib
+    rec = NCU_TRAFFIC.get((name, workload))
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "gated_deltanet_linear_bwd_gb300", "csrc", rec["file"])
+    try:
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    return rec["bytes"] if digest == rec["sha256"] else None
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled during the timed region."""
@@ -198,6 +236,14 @@ def run_reference(args, rank, world):
     return 0
 
 
+def kernel_entry(name, launches, ms, total_ms, p, th, e_in):
+    ent = {"name": name, "launches": launches, "ms": ms, "share": ms / total_ms}
+    by_th = kernel_bytes_per_token_head(name, p.K, p.V, e_in, e_in)
+    if by_th is not None:
+        ent["gbs"] = by_th * th / (ms / launches / 1e3) / 1e9
+    return ent
+
+
 def run_ours(args, rank, world, local):
     import torch
     import gated_deltanet_linear_bwd_gb300 as gdn
@@ -319,15 +365,26 @@ def run_ours(args, rank, world, local):
     dom = max(prof, key=lambda s: s[2])
     dom_name, dom_launches, dom_ms = dom
     avg_s = dom_ms / dom_launches / 1e3
-    per_th = kernel_flops_per_token_head(dom_name, p.K, p.V)
-    sm_max = (clk or {}).get("sm_max_mhz") or peaks.get("sm_max_mhz", 2070.0)
-    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    alu_peak = n_sms * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
-    roof = {"kernel": dom_name, "bound": "alu", "unit": "TFLOP/s",
-            "achieved": None if per_th is None else per_th * th / avg_s / 1e12,
-            "peak": alu_peak, "peak_source": "fp32 FMA: SMs x 128 lanes x 2 x max SM clock",
-            "traffic": None, "avg_launch_ms": avg_s * 1e3, "launches_per_step":
-                dom_launches / args.steps}
+    hbm_src = "measured" if "hbm_gbs" in peaks else "fallback"
+    by_th = kernel_bytes_per_token_head(dom_name, p.K, p.V, e_in, e_in)
+    if by_th is not None:
+        # the tensor-core kernels move more bytes than their few MMAs can hide: HBM roofline
+        roof = {"kernel": dom_name, "bound": "hbm", "unit": "GB/s",
+                "achieved": by_th * th / avg_s / 1e9, "peak": hbm,
+                "peak_source": f"{hbm_src} HBM copy bandwidth",
+                "bytes_per_launch": by_th * th,
+                "traffic": measured_traffic(dom_name, args.workload),
+                "avg_launch_ms": avg_s * 1e3, "launches_per_step": dom_launches / args.steps}
+    else:
+        per_th = kernel_flops_per_token_head(dom_name, p.K, p.V)
+        sm_max = (clk or {}).get("sm_max_mhz") or peaks.get("sm_max_mhz", 2070.0)
+        n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        alu_peak = n_sms * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
+        roof = {"kernel": dom_name, "bound": "alu", "unit": "TFLOP/s",
+                "achieved": None if per_th is None else per_th * th / avg_s / 1e12,
+                "peak": alu_peak, "peak_source": "fp32 FMA: SMs x 128 lanes x 2 x max SM clock",
+                "traffic": None, "avg_launch_ms": avg_s * 1e3,
+                "launches_per_step": dom_launches / args.steps}
     roof["frac"] = None if roof["achieved"] is None else roof["achieved"] / roof["peak"]
 
     cpu = None
@@ -348,7 +405,7 @@ def run_ours(args, rank, world, local):
                               "peaks": {"hbm_gbs": hbm, "bf16_tflops": bf16,
                                         "source": "measured" if peaks else "fallback"}},
             "roofline": roof,
-            "kernels": [{"name": n, "launches": l, "ms": m, "share": m / sum(s[2] for s in prof)}
+            "kernels": [kernel_entry(n, l, m, sum(s[2] for s in prof), p, th, e_in)
                         for n, l, m in prof],
             "gpu_launches": total_launches,
             "e2e": {"value": world * tokens / (ms_e2e / 1e3), "unit": "tokens/s",

@@ -224,7 +224,7 @@ static size_t ctx_layout(Plan &p, char *base) {
     void *w = take(tiles * g.K);
     void *u = take(tiles * g.V);
     float *tm = (float *)take((size_t)p.max_chunks * g.H * 64 * 64 * sizeof(float));
-    float *hc = (float *)take((size_t)p.max_chunks * g.H * g.K * g.V * sizeof(float));
+    float *hc = (float *)take((size_t)p.max_chunks * g.H * g.K * g.V * 2);   // bf16 tiles
     if (base) {
         p.ws.gam = gam;
         p.ws.w = w;

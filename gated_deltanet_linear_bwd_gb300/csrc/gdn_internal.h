@@ -22,8 +22,9 @@ struct Ws {
     int32_t *warm = nullptr;       // [N, H] warmup decision
     float *maps = nullptr;         // [segs, H, K, K+V] affine maps
     float *seg_state = nullptr;    // [segs, H, K, V] segment start states / end gradients
-    float *hc = nullptr;           // [chunks, H, K, V] chunk start states (bwd)
-    float *dhc = nullptr;          // [chunks, H, K, V] chunk end gradients (bwd)
+    float *hc = nullptr;           // chunk start states (bwd): fp32 [chunks, H, K, V] (CUDA
+                                   // cores) or bf16 H^T tiles [chunk][H][k half][v][64] (tensor cores)
+    float *dhc = nullptr;          // chunk end gradients (bwd): likewise, dH^T tiles on tensor cores
     void *du = nullptr;            // [chunk][H][V][64] bf16 dU^T of the reverse walk (bwd, tensor cores)
     float *tmat = nullptr;         // [chunks, H, 64, 64] fp32 T = (I + A)^-1 by column (bwd, tensor cores)
     float *scratch = nullptr;      // per-CTA scratch (bwd, CUDA-core path)

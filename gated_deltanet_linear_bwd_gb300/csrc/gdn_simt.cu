@@ -613,8 +613,19 @@ local_grad_kernel(Geo g, LocalArgs a) {
         if (!chunk_ref(g, ci, cr)) break;
         const int L = cr.len;
         const long long bos = cr.bos;
-        const float *H0 = a.hc + ((long long)ci * H + h) * K * V;
-        const float *dHL = a.dhc + ((long long)ci * H + h) * K * V;
+        // chunk states: fp32 [K][V] from the CUDA-core walks, bf16 transposed tiles
+        // [k half][v][64] from the tensor-core walks (K = V = 128 there)
+        const long long hoff = ((long long)ci * H + h) * K * V;
+        const float *hc32 = a.hc + hoff, *dhc32 = a.dhc + hoff;
+        const __nv_bfloat16 *hc16 = (const __nv_bfloat16 *)a.hc + hoff,
+                            *dhc16 = (const __nv_bfloat16 *)a.dhc + hoff;
+        auto tile_at = [&](int i, int j) { return ((i >> 6) * V + j) * 64 + (i & 63); };
+        auto H0at = [&](int i, int j) {
+            return sizeof(TW) == 4 ? hc32[i * V + j] : __bfloat162float(hc16[tile_at(i, j)]);
+        };
+        auto dHLat = [&](int i, int j) {
+            return sizeof(TW) == 4 ? dhc32[i * V + j] : __bfloat162float(dhc16[tile_at(i, j)]);
+        };
         auto dOat = [&](int r, int j) { return to_f(dOin[((bos + r) * H + h) * (long long)V + j]); };
         auto Vat = [&](int r, int j) { return to_f(vin[((bos + r) * H + h) * (long long)V + j]); };
 
@@ -668,8 +679,8 @@ local_grad_kernel(Geo g, LocalArgs a) {
             float u = uat(r, j);
             float kd = 0.f;
             for (int i = 0; i < K; ++i) {
-                u -= Wat(r, i) * H0[i * V + j];
-                kd += Ks[r * (K + 1) + i] * dHL[i * V + j];
+                u -= Wat(r, i) * H0at(i, j);
+                kd += Ks[r * (K + 1) + i] * dHLat(i, j);
             }
             float pd = 0.f;
             for (int rr = r; rr < L; ++rr) pd += QK[rr * 65 + r] * Dm[rr * 65 + r] * dOat(rr, j);
@@ -690,7 +701,7 @@ local_grad_kernel(Geo g, LocalArgs a) {
         for (int idx = tid; idx < L * K; idx += blockDim.x) {
             const int r = idx / K, i = idx % K;
             float acc = 0.f;
-            for (int j = 0; j < V; ++j) acc += dU[r * V + j] * H0[i * V + j];
+            for (int j = 0; j < V; ++j) acc += dU[r * V + j] * H0at(i, j);
             dW[r * K + i] = -acc;
         }
         __syncthreads();
@@ -746,8 +757,8 @@ local_grad_kernel(Geo g, LocalArgs a) {
             for (int j = lane; j < V; j += 32) {
                 float qh = 0.f, kd = 0.f;
                 for (int i = 0; i < K; ++i) {
-                    qh += Qs[r * (K + 1) + i] * H0[i * V + j];
-                    kd += Ks[r * (K + 1) + i] * dHL[i * V + j];
+                    qh += Qs[r * (K + 1) + i] * H0at(i, j);
+                    kd += Ks[r * (K + 1) + i] * dHLat(i, j);
                 }
                 sa += dOat(r, j) * qh;
                 sb += kd * U[r * V + j];
@@ -763,7 +774,8 @@ local_grad_kernel(Geo g, LocalArgs a) {
         }
         // <dHL, H0>
         float part = 0.f;
-        for (int idx = tid; idx < K * V; idx += blockDim.x) part += dHL[idx] * H0[idx];
+        for (int idx = tid; idx < K * V; idx += blockDim.x)
+            part += dHLat(idx / V, idx % V) * H0at(idx / V, idx % V);
         for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
         if (lane == 0) red[warp] = part;
         __syncthreads();
@@ -807,8 +819,8 @@ local_grad_kernel(Geo g, LocalArgs a) {
                 const int i = lane + 32 * t;
                 float aq = 0.f, ak = 0.f;
                 for (int j = 0; j < V; ++j) {
-                    aq += dOat(r, j) * H0[i * V + j];
-                    ak += U[r * V + j] * dHL[i * V + j];
+                    aq += dOat(r, j) * H0at(i, j);
+                    ak += U[r * V + j] * dHLat(i, j);
                 }
                 aq *= scale * e[r];
                 ak = f[r] * ak + bet[r] * e[r] * dYw[r * K + i];

@@ -53,7 +53,8 @@ struct TcDWalkArgs {
     const float *dht;         // [N, H, K, V] nullable
     const float *seg_end;     // [segs, H, K, V] (CP): gradient at each segment's end
     float *dh0;               // [N, H, K, V] nullable
-    float *dhc;               // [chunks, H, K, V] gradient at every chunk's end (kOut)
+    __nv_bfloat16 *dhc;       // gradient at every chunk's end (kOut), bf16 dH^T tiles
+                              // [chunk][H][k half][v][64]
     __nv_bfloat16 *du;        // [chunk][H][V][64] dU^T tiles (kOut), nullable
     float *maps;              // [segs, H, K, K+V] (kMap)
     int cp;
@@ -166,9 +167,19 @@ tc_dwalk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (tid < 64) gnext = a.ws_gam[(bos - kChunk + tid) * H + h];   // a full chunk
         }
         if (MODE == kDOut) {
-            float *dst = a.dhc + ((long long)(cbase + c) * H + h) * kD * kD;
+            // row v, k half hs of dH^T: 128 contiguous bytes of the chunk's tile
+            uint4 *dst = reinterpret_cast<uint4 *>(
+                a.dhc + ((((long long)(cbase + c) * H + h) * 2 + hs) * kD + v) * 64);
 #pragma unroll
-            for (int i = 0; i < 64; ++i) dst[(64 * hs + i) * kD + v] = dH[i];
+            for (int q = 0; q < 8; ++q) {
+                uint32_t w4[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    __nv_bfloat162 b2 = __floats2bfloat162_rn(dH[8 * q + 2 * e], dH[8 * q + 2 * e + 1]);
+                    w4[e] = *reinterpret_cast<uint32_t *>(&b2);
+                }
+                dst[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
         }
         bool ok = mbar_wait(&s.tma_bar[st], (it >> 1) & 1, g.spin_limit, g.status);
         if (__syncthreads_or(!ok)) { bailed = true; break; }
@@ -375,7 +386,7 @@ cudaError_t backward(const Plan &p, cudaStream_t s, bool have_ctx) {
     a.ws_gam = p.ws.gam;
     a.dht = p.dht;
     a.dh0 = p.dh0;
-    a.dhc = p.ws.dhc;
+    a.dhc = (__nv_bfloat16 *)p.ws.dhc;
     a.du = (__nv_bfloat16 *)p.ws.du;
     if (p.cp) {
         a.cp = 1;

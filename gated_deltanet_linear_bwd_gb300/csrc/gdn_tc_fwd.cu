@@ -282,7 +282,7 @@ struct TcWalkArgs {
     int warm_chunks;
     __nv_bfloat16 *o;         // [tokens, H, V] (kWalkOut with output) nullable
     float *final_state;       // nullable
-    float *hc;                // [chunks, H, K, V] chunk start states, nullable
+    __nv_bfloat16 *hc;        // chunk start states as bf16 H^T tiles [chunk][H][k half][v][64], nullable
     float *maps;              // [segs, H, K, K+V] (kWalkMap)
     int cp;
 };
@@ -403,9 +403,19 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             if (tid < 64 && tid < Ln) gnext = a.ws_gam[(bos + kChunk + tid) * H + h];
         }
         if (states && c >= c0) {
-            float *dst = a.hc + ((long long)(cbase + c) * H + h) * kD * kD;
+            // row v, k half hs of H^T: 128 contiguous bytes of the chunk's state tile
+            uint4 *dst = reinterpret_cast<uint4 *>(
+                a.hc + ((((long long)(cbase + c) * H + h) * 2 + hs) * kD + v) * 64);
 #pragma unroll
-            for (int i = 0; i < 64; ++i) dst[(64 * hs + i) * kD + v] = Hr[i];
+            for (int q = 0; q < 8; ++q) {
+                uint32_t w4[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    __nv_bfloat162 b2 = __floats2bfloat162_rn(Hr[8 * q + 2 * e], Hr[8 * q + 2 * e + 1]);
+                    w4[e] = *reinterpret_cast<uint32_t *>(&b2);
+                }
+                dst[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
         }
         bool ok = mbar_wait(&s.tma_bar[st], (it >> 1) & 1, g.spin_limit, g.status);
         if (__syncthreads_or(!ok)) { bailed = true; break; }
@@ -658,7 +668,7 @@ static cudaError_t run_forward(const Plan &p, cudaStream_t s, bool states_only, 
     a.h0 = p.h0;
     a.o = states_only ? nullptr : (__nv_bfloat16 *)p.o;
     a.final_state = states_only ? nullptr : p.final_state;
-    a.hc = (states_only || save) ? p.ws.hc : nullptr;
+    a.hc = (states_only || save) ? (__nv_bfloat16 *)p.ws.hc : nullptr;
     const char *out_name = states_only ? "tc_walk_states" : "tc_walk_out";
     if (p.cp) {
         a.cp = 1;

@@ -1,9 +1,9 @@
 // gdn_tc_local.cu -- tensor-core chunk-local gradients for bf16 q/k/v with
 // K = V = 128 (no q/k L2 normalisation), one (chunk, head) per CTA.
 //
-// Inputs per chunk: q, k, v, dO (TMA), dU^T and W^T (workspace chunk tiles,
-// TMA), u^T (workspace chunk tile), the chunk start state H0 and the gradient at its end dHL
-// (workspace, fp32), gam and beta.  With D = exp(gam_r - gam_s),
+// Inputs per chunk: q, k, v, dO (TMA); the workspace's bf16 chunk tiles of
+// dU^T, W^T, the chunk start state H0^T and the gradient at its end dHL^T
+// (TMA) and u^T; T, gam and beta.  With D = exp(gam_r - gam_s),
 // e = exp(gam), f = exp(gam_L - gam), and T = (I + A)^-1 recomputed:
 //   U    = u - W H0   (T itself is kept by the recompute's prep kernel)
 //   dS   = scale (dO U^T) .* lower_incl .* D
@@ -36,26 +36,29 @@ constexpr uint32_t kKK = idesc_bf16(128, 64, false, false);   // A K-major, B K-
 constexpr uint32_t kMK = idesc_bf16(128, 64, true, false);    // A MN-major, B K-major
 constexpr uint32_t kKM = idesc_bf16(128, 64, false, true);    // A K-major, B MN-major
 constexpr uint32_t kMM = idesc_bf16(128, 64, true, true);     // A MN-major, B MN-major
+constexpr uint32_t kKK128 = idesc_bf16(128, 128, false, false);   // N = 128, both K-major
 
 struct LocalSmem {
     uint8_t qk[4 * kTile];     // [dk half][Q rows 0-63, K rows 64-127][128 B]
     uint8_t v[2 * kTile];      // [dv half][64 rows][128 B]
-    uint8_t dO[2 * kTile];     // after wave 2: dHL^T k half 0
+    // dO, du, w, h0T, ds, tt, gs (104 KB, contiguous) stage dq, dk, dv after wave 3
+    uint8_t dO[2 * kTile];
     uint8_t du[2 * kTile];     // dU^T: [128 rows v][64 chunk rows]
-    uint8_t w[2 * kTile];      // W^T: [128 rows k][64 chunk rows]; after wave 1: dHL^T k half 1
-    uint8_t h0T[4 * kTile];    // [k half][128 rows v][128 B]; after wave 1: uT, dwT
+    uint8_t w[2 * kTile];      // W^T: [128 rows k][64 chunk rows]
+    uint8_t h0T[4 * kTile];    // H0^T: [k half][128 rows v][128 B]; after wave 1: uT, dwT
     uint8_t ds[kTile];         // dS rows r
     uint8_t tt[kTile];         // row r = column r of T
     uint8_t gs[kTile];         // Gs rows r
-    float xm[64][64];          // X = dT T^T, row-major
+    float xm[64][64];          // dHL^T k half 0 until wave 2 is done; then X = dT T^T
+    float fd[64 * 68];         // dHL^T k half 1 (first 16 KB) until wave 2 is done; then
+                               // dT^T (stride 68), then dA row-major (stride 65)
     float tf[64][64];          // T, row-major
     float tft[64][64];         // T^T
-    float fd[64 * 68];         // dT^T (stride 68), then dA row-major (stride 65)
     float gam[64], bet[64], ee[64], ff[64];
     float red[8][32];
     float zrow[2][64], zprow[2][64], dbA[2][64];
     float zcol[64], rowA[64], yw[64], yu[64], zpp[64];
-    float hdot[16];            // [0]: <dHL, H0>; [8..15]: block_sum scratch
+    float hdot[16];            // [0..3]: per-warp parts of <dHL, H0>; [8..15]: block_sum scratch
     uint64_t tma_bar, mma_bar;
     uint32_t tmem_base;
 };
@@ -104,7 +107,7 @@ __device__ __forceinline__ float block_sum(float x, float *scratch8) {
 }
 
 struct TcLocalArgs {
-    const float *ws_gam, *hc, *dhc, *tmat;
+    const float *ws_gam, *tmat;
     const __nv_bfloat16 *ws_u;
     void *dq, *dk, *dv;
     float *dg, *dbeta;
@@ -125,6 +128,7 @@ __global__ void __launch_bounds__(256, 1)
 tc_local_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                 const __grid_constant__ CUtensorMap tm_du, const __grid_constant__ CUtensorMap tm_w,
+                const __grid_constant__ CUtensorMap tm_hc, const __grid_constant__ CUtensorMap tm_dhc,
                 Geo g, TcLocalArgs a) {
     extern __shared__ uint8_t smem_raw[];
     LocalSmem &s = *reinterpret_cast<LocalSmem *>(
@@ -152,12 +156,12 @@ tc_local_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     tc_fence_after();
     const uint32_t tb = s.tmem_base;
     const uint32_t t_u = tb, t_p = tb + 64, t_dw = tb + 128, t_q1 = tb + 192, t_tu = tb + 256,
-                   t_qh = tb + 320;
-    const uint32_t t_dp = tb, t_tw = tb + 128;
-    const uint32_t t_q2 = tb, t_dk = tb + 128, t_dkh = tb + 256, t_yw = tb + 320, t_yu = tb + 384;
+                   t_qh = tb + 320, t_hd = tb + 384;
+    const uint32_t t_dp = tb, t_tw = tb + 128, t_dkh = tb + 448;
+    const uint32_t t_q2 = tb, t_dk = tb + 128, t_yw = tb + 320, t_yu = tb + 384;
     if (tid == 0) {
         const int tok0 = (int)bos;
-        mbar_arrive_expect_tx(&s.tma_bar, 12 * kTile);
+        mbar_arrive_expect_tx(&s.tma_bar, 20 * kTile);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             tma_load_3d(s.qk + half * 2 * kTile, &tm_q, &s.tma_bar, half * 64, h, tok0);
@@ -168,21 +172,16 @@ tc_local_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int trow = (int)(((long long)ci * H + h) * kD);
         tma_load_2d(s.du, &tm_du, &s.tma_bar, 0, trow);
         tma_load_2d(s.w, &tm_w, &s.tma_bar, 0, trow);
+        // bf16 H0^T and dHL^T tiles, [k half][128 rows v][64]
+        tma_load_2d(s.h0T, &tm_hc, &s.tma_bar, 0, 2 * trow);
+        tma_load_2d(s.h0T + 2 * kTile, &tm_hc, &s.tma_bar, 0, 2 * trow + kD);
+        tma_load_2d(s.xm, &tm_dhc, &s.tma_bar, 0, 2 * trow);
+        tma_load_2d(s.fd, &tm_dhc, &s.tma_bar, 0, 2 * trow + kD);
     }
     if (tid < 64) {
         s.gam[tid] = tid < L ? a.ws_gam[(bos + tid) * H + h] : 0.f;
         s.bet[tid] = tid < L ? g.beta[(bos + tid) * H + h] : 0.f;
     }
-    const float *H0 = a.hc + ((long long)ci * H + h) * kD * kD;
-    const float *dHL = a.dhc + ((long long)ci * H + h) * kD * kD;
-    {
-        // k half hs of column v of H0 -> row v of H0^T
-        float x[64];
-#pragma unroll
-        for (int i = 0; i < 64; ++i) x[i] = H0[(64 * hs + i) * kD + v];
-        st_row64(s.h0T + hs * 2 * kTile, v, x);
-    }
-    fence_proxy_async();
     __syncthreads();
     if (tid < 64) {
         s.ee[tid] = tid < L ? __expf(s.gam[tid]) : 0.f;
@@ -199,7 +198,8 @@ tc_local_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (tid == 0) {
         tc_fence_after();
         const uint32_t qk = smem_u32(s.qk), h0 = smem_u32(s.h0T), w = smem_u32(s.w),
-                       du = smem_u32(s.du), vv = smem_u32(s.v), dO = smem_u32(s.dO);
+                       du = smem_u32(s.du), vv = smem_u32(s.v), dO = smem_u32(s.dO),
+                       dl0 = smem_u32(s.xm), dl1 = smem_u32(s.fd);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
             const uint32_t hh = kk >> 2, sub = (kk & 3) * 32;
@@ -215,6 +215,8 @@ tc_local_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const uint64_t aHm = desc_sw128(h0 + kk * 2048, 2 * kTile, 1024);   // H0, MN-major
             mma_bf16(t_dw, aHm, desc_sw128(du + kk * 2048, 2 * kTile, 1024), kMM, kk > 0);
             mma_bf16(t_q1, aHm, desc_sw128(dO + hh * kTile + sub, 16, 1024), kMK, kk > 0);
+            // dHL^T H0 (128 x 128): its trace is <dHL, H0>
+            mma_bf16(t_hd, desc_sw128((hh ? dl1 : dl0) + sub, 16, 1024), aH, kKK128, kk > 0);
         }
         mma_commit(&s.mma_bar);
     }
@@ -246,9 +248,19 @@ tc_local_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) x[jj] = (c0 + jj) < L ? -x[jj] : 0.f;
         st_row32(dwT, v, c0, x);
+        if (hs == 0) {
+            // lane v's diagonal entry of dHL^T H0 sits in column v of t_hd
+            const int lane = tid & 31;
+            tmem_ld32(tmem_addr(t_hd, warp, 32 * warp), x);
+            float d = 0.f;
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) d = jj == lane ? x[jj] : d;
+            for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+            if (lane == 0) s.hdot[warp] = d;
+        }
         tc_fence_before();
         fence_proxy_async();
-        reduce32(y, s.rowA, s.red, false);    // its barriers publish uT and dwT
+        reduce32(y, s.rowA, s.red, false);    // its barriers publish uT, dwT and hdot
     }
 
     // ---------------- wave 2: dP = dO U^T, dW K^T (lanes 0-63); T from the recompute
@@ -256,7 +268,7 @@ tc_local_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (tid == 0) {
         tc_fence_after();
         const uint32_t qk = smem_u32(s.qk), dO = smem_u32(s.dO), uTa = smem_u32(uT),
-                       dwa = smem_u32(dwT);
+                       dwa = smem_u32(dwT), dl0 = smem_u32(s.xm), dl1 = smem_u32(s.fd);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
             const uint32_t hh = kk >> 2, sub = (kk & 3) * 32;
@@ -264,6 +276,9 @@ tc_local_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                      desc_sw128(uTa + kk * 2048, kTile, 1024), kKM, kk > 0);
             mma_bf16(t_tw, desc_sw128(dwa + kk * 2048, 0, 1024),
                      desc_sw128(qk + hh * 2 * kTile + kTile + sub, 16, 1024), kMK, kk > 0);
+            // dHL U^T: A = dHL from the dHL^T tiles (MN-major, k halves dl1 - dl0 apart)
+            mma_bf16(t_dkh, desc_sw128(dl0 + kk * 2048, dl1 - dl0, 1024),
+                     desc_sw128(uTa + kk * 2048, kTile, 1024), kMM, kk > 0);
         }
         mma_commit(&s.mma_bar);
     }
@@ -321,22 +336,7 @@ tc_local_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) z[jj] = 0.f;
         }
-        // dHL^T rows (feature v, k half hs): k half 0 into the dO tile, 1 into the W tile
-        float hd = 0.f;
-        {
-            float x[64];
-#pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                const int k = 64 * hs + i;
-                const float d = dHL[k * kD + v];
-                hd += d * H0[k * kD + v];
-                x[i] = d;
-            }
-            st_row64(hs ? s.w : s.dO, v, x);
-        }
         reduce32(z, s.zcol, s.red, false);
-        hd = block_sum(hd, s.hdot + 8);
-        if (tid == 0) s.hdot[0] = hd;
     }
     // ---------------- X = dT T^T, then dA = -T^T X (strict lower), fp32, 4 x 4 per thread
     {
@@ -425,9 +425,7 @@ tc_local_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (tid == 0) {
         tc_fence_after();
         const uint32_t qk = smem_u32(s.qk), ds = smem_u32(s.ds), gs = smem_u32(s.gs),
-                       tt = smem_u32(s.tt), dhL = smem_u32(s.dO), uTa = smem_u32(uT),
-                       dwa = smem_u32(dwT), du = smem_u32(s.du);
-        const uint32_t dh_lbo = smem_u32(s.w) - smem_u32(s.dO);
+                       tt = smem_u32(s.tt), dwa = smem_u32(dwT), du = smem_u32(s.du);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
             const uint64_t aK = desc_sw128(qk + kTile + kk * 2048, 2 * kTile, 1024);   // K, MN-major
@@ -440,21 +438,15 @@ tc_local_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             mma_bf16(t_yu, desc_sw128(du + kk * 32, 16, 1024), desc_sw128(tt + kk * 32, 16, 1024),
                      kKK, kk > 0);   // dU^T, K-major
         }
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-            mma_bf16(t_dkh, desc_sw128(dhL + kk * 2048, dh_lbo, 1024),
-                     desc_sw128(uTa + kk * 2048, kTile, 1024), kMM, kk > 0);
         mma_commit(&s.mma_bar);
     }
     ok = mbar_wait(&s.mma_bar, 0, g.spin_limit, g.status);
     if (__syncthreads_or(!ok)) goto bail;
     tc_fence_after();
     {
-        // feature v (= k for dq, dk; = v for dv), chunk rows c0 .. c0+31
-        const long long rs = (long long)H * kD;
-        TG *dq = (TG *)a.dq + (bos * H + h) * (long long)kD + v;
-        TG *dk = (TG *)a.dk + (bos * H + h) * (long long)kD + v;
-        TG *dv = (TG *)a.dv + (bos * H + h) * (long long)kD + v;
+        // feature v (= k for dq, dk; = v for dv), chunk rows c0 .. c0+31, staged as
+        // row-major [3][64 rows][128] in the dead tiles, then written out in 16-byte rows
+        TG *stg = reinterpret_cast<TG *>(s.dO);
         const uint8_t *krow = s.qk + (v >> 6) * 2 * kTile + kTile;
         const uint8_t *vrow = s.v + (v >> 6) * kTile;
         float x[32], y[32], pz[32], pw[32];
@@ -463,7 +455,7 @@ tc_local_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) {
             const int c = c0 + jj;
-            if (c < L) from_f(dq + c * rs, scale * s.ee[c] * x[jj] + y[jj]);
+            from_f(stg + c * kD + v, scale * s.ee[c] * x[jj] + y[jj]);
         }
         tmem_ld32(tmem_addr(t_dk, warp, c0), x);
         tmem_ld32(tmem_addr(t_dkh, warp, c0), y);
@@ -473,7 +465,7 @@ tc_local_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const int c = c0 + jj;
             const float kv = c < L ? ld_bf16(krow, c, v & 63) : 0.f;
             const float dkh = s.ff[c] * y[jj];
-            if (c < L) from_f(dk + c * rs, x[jj] + dkh + s.bet[c] * s.ee[c] * pw[jj]);
+            from_f(stg + (64 + c) * kD + v, x[jj] + dkh + s.bet[c] * s.ee[c] * pw[jj]);
             pz[jj] = dkh * kv;
             pw[jj] *= kv;
         }
@@ -483,10 +475,20 @@ tc_local_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) {
             const int c = c0 + jj;
-            if (c < L) from_f(dv + c * rs, s.bet[c] * y[jj]);
+            from_f(stg + (128 + c) * kD + v, s.bet[c] * y[jj]);
             pz[jj] = c < L ? y[jj] * ld_bf16(vrow, c, v & 63) : 0.f;
         }
-        reduce32(pz, s.yu, s.red, false);
+        reduce32(pz, s.yu, s.red, false);     // its barriers also publish the staged rows
+        constexpr int kVec = 16 / sizeof(TG), kPerRow = kD / kVec;
+#pragma unroll
+        for (int o = 0; o < 3; ++o) {
+            TG *out = (TG *)(o == 0 ? a.dq : o == 1 ? a.dk : a.dv) + (bos * H + h) * (long long)kD;
+            for (int i = tid; i < L * kPerRow; i += 256) {
+                const int r = i / kPerRow, q = i % kPerRow;
+                *reinterpret_cast<uint4 *>(out + (long long)r * H * kD + q * kVec) =
+                    *reinterpret_cast<const uint4 *>(stg + (o * 64 + r) * kD + q * kVec);
+            }
+        }
     }
     {
         const float zsum = block_sum(tid < 64 ? s.zpp[tid] : 0.f, s.hdot + 8);
@@ -496,7 +498,8 @@ tc_local_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (r < L) {
                 dgam = s.zrow[0][r] + s.zrow[1][r] + s.zprow[0][r] + s.zprow[1][r] + s.zcol[r] +
                        s.bet[r] * s.ee[r] * s.yw[r] + scale * s.ee[r] * s.rowA[r] - s.zpp[r];
-                if (r == L - 1) dgam += zsum + s.ee[r] * s.hdot[0];
+                if (r == L - 1)
+                    dgam += zsum + s.ee[r] * (s.hdot[0] + s.hdot[1] + s.hdot[2] + s.hdot[3]);
                 a.dbeta[(bos + r) * H + h] = s.yu[r] + s.ee[r] * s.yw[r] + s.dbA[0][r] + s.dbA[1][r];
             }
             s.red[r >> 5][r & 31] = dgam;
@@ -539,7 +542,7 @@ cudaError_t local_grads(const Plan &p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     const Geo &g = p.g;
     const long long tokens = (long long)g.B * g.T;
-    CUtensorMap mq, mk, mv, mdo, mdu, mw;
+    CUtensorMap mq, mk, mv, mdo, mdu, mw, mhc, mdhc;
     if ((e = make_map(&mq, g.q, tokens, g.H)) != cudaSuccess) return e;
     if ((e = make_map(&mk, g.k, tokens, g.H)) != cudaSuccess) return e;
     if ((e = make_map(&mv, g.v, tokens, g.H)) != cudaSuccess) return e;
@@ -547,10 +550,10 @@ cudaError_t local_grads(const Plan &p, cudaStream_t s) {
     const long long tile_rows = (long long)p.max_chunks * g.H * kD;
     if ((e = make_map_tiles(&mdu, p.ws.du, tile_rows)) != cudaSuccess) return e;
     if ((e = make_map_tiles(&mw, p.ws.w, tile_rows)) != cudaSuccess) return e;
+    if ((e = make_map_tiles(&mhc, p.ws.hc, 2 * tile_rows)) != cudaSuccess) return e;
+    if ((e = make_map_tiles(&mdhc, p.ws.dhc, 2 * tile_rows)) != cudaSuccess) return e;
     TcLocalArgs a{};
     a.ws_gam = p.ws.gam;
-    a.hc = p.ws.hc;
-    a.dhc = p.ws.dhc;
     a.tmat = p.ws.tmat;
     a.ws_u = (const __nv_bfloat16 *)p.ws.u;
     a.dq = p.dq;
@@ -563,10 +566,10 @@ cudaError_t local_grads(const Plan &p, cudaStream_t s) {
     prof_before("tc_local_grad", s);
     if (p.grad_dtype == GDN_BF16) {
         if ((e = set_smem(tc_local_kernel<__nv_bfloat16>, smem)) != cudaSuccess) return e;
-        tc_local_kernel<__nv_bfloat16><<<grid, 256, smem, s>>>(mq, mk, mv, mdo, mdu, mw, g, a);
+        tc_local_kernel<__nv_bfloat16><<<grid, 256, smem, s>>>(mq, mk, mv, mdo, mdu, mw, mhc, mdhc, g, a);
     } else {
         if ((e = set_smem(tc_local_kernel<float>, smem)) != cudaSuccess) return e;
-        tc_local_kernel<float><<<grid, 256, smem, s>>>(mq, mk, mv, mdo, mdu, mw, g, a);
+        tc_local_kernel<float><<<grid, 256, smem, s>>>(mq, mk, mv, mdo, mdu, mw, mhc, mdhc, g, a);
     }
     prof_after(s);
     return cudaGetLastError();
