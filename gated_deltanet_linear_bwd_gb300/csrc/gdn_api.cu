@@ -196,7 +196,7 @@ static size_t layout(Plan &p, bool bwd, char *base) {
         w.hc = (float *)take(st);
         w.dhc = (float *)take(st);
         w.du = take(tiles * g.V);
-        w.tmat = (float *)take((size_t)p.max_chunks * g.H * 64 * 64 * sizeof(float));
+        w.tmat = take((size_t)p.max_chunks * g.H * 64 * 64 * 2);
         w.scratch = (float *)take((size_t)p.scratch_ctas *
                                   simt::scratch_floats_per_cta(g.K, g.V) * sizeof(float));
     }
@@ -223,7 +223,7 @@ static size_t ctx_layout(Plan &p, char *base) {
     const size_t tiles = (size_t)p.max_chunks * g.H * 64 * 2;   // bf16 chunk tiles
     void *w = take(tiles * g.K);
     void *u = take(tiles * g.V);
-    float *tm = (float *)take((size_t)p.max_chunks * g.H * 64 * 64 * sizeof(float));
+    void *tm = take((size_t)p.max_chunks * g.H * 64 * 64 * 2);
     float *hc = (float *)take((size_t)p.max_chunks * g.H * g.K * g.V * 2);   // bf16 tiles
     if (base) {
         p.ws.gam = gam;

@@ -26,7 +26,7 @@ struct Ws {
                                    // cores) or bf16 H^T tiles [chunk][H][k half][v][64] (tensor cores)
     float *dhc = nullptr;          // chunk end gradients (bwd): likewise, dH^T tiles on tensor cores
     void *du = nullptr;            // [chunk][H][V][64] bf16 dU^T of the reverse walk (bwd, tensor cores)
-    float *tmat = nullptr;         // [chunks, H, 64, 64] fp32 T = (I + A)^-1 by column (bwd, tensor cores)
+    void *tmat = nullptr;          // [chunks, H, 64, 64] bf16 T = (I + A)^-1 by column (bwd, tensor cores)
     float *scratch = nullptr;      // per-CTA scratch (bwd, CUDA-core path)
     int32_t *counters = nullptr;   // small zeroed counters
 };
@@ -90,7 +90,8 @@ cudaError_t local_grads(const Plan &p, cudaStream_t s);
 cudaError_t encoder();
 cudaError_t make_map(CUtensorMap *m, const void *base, long long tokens, int H);
 // Chunk-major transposed tiles [chunk][H][128][64] bf16 (W^T, u^T, dU^T): one box per tile.
-cudaError_t make_map_tiles(CUtensorMap *m, const void *base, long long rows_total);
+cudaError_t make_map_tiles(CUtensorMap *m, const void *base, long long rows_total,
+                           int box_rows = 128);
 }  // namespace tc
 
 }  // namespace gdn

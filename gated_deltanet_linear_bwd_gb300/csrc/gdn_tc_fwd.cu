@@ -58,7 +58,8 @@ __device__ __forceinline__ float scan64(float x, float *wsum) {
 
 __global__ void __launch_bounds__(128, 2)
 tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-            Geo g, float *ws_gam, __nv_bfloat16 *ws_w, __nv_bfloat16 *ws_u, float *ws_t) {
+            Geo g, float *ws_gam, __nv_bfloat16 *ws_w, __nv_bfloat16 *ws_u,
+            __nv_bfloat16 *ws_t) {
     extern __shared__ uint8_t smem_raw[];
     PrepSmem &s = *reinterpret_cast<PrepSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -168,13 +169,23 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             }
             col[i] = acc;
         }
-        if (ws_t && r < L) {
-            // the backward keeps T: column r of this chunk's T, [chunk][h][col][row]
-            float4 *dst = reinterpret_cast<float4 *>(
+        if (ws_t && (!ch || has_b)) {
+            // the backward keeps T as bf16: row r of the tile [chunk][h][64][64] is
+            // column r of this chunk's T (zero past the chunk's end)
+            uint4 *dst = reinterpret_cast<uint4 *>(
                 ws_t + (((long long)(2 * blockIdx.x + ch) * H + h) * 64 + r) * 64);
 #pragma unroll
-            for (int i4 = 0; i4 < 16; ++i4)
-                dst[i4] = make_float4(col[4 * i4], col[4 * i4 + 1], col[4 * i4 + 2], col[4 * i4 + 3]);
+            for (int q = 0; q < 8; ++q) {
+                uint32_t w4[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int i = 8 * q + 2 * e;
+                    __nv_bfloat162 b2 = __floats2bfloat162_rn(r < L ? col[i] : 0.f,
+                                                              r < L ? col[i + 1] : 0.f);
+                    w4[e] = *reinterpret_cast<uint32_t *>(&b2);
+                }
+                dst[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
         }
         __syncthreads();  // every column done: A's space becomes bw / bu
         // MN-major B operands: row j = r holds T[.][j] scaled by beta_j e_j rk_j (W)
@@ -615,12 +626,13 @@ cudaError_t make_map(CUtensorMap *m, const void *base, long long tokens, int H) 
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// Chunk-major transposed tiles [chunk][H][128 features][64 rows] bf16 viewed as
-// 2-D (64 rows, rows_total features); one 64 x 128 box = one (chunk, head) tile.
-cudaError_t make_map_tiles(CUtensorMap *m, const void *base, long long rows_total) {
+// Chunk-major tiles of 64 bf16 columns ([chunk][H][box_rows][64], e.g. the
+// transposed [128 features][64 rows] tiles) viewed as 2-D (64, rows_total);
+// one 64 x box_rows box = one (chunk, head) tile.
+cudaError_t make_map_tiles(CUtensorMap *m, const void *base, long long rows_total, int box_rows) {
     const cuuint64_t dims[2] = {64, (cuuint64_t)rows_total};
     const cuuint64_t strides[1] = {64 * 2};
-    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
     const cuuint32_t es[2] = {1, 1};
     const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base),
                                 dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -659,7 +671,7 @@ static cudaError_t run_forward(const Plan &p, cudaStream_t s, bool states_only, 
     prof_before("tc_prep", s);
     tc_prep_kernel<<<dim3((p.max_chunks + 1) / 2, g.H), 128, prep_smem, s>>>(
         mk, mv, g, p.ws.gam, (__nv_bfloat16 *)p.ws.w, (__nv_bfloat16 *)p.ws.u,
-        (states_only || save) ? p.ws.tmat : nullptr);
+        (states_only || save) ? (__nv_bfloat16 *)p.ws.tmat : nullptr);
     prof_after(s);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 

@@ -151,6 +151,32 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Same for 8 consecutive columns.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float *v) {
+    uint32_t r[8];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Writes 8 bf16 values (columns 8 * chunk .. +7) of a 128-byte swizzled row.
+__device__ __forceinline__ void st_row8(uint8_t *tile, int row, int chunk, const float *x) {
+    uint32_t w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        __nv_bfloat162 b = __floats2bfloat162_rn(x[2 * j], x[2 * j + 1]);
+        w[j] = *reinterpret_cast<uint32_t *>(&b);
+    }
+    const uint32_t c = (uint32_t)chunk ^ (uint32_t)(row & 7);
+    *reinterpret_cast<uint4 *>(tile + row * 128 + c * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 // TMEM address of (lane base of this warp, column col).
 __device__ __forceinline__ uint32_t tmem_addr(uint32_t base, int warp, int col) {
     return base + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)col;

@@ -145,9 +145,9 @@ gdn_status gdn_chunk_fwd(const gdn_fwd_args *args, void *workspace, size_t works
 /* Bytes of the saved forward context for these arguments: 0 when the path
  * keeps none (then gdn_chunk_fwd ignores args->ctx and gdn_chunk_bwd
  * recomputes).  The tensor-core path (bf16, K = V = 128) keeps the
- * within-chunk cumsum of g, W, u (bf16), each chunk's (I + A)^-1 (fp32) and
- * each chunk's start state (bf16): about 2 K V / 64 + 2 (K + V) + 260 bytes
- * per token and head.
+ * within-chunk cumsum of g and, in bf16, W, u, each chunk's (I + A)^-1 and
+ * each chunk's start state: about 2 K V / 64 + 2 (K + V) + 132 bytes per
+ * token and head.
  * The contents are only meaningful to a gdn_chunk_bwd call with the same
  * inputs, sizes and flags; the library cannot check that. */
 size_t gdn_fwd_ctx_size(const gdn_fwd_args *args);
