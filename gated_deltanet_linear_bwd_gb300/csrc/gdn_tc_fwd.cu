@@ -281,7 +281,7 @@ struct WalkSmem {
     float gam[2][64];
     float fr[64], er[64];          // exp(gam_L - gam_r) (x rk_r), exp(gam_r) (x rq_r); 0 past L
     float rq[64], rk[64];
-    uint64_t tma_bar[2], mma_bar;
+    uint64_t tma_bar[2], bar_u, bar_po, bar_dh, bar_oa;
     uint32_t tmem_base;
 };
 
@@ -345,7 +345,10 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     if (tid == 0) {
         mbar_init(&s.tma_bar[0], 1);
         mbar_init(&s.tma_bar[1], 1);
-        mbar_init(&s.mma_bar, 1);
+        mbar_init(&s.bar_u, 1);
+        mbar_init(&s.bar_po, 1);
+        mbar_init(&s.bar_dh, 1);
+        mbar_init(&s.bar_oa, 1);
         fence_barrier_init();
     }
     if (warp == 0) {
@@ -394,16 +397,23 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         tma_load_2d(s.u[st], &tm_u, &s.tma_bar[st], 0, trow);
     };
 
-    int it = 0, mma_n = 0, tma_pending = 0;   // uniform bookkeeping for the bail-out path
+    // Per chunk four MMA groups, each committed once to its own barrier (so
+    // every barrier's parity is the chunk iteration's): U = W H first, then
+    // [Q; K] K^T and H^T Q^T; after the U epilogue the state update K^T diag(f)
+    // U runs while the threads mask P, and U^T P^T runs while they update H.
+    // `pend` marks the groups committed in this iteration and not yet waited.
+    int it = 0, tma_pending = 0, pend = 0;   // uniform bookkeeping for the bail-out path
     bool bailed = false;
     if (tid == 0 && cstart < c1) issue_tma(0, cstart);
     if (cstart < c1) tma_pending |= 1;
     for (int c = cstart; c < c1; ++c, ++it) {
         const int st = it & 1;
+        const uint32_t par = it & 1;
         const long long bos = sbos + (long long)c * kChunk;
         const int L = min(kChunk, slen - c * kChunk);
         const bool out_now = emit && c >= c0;
         float gnext = 0.f;                     // gam of the next chunk, stored at the end
+        pend = 0;
         if (c + 1 < c1) {
             if (tid == 0) {
                 fence_proxy_async();
@@ -445,109 +455,126 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 }
             (tid >= 64 ? s.rk : s.rq)[r] = rsqrtf(ss + 1e-6f);
         }
-        ++mma_n;
         if (tid == 0) {
             tc_fence_after();
             const uint32_t qk = smem_u32(s.qk[st]), wt = smem_u32(s.w[st]), hT = smem_u32(s.hT);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t half = kk >> 2, sub = (kk & 3) * 32;
-                const uint64_t ah = desc_sw128(hT + half * 2 * kTile + sub, 16, 1024);
+                const uint64_t ah = desc_sw128(hT + (kk >> 2) * 2 * kTile + (kk & 3) * 32, 16, 1024);
                 const uint64_t bw = desc_sw128(wt + kk * 2048, 2 * kTile, 1024);   // W^T, MN-major
                 mma_bf16(t_u, ah, bw, kIdescKM64, kk > 0);
-                if (out_now) {
+            }
+            mma_commit(&s.bar_u);
+            if (MODE == kWalkOut && out_now) {
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t half = kk >> 2, sub = (kk & 3) * 32;
+                    const uint64_t ah = desc_sw128(hT + half * 2 * kTile + sub, 16, 1024);
                     const uint64_t aq = desc_sw128(qk + half * 2 * kTile + sub, 16, 1024);
                     const uint64_t bk = desc_sw128(qk + half * 2 * kTile + kTile + sub, 16, 1024);
                     mma_bf16(t_p, aq, bk, kIdesc64, kk > 0);   // rows 0-63 of [Q; K] K^T
                     mma_bf16(t_oi, ah, aq, kIdesc64, kk > 0);  // H^T Q^T
                 }
             }
-            mma_commit(&s.mma_bar);
+            if (MODE == kWalkOut) mma_commit(&s.bar_po);
         }
+        pend = MODE == kWalkOut ? 3 : 1;
         if (g.l2norm) __syncthreads();        // rq, rk visible below
         if (tid < 64) {
             const float gl = s.gam[st][L - 1], gr = s.gam[st][tid];
             s.fr[tid] = tid < L ? __expf(gl - gr) * (g.l2norm ? s.rk[tid] : 1.f) : 0.f;
             s.er[tid] = tid < L ? __expf(gr) * (g.l2norm ? s.rq[tid] : 1.f) : 0.f;
         }
-        ok = mbar_wait(&s.mma_bar, (mma_n - 1) & 1, g.spin_limit, g.status);
+        ok = mbar_wait(&s.bar_u, par, g.spin_limit, g.status);
         if (__syncthreads_or(!ok)) { bailed = true; break; }
+        pend &= ~1;
         tc_fence_after();
-        {
-            // U = u - W H for chunk rows 32*hs .. +31 of this thread's state column
-            float acc[32], U[32];
-            tmem_ld32(tmem_addr(t_u, warp, 32 * hs), acc);
+        // U = u - W H, chunk rows 32*hs .. +31 of this thread's state column, in
+        // rolled groups of 8: U^T and U^T diag(f) rows v
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+            float x[8], uu[8];
+            tmem_ld8(tmem_addr(t_u, warp, 32 * hs + 8 * q), x);
+            const int chunk = 4 * hs + q;
+            uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+            if (!a_cols)
+                raw = *reinterpret_cast<const uint4 *>(s.u[st] + v * 128 + ((chunk ^ (v & 7)) << 4));
+            const __nv_bfloat16 *bv = reinterpret_cast<const __nv_bfloat16 *>(&raw);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                // 8 chunk rows of u^T row v: one 16-byte swizzled chunk
-                uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-                if (!a_cols)
-                    raw = *reinterpret_cast<const uint4 *>(
-                        s.u[st] + v * 128 + ((((32 * hs) >> 3) + q) ^ (v & 7)) * 16);
-                const __nv_bfloat16 *bv = reinterpret_cast<const __nv_bfloat16 *>(&raw);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int jj = 8 * q + e, r = 32 * hs + jj;
-                    U[jj] = r < L ? __bfloat162float(bv[e]) - acc[jj] : 0.f;
-                }
+            for (int e = 0; e < 8; ++e) {
+                const int r = 8 * chunk + e;
+                uu[e] = r < L ? __bfloat162float(bv[e]) - x[e] : 0.f;
             }
-            st_row32(s.uT, v, 32 * hs, U);
+            st_row8(s.uT, v, chunk, uu);
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) U[jj] *= s.fr[32 * hs + jj];
-            st_row32(s.uTs, v, 32 * hs, U);
-        }
-        if (out_now && v < 64) {
-            // P row r = v, columns 32*hs .. +31: masked, decayed Q K^T
-            const int r = v;
-            const float gr = s.gam[st][r];
-            const float sr = g.l2norm ? s.rq[r] : 1.f;
-            float qk[32];
-            tmem_ld32(tmem_addr(t_p, warp, 32 * hs), qk);
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-                const int c2 = 32 * hs + jj;
-                qk[jj] = (c2 <= r && r < L)
-                             ? qk[jj] * __expf(gr - s.gam[st][c2]) * sr * (g.l2norm ? s.rk[c2] : 1.f)
-                             : 0.f;
-            }
-            st_row32(s.p, r, 32 * hs, qk);
+            for (int e = 0; e < 8; ++e) uu[e] *= s.fr[8 * chunk + e];
+            st_row8(s.uTs, v, chunk, uu);
         }
         tc_fence_before();
         fence_proxy_async();
         __syncthreads();
-        ++mma_n;
         if (tid == 0) {
             tc_fence_after();
-            const uint32_t uT = smem_u32(s.uT), uTs = smem_u32(s.uTs), pp = smem_u32(s.p);
+            const uint32_t uTs = smem_u32(s.uTs);
             const uint32_t kt = smem_u32(s.qk[st]) + kTile;   // K rows of the stack
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
                 const uint64_t au = desc_sw128(uTs + kk * 32, 16, 1024);
                 const uint64_t bk = desc_sw128(kt + kk * 2048, 2 * kTile, 1024);
                 mma_bf16(t_dh, au, bk, kIdescDH, kk > 0);
-                if (out_now) {
+            }
+            mma_commit(&s.bar_dh);
+        }
+        pend |= 4;
+        if (MODE == kWalkOut) {
+            ok = mbar_wait(&s.bar_po, par, g.spin_limit, g.status);
+            if (__syncthreads_or(!ok)) { bailed = true; break; }
+        }
+        pend &= ~2;
+        if (MODE == kWalkOut && out_now) {
+            tc_fence_after();
+            if (v < 64) {
+                // P row r = v, columns 32*hs .. +31: masked, decayed Q K^T
+                const int r = v;
+                const float gr = s.gam[st][r];
+                const float sr = g.l2norm ? s.rq[r] : 1.f;
+#pragma unroll 1
+                for (int q = 0; q < 4; ++q) {
+                    float x[8];
+                    tmem_ld8(tmem_addr(t_p, warp, 32 * hs + 8 * q), x);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int c2 = 32 * hs + 8 * q + e;
+                        x[e] = (c2 <= r && r < L)
+                                   ? x[e] * __expf(gr - s.gam[st][c2]) * sr *
+                                         (g.l2norm ? s.rk[c2] : 1.f)
+                                   : 0.f;
+                    }
+                    st_row8(s.p, r, 4 * hs + q, x);
+                }
+            }
+            tc_fence_before();
+            fence_proxy_async();
+            __syncthreads();
+        }
+        if (MODE == kWalkOut && tid == 0) {
+            tc_fence_after();
+            if (out_now) {
+                const uint32_t uT = smem_u32(s.uT), pp = smem_u32(s.p);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
                     const uint64_t a2 = desc_sw128(uT + kk * 32, 16, 1024);
                     const uint64_t b2 = desc_sw128(pp + kk * 32, 16, 1024);
                     mma_bf16(t_oa, a2, b2, kIdesc64, kk > 0);
                 }
             }
-            mma_commit(&s.mma_bar);
+            mma_commit(&s.bar_oa);
         }
-        ok = mbar_wait(&s.mma_bar, (mma_n - 1) & 1, g.spin_limit, g.status);
+        if (MODE == kWalkOut) pend |= 8;
+        ok = mbar_wait(&s.bar_dh, par, g.spin_limit, g.status);
         if (__syncthreads_or(!ok)) { bailed = true; break; }
+        pend &= ~4;
         tc_fence_after();
-        if (out_now) {
-            __nv_bfloat16 *o = a.o + (bos * H + h) * (long long)kD + v;
-            float oi[32], oa[32];
-            tmem_ld32(tmem_addr(t_oi, warp, 32 * hs), oi);
-            tmem_ld32(tmem_addr(t_oa, warp, 32 * hs), oa);
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-                const int r = 32 * hs + jj;
-                if (r < L)
-                    o[(long long)r * H * kD] = __float2bfloat16_rn(g.scale * (oi[jj] * s.er[r] + oa[jj]));
-            }
-        }
         {
             const float el = __expf(s.gam[st][L - 1]);
 #pragma unroll
@@ -559,6 +586,35 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
         }
         st_row64(s.hT + hs * 2 * kTile, v, Hr);
+        if (MODE == kWalkOut) {
+            ok = mbar_wait(&s.bar_oa, par, g.spin_limit, g.status);
+            if (__syncthreads_or(!ok)) { bailed = true; break; }
+        }
+        pend &= ~8;
+        if (MODE == kWalkOut && out_now) {
+            // O rows: staged row-major [64 r][128 v] bf16 in the U^T diag(f) tile
+            // (its MMA is done), then written out in 16-byte pieces
+            tc_fence_after();
+            __nv_bfloat16 *ost = reinterpret_cast<__nv_bfloat16 *>(s.uTs);
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+                float oi[8], oa[8];
+                tmem_ld8(tmem_addr(t_oi, warp, 32 * hs + 8 * q), oi);
+                tmem_ld8(tmem_addr(t_oa, warp, 32 * hs + 8 * q), oa);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int r = 32 * hs + 8 * q + e;
+                    ost[r * kD + v] = __float2bfloat16_rn(g.scale * (oi[e] * s.er[r] + oa[e]));
+                }
+            }
+            __syncthreads();
+            __nv_bfloat16 *o = a.o + (bos * H + h) * (long long)kD;
+            for (int i = tid; i < L * 16; i += 256) {
+                const int r = i >> 4, q = i & 15;
+                *reinterpret_cast<uint4 *>(o + (long long)r * H * kD + 8 * q) =
+                    *reinterpret_cast<const uint4 *>(ost + r * kD + 8 * q);
+            }
+        }
         if (tid < 64) s.gam[st ^ 1][tid] = gnext;
         tc_fence_before();
         fence_proxy_async();
@@ -570,7 +626,9 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             for (int st = 0; st < 2; ++st)
                 if (tma_pending & (1 << st))
                     mbar_drain(&s.tma_bar[st], ((it + (st != (it & 1))) >> 1) & 1);
-            if (mma_n > 0) mbar_drain(&s.mma_bar, (mma_n - 1) & 1);
+            uint64_t *bars[4] = {&s.bar_u, &s.bar_po, &s.bar_dh, &s.bar_oa};
+            for (int i = 0; i < 4; ++i)
+                if (pend & (1 << i)) mbar_drain(bars[i], it & 1);
         }
     } else if (MODE == kWalkMap) {
         float *dst = a.maps + ((long long)(seq_seg_base(g, n) + j) * H + h) * kD * (2 * kD);
