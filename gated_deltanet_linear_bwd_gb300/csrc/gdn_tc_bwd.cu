@@ -199,7 +199,7 @@ tc_dwalk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         // group 1: P (rows of [Q; K] K^T) and X^T = dH^T K^T
         ++mma_n;
-        if (tid == 0) {
+        if (warp == 0) {
             tc_fence_after();
             const uint32_t qk = smem_u32(s.qk[st]), dhT = smem_u32(s.dhT);
 #pragma unroll
@@ -258,7 +258,7 @@ tc_dwalk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             fence_proxy_async();
             __syncthreads();
             ++mma_n;
-            if (tid == 0) {
+            if (warp == 0) {
                 tc_fence_after();
                 const uint32_t dO = smem_u32(s.dO[st]), pp = smem_u32(s.p);
 #pragma unroll
@@ -305,7 +305,7 @@ tc_dwalk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         __syncthreads();
         // group 3: Z^T = dO^T (diag(scale e^gam) Q) - dU^T W
         ++mma_n;
-        if (tid == 0) {
+        if (warp == 0) {
             tc_fence_after();
             const uint32_t dO = smem_u32(s.dO[st]), qs = smem_u32(s.qs), du = smem_u32(s.duT),
                            wt = smem_u32(s.w[st]);

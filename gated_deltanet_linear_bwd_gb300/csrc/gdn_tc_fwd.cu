@@ -109,7 +109,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     if (__syncthreads_or(!ok)) goto bail;
     tma_pending = false;
     ++mma_n;
-    if (tid == 0) {
+    if (warp == 0) {
         tc_fence_after();
         const uint32_t kb = smem_u32(s.k);
 #pragma unroll
@@ -207,7 +207,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     fence_proxy_async();
     __syncthreads();
     ++mma_n;
-    if (tid == 0) {
+    if (warp == 0) {
         tc_fence_after();
         const uint32_t kb = smem_u32(s.k), vb = smem_u32(s.v);
         const uint32_t bw = smem_u32(&s.A[0][0][0]), bu = bw + 2 * kTile;
@@ -455,7 +455,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 }
             (tid >= 64 ? s.rk : s.rq)[r] = rsqrtf(ss + 1e-6f);
         }
-        if (tid == 0) {
+        if (warp == 0) {
             tc_fence_after();
             const uint32_t qk = smem_u32(s.qk[st]), wt = smem_u32(s.w[st]), hT = smem_u32(s.hT);
 #pragma unroll
@@ -513,7 +513,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         tc_fence_before();
         fence_proxy_async();
         __syncthreads();
-        if (tid == 0) {
+        if (warp == 0) {
             tc_fence_after();
             const uint32_t uTs = smem_u32(s.uTs);
             const uint32_t kt = smem_u32(s.qk[st]) + kTile;   // K rows of the stack
@@ -557,7 +557,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             fence_proxy_async();
             __syncthreads();
         }
-        if (MODE == kWalkOut && tid == 0) {
+        if (MODE == kWalkOut && warp == 0) {
             tc_fence_after();
             if (out_now) {
                 const uint32_t uT = smem_u32(s.uT), pp = smem_u32(s.p);

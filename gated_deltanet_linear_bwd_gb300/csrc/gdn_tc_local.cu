@@ -220,7 +220,7 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
 
     // ---------------- wave 1: W H0, [Q; K] K^T, H0^T Q^T, H0 dU^T, H0 dO^T, dHL^T H0
     ++mma_n;
-    if (tid == 0) {
+    if (warp == 0) {
         tc_fence_after();
         const uint32_t qk = smem_u32(s.qk), h0 = smem_u32(s.h0T), w = smem_u32(s.w),
                        du = smem_u32(s.du), dO = smem_u32(s.dO), dl = smem_u32(s.dl);
@@ -283,7 +283,7 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
 
     // ---------------- wave 2: dO U^T, dHL U^T, T^T dW, T^T dU
     ++mma_n;
-    if (tid == 0) {
+    if (warp == 0) {
         tc_fence_after();
         const uint32_t dO = smem_u32(s.dO), uTa = smem_u32(uT), dwa = smem_u32(dwT),
                        dl = smem_u32(s.dl), du = smem_u32(s.du), tt = smem_u32(s.tt);
@@ -367,7 +367,7 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
 
     // ---------------- wave 2.5: dA = -(dYu u^T + dYw W^T), rows duplicated on lanes 64-127
     ++mma_n;
-    if (tid == 0) {
+    if (warp == 0) {
         tc_fence_after();
         const uint32_t yu = smem_u32(dyuT), yw = smem_u32(dywT), ua = smem_u32(s.ut),
                        wa = smem_u32(s.w);
@@ -424,7 +424,7 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
 
     // ---------------- wave 3: dS K, dS^T Q + (G + G^T) K
     ++mma_n;
-    if (tid == 0) {
+    if (warp == 0) {
         tc_fence_after();
         const uint32_t qk = smem_u32(s.qk), ds = smem_u32(s.ds), gs = smem_u32(s.gs);
 #pragma unroll
