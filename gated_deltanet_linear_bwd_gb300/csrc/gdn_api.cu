@@ -191,6 +191,10 @@ static size_t layout(Plan &p, bool bwd, char *base) {
         w.maps = (float *)take((size_t)p.max_segs * g.H * g.K * (g.K + g.V) * sizeof(float));
         w.seg_state = (float *)take((size_t)p.max_segs * g.H * g.K * g.V * sizeof(float));
     }
+    if (!bwd) {
+        // chunk start states (bf16 tiles) the tensor-core walk hands to the output kernel
+        w.hc = (float *)take((size_t)p.max_chunks * g.H * g.K * g.V * 2);
+    }
     if (bwd) {
         const size_t st = (size_t)p.max_chunks * g.H * g.K * g.V * sizeof(float);
         w.hc = (float *)take(st);

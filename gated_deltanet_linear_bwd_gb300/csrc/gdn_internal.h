@@ -82,6 +82,8 @@ bool supported(const Plan &p);
 cudaError_t forward(const Plan &p, cudaStream_t s, bool save);
 // Backward pieces: prep + walk storing chunk start states (p.ws.hc).
 cudaError_t recompute_states(const Plan &p, cudaStream_t s);
+// Chunk-parallel outputs O from the stored chunk start states (after the walk).
+cudaError_t output(const Plan &p, cudaStream_t s);
 // have_ctx: gam, W, u, T and the chunk start states are already in p.ws.
 cudaError_t backward(const Plan &p, cudaStream_t s, bool have_ctx);
 // Chunk-local gradients on tensor cores (no q/k L2 normalisation).

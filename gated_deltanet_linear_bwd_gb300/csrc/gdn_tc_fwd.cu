@@ -11,10 +11,9 @@
 //   [Ka; Kb] [Ka; Kb]^T                -> the two 64x64 K K^T blocks
 //   A = strict_lower(diag(beta) K K^T .* D),  T = (I + A)^-1 (CUDA cores)
 //   W^T = K^T (diag(beta e) T^T),  u^T = V^T (diag(beta) T^T)
-// Walk kernel (per sequence or segment, sequential over chunks):
-//   P   = [Q; K] K^T (rows of Q)        masked, decayed          (64 x 64)
+// Walk kernel (per sequence or segment, sequential over chunks; only the
+// state recurrence, every chunk's start state stored for the output kernel):
 //   U^T = u^T - H^T W^T                 (state product)
-//   O^T = H^T Q^T (inter) ; O^T += U^T P^T (intra)
 //   dH^T = (U^T diag(f)) K              H <- exp(gam_L) H + dH,  f = exp(gam_L - gam)
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -270,18 +269,18 @@ done:
 }
 
 // ------------------------------------------------------------------ walk
+// The walk carries only the state recurrence; outputs come from the
+// chunk-parallel output kernel, which reads the chunk start states it stores.
 struct WalkSmem {
-    uint8_t qk[2][4 * kTile];      // per stage: [dk half][rows 0-63 Q, 64-127 K][128 B]
+    uint8_t k[2][2 * kTile];       // per stage: K, [dk half][64 chunk rows][128 B]
     uint8_t w[2][2 * kTile];       // per stage: W^T, [128 rows k][64 chunk rows]
     uint8_t u[2][2 * kTile];       // per stage: u^T, [128 rows v][64 chunk rows]
     uint8_t hT[4 * kTile];         // [dk half][128 state rows][128 B]  (A operand)
-    uint8_t uT[2 * kTile];         // [128 state rows][64 chunk rows]   (A operand)
-    uint8_t uTs[2 * kTile];        // U^T diag(f)                        (A operand)
-    uint8_t p[kTile];              // [64 rows r][64 cols s]            (B operand)
+    uint8_t uTs[2 * kTile];        // U^T diag(f): [128 state rows][64 chunk rows] (A operand)
     float gam[2][64];
-    float fr[64], er[64];          // exp(gam_L - gam_r) (x rk_r), exp(gam_r) (x rq_r); 0 past L
-    float rq[64], rk[64];
-    uint64_t tma_bar[2], bar_u, bar_po, bar_dh, bar_oa;
+    float fr[64];                  // exp(gam_L - gam_r) (x 1/|k_r|); 0 past L
+    float rk[64];
+    uint64_t tma_bar[2], bar_u, bar_dh;
     uint32_t tmem_base;
 };
 
@@ -291,7 +290,6 @@ struct TcWalkArgs {
     const float *seg_start;   // [segs, H, K, V] (CP)
     const int32_t *warm;      // [N, H] (CP warmup)
     int warm_chunks;
-    __nv_bfloat16 *o;         // [tokens, H, V] (kWalkOut with output) nullable
     float *final_state;       // nullable
     __nv_bfloat16 *hc;        // chunk start states as bf16 H^T tiles [chunk][H][k half][v][64], nullable
     float *maps;              // [segs, H, K, K+V] (kWalkMap)
@@ -300,18 +298,18 @@ struct TcWalkArgs {
 
 enum { kWalkOut = 0, kWalkMap = 1 };
 
-constexpr uint32_t kIdesc64 = idesc_bf16(128, 64, false, false);      // K-major A and B
 constexpr uint32_t kIdescDH = idesc_bf16(128, 128, false, true);      // B MN-major
 constexpr uint32_t kIdescKM64 = idesc_bf16(128, 64, false, true);     // B MN-major, N = 64
 
 // 256 threads: thread t owns state row v = t % 128 (TMEM lane v) and the
 // column half hs = t / 128; warps w and w + 4 share a TMEM lane quarter and
-// split every epilogue's columns between them.
+// split every epilogue's columns between them.  Per chunk: U = u - W H (one
+// MMA group), U^T diag(f) into shared memory, K^T diag(f) U (second group),
+// H <- exp(gam_L) H + that.
 template <int MODE>
 __global__ void __launch_bounds__(256, 1)
-tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_u,
-               Geo g, TcWalkArgs a) {
+tc_walk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_w,
+               const __grid_constant__ CUtensorMap tm_u, Geo g, TcWalkArgs a) {
     extern __shared__ uint8_t smem_raw[];
     WalkSmem &s = *reinterpret_cast<WalkSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -327,7 +325,6 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
     if (MODE == kWalkMap && (j == nseg - 1 || (a.warm && a.warm[n * H + h]))) return;
     const bool a_cols = MODE == kWalkMap && cb == 0;   // A columns: start I, u = 0
-    const bool emit = MODE == kWalkOut && a.o != nullptr;
     const bool states = MODE == kWalkOut && a.hc != nullptr;
     const int nc = seq_nchunks(g, n);
     const int c0 = min(nc, j * g.seg_chunks), c1 = min(nc, (j + 1) * g.seg_chunks);
@@ -346,13 +343,11 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         mbar_init(&s.tma_bar[0], 1);
         mbar_init(&s.tma_bar[1], 1);
         mbar_init(&s.bar_u, 1);
-        mbar_init(&s.bar_po, 1);
         mbar_init(&s.bar_dh, 1);
-        mbar_init(&s.bar_oa, 1);
         fence_barrier_init();
     }
     if (warp == 0) {
-        tmem_alloc(&s.tmem_base, 512);
+        tmem_alloc(&s.tmem_base, 256);
         tmem_relinquish();
         tc_fence_before();
     }
@@ -381,27 +376,20 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = s.tmem_base;
-    const uint32_t t_p = tbase, t_u = tbase + 64, t_oi = tbase + 128, t_oa = tbase + 192,
-                   t_dh = tbase + 256;
+    const uint32_t t_u = tbase, t_dh = tbase + 128;
 
     auto issue_tma = [&](int st, int c) {
         const int tok0 = (int)(sbos + (long long)c * kChunk);
-        mbar_arrive_expect_tx(&s.tma_bar[st], 8 * kTile);   // 2 halves x (q, k, w, u)
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            tma_load_3d(s.qk[st] + half * 2 * kTile, &tm_q, &s.tma_bar[st], half * 64, h, tok0);
-            tma_load_3d(s.qk[st] + half * 2 * kTile + kTile, &tm_k, &s.tma_bar[st], half * 64, h, tok0);
-        }
+        mbar_arrive_expect_tx(&s.tma_bar[st], 6 * kTile);   // K (2 halves), W^T, u^T
+        tma_load_3d(s.k[st], &tm_k, &s.tma_bar[st], 0, h, tok0);
+        tma_load_3d(s.k[st] + kTile, &tm_k, &s.tma_bar[st], 64, h, tok0);
         const int trow = (int)(((long long)(cbase + c) * H + h) * kD);
         tma_load_2d(s.w[st], &tm_w, &s.tma_bar[st], 0, trow);
         tma_load_2d(s.u[st], &tm_u, &s.tma_bar[st], 0, trow);
     };
 
-    // Per chunk four MMA groups, each committed once to its own barrier (so
-    // every barrier's parity is the chunk iteration's): U = W H first, then
-    // [Q; K] K^T and H^T Q^T; after the U epilogue the state update K^T diag(f)
-    // U runs while the threads mask P, and U^T P^T runs while they update H.
-    // `pend` marks the groups committed in this iteration and not yet waited.
+    // one commit per barrier per chunk: every barrier's parity is the chunk
+    // iteration's; `pend` marks groups committed in this iteration, not yet waited
     int it = 0, tma_pending = 0, pend = 0;   // uniform bookkeeping for the bail-out path
     bool bailed = false;
     if (tid == 0 && cstart < c1) issue_tma(0, cstart);
@@ -411,7 +399,6 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const uint32_t par = it & 1;
         const long long bos = sbos + (long long)c * kChunk;
         const int L = min(kChunk, slen - c * kChunk);
-        const bool out_now = emit && c >= c0;
         float gnext = 0.f;                     // gam of the next chunk, stored at the end
         pend = 0;
         if (c + 1 < c1) {
@@ -441,23 +428,9 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         bool ok = mbar_wait(&s.tma_bar[st], (it >> 1) & 1, g.spin_limit, g.status);
         if (__syncthreads_or(!ok)) { bailed = true; break; }
         tma_pending &= ~(1 << st);
-        if (g.l2norm && tid < 128) {
-            // |q_r| from the Q rows (threads 0-63), |k_r| from the K rows (64-127)
-            const int r = tid & 63;
-            const uint8_t *base = s.qk[st] + (tid >= 64 ? kTile : 0);
-            float ss = 0.f;
-#pragma unroll
-            for (int half = 0; half < 2; ++half)
-#pragma unroll 8
-                for (int col = 0; col < 64; ++col) {
-                    const float x = ld_bf16(base + half * 2 * kTile, r, col);
-                    ss += x * x;
-                }
-            (tid >= 64 ? s.rk : s.rq)[r] = rsqrtf(ss + 1e-6f);
-        }
         if (warp == 0) {
             tc_fence_after();
-            const uint32_t qk = smem_u32(s.qk[st]), wt = smem_u32(s.w[st]), hT = smem_u32(s.hT);
+            const uint32_t wt = smem_u32(s.w[st]), hT = smem_u32(s.hT);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 const uint64_t ah = desc_sw128(hT + (kk >> 2) * 2 * kTile + (kk & 3) * 32, 16, 1024);
@@ -465,32 +438,31 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 mma_bf16(t_u, ah, bw, kIdescKM64, kk > 0);
             }
             mma_commit(&s.bar_u);
-            if (MODE == kWalkOut && out_now) {
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t half = kk >> 2, sub = (kk & 3) * 32;
-                    const uint64_t ah = desc_sw128(hT + half * 2 * kTile + sub, 16, 1024);
-                    const uint64_t aq = desc_sw128(qk + half * 2 * kTile + sub, 16, 1024);
-                    const uint64_t bk = desc_sw128(qk + half * 2 * kTile + kTile + sub, 16, 1024);
-                    mma_bf16(t_p, aq, bk, kIdesc64, kk > 0);   // rows 0-63 of [Q; K] K^T
-                    mma_bf16(t_oi, ah, aq, kIdesc64, kk > 0);  // H^T Q^T
-                }
-            }
-            if (MODE == kWalkOut) mma_commit(&s.bar_po);
         }
-        pend = MODE == kWalkOut ? 3 : 1;
-        if (g.l2norm) __syncthreads();        // rq, rk visible below
+        pend = 1;
+        if (g.l2norm && tid >= 64 && tid < 128) {
+            // 1 / |k_r| from the K rows
+            const int r = tid - 64;
+            float ss = 0.f;
+#pragma unroll
+            for (int half = 0; half < 2; ++half)
+#pragma unroll 8
+                for (int col = 0; col < 64; ++col) {
+                    const float x = ld_bf16(s.k[st] + half * kTile, r, col);
+                    ss += x * x;
+                }
+            s.rk[r] = rsqrtf(ss + 1e-6f);
+        }
+        if (g.l2norm) __syncthreads();
         if (tid < 64) {
             const float gl = s.gam[st][L - 1], gr = s.gam[st][tid];
             s.fr[tid] = tid < L ? __expf(gl - gr) * (g.l2norm ? s.rk[tid] : 1.f) : 0.f;
-            s.er[tid] = tid < L ? __expf(gr) * (g.l2norm ? s.rq[tid] : 1.f) : 0.f;
         }
         ok = mbar_wait(&s.bar_u, par, g.spin_limit, g.status);
         if (__syncthreads_or(!ok)) { bailed = true; break; }
-        pend &= ~1;
+        pend = 0;
         tc_fence_after();
-        // U = u - W H, chunk rows 32*hs .. +31 of this thread's state column, in
-        // rolled groups of 8: U^T and U^T diag(f) rows v
+        // U^T diag(f) rows v, chunk rows 32*hs .. +31 in rolled groups of 8
 #pragma unroll 1
         for (int q = 0; q < 4; ++q) {
             float x[8], uu[8];
@@ -503,11 +475,8 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const int r = 8 * chunk + e;
-                uu[e] = r < L ? __bfloat162float(bv[e]) - x[e] : 0.f;
+                uu[e] = r < L ? (__bfloat162float(bv[e]) - x[e]) * s.fr[r] : 0.f;
             }
-            st_row8(s.uT, v, chunk, uu);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) uu[e] *= s.fr[8 * chunk + e];
             st_row8(s.uTs, v, chunk, uu);
         }
         tc_fence_before();
@@ -515,65 +484,19 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         __syncthreads();
         if (warp == 0) {
             tc_fence_after();
-            const uint32_t uTs = smem_u32(s.uTs);
-            const uint32_t kt = smem_u32(s.qk[st]) + kTile;   // K rows of the stack
+            const uint32_t uTs = smem_u32(s.uTs), kt = smem_u32(s.k[st]);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
                 const uint64_t au = desc_sw128(uTs + kk * 32, 16, 1024);
-                const uint64_t bk = desc_sw128(kt + kk * 2048, 2 * kTile, 1024);
+                const uint64_t bk = desc_sw128(kt + kk * 2048, kTile, 1024);   // K, MN-major
                 mma_bf16(t_dh, au, bk, kIdescDH, kk > 0);
             }
             mma_commit(&s.bar_dh);
         }
-        pend |= 4;
-        if (MODE == kWalkOut) {
-            ok = mbar_wait(&s.bar_po, par, g.spin_limit, g.status);
-            if (__syncthreads_or(!ok)) { bailed = true; break; }
-        }
-        pend &= ~2;
-        if (MODE == kWalkOut && out_now) {
-            tc_fence_after();
-            if (v < 64) {
-                // P row r = v, columns 32*hs .. +31: masked, decayed Q K^T
-                const int r = v;
-                const float gr = s.gam[st][r];
-                const float sr = g.l2norm ? s.rq[r] : 1.f;
-#pragma unroll 1
-                for (int q = 0; q < 4; ++q) {
-                    float x[8];
-                    tmem_ld8(tmem_addr(t_p, warp, 32 * hs + 8 * q), x);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int c2 = 32 * hs + 8 * q + e;
-                        x[e] = (c2 <= r && r < L)
-                                   ? x[e] * __expf(gr - s.gam[st][c2]) * sr *
-                                         (g.l2norm ? s.rk[c2] : 1.f)
-                                   : 0.f;
-                    }
-                    st_row8(s.p, r, 4 * hs + q, x);
-                }
-            }
-            tc_fence_before();
-            fence_proxy_async();
-            __syncthreads();
-        }
-        if (MODE == kWalkOut && warp == 0) {
-            tc_fence_after();
-            if (out_now) {
-                const uint32_t uT = smem_u32(s.uT), pp = smem_u32(s.p);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t a2 = desc_sw128(uT + kk * 32, 16, 1024);
-                    const uint64_t b2 = desc_sw128(pp + kk * 32, 16, 1024);
-                    mma_bf16(t_oa, a2, b2, kIdesc64, kk > 0);
-                }
-            }
-            mma_commit(&s.bar_oa);
-        }
-        if (MODE == kWalkOut) pend |= 8;
+        pend = 2;
         ok = mbar_wait(&s.bar_dh, par, g.spin_limit, g.status);
         if (__syncthreads_or(!ok)) { bailed = true; break; }
-        pend &= ~4;
+        pend = 0;
         tc_fence_after();
         {
             const float el = __expf(s.gam[st][L - 1]);
@@ -586,35 +509,6 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
         }
         st_row64(s.hT + hs * 2 * kTile, v, Hr);
-        if (MODE == kWalkOut) {
-            ok = mbar_wait(&s.bar_oa, par, g.spin_limit, g.status);
-            if (__syncthreads_or(!ok)) { bailed = true; break; }
-        }
-        pend &= ~8;
-        if (MODE == kWalkOut && out_now) {
-            // O rows: staged row-major [64 r][128 v] bf16 in the U^T diag(f) tile
-            // (its MMA is done), then written out in 16-byte pieces
-            tc_fence_after();
-            __nv_bfloat16 *ost = reinterpret_cast<__nv_bfloat16 *>(s.uTs);
-#pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
-                float oi[8], oa[8];
-                tmem_ld8(tmem_addr(t_oi, warp, 32 * hs + 8 * q), oi);
-                tmem_ld8(tmem_addr(t_oa, warp, 32 * hs + 8 * q), oa);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int r = 32 * hs + 8 * q + e;
-                    ost[r * kD + v] = __float2bfloat16_rn(g.scale * (oi[e] * s.er[r] + oa[e]));
-                }
-            }
-            __syncthreads();
-            __nv_bfloat16 *o = a.o + (bos * H + h) * (long long)kD;
-            for (int i = tid; i < L * 16; i += 256) {
-                const int r = i >> 4, q = i & 15;
-                *reinterpret_cast<uint4 *>(o + (long long)r * H * kD + 8 * q) =
-                    *reinterpret_cast<const uint4 *>(ost + r * kD + 8 * q);
-            }
-        }
         if (tid < 64) s.gam[st ^ 1][tid] = gnext;
         tc_fence_before();
         fence_proxy_async();
@@ -626,9 +520,8 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             for (int st = 0; st < 2; ++st)
                 if (tma_pending & (1 << st))
                     mbar_drain(&s.tma_bar[st], ((it + (st != (it & 1))) >> 1) & 1);
-            uint64_t *bars[4] = {&s.bar_u, &s.bar_po, &s.bar_dh, &s.bar_oa};
-            for (int i = 0; i < 4; ++i)
-                if (pend & (1 << i)) mbar_drain(bars[i], it & 1);
+            if (pend & 1) mbar_drain(&s.bar_u, it & 1);
+            if (pend & 2) mbar_drain(&s.bar_dh, it & 1);
         }
     } else if (MODE == kWalkMap) {
         float *dst = a.maps + ((long long)(seq_seg_base(g, n) + j) * H + h) * kD * (2 * kD);
@@ -641,7 +534,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tbase, 512);
+    if (warp == 0) tmem_dealloc(tbase, 256);
 }
 
 // ------------------------------------------------------------------ host side
@@ -713,8 +606,7 @@ static cudaError_t run_forward(const Plan &p, cudaStream_t s, bool states_only, 
     if (e != cudaSuccess) return e;
     const Geo &g = p.g;
     const long long tokens = (long long)g.B * g.T;
-    CUtensorMap mq, mk, mv, mw, mu;
-    if ((e = make_map(&mq, g.q, tokens, g.H)) != cudaSuccess) return e;
+    CUtensorMap mk, mv, mw, mu;
     if ((e = make_map(&mk, g.k, tokens, g.H)) != cudaSuccess) return e;
     if ((e = make_map(&mv, g.v, tokens, g.H)) != cudaSuccess) return e;
     const long long tile_rows = (long long)p.max_chunks * g.H * kD;
@@ -733,13 +625,14 @@ static cudaError_t run_forward(const Plan &p, cudaStream_t s, bool states_only, 
     prof_after(s);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
+    // the walk stores every chunk's start state: the output kernel and the
+    // backward read them
     TcWalkArgs a{};
     a.ws_gam = p.ws.gam;
     a.h0 = p.h0;
-    a.o = states_only ? nullptr : (__nv_bfloat16 *)p.o;
     a.final_state = states_only ? nullptr : p.final_state;
-    a.hc = (states_only || save) ? (__nv_bfloat16 *)p.ws.hc : nullptr;
-    const char *out_name = states_only ? "tc_walk_states" : "tc_walk_out";
+    a.hc = (__nv_bfloat16 *)p.ws.hc;
+    const char *out_name = states_only ? "tc_walk_states" : "tc_walk";
     if (p.cp) {
         a.cp = 1;
         a.maps = p.ws.maps;
@@ -750,19 +643,20 @@ static cudaError_t run_forward(const Plan &p, cudaStream_t s, bool states_only, 
             a.warm_chunks = p.warm_chunks;
         }
         prof_before("tc_walk_map", s);
-        tc_walk_kernel<kWalkMap><<<dim3(p.max_segs, g.H, 2), 256, walk_smem, s>>>(mq, mk, mw, mu, g, a);
+        tc_walk_kernel<kWalkMap><<<dim3(p.max_segs, g.H, 2), 256, walk_smem, s>>>(mk, mw, mu, g, a);
         prof_after(s);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if ((e = simt::cp_scan(p, a.warm, s)) != cudaSuccess) return e;
         prof_before(out_name, s);
-        tc_walk_kernel<kWalkOut><<<dim3(p.max_segs, g.H, 1), 256, walk_smem, s>>>(mq, mk, mw, mu, g, a);
+        tc_walk_kernel<kWalkOut><<<dim3(p.max_segs, g.H, 1), 256, walk_smem, s>>>(mk, mw, mu, g, a);
         prof_after(s);
     } else {
         prof_before(out_name, s);
-        tc_walk_kernel<kWalkOut><<<dim3(g.N, g.H, 1), 256, walk_smem, s>>>(mq, mk, mw, mu, g, a);
+        tc_walk_kernel<kWalkOut><<<dim3(g.N, g.H, 1), 256, walk_smem, s>>>(mk, mw, mu, g, a);
         prof_after(s);
     }
-    return cudaGetLastError();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    return states_only ? cudaSuccess : output(p, s);
 }
 
 cudaError_t forward(const Plan &p, cudaStream_t s, bool save) {

@@ -1,0 +1,239 @@
+// gdn_tc_out.cu -- tensor-core output kernel of the forward for bf16 q/k/v
+// with K = V = 128: chunk-parallel, one (chunk, head) per CTA, two CTAs per
+// SM.  From the chunk start state H0 that the walk stored (bf16 H0^T tile)
+// and the prep kernel's W^T and u^T tiles:
+//   U^T = u^T - H0^T W^T                           (pseudo-values of the chunk)
+//   P   = scale (Q K^T .* lower_incl .* D)          D_rs = exp(gam_r - gam_s)
+//   O^T = scale H0^T Q^T diag(e) + U^T P^T          e = exp(gam)
+// with q, k replaced by their L2-normalised rows when the caller asks for it
+// (the norms scale the rows of P and the columns of H0^T Q^T).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "gdn_common.cuh"
+#include "gdn_internal.h"
+#include "tc_ptx.cuh"
+
+namespace gdn {
+namespace tc {
+
+namespace {
+constexpr int kD = 128;
+constexpr int kTile = 8192;
+constexpr uint32_t kKK64 = idesc_bf16(128, 64, false, false);   // K-major A and B
+constexpr uint32_t kKM64 = idesc_bf16(128, 64, false, true);    // B MN-major
+
+struct OutSmem {
+    uint8_t qk[4 * kTile];     // [dk half][Q rows 0-63, K rows 64-127][128 B]; then O rows
+    uint8_t w[2 * kTile];      // W^T: [128 rows k][64 chunk rows]
+    uint8_t u[2 * kTile];      // u^T: [128 rows v][64 chunk rows]
+    uint8_t h0T[4 * kTile];    // H0^T: [k half][128 rows v][64]; after wave 1: U^T
+    uint8_t p[kTile];          // P rows r
+    float gam[64], er[64], rq[64], rk[64];
+    uint64_t tma_bar, mma_bar;
+    uint32_t tmem_base;
+};
+
+template <typename F>
+cudaError_t set_smem(F kernel, size_t bytes) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+}  // namespace
+
+// 256 threads: thread t reads TMEM lane v = t % 128 and chunk-row half
+// hs = t / 128 (columns 32 hs .. +31); rows r of P sit on lanes 0-63.
+__global__ void __launch_bounds__(256, 2)
+tc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+              const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_u,
+              const __grid_constant__ CUtensorMap tm_hc, Geo g, const float *ws_gam,
+              __nv_bfloat16 *o) {
+    extern __shared__ uint8_t smem_raw[];
+    OutSmem &s = *reinterpret_cast<OutSmem *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, h = blockIdx.y, H = g.H, ci = blockIdx.x;
+    const int v = tid & 127, hs = tid >> 7, c0 = 32 * hs, cq = c0 >> 3;
+    ChunkRef cr;
+    if (!chunk_ref(g, ci, cr)) return;
+    const int L = cr.len;
+    const long long bos = cr.bos;
+    uint8_t *uT = s.h0T;                       // after wave 1
+
+    if (tid == 0) {
+        mbar_init(&s.tma_bar, 1);
+        mbar_init(&s.mma_bar, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&s.tmem_base, 256);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = s.tmem_base;
+    const uint32_t t_u = tb, t_p = tb + 64, t_oi = tb + 128, t_oa = tb + 192;
+    if (tid == 0) {
+        const int tok0 = (int)bos;
+        const int trow = (int)(((long long)ci * H + h) * kD);
+        mbar_arrive_expect_tx(&s.tma_bar, 12 * kTile);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            tma_load_3d(s.qk + half * 2 * kTile, &tm_q, &s.tma_bar, half * 64, h, tok0);
+            tma_load_3d(s.qk + half * 2 * kTile + kTile, &tm_k, &s.tma_bar, half * 64, h, tok0);
+            tma_load_2d(s.h0T + half * 2 * kTile, &tm_hc, &s.tma_bar, 0, 2 * trow + half * kD);
+        }
+        tma_load_2d(s.w, &tm_w, &s.tma_bar, 0, trow);
+        tma_load_2d(s.u, &tm_u, &s.tma_bar, 0, trow);
+    }
+    if (tid < 64) s.gam[tid] = tid < L ? ws_gam[(bos + tid) * H + h] : 0.f;
+    int mma_n = 0;
+    bool tma_pending = true;
+    bool ok = mbar_wait(&s.tma_bar, 0, g.spin_limit, g.status);
+    if (__syncthreads_or(!ok)) goto bail;
+    tma_pending = false;
+
+    ++mma_n;
+    if (warp == 0) {
+        tc_fence_after();
+        const uint32_t qk = smem_u32(s.qk), wt = smem_u32(s.w), h0 = smem_u32(s.h0T);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t half = kk >> 2, sub = (kk & 3) * 32;
+            const uint64_t ah = desc_sw128(h0 + half * 2 * kTile + sub, 16, 1024);
+            const uint64_t aq = desc_sw128(qk + half * 2 * kTile + sub, 16, 1024);
+            const uint64_t bk = desc_sw128(qk + half * 2 * kTile + kTile + sub, 16, 1024);
+            mma_bf16(t_u, ah, desc_sw128(wt + kk * 2048, 2 * kTile, 1024), kKM64, kk > 0);
+            mma_bf16(t_p, aq, bk, kKK64, kk > 0);       // rows 0-63: Q K^T
+            mma_bf16(t_oi, ah, aq, kKK64, kk > 0);      // H0^T Q^T
+        }
+        mma_commit(&s.mma_bar);
+    }
+    if (g.l2norm && tid < 128) {
+        // 1 / |q_r| from the Q rows (threads 0-63), 1 / |k_r| from the K rows (64-127)
+        const int r = tid & 63;
+        const uint8_t *base = s.qk + (tid >= 64 ? kTile : 0);
+        float ss = 0.f;
+#pragma unroll
+        for (int half = 0; half < 2; ++half)
+#pragma unroll 8
+            for (int col = 0; col < 64; ++col) {
+                const float x = ld_bf16(base + half * 2 * kTile, r, col);
+                ss += x * x;
+            }
+        (tid >= 64 ? s.rk : s.rq)[r] = rsqrtf(ss + 1e-6f);
+    }
+    if (g.l2norm) __syncthreads();
+    if (tid < 64) s.er[tid] = tid < L ? __expf(s.gam[tid]) * (g.l2norm ? s.rq[tid] : 1.f) : 0.f;
+    ok = mbar_wait(&s.mma_bar, 0, g.spin_limit, g.status);
+    if (__syncthreads_or(!ok)) goto bail;
+    tc_fence_after();
+    {
+        // U^T rows v into the dead H0^T tile; P rows r = v < 64
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+            float x[8];
+            tmem_ld8(tmem_addr(t_u, warp, c0 + 8 * q), x);
+            const uint4 raw = *reinterpret_cast<const uint4 *>(
+                s.u + v * 128 + (((cq + q) ^ (v & 7)) << 4));
+            const __nv_bfloat16 *bv = reinterpret_cast<const __nv_bfloat16 *>(&raw);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int r = c0 + 8 * q + e;
+                x[e] = r < L ? __bfloat162float(bv[e]) - x[e] : 0.f;
+            }
+            st_row8(uT, v, cq + q, x);
+        }
+        if (v < 64) {
+            const int r = v;
+            const float gr = s.gam[r];
+            const float sr = g.l2norm ? s.rq[r] : 1.f;
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+                float x[8];
+                tmem_ld8(tmem_addr(t_p, warp, c0 + 8 * q), x);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int c = c0 + 8 * q + e;
+                    x[e] = (c <= r && r < L)
+                               ? x[e] * __expf(gr - s.gam[c]) * sr * (g.l2norm ? s.rk[c] : 1.f)
+                               : 0.f;
+                }
+                st_row8(s.p, r, cq + q, x);
+            }
+        }
+    }
+    tc_fence_before();
+    fence_proxy_async();
+    __syncthreads();
+    ++mma_n;
+    if (warp == 0) {
+        tc_fence_after();
+        const uint32_t ua = smem_u32(uT), pp = smem_u32(s.p);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            mma_bf16(t_oa, desc_sw128(ua + kk * 32, 16, 1024), desc_sw128(pp + kk * 32, 16, 1024),
+                     kKK64, kk > 0);
+        mma_commit(&s.mma_bar);
+    }
+    ok = mbar_wait(&s.mma_bar, 1, g.spin_limit, g.status);
+    if (__syncthreads_or(!ok)) goto bail;
+    tc_fence_after();
+    {
+        // O rows staged row-major [64 r][128 v] bf16 in the dead Q/K tiles, then
+        // written out in 16-byte pieces
+        __nv_bfloat16 *ost = reinterpret_cast<__nv_bfloat16 *>(s.qk);
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+            float oi[8], oa[8];
+            tmem_ld8(tmem_addr(t_oi, warp, c0 + 8 * q), oi);
+            tmem_ld8(tmem_addr(t_oa, warp, c0 + 8 * q), oa);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int r = c0 + 8 * q + e;
+                ost[r * kD + v] = __float2bfloat16_rn(g.scale * (oi[e] * s.er[r] + oa[e]));
+            }
+        }
+        __syncthreads();
+        __nv_bfloat16 *dst = o + (bos * H + h) * (long long)kD;
+        for (int i = tid; i < L * 16; i += 256) {
+            const int r = i >> 4, q = i & 15;
+            *reinterpret_cast<uint4 *>(dst + (long long)r * H * kD + 8 * q) =
+                *reinterpret_cast<const uint4 *>(ost + r * kD + 8 * q);
+        }
+    }
+    goto done;
+bail:
+    if (tid == 0) {
+        if (tma_pending) mbar_drain(&s.tma_bar, 0);
+        if (mma_n > 0) mbar_drain(&s.mma_bar, (mma_n - 1) & 1);
+    }
+done:
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tb, 256);
+}
+
+cudaError_t output(const Plan &p, cudaStream_t s) {
+    cudaError_t e = encoder();
+    if (e != cudaSuccess) return e;
+    const Geo &g = p.g;
+    const long long tokens = (long long)g.B * g.T;
+    const long long tile_rows = (long long)p.max_chunks * g.H * kD;
+    CUtensorMap mq, mk, mw, mu, mhc;
+    if ((e = make_map(&mq, g.q, tokens, g.H)) != cudaSuccess) return e;
+    if ((e = make_map(&mk, g.k, tokens, g.H)) != cudaSuccess) return e;
+    if ((e = make_map_tiles(&mw, p.ws.w, tile_rows)) != cudaSuccess) return e;
+    if ((e = make_map_tiles(&mu, p.ws.u, tile_rows)) != cudaSuccess) return e;
+    if ((e = make_map_tiles(&mhc, p.ws.hc, 2 * tile_rows)) != cudaSuccess) return e;
+    const size_t smem = sizeof(OutSmem) + 1024;
+    if ((e = set_smem(tc_out_kernel, smem)) != cudaSuccess) return e;
+    prof_before("tc_out", s);
+    tc_out_kernel<<<dim3(p.max_chunks, g.H), 256, smem, s>>>(mq, mk, mw, mu, mhc, g, p.ws.gam,
+                                                             (__nv_bfloat16 *)p.o);
+    prof_after(s);
+    return cudaGetLastError();
+}
+
+}  // namespace tc
+}  // namespace gdn
