@@ -200,6 +200,8 @@ static size_t layout(Plan &p, bool bwd, char *base) {
         w.hc = (float *)take(st);
         w.dhc = (float *)take(st);
         w.du = take(tiles * g.V);
+        w.qs = take(tiles * g.K);
+        w.yt = take(tiles * g.V);
         w.tmat = take((size_t)p.max_chunks * g.H * 64 * 64 * 2);
         w.scratch = (float *)take((size_t)p.scratch_ctas *
                                   simt::scratch_floats_per_cta(g.K, g.V) * sizeof(float));

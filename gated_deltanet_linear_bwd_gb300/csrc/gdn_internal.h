@@ -26,6 +26,8 @@ struct Ws {
                                    // cores) or bf16 H^T tiles [chunk][H][k half][v][64] (tensor cores)
     float *dhc = nullptr;          // chunk end gradients (bwd): likewise, dH^T tiles on tensor cores
     void *du = nullptr;            // [chunk][H][V][64] bf16 dU^T of the reverse walk (bwd, tensor cores)
+    void *qs = nullptr;            // [chunk][H][dk half][64][64] bf16 diag(scale e^gam) Q (bwd, tensor cores)
+    void *yt = nullptr;            // [chunk][H][V][64] bf16 (dO^T P) tiles (bwd, tensor cores)
     void *tmat = nullptr;          // [chunks, H, 64, 64] bf16 T = (I + A)^-1 by column (bwd, tensor cores)
     float *scratch = nullptr;      // per-CTA scratch (bwd, CUDA-core path)
     int32_t *counters = nullptr;   // small zeroed counters

@@ -5,10 +5,13 @@
 // chunks last to first.  With dH the gradient at a chunk's end, held as
 // dH^T (V rows x K columns, one row per thread, fp32 registers):
 //   X^T  = dH^T K^T                      (K dH)^T
-//   Y^T  = dO^T P,  P = scale (Q K^T .* lower_incl .* D)
 //   dU^T = Y^T + X^T diag(f),            f = exp(gam_L - gam)
-//   dH^T <- exp(gam_L) dH^T + dO^T (diag(scale e^gam) Q) - dU^T W
-// The segment map of this walk ([A' | B'], A' the transpose of the forward
+//   dH^T <- exp(gam_L) dH^T + dO^T Qs - dU^T W
+// where the parts that do not depend on dH come from the chunk-parallel
+// intra kernel run first:
+//   P    = scale (Q K^T .* lower_incl .* D),  Y^T = dO^T P
+//   Qs   = diag(scale e^gam) Q
+// The segment map of the walk ([A' | B'], A' the transpose of the forward
 // map) is walked the same way with dO = 0 on its A' columns.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -33,18 +36,198 @@ constexpr uint32_t kIdMM64 = idesc_bf16(128, 64, true, true);     // MN-major A 
 constexpr uint32_t kIdMM128 = idesc_bf16(128, 128, true, true);   // MN-major A and B, N = 128
 constexpr uint32_t kIdKK128Neg = idesc_neg_a(idesc_bf16(128, 128, false, false));
 
+template <typename F>
+cudaError_t set_smem(F kernel, size_t bytes) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+// ------------------------------------------------------------------ intra kernel
+struct IntraSmem {
+    uint8_t qk[4 * kTile];         // [dk half][Q rows 0-63, K rows 64-127][128 B]
+    uint8_t dO[2 * kTile];         // [dv half][64 rows][128 B]
+    uint8_t qs[2 * kTile];         // Qs, [dk half][64 rows][128 B]
+    uint8_t yT[2 * kTile];         // Y^T, [128 rows v][64 chunk rows]
+    uint8_t p[kTile];              // P rows r (scale included)
+    float gam[64], rq[64], rk[64];
+    uint64_t tma_bar, mma_bar;
+    uint32_t tmem_base;
+};
+}  // namespace
+
+// Per (chunk, head), 256 threads: P on lanes 0-63 (row r = v), Qs rows by
+// threads 128-191, then Y^T = dO^T P feature-major (thread: row v, column
+// half hs); Qs and Y^T leave by TMA from shared memory.
+__global__ void __launch_bounds__(256, 2)
+tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_qs,
+                    const __grid_constant__ CUtensorMap tm_y, Geo g, const float *ws_gam) {
+    extern __shared__ uint8_t smem_raw[];
+    IntraSmem &s = *reinterpret_cast<IntraSmem *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, h = blockIdx.y, H = g.H, ci = blockIdx.x;
+    const int v = tid & 127, hs = tid >> 7, c0 = 32 * hs, cq = c0 >> 3;
+    ChunkRef cr;
+    if (!chunk_ref(g, ci, cr)) return;
+    const int L = cr.len;
+    const long long bos = cr.bos;
+
+    if (tid == 0) {
+        mbar_init(&s.tma_bar, 1);
+        mbar_init(&s.mma_bar, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&s.tmem_base, 128);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = s.tmem_base;
+    const uint32_t t_p = tb, t_y = tb + 64;
+    if (tid == 0) {
+        const int tok0 = (int)bos;
+        mbar_arrive_expect_tx(&s.tma_bar, 6 * kTile);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            tma_load_3d(s.qk + half * 2 * kTile, &tm_q, &s.tma_bar, half * 64, h, tok0);
+            tma_load_3d(s.qk + half * 2 * kTile + kTile, &tm_k, &s.tma_bar, half * 64, h, tok0);
+            tma_load_3d(s.dO + half * kTile, &tm_do, &s.tma_bar, half * 64, h, tok0);
+        }
+    }
+    if (tid < 64) s.gam[tid] = tid < L ? ws_gam[(bos + tid) * H + h] : 0.f;
+    int mma_n = 0;
+    bool tma_pending = true;
+    bool ok = mbar_wait(&s.tma_bar, 0, g.spin_limit, g.status);
+    if (__syncthreads_or(!ok)) goto bail;
+    tma_pending = false;
+    ++mma_n;
+    if (warp == 0) {
+        tc_fence_after();
+        const uint32_t qk = smem_u32(s.qk);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t half = kk >> 2, sub = (kk & 3) * 32;
+            mma_bf16(t_p, desc_sw128(qk + half * 2 * kTile + sub, 16, 1024),
+                     desc_sw128(qk + half * 2 * kTile + kTile + sub, 16, 1024), kIdKK64, kk > 0);
+        }
+        mma_commit(&s.mma_bar);
+    }
+    if (g.l2norm && tid < 128) {
+        // 1 / |q_r| from the Q rows (threads 0-63), 1 / |k_r| from the K rows (64-127)
+        const int r = tid & 63;
+        const uint8_t *base = s.qk + (tid >= 64 ? kTile : 0);
+        float ss = 0.f;
+#pragma unroll
+        for (int half = 0; half < 2; ++half)
+#pragma unroll 8
+            for (int col = 0; col < 64; ++col) {
+                const float x = ld_bf16(base + half * 2 * kTile, r, col);
+                ss += x * x;
+            }
+        (tid >= 64 ? s.rk : s.rq)[r] = rsqrtf(ss + 1e-6f);
+    }
+    if (g.l2norm) __syncthreads();
+    if (tid >= 128 && tid < 192) {
+        // row r of Qs = diag(scale e^gam (x 1/|q_r|)) Q, both dk halves
+        const int r = tid - 128;
+        const float f = r < L ? g.scale * __expf(s.gam[r]) * (g.l2norm ? s.rq[r] : 1.f) : 0.f;
+#pragma unroll 1
+        for (int q = 0; q < 16; ++q) {
+            const int half = q >> 3, chunk = q & 7;
+            float x[8];
+            const uint4 raw = *reinterpret_cast<const uint4 *>(
+                s.qk + half * 2 * kTile + r * 128 + ((chunk ^ (r & 7)) << 4));
+            const __nv_bfloat16 *b = reinterpret_cast<const __nv_bfloat16 *>(&raw);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = f * __bfloat162float(b[e]);
+            st_row8(s.qs + half * kTile, r, chunk, x);
+        }
+    }
+    ok = mbar_wait(&s.mma_bar, 0, g.spin_limit, g.status);
+    if (__syncthreads_or(!ok)) goto bail;
+    tc_fence_after();
+    if (v < 64) {
+        // P row r = v, columns c0 .. c0+31, scale included
+        const int r = v;
+        const float gr = s.gam[r];
+        const float sr = g.l2norm ? s.rq[r] : 1.f;
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+            float x[8];
+            tmem_ld8(tmem_addr(t_p, warp, c0 + 8 * q), x);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int c = c0 + 8 * q + e;
+                x[e] = (c <= r && r < L) ? g.scale * x[e] * __expf(gr - s.gam[c]) * sr *
+                                               (g.l2norm ? s.rk[c] : 1.f)
+                                         : 0.f;
+            }
+            st_row8(s.p, r, cq + q, x);
+        }
+    }
+    tc_fence_before();
+    fence_proxy_async();
+    __syncthreads();
+    if (tid == 0) {
+        // Qs is complete: store it while Y^T is computed
+        const int row = (int)(((long long)ci * H + h) * 2 * 64);
+        tma_store_2d(&tm_qs, s.qs, 0, row);
+        tma_store_2d(&tm_qs, s.qs + kTile, 0, row + 64);
+        bulk_commit();
+    }
+    ++mma_n;
+    if (warp == 0) {
+        tc_fence_after();
+        const uint32_t dO = smem_u32(s.dO), pp = smem_u32(s.p);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            mma_bf16(t_y, desc_sw128(dO + kk * 2048, kTile, 1024),    // dO^T, MN-major
+                     desc_sw128(pp + kk * 2048, kTile, 1024), kIdMM64, kk > 0);   // P, MN-major
+        mma_commit(&s.mma_bar);
+    }
+    ok = mbar_wait(&s.mma_bar, 1, g.spin_limit, g.status);
+    if (__syncthreads_or(!ok)) goto bail;
+    tc_fence_after();
+#pragma unroll 1
+    for (int q = 0; q < 4; ++q) {
+        float x[8];
+        tmem_ld8(tmem_addr(t_y, warp, c0 + 8 * q), x);
+        st_row8(s.yT, v, cq + q, x);
+    }
+    fence_proxy_async();
+    __syncthreads();
+    if (tid == 0) {
+        tma_store_2d(&tm_y, s.yT, 0, (int)(((long long)ci * H + h) * kD));
+        bulk_commit();
+    }
+    goto done;
+bail:
+    if (tid == 0) {
+        if (tma_pending) mbar_drain(&s.tma_bar, 0);
+        if (mma_n > 0) mbar_drain(&s.mma_bar, (mma_n - 1) & 1);
+    }
+done:
+    if (tid == 0) bulk_wait_all();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tb, 128);
+}
+
+// ------------------------------------------------------------------ reverse walk
+namespace {
 struct DWalkSmem {
-    uint8_t qk[2][4 * kTile];      // per stage: [dk half][Q rows 0-63, K rows 64-127][128 B]
+    uint8_t k[2][2 * kTile];       // per stage: K, [dk half][64 rows][128 B]
     uint8_t w[2][2 * kTile];       // per stage: W^T, [128 rows k][64 chunk rows]  K-major B
-    uint8_t dO[2][2 * kTile];      // per stage: [dv half][64 rows][128 B]
-    uint8_t dhT[4 * kTile];        // [dk half][128 rows (v)][128 B]      K-major A
-    uint8_t qs[2 * kTile];         // diag(scale e^gam) Q: [dk half][64 rows r][128 B], MN-major B
-    uint8_t duT[2 * kTile];        // [128 rows (v)][64 c]                 K-major A
-    uint8_t p[kTile];              // [64 rows r][64 c], includes scale    MN-major B
+    uint8_t dO[2][2 * kTile];      // per stage: dO, [dv half][64 rows][128 B]
+    uint8_t qs[2][2 * kTile];      // per stage: Qs, [dk half][64 rows][128 B]
+    uint8_t y[2][2 * kTile];       // per stage: Y^T, [128 rows v][64 chunk rows]
+    uint8_t dhT[4 * kTile];        // dH^T: [k half][128 rows v][128 B]   K-major A
+    uint8_t duT[2 * kTile];        // dU^T: [128 rows v][64 chunk rows]    K-major A
     float gam[2][64];
-    float fr[64];                  // exp(gam_L - gam_r) (x rk_r), 0 past L
-    float rq[64], rk[64];
-    uint64_t tma_bar[2], mma_bar;
+    float fr[64];                  // exp(gam_L - gam_r) (x 1/|k_r|), 0 past L
+    float rk[64];
+    uint64_t tma_bar[2], bar_x, bar_z;
     uint32_t tmem_base;
 };
 
@@ -53,28 +236,26 @@ struct TcDWalkArgs {
     const float *dht;         // [N, H, K, V] nullable
     const float *seg_end;     // [segs, H, K, V] (CP): gradient at each segment's end
     float *dh0;               // [N, H, K, V] nullable
-    __nv_bfloat16 *dhc;       // gradient at every chunk's end (kOut), bf16 dH^T tiles
-                              // [chunk][H][k half][v][64]
-    __nv_bfloat16 *du;        // [chunk][H][V][64] dU^T tiles (kOut), nullable
-    float *maps;              // [segs, H, K, K+V] (kMap)
+    float *maps;              // [segs, H, K, K+V] (kDMap)
     int cp;
 };
 
-enum { kDOut = 0, kDMap = 1 };
+struct DWalkMaps {
+    CUtensorMap k, w, dO, qs, y, dhc, du;
+};
 
-template <typename F>
-cudaError_t set_smem(F kernel, size_t bytes) {
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-}
+enum { kDOut = 0, kDMap = 1 };
 }  // namespace
 
 // 256 threads: thread t owns row v = t % 128 of dH^T (TMEM lane v) and the
 // column half hs = t / 128; warps w and w + 4 split each epilogue's columns.
+// Per chunk: X^T = dH^T K^T (first MMA group; dO^T Qs is issued behind it
+// into the state-update accumulator), dU^T = Y^T + X^T diag(f), then
+// -dU^T W onto that accumulator (second group) and the dH^T update.  The
+// gradient at each chunk's end (bf16 dH^T) and dU^T leave by TMA stores.
 template <int MODE>
 __global__ void __launch_bounds__(256, 1)
-tc_dwalk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_do,
-                Geo g, TcDWalkArgs a) {
+tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
     extern __shared__ uint8_t smem_raw[];
     DWalkSmem &s = *reinterpret_cast<DWalkSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -97,15 +278,17 @@ tc_dwalk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     long long sbos;
     int slen;
     seq_range(g, n, sbos, slen);
+    const bool tma_thread = tid == 255;
 
     if (tid == 0) {
         mbar_init(&s.tma_bar[0], 1);
         mbar_init(&s.tma_bar[1], 1);
-        mbar_init(&s.mma_bar, 1);
+        mbar_init(&s.bar_x, 1);
+        mbar_init(&s.bar_z, 1);
         fence_barrier_init();
     }
     if (warp == 0) {
-        tmem_alloc(&s.tmem_base, 512);
+        tmem_alloc(&s.tmem_base, 256);
         tmem_relinquish();
         tc_fence_before();
     }
@@ -133,200 +316,136 @@ tc_dwalk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = s.tmem_base;
-    const uint32_t t_p = tbase, t_x = tbase + 64, t_y = tbase + 128, t_z = tbase + 256;
+    const uint32_t t_x = tbase, t_z = tbase + 128;
 
     auto issue_tma = [&](int st, int c) {
         const int tok0 = (int)(sbos + (long long)c * kChunk);
-        mbar_arrive_expect_tx(&s.tma_bar[st], 8 * kTile);   // 2 halves x (q, k, w, dO)
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            tma_load_3d(s.qk[st] + half * 2 * kTile, &tm_q, &s.tma_bar[st], half * 64, h, tok0);
-            tma_load_3d(s.qk[st] + half * 2 * kTile + kTile, &tm_k, &s.tma_bar[st], half * 64, h, tok0);
-            tma_load_3d(s.dO[st] + half * kTile, &tm_do, &s.tma_bar[st], half * 64, h, tok0);
+        const int trow = (int)(((long long)(cbase + c) * H + h) * kD);
+        mbar_arrive_expect_tx(&s.tma_bar[st], (use_do ? 10 : 4) * kTile);
+        tma_load_3d(s.k[st], &m.k, &s.tma_bar[st], 0, h, tok0);
+        tma_load_3d(s.k[st] + kTile, &m.k, &s.tma_bar[st], 64, h, tok0);
+        tma_load_2d(s.w[st], &m.w, &s.tma_bar[st], 0, trow);
+        if (use_do) {
+            tma_load_3d(s.dO[st], &m.dO, &s.tma_bar[st], 0, h, tok0);
+            tma_load_3d(s.dO[st] + kTile, &m.dO, &s.tma_bar[st], 64, h, tok0);
+            tma_load_2d(s.qs[st], &m.qs, &s.tma_bar[st], 0, trow);
+            tma_load_2d(s.qs[st] + kTile, &m.qs, &s.tma_bar[st], 0, trow + 64);
+            tma_load_2d(s.y[st], &m.y, &s.tma_bar[st], 0, trow);
         }
-        tma_load_2d(s.w[st], &tm_w, &s.tma_bar[st], 0, (int)(((long long)(cbase + c) * H + h) * kD));
     };
 
-    int it = 0, mma_n = 0, tma_pending = 0;
+    // one commit per barrier per chunk: every barrier's parity is the chunk
+    // iteration's; `pend` marks groups committed in this iteration, not yet waited
+    int it = 0, tma_pending = 0, pend = 0;
     bool bailed = false;
     if (c1 > c0) {
-        if (tid == 0) issue_tma(0, c1 - 1);
+        if (tma_thread) issue_tma(0, c1 - 1);
         tma_pending |= 1;
     }
     for (int c = c1 - 1; c >= c0; --c, ++it) {
         const int st = it & 1;
+        const uint32_t par = it & 1;
         const long long bos = sbos + (long long)c * kChunk;
         const int L = min(kChunk, slen - c * kChunk);
+        const int trow = (int)(((long long)(cbase + c) * H + h) * kD);
         float gnext = 0.f;                     // gam of chunk c - 1, stored at the end
+        pend = 0;
         if (c - 1 >= c0) {
-            if (tid == 0) {
+            if (tma_thread) {
                 fence_proxy_async();
                 issue_tma(st ^ 1, c - 1);
             }
             tma_pending |= 1 << (st ^ 1);
             if (tid < 64) gnext = a.ws_gam[(bos - kChunk + tid) * H + h];   // a full chunk
         }
-        if (MODE == kDOut) {
-            // row v, k half hs of dH^T: 128 contiguous bytes of the chunk's tile
-            uint4 *dst = reinterpret_cast<uint4 *>(
-                a.dhc + ((((long long)(cbase + c) * H + h) * 2 + hs) * kD + v) * 64);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                uint32_t w4[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    __nv_bfloat162 b2 = __floats2bfloat162_rn(dH[8 * q + 2 * e], dH[8 * q + 2 * e + 1]);
-                    w4[e] = *reinterpret_cast<uint32_t *>(&b2);
-                }
-                dst[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-            }
+        if (MODE == kDOut && tma_thread) {
+            // the gradient at this chunk's end: the bf16 dH^T tile, by TMA
+            tma_store_2d(&m.dhc, s.dhT, 0, 2 * trow);
+            tma_store_2d(&m.dhc, s.dhT + 2 * kTile, 0, 2 * trow + kD);
+            bulk_commit();
         }
         bool ok = mbar_wait(&s.tma_bar[st], (it >> 1) & 1, g.spin_limit, g.status);
         if (__syncthreads_or(!ok)) { bailed = true; break; }
         tma_pending &= ~(1 << st);
-        if (g.l2norm && tid < 128) {
-            const int r = tid & 63;
-            const uint8_t *base = s.qk[st] + (tid >= 64 ? kTile : 0);
+        if (warp == 0) {
+            tc_fence_after();
+            const uint32_t kt = smem_u32(s.k[st]), dhT = smem_u32(s.dhT);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t half = kk >> 2, sub = (kk & 3) * 32;
+                mma_bf16(t_x, desc_sw128(dhT + half * 2 * kTile + sub, 16, 1024),
+                         desc_sw128(kt + half * kTile + sub, 16, 1024), kIdKK64, kk > 0);
+            }
+            mma_commit(&s.bar_x);
+            if (use_do) {
+                const uint32_t dO = smem_u32(s.dO[st]), qs = smem_u32(s.qs[st]);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(t_z, desc_sw128(dO + kk * 2048, kTile, 1024),   // dO^T, MN-major
+                             desc_sw128(qs + kk * 2048, kTile, 1024), kIdMM128, kk > 0);
+            }
+        }
+        pend = 1;
+        if (g.l2norm && tid >= 64 && tid < 128) {
+            const int r = tid - 64;
             float ss = 0.f;
 #pragma unroll
             for (int half = 0; half < 2; ++half)
 #pragma unroll 8
                 for (int col = 0; col < 64; ++col) {
-                    const float x = ld_bf16(base + half * 2 * kTile, r, col);
+                    const float x = ld_bf16(s.k[st] + half * kTile, r, col);
                     ss += x * x;
                 }
-            (tid >= 64 ? s.rk : s.rq)[r] = rsqrtf(ss + 1e-6f);
-        }
-        // group 1: P (rows of [Q; K] K^T) and X^T = dH^T K^T
-        ++mma_n;
-        if (warp == 0) {
-            tc_fence_after();
-            const uint32_t qk = smem_u32(s.qk[st]), dhT = smem_u32(s.dhT);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t half = kk >> 2, sub = (kk & 3) * 32;
-                const uint64_t bk = desc_sw128(qk + half * 2 * kTile + kTile + sub, 16, 1024);
-                const uint64_t ad = desc_sw128(dhT + half * 2 * kTile + sub, 16, 1024);
-                mma_bf16(t_x, ad, bk, kIdKK64, kk > 0);
-                if (use_do) {
-                    const uint64_t aq = desc_sw128(qk + half * 2 * kTile + sub, 16, 1024);
-                    mma_bf16(t_p, aq, bk, kIdKK64, kk > 0);
-                }
-            }
-            mma_commit(&s.mma_bar);
+            s.rk[r] = rsqrtf(ss + 1e-6f);
         }
         if (g.l2norm) __syncthreads();
         if (tid < 64) {
             const float gl = s.gam[st][L - 1];
             s.fr[tid] = tid < L ? __expf(gl - s.gam[st][tid]) * (g.l2norm ? s.rk[tid] : 1.f) : 0.f;
         }
-        if (use_do && v >= 64) {
-            // row r of diag(scale e^gam) Q, dk half hs (the Q tile is already in place)
-            const int r = v - 64;
-            const float f = r < L ? g.scale * __expf(s.gam[st][r]) * (g.l2norm ? s.rq[r] : 1.f) : 0.f;
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                float x[32];
-#pragma unroll
-                for (int jj = 0; jj < 32; ++jj)
-                    x[jj] = f * ld_bf16(s.qk[st] + hs * 2 * kTile, r, q * 32 + jj);
-                st_row32(s.qs + hs * kTile, r, q * 32, x);
-            }
-        }
-        ok = mbar_wait(&s.mma_bar, (mma_n - 1) & 1, g.spin_limit, g.status);
+        ok = mbar_wait(&s.bar_x, par, g.spin_limit, g.status);
         if (__syncthreads_or(!ok)) { bailed = true; break; }
+        pend = 0;
         tc_fence_after();
-        if (use_do) {
-            if (v < 64) {
-                // P row r = v, columns 32*hs .. +31, scale included
-                const int r = v;
-                const float gr = s.gam[st][r];
-                const float sr = g.l2norm ? s.rq[r] : 1.f;
-                float x[32];
-                tmem_ld32(tmem_addr(t_p, warp, 32 * hs), x);
+        // dU^T row v, chunk rows 32*hs .. +31 in rolled groups of 8: Y^T + X^T diag(f)
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+            float x[8];
+            tmem_ld8(tmem_addr(t_x, warp, 32 * hs + 8 * q), x);
+            const int chunk = 4 * hs + q;
+            uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+            if (use_do)
+                raw = *reinterpret_cast<const uint4 *>(s.y[st] + v * 128 + ((chunk ^ (v & 7)) << 4));
+            const __nv_bfloat16 *bv = reinterpret_cast<const __nv_bfloat16 *>(&raw);
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    const int c2 = 32 * hs + jj;
-                    x[jj] = (c2 <= r && r < L)
-                                ? g.scale * x[jj] * __expf(gr - s.gam[st][c2]) * sr *
-                                      (g.l2norm ? s.rk[c2] : 1.f)
-                                : 0.f;
-                }
-                st_row32(s.p, r, 32 * hs, x);
+            for (int e = 0; e < 8; ++e) {
+                const int r = 8 * chunk + e;
+                x[e] = r < L ? __bfloat162float(bv[e]) + s.fr[r] * x[e] : 0.f;
             }
-            tc_fence_before();
-            fence_proxy_async();
-            __syncthreads();
-            ++mma_n;
-            if (warp == 0) {
-                tc_fence_after();
-                const uint32_t dO = smem_u32(s.dO[st]), pp = smem_u32(s.p);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t ao = desc_sw128(dO + kk * 2048, kTile, 1024);   // dO^T, MN-major
-                    const uint64_t bp = desc_sw128(pp + kk * 2048, kTile, 1024);   // P, MN-major
-                    mma_bf16(t_y, ao, bp, kIdMM64, kk > 0);
-                }
-                mma_commit(&s.mma_bar);
-            }
-            ok = mbar_wait(&s.mma_bar, (mma_n - 1) & 1, g.spin_limit, g.status);
-            if (__syncthreads_or(!ok)) { bailed = true; break; }
-            tc_fence_after();
-        }
-        {
-            // dU^T row v, chunk rows 32*hs .. +31: Y^T + X^T diag(f)
-            float x[32], y[32];
-            tmem_ld32(tmem_addr(t_x, warp, 32 * hs), x);
-            if (use_do) tmem_ld32(tmem_addr(t_y, warp, 32 * hs), y);
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-                const int r = 32 * hs + jj;
-                x[jj] = r < L ? (use_do ? y[jj] : 0.f) + s.fr[r] * x[jj] : 0.f;
-            }
-            st_row32(s.duT, v, 32 * hs, x);
-            if (MODE == kDOut && a.du) {
-                // 32 chunk rows of dU^T row v: 64 contiguous bytes of the chunk tile
-                uint4 *dst = reinterpret_cast<uint4 *>(
-                    a.du + (((long long)(cbase + c) * H + h) * kD + v) * 64 + 32 * hs);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint32_t w4[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        __nv_bfloat162 b2 = __floats2bfloat162_rn(x[8 * q + 2 * e], x[8 * q + 2 * e + 1]);
-                        w4[e] = *reinterpret_cast<uint32_t *>(&b2);
-                    }
-                    dst[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-                }
-            }
+            st_row8(s.duT, v, chunk, x);
         }
         tc_fence_before();
         fence_proxy_async();
         __syncthreads();
-        // group 3: Z^T = dO^T (diag(scale e^gam) Q) - dU^T W
-        ++mma_n;
+        if (MODE == kDOut && tma_thread) {
+            tma_store_2d(&m.du, s.duT, 0, trow);
+            bulk_commit();
+        }
         if (warp == 0) {
             tc_fence_after();
-            const uint32_t dO = smem_u32(s.dO[st]), qs = smem_u32(s.qs), du = smem_u32(s.duT),
-                           wt = smem_u32(s.w[st]);
+            const uint32_t du = smem_u32(s.duT), wt = smem_u32(s.w[st]);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                if (use_do) {
-                    const uint64_t ao = desc_sw128(dO + kk * 2048, kTile, 1024);
-                    const uint64_t bq = desc_sw128(qs + kk * 2048, kTile, 1024);
-                    mma_bf16(t_z, ao, bq, kIdMM128, kk > 0);
-                }
-            }
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t au = desc_sw128(du + kk * 32, 16, 1024);
-                const uint64_t bw = desc_sw128(wt + kk * 32, 16, 1024);   // W^T, K-major
-                mma_bf16(t_z, au, bw, kIdKK128Neg, (use_do || kk > 0) ? 1u : 0u);
-            }
-            mma_commit(&s.mma_bar);
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16(t_z, desc_sw128(du + kk * 32, 16, 1024),
+                         desc_sw128(wt + kk * 32, 16, 1024),             // W^T, K-major
+                         kIdKK128Neg, (use_do || kk > 0) ? 1u : 0u);
+            mma_commit(&s.bar_z);
         }
-        ok = mbar_wait(&s.mma_bar, (mma_n - 1) & 1, g.spin_limit, g.status);
+        pend = 2;
+        if (tma_thread) bulk_wait_read();     // the dH^T and dU^T stores have read their tiles
+        ok = mbar_wait(&s.bar_z, par, g.spin_limit, g.status);
         if (__syncthreads_or(!ok)) { bailed = true; break; }
+        pend = 0;
         tc_fence_after();
         {
             const float el = __expf(s.gam[st][L - 1]);
@@ -345,12 +464,14 @@ tc_dwalk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         __syncthreads();
     }
 
+    if (tma_thread) bulk_wait_all();
     if (bailed) {
         if (tid == 0) {
             for (int st = 0; st < 2; ++st)
                 if (tma_pending & (1 << st))
                     mbar_drain(&s.tma_bar[st], ((it + (st != (it & 1))) >> 1) & 1);
-            if (mma_n > 0) mbar_drain(&s.mma_bar, (mma_n - 1) & 1);
+            if (pend & 1) mbar_drain(&s.bar_x, it & 1);
+            if (pend & 2) mbar_drain(&s.bar_z, it & 1);
         }
     } else if (MODE == kDMap) {
         float *dst = a.maps + ((long long)(seq_seg_base(g, n) + j) * H + h) * kD * (2 * kD);
@@ -363,7 +484,7 @@ tc_dwalk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tbase, 512);
+    if (warp == 0) tmem_dealloc(tbase, 256);
 }
 
 // ------------------------------------------------------------------ host side
@@ -371,14 +492,29 @@ cudaError_t backward(const Plan &p, cudaStream_t s, bool have_ctx) {
     cudaError_t e = simt::tables(p, s);
     if (e != cudaSuccess) return e;
     if (!have_ctx && (e = recompute_states(p, s)) != cudaSuccess) return e;
+    if ((e = encoder()) != cudaSuccess) return e;
     const Geo &g = p.g;
     const long long tokens = (long long)g.B * g.T;
-    CUtensorMap mq, mk, mw, mdo;
+    const long long tile_rows = (long long)p.max_chunks * g.H * kD;
+    DWalkMaps m;
+    CUtensorMap mq;
     if ((e = make_map(&mq, g.q, tokens, g.H)) != cudaSuccess) return e;
-    if ((e = make_map(&mk, g.k, tokens, g.H)) != cudaSuccess) return e;
-    if ((e = make_map_tiles(&mw, p.ws.w, (long long)p.max_chunks * g.H * kD)) != cudaSuccess)
-        return e;
-    if ((e = make_map(&mdo, p.d_o, tokens, g.H)) != cudaSuccess) return e;
+    if ((e = make_map(&m.k, g.k, tokens, g.H)) != cudaSuccess) return e;
+    if ((e = make_map(&m.dO, p.d_o, tokens, g.H)) != cudaSuccess) return e;
+    if ((e = make_map_tiles(&m.w, p.ws.w, tile_rows)) != cudaSuccess) return e;
+    if ((e = make_map_tiles(&m.qs, p.ws.qs, tile_rows, 64)) != cudaSuccess) return e;
+    if ((e = make_map_tiles(&m.y, p.ws.yt, tile_rows)) != cudaSuccess) return e;
+    if ((e = make_map_tiles(&m.dhc, p.ws.dhc, 2 * tile_rows)) != cudaSuccess) return e;
+    if ((e = make_map_tiles(&m.du, p.ws.du, tile_rows)) != cudaSuccess) return e;
+
+    const size_t ismem = sizeof(IntraSmem) + 1024;
+    if ((e = set_smem(tc_bwd_intra_kernel, ismem)) != cudaSuccess) return e;
+    prof_before("tc_bwd_intra", s);
+    tc_bwd_intra_kernel<<<dim3(p.max_chunks, g.H), 256, ismem, s>>>(mq, m.k, m.dO, m.qs, m.y, g,
+                                                                     p.ws.gam);
+    prof_after(s);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
     const size_t smem = sizeof(DWalkSmem) + 1024;
     if ((e = set_smem(tc_dwalk_kernel<kDOut>, smem)) != cudaSuccess) return e;
     if ((e = set_smem(tc_dwalk_kernel<kDMap>, smem)) != cudaSuccess) return e;
@@ -386,23 +522,21 @@ cudaError_t backward(const Plan &p, cudaStream_t s, bool have_ctx) {
     a.ws_gam = p.ws.gam;
     a.dht = p.dht;
     a.dh0 = p.dh0;
-    a.dhc = (__nv_bfloat16 *)p.ws.dhc;
-    a.du = (__nv_bfloat16 *)p.ws.du;
     if (p.cp) {
         a.cp = 1;
         a.maps = p.ws.maps;
         a.seg_end = p.ws.seg_state;
         prof_before("tc_dwalk_map", s);
-        tc_dwalk_kernel<kDMap><<<dim3(p.max_segs, g.H, 2), 256, smem, s>>>(mq, mk, mw, mdo, g, a);
+        tc_dwalk_kernel<kDMap><<<dim3(p.max_segs, g.H, 2), 256, smem, s>>>(m, g, a);
         prof_after(s);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if ((e = simt::cp_rscan(p, s)) != cudaSuccess) return e;
         prof_before("tc_dwalk_out", s);
-        tc_dwalk_kernel<kDOut><<<dim3(p.max_segs, g.H, 1), 256, smem, s>>>(mq, mk, mw, mdo, g, a);
+        tc_dwalk_kernel<kDOut><<<dim3(p.max_segs, g.H, 1), 256, smem, s>>>(m, g, a);
         prof_after(s);
     } else {
         prof_before("tc_dwalk_out", s);
-        tc_dwalk_kernel<kDOut><<<dim3(g.N, g.H, 1), 256, smem, s>>>(mq, mk, mw, mdo, g, a);
+        tc_dwalk_kernel<kDOut><<<dim3(g.N, g.H, 1), 256, smem, s>>>(m, g, a);
         prof_after(s);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

@@ -57,8 +57,8 @@ __device__ __forceinline__ float scan64(float x, float *wsum) {
 
 __global__ void __launch_bounds__(128, 2)
 tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-            Geo g, float *ws_gam, __nv_bfloat16 *ws_w, __nv_bfloat16 *ws_u,
-            __nv_bfloat16 *ws_t) {
+               const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_u,
+               Geo g, float *ws_gam, __nv_bfloat16 *ws_t) {
     extern __shared__ uint8_t smem_raw[];
     PrepSmem &s = *reinterpret_cast<PrepSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -227,34 +227,34 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     ok = mbar_wait(&s.mma_bar, 1, g.spin_limit, g.status);
     if (__syncthreads_or(!ok)) goto bail;
     tc_fence_after();
-    // thread t = feature index (dk for W, dv for u); its 64 chunk rows form one
-    // contiguous 128-byte row of the chunk-major tile [chunk][H][feature][row]
+    // thread t = feature index (dk for W, dv for u): its 64 chunk rows form row t
+    // of the W^T / u^T tile, staged swizzled in the dead K / V tiles ([chunk]
+    // [128 rows][128 B]) and stored by TMA
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
         const int c = m & 1;                  // chunk
         const bool isu = m >= 2;
-        if (c && !has_b) continue;
-        const ChunkRef &cr = c ? rb : ra;
-        const int Lc = cr.len;
-        uint4 *dst = reinterpret_cast<uint4 *>(
-            (isu ? ws_u : ws_w) + (((long long)(2 * blockIdx.x + c) * H + h) * kD + tid) * 64);
+        const int Lc = (c && !has_b) ? 0 : (c ? rb.len : ra.len);
+        uint8_t *tile = (isu ? s.v : s.k) + c * 2 * kTile;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             float x[32];
             tmem_ld32(tmem_addr(tbase, warp, (isu ? 128 : 0) + c * 64 + 32 * half), x);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint32_t w4[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int j0 = 8 * q + 2 * e, r0 = 32 * half + j0;
-                    __nv_bfloat162 b2 = __floats2bfloat162_rn(r0 < Lc ? x[j0] : 0.f,
-                                                              r0 + 1 < Lc ? x[j0 + 1] : 0.f);
-                    w4[e] = *reinterpret_cast<uint32_t *>(&b2);
-                }
-                dst[4 * half + q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-            }
+            for (int j = 0; j < 32; ++j) x[j] = 32 * half + j < Lc ? x[j] : 0.f;
+            st_row32(tile, tid, 32 * half, x);
         }
+    }
+    fence_proxy_async();
+    __syncthreads();
+    if (tid == 0) {
+        for (int c = 0; c < (has_b ? 2 : 1); ++c) {
+            const int row = (int)(((long long)(2 * blockIdx.x + c) * H + h) * kD);
+            tma_store_2d(&tm_w, s.k + c * 2 * kTile, 0, row);
+            tma_store_2d(&tm_u, s.v + c * 2 * kTile, 0, row);
+        }
+        bulk_commit();
+        bulk_wait_all();
     }
     goto done;
 bail:
@@ -309,7 +309,8 @@ constexpr uint32_t kIdescKM64 = idesc_bf16(128, 64, false, true);     // B MN-ma
 template <int MODE>
 __global__ void __launch_bounds__(256, 1)
 tc_walk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_w,
-               const __grid_constant__ CUtensorMap tm_u, Geo g, TcWalkArgs a) {
+               const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_hc,
+               Geo g, TcWalkArgs a) {
     extern __shared__ uint8_t smem_raw[];
     WalkSmem &s = *reinterpret_cast<WalkSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -392,7 +393,10 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     // iteration's; `pend` marks groups committed in this iteration, not yet waited
     int it = 0, tma_pending = 0, pend = 0;   // uniform bookkeeping for the bail-out path
     bool bailed = false;
-    if (tid == 0 && cstart < c1) issue_tma(0, cstart);
+    // the last warp issues the loads, away from warp 0 (MMA issue) and the
+    // threads that read gam
+    const bool tma_thread = tid == 255;
+    if (tma_thread && cstart < c1) issue_tma(0, cstart);
     if (cstart < c1) tma_pending |= 1;
     for (int c = cstart; c < c1; ++c, ++it) {
         const int st = it & 1;
@@ -402,7 +406,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         float gnext = 0.f;                     // gam of the next chunk, stored at the end
         pend = 0;
         if (c + 1 < c1) {
-            if (tid == 0) {
+            if (tma_thread) {
                 fence_proxy_async();
                 issue_tma(st ^ 1, c + 1);
             }
@@ -410,20 +414,12 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             const int Ln = min(kChunk, slen - (c + 1) * kChunk);
             if (tid < 64 && tid < Ln) gnext = a.ws_gam[(bos + kChunk + tid) * H + h];
         }
-        if (states && c >= c0) {
-            // row v, k half hs of H^T: 128 contiguous bytes of the chunk's state tile
-            uint4 *dst = reinterpret_cast<uint4 *>(
-                a.hc + ((((long long)(cbase + c) * H + h) * 2 + hs) * kD + v) * 64);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                uint32_t w4[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    __nv_bfloat162 b2 = __floats2bfloat162_rn(Hr[8 * q + 2 * e], Hr[8 * q + 2 * e + 1]);
-                    w4[e] = *reinterpret_cast<uint32_t *>(&b2);
-                }
-                dst[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-            }
+        if (states && c >= c0 && tma_thread) {
+            // the chunk's start state: the bf16 H^T tile in shared memory, by TMA
+            const int row = (int)(((long long)(cbase + c) * H + h) * 2 * kD);
+            tma_store_2d(&tm_hc, s.hT, 0, row);
+            tma_store_2d(&tm_hc, s.hT + 2 * kTile, 0, row + kD);
+            bulk_commit();
         }
         bool ok = mbar_wait(&s.tma_bar[st], (it >> 1) & 1, g.spin_limit, g.status);
         if (__syncthreads_or(!ok)) { bailed = true; break; }
@@ -494,6 +490,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             mma_commit(&s.bar_dh);
         }
         pend = 2;
+        if (tma_thread) bulk_wait_read();     // the state store has read H^T
         ok = mbar_wait(&s.bar_dh, par, g.spin_limit, g.status);
         if (__syncthreads_or(!ok)) { bailed = true; break; }
         pend = 0;
@@ -515,6 +512,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         __syncthreads();
     }
 
+    if (tma_thread) bulk_wait_all();
     if (bailed) {
         if (tid == 0) {
             for (int st = 0; st < 2; ++st)
@@ -612,6 +610,8 @@ static cudaError_t run_forward(const Plan &p, cudaStream_t s, bool states_only, 
     const long long tile_rows = (long long)p.max_chunks * g.H * kD;
     if ((e = make_map_tiles(&mw, p.ws.w, tile_rows)) != cudaSuccess) return e;
     if ((e = make_map_tiles(&mu, p.ws.u, tile_rows)) != cudaSuccess) return e;
+    CUtensorMap mhc;
+    if ((e = make_map_tiles(&mhc, p.ws.hc, 2 * tile_rows)) != cudaSuccess) return e;
 
     const size_t prep_smem = sizeof(PrepSmem) + 1024, walk_smem = sizeof(WalkSmem) + 1024;
     if ((e = set_smem(tc_prep_kernel, prep_smem)) != cudaSuccess) return e;
@@ -620,7 +620,7 @@ static cudaError_t run_forward(const Plan &p, cudaStream_t s, bool states_only, 
 
     prof_before("tc_prep", s);
     tc_prep_kernel<<<dim3((p.max_chunks + 1) / 2, g.H), 128, prep_smem, s>>>(
-        mk, mv, g, p.ws.gam, (__nv_bfloat16 *)p.ws.w, (__nv_bfloat16 *)p.ws.u,
+        mk, mv, mw, mu, g, p.ws.gam,
         (states_only || save) ? (__nv_bfloat16 *)p.ws.tmat : nullptr);
     prof_after(s);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -643,16 +643,16 @@ static cudaError_t run_forward(const Plan &p, cudaStream_t s, bool states_only, 
             a.warm_chunks = p.warm_chunks;
         }
         prof_before("tc_walk_map", s);
-        tc_walk_kernel<kWalkMap><<<dim3(p.max_segs, g.H, 2), 256, walk_smem, s>>>(mk, mw, mu, g, a);
+        tc_walk_kernel<kWalkMap><<<dim3(p.max_segs, g.H, 2), 256, walk_smem, s>>>(mk, mw, mu, mhc, g, a);
         prof_after(s);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if ((e = simt::cp_scan(p, a.warm, s)) != cudaSuccess) return e;
         prof_before(out_name, s);
-        tc_walk_kernel<kWalkOut><<<dim3(p.max_segs, g.H, 1), 256, walk_smem, s>>>(mk, mw, mu, g, a);
+        tc_walk_kernel<kWalkOut><<<dim3(p.max_segs, g.H, 1), 256, walk_smem, s>>>(mk, mw, mu, mhc, g, a);
         prof_after(s);
     } else {
         prof_before(out_name, s);
-        tc_walk_kernel<kWalkOut><<<dim3(g.N, g.H, 1), 256, walk_smem, s>>>(mk, mw, mu, g, a);
+        tc_walk_kernel<kWalkOut><<<dim3(g.N, g.H, 1), 256, walk_smem, s>>>(mk, mw, mu, mhc, g, a);
         prof_after(s);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
