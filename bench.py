@@ -27,6 +27,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "GDN chunked-prefill tokens/s (fwd; fwd+bwd) on 1 GB300 + % of roofline"
 CHUNK = 64
+GRAD_BYTES = 4          # dq, dk, dv come back in fp32 (the library's default)
 L2_BYTES = 129 * 2 ** 20
 
 
@@ -68,18 +69,21 @@ FP32_LANES_PER_SM = 128
 
 
 # Per-kernel algorithmic HBM bytes per token-head for the tensor-core path
-# (bf16 q/k/v/dO, bf16 gradients, K = V = 128, chunk C = 64): every operand
-# read once, every result written once.  W^T, u^T, dU^T are the bf16 chunk
-# tiles; T is the fp32 64 x 64 inverse and hc / dhc the fp32 chunk states,
-# so per token they cost 64 * 4 and K * V * 4 / C bytes.
-def kernel_bytes_per_token_head(name, K, V, e=2, eg=2):
+# (bf16 q/k/v/dO, K = V = 128, chunk C = 64; gradients of eg bytes): every
+# operand the kernel needs read once, every result written once.  W^T, u^T,
+# dU^T, Y^T = (dO^T P)^T and Qs are bf16 chunk tiles (2 bytes per feature per
+# token); T is the bf16 64 x 64 inverse (128 bytes per token); hc / dhc are
+# the bf16 chunk states (K V 2 / C bytes per token).
+def kernel_bytes_per_token_head(name, K, V, e=2, eg=4):
     C = CHUNK
-    t_mat = C * 4
-    state = K * V * 4 / C
+    t_mat = C * 2
+    state = K * V * 2 / C
     table = {
         "tc_prep": e * (K + V) + 8 + 4 + 2 * (K + V) + t_mat,
-        "tc_walk_out": 2 * e * K + 2 * (K + V) + 4 + e * V + state,
-        "tc_dwalk_out": 2 * e * K + 2 * K + e * V + 4 + state + 2 * V,
+        "tc_walk": e * K + 2 * (K + V) + 4 + state,
+        "tc_out": 2 * e * K + 2 * (K + V) + state + 4 + e * V,
+        "tc_bwd_intra": e * (2 * K + V) + 4 + 2 * K + 2 * V,
+        "tc_dwalk_out": e * K + 2 * K + e * V + 2 * K + 2 * V + 4 + state + 2 * V,
         "tc_local_grad": (e * (2 * K + 2 * V) + 2 * (K + 2 * V) + 2 * state + t_mat + 8 +
                           eg * (2 * K + V) + 8),
     }
@@ -89,7 +93,11 @@ def kernel_bytes_per_token_head(name, K, V, e=2, eg=2):
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
 # ncu capture of the named kernel on the named workload, valid while the
 # kernel's source file still hashes to `sha256` (otherwise reported as null).
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    ("tc_local_grad", "edge"): {
+        "file": "gdn_tc_local.cu", "bytes": 193943808 + 62096896,
+        "sha256": "fbe547dc89fc5e0dd9676349cf18728089d2cfd3d41cb4b7fe17ac69d64e1a0d"},
+}
 
 
 def measured_traffic(name, workload):
@@ -238,7 +246,7 @@ def run_reference(args, rank, world):
 
 def kernel_entry(name, launches, ms, total_ms, p, th, e_in):
     ent = {"name": name, "launches": launches, "ms": ms, "share": ms / total_ms}
-    by_th = kernel_bytes_per_token_head(name, p.K, p.V, e_in, e_in)
+    by_th = kernel_bytes_per_token_head(name, p.K, p.V, e_in, GRAD_BYTES)
     if by_th is not None:
         ent["gbs"] = by_th * th / (ms / launches / 1e3) / 1e9
     return ent
@@ -366,7 +374,7 @@ def run_ours(args, rank, world, local):
     dom_name, dom_launches, dom_ms = dom
     avg_s = dom_ms / dom_launches / 1e3
     hbm_src = "measured" if "hbm_gbs" in peaks else "fallback"
-    by_th = kernel_bytes_per_token_head(dom_name, p.K, p.V, e_in, e_in)
+    by_th = kernel_bytes_per_token_head(dom_name, p.K, p.V, e_in, GRAD_BYTES)
     if by_th is not None:
         # the tensor-core kernels move more bytes than their few MMAs can hide: HBM roofline
         roof = {"kernel": dom_name, "bound": "hbm", "unit": "GB/s",

@@ -121,6 +121,28 @@ static bool cp_auto(long long units, long long avg_len, int sms) {
     return units * 132 <= 40ll * sms || (units * 132 <= 56ll * sms && avg_len >= 8192);
 }
 
+// Segments per sequence for the tensor-core path: the P minimising a cost
+// model in units of one chunk step of a walk.  The map walk runs 2 (P - 1)
+// CTAs per unit (its last segment needs no map), the output walk P, each
+// over G = ceil(nc / P) chunks, in waves of one CTA per SM; the scan takes
+// P - 1 dependent steps of about 1.6 chunk steps per wave of its 16 column
+// blocks per unit.
+static long long tc_segments(long long units, int nc, int sms) {
+    auto waves = [&](long long ctas) { return (ctas + sms - 1) / sms; };
+    long long best_p = 2;
+    double best = 1e300;
+    for (long long P = 2; P <= 64 && P <= nc; ++P) {
+        const long long G = (nc + P - 1) / P;
+        const double cost = (double)(waves(2 * (P - 1) * units) + waves(P * units)) * (double)G +
+                            1.6 * (double)(P - 1) * (double)waves(16 * units);
+        if (cost < best) {
+            best = cost;
+            best_p = P;
+        }
+    }
+    return best_p;
+}
+
 static gdn_status make_plan(const Common &c, bool bwd, int sms, Plan &p) {
     gdn_status st = validate(c);
     if (st != GDN_OK) return st;
@@ -146,6 +168,8 @@ static gdn_status make_plan(const Common &c, bool bwd, int sms, Plan &p) {
         int G = c.seg_chunks;
         if (G <= 0) {
             long long P = sms > 0 ? (sms + units - 1) / units : 2;
+            if (c.dtype == GDN_BF16 && c.K == 128 && c.V == 128 && sms > 0)
+                P = tc_segments(units, nc_avg, sms);
             if (P < 2) P = 2;
             if (P > nc_avg) P = nc_avg > 0 ? nc_avg : 1;
             G = (int)((nc_avg + P - 1) / P);
