@@ -26,6 +26,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
 #include "tc_ptx.cuh"
@@ -45,7 +47,6 @@ constexpr uint32_t kKK128 = idesc_bf16(128, 128, false, false);   // N = 128, bo
 struct LocalSmem {
     uint8_t qk[4 * kTile];     // [dk half][Q rows 0-63, K rows 64-127][128 B]
     uint8_t v[2 * kTile];      // [dv half][64 rows][128 B]
-    // dO .. dl (128 KB, contiguous) stage dq, dk, dv after wave 3
     uint8_t dO[2 * kTile];     // [dv half][64 rows][128 B]
     uint8_t du[2 * kTile];     // dU^T: [128 rows v][64 chunk rows]
     uint8_t w[2 * kTile];      // W^T: [128 rows k][64 chunk rows]
@@ -56,11 +57,11 @@ struct LocalSmem {
     uint8_t ds[kTile];         // dS rows r
     uint8_t gs[kTile];         // G rows r
     float gam[64], bet[64], ee[64], ff[64];
-    float red[8][32], red2[8][32], red3[8][32];
+    float red[8][32], red2[8][32], red3[8][32], red4[8][32];
     float zrow[2][64], zprow[2][64], dbA[2][64];
     float zcol[64], rowA[64], yw[64], yu[64], zpp[64];
     float hdot[16];            // [0..3]: per-warp parts of <dHL, H0>; [8..15]: block_sum scratch
-    uint64_t tma_bar, mma_bar;
+    uint64_t load_bar[3], mma_bar;  // load groups: {v, dO, dU^T, H0^T, T}, {W^T, u^T, dHL^T}, {q, k}
     uint32_t tmem_base;
 };
 
@@ -131,6 +132,7 @@ struct TcLocalArgs {
     const float *ws_gam;
     void *dq, *dk, *dv;
     float *dg, *dbeta;
+    int n_items;               // chunk capacity x H; item i = (chunk i / H, head i % H)
 };
 
 struct LocalMaps {
@@ -143,6 +145,12 @@ cudaError_t set_smem(F kernel, size_t bytes) {
 }
 }  // namespace
 
+// Persistent: one CTA per SM walks the (chunk, head) items with a stride of
+// the grid.  Each item's tiles arrive in three TMA groups that are issued
+// while the previous item is still computing, each as soon as the regions it
+// fills are dead: {v, dO, dU^T, H0^T, T} after the second epilogue, {W^T, u^T,
+// dHL^T} after the dA product, {q, k} after the last product.
+//
 // 256 threads.  Feature-major results: thread t reads TMEM lane v = t % 128
 // (feature v) and the chunk-row half hs = t / 128 (columns c0 = 32 hs ..
 // +31).  Row-major 64 x 64 results sit on lanes 0-63 (warps 0, 1, 4, 5: row
@@ -154,18 +162,52 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
     extern __shared__ uint8_t smem_raw[];
     LocalSmem &s = *reinterpret_cast<LocalSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, h = blockIdx.y, H = g.H;
-    const int ci = blockIdx.x, v = tid & 127, hs = tid >> 7, c0 = 32 * hs, cq = c0 >> 3;
-    ChunkRef cr;
-    if (!chunk_ref(g, ci, cr)) return;
-    const int L = cr.len;
-    const long long bos = cr.bos;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, H = g.H;
+    const int v = tid & 127, hs = tid >> 7, c0 = 32 * hs, cq = c0 >> 3;
     const float scale = g.scale;
+    const bool tma_thread = tid == 255;
     uint8_t *uT = s.h0T, *dwT = s.h0T + 2 * kTile;    // after wave 1
     uint8_t *dyuT = s.dl, *dywT = s.dl + 2 * kTile;   // after wave 2
 
+    auto item_ref = [&](int i, int &ci, int &hh, ChunkRef &r) -> bool {
+        if (i >= a.n_items) return false;
+        ci = i / H;
+        hh = i % H;
+        return chunk_ref(g, ci, r);
+    };
+    // the three load groups of item (ci, hh) starting at token bos
+    auto load_group = [&](int grp, int ci, int hh, long long bos) {
+        const int tok0 = (int)bos;
+        const int trow = (int)(((long long)ci * H + hh) * kD);
+        uint64_t *bar = &s.load_bar[grp];
+        if (grp == 0) {
+            mbar_arrive_expect_tx(bar, 11 * kTile);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                tma_load_3d(s.v + half * kTile, &m.v, bar, half * 64, hh, tok0);
+                tma_load_3d(s.dO + half * kTile, &m.dO, bar, half * 64, hh, tok0);
+                tma_load_2d(s.h0T + half * 2 * kTile, &m.hc, bar, 0, 2 * trow + half * kD);
+            }
+            tma_load_2d(s.du, &m.du, bar, 0, trow);
+            tma_load_2d(s.tt, &m.t, bar, 0, trow / 2);
+        } else if (grp == 1) {
+            mbar_arrive_expect_tx(bar, 8 * kTile);
+            tma_load_2d(s.w, &m.w, bar, 0, trow);
+            tma_load_2d(s.ut, &m.u, bar, 0, trow);
+            tma_load_2d(s.dl, &m.dhc, bar, 0, 2 * trow);
+            tma_load_2d(s.dl + 2 * kTile, &m.dhc, bar, 0, 2 * trow + kD);
+        } else {
+            mbar_arrive_expect_tx(bar, 4 * kTile);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                tma_load_3d(s.qk + half * 2 * kTile, &m.q, bar, half * 64, hh, tok0);
+                tma_load_3d(s.qk + half * 2 * kTile + kTile, &m.k, bar, half * 64, hh, tok0);
+            }
+        }
+    };
+
     if (tid == 0) {
-        mbar_init(&s.tma_bar, 1);
+        for (int i = 0; i < 3; ++i) mbar_init(&s.load_bar[i], 1);
         mbar_init(&s.mma_bar, 1);
         fence_barrier_init();
     }
@@ -184,351 +226,379 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
     const uint32_t t_dp = tb, t_dkh = tb + 128, t_yw = tb + 256, t_yu = tb + 320;
     const uint32_t t_da = tb + 384;
     const uint32_t t_dk = tb, t_q2 = tb + 448;
-    if (tid == 0) {
-        const int tok0 = (int)bos;
-        const int trow = (int)(((long long)ci * H + h) * kD);
-        mbar_arrive_expect_tx(&s.tma_bar, 23 * kTile);
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            tma_load_3d(s.qk + half * 2 * kTile, &m.q, &s.tma_bar, half * 64, h, tok0);
-            tma_load_3d(s.qk + half * 2 * kTile + kTile, &m.k, &s.tma_bar, half * 64, h, tok0);
-            tma_load_3d(s.v + half * kTile, &m.v, &s.tma_bar, half * 64, h, tok0);
-            tma_load_3d(s.dO + half * kTile, &m.dO, &s.tma_bar, half * 64, h, tok0);
-            tma_load_2d(s.h0T + half * 2 * kTile, &m.hc, &s.tma_bar, 0, 2 * trow + half * kD);
-            tma_load_2d(s.dl + half * 2 * kTile, &m.dhc, &s.tma_bar, 0, 2 * trow + half * kD);
-        }
-        tma_load_2d(s.du, &m.du, &s.tma_bar, 0, trow);
-        tma_load_2d(s.w, &m.w, &s.tma_bar, 0, trow);
-        tma_load_2d(s.ut, &m.u, &s.tma_bar, 0, trow);
-        tma_load_2d(s.tt, &m.t, &s.tma_bar, 0, trow / 2);
-    }
-    if (tid < 64) {
-        const float gm = tid < L ? a.ws_gam[(bos + tid) * H + h] : 0.f;
-        s.gam[tid] = gm;
-        s.bet[tid] = tid < L ? g.beta[(bos + tid) * H + h] : 0.f;
-    }
-    __syncthreads();
-    if (tid < 64) {
-        s.ee[tid] = tid < L ? __expf(s.gam[tid]) : 0.f;
-        s.ff[tid] = tid < L ? __expf(s.gam[L - 1] - s.gam[tid]) : 0.f;
-    }
-    int mma_n = 0;
-    bool tma_pending = true;
-    bool ok = mbar_wait(&s.tma_bar, 0, g.spin_limit, g.status);
-    if (__syncthreads_or(!ok)) goto bail;
-    tma_pending = false;
 
-    // ---------------- wave 1: W H0, [Q; K] K^T, H0^T Q^T, H0 dU^T, H0 dO^T, dHL^T H0
-    ++mma_n;
-    if (warp == 0) {
-        tc_fence_after();
-        const uint32_t qk = smem_u32(s.qk), h0 = smem_u32(s.h0T), w = smem_u32(s.w),
-                       du = smem_u32(s.du), dO = smem_u32(s.dO), dl = smem_u32(s.dl);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t hh = kk >> 2, sub = (kk & 3) * 32;
-            const uint64_t aH = desc_sw128(h0 + hh * 2 * kTile + sub, 16, 1024);
-            const uint64_t aQK = desc_sw128(qk + hh * 2 * kTile + sub, 16, 1024);
-            const uint64_t bK = desc_sw128(qk + hh * 2 * kTile + kTile + sub, 16, 1024);
-            const uint64_t aHm = desc_sw128(h0 + kk * 2048, 2 * kTile, 1024);   // H0, MN-major
-            mma_bf16(t_u, aH, desc_sw128(w + kk * 2048, 2 * kTile, 1024), kKM, kk > 0);
-            mma_bf16(t_p, aQK, bK, kKK, kk > 0);
-            mma_bf16(t_qh, aH, aQK, kKK, kk > 0);
-            mma_bf16(t_dw, aHm, desc_sw128(du + kk * 2048, 2 * kTile, 1024), kMM, kk > 0);
-            mma_bf16(t_q1, aHm, desc_sw128(dO + hh * kTile + sub, 16, 1024), kMK, kk > 0);
-            // dHL^T H0 (128 x 128): its trace is <dHL, H0>
-            mma_bf16(t_hd, desc_sw128(dl + hh * 2 * kTile + sub, 16, 1024), aH, kKK128, kk > 0);
-        }
-        mma_commit(&s.mma_bar);
+    int item = blockIdx.x, ci = 0, h = 0;
+    ChunkRef cr;
+    bool have = item_ref(item, ci, h, cr);
+    int issued[3] = {0, 0, 0};                // loads issued per group (uniform bookkeeping)
+    if (have) {
+        if (tma_thread)
+            for (int grp = 0; grp < 3; ++grp) load_group(grp, ci, h, cr.bos);
+        issued[0] = issued[1] = issued[2] = 1;
     }
-    ok = mbar_wait(&s.mma_bar, 0, g.spin_limit, g.status);
-    if (__syncthreads_or(!ok)) goto bail;
-    tc_fence_after();
-    {
-        // U^T and dW^T = -(H0 dU^T) rows v into the dead H0^T tile; partial sums
-        // of dO[r][v] (Q H0)[r][v] over v for rowA
-#pragma unroll 1
-        for (int q = 0; q < 4; ++q) {
-            float x[8], y[8], uu[8];
-            tmem_ld8(tmem_addr(t_u, warp, c0 + 8 * q), x);
-            tmem_ld8(tmem_addr(t_qh, warp, c0 + 8 * q), y);
-            ld_row8(s.ut, v, cq + q, uu);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int c = c0 + 8 * q + e;
-                x[e] = c < L ? uu[e] - x[e] : 0.f;
-                y[e] = c < L ? ld_bf16(s.dO + (v >> 6) * kTile, c, v & 63) * y[e] : 0.f;
-            }
-            st_row8(uT, v, cq + q, x);
-            warp_sum8(y, s.red[warp] + 8 * q);
-            tmem_ld8(tmem_addr(t_dw, warp, c0 + 8 * q), x);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = (c0 + 8 * q + e) < L ? -x[e] : 0.f;
-            st_row8(dwT, v, cq + q, x);
-        }
-        if (hs == 0) {
-            // lane v's diagonal entry of dHL^T H0 sits in column v of t_hd
-            float x[32];
-            tmem_ld32(tmem_addr(t_hd, warp, 32 * warp), x);
-            float d = 0.f;
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) d = jj == lane ? x[jj] : d;
-            for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-            if (lane == 0) s.hdot[warp] = d;
-        }
+    int it = 0, mma_n = 0;
+    bool bailed = false;
+    float pre_g = 0.f, pre_b = 0.f;           // the next item's gam / beta (threads < 64), read early
+    bool pre = false;
+    while (have) {
+        const int L = cr.len;
+        const long long bos = cr.bos;
+        int ci_n = 0, h_n = 0;
+        ChunkRef cr_n;
+        const bool have_next = item_ref(item + (int)gridDim.x, ci_n, h_n, cr_n);
         tc_fence_before();
-        fence_proxy_async();
-        red_combine(s.rowA, s.red, false);    // its barriers publish U^T, dW^T and hdot
-    }
+        __syncthreads();                          // the previous item's last reads are done
+        if (tid < 64) {
+            s.gam[tid] = pre ? pre_g : (tid < L ? a.ws_gam[(bos + tid) * H + h] : 0.f);
+            s.bet[tid] = pre ? pre_b : (tid < L ? g.beta[(bos + tid) * H + h] : 0.f);
+        }
+        __syncthreads();
+        if (tid < 64) {
+            s.ee[tid] = tid < L ? __expf(s.gam[tid]) : 0.f;
+            s.ff[tid] = tid < L ? __expf(s.gam[L - 1] - s.gam[tid]) : 0.f;
+        }
+        {
+            bool ok = true;
+            for (int grp = 0; grp < 3; ++grp)
+                ok = mbar_wait(&s.load_bar[grp], it & 1, g.spin_limit, g.status) && ok;
+            if (__syncthreads_or(!ok)) { bailed = true; break; }
+        }
+        bool ok;
 
-    // ---------------- wave 2: dO U^T, dHL U^T, T^T dW, T^T dU
-    ++mma_n;
-    if (warp == 0) {
+        // ---------------- wave 1: W H0, [Q; K] K^T, H0^T Q^T, H0 dU^T, H0 dO^T, dHL^T H0
+        ++mma_n;
+        if (warp == 0) {
+            tc_fence_after();
+            const uint32_t qk = smem_u32(s.qk), h0 = smem_u32(s.h0T), w = smem_u32(s.w),
+                           du = smem_u32(s.du), dO = smem_u32(s.dO), dl = smem_u32(s.dl);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t hh = kk >> 2, sub = (kk & 3) * 32;
+                const uint64_t aH = desc_sw128(h0 + hh * 2 * kTile + sub, 16, 1024);
+                const uint64_t aQK = desc_sw128(qk + hh * 2 * kTile + sub, 16, 1024);
+                const uint64_t bK = desc_sw128(qk + hh * 2 * kTile + kTile + sub, 16, 1024);
+                const uint64_t aHm = desc_sw128(h0 + kk * 2048, 2 * kTile, 1024);   // H0, MN-major
+                mma_bf16(t_u, aH, desc_sw128(w + kk * 2048, 2 * kTile, 1024), kKM, kk > 0);
+                mma_bf16(t_p, aQK, bK, kKK, kk > 0);
+                mma_bf16(t_qh, aH, aQK, kKK, kk > 0);
+                mma_bf16(t_dw, aHm, desc_sw128(du + kk * 2048, 2 * kTile, 1024), kMM, kk > 0);
+                mma_bf16(t_q1, aHm, desc_sw128(dO + hh * kTile + sub, 16, 1024), kMK, kk > 0);
+                // dHL^T H0 (128 x 128): its trace is <dHL, H0>
+                mma_bf16(t_hd, desc_sw128(dl + hh * 2 * kTile + sub, 16, 1024), aH, kKK128, kk > 0);
+            }
+            mma_commit(&s.mma_bar);
+        }
+        ok = mbar_wait(&s.mma_bar, 0, g.spin_limit, g.status);
+        if (__syncthreads_or(!ok)) { bailed = true; break; }
         tc_fence_after();
-        const uint32_t dO = smem_u32(s.dO), uTa = smem_u32(uT), dwa = smem_u32(dwT),
-                       dl = smem_u32(s.dl), du = smem_u32(s.du), tt = smem_u32(s.tt);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t hh = kk >> 2, sub = (kk & 3) * 32;
-            const uint64_t bU = desc_sw128(uTa + kk * 2048, kTile, 1024);   // U, MN-major
-            mma_bf16(t_dp, desc_sw128(dO + hh * kTile + sub, 16, 1024), bU, kKM, kk > 0);
-            mma_bf16(t_dkh, desc_sw128(dl + kk * 2048, 2 * kTile, 1024), bU, kMM, kk > 0);
-        }
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t bT = desc_sw128(tt + kk * 32, 16, 1024);
-            mma_bf16(t_yw, desc_sw128(dwa + kk * 32, 16, 1024), bT, kKK, kk > 0);
-            mma_bf16(t_yu, desc_sw128(du + kk * 32, 16, 1024), bT, kKK, kk > 0);
-        }
-        mma_commit(&s.mma_bar);
-    }
-    ok = mbar_wait(&s.mma_bar, 1, g.spin_limit, g.status);
-    if (__syncthreads_or(!ok)) goto bail;
-    tc_fence_after();
-    {
-        // rows r = v < 64: dS and z = dS .* Q K^T (row sums, negated column sums)
-        const bool act = v < 64;
-        const int r = v;
-        if (act) {
-            const float gr = s.gam[r];
-            float zr = 0.f;
+        {
+            // U^T and dW^T = -(H0 dU^T) rows v into the dead H0^T tile; partial sums
+            // of dO[r][v] (Q H0)[r][v] over v for rowA
 #pragma unroll 1
             for (int q = 0; q < 4; ++q) {
-                float dp[8], qk[8], zc[8];
-                tmem_ld8(tmem_addr(t_dp, warp, c0 + 8 * q), dp);
-                tmem_ld8(tmem_addr(t_p, warp, c0 + 8 * q), qk);
+                float x[8], y[8], uu[8];
+                float dw[8];
+                tmem_ld8x3(tmem_addr(t_u, warp, c0 + 8 * q), tmem_addr(t_qh, warp, c0 + 8 * q),
+                           tmem_addr(t_dw, warp, c0 + 8 * q), x, y, dw);
+                ld_row8(s.ut, v, cq + q, uu);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int c = c0 + 8 * q + e;
-                    const float ds =
-                        (c <= r && r < L) ? scale * dp[e] * __expf(gr - s.gam[c]) : 0.f;
-                    const float zz = ds * qk[e];
-                    zr += zz;
-                    zc[e] = -zz;
-                    dp[e] = ds;
+                    x[e] = c < L ? uu[e] - x[e] : 0.f;
+                    y[e] = c < L ? ld_bf16(s.dO + (v >> 6) * kTile, c, v & 63) * y[e] : 0.f;
                 }
-                st_row8(s.ds, r, cq + q, dp);
-                warp_sum8(zc, s.red[warp] + 8 * q);
-            }
-            s.zrow[hs][r] = zr;
-        } else {
-            s.red[warp][lane] = 0.f;
-        }
-        // every feature f = v: dYw^T, dYu^T rows into the dead dHL^T tiles, and
-        // sums over f of dYw .* K (yw) and dYu .* V (yu)
-        const uint8_t *krow = s.qk + (v >> 6) * 2 * kTile + kTile;
-        const uint8_t *vrow = s.v + (v >> 6) * kTile;
-#pragma unroll 1
-        for (int q = 0; q < 4; ++q) {
-            float yw[8], yu[8];
-            tmem_ld8(tmem_addr(t_yw, warp, c0 + 8 * q), yw);
-            tmem_ld8(tmem_addr(t_yu, warp, c0 + 8 * q), yu);
-            st_row8(dywT, v, cq + q, yw);
-            st_row8(dyuT, v, cq + q, yu);
+                st_row8(uT, v, cq + q, x);
+                warp_sum8(y, s.red[warp] + 8 * q);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int c = c0 + 8 * q + e;
-                yw[e] = c < L ? yw[e] * ld_bf16(krow, c, v & 63) : 0.f;
-                yu[e] = c < L ? yu[e] * ld_bf16(vrow, c, v & 63) : 0.f;
+                for (int e = 0; e < 8; ++e) dw[e] = (c0 + 8 * q + e) < L ? -dw[e] : 0.f;
+                st_row8(dwT, v, cq + q, dw);
             }
-            warp_sum8(yw, s.red2[warp] + 8 * q);
-            warp_sum8(yu, s.red3[warp] + 8 * q);
+            if (hs == 0) {
+                // lane v's diagonal entry of dHL^T H0 sits in column v of t_hd
+                float x[32];
+                tmem_ld32(tmem_addr(t_hd, warp, 32 * warp), x);
+                float d = 0.f;
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) d = jj == lane ? x[jj] : d;
+                for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+                if (lane == 0) s.hdot[warp] = d;
+            }
+            tc_fence_before();
+            fence_proxy_async();
+            red_combine(s.rowA, s.red, false);    // its barriers publish U^T, dW^T and hdot
         }
-        tc_fence_before();
-        fence_proxy_async();
-        __syncthreads();
-        if (tid < 64) {
-            s.zcol[tid] = quad_sum(s.red, tid);
-            s.yw[tid] = quad_sum(s.red2, tid);
-            s.yu[tid] = quad_sum(s.red3, tid);
-        }
-        __syncthreads();
-    }
 
-    // ---------------- wave 2.5: dA = -(dYu u^T + dYw W^T), rows duplicated on lanes 64-127
-    ++mma_n;
-    if (warp == 0) {
-        tc_fence_after();
-        const uint32_t yu = smem_u32(dyuT), yw = smem_u32(dywT), ua = smem_u32(s.ut),
-                       wa = smem_u32(s.w);
+        // ---------------- wave 2: dO U^T, dHL U^T, T^T dW, T^T dU
+        ++mma_n;
+        if (warp == 0) {
+            tc_fence_after();
+            const uint32_t dO = smem_u32(s.dO), uTa = smem_u32(uT), dwa = smem_u32(dwT),
+                           dl = smem_u32(s.dl), du = smem_u32(s.du), tt = smem_u32(s.tt);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-            mma_bf16(t_da, desc_sw128(yu + kk * 2048, 0, 1024),
-                     desc_sw128(ua + kk * 2048, kTile, 1024), kMM, kk > 0);
-            mma_bf16(t_da, desc_sw128(yw + kk * 2048, 0, 1024),
-                     desc_sw128(wa + kk * 2048, kTile, 1024), kMM, 1);
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t hh = kk >> 2, sub = (kk & 3) * 32;
+                const uint64_t bU = desc_sw128(uTa + kk * 2048, kTile, 1024);   // U, MN-major
+                mma_bf16(t_dp, desc_sw128(dO + hh * kTile + sub, 16, 1024), bU, kKM, kk > 0);
+                mma_bf16(t_dkh, desc_sw128(dl + kk * 2048, 2 * kTile, 1024), bU, kMM, kk > 0);
+            }
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t bT = desc_sw128(tt + kk * 32, 16, 1024);
+                mma_bf16(t_yw, desc_sw128(dwa + kk * 32, 16, 1024), bT, kKK, kk > 0);
+                mma_bf16(t_yu, desc_sw128(du + kk * 32, 16, 1024), bT, kKK, kk > 0);
+            }
+            mma_commit(&s.mma_bar);
         }
-        mma_commit(&s.mma_bar);
-    }
-    ok = mbar_wait(&s.mma_bar, 0, g.spin_limit, g.status);
-    if (__syncthreads_or(!ok)) goto bail;
-    tc_fence_after();
-    {
-        // rows r = v - 64 (lanes 64-127): G = dA .* D .* beta_r, z' = G .* K K^T and
-        // the dA part of dbeta
-        const bool act = v >= 64;
-        const int r = v - 64;
-        if (act) {
-            const float gr = s.gam[r], br = s.bet[r];
-            float zpr = 0.f, dba = 0.f;
+        ok = mbar_wait(&s.mma_bar, 1, g.spin_limit, g.status);
+        if (__syncthreads_or(!ok)) { bailed = true; break; }
+        tc_fence_after();
+        {
+            // rows r = v < 64: dS and z = dS .* Q K^T (row sums, negated column sums)
+            const bool act = v < 64;
+            const int r = v;
+            if (act) {
+                const float gr = s.gam[r];
+                float zr = 0.f;
+#pragma unroll 1
+                for (int q = 0; q < 4; ++q) {
+                    float dp[8], qk[8], zc[8];
+                    tmem_ld8x2(tmem_addr(t_dp, warp, c0 + 8 * q), tmem_addr(t_p, warp, c0 + 8 * q),
+                               dp, qk);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int c = c0 + 8 * q + e;
+                        const float ds =
+                            (c <= r && r < L) ? scale * dp[e] * __expf(gr - s.gam[c]) : 0.f;
+                        const float zz = ds * qk[e];
+                        zr += zz;
+                        zc[e] = -zz;
+                        dp[e] = ds;
+                    }
+                    st_row8(s.ds, r, cq + q, dp);
+                    warp_sum8(zc, s.red[warp] + 8 * q);
+                }
+                s.zrow[hs][r] = zr;
+            } else {
+                s.red[warp][lane] = 0.f;
+            }
+            // every feature f = v: dYw^T, dYu^T rows into the dead dHL^T tiles, and
+            // sums over f of dYw .* K (yw) and dYu .* V (yu)
+            const uint8_t *krow = s.qk + (v >> 6) * 2 * kTile + kTile;
+            const uint8_t *vrow = s.v + (v >> 6) * kTile;
+            // dV = diag(beta) dYu leaves now; a warp's lanes write 32 consecutive features
+            TG *dv = (TG *)a.dv + (bos * H + h) * (long long)kD + v;
 #pragma unroll 1
             for (int q = 0; q < 4; ++q) {
-                float da[8], kk[8], zc[8];
-                tmem_ld8(tmem_addr(t_da, warp, c0 + 8 * q), da);
-                tmem_ld8(tmem_addr(t_p, warp, c0 + 8 * q), kk);
+                float yw[8], yu[8], pz[8];
+                tmem_ld8x3(tmem_addr(t_yw, warp, c0 + 8 * q), tmem_addr(t_yu, warp, c0 + 8 * q),
+                           tmem_addr(t_dkh, warp, c0 + 8 * q), yw, yu, pz);
+                st_row8(dywT, v, cq + q, yw);
+                st_row8(dyuT, v, cq + q, yu);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int c = c0 + 8 * q + e;
-                    const bool low = c < r && r < L;
-                    const float d_rc = low ? __expf(gr - s.gam[c]) : 0.f;
-                    const float dA = -da[e] * d_rc;     // dA .* D on the strict lower part
-                    const float g_rc = dA * br;
-                    const float zz = g_rc * kk[e];
-                    zpr += zz;
-                    zc[e] = -zz;
-                    dba += dA * kk[e];
-                    da[e] = g_rc;
+                    if (c < L) from_f(dv + (long long)c * H * kD, s.bet[c] * yu[e]);
+                    const float kv = c < L ? ld_bf16(krow, c, v & 63) : 0.f;
+                    yw[e] *= kv;
+                    yu[e] = c < L ? yu[e] * ld_bf16(vrow, c, v & 63) : 0.f;
+                    pz[e] *= s.ff[c] * kv;           // (diag(f) U dHL^T) .* K, summed over k below
                 }
-                st_row8(s.gs, r, cq + q, da);
-                warp_sum8(zc, s.red[warp] + 8 * q);
+                warp_sum8(yw, s.red2[warp] + 8 * q);
+                warp_sum8(yu, s.red3[warp] + 8 * q);
+                warp_sum8(pz, s.red4[warp] + 8 * q);
             }
-            s.zprow[hs][r] = zpr;
-            s.dbA[hs][r] = dba;
-        } else {
-            s.red[warp][lane] = 0.f;
+            tc_fence_before();
+            fence_proxy_async();
+            __syncthreads();
+            if (tid < 64) {
+                s.zcol[tid] = quad_sum(s.red, tid);
+                s.yw[tid] = quad_sum(s.red2, tid);
+                s.yu[tid] = quad_sum(s.red3, tid);
+                s.zpp[tid] = quad_sum(s.red4, tid);
+            }
+            __syncthreads();
         }
-        tc_fence_before();
-        fence_proxy_async();
-        red_combine(s.zcol, s.red, true);
+        // v, dO, dU^T, the H0^T / U^T / dW^T tile and T are dead: next item's group 0
+        if (have_next) {
+            if (tma_thread) {
+                fence_proxy_async();
+                load_group(0, ci_n, h_n, cr_n.bos);
+            }
+            ++issued[0];
+        }
+
+        // ---------------- wave 2.5: dA = -(dYu u^T + dYw W^T), rows duplicated on lanes 64-127
+        ++mma_n;
+        if (warp == 0) {
+            tc_fence_after();
+            const uint32_t yu = smem_u32(dyuT), yw = smem_u32(dywT), ua = smem_u32(s.ut),
+                           wa = smem_u32(s.w);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                mma_bf16(t_da, desc_sw128(yu + kk * 2048, 0, 1024),
+                         desc_sw128(ua + kk * 2048, kTile, 1024), kMM, kk > 0);
+                mma_bf16(t_da, desc_sw128(yw + kk * 2048, 0, 1024),
+                         desc_sw128(wa + kk * 2048, kTile, 1024), kMM, 1);
+            }
+            mma_commit(&s.mma_bar);
+        }
+        ok = mbar_wait(&s.mma_bar, 0, g.spin_limit, g.status);
+        if (__syncthreads_or(!ok)) { bailed = true; break; }
+        // W^T, u^T and the dHL^T / dYu^T / dYw^T tiles are dead: next item's group 1
+        if (have_next) {
+            if (tma_thread) {
+                fence_proxy_async();
+                load_group(1, ci_n, h_n, cr_n.bos);
+            }
+            ++issued[1];
+        }
+        tc_fence_after();
+        {
+            // rows r = v - 64 (lanes 64-127): G = dA .* D .* beta_r, z' = G .* K K^T and
+            // the dA part of dbeta
+            const bool act = v >= 64;
+            const int r = v - 64;
+            if (act) {
+                const float gr = s.gam[r], br = s.bet[r];
+                float zpr = 0.f, dba = 0.f;
+#pragma unroll 1
+                for (int q = 0; q < 4; ++q) {
+                    float da[8], kk[8], zc[8];
+                    tmem_ld8x2(tmem_addr(t_da, warp, c0 + 8 * q), tmem_addr(t_p, warp, c0 + 8 * q),
+                               da, kk);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int c = c0 + 8 * q + e;
+                        const bool low = c < r && r < L;
+                        const float d_rc = low ? __expf(gr - s.gam[c]) : 0.f;
+                        const float dA = -da[e] * d_rc;     // dA .* D on the strict lower part
+                        const float g_rc = dA * br;
+                        const float zz = g_rc * kk[e];
+                        zpr += zz;
+                        zc[e] = -zz;
+                        dba += dA * kk[e];
+                        da[e] = g_rc;
+                    }
+                    st_row8(s.gs, r, cq + q, da);
+                    warp_sum8(zc, s.red[warp] + 8 * q);
+                }
+                s.zprow[hs][r] = zpr;
+                s.dbA[hs][r] = dba;
+            } else {
+                s.red[warp][lane] = 0.f;
+            }
+            tc_fence_before();
+            fence_proxy_async();
+            red_combine(s.zcol, s.red, true);
+        }
+
+        // ---------------- wave 3: dS K, dS^T Q + (G + G^T) K
+        ++mma_n;
+        if (warp == 0) {
+            tc_fence_after();
+            const uint32_t qk = smem_u32(s.qk), ds = smem_u32(s.ds), gs = smem_u32(s.gs);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t aK = desc_sw128(qk + kTile + kk * 2048, 2 * kTile, 1024);   // K, MN-major
+                const uint64_t aQ = desc_sw128(qk + kk * 2048, 2 * kTile, 1024);           // Q, MN-major
+                mma_bf16(t_q2, aK, desc_sw128(ds + kk * 32, 16, 1024), kMK, kk > 0);
+                mma_bf16(t_dk, aQ, desc_sw128(ds + kk * 2048, kTile, 1024), kMM, kk > 0);
+                mma_bf16(t_dk, aK, desc_sw128(gs + kk * 32, 16, 1024), kMK, 1);         // G K
+                mma_bf16(t_dk, aK, desc_sw128(gs + kk * 2048, kTile, 1024), kMM, 1);    // G^T K
+            }
+            mma_commit(&s.mma_bar);
+        }
+        ok = mbar_wait(&s.mma_bar, 1, g.spin_limit, g.status);
+        if (__syncthreads_or(!ok)) { bailed = true; break; }
+        // q, k are dead (their last reader was wave 3): next item's group 2
+        if (have_next) {
+            if (tma_thread) {
+                fence_proxy_async();
+                load_group(2, ci_n, h_n, cr_n.bos);
+            }
+            ++issued[2];
+            if (tid < 64) {
+                pre_g = tid < cr_n.len ? a.ws_gam[(cr_n.bos + tid) * H + h_n] : 0.f;
+                pre_b = tid < cr_n.len ? g.beta[(cr_n.bos + tid) * H + h_n] : 0.f;
+            }
+        }
+        pre = have_next;
+        tc_fence_after();
+        {
+            // feature v (= k), chunk rows c0 .. c0+31: a warp's lanes write 32
+            // consecutive features of one row per store
+            const long long rs = (long long)H * kD;
+            TG *dq = (TG *)a.dq + (bos * H + h) * (long long)kD + v;
+            TG *dk = (TG *)a.dk + (bos * H + h) * (long long)kD + v;
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+                float x[8], y[8], pw[8];
+                tmem_ld8x2(tmem_addr(t_q1, warp, c0 + 8 * q), tmem_addr(t_q2, warp, c0 + 8 * q),
+                           x, y);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int c = c0 + 8 * q + e;
+                    if (c < L) from_f(dq + c * rs, scale * s.ee[c] * x[e] + y[e]);
+                }
+                tmem_ld8x3(tmem_addr(t_dk, warp, c0 + 8 * q), tmem_addr(t_dkh, warp, c0 + 8 * q),
+                           tmem_addr(t_yw, warp, c0 + 8 * q), x, y, pw);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int c = c0 + 8 * q + e;
+                    if (c < L)
+                        from_f(dk + c * rs, x[e] + s.ff[c] * y[e] + s.bet[c] * s.ee[c] * pw[e]);
+                }
+            }
+        }
+        {
+            const float zsum = block_sum(tid < 64 ? s.zpp[tid] : 0.f, s.hdot + 8);
+            if (tid < 64) {
+                const int r = tid;
+                float dgam = 0.f;
+                if (r < L) {
+                    dgam = s.zrow[0][r] + s.zrow[1][r] + s.zprow[0][r] + s.zprow[1][r] + s.zcol[r] +
+                           s.bet[r] * s.ee[r] * s.yw[r] + scale * s.ee[r] * s.rowA[r] - s.zpp[r];
+                    if (r == L - 1)
+                        dgam += zsum + s.ee[r] * (s.hdot[0] + s.hdot[1] + s.hdot[2] + s.hdot[3]);
+                    a.dbeta[(bos + r) * H + h] = s.yu[r] + s.ee[r] * s.yw[r] + s.dbA[0][r] + s.dbA[1][r];
+                }
+                s.red[r >> 5][r & 31] = dgam;
+            }
+            __syncthreads();
+            if (tid < 64) {
+                // dg = reverse cumsum of dgam within the chunk (warp scans over 2 x 32)
+                const int w = tid >> 5;
+                float x = s.red[1 - w][31 - lane];          // reversed order: position p = 63 - r
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float yv = __shfl_up_sync(0xffffffffu, x, o);
+                    if (lane >= o) x += yv;
+                }
+                s.red[2 + w][lane] = x;
+            }
+            __syncthreads();
+            if (tid < 64) {
+                const int pidx = tid;                        // position in reversed order
+                const int r = 63 - pidx;
+                float x = s.red[2 + (pidx >> 5)][pidx & 31];
+                if (pidx >= 32) x += s.red[2][31];
+                if (r < L) a.dg[(bos + r) * H + h] = x;
+            }
+        }
+        item += (int)gridDim.x;
+        ci = ci_n;
+        h = h_n;
+        cr = cr_n;
+        have = have_next;
+        ++it;
     }
 
-    // ---------------- wave 3: dS K, dS^T Q + (G + G^T) K
-    ++mma_n;
-    if (warp == 0) {
-        tc_fence_after();
-        const uint32_t qk = smem_u32(s.qk), ds = smem_u32(s.ds), gs = smem_u32(s.gs);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t aK = desc_sw128(qk + kTile + kk * 2048, 2 * kTile, 1024);   // K, MN-major
-            const uint64_t aQ = desc_sw128(qk + kk * 2048, 2 * kTile, 1024);           // Q, MN-major
-            mma_bf16(t_q2, aK, desc_sw128(ds + kk * 32, 16, 1024), kMK, kk > 0);
-            mma_bf16(t_dk, aQ, desc_sw128(ds + kk * 2048, kTile, 1024), kMM, kk > 0);
-            mma_bf16(t_dk, aK, desc_sw128(gs + kk * 32, 16, 1024), kMK, 1);         // G K
-            mma_bf16(t_dk, aK, desc_sw128(gs + kk * 2048, kTile, 1024), kMM, 1);    // G^T K
-        }
-        mma_commit(&s.mma_bar);
-    }
-    ok = mbar_wait(&s.mma_bar, 1, g.spin_limit, g.status);
-    if (__syncthreads_or(!ok)) goto bail;
-    tc_fence_after();
-    {
-        // feature v (= k for dq, dk; = v for dv), chunk rows c0 .. c0+31, staged as
-        // row-major [3][64 rows][128] in the dead tiles, then written out in 16-byte rows
-        TG *stg = reinterpret_cast<TG *>(s.dO);
-        const uint8_t *krow = s.qk + (v >> 6) * 2 * kTile + kTile;
-#pragma unroll 1
-        for (int q = 0; q < 4; ++q) {
-            float x[8], y[8], pw[8], pz[8];
-            tmem_ld8(tmem_addr(t_q1, warp, c0 + 8 * q), x);
-            tmem_ld8(tmem_addr(t_q2, warp, c0 + 8 * q), y);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int c = c0 + 8 * q + e;
-                from_f(stg + c * kD + v, scale * s.ee[c] * x[e] + y[e]);
-            }
-            tmem_ld8(tmem_addr(t_dk, warp, c0 + 8 * q), x);
-            tmem_ld8(tmem_addr(t_dkh, warp, c0 + 8 * q), y);
-            tmem_ld8(tmem_addr(t_yw, warp, c0 + 8 * q), pw);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int c = c0 + 8 * q + e;
-                const float kv = c < L ? ld_bf16(krow, c, v & 63) : 0.f;
-                const float dkh = s.ff[c] * y[e];
-                from_f(stg + (64 + c) * kD + v, x[e] + dkh + s.bet[c] * s.ee[c] * pw[e]);
-                pz[e] = dkh * kv;
-            }
-            warp_sum8(pz, s.red[warp] + 8 * q);
-            tmem_ld8(tmem_addr(t_yu, warp, c0 + 8 * q), y);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int c = c0 + 8 * q + e;
-                from_f(stg + (128 + c) * kD + v, s.bet[c] * y[e]);
-            }
-        }
-        red_combine(s.zpp, s.red, false);     // its barriers also publish the staged rows
-        constexpr int kVec = 16 / sizeof(TG), kPerRow = kD / kVec;
-#pragma unroll 1
-        for (int o = 0; o < 3; ++o) {
-            TG *out = (TG *)(o == 0 ? a.dq : o == 1 ? a.dk : a.dv) + (bos * H + h) * (long long)kD;
-            for (int i = tid; i < L * kPerRow; i += 256) {
-                const int r = i / kPerRow, q = i % kPerRow;
-                *reinterpret_cast<uint4 *>(out + (long long)r * H * kD + q * kVec) =
-                    *reinterpret_cast<const uint4 *>(stg + (o * 64 + r) * kD + q * kVec);
-            }
-        }
-    }
-    {
-        const float zsum = block_sum(tid < 64 ? s.zpp[tid] : 0.f, s.hdot + 8);
-        if (tid < 64) {
-            const int r = tid;
-            float dgam = 0.f;
-            if (r < L) {
-                dgam = s.zrow[0][r] + s.zrow[1][r] + s.zprow[0][r] + s.zprow[1][r] + s.zcol[r] +
-                       s.bet[r] * s.ee[r] * s.yw[r] + scale * s.ee[r] * s.rowA[r] - s.zpp[r];
-                if (r == L - 1)
-                    dgam += zsum + s.ee[r] * (s.hdot[0] + s.hdot[1] + s.hdot[2] + s.hdot[3]);
-                a.dbeta[(bos + r) * H + h] = s.yu[r] + s.ee[r] * s.yw[r] + s.dbA[0][r] + s.dbA[1][r];
-            }
-            s.red[r >> 5][r & 31] = dgam;
-        }
-        __syncthreads();
-        if (tid < 64) {
-            // dg = reverse cumsum of dgam within the chunk (warp scans over 2 x 32)
-            const int w = tid >> 5;
-            float x = s.red[1 - w][31 - lane];          // reversed order: position p = 63 - r
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float yv = __shfl_up_sync(0xffffffffu, x, o);
-                if (lane >= o) x += yv;
-            }
-            s.red[2 + w][lane] = x;
-        }
-        __syncthreads();
-        if (tid < 64) {
-            const int pidx = tid;                        // position in reversed order
-            const int r = 63 - pidx;
-            float x = s.red[2 + (pidx >> 5)][pidx & 31];
-            if (pidx >= 32) x += s.red[2][31];
-            if (r < L) a.dg[(bos + r) * H + h] = x;
-        }
-    }
-    goto done;
-bail:
-    if (tid == 0) {
-        if (tma_pending) mbar_drain(&s.tma_bar, 0);
+    if (bailed && tid == 0) {
+        // loads of this item (issued, not yet seen) or of the next one, and the last MMA phase
+        for (int grp = 0; grp < 3; ++grp)
+            if (issued[grp] > 0) mbar_drain(&s.load_bar[grp], (issued[grp] - 1) & 1);
         if (mma_n > 0) mbar_drain(&s.mma_bar, (mma_n - 1) & 1);
     }
-done:
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tb, 512);
@@ -558,8 +628,9 @@ cudaError_t local_grads(const Plan &p, cudaStream_t s) {
     a.dv = p.dv;
     a.dg = p.dg;
     a.dbeta = p.dbeta;
+    a.n_items = p.max_chunks * g.H;
     const size_t smem = sizeof(LocalSmem) + 1024;
-    const dim3 grid(p.max_chunks, g.H);
+    const dim3 grid(std::min(a.n_items, std::max(p.sms, 1)));
     prof_before("tc_local_grad", s);
     if (p.grad_dtype == GDN_BF16) {
         if ((e = set_smem(tc_local_kernel<__nv_bfloat16>, smem)) != cudaSuccess) return e;
