@@ -348,7 +348,6 @@ tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
         const long long bos = sbos + (long long)c * kChunk;
         const int L = min(kChunk, slen - c * kChunk);
         const int trow = (int)(((long long)(cbase + c) * H + h) * kD);
-        float gnext = 0.f;                     // gam of chunk c - 1, stored at the end
         pend = 0;
         if (c - 1 >= c0) {
             if (tma_thread) {
@@ -356,7 +355,8 @@ tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
                 issue_tma(st ^ 1, c - 1);
             }
             tma_pending |= 1 << (st ^ 1);
-            if (tid < 64) gnext = a.ws_gam[(bos - kChunk + tid) * H + h];   // a full chunk
+            // gam of chunk c - 1 (a full chunk) into the other buffer, asynchronously
+            if (tid < 64) cp_async4(&s.gam[st ^ 1][tid], a.ws_gam + (bos - kChunk + tid) * H + h, true);
         }
         if (MODE == kDOut && tma_thread) {
             // the gradient at this chunk's end: the bf16 dH^T tile, by TMA
@@ -407,11 +407,12 @@ tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
         if (__syncthreads_or(!ok)) { bailed = true; break; }
         pend = 0;
         tc_fence_after();
-        // dU^T row v, chunk rows 32*hs .. +31 in rolled groups of 8: Y^T + X^T diag(f)
-#pragma unroll 1
+        // dU^T row v, chunk rows 32*hs .. +31 (one TMEM load, groups of 8): Y^T + X^T diag(f)
+        float xs[32];
+        tmem_ld32(tmem_addr(t_x, warp, 32 * hs), xs);
+#pragma unroll
         for (int q = 0; q < 4; ++q) {
-            float x[8];
-            tmem_ld8(tmem_addr(t_x, warp, 32 * hs + 8 * q), x);
+            float *x = xs + 8 * q;
             const int chunk = 4 * hs + q;
             uint4 raw = make_uint4(0u, 0u, 0u, 0u);
             if (use_do)
@@ -458,13 +459,14 @@ tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
             }
         }
         st_row64(s.dhT + hs * 2 * kTile, v, dH);
-        if (tid < 64) s.gam[st ^ 1][tid] = gnext;
+        if (tid < 64) cp_async_wait_all();
         tc_fence_before();
         fence_proxy_async();
         __syncthreads();
     }
 
     if (tma_thread) bulk_wait_all();
+    if (tid < 64) cp_async_wait_all();    // a gam prefetch may still be in flight after a bail
     if (bailed) {
         if (tid == 0) {
             for (int st = 0; st < 2; ++st)

@@ -271,16 +271,18 @@ done:
 // ------------------------------------------------------------------ walk
 // The walk carries only the state recurrence; outputs come from the
 // chunk-parallel output kernel, which reads the chunk start states it stores.
+constexpr int kWalkStages = 3;    // chunks in flight: the current one and two prefetched
+
 struct WalkSmem {
-    uint8_t k[2][2 * kTile];       // per stage: K, [dk half][64 chunk rows][128 B]
-    uint8_t w[2][2 * kTile];       // per stage: W^T, [128 rows k][64 chunk rows]
-    uint8_t u[2][2 * kTile];       // per stage: u^T, [128 rows v][64 chunk rows]
+    uint8_t k[kWalkStages][2 * kTile];   // per stage: K, [dk half][64 chunk rows][128 B]
+    uint8_t w[kWalkStages][2 * kTile];   // per stage: W^T, [128 rows k][64 chunk rows]
+    uint8_t u[kWalkStages][2 * kTile];   // per stage: u^T, [128 rows v][64 chunk rows]
     uint8_t hT[4 * kTile];         // [dk half][128 state rows][128 B]  (A operand)
     uint8_t uTs[2 * kTile];        // U^T diag(f): [128 state rows][64 chunk rows] (A operand)
     float gam[2][64];
     float fr[64];                  // exp(gam_L - gam_r) (x 1/|k_r|); 0 past L
     float rk[64];
-    uint64_t tma_bar[2], bar_u, bar_dh;
+    uint64_t tma_bar[kWalkStages], bar_u, bar_dh;
     uint32_t tmem_base;
 };
 
@@ -341,8 +343,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     }
 
     if (tid == 0) {
-        mbar_init(&s.tma_bar[0], 1);
-        mbar_init(&s.tma_bar[1], 1);
+        for (int i = 0; i < kWalkStages; ++i) mbar_init(&s.tma_bar[i], 1);
         mbar_init(&s.bar_u, 1);
         mbar_init(&s.bar_dh, 1);
         fence_barrier_init();
@@ -391,28 +392,44 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
 
     // one commit per barrier per chunk: every barrier's parity is the chunk
     // iteration's; `pend` marks groups committed in this iteration, not yet waited
-    int it = 0, tma_pending = 0, pend = 0;   // uniform bookkeeping for the bail-out path
+    // uniform bookkeeping for the bail-out path: loads issued per stage, and
+    // the stages whose latest load has not been waited for
+    int it = 0, tma_pending = 0, pend = 0;
+    unsigned loaded = 0, ld_par = 0;   // per stage: loaded at least once; parity of its latest load
+    auto note_load = [&](int sn) {
+        if (loaded & (1u << sn)) ld_par ^= 1u << sn;
+        loaded |= 1u << sn;
+        tma_pending |= 1 << sn;
+    };
     bool bailed = false;
     // the last warp issues the loads, away from warp 0 (MMA issue) and the
     // threads that read gam
     const bool tma_thread = tid == 255;
-    if (tma_thread && cstart < c1) issue_tma(0, cstart);
-    if (cstart < c1) tma_pending |= 1;
+    for (int i = 0; i < kWalkStages - 1 && cstart + i < c1; ++i) {
+        if (tma_thread) issue_tma(i, cstart + i);
+        note_load(i);
+    }
     for (int c = cstart; c < c1; ++c, ++it) {
-        const int st = it & 1;
+        const int st = it % kWalkStages, gb = it & 1;
         const uint32_t par = it & 1;
         const long long bos = sbos + (long long)c * kChunk;
         const int L = min(kChunk, slen - c * kChunk);
-        float gnext = 0.f;                     // gam of the next chunk, stored at the end
         pend = 0;
-        if (c + 1 < c1) {
+        if (c + kWalkStages - 1 < c1) {
+            // the stage the previous chunk used takes the chunk two ahead
+            const int sn = (it + kWalkStages - 1) % kWalkStages;
             if (tma_thread) {
                 fence_proxy_async();
-                issue_tma(st ^ 1, c + 1);
+                issue_tma(sn, c + kWalkStages - 1);
             }
-            tma_pending |= 1 << (st ^ 1);
+            note_load(sn);
+        }
+        if (c + 1 < c1) {
             const int Ln = min(kChunk, slen - (c + 1) * kChunk);
-            if (tid < 64 && tid < Ln) gnext = a.ws_gam[(bos + kChunk + tid) * H + h];
+            // gam of the next chunk into the other buffer, asynchronously
+            if (tid < 64)
+                cp_async4(&s.gam[gb ^ 1][tid], a.ws_gam + (bos + kChunk + min(tid, Ln - 1)) * H + h,
+                          tid < Ln);
         }
         if (states && c >= c0 && tma_thread) {
             // the chunk's start state: the bf16 H^T tile in shared memory, by TMA
@@ -421,7 +438,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             tma_store_2d(&tm_hc, s.hT + 2 * kTile, 0, row + kD);
             bulk_commit();
         }
-        bool ok = mbar_wait(&s.tma_bar[st], (it >> 1) & 1, g.spin_limit, g.status);
+        bool ok = mbar_wait(&s.tma_bar[st], (it / kWalkStages) & 1, g.spin_limit, g.status);
         if (__syncthreads_or(!ok)) { bailed = true; break; }
         tma_pending &= ~(1 << st);
         if (warp == 0) {
@@ -451,18 +468,19 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         }
         if (g.l2norm) __syncthreads();
         if (tid < 64) {
-            const float gl = s.gam[st][L - 1], gr = s.gam[st][tid];
+            const float gl = s.gam[gb][L - 1], gr = s.gam[gb][tid];
             s.fr[tid] = tid < L ? __expf(gl - gr) * (g.l2norm ? s.rk[tid] : 1.f) : 0.f;
         }
         ok = mbar_wait(&s.bar_u, par, g.spin_limit, g.status);
         if (__syncthreads_or(!ok)) { bailed = true; break; }
         pend = 0;
         tc_fence_after();
-        // U^T diag(f) rows v, chunk rows 32*hs .. +31 in rolled groups of 8
-#pragma unroll 1
+        // U^T diag(f) rows v, chunk rows 32*hs .. +31 (one TMEM load, groups of 8)
+        float xu[32];
+        tmem_ld32(tmem_addr(t_u, warp, 32 * hs), xu);
+#pragma unroll
         for (int q = 0; q < 4; ++q) {
-            float x[8], uu[8];
-            tmem_ld8(tmem_addr(t_u, warp, 32 * hs + 8 * q), x);
+            float *x = xu + 8 * q, uu[8];
             const int chunk = 4 * hs + q;
             uint4 raw = make_uint4(0u, 0u, 0u, 0u);
             if (!a_cols)
@@ -496,7 +514,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         pend = 0;
         tc_fence_after();
         {
-            const float el = __expf(s.gam[st][L - 1]);
+            const float el = __expf(s.gam[gb][L - 1]);
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
                 float d[32];
@@ -506,18 +524,18 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             }
         }
         st_row64(s.hT + hs * 2 * kTile, v, Hr);
-        if (tid < 64) s.gam[st ^ 1][tid] = gnext;
+        if (tid < 64) cp_async_wait_all();
         tc_fence_before();
         fence_proxy_async();
         __syncthreads();
     }
 
     if (tma_thread) bulk_wait_all();
+    if (tid < 64) cp_async_wait_all();    // a gam prefetch may still be in flight after a bail
     if (bailed) {
         if (tid == 0) {
-            for (int st = 0; st < 2; ++st)
-                if (tma_pending & (1 << st))
-                    mbar_drain(&s.tma_bar[st], ((it + (st != (it & 1))) >> 1) & 1);
+            for (int st = 0; st < kWalkStages; ++st)
+                if (tma_pending & (1 << st)) mbar_drain(&s.tma_bar[st], (ld_par >> st) & 1u);
             if (pend & 1) mbar_drain(&s.bar_u, it & 1);
             if (pend & 2) mbar_drain(&s.bar_dh, it & 1);
         }
