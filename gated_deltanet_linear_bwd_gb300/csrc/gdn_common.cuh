@@ -18,6 +18,15 @@ namespace gdn {
 
 constexpr int kChunk = 64;
 
+// Kernels launched with programmatic stream serialization start while the
+// previous kernel on the stream is still running: each lets its own
+// dependents launch at once, then waits for its predecessor's grid (and its
+// memory) before touching anything in global memory.
+__device__ __forceinline__ void pdl_enter() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Everything a kernel needs to locate a sequence, chunk or segment and to
 // read the inputs.  Passed by value.
 struct Geo {

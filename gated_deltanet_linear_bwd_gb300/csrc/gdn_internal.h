@@ -64,6 +64,25 @@ enum { kPathSimt = 0, kPathTc = 1 };
 void prof_before(const char *name, cudaStream_t s);
 void prof_after(cudaStream_t s);
 
+// Launches `kernel` with programmatic stream serialization: it may start while
+// the previous kernel on the stream is finishing.  Only for kernels that call
+// pdl_enter() before their first global memory access.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 namespace simt {
 // Per-CTA scratch floats of the local-gradient kernel.
 size_t scratch_floats_per_cta(int K, int V);

@@ -311,6 +311,7 @@ __device__ __forceinline__ void cp_async_wait() {
 __global__ void __launch_bounds__(256)
 map_scan_kernel(Geo g, const float *maps, const float *init, const int32_t *warm, float *out,
                 int reverse) {
+    pdl_enter();
     const int n = blockIdx.x, h = blockIdx.y, col0 = blockIdx.z * kSB, K = g.K, V = g.V,
               H = g.H;
     if (n >= g.N || col0 >= V) return;
@@ -925,6 +926,20 @@ static size_t local_smem(int K) {
         if (e_ != cudaSuccess) return e_;                                                    \
     } while (0)
 
+// Same with programmatic stream serialization, for kernels that begin with pdl_enter().
+#define GDN_LAUNCH_PDL(name, kernel, grid, smem, stream, ...)                                \
+    do {                                                                                     \
+        cudaError_t e_ = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                              (int)(smem));                                  \
+        if (e_ != cudaSuccess) return e_;                                                    \
+        if ((grid).x > 0 && (grid).y > 0 && (grid).z > 0) {                                   \
+            prof_before(name, stream);                                                       \
+            e_ = launch_pdl(kernel, (grid), dim3(kThreads), (size_t)(smem), (stream), __VA_ARGS__); \
+            if (e_ != cudaSuccess) return e_;                                                \
+            prof_after(stream);                                                              \
+        }                                                                                    \
+    } while (0)
+
 cudaError_t tables(const Plan &p, cudaStream_t s) {
     if (!p.g.cu) return cudaSuccess;
     prof_before("tables", s);
@@ -964,7 +979,7 @@ static cudaError_t forward_t(const Plan &p, cudaStream_t s, bool states_only) {
         }
         GDN_LAUNCH("simt_walk_map", (walk_kernel<TI, kMap>), dim3(p.max_segs, H, (K + V) / kBV), walk_smem(K), s,
                    g, a);
-        GDN_LAUNCH("map_scan", map_scan_kernel, dim3(g.N, H, V / kSB), map_scan_smem(K), s, g,
+        GDN_LAUNCH_PDL("map_scan", map_scan_kernel, dim3(g.N, H, V / kSB), map_scan_smem(K), s, g,
                    (const float *)p.ws.maps, p.h0, (const int32_t *)a.warm, p.ws.seg_state, 0);
         GDN_LAUNCH(states_only ? "simt_walk_states" : "simt_walk_out", (walk_kernel<TI, kOut>), dim3(p.max_segs, H, V / kBV), walk_smem(K), s, g, a);
     } else {
@@ -983,7 +998,7 @@ cudaError_t warm_decide(const Plan &p, cudaStream_t s) {
 
 cudaError_t cp_scan(const Plan &p, const int32_t *warm, cudaStream_t s) {
     const Geo &g = p.g;
-    GDN_LAUNCH("map_scan", map_scan_kernel, dim3(g.N, g.H, g.V / kSB), map_scan_smem(g.K), s, g,
+    GDN_LAUNCH_PDL("map_scan", map_scan_kernel, dim3(g.N, g.H, g.V / kSB), map_scan_smem(g.K), s, g,
                (const float *)p.ws.maps, p.h0, warm, p.ws.seg_state, 0);
     return cudaSuccess;
 }
@@ -1037,7 +1052,7 @@ static cudaError_t backward_t(const Plan &p, cudaStream_t s) {
         d.cp = 1;
         GDN_LAUNCH("simt_dwalk_map", (dwalk_kernel<TI, kMap>), dim3(p.max_segs, H, (K + V) / kBV), dwalk_smem(K), s,
                    g, d);
-        GDN_LAUNCH("map_rscan", map_scan_kernel, dim3(g.N, H, V / kSB), map_scan_smem(K), s, g,
+        GDN_LAUNCH_PDL("map_rscan", map_scan_kernel, dim3(g.N, H, V / kSB), map_scan_smem(K), s, g,
                    (const float *)p.ws.maps, p.dht, (const int32_t *)nullptr, p.ws.seg_state, 1);
         GDN_LAUNCH("simt_dwalk_out", (dwalk_kernel<TI, kOut>), dim3(p.max_segs, H, V / kBV), dwalk_smem(K), s, g,
                    d);
@@ -1063,7 +1078,7 @@ cudaError_t local_grads(const Plan &p, cudaStream_t s, bool ws_bf16) {
 
 cudaError_t cp_rscan(const Plan &p, cudaStream_t s) {
     const Geo &g = p.g;
-    GDN_LAUNCH("map_rscan", map_scan_kernel, dim3(g.N, g.H, g.V / kSB), map_scan_smem(g.K), s, g,
+    GDN_LAUNCH_PDL("map_rscan", map_scan_kernel, dim3(g.N, g.H, g.V / kSB), map_scan_smem(g.K), s, g,
                (const float *)p.ws.maps, p.dht, (const int32_t *)nullptr, p.ws.seg_state, 1);
     return cudaSuccess;
 }

@@ -61,6 +61,7 @@ __global__ void __launch_bounds__(256, 2)
 tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_qs,
                     const __grid_constant__ CUtensorMap tm_y, Geo g, const float *ws_gam) {
+    pdl_enter();
     extern __shared__ uint8_t smem_raw[];
     IntraSmem &s = *reinterpret_cast<IntraSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -208,7 +209,7 @@ bail:
         if (mma_n > 0) mbar_drain(&s.mma_bar, (mma_n - 1) & 1);
     }
 done:
-    if (tid == 0) bulk_wait_all();
+    if (tid == 0) bulk_wait_read();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tb, 128);
@@ -256,6 +257,7 @@ enum { kDOut = 0, kDMap = 1 };
 template <int MODE>
 __global__ void __launch_bounds__(256, 1)
 tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
+    pdl_enter();
     extern __shared__ uint8_t smem_raw[];
     DWalkSmem &s = *reinterpret_cast<DWalkSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -465,7 +467,7 @@ tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
         __syncthreads();
     }
 
-    if (tma_thread) bulk_wait_all();
+    if (tma_thread) bulk_wait_read();
     if (tid < 64) cp_async_wait_all();    // a gam prefetch may still be in flight after a bail
     if (bailed) {
         if (tid == 0) {
@@ -512,8 +514,9 @@ cudaError_t backward(const Plan &p, cudaStream_t s, bool have_ctx) {
     const size_t ismem = sizeof(IntraSmem) + 1024;
     if ((e = set_smem(tc_bwd_intra_kernel, ismem)) != cudaSuccess) return e;
     prof_before("tc_bwd_intra", s);
-    tc_bwd_intra_kernel<<<dim3(p.max_chunks, g.H), 256, ismem, s>>>(mq, m.k, m.dO, m.qs, m.y, g,
-                                                                     p.ws.gam);
+    if ((e = launch_pdl(tc_bwd_intra_kernel, dim3(p.max_chunks, g.H), dim3(256), ismem, s,
+                        mq, m.k, m.dO, m.qs, m.y, g, p.ws.gam)) != cudaSuccess)
+        return e;
     prof_after(s);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
@@ -529,16 +532,22 @@ cudaError_t backward(const Plan &p, cudaStream_t s, bool have_ctx) {
         a.maps = p.ws.maps;
         a.seg_end = p.ws.seg_state;
         prof_before("tc_dwalk_map", s);
-        tc_dwalk_kernel<kDMap><<<dim3(p.max_segs, g.H, 2), 256, smem, s>>>(m, g, a);
+        if ((e = launch_pdl(tc_dwalk_kernel<kDMap>, dim3(p.max_segs, g.H, 2), dim3(256), smem, s,
+                            m, g, a)) != cudaSuccess)
+            return e;
         prof_after(s);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if ((e = simt::cp_rscan(p, s)) != cudaSuccess) return e;
         prof_before("tc_dwalk_out", s);
-        tc_dwalk_kernel<kDOut><<<dim3(p.max_segs, g.H, 1), 256, smem, s>>>(m, g, a);
+        if ((e = launch_pdl(tc_dwalk_kernel<kDOut>, dim3(p.max_segs, g.H, 1), dim3(256), smem, s,
+                            m, g, a)) != cudaSuccess)
+            return e;
         prof_after(s);
     } else {
         prof_before("tc_dwalk_out", s);
-        tc_dwalk_kernel<kDOut><<<dim3(g.N, g.H, 1), 256, smem, s>>>(m, g, a);
+        if ((e = launch_pdl(tc_dwalk_kernel<kDOut>, dim3(g.N, g.H, 1), dim3(256), smem, s,
+                            m, g, a)) != cudaSuccess)
+            return e;
         prof_after(s);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

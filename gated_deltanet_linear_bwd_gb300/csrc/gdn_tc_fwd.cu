@@ -59,6 +59,7 @@ __global__ void __launch_bounds__(128, 2)
 tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_u,
                Geo g, float *ws_gam, __nv_bfloat16 *ws_t) {
+    pdl_enter();
     extern __shared__ uint8_t smem_raw[];
     PrepSmem &s = *reinterpret_cast<PrepSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -254,7 +255,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             tma_store_2d(&tm_u, s.v + c * 2 * kTile, 0, row);
         }
         bulk_commit();
-        bulk_wait_all();
+        bulk_wait_read();                     // the staged tiles may be released once read
     }
     goto done;
 bail:
@@ -313,6 +314,7 @@ __global__ void __launch_bounds__(256, 1)
 tc_walk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_w,
                const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_hc,
                Geo g, TcWalkArgs a) {
+    pdl_enter();
     extern __shared__ uint8_t smem_raw[];
     WalkSmem &s = *reinterpret_cast<WalkSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -530,7 +532,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         __syncthreads();
     }
 
-    if (tma_thread) bulk_wait_all();
+    if (tma_thread) bulk_wait_read();
     if (tid < 64) cp_async_wait_all();    // a gam prefetch may still be in flight after a bail
     if (bailed) {
         if (tid == 0) {
@@ -637,9 +639,10 @@ static cudaError_t run_forward(const Plan &p, cudaStream_t s, bool states_only, 
     if ((e = set_smem(tc_walk_kernel<kWalkMap>, walk_smem)) != cudaSuccess) return e;
 
     prof_before("tc_prep", s);
-    tc_prep_kernel<<<dim3((p.max_chunks + 1) / 2, g.H), 128, prep_smem, s>>>(
-        mk, mv, mw, mu, g, p.ws.gam,
-        (states_only || save) ? (__nv_bfloat16 *)p.ws.tmat : nullptr);
+    if ((e = launch_pdl(tc_prep_kernel, dim3((p.max_chunks + 1) / 2, g.H), dim3(128), prep_smem, s,
+                        mk, mv, mw, mu, g, p.ws.gam,
+                        (states_only || save) ? (__nv_bfloat16 *)p.ws.tmat : nullptr)) != cudaSuccess)
+        return e;
     prof_after(s);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
@@ -661,16 +664,22 @@ static cudaError_t run_forward(const Plan &p, cudaStream_t s, bool states_only, 
             a.warm_chunks = p.warm_chunks;
         }
         prof_before("tc_walk_map", s);
-        tc_walk_kernel<kWalkMap><<<dim3(p.max_segs, g.H, 2), 256, walk_smem, s>>>(mk, mw, mu, mhc, g, a);
+        if ((e = launch_pdl(tc_walk_kernel<kWalkMap>, dim3(p.max_segs, g.H, 2), dim3(256), walk_smem, s,
+                            mk, mw, mu, mhc, g, a)) != cudaSuccess)
+            return e;
         prof_after(s);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if ((e = simt::cp_scan(p, a.warm, s)) != cudaSuccess) return e;
         prof_before(out_name, s);
-        tc_walk_kernel<kWalkOut><<<dim3(p.max_segs, g.H, 1), 256, walk_smem, s>>>(mk, mw, mu, mhc, g, a);
+        if ((e = launch_pdl(tc_walk_kernel<kWalkOut>, dim3(p.max_segs, g.H, 1), dim3(256), walk_smem, s,
+                            mk, mw, mu, mhc, g, a)) != cudaSuccess)
+            return e;
         prof_after(s);
     } else {
         prof_before(out_name, s);
-        tc_walk_kernel<kWalkOut><<<dim3(g.N, g.H, 1), 256, walk_smem, s>>>(mk, mw, mu, mhc, g, a);
+        if ((e = launch_pdl(tc_walk_kernel<kWalkOut>, dim3(g.N, g.H, 1), dim3(256), walk_smem, s,
+                            mk, mw, mu, mhc, g, a)) != cudaSuccess)
+            return e;
         prof_after(s);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

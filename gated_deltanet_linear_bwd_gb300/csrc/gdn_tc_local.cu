@@ -159,6 +159,7 @@ cudaError_t set_smem(F kernel, size_t bytes) {
 template <typename TG>
 __global__ void __launch_bounds__(256, 1)
 tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
+    pdl_enter();
     extern __shared__ uint8_t smem_raw[];
     LocalSmem &s = *reinterpret_cast<LocalSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -634,10 +635,14 @@ cudaError_t local_grads(const Plan &p, cudaStream_t s) {
     prof_before("tc_local_grad", s);
     if (p.grad_dtype == GDN_BF16) {
         if ((e = set_smem(tc_local_kernel<__nv_bfloat16>, smem)) != cudaSuccess) return e;
-        tc_local_kernel<__nv_bfloat16><<<grid, 256, smem, s>>>(m, g, a);
+        if ((e = launch_pdl(tc_local_kernel<__nv_bfloat16>, grid, dim3(256), smem, s,
+                            m, g, a)) != cudaSuccess)
+            return e;
     } else {
         if ((e = set_smem(tc_local_kernel<float>, smem)) != cudaSuccess) return e;
-        tc_local_kernel<float><<<grid, 256, smem, s>>>(m, g, a);
+        if ((e = launch_pdl(tc_local_kernel<float>, grid, dim3(256), smem, s,
+                            m, g, a)) != cudaSuccess)
+            return e;
     }
     prof_after(s);
     return cudaGetLastError();

@@ -48,6 +48,7 @@ tc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
               const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_u,
               const __grid_constant__ CUtensorMap tm_hc, Geo g, const float *ws_gam,
               __nv_bfloat16 *o) {
+    pdl_enter();
     extern __shared__ uint8_t smem_raw[];
     OutSmem &s = *reinterpret_cast<OutSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -229,8 +230,9 @@ cudaError_t output(const Plan &p, cudaStream_t s) {
     const size_t smem = sizeof(OutSmem) + 1024;
     if ((e = set_smem(tc_out_kernel, smem)) != cudaSuccess) return e;
     prof_before("tc_out", s);
-    tc_out_kernel<<<dim3(p.max_chunks, g.H), 256, smem, s>>>(mq, mk, mw, mu, mhc, g, p.ws.gam,
-                                                             (__nv_bfloat16 *)p.o);
+    if ((e = launch_pdl(tc_out_kernel, dim3(p.max_chunks, g.H), dim3(256), smem, s,
+                        mq, mk, mw, mu, mhc, g, p.ws.gam, (__nv_bfloat16 *)p.o)) != cudaSuccess)
+        return e;
     prof_after(s);
     return cudaGetLastError();
 }
