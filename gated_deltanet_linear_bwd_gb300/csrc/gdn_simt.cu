@@ -289,10 +289,11 @@ walk_kernel(Geo g, WalkArgs a) {
 // block of kSB state columns).  Forward (reverse = 0): start[0] = h0 and
 // start[j+1] = A_j start[j] + B_j.  Backward (reverse = 1): end[nseg-1] =
 // d(final state) and end[j-1] = A'_j end[j] + B'_j.  The maps of the next
-// step are copied into shared memory (cp.async, double-buffered, rows padded
-// by 4 floats against bank conflicts) while the current step computes;
-// thread t owns row t/2 and four of the kSB columns.
+// two steps are copied into shared memory (cp.async, three buffers, rows
+// padded by 4 floats against bank conflicts) while the current step
+// computes; thread t owns row t/2 and four of the kSB columns.
 constexpr int kSB = 8;
+constexpr int kScanStages = 3;
 
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
@@ -308,33 +309,34 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+template <int K>
 __global__ void __launch_bounds__(256)
 map_scan_kernel(Geo g, const float *maps, const float *init, const int32_t *warm, float *out,
                 int reverse) {
     pdl_enter();
-    const int n = blockIdx.x, h = blockIdx.y, col0 = blockIdx.z * kSB, K = g.K, V = g.V,
-              H = g.H;
+    const int n = blockIdx.x, h = blockIdx.y, col0 = blockIdx.z * kSB, V = g.V, H = g.H;
     if (n >= g.N || col0 >= V) return;
     if (warm && warm[n * H + h]) return;
     const int nseg = seq_nsegs(g, n), sbase = seq_seg_base(g, n);
     extern __shared__ __align__(16) float sm[];
     const int ld = K + 4;                        // padded row stride of the A buffers
-    float *Abuf = sm;                            // [2][K][ld]
-    float *Bbuf = Abuf + 2 * K * ld;             // [2][K][kSB]
-    float *S = Bbuf + 2 * K * kSB;               // [K][kSB]
+    float *Abuf = sm;                            // [kScanStages][K][ld]
+    float *Bbuf = Abuf + kScanStages * K * ld;   // [kScanStages][K][kSB]
+    float *S = Bbuf + kScanStages * K * kSB;     // [K][kSB]
     const int t = threadIdx.x, i = t >> 1, jq = (t & 1) * 4;
     const bool act = i < K;
     auto stage = [&](int step, int buf) {
         const int j = reverse ? nseg - 1 - step : step;
         const float *M = maps + ((long long)(sbase + j) * H + h) * K * (K + V);
         float *A = Abuf + buf * K * ld, *Bm = Bbuf + buf * K * kSB;
-        const int per_row = K / 4;
-        for (int idx = t; idx < K * per_row; idx += blockDim.x) {
-            const int row = idx / per_row, c4 = idx % per_row;
+        constexpr int per_row = K / 4;
+#pragma unroll
+        for (int m = 0; m < K * per_row / 256; ++m) {
+            const int idx = t + 256 * m, row = idx / per_row, c4 = idx % per_row;
             cp_async16(A + row * ld + 4 * c4, M + (long long)row * (K + V) + 4 * c4);
         }
-        for (int idx = t; idx < K * (kSB / 4); idx += blockDim.x) {
-            const int row = idx / (kSB / 4), c4 = idx % (kSB / 4);
+        if (t < K * (kSB / 4)) {
+            const int row = t / (kSB / 4), c4 = t % (kSB / 4);
             cp_async16(Bm + row * kSB + 4 * c4, M + (long long)row * (K + V) + K + col0 + 4 * c4);
         }
         cp_async_commit();
@@ -344,11 +346,14 @@ map_scan_kernel(Geo g, const float *maps, const float *init, const int32_t *warm
         S[idx] = init ? init[(((long long)n * H + h) * K + r) * V + c] : 0.f;
     }
     const int steps = nseg - 1;
-    if (steps > 0) stage(0, 0);
+    for (int st = 0; st < kScanStages - 1 && st < steps; ++st) stage(st, st);
     for (int step = 0; step < steps; ++step) {
-        const int buf = step & 1;
-        if (step + 1 < steps) {
-            stage(step + 1, buf ^ 1);
+        const int buf = step % kScanStages;
+        // the buffer of step - 1 (every thread is past its reads) takes step + 2
+        if (step + 2 < steps) {
+            stage(step + 2, (step + 2) % kScanStages);
+            cp_async_wait<2>();
+        } else if (step + 1 < steps) {
             cp_async_wait<1>();
         } else {
             cp_async_wait<0>();
@@ -360,6 +365,7 @@ map_scan_kernel(Geo g, const float *maps, const float *init, const int32_t *warm
         if (act) {
             const float *A = Abuf + buf * K * ld + i * ld;
             acc = *reinterpret_cast<const float4 *>(Bbuf + buf * K * kSB + i * kSB + jq);
+#pragma unroll
             for (int l4 = 0; l4 < K / 4; ++l4) {
                 const float4 a4 = *reinterpret_cast<const float4 *>(A + 4 * l4);
                 const float av[4] = {a4.x, a4.y, a4.z, a4.w};
@@ -383,7 +389,8 @@ map_scan_kernel(Geo g, const float *maps, const float *init, const int32_t *warm
 }
 
 static size_t map_scan_smem(int K) {
-    return sizeof(float) * (2 * K * (K + 4) + 2 * K * kSB + K * kSB);
+    // K in {64, 128}; the kernel is instantiated for both
+    return sizeof(float) * (kScanStages * K * (K + 4) + kScanStages * K * kSB + K * kSB);
 }
 
 // Warmup shortcut decision per (sequence, head): every segment j > 0 must
@@ -979,7 +986,7 @@ static cudaError_t forward_t(const Plan &p, cudaStream_t s, bool states_only) {
         }
         GDN_LAUNCH("simt_walk_map", (walk_kernel<TI, kMap>), dim3(p.max_segs, H, (K + V) / kBV), walk_smem(K), s,
                    g, a);
-        GDN_LAUNCH_PDL("map_scan", map_scan_kernel, dim3(g.N, H, V / kSB), map_scan_smem(K), s, g,
+        GDN_LAUNCH_PDL("map_scan", (K == 128 ? map_scan_kernel<128> : map_scan_kernel<64>), dim3(g.N, H, V / kSB), map_scan_smem(K), s, g,
                    (const float *)p.ws.maps, p.h0, (const int32_t *)a.warm, p.ws.seg_state, 0);
         GDN_LAUNCH(states_only ? "simt_walk_states" : "simt_walk_out", (walk_kernel<TI, kOut>), dim3(p.max_segs, H, V / kBV), walk_smem(K), s, g, a);
     } else {
@@ -998,7 +1005,7 @@ cudaError_t warm_decide(const Plan &p, cudaStream_t s) {
 
 cudaError_t cp_scan(const Plan &p, const int32_t *warm, cudaStream_t s) {
     const Geo &g = p.g;
-    GDN_LAUNCH_PDL("map_scan", map_scan_kernel, dim3(g.N, g.H, g.V / kSB), map_scan_smem(g.K), s, g,
+    GDN_LAUNCH_PDL("map_scan", (g.K == 128 ? map_scan_kernel<128> : map_scan_kernel<64>), dim3(g.N, g.H, g.V / kSB), map_scan_smem(g.K), s, g,
                (const float *)p.ws.maps, p.h0, warm, p.ws.seg_state, 0);
     return cudaSuccess;
 }
@@ -1052,7 +1059,7 @@ static cudaError_t backward_t(const Plan &p, cudaStream_t s) {
         d.cp = 1;
         GDN_LAUNCH("simt_dwalk_map", (dwalk_kernel<TI, kMap>), dim3(p.max_segs, H, (K + V) / kBV), dwalk_smem(K), s,
                    g, d);
-        GDN_LAUNCH_PDL("map_rscan", map_scan_kernel, dim3(g.N, H, V / kSB), map_scan_smem(K), s, g,
+        GDN_LAUNCH_PDL("map_rscan", (K == 128 ? map_scan_kernel<128> : map_scan_kernel<64>), dim3(g.N, H, V / kSB), map_scan_smem(K), s, g,
                    (const float *)p.ws.maps, p.dht, (const int32_t *)nullptr, p.ws.seg_state, 1);
         GDN_LAUNCH("simt_dwalk_out", (dwalk_kernel<TI, kOut>), dim3(p.max_segs, H, V / kBV), dwalk_smem(K), s, g,
                    d);
@@ -1078,7 +1085,7 @@ cudaError_t local_grads(const Plan &p, cudaStream_t s, bool ws_bf16) {
 
 cudaError_t cp_rscan(const Plan &p, cudaStream_t s) {
     const Geo &g = p.g;
-    GDN_LAUNCH_PDL("map_rscan", map_scan_kernel, dim3(g.N, g.H, g.V / kSB), map_scan_smem(g.K), s, g,
+    GDN_LAUNCH_PDL("map_rscan", (g.K == 128 ? map_scan_kernel<128> : map_scan_kernel<64>), dim3(g.N, g.H, g.V / kSB), map_scan_smem(g.K), s, g,
                (const float *)p.ws.maps, p.dht, (const int32_t *)nullptr, p.ws.seg_state, 1);
     return cudaSuccess;
 }
