@@ -17,6 +17,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
 #include "tc_ptx.cuh"
@@ -49,31 +51,53 @@ struct IntraSmem {
     uint8_t yT[2 * kTile];         // Y^T, [128 rows v][64 chunk rows]
     uint8_t p[kTile];              // P rows r (scale included)
     float gam[64], rq[64], rk[64];
-    uint64_t tma_bar, mma_bar;
+    uint64_t load_bar[2], mma_bar; // loads: {q, k}, {dO}
     uint32_t tmem_base;
 };
 }  // namespace
 
-// Per (chunk, head), 256 threads: P on lanes 0-63 (row r = v), Qs rows by
+// Persistent over (chunk, head) items with a stride of the grid, two CTAs
+// per SM.  Per item, 256 threads: P on lanes 0-63 (row r = v), Qs rows by
 // threads 128-191, then Y^T = dO^T P feature-major (thread: row v, column
-// half hs); Qs and Y^T leave by TMA from shared memory.
+// half hs); Qs and Y^T leave by TMA from shared memory.  The next item's
+// q, k are fetched as soon as P and Qs are done with them, its dO once
+// Y^T's product has read the current one.
 __global__ void __launch_bounds__(256, 2)
 tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_qs,
-                    const __grid_constant__ CUtensorMap tm_y, Geo g, const float *ws_gam) {
+                    const __grid_constant__ CUtensorMap tm_y, Geo g, const float *ws_gam,
+                    int n_items) {
     pdl_enter();
     extern __shared__ uint8_t smem_raw[];
     IntraSmem &s = *reinterpret_cast<IntraSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int tid = threadIdx.x, warp = tid >> 5, h = blockIdx.y, H = g.H, ci = blockIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, H = g.H;
     const int v = tid & 127, hs = tid >> 7, c0 = 32 * hs, cq = c0 >> 3;
-    ChunkRef cr;
-    if (!chunk_ref(g, ci, cr)) return;
-    const int L = cr.len;
-    const long long bos = cr.bos;
+
+    auto item_ref = [&](int i, int &ci, int &hh, ChunkRef &r) -> bool {
+        if (i >= n_items) return false;
+        ci = i / H;
+        hh = i % H;
+        return chunk_ref(g, ci, r);
+    };
+    auto load_qk = [&](int hh, long long bos) {
+        mbar_arrive_expect_tx(&s.load_bar[0], 4 * kTile);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            tma_load_3d(s.qk + half * 2 * kTile, &tm_q, &s.load_bar[0], half * 64, hh, (int)bos);
+            tma_load_3d(s.qk + half * 2 * kTile + kTile, &tm_k, &s.load_bar[0], half * 64, hh,
+                        (int)bos);
+        }
+    };
+    auto load_do = [&](int hh, long long bos) {
+        mbar_arrive_expect_tx(&s.load_bar[1], 2 * kTile);
+        tma_load_3d(s.dO, &tm_do, &s.load_bar[1], 0, hh, (int)bos);
+        tma_load_3d(s.dO + kTile, &tm_do, &s.load_bar[1], 64, hh, (int)bos);
+    };
 
     if (tid == 0) {
-        mbar_init(&s.tma_bar, 1);
+        mbar_init(&s.load_bar[0], 1);
+        mbar_init(&s.load_bar[1], 1);
         mbar_init(&s.mma_bar, 1);
         fence_barrier_init();
     }
@@ -86,129 +110,154 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     tc_fence_after();
     const uint32_t tb = s.tmem_base;
     const uint32_t t_p = tb, t_y = tb + 64;
-    if (tid == 0) {
-        const int tok0 = (int)bos;
-        mbar_arrive_expect_tx(&s.tma_bar, 6 * kTile);
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            tma_load_3d(s.qk + half * 2 * kTile, &tm_q, &s.tma_bar, half * 64, h, tok0);
-            tma_load_3d(s.qk + half * 2 * kTile + kTile, &tm_k, &s.tma_bar, half * 64, h, tok0);
-            tma_load_3d(s.dO + half * kTile, &tm_do, &s.tma_bar, half * 64, h, tok0);
+
+    int item = blockIdx.x, ci = 0, h = 0;
+    ChunkRef cr;
+    bool have = item_ref(item, ci, h, cr);
+    int issued[2] = {0, 0};                   // loads issued per group (uniform bookkeeping)
+    if (have) {
+        if (tid == 0) {
+            load_qk(h, cr.bos);
+            load_do(h, cr.bos);
         }
+        issued[0] = issued[1] = 1;
     }
-    if (tid < 64) s.gam[tid] = tid < L ? ws_gam[(bos + tid) * H + h] : 0.f;
-    int mma_n = 0;
-    bool tma_pending = true;
-    bool ok = mbar_wait(&s.tma_bar, 0, g.spin_limit, g.status);
-    if (__syncthreads_or(!ok)) goto bail;
-    tma_pending = false;
-    ++mma_n;
-    if (warp == 0) {
-        tc_fence_after();
-        const uint32_t qk = smem_u32(s.qk);
+    int it = 0, mma_n = 0;
+    bool bailed = false;
+    while (have) {
+        const int L = cr.len;
+        const long long bos = cr.bos;
+        int ci_n = 0, h_n = 0;
+        ChunkRef cr_n;
+        const bool have_next = item_ref(item + (int)gridDim.x, ci_n, h_n, cr_n);
+        if (tid == 0) bulk_wait_read();       // the previous item's stores have read Qs, Y^T
+        tc_fence_before();
+        __syncthreads();
+        if (tid < 64) s.gam[tid] = tid < L ? ws_gam[(bos + tid) * H + h] : 0.f;
+        bool ok = mbar_wait(&s.load_bar[0], it & 1, g.spin_limit, g.status);
+        if (__syncthreads_or(!ok)) { bailed = true; break; }
+        ++mma_n;
+        if (warp == 0) {
+            tc_fence_after();
+            const uint32_t qk = smem_u32(s.qk);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t half = kk >> 2, sub = (kk & 3) * 32;
-            mma_bf16(t_p, desc_sw128(qk + half * 2 * kTile + sub, 16, 1024),
-                     desc_sw128(qk + half * 2 * kTile + kTile + sub, 16, 1024), kIdKK64, kk > 0);
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t half = kk >> 2, sub = (kk & 3) * 32;
+                mma_bf16(t_p, desc_sw128(qk + half * 2 * kTile + sub, 16, 1024),
+                         desc_sw128(qk + half * 2 * kTile + kTile + sub, 16, 1024), kIdKK64, kk > 0);
+            }
+            mma_commit(&s.mma_bar);
         }
-        mma_commit(&s.mma_bar);
-    }
-    if (g.l2norm && tid < 128) {
-        // 1 / |q_r| from the Q rows (threads 0-63), 1 / |k_r| from the K rows (64-127)
-        const int r = tid & 63;
-        const uint8_t *base = s.qk + (tid >= 64 ? kTile : 0);
-        float ss = 0.f;
+        if (g.l2norm && tid < 128) {
+            // 1 / |q_r| from the Q rows (threads 0-63), 1 / |k_r| from the K rows (64-127)
+            const int r = tid & 63;
+            const uint8_t *base = s.qk + (tid >= 64 ? kTile : 0);
+            float ss = 0.f;
 #pragma unroll
-        for (int half = 0; half < 2; ++half)
+            for (int half = 0; half < 2; ++half)
 #pragma unroll 8
-            for (int col = 0; col < 64; ++col) {
-                const float x = ld_bf16(base + half * 2 * kTile, r, col);
-                ss += x * x;
-            }
-        (tid >= 64 ? s.rk : s.rq)[r] = rsqrtf(ss + 1e-6f);
-    }
-    if (g.l2norm) __syncthreads();
-    if (tid >= 128 && tid < 192) {
-        // row r of Qs = diag(scale e^gam (x 1/|q_r|)) Q, both dk halves
-        const int r = tid - 128;
-        const float f = r < L ? g.scale * __expf(s.gam[r]) * (g.l2norm ? s.rq[r] : 1.f) : 0.f;
-#pragma unroll 1
-        for (int q = 0; q < 16; ++q) {
-            const int half = q >> 3, chunk = q & 7;
-            float x[8];
-            const uint4 raw = *reinterpret_cast<const uint4 *>(
-                s.qk + half * 2 * kTile + r * 128 + ((chunk ^ (r & 7)) << 4));
-            const __nv_bfloat16 *b = reinterpret_cast<const __nv_bfloat16 *>(&raw);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = f * __bfloat162float(b[e]);
-            st_row8(s.qs + half * kTile, r, chunk, x);
+                for (int col = 0; col < 64; ++col) {
+                    const float x = ld_bf16(base + half * 2 * kTile, r, col);
+                    ss += x * x;
+                }
+            (tid >= 64 ? s.rk : s.rq)[r] = rsqrtf(ss + 1e-6f);
         }
-    }
-    ok = mbar_wait(&s.mma_bar, 0, g.spin_limit, g.status);
-    if (__syncthreads_or(!ok)) goto bail;
-    tc_fence_after();
-    if (v < 64) {
-        // P row r = v, columns c0 .. c0+31, scale included
-        const int r = v;
-        const float gr = s.gam[r];
-        const float sr = g.l2norm ? s.rq[r] : 1.f;
+        if (g.l2norm) __syncthreads();
+        if (tid >= 128 && tid < 192) {
+            // row r of Qs = diag(scale e^gam (x 1/|q_r|)) Q, both dk halves
+            const int r = tid - 128;
+            const float f = r < L ? g.scale * __expf(s.gam[r]) * (g.l2norm ? s.rq[r] : 1.f) : 0.f;
 #pragma unroll 1
-        for (int q = 0; q < 4; ++q) {
-            float x[8];
-            tmem_ld8(tmem_addr(t_p, warp, c0 + 8 * q), x);
+            for (int q = 0; q < 16; ++q) {
+                const int half = q >> 3, chunk = q & 7;
+                float x[8];
+                const uint4 raw = *reinterpret_cast<const uint4 *>(
+                    s.qk + half * 2 * kTile + r * 128 + ((chunk ^ (r & 7)) << 4));
+                const __nv_bfloat16 *bb = reinterpret_cast<const __nv_bfloat16 *>(&raw);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int c = c0 + 8 * q + e;
-                x[e] = (c <= r && r < L) ? g.scale * x[e] * __expf(gr - s.gam[c]) * sr *
-                                               (g.l2norm ? s.rk[c] : 1.f)
-                                         : 0.f;
+                for (int e = 0; e < 8; ++e) x[e] = f * __bfloat162float(bb[e]);
+                st_row8(s.qs + half * kTile, r, chunk, x);
             }
-            st_row8(s.p, r, cq + q, x);
         }
-    }
-    tc_fence_before();
-    fence_proxy_async();
-    __syncthreads();
-    if (tid == 0) {
-        // Qs is complete: store it while Y^T is computed
-        const int row = (int)(((long long)ci * H + h) * 2 * 64);
-        tma_store_2d(&tm_qs, s.qs, 0, row);
-        tma_store_2d(&tm_qs, s.qs + kTile, 0, row + 64);
-        bulk_commit();
-    }
-    ++mma_n;
-    if (warp == 0) {
+        ok = mbar_wait(&s.mma_bar, 0, g.spin_limit, g.status);
+        if (__syncthreads_or(!ok)) { bailed = true; break; }
         tc_fence_after();
-        const uint32_t dO = smem_u32(s.dO), pp = smem_u32(s.p);
+        if (v < 64) {
+            // P row r = v, columns c0 .. c0+31, scale included
+            const int r = v;
+            const float gr = s.gam[r];
+            const float sr = g.l2norm ? s.rq[r] : 1.f;
+            float xs[32];
+            tmem_ld32(tmem_addr(t_p, warp, c0), xs);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-            mma_bf16(t_y, desc_sw128(dO + kk * 2048, kTile, 1024),    // dO^T, MN-major
-                     desc_sw128(pp + kk * 2048, kTile, 1024), kIdMM64, kk > 0);   // P, MN-major
-        mma_commit(&s.mma_bar);
+            for (int q = 0; q < 4; ++q) {
+                float *x = xs + 8 * q;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int c = c0 + 8 * q + e;
+                    x[e] = (c <= r && r < L) ? g.scale * x[e] * __expf(gr - s.gam[c]) * sr *
+                                                   (g.l2norm ? s.rk[c] : 1.f)
+                                             : 0.f;
+                }
+                st_row8(s.p, r, cq + q, x);
+            }
+        }
+        tc_fence_before();
+        fence_proxy_async();
+        __syncthreads();
+        if (tid == 0) {
+            // Qs is complete: store it while Y^T is computed; q, k are free for the next item
+            const int row = (int)(((long long)ci * H + h) * 2 * 64);
+            tma_store_2d(&tm_qs, s.qs, 0, row);
+            tma_store_2d(&tm_qs, s.qs + kTile, 0, row + 64);
+            bulk_commit();
+            if (have_next) load_qk(h_n, cr_n.bos);
+        }
+        if (have_next) ++issued[0];
+        ok = mbar_wait(&s.load_bar[1], it & 1, g.spin_limit, g.status);
+        if (__syncthreads_or(!ok)) { bailed = true; break; }
+        ++mma_n;
+        if (warp == 0) {
+            tc_fence_after();
+            const uint32_t dO = smem_u32(s.dO), pp = smem_u32(s.p);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16(t_y, desc_sw128(dO + kk * 2048, kTile, 1024),    // dO^T, MN-major
+                         desc_sw128(pp + kk * 2048, kTile, 1024), kIdMM64, kk > 0);   // P, MN-major
+            mma_commit(&s.mma_bar);
+        }
+        ok = mbar_wait(&s.mma_bar, 1, g.spin_limit, g.status);
+        if (__syncthreads_or(!ok)) { bailed = true; break; }
+        if (tid == 0 && have_next) {
+            fence_proxy_async();
+            load_do(h_n, cr_n.bos);           // dO's last reader was the product above
+        }
+        if (have_next) ++issued[1];
+        tc_fence_after();
+        {
+            float xs[32];
+            tmem_ld32(tmem_addr(t_y, warp, c0), xs);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) st_row8(s.yT, v, cq + q, xs + 8 * q);
+        }
+        fence_proxy_async();
+        __syncthreads();
+        if (tid == 0) {
+            tma_store_2d(&tm_y, s.yT, 0, (int)(((long long)ci * H + h) * kD));
+            bulk_commit();
+        }
+        item += (int)gridDim.x;
+        ci = ci_n;
+        h = h_n;
+        cr = cr_n;
+        have = have_next;
+        ++it;
     }
-    ok = mbar_wait(&s.mma_bar, 1, g.spin_limit, g.status);
-    if (__syncthreads_or(!ok)) goto bail;
-    tc_fence_after();
-#pragma unroll 1
-    for (int q = 0; q < 4; ++q) {
-        float x[8];
-        tmem_ld8(tmem_addr(t_y, warp, c0 + 8 * q), x);
-        st_row8(s.yT, v, cq + q, x);
-    }
-    fence_proxy_async();
-    __syncthreads();
-    if (tid == 0) {
-        tma_store_2d(&tm_y, s.yT, 0, (int)(((long long)ci * H + h) * kD));
-        bulk_commit();
-    }
-    goto done;
-bail:
-    if (tid == 0) {
-        if (tma_pending) mbar_drain(&s.tma_bar, 0);
+    if (bailed && tid == 0) {
+        for (int grp = 0; grp < 2; ++grp)
+            if (issued[grp] > 0) mbar_drain(&s.load_bar[grp], (issued[grp] - 1) & 1);
         if (mma_n > 0) mbar_drain(&s.mma_bar, (mma_n - 1) & 1);
     }
-done:
     if (tid == 0) bulk_wait_read();
     tc_fence_before();
     __syncthreads();
@@ -514,8 +563,10 @@ cudaError_t backward(const Plan &p, cudaStream_t s, bool have_ctx) {
     const size_t ismem = sizeof(IntraSmem) + 1024;
     if ((e = set_smem(tc_bwd_intra_kernel, ismem)) != cudaSuccess) return e;
     prof_before("tc_bwd_intra", s);
-    if ((e = launch_pdl(tc_bwd_intra_kernel, dim3(p.max_chunks, g.H), dim3(256), ismem, s,
-                        mq, m.k, m.dO, m.qs, m.y, g, p.ws.gam)) != cudaSuccess)
+    const int n_items = p.max_chunks * g.H;
+    if ((e = launch_pdl(tc_bwd_intra_kernel, dim3(std::min(n_items, 2 * std::max(p.sms, 1))),
+                        dim3(256), ismem, s, mq, m.k, m.dO, m.qs, m.y, g, p.ws.gam, n_items)) !=
+        cudaSuccess)
         return e;
     prof_after(s);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
