@@ -57,7 +57,7 @@ struct LocalSmem {
     uint8_t ds[kTile];         // dS rows r
     uint8_t gs[kTile];         // G rows r
     float gam[64], bet[64], ee[64], ff[64];
-    float red[8][32], red2[8][32], red3[8][32], red4[8][32];
+    float red[8][32], red2[8][32], red3[8][32], red4[8][32], red5[8][32];
     float zrow[2][64], zprow[2][64], dbA[2][64];
     float zcol[64], rowA[64], yw[64], yu[64], zpp[64];
     float hdot[16];            // [0..3]: per-warp parts of <dHL, H0>; [8..15]: block_sum scratch
@@ -354,34 +354,6 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
         if (__syncthreads_or(!ok)) { bailed = true; break; }
         tc_fence_after();
         {
-            // rows r = v < 64: dS and z = dS .* Q K^T (row sums, negated column sums)
-            const bool act = v < 64;
-            const int r = v;
-            if (act) {
-                const float gr = s.gam[r];
-                float zr = 0.f;
-#pragma unroll 1
-                for (int q = 0; q < 4; ++q) {
-                    float dp[8], qk[8], zc[8];
-                    tmem_ld8x2(tmem_addr(t_dp, warp, c0 + 8 * q), tmem_addr(t_p, warp, c0 + 8 * q),
-                               dp, qk);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int c = c0 + 8 * q + e;
-                        const float ds =
-                            (c <= r && r < L) ? scale * dp[e] * __expf(gr - s.gam[c]) : 0.f;
-                        const float zz = ds * qk[e];
-                        zr += zz;
-                        zc[e] = -zz;
-                        dp[e] = ds;
-                    }
-                    st_row8(s.ds, r, cq + q, dp);
-                    warp_sum8(zc, s.red[warp] + 8 * q);
-                }
-                s.zrow[hs][r] = zr;
-            } else {
-                s.red[warp][lane] = 0.f;
-            }
             // every feature f = v: dYw^T, dYu^T rows into the dead dHL^T tiles, and
             // sums over f of dYw .* K (yw) and dYu .* V (yu)
             const uint8_t *krow = s.qk + (v >> 6) * 2 * kTile + kTile;
@@ -412,12 +384,10 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
             fence_proxy_async();
             __syncthreads();
             if (tid < 64) {
-                s.zcol[tid] = quad_sum(s.red, tid);
                 s.yw[tid] = quad_sum(s.red2, tid);
                 s.yu[tid] = quad_sum(s.red3, tid);
                 s.zpp[tid] = quad_sum(s.red4, tid);
             }
-            __syncthreads();
         }
         // v, dO, dU^T, the H0^T / U^T / dW^T tile and T are dead: next item's group 0
         if (have_next) {
@@ -443,23 +413,42 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
             }
             mma_commit(&s.mma_bar);
         }
-        ok = mbar_wait(&s.mma_bar, 0, g.spin_limit, g.status);
-        if (__syncthreads_or(!ok)) { bailed = true; break; }
-        // W^T, u^T and the dHL^T / dYu^T / dYw^T tiles are dead: next item's group 1
-        if (have_next) {
-            if (tma_thread) {
-                fence_proxy_async();
-                load_group(1, ci_n, h_n, cr_n.bos);
+        // While the dA product runs, lanes 0-63 form dS; lanes 64-127 then take
+        // the dA epilogue.  Each half reduces into its own array.
+        ok = true;
+        if (v < 64) {
+            // rows r = v: dS and z = dS .* Q K^T (row sums, negated column sums)
+            const int r = v;
+            const float gr = s.gam[r];
+            float zr = 0.f;
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+                float dp[8], qk[8], zc[8];
+                tmem_ld8x2(tmem_addr(t_dp, warp, c0 + 8 * q), tmem_addr(t_p, warp, c0 + 8 * q),
+                           dp, qk);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int c = c0 + 8 * q + e;
+                    const float ds =
+                        (c <= r && r < L) ? scale * dp[e] * __expf(gr - s.gam[c]) : 0.f;
+                    const float zz = ds * qk[e];
+                    zr += zz;
+                    zc[e] = -zz;
+                    dp[e] = ds;
+                }
+                st_row8(s.ds, r, cq + q, dp);
+                warp_sum8(zc, s.red[warp] + 8 * q);
             }
-            ++issued[1];
-        }
-        tc_fence_after();
-        {
-            // rows r = v - 64 (lanes 64-127): G = dA .* D .* beta_r, z' = G .* K K^T and
-            // the dA part of dbeta
-            const bool act = v >= 64;
-            const int r = v - 64;
-            if (act) {
+            s.zrow[hs][r] = zr;
+            s.red5[warp][lane] = 0.f;
+        } else {
+            // rows r = v - 64: G = dA .* D .* beta_r, z' = G .* K K^T and the dA part
+            // of dbeta
+            s.red[warp][lane] = 0.f;
+            ok = mbar_wait(&s.mma_bar, 0, g.spin_limit, g.status);
+            if (ok) {
+                tc_fence_after();
+                const int r = v - 64;
                 const float gr = s.gam[r], br = s.bet[r];
                 float zpr = 0.f, dba = 0.f;
 #pragma unroll 1
@@ -481,17 +470,25 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
                         da[e] = g_rc;
                     }
                     st_row8(s.gs, r, cq + q, da);
-                    warp_sum8(zc, s.red[warp] + 8 * q);
+                    warp_sum8(zc, s.red5[warp] + 8 * q);
                 }
                 s.zprow[hs][r] = zpr;
                 s.dbA[hs][r] = dba;
-            } else {
-                s.red[warp][lane] = 0.f;
             }
-            tc_fence_before();
-            fence_proxy_async();
-            red_combine(s.zcol, s.red, true);
         }
+        tc_fence_before();
+        fence_proxy_async();
+        if (__syncthreads_or(!ok)) { bailed = true; break; }
+        // the dA product is done (lanes 64-127 saw it): W^T, u^T and the dHL^T /
+        // dYu^T / dYw^T tiles are dead, the next item's group 1 can come
+        if (have_next) {
+            if (tma_thread) {
+                fence_proxy_async();
+                load_group(1, ci_n, h_n, cr_n.bos);
+            }
+            ++issued[1];
+        }
+        if (tid < 64) s.zcol[tid] = quad_sum(s.red, tid) + quad_sum(s.red5, tid);
 
         // ---------------- wave 3: dS K, dS^T Q + (G + G^T) K
         ++mma_n;
