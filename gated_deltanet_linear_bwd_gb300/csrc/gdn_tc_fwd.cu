@@ -19,6 +19,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
 #include "tc_ptx.cuh"
@@ -55,22 +57,42 @@ __device__ __forceinline__ float scan64(float x, float *wsum) {
     return x;
 }
 
+// Persistent over (chunk pair, head) items with a stride of the grid, two
+// CTAs per SM.  The next item's K and V tiles are fetched as soon as the W/u
+// products have read the current ones; W^T and u^T leave through the dead A
+// region in two TMA-stored passes.
 __global__ void __launch_bounds__(128, 2)
 tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_u,
-               Geo g, float *ws_gam, __nv_bfloat16 *ws_t) {
+               Geo g, float *ws_gam, __nv_bfloat16 *ws_t, int n_items) {
     pdl_enter();
     extern __shared__ uint8_t smem_raw[];
     PrepSmem &s = *reinterpret_cast<PrepSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int tid = threadIdx.x, warp = tid >> 5, h = blockIdx.y, H = g.H;
-    ChunkRef ra, rb;
-    if (!chunk_ref(g, 2 * blockIdx.x, ra)) return;
-    const bool has_b = chunk_ref(g, 2 * blockIdx.x + 1, rb);
-    if (!has_b) rb = ra;
+    const int tid = threadIdx.x, warp = tid >> 5, H = g.H;
     const int ch = tid >> 6, r = tid & 63;
-    const ChunkRef &mine = ch ? rb : ra;
-    const int L = (ch && !has_b) ? 0 : mine.len;
+    uint8_t *stage = reinterpret_cast<uint8_t *>(&s.A[0][0][0]);   // 32 KB after the W/u products
+
+    // item i: chunks 2 (i / H) and 2 (i / H) + 1 of head i % H
+    auto item_ref = [&](int i, int &pair, int &hh, ChunkRef &ra, ChunkRef &rb, bool &hb) -> bool {
+        if (i >= n_items) return false;
+        pair = i / H;
+        hh = i % H;
+        if (!chunk_ref(g, 2 * pair, ra)) return false;
+        hb = chunk_ref(g, 2 * pair + 1, rb);
+        if (!hb) rb = ra;
+        return true;
+    };
+    auto load_kv = [&](int hh, const ChunkRef &ra, const ChunkRef &rb) {
+        mbar_arrive_expect_tx(&s.tma_bar, 8 * kTile);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            tma_load_3d(s.k + half * 2 * kTile, &tm_k, &s.tma_bar, half * 64, hh, (int)ra.bos);
+            tma_load_3d(s.k + half * 2 * kTile + kTile, &tm_k, &s.tma_bar, half * 64, hh, (int)rb.bos);
+            tma_load_3d(s.v + half * 2 * kTile, &tm_v, &s.tma_bar, half * 64, hh, (int)ra.bos);
+            tma_load_3d(s.v + half * 2 * kTile + kTile, &tm_v, &s.tma_bar, half * 64, hh, (int)rb.bos);
+        }
+    };
 
     if (tid == 0) {
         mbar_init(&s.tma_bar, 1);
@@ -85,185 +107,208 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = s.tmem_base;
-    if (tid == 0) {
-        mbar_arrive_expect_tx(&s.tma_bar, 8 * kTile);
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            tma_load_3d(s.k + half * 2 * kTile, &tm_k, &s.tma_bar, half * 64, h, (int)ra.bos);
-            tma_load_3d(s.k + half * 2 * kTile + kTile, &tm_k, &s.tma_bar, half * 64, h, (int)rb.bos);
-            tma_load_3d(s.v + half * 2 * kTile, &tm_v, &s.tma_bar, half * 64, h, (int)ra.bos);
-            tma_load_3d(s.v + half * 2 * kTile + kTile, &tm_v, &s.tma_bar, half * 64, h, (int)rb.bos);
-        }
-    }
-    // gam = cumsum(g), beta (zero beyond the chunk)
-    const long long tok = mine.bos + r;
-    const float graw = r < L ? g.g[tok * H + h] : 0.f;
-    const float gam = scan64(graw, s.wsum);
-    s.gam[ch][r] = gam;
-    s.bet[ch][r] = r < L ? g.beta[tok * H + h] : 0.f;
-    if (r < L) ws_gam[tok * H + h] = gam;
 
-    int mma_n = 0;              // commits issued (uniform across threads)
-    bool tma_pending = true;
-    bool ok = mbar_wait(&s.tma_bar, 0, g.spin_limit, g.status);
-    if (__syncthreads_or(!ok)) goto bail;
-    tma_pending = false;
-    ++mma_n;
-    if (warp == 0) {
-        tc_fence_after();
-        const uint32_t kb = smem_u32(s.k);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = (kk >> 2) * 2 * kTile + (kk & 3) * 32;
-            const uint64_t d = desc_sw128(kb + off, 16, 1024);
-            mma_bf16(tbase, d, d, kIdescKK, kk > 0);
-        }
-        mma_commit(&s.mma_bar);
-    }
-    ok = mbar_wait(&s.mma_bar, 0, g.spin_limit, g.status);
-    if (__syncthreads_or(!ok)) goto bail;
-    tc_fence_after();
-    {
-        // row r of this chunk's K K^T block
-        float kk[64];
-        tmem_ld32(tmem_addr(tbase, warp, ch * 64), kk);
-        tmem_ld32(tmem_addr(tbase, warp, ch * 64 + 32), kk + 32);
-        float nrm = 0.f;
-#pragma unroll
-        for (int c = 0; c < 64; ++c) nrm = (c == r) ? kk[c] : nrm;
-        const float rk = (r < L) ? (g.l2norm ? rsqrtf(nrm + 1e-6f) : 1.f) : 0.f;
-        s.rk[ch][r] = rk;
+    int item = blockIdx.x, pair = 0, h = 0;
+    ChunkRef ra, rb;
+    bool has_b = false;
+    bool have = item_ref(item, pair, h, ra, rb, has_b);
+    if (have && tid == 0) load_kv(h, ra, rb);
+    int loads = have ? 1 : 0;                 // TMA loads issued (uniform bookkeeping)
+    int it = 0, mma_n = 0;
+    bool bailed = false;
+    while (have) {
+        int pair_n = 0, h_n = 0;
+        ChunkRef ra_n, rb_n;
+        bool has_b_n = false;
+        const bool have_next = item_ref(item + (int)gridDim.x, pair_n, h_n, ra_n, rb_n, has_b_n);
+        const ChunkRef &mine = ch ? rb : ra;
+        const int L = (ch && !has_b) ? 0 : mine.len;
+        if (tid == 0) bulk_wait_read();       // the previous item's u^T stores have read the A region
         tc_fence_before();
         __syncthreads();
-        const float br = s.bet[ch][r], gr = s.gam[ch][r];
-        float4 *arow = reinterpret_cast<float4 *>(s.A[ch][r]);
+        // gam = cumsum(g), beta (zero beyond the chunk)
+        const long long tok = mine.bos + r;
+        const float graw = r < L ? g.g[tok * H + h] : 0.f;
+        const float gam = scan64(graw, s.wsum);
+        s.gam[ch][r] = gam;
+        s.bet[ch][r] = r < L ? g.beta[tok * H + h] : 0.f;
+        if (r < L) ws_gam[tok * H + h] = gam;
+
+        bool ok = mbar_wait(&s.tma_bar, it & 1, g.spin_limit, g.status);
+        if (__syncthreads_or(!ok)) { bailed = true; break; }
+        ++mma_n;
+        if (warp == 0) {
+            tc_fence_after();
+            const uint32_t kb = smem_u32(s.k);
 #pragma unroll
-        for (int c4 = 0; c4 < 16; ++c4) {
-            float x[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int c = 4 * c4 + j;
-                x[j] = (c < r && r < L) ? br * kk[c] * rk * s.rk[ch][c] * __expf(gr - s.gam[ch][c])
-                                        : 0.f;
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t off = (kk >> 2) * 2 * kTile + (kk & 3) * 32;
+                const uint64_t d = desc_sw128(kb + off, 16, 1024);
+                mma_bf16(tbase, d, d, kIdescKK, kk > 0);
             }
-            arow[c4] = make_float4(x[0], x[1], x[2], x[3]);
+            mma_commit(&s.mma_bar);
         }
-    }
-    __syncthreads();
-    {
-        // column r of T = (I + A)^-1 by forward substitution (A read by broadcast)
-        float col[64];
-#pragma unroll
-        for (int i = 0; i < 64; ++i) col[i] = (i == r) ? 1.f : 0.f;
-#pragma unroll
-        for (int i = 1; i < 64; ++i) {
-            const float4 *ar = reinterpret_cast<const float4 *>(s.A[ch][i]);
-            float acc = col[i];
-#pragma unroll
-            for (int c4 = 0; c4 < (i + 3) / 4; ++c4) {
-                const float4 a4 = ar[c4];
-                if (4 * c4 + 0 < i) acc -= a4.x * col[4 * c4 + 0];
-                if (4 * c4 + 1 < i) acc -= a4.y * col[4 * c4 + 1];
-                if (4 * c4 + 2 < i) acc -= a4.z * col[4 * c4 + 2];
-                if (4 * c4 + 3 < i) acc -= a4.w * col[4 * c4 + 3];
-            }
-            col[i] = acc;
-        }
-        if (ws_t && (!ch || has_b)) {
-            // the backward keeps T as bf16: row r of the tile [chunk][h][64][64] is
-            // column r of this chunk's T (zero past the chunk's end)
-            uint4 *dst = reinterpret_cast<uint4 *>(
-                ws_t + (((long long)(2 * blockIdx.x + ch) * H + h) * 64 + r) * 64);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                uint32_t w4[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int i = 8 * q + 2 * e;
-                    __nv_bfloat162 b2 = __floats2bfloat162_rn(r < L ? col[i] : 0.f,
-                                                              r < L ? col[i + 1] : 0.f);
-                    w4[e] = *reinterpret_cast<uint32_t *>(&b2);
-                }
-                dst[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-            }
-        }
-        __syncthreads();  // every column done: A's space becomes bw / bu
-        // MN-major B operands: row j = r holds T[.][j] scaled by beta_j e_j rk_j (W)
-        // and by beta_j (u).
-        uint8_t *bw = reinterpret_cast<uint8_t *>(&s.A[0][0][0]);
-        uint8_t *bu = bw + 2 * kTile;
-        const float bj = s.bet[ch][r], ej = __expf(s.gam[ch][r]), rkj = s.rk[ch][r];
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            float x[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) x[i] = col[32 * q + i] * bj * ej * rkj;
-            st_row32(bw + ch * kTile, r, 32 * q, x);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) x[i] = col[32 * q + i] * bj;
-            st_row32(bu + ch * kTile, r, 32 * q, x);
-        }
-    }
-    fence_proxy_async();
-    __syncthreads();
-    ++mma_n;
-    if (warp == 0) {
+        ok = mbar_wait(&s.mma_bar, 0, g.spin_limit, g.status);
+        if (__syncthreads_or(!ok)) { bailed = true; break; }
         tc_fence_after();
-        const uint32_t kb = smem_u32(s.k), vb = smem_u32(s.v);
-        const uint32_t bw = smem_u32(&s.A[0][0][0]), bu = bw + 2 * kTile;
+        {
+            // row r of this chunk's K K^T block
+            float kk[64];
+            tmem_ld32(tmem_addr(tbase, warp, ch * 64), kk);
+            tmem_ld32(tmem_addr(tbase, warp, ch * 64 + 32), kk + 32);
+            float nrm = 0.f;
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < 64; ++c) nrm = (c == r) ? kk[c] : nrm;
+            const float rk = (r < L) ? (g.l2norm ? rsqrtf(nrm + 1e-6f) : 1.f) : 0.f;
+            s.rk[ch][r] = rk;
+            tc_fence_before();
+            __syncthreads();
+            const float br = s.bet[ch][r], gr = s.gam[ch][r];
+            float4 *arow = reinterpret_cast<float4 *>(s.A[ch][r]);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t bdw = desc_sw128(bw + c * kTile + kk * 2048, kTile, 1024);
-                const uint64_t bdu = desc_sw128(bu + c * kTile + kk * 2048, kTile, 1024);
-                const uint64_t ak = desc_sw128(kb + c * kTile + kk * 2048, 2 * kTile, 1024);
-                const uint64_t av = desc_sw128(vb + c * kTile + kk * 2048, 2 * kTile, 1024);
-                mma_bf16(tbase + c * 64, ak, bdw, kIdescPrepMN, kk > 0);
-                mma_bf16(tbase + 128 + c * 64, av, bdu, kIdescPrepMN, kk > 0);
+            for (int c4 = 0; c4 < 16; ++c4) {
+                float x[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int c = 4 * c4 + j;
+                    x[j] = (c < r && r < L)
+                               ? br * kk[c] * rk * s.rk[ch][c] * __expf(gr - s.gam[ch][c])
+                               : 0.f;
+                }
+                arow[c4] = make_float4(x[0], x[1], x[2], x[3]);
             }
         }
-        mma_commit(&s.mma_bar);
-    }
-    ok = mbar_wait(&s.mma_bar, 1, g.spin_limit, g.status);
-    if (__syncthreads_or(!ok)) goto bail;
-    tc_fence_after();
-    // thread t = feature index (dk for W, dv for u): its 64 chunk rows form row t
-    // of the W^T / u^T tile, staged swizzled in the dead K / V tiles ([chunk]
-    // [128 rows][128 B]) and stored by TMA
+        __syncthreads();
+        {
+            // column r of T = (I + A)^-1 by forward substitution (A read by broadcast)
+            float col[64];
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        const int c = m & 1;                  // chunk
-        const bool isu = m >= 2;
-        const int Lc = (c && !has_b) ? 0 : (c ? rb.len : ra.len);
-        uint8_t *tile = (isu ? s.v : s.k) + c * 2 * kTile;
+            for (int i = 0; i < 64; ++i) col[i] = (i == r) ? 1.f : 0.f;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            float x[32];
-            tmem_ld32(tmem_addr(tbase, warp, (isu ? 128 : 0) + c * 64 + 32 * half), x);
+            for (int i = 1; i < 64; ++i) {
+                const float4 *ar = reinterpret_cast<const float4 *>(s.A[ch][i]);
+                float acc = col[i];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) x[j] = 32 * half + j < Lc ? x[j] : 0.f;
-            st_row32(tile, tid, 32 * half, x);
+                for (int c4 = 0; c4 < (i + 3) / 4; ++c4) {
+                    const float4 a4 = ar[c4];
+                    if (4 * c4 + 0 < i) acc -= a4.x * col[4 * c4 + 0];
+                    if (4 * c4 + 1 < i) acc -= a4.y * col[4 * c4 + 1];
+                    if (4 * c4 + 2 < i) acc -= a4.z * col[4 * c4 + 2];
+                    if (4 * c4 + 3 < i) acc -= a4.w * col[4 * c4 + 3];
+                }
+                col[i] = acc;
+            }
+            if (ws_t && (!ch || has_b)) {
+                // the backward keeps T as bf16: row r of the tile [chunk][h][64][64] is
+                // column r of this chunk's T (zero past the chunk's end)
+                uint4 *dst = reinterpret_cast<uint4 *>(
+                    ws_t + (((long long)(2 * pair + ch) * H + h) * 64 + r) * 64);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    uint32_t w4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int i = 8 * q + 2 * e;
+                        __nv_bfloat162 b2 = __floats2bfloat162_rn(r < L ? col[i] : 0.f,
+                                                                  r < L ? col[i + 1] : 0.f);
+                        w4[e] = *reinterpret_cast<uint32_t *>(&b2);
+                    }
+                    dst[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                }
+            }
+            __syncthreads();  // every column done: A's space becomes bw / bu
+            // MN-major B operands: row j = r holds T[.][j] scaled by beta_j e_j rk_j (W)
+            // and by beta_j (u).
+            uint8_t *bw = stage;
+            uint8_t *bu = bw + 2 * kTile;
+            const float bj = s.bet[ch][r], ej = __expf(s.gam[ch][r]), rkj = s.rk[ch][r];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                float x[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) x[i] = col[32 * q + i] * bj * ej * rkj;
+                st_row32(bw + ch * kTile, r, 32 * q, x);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) x[i] = col[32 * q + i] * bj;
+                st_row32(bu + ch * kTile, r, 32 * q, x);
+            }
         }
-    }
-    fence_proxy_async();
-    __syncthreads();
-    if (tid == 0) {
-        for (int c = 0; c < (has_b ? 2 : 1); ++c) {
-            const int row = (int)(((long long)(2 * blockIdx.x + c) * H + h) * kD);
-            tma_store_2d(&tm_w, s.k + c * 2 * kTile, 0, row);
-            tma_store_2d(&tm_u, s.v + c * 2 * kTile, 0, row);
+        fence_proxy_async();
+        __syncthreads();
+        ++mma_n;
+        if (warp == 0) {
+            tc_fence_after();
+            const uint32_t kb = smem_u32(s.k), vb = smem_u32(s.v);
+            const uint32_t bw = smem_u32(stage), bu = bw + 2 * kTile;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t bdw = desc_sw128(bw + c * kTile + kk * 2048, kTile, 1024);
+                    const uint64_t bdu = desc_sw128(bu + c * kTile + kk * 2048, kTile, 1024);
+                    const uint64_t ak = desc_sw128(kb + c * kTile + kk * 2048, 2 * kTile, 1024);
+                    const uint64_t av = desc_sw128(vb + c * kTile + kk * 2048, 2 * kTile, 1024);
+                    mma_bf16(tbase + c * 64, ak, bdw, kIdescPrepMN, kk > 0);
+                    mma_bf16(tbase + 128 + c * 64, av, bdu, kIdescPrepMN, kk > 0);
+                }
+            }
+            mma_commit(&s.mma_bar);
         }
-        bulk_commit();
-        bulk_wait_read();                     // the staged tiles may be released once read
+        ok = mbar_wait(&s.mma_bar, 1, g.spin_limit, g.status);
+        if (__syncthreads_or(!ok)) { bailed = true; break; }
+        // K and V are dead: the next item's
+        if (tid == 0 && have_next) {
+            fence_proxy_async();
+            load_kv(h_n, ra_n, rb_n);
+        }
+        if (have_next) ++loads;
+        tc_fence_after();
+        // thread t = feature index (dk for W, dv for u): its 64 chunk rows form row t
+        // of the W^T / u^T tile, staged swizzled in the dead A region (two tiles of
+        // [128 rows][128 B] per pass) and stored by TMA
+#pragma unroll 1
+        for (int pass = 0; pass < 2; ++pass) {
+            if (pass == 1) {
+                if (tid == 0) bulk_wait_read();   // the W^T tiles have been read
+                __syncthreads();
+            }
+#pragma unroll 1
+            for (int c = 0; c < 2; ++c) {
+                const int Lc = (c && !has_b) ? 0 : (c ? rb.len : ra.len);
+                uint8_t *tile = stage + c * 2 * kTile;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    float x[32];
+                    tmem_ld32(tmem_addr(tbase, warp, 128 * pass + c * 64 + 32 * half), x);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) x[j] = 32 * half + j < Lc ? x[j] : 0.f;
+                    st_row32(tile, tid, 32 * half, x);
+                }
+            }
+            fence_proxy_async();
+            __syncthreads();
+            if (tid == 0) {
+                for (int c = 0; c < (has_b ? 2 : 1); ++c) {
+                    const int row = (int)(((long long)(2 * pair + c) * H + h) * kD);
+                    tma_store_2d(pass ? &tm_u : &tm_w, stage + c * 2 * kTile, 0, row);
+                }
+                bulk_commit();
+            }
+        }
+        item += (int)gridDim.x;
+        pair = pair_n;
+        h = h_n;
+        ra = ra_n;
+        rb = rb_n;
+        has_b = has_b_n;
+        have = have_next;
+        ++it;
     }
-    goto done;
-bail:
-    if (tid == 0) {
-        if (tma_pending) mbar_drain(&s.tma_bar, 0);
+    if (bailed && tid == 0) {
+        if (loads > 0) mbar_drain(&s.tma_bar, (loads - 1) & 1);
         if (mma_n > 0) mbar_drain(&s.mma_bar, (mma_n - 1) & 1);
     }
-done:
+    if (tid == 0) bulk_wait_read();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tbase, 256);
@@ -639,9 +684,11 @@ static cudaError_t run_forward(const Plan &p, cudaStream_t s, bool states_only, 
     if ((e = set_smem(tc_walk_kernel<kWalkMap>, walk_smem)) != cudaSuccess) return e;
 
     prof_before("tc_prep", s);
-    if ((e = launch_pdl(tc_prep_kernel, dim3((p.max_chunks + 1) / 2, g.H), dim3(128), prep_smem, s,
-                        mk, mv, mw, mu, g, p.ws.gam,
-                        (states_only || save) ? (__nv_bfloat16 *)p.ws.tmat : nullptr)) != cudaSuccess)
+    const int prep_items = (p.max_chunks + 1) / 2 * g.H;
+    if ((e = launch_pdl(tc_prep_kernel, dim3(std::min(prep_items, 2 * std::max(p.sms, 1))),
+                        dim3(128), prep_smem, s, mk, mv, mw, mu, g, p.ws.gam,
+                        (states_only || save) ? (__nv_bfloat16 *)p.ws.tmat : nullptr,
+                        prep_items)) != cudaSuccess)
         return e;
     prof_after(s);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
