@@ -35,6 +35,10 @@ def _configure(lib):
                                    dp, dp, dp, dp, dp, dp, dp, dp, ip, i, i]
     lib.gdn_oracle_bwd.restype = ctypes.c_int
     lib.gdn_oracle_max_threads.restype = ctypes.c_int
+    lib.gdn_oracle_gate.argtypes = [dp, dp, ctypes.c_long, i, dp]
+    lib.gdn_oracle_gate.restype = ctypes.c_int
+    lib.gdn_oracle_gate_bwd.argtypes = [dp, dp, dp, ctypes.c_long, i, dp, dp]
+    lib.gdn_oracle_gate_bwd.restype = ctypes.c_int
     return lib
 
 
@@ -132,3 +136,27 @@ def bwd(q, k, v, g, beta, do, h0=None, dht=None, cu_seqlens=None, scale=None,
     if rc != 0:
         raise ValueError("oracle bwd rejected its arguments")
     return out
+
+
+def gate(x, a, lib=None):
+    """Log decay g = -a_h * softplus(x) from gate logits x [..., H] and a [H] (float64)."""
+    lib = lib or _load()
+    x, a = _f64(x), _f64(a)
+    H = int(a.shape[0])
+    g = np.empty_like(x)
+    if lib.gdn_oracle_gate(_ptr(x), _ptr(a), int(x.size // H), H, _ptr(g)) != 0:
+        raise ValueError("oracle gate rejected its arguments")
+    return g
+
+
+def gate_bwd(x, a, dg, lib=None):
+    """Gradients (dx, da) of the gate from dg = dL/dg (float64)."""
+    lib = lib or _load()
+    x, a, dg = _f64(x), _f64(a), _f64(dg)
+    H = int(a.shape[0])
+    dx = np.empty_like(x)
+    da = np.empty(H)
+    if lib.gdn_oracle_gate_bwd(_ptr(x), _ptr(a), _ptr(dg), int(x.size // H), H, _ptr(dx),
+                               _ptr(da)) != 0:
+        raise ValueError("oracle gate_bwd rejected its arguments")
+    return dx, da

@@ -343,3 +343,35 @@ int gdn_oracle_bwd(const double *q, const double *k, const double *v, const doub
     run_units(&p, N, unit_list, n_units, nthreads, backward_unit);
     return 0;
 }
+
+/*
+ * Gate preprocessing (the pages' "gate preprocessing" ahead of the kernels,
+ * aivizor, FLA-flow paragraph; its form is the GDN layer's decay gate):
+ * the log decay of token t, head h is g = -a_h * softplus(x_t,h) from a raw
+ * gate logit x and a positive per-head scale a_h, softplus(x) = log(1 + e^x).
+ * Its backward: dx = dg * (-a_h * sigmoid(x)), da_h = sum_t dg * (-softplus(x)).
+ * x, g, dg, dx: [n_tok, Hh];  a, da: [Hh].
+ */
+static double softplus(double x) { return x > 0.0 ? x + log1p(exp(-x)) : log1p(exp(x)); }
+
+int gdn_oracle_gate(const double *x, const double *a, long n_tok, int Hh, double *g) {
+    if (!x || !a || !g || n_tok < 0 || Hh <= 0) return 1;
+    for (long t = 0; t < n_tok; ++t)
+        for (int h = 0; h < Hh; ++h) g[t * Hh + h] = -a[h] * softplus(x[t * Hh + h]);
+    return 0;
+}
+
+int gdn_oracle_gate_bwd(const double *x, const double *a, const double *dg, long n_tok, int Hh,
+                        double *dx, double *da) {
+    if (!x || !a || !dg || !dx || n_tok < 0 || Hh <= 0) return 1;
+    for (int h = 0; h < Hh; ++h) {
+        double acc = 0.0;
+        for (long t = 0; t < n_tok; ++t) {
+            const double xv = x[t * Hh + h], d = dg[t * Hh + h];
+            dx[t * Hh + h] = -a[h] * d / (1.0 + exp(-xv));
+            acc -= d * softplus(xv);
+        }
+        if (da) da[h] = acc;
+    }
+    return 0;
+}

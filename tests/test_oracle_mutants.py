@@ -35,6 +35,12 @@ MUTANTS = [
     ("dH[(long)i * V + j] += p->scale * qt[i] * dot[j];", "dH[(long)i * V + j] += qt[i] * dot[j];"),
     ("const long th = (bos + t) * Hh + h;\n            const double *Hprev",
      "const long th = (bos + t) * Hh + (Hh - 1 - h);\n            const double *Hprev"),
+    # gate preprocessing
+    ("return x > 0.0 ? x + log1p(exp(-x)) : log1p(exp(x));", "return x > 0.0 ? x : log1p(exp(x));"),
+    ("dx[t * Hh + h] = -a[h] * d / (1.0 + exp(-xv));", "dx[t * Hh + h] = a[h] * d / (1.0 + exp(-xv));"),
+    ("/ (1.0 + exp(-xv));", "/ (1.0 + exp(xv));"),
+    ("acc -= d * softplus(xv);", "acc -= d * xv;"),
+    ("g[t * Hh + h] = -a[h] * softplus(x[t * Hh + h]);", "g[t * Hh + h] = -softplus(x[t * Hh + h]);"),
 ]
 
 
@@ -93,9 +99,42 @@ def _fd(lib, l2):
     return True
 
 
+def _gate(lib):
+    # closed forms: softplus(0) = ln 2; a = 0 gives no decay; very negative logits none either
+    g0 = oracle.gate(np.zeros((2, 3)), np.array([0.5, 1.0, 2.0]), lib=lib)
+    if not np.allclose(g0, -np.array([0.5, 1.0, 2.0]) * np.log(2.0), rtol=1e-14):
+        return False
+    r = np.random.default_rng(7)
+    x, a = 4.0 * r.standard_normal((5, 3)), r.uniform(0.1, 2.0, 3)
+    if np.any(oracle.gate(x, np.zeros(3), lib=lib) != 0.0):
+        return False
+    if not np.allclose(oracle.gate(x + 40.0, a, lib=lib), -a * (x + 40.0), rtol=1e-12):
+        return False
+    # the backward against central differences of the forward
+    dg = r.standard_normal(x.shape)
+    dx, da = oracle.gate_bwd(x, a, dg, lib=lib)
+
+    def loss(xx, aa):
+        return float((oracle.gate(xx, aa, lib=lib) * dg).sum())
+
+    for idx in np.ndindex(x.shape):
+        xp, xm = x.copy(), x.copy()
+        xp[idx] += 1e-6
+        xm[idx] -= 1e-6
+        if abs((loss(xp, a) - loss(xm, a)) / 2e-6 - dx[idx]) > 1e-7 * max(1.0, abs(dx[idx])):
+            return False
+    for h in range(3):
+        ap, am = a.copy(), a.copy()
+        ap[h] += 1e-6
+        am[h] -= 1e-6
+        if abs((loss(x, ap) - loss(x, am)) / 2e-6 - da[h]) > 1e-7 * max(1.0, abs(da[h])):
+            return False
+    return True
+
+
 def pins_pass(lib):
     return (_hand(lib) and _chunked(lib, False) and _chunked(lib, True) and _eps(lib)
-            and _fd(lib, False) and _fd(lib, True))
+            and _fd(lib, False) and _fd(lib, True) and _gate(lib))
 
 
 def test_unmutated_oracle_passes_the_quick_pins():
