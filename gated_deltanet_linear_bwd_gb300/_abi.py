@@ -26,7 +26,8 @@ class gdn_fwd_args(ctypes.Structure):
                 ("B", _i32), ("T", _i32), ("H", _i32), ("K", _i32), ("V", _i32), ("N", _i32),
                 ("dtype", _i32), ("scale", _f32), ("use_qk_l2norm", _i32), ("cp_mode", _i32),
                 ("cp_segment_chunks", _i32), ("cp_warmup_chunks", _i32), ("cp_warmup_tau", _f32),
-                ("o", _vp), ("final_state", _vp), ("cp_stats", _vp), ("ctx", _vp)]
+                ("o", _vp), ("final_state", _vp), ("cp_stats", _vp), ("ctx", _vp),
+                ("gate_scale", _vp)]
 
 
 class gdn_bwd_args(ctypes.Structure):
@@ -37,7 +38,8 @@ class gdn_bwd_args(ctypes.Structure):
                 ("cp_segment_chunks", _i32),
                 ("d_o", _vp), ("d_final_state", _vp),
                 ("grad_dtype", _i32), ("dq", _vp), ("dk", _vp), ("dv", _vp), ("dg", _vp),
-                ("dbeta", _vp), ("d_initial_state", _vp), ("ctx", _vp)]
+                ("dbeta", _vp), ("d_initial_state", _vp), ("ctx", _vp),
+                ("gate_scale", _vp), ("d_gate_scale", _vp)]
 
 
 class gdn_kernel_stat(ctypes.Structure):

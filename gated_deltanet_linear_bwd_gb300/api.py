@@ -37,7 +37,7 @@ def _check(name, t, dtype=None, shape=None, device=None):
 
 
 def _common(args, q, k, v, g, beta, initial_state, cu_seqlens, scale, use_qk_l2norm, cp,
-            cp_segment_chunks):
+            cp_segment_chunks, gate_scale=None):
     if q.dtype not in _DT:
         raise ValueError(f"unsupported dtype {q.dtype}")
     B, T, H, K = q.shape
@@ -51,6 +51,7 @@ def _common(args, q, k, v, g, beta, initial_state, cu_seqlens, scale, use_qk_l2n
     _check("beta", beta, torch.float32, (B, T, H), dev)
     _check("initial_state", initial_state, torch.float32, (N, H, K, V), dev)
     _check("cu_seqlens", cu_seqlens, torch.int32, None, dev)
+    _check("gate_scale", gate_scale, torch.float32, (H,), dev)
     args.q, args.k, args.v = q.data_ptr(), k.data_ptr(), v.data_ptr()
     args.g, args.beta = g.data_ptr(), beta.data_ptr()
     args.initial_state = _ptr(initial_state)
@@ -61,19 +62,23 @@ def _common(args, q, k, v, g, beta, initial_state, cu_seqlens, scale, use_qk_l2n
     args.use_qk_l2norm = int(bool(use_qk_l2norm))
     args.cp_mode = _CP[cp]
     args.cp_segment_chunks = int(cp_segment_chunks)
+    args.gate_scale = _ptr(gate_scale)
     return B, T, H, K, V, N, dev
 
 
 def chunk_gated_delta_rule_fwd(q, k, v, g, beta, scale=None, initial_state=None,
                                output_final_state=True, cu_seqlens=None, use_qk_l2norm=False,
                                cp="auto", cp_segment_chunks=0, cp_warmup_chunks=0,
-                               cp_warmup_tau=1e-3, cp_stats=None, save_ctx=False):
+                               cp_warmup_tau=1e-3, cp_stats=None, save_ctx=False,
+                               gate_scale=None):
     """Low-level forward: returns (o, final_state or None), or
     (o, final_state, ctx) with save_ctx=True, where ctx is the saved-context
-    buffer for chunk_gated_delta_rule_bwd (None when the path keeps none)."""
+    buffer for chunk_gated_delta_rule_bwd (None when the path keeps none).
+    With `gate_scale` ([H] fp32, a_h > 0), g holds raw gate logits x and the
+    log decay is -a_h * softplus(x)."""
     a = _abi.gdn_fwd_args()
     B, T, H, K, V, N, dev = _common(a, q, k, v, g, beta, initial_state, cu_seqlens, scale,
-                                    use_qk_l2norm, cp, cp_segment_chunks)
+                                    use_qk_l2norm, cp, cp_segment_chunks, gate_scale)
     o = torch.empty(B, T, H, V, dtype=q.dtype, device=dev)
     fs = torch.empty(N, H, K, V, dtype=torch.float32, device=dev) if output_final_state else None
     a.o, a.final_state = o.data_ptr(), _ptr(fs)
@@ -95,12 +100,14 @@ def chunk_gated_delta_rule_fwd(q, k, v, g, beta, scale=None, initial_state=None,
 def chunk_gated_delta_rule_bwd(q, k, v, g, beta, do, dht=None, scale=None, initial_state=None,
                                cu_seqlens=None, use_qk_l2norm=False, cp="auto",
                                cp_segment_chunks=0, grad_dtype=torch.float32,
-                               want_dh0=True, ctx=None):
-    """Low-level backward: returns (dq, dk, dv, dg, dbeta, dh0 or None).
-    `ctx` (optional) is the buffer a forward with the same inputs saved."""
+                               want_dh0=True, ctx=None, gate_scale=None):
+    """Low-level backward: returns (dq, dk, dv, dg, dbeta, dh0 or None), plus
+    d(gate_scale) when `gate_scale` is given (dg is then the gradient with
+    respect to the gate logits).  `ctx` (optional) is the buffer a forward with
+    the same inputs saved."""
     a = _abi.gdn_bwd_args()
     B, T, H, K, V, N, dev = _common(a, q, k, v, g, beta, initial_state, cu_seqlens, scale,
-                                    use_qk_l2norm, cp, cp_segment_chunks)
+                                    use_qk_l2norm, cp, cp_segment_chunks, gate_scale)
     _check("do", do, q.dtype, (B, T, H, V), dev)
     _check("dht", dht, torch.float32, (N, H, K, V), dev)
     if grad_dtype not in _DT:
@@ -116,43 +123,52 @@ def chunk_gated_delta_rule_bwd(q, k, v, g, beta, do, dht=None, scale=None, initi
     a.dq, a.dk, a.dv, a.dg, a.dbeta = (t.data_ptr() for t in (dq, dk, dv, dg, db))
     a.d_initial_state = _ptr(dh0)
     a.ctx = _ptr(ctx)
+    dgs = torch.empty(H, dtype=torch.float32, device=dev) if gate_scale is not None else None
+    a.d_gate_scale = _ptr(dgs)
     n = _abi.gdn_bwd_workspace_size(a)
     ws = torch.empty(n, dtype=torch.uint8, device=dev)
     _abi.gdn_chunk_bwd(a, ws.data_ptr(), n, torch.cuda.current_stream(dev).cuda_stream)
+    if gate_scale is not None:
+        return dq, dk, dv, dg, db, dh0, dgs
     return dq, dk, dv, dg, db, dh0
 
 
 class _ChunkGatedDeltaRule(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, q, k, v, g, beta, initial_state, scale, cu_seqlens, use_qk_l2norm, cp):
+    def forward(ctx, q, k, v, g, beta, initial_state, gate_scale, scale, cu_seqlens,
+                use_qk_l2norm, cp):
         o, fs, saved = chunk_gated_delta_rule_fwd(q, k, v, g, beta, scale=scale,
                                                   initial_state=initial_state,
                                                   output_final_state=True,
                                                   cu_seqlens=cu_seqlens,
                                                   use_qk_l2norm=use_qk_l2norm, cp=cp,
-                                                  save_ctx=True)
-        ctx.save_for_backward(q, k, v, g, beta, initial_state, cu_seqlens, saved)
+                                                  save_ctx=True, gate_scale=gate_scale)
+        ctx.save_for_backward(q, k, v, g, beta, initial_state, cu_seqlens, saved, gate_scale)
         ctx.cfg = (scale, use_qk_l2norm, cp)
         return o, fs
 
     @staticmethod
     def backward(ctx, do, dht):
-        q, k, v, g, beta, h0, cu, saved = ctx.saved_tensors
+        q, k, v, g, beta, h0, cu, saved, gs = ctx.saved_tensors
         scale, l2, cp = ctx.cfg
-        dq, dk, dv, dg, db, dh0 = chunk_gated_delta_rule_bwd(
+        out = chunk_gated_delta_rule_bwd(
             q, k, v, g, beta, do.contiguous().to(q.dtype),
             dht=None if dht is None else dht.contiguous(), scale=scale, initial_state=h0,
-            cu_seqlens=cu, use_qk_l2norm=l2, cp=cp, want_dh0=h0 is not None, ctx=saved)
-        return (dq.to(q.dtype), dk.to(k.dtype), dv.to(v.dtype), dg, db, dh0, None, None, None,
-                None)
+            cu_seqlens=cu, use_qk_l2norm=l2, cp=cp, want_dh0=h0 is not None, ctx=saved,
+            gate_scale=gs)
+        dq, dk, dv, dg, db, dh0 = out[:6]
+        dgs = out[6] if gs is not None else None
+        return (dq.to(q.dtype), dk.to(k.dtype), dv.to(v.dtype), dg, db, dh0, dgs, None, None,
+                None, None)
 
 
 def chunk_gated_delta_rule(q, k, v, g, beta, scale=None, initial_state=None,
                            output_final_state=False, cu_seqlens=None, use_qk_l2norm=False,
-                           cp="auto"):
+                           cp="auto", gate_scale=None):
     """High-level call: (o, final_state or None), differentiable in q, k, v, g,
-    beta and initial_state.  Gradients are cast to the inputs' dtypes only at
-    this autograd boundary."""
-    o, fs = _ChunkGatedDeltaRule.apply(q, k, v, g, beta, initial_state, scale, cu_seqlens,
-                                       use_qk_l2norm, cp)
+    beta, initial_state and gate_scale.  With `gate_scale` ([H], a_h > 0), g
+    holds raw gate logits x and the log decay is -a_h * softplus(x).  Gradients
+    are cast to the inputs' dtypes only at this autograd boundary."""
+    o, fs = _ChunkGatedDeltaRule.apply(q, k, v, g, beta, initial_state, gate_scale, scale,
+                                       cu_seqlens, use_qk_l2norm, cp)
     return o, (fs if output_final_state else None)

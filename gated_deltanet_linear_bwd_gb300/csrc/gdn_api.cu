@@ -81,6 +81,7 @@ struct Common {
     const int32_t *cu;
     int B, T, H, K, V, N, dtype, l2, cp_mode, seg_chunks;
     float scale;
+    const float *gate_scale;
 };
 
 static constexpr size_t kAlign = 256;
@@ -106,7 +107,8 @@ static gdn_status validate(const Common &c) {
         return fail(GDN_ERR_INVALID_ARG, "cp_mode %d", c.cp_mode);
     if (c.seg_chunks < 0) return fail(GDN_ERR_INVALID_ARG, "cp_segment_chunks < 0");
     if (!aligned16(c.q) || !aligned16(c.k) || !aligned16(c.v) || !aligned16(c.g) ||
-        !aligned16(c.beta) || (c.h0 && !aligned16(c.h0)) || (c.cu && !aligned16(c.cu)))
+        !aligned16(c.beta) || (c.h0 && !aligned16(c.h0)) || (c.cu && !aligned16(c.cu)) ||
+        (c.gate_scale && !aligned16(c.gate_scale)))
         return fail(GDN_ERR_INVALID_ARG, "every tensor must be 16-byte aligned");
     const long long tokens = (long long)c.B * c.T;
     if (tokens * c.H * (long long)(c.K > c.V ? c.K : c.V) >= (1ll << 40))
@@ -149,6 +151,7 @@ static gdn_status make_plan(const Common &c, bool bwd, int sms, Plan &p) {
     Geo &g = p.g;
     g = Geo{};
     g.q = c.q; g.k = c.k; g.v = c.v; g.g = c.g; g.beta = c.beta; g.cu = c.cu;
+    g.gate_a = c.gate_scale;
     g.B = c.B; g.T = c.T; g.H = c.H; g.K = c.K; g.V = c.V;
     g.N = c.cu ? c.N : c.B;
     g.nc_fixed = (c.T + kChunk - 1) / kChunk;
@@ -268,12 +271,12 @@ static size_t ctx_layout(Plan &p, char *base) {
 static Common common_of(const gdn_fwd_args *a) {
     return Common{a->q, a->k, a->v, a->g, a->beta, a->initial_state, a->cu_seqlens,
                   a->B, a->T, a->H, a->K, a->V, a->N, a->dtype, a->use_qk_l2norm,
-                  a->cp_mode, a->cp_segment_chunks, a->scale};
+                  a->cp_mode, a->cp_segment_chunks, a->scale, a->gate_scale};
 }
 static Common common_of(const gdn_bwd_args *a) {
     return Common{a->q, a->k, a->v, a->g, a->beta, a->initial_state, a->cu_seqlens,
                   a->B, a->T, a->H, a->K, a->V, a->N, a->dtype, a->use_qk_l2norm,
-                  a->cp_mode, a->cp_segment_chunks, a->scale};
+                  a->cp_mode, a->cp_segment_chunks, a->scale, a->gate_scale};
 }
 
 }  // namespace gdn
@@ -379,7 +382,8 @@ gdn_status gdn_chunk_bwd(const gdn_bwd_args *a, void *ws, size_t ws_bytes, void 
     if (!aligned16(a->d_o) || !aligned16(a->dq) || !aligned16(a->dk) || !aligned16(a->dv) ||
         !aligned16(a->dg) || !aligned16(a->dbeta) ||
         (a->d_final_state && !aligned16(a->d_final_state)) ||
-        (a->d_initial_state && !aligned16(a->d_initial_state)))
+        (a->d_initial_state && !aligned16(a->d_initial_state)) ||
+        (a->d_gate_scale && !aligned16(a->d_gate_scale)))
         return fail(GDN_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
     Plan p;
     gdn_status st = prepare(common_of(a), true, ws, ws_bytes, p);
@@ -397,6 +401,8 @@ gdn_status gdn_chunk_bwd(const gdn_bwd_args *a, void *ws, size_t ws_bytes, void 
     }
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = tc::supported(p) ? tc::backward(p, s, have_ctx) : simt::backward(p, s);
+    if (e == cudaSuccess && a->gate_scale)
+        e = simt::gate_bwd(p, a->gate_scale, a->d_gate_scale, s);
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
     return GDN_OK;
 }

@@ -32,6 +32,7 @@ __device__ __forceinline__ void pdl_enter() {
 struct Geo {
     const void *q, *k, *v;
     const float *g, *beta;
+    const float *gate_a;        // nullable: g holds gate logits x, the log decay is -a_h softplus(x)
     const int32_t *cu;          // nullable: fixed-length rows
     const int32_t *chunk_off;   // [N+1] chunk offsets (varlen only)
     const int32_t *seg_off;     // [N+1] segment offsets (varlen + CP only)
@@ -44,6 +45,15 @@ struct Geo {
     int *status;                // device status word
     long long spin_limit;       // bounded waits
 };
+
+// Log decay of token row i (index of [tokens, H]) and head h: g itself, or
+// -a_h softplus(x) from a gate logit.
+__device__ __forceinline__ float decay_at(const Geo &g, long long i, int h) {
+    const float x = g.g[i];
+    if (!g.gate_a) return x;
+    const float sp = x > 0.f ? x + log1pf(expf(-x)) : log1pf(expf(x));
+    return -g.gate_a[h] * sp;
+}
 
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }

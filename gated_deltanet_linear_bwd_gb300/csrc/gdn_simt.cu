@@ -54,11 +54,11 @@ __device__ void load_rows(float *dst, int ld, const TI *src, long long bos, int 
 }
 
 // gam = inclusive cumsum of g over the chunk (thread 0; 64 adds).
-__device__ void chunk_cumsum(float *gam, const float *g, long long bos, int L, int H, int h) {
+__device__ void chunk_cumsum(float *gam, const Geo &g, long long bos, int L, int H, int h) {
     if (threadIdx.x == 0) {
         float s = 0.f;
         for (int r = 0; r < L; ++r) {
-            s += g[(bos + r) * H + h];
+            s += decay_at(g, (bos + r) * H + h, h);
             gam[r] = s;
         }
     }
@@ -100,7 +100,7 @@ prep_kernel(Geo g, float *ws_gam, float *ws_w, float *ws_u) {
     float *bet = gam + kChunk;            // [64]
     load_rows(Ks, K + 1, (const TI *)g.k, cr.bos, L, H, h, K, g.l2norm, nullptr);
     load_rows(Vs, V + 1, (const TI *)g.v, cr.bos, L, H, h, V, false, nullptr);
-    chunk_cumsum(gam, g.g, cr.bos, L, H, h);
+    chunk_cumsum(gam, g, cr.bos, L, H, h);
     for (int r = threadIdx.x; r < L; r += blockDim.x) bet[r] = g.beta[(cr.bos + r) * H + h];
     __syncthreads();
     for (int r = threadIdx.x; r < L; r += blockDim.x) ws_gam[(cr.bos + r) * H + h] = gam[r];
@@ -413,7 +413,7 @@ __global__ void warm_decide_kernel(Geo g, int wc, float tau, int32_t *warm, int3
             const int t1 = min(len, j * g.seg_chunks * kChunk);
             const int t0 = max(0, t1 - wc * kChunk);
             float s = 0.f;
-            for (int t = t0; t < t1; ++t) s += g.g[(bos + t) * g.H + h];
+            for (int t = t0; t < t1; ++t) s += decay_at(g, (bos + t) * g.H + h, h);
             ok = s < lt;
         }
         warm[n * g.H + h] = ok;
@@ -993,6 +993,42 @@ static cudaError_t forward_t(const Plan &p, cudaStream_t s, bool states_only) {
         GDN_LAUNCH(states_only ? "simt_walk_states" : "simt_walk_out", (walk_kernel<TI, kOut>), dim3(g.N, H, V / kBV), walk_smem(K), s, g, a);
     }
     return cudaSuccess;
+}
+
+// Gate backward over every token of head h (one CTA per head): with the log
+// decay -a_h softplus(x), dx = dg * (-a_h sigmoid(x)) replaces dg, and
+// d a_h = sum over tokens of dg * (-softplus(x)) (a fixed-order block sum).
+__global__ void __launch_bounds__(256)
+gate_bwd_kernel(const float *x, const float *a, float *dg, float *da, long long tokens, int H) {
+    const int h = blockIdx.x;
+    __shared__ float part[256];
+    float acc = 0.f;
+    for (long long t = threadIdx.x; t < tokens; t += blockDim.x) {
+        const long long i = t * H + h;
+        const float xv = x[i], d = dg[i];
+        const float sp = xv > 0.f ? xv + log1pf(expf(-xv)) : log1pf(expf(xv));
+        dg[i] = -a[h] * d / (1.f + expf(-xv));
+        acc -= d * sp;
+    }
+    part[threadIdx.x] = acc;
+    __syncthreads();
+    for (int o = 128; o > 0; o >>= 1) {
+        if ((int)threadIdx.x < o) part[threadIdx.x] += part[threadIdx.x + o];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0 && da) da[h] = part[0];
+}
+
+cudaError_t gate_bwd(const Plan &p, const float *gate_scale, float *d_gate_scale, cudaStream_t s) {
+    const long long tokens = (long long)p.g.B * p.g.T;
+    if (tokens <= 0 || p.g.H <= 0) {
+        if (d_gate_scale && p.g.H > 0) return cudaMemsetAsync(d_gate_scale, 0, sizeof(float) * p.g.H, s);
+        return cudaSuccess;
+    }
+    prof_before("gate_bwd", s);
+    gate_bwd_kernel<<<p.g.H, 256, 0, s>>>(p.g.g, gate_scale, p.dg, d_gate_scale, tokens, p.g.H);
+    prof_after(s);
+    return cudaGetLastError();
 }
 
 cudaError_t warm_decide(const Plan &p, cudaStream_t s) {

@@ -128,7 +128,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         __syncthreads();
         // gam = cumsum(g), beta (zero beyond the chunk)
         const long long tok = mine.bos + r;
-        const float graw = r < L ? g.g[tok * H + h] : 0.f;
+        const float graw = r < L ? decay_at(g, tok * H + h, h) : 0.f;
         const float gam = scan64(graw, s.wsum);
         s.gam[ch][r] = gam;
         s.bet[ch][r] = r < L ? g.beta[tok * H + h] : 0.f;

@@ -145,3 +145,13 @@ def make(name="tiny", seed=None, B=None, T=None, H=None, K=None, V=None, dtype=N
     meta = dict(w, seed=seed, lengths=lengths, dtype=dtype or w["dtype"])
     return Problem(name, q.to(dt), k.to(dt), v.to(dt), g.float().contiguous(),
                    beta.float().contiguous(), h0, cu, do.to(dt), dht, meta)
+
+
+def gate_draws(p: Problem, seed: int = 0, a_lo: float = 0.01):
+    """Seeded raw gate inputs for problem p: logits x ~ N(0, 1) with the shape
+    of p.g, and per-head scales a_h ~ U(a_lo, 1).  Random draws only; the gate
+    itself is applied by each side."""
+    gen = torch.Generator().manual_seed(1000 + int(seed))
+    x = torch.randn(tuple(p.g.shape), generator=gen).float().contiguous()
+    a = (a_lo + (1.0 - a_lo) * torch.rand(p.H, generator=gen)).float().contiguous()
+    return x, a

@@ -44,7 +44,7 @@
 extern "C" {
 #endif
 
-#define GDN_ABI_VERSION 2
+#define GDN_ABI_VERSION 3
 
 typedef int32_t gdn_status;
 enum {
@@ -99,6 +99,11 @@ typedef struct gdn_fwd_args {
                                    gdn_fwd_ctx_size() bytes (256-byte aligned): the
                                    forward also keeps what the backward would
                                    otherwise recompute (see gdn_fwd_ctx_size)        */
+    /* gate preprocessing (the pages' "gate preprocessing" ahead of the kernels,
+       aivizor, FLA-flow paragraph) */
+    const float *gate_scale;    /* NULL: g is the log decay itself.  Else [H] fp32,
+                                   a_h > 0, and g holds raw gate logits x: the log
+                                   decay is -a_h * softplus(x), softplus(x) = log(1 + e^x) */
 } gdn_fwd_args;
 
 typedef struct gdn_bwd_args {
@@ -127,6 +132,10 @@ typedef struct gdn_bwd_args {
     const void *ctx;            /* NULL, or the buffer a gdn_chunk_fwd call with the same
                                    inputs and sizes filled: the backward then skips
                                    recomputing the forward's per-chunk quantities   */
+    const float *gate_scale;    /* as in gdn_fwd_args.  When given, dg receives the
+                                   gradient with respect to the logits x            */
+    float *d_gate_scale;        /* [H] fp32 gradient with respect to gate_scale;
+                                   NULL = not written (ignored without gate_scale)  */
 } gdn_bwd_args;
 
 /* GDN_ABI_VERSION of the loaded library. */

@@ -86,7 +86,7 @@ def _fwd_args(abi, **kw):
 
 
 def test_abi_version_and_workspace_query_need_no_gpu(abi):
-    assert abi.gdn_abi_version() == 2
+    assert abi.gdn_abi_version() == 3
     n_off = abi.gdn_fwd_workspace_size(_fwd_args(abi, cp_mode=abi.GDN_CP_OFF))
     n_cp = abi.gdn_fwd_workspace_size(_fwd_args(abi, cp_mode=abi.GDN_CP_FORCE))
     assert 0 < n_off < n_cp
