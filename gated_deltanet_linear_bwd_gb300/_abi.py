@@ -42,13 +42,21 @@ class gdn_bwd_args(ctypes.Structure):
                 ("gate_scale", _vp), ("d_gate_scale", _vp)]
 
 
+class gdn_step_args(ctypes.Structure):
+    _fields_ = [("q", _vp), ("k", _vp), ("v", _vp), ("g", _vp), ("beta", _vp),
+                ("gate_scale", _vp), ("state", _vp),
+                ("N", _i32), ("H", _i32), ("K", _i32), ("V", _i32), ("dtype", _i32),
+                ("scale", _f32), ("use_qk_l2norm", _i32), ("o", _vp)]
+
+
 class gdn_kernel_stat(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 64), ("launches", _i32), ("total_ms", ctypes.c_double)]
 
 
 EXPORTS = ("gdn_abi_version", "gdn_fwd_workspace_size", "gdn_chunk_fwd", "gdn_bwd_workspace_size",
            "gdn_chunk_bwd", "gdn_sync_status", "gdn_last_error", "gdn_set_spin_limit",
-           "gdn_profile_begin", "gdn_profile_end", "gdn_chunk_fwd_static", "gdn_fwd_ctx_size")
+           "gdn_profile_begin", "gdn_profile_end", "gdn_chunk_fwd_static", "gdn_fwd_ctx_size",
+           "gdn_recurrent_step")
 GDN_STATIC_SCRATCH_BYTES = 64 << 20
 
 _lib = None
@@ -83,6 +91,8 @@ def load(path: str = LIB_PATH):
     lib.gdn_fwd_ctx_size.argtypes = [ctypes.POINTER(gdn_fwd_args)]
     lib.gdn_chunk_fwd_static.restype = _i32
     lib.gdn_chunk_fwd_static.argtypes = [ctypes.POINTER(gdn_fwd_args), _vp]
+    lib.gdn_recurrent_step.restype = _i32
+    lib.gdn_recurrent_step.argtypes = [ctypes.POINTER(gdn_step_args), _vp]
     lib.gdn_profile_begin.restype = _i32
     lib.gdn_profile_begin.argtypes = []
     lib.gdn_profile_end.restype = _i32
@@ -163,3 +173,9 @@ def gdn_chunk_fwd_static(args: gdn_fwd_args, stream: int) -> None:
     rc = load().gdn_chunk_fwd_static(ctypes.byref(args), _vp(stream))
     if rc != GDN_OK:
         raise GdnError("gdn_chunk_fwd_static", rc)
+
+
+def gdn_recurrent_step(args: gdn_step_args, stream: int) -> None:
+    rc = load().gdn_recurrent_step(ctypes.byref(args), _vp(stream))
+    if rc != GDN_OK:
+        raise GdnError("gdn_recurrent_step", rc)

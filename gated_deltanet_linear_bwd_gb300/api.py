@@ -172,3 +172,32 @@ def chunk_gated_delta_rule(q, k, v, g, beta, scale=None, initial_state=None,
     o, fs = _ChunkGatedDeltaRule.apply(q, k, v, g, beta, initial_state, gate_scale, scale,
                                        cu_seqlens, use_qk_l2norm, cp)
     return o, (fs if output_final_state else None)
+
+
+def recurrent_step(q, k, v, g, beta, state, scale=None, use_qk_l2norm=False, gate_scale=None):
+    """One decode step per (sequence, head): q, k [N, H, K], v [N, H, V], g, beta
+    [N, H], state [N, H, K, V] fp32 (updated in place).  Returns o [N, H, V].
+    With `gate_scale`, g holds gate logits as in the chunked forward."""
+    N, H, K = q.shape
+    V = v.shape[-1]
+    dev = q.device
+    if q.dtype not in _DT:
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    _check("q", q, q.dtype, (N, H, K), dev)
+    _check("k", k, q.dtype, (N, H, K), dev)
+    _check("v", v, q.dtype, (N, H, V), dev)
+    _check("g", g, torch.float32, (N, H), dev)
+    _check("beta", beta, torch.float32, (N, H), dev)
+    _check("state", state, torch.float32, (N, H, K, V), dev)
+    _check("gate_scale", gate_scale, torch.float32, (H,), dev)
+    o = torch.empty(N, H, V, dtype=q.dtype, device=dev)
+    a = _abi.gdn_step_args()
+    a.q, a.k, a.v, a.g, a.beta = (t.data_ptr() for t in (q, k, v, g, beta))
+    a.gate_scale = _ptr(gate_scale)
+    a.state, a.o = state.data_ptr(), o.data_ptr()
+    a.N, a.H, a.K, a.V = N, H, K, V
+    a.dtype = _DT[q.dtype]
+    a.scale = float(scale) if scale is not None else 0.0
+    a.use_qk_l2norm = int(bool(use_qk_l2norm))
+    _abi.gdn_recurrent_step(a, torch.cuda.current_stream(dev).cuda_stream)
+    return o

@@ -373,6 +373,28 @@ gdn_status gdn_chunk_fwd(const gdn_fwd_args *a, void *ws, size_t ws_bytes, void 
     return GDN_OK;
 }
 
+gdn_status gdn_recurrent_step(const gdn_step_args *a, void *stream) {
+    if (!a) return fail(GDN_ERR_INVALID_ARG, "null args");
+    if (a->N < 0 || a->H < 0) return fail(GDN_ERR_INVALID_ARG, "N and H must be >= 0");
+    if ((a->K != 64 && a->K != 128) || (a->V != 64 && a->V != 128))
+        return fail(GDN_ERR_UNSUPPORTED, "K = %d, V = %d (64 or 128 supported)", a->K, a->V);
+    if (a->dtype != GDN_FP32 && a->dtype != GDN_BF16)
+        return fail(GDN_ERR_UNSUPPORTED, "dtype %d", a->dtype);
+    if ((long long)a->N * a->H == 0) return GDN_OK;
+    if (!a->q || !a->k || !a->v || !a->g || !a->beta || !a->state || !a->o)
+        return fail(GDN_ERR_INVALID_ARG, "q, k, v, g, beta, state and o are required");
+    if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || !aligned16(a->g) ||
+        !aligned16(a->beta) || !aligned16(a->state) || !aligned16(a->o) ||
+        (a->gate_scale && !aligned16(a->gate_scale)))
+        return fail(GDN_ERR_INVALID_ARG, "every tensor must be 16-byte aligned");
+    DeviceInfo *dev = nullptr;
+    gdn_status st = device_info(&dev);
+    if (st != GDN_OK) return st;
+    const cudaError_t e = step::run(a, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "recurrent step launch");
+    return GDN_OK;
+}
+
 gdn_status gdn_chunk_bwd(const gdn_bwd_args *a, void *ws, size_t ws_bytes, void *stream) {
     if (!a) return fail(GDN_ERR_INVALID_ARG, "null args");
     if ((long long)a->B * a->T > 0 && (!a->d_o || !a->dq || !a->dk || !a->dv || !a->dg || !a->dbeta))

@@ -83,6 +83,11 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+namespace step {
+// One decode step per (sequence, head), the state updated in place.
+cudaError_t run(const gdn_step_args *args, cudaStream_t s);
+}  // namespace step
+
 namespace simt {
 // Per-CTA scratch floats of the local-gradient kernel.
 size_t scratch_floats_per_cta(int K, int V);

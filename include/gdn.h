@@ -197,6 +197,34 @@ gdn_status gdn_chunk_bwd(const gdn_bwd_args *args, void *workspace, size_t works
 #define GDN_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
 gdn_status gdn_chunk_fwd_static(const gdn_fwd_args *args, void *stream);
 
+/* One decode step: the recurrence advanced by a single token per (sequence,
+ * head), the state updated in place.  The pages target prefill ("FlashQLA是什么"
+ * on ollai.cn, section "FlashQLA的主要功能"); this entry point carries the same
+ * gated delta rule to token-by-token generation, so that a model prefilled with
+ * gdn_chunk_fwd can continue from its final state:
+ *     Hbar = exp(g) H;  r = v - Hbar^T k;  H <- Hbar + beta k r^T;  o = scale H^T q
+ * (H = S^T, [K, V]).  Steps taken one after another equal the prefill over
+ * the same tokens up to rounding. */
+typedef struct gdn_step_args {
+    const void *q;              /* [N, H, K], dtype                                 */
+    const void *k;              /* [N, H, K], dtype                                 */
+    const void *v;              /* [N, H, V], dtype                                 */
+    const float *g;             /* [N, H] log decay, or gate logits (gate_scale)    */
+    const float *beta;          /* [N, H]                                           */
+    const float *gate_scale;    /* NULL, or [H]: the log decay is -a_h softplus(g)  */
+    float *state;               /* [N, H, K, V] fp32, read and overwritten          */
+    int32_t N, H, K, V;         /* K, V in {64, 128}                                */
+    int32_t dtype;              /* GDN_FP32 or GDN_BF16                              */
+    float scale;                /* <= 0 means K^-1/2                                */
+    int32_t use_qk_l2norm;      /* as in gdn_fwd_args                                */
+    void *o;                    /* [N, H, V], dtype                                 */
+} gdn_step_args;
+
+/* Asynchronous on `stream`; needs no workspace.  Every pointer 16-byte
+ * aligned.  GDN_ERR_INVALID_ARG / GDN_ERR_UNSUPPORTED for bad arguments
+ * (nothing is launched), GDN_ERR_CUDA for a launch failure. */
+gdn_status gdn_recurrent_step(const gdn_step_args *args, void *stream);
+
 /* Synchronises `stream`, then reads and clears this device's status word:
  * GDN_OK, GDN_ERR_BAD_SEQLENS, GDN_ERR_TIMEOUT or GDN_ERR_CUDA. */
 gdn_status gdn_sync_status(void *stream);
