@@ -326,6 +326,41 @@ def run_ours(args, rank, world, local):
                           else uuid)
     ms_step, _ = timed(lambda: step(d), args.steps)
     ms_fwd, _ = timed(lambda: fwd_only(d), args.steps)
+
+    # the same step with the gate formed inside the library from raw logits
+    import gdn_synth
+    gx, ga = (t.to(dev) for t in gdn_synth.gate_draws(p, seed=0))
+
+    def gated_step(x):
+        o, fs, saved = gdn.chunk_gated_delta_rule_fwd(x.q, x.k, x.v, gx, x.beta,
+                                                      initial_state=x.h0, output_final_state=True,
+                                                      cu_seqlens=x.cu_seqlens, cp=cp,
+                                                      save_ctx=True, gate_scale=ga)
+        return gdn.chunk_gated_delta_rule_bwd(x.q, x.k, x.v, gx, x.beta, x.do, dht=x.dht,
+                                              initial_state=x.h0, cu_seqlens=x.cu_seqlens,
+                                              cp=cp, ctx=saved, gate_scale=ga)
+
+    for _ in range(max(args.warmup, 3)):
+        gated_step(d)
+    ms_gated, _ = timed(lambda: gated_step(d), args.steps)
+
+    # decode: one token for each of 64 sequences x 32 heads from resident fp32 states
+    dn, dh = 64, 32
+    dgen = torch.Generator(device="cpu").manual_seed(7)
+    dq_ = (torch.randn(dn, dh, p.K, generator=dgen) / p.K ** 0.5).to(dev, d.q.dtype)
+    dk_ = (torch.randn(dn, dh, p.K, generator=dgen) / p.K ** 0.5).to(dev, d.q.dtype)
+    dv_ = torch.randn(dn, dh, p.V, generator=dgen).to(dev, d.q.dtype)
+    dg_ = -torch.rand(dn, dh, generator=dgen).to(dev)
+    db_ = torch.rand(dn, dh, generator=dgen).to(dev)
+    dst = (0.1 * torch.randn(dn, dh, p.K, p.V, generator=dgen)).to(dev)
+
+    def decode_step():
+        gdn.recurrent_step(dq_, dk_, dv_, dg_, db_, dst)
+
+    for _ in range(max(args.warmup, 3)):
+        decode_step()
+    ms_dec, _ = timed(decode_step, args.steps)
+    dec_bytes = 2 * dst.numel() * 4 + dn * dh * (2 * p.K + 2 * p.V) * e_in + dn * dh * 8
     # per-kernel times from the library's own CUDA events, in a separate pass: the
     # events between kernels stop them from overlapping, so they stay out of ms_step
     _, prof = timed(lambda: step(d), args.steps, profile=True)
@@ -411,6 +446,15 @@ def run_ours(args, rank, world, local):
             "data": "synthetic (seeded; see gdn_synth.py)", "config": config_of(p, args.workload),
             "fwd": {"value": world * tokens / (ms_fwd / 1e3), "unit": "tokens/s",
                     "ms_per_step": ms_fwd},
+            "decode": {"value": world * dn / (ms_dec / 1e3), "unit": "tokens/s",
+                       "ms_per_step": ms_dec, "batch": f"{dn} sequences x {dh} heads",
+                       "hbm_gbs": dec_bytes / (ms_dec / 1e3) / 1e9,
+                       "frac_of_hbm": dec_bytes / (ms_dec / 1e3) / 1e9 / hbm,
+                       "what": "one gdn_recurrent_step: state read and written once"},
+            "gated": {"value": world * tokens / (ms_gated / 1e3), "unit": "tokens/s",
+                      "ms_per_step": ms_gated,
+                      "what": "the same fwd+bwd step with the decay formed inside from gate "
+                              "logits (gate_scale), d(logits) and d(gate_scale) returned"},
             "step_roofline": {"t_roof_ms": t_roof * 1e3, "frac": t_roof * 1e3 / ms_step,
                               "bytes": step_bytes, "flops": step_flops,
                               "peaks": {"hbm_gbs": hbm, "bf16_tflops": bf16,
