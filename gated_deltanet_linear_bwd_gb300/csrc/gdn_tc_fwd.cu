@@ -37,7 +37,7 @@ constexpr uint32_t kIdescPrepMN = idesc_bf16(128, 64, true, true);
 struct PrepSmem {
     uint8_t k[4 * kTile];          // [dk half][rows 0-63 chunk a, 64-127 chunk b][128 B]
     uint8_t v[4 * kTile];          // same for v
-    float A[2][64][64];            // strict-lower A per chunk; reused for bw/bu below
+    float A[2][64][64];            // A^T per chunk (row j = column j of strict-lower A); reused for bw/bu below
     float gam[2][64], bet[2][64], rk[2][64], wsum[4];
     uint64_t tma_bar, mma_bar;
     uint32_t tmem_base;
@@ -163,40 +163,48 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             s.rk[ch][r] = rk;
             tc_fence_before();
             __syncthreads();
-            const float br = s.bet[ch][r], gr = s.gam[ch][r];
+            // K K^T is symmetric, so this row is also column r: thread r writes
+            // A[i][r] = beta_i (k_i . k_r) e^(gamma_i - gamma_r) for i > r, i.e. row r of A^T
+            const float gr = s.gam[ch][r];
             float4 *arow = reinterpret_cast<float4 *>(s.A[ch][r]);
 #pragma unroll
-            for (int c4 = 0; c4 < 16; ++c4) {
+            for (int i4 = 0; i4 < 16; ++i4) {
                 float x[4];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int c = 4 * c4 + j;
-                    x[j] = (c < r && r < L)
-                               ? br * kk[c] * rk * s.rk[ch][c] * __expf(gr - s.gam[ch][c])
-                               : 0.f;
+                for (int e = 0; e < 4; ++e) {
+                    const int i = 4 * i4 + e;
+                    x[e] = (i > r && i < L) ? s.bet[ch][i] * kk[i] * rk * s.rk[ch][i] *
+                                                  __expf(s.gam[ch][i] - gr)
+                                            : 0.f;
                 }
-                arow[c4] = make_float4(x[0], x[1], x[2], x[3]);
+                arow[i4] = make_float4(x[0], x[1], x[2], x[3]);
             }
         }
         __syncthreads();
         {
-            // column r of T = (I + A)^-1 by forward substitution (A read by broadcast)
+            // column r of T = (I + A)^-1 by right-looking forward substitution: once
+            // entry j is final, it is eliminated from every later row at once (column j
+            // of A = row j of A^T, read by broadcast), so each step is up to 63
+            // independent FMAs and the dependent chain is only 64 long
+            // (a warp whose columns are all >= 32 skips the first 32 steps: they only
+            // touch entries that are zero in its columns)
             float col[64];
 #pragma unroll
             for (int i = 0; i < 64; ++i) col[i] = (i == r) ? 1.f : 0.f;
+            const bool upper = (warp & 1) != 0;
 #pragma unroll
-            for (int i = 1; i < 64; ++i) {
-                const float4 *ar = reinterpret_cast<const float4 *>(s.A[ch][i]);
-                float acc = col[i];
+            for (int j = 0; j < 63; ++j) {
+                if (j < 32 && upper) continue;
+                const float t = col[j];
+                const float4 *ar = reinterpret_cast<const float4 *>(s.A[ch][j]);
 #pragma unroll
-                for (int c4 = 0; c4 < (i + 3) / 4; ++c4) {
-                    const float4 a4 = ar[c4];
-                    if (4 * c4 + 0 < i) acc -= a4.x * col[4 * c4 + 0];
-                    if (4 * c4 + 1 < i) acc -= a4.y * col[4 * c4 + 1];
-                    if (4 * c4 + 2 < i) acc -= a4.z * col[4 * c4 + 2];
-                    if (4 * c4 + 3 < i) acc -= a4.w * col[4 * c4 + 3];
+                for (int i4 = (j + 1) / 4; i4 < 16; ++i4) {
+                    const float4 a4 = ar[i4];
+                    if (4 * i4 + 0 > j) col[4 * i4 + 0] -= a4.x * t;
+                    if (4 * i4 + 1 > j) col[4 * i4 + 1] -= a4.y * t;
+                    if (4 * i4 + 2 > j) col[4 * i4 + 2] -= a4.z * t;
+                    if (4 * i4 + 3 > j) col[4 * i4 + 3] -= a4.w * t;
                 }
-                col[i] = acc;
             }
             if (ws_t && (!ch || has_b)) {
                 // the backward keeps T as bf16: row r of the tile [chunk][h][64][64] is
