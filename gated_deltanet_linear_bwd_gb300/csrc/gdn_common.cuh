@@ -48,11 +48,13 @@ struct Geo {
 
 // Log decay of token row i (index of [tokens, H]) and head h: g itself, or
 // -a_h softplus(x) from a gate logit.
-__device__ __forceinline__ float decay_at(const Geo &g, long long i, int h) {
-    const float x = g.g[i];
+__device__ __forceinline__ float decay_of(const Geo &g, float x, int h) {
     if (!g.gate_a) return x;
     const float sp = x > 0.f ? x + log1pf(expf(-x)) : log1pf(expf(x));
     return -g.gate_a[h] * sp;
+}
+__device__ __forceinline__ float decay_at(const Geo &g, long long i, int h) {
+    return decay_of(g, g.g[i], h);
 }
 
 __device__ __forceinline__ float to_f(float x) { return x; }

@@ -38,7 +38,8 @@ struct PrepSmem {
     uint8_t k[4 * kTile];          // [dk half][rows 0-63 chunk a, 64-127 chunk b][128 B]
     uint8_t v[4 * kTile];          // same for v
     float A[2][64][64];            // A^T per chunk (row j = column j of strict-lower A); reused for bw/bu below
-    float gam[2][64], bet[2][64], rk[2][64], wsum[4];
+    float gam[2][64], bet[2][64], brk[2][64], wsum[4];
+    float gpre[2][64], bpre[2][64];  // g and beta of the item, fetched during the previous one
     uint64_t tma_bar, mma_bar;
     uint32_t tmem_base;
 };
@@ -94,6 +95,15 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         }
     };
 
+    // g and beta of this thread's token in an item, fetched asynchronously (a plain
+    // load would be waited for by the fences between here and its use)
+    auto fetch_gb = [&](int hh, const ChunkRef &rc, bool valid_chunk) {
+        const bool ok = valid_chunk && r < rc.len;
+        const long long i = ok ? (rc.bos + r) * H + hh : 0;
+        cp_async4(&s.gpre[ch][r], g.g + i, ok);
+        cp_async4(&s.bpre[ch][r], g.beta + i, ok);
+    };
+
     if (tid == 0) {
         mbar_init(&s.tma_bar, 1);
         mbar_init(&s.mma_bar, 1);
@@ -113,6 +123,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     bool has_b = false;
     bool have = item_ref(item, pair, h, ra, rb, has_b);
     if (have && tid == 0) load_kv(h, ra, rb);
+    if (have) fetch_gb(h, ch ? rb : ra, !ch || has_b);
     int loads = have ? 1 : 0;                 // TMA loads issued (uniform bookkeeping)
     int it = 0, mma_n = 0;
     bool bailed = false;
@@ -128,10 +139,11 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         __syncthreads();
         // gam = cumsum(g), beta (zero beyond the chunk)
         const long long tok = mine.bos + r;
-        const float graw = r < L ? decay_at(g, tok * H + h, h) : 0.f;
+        cp_async_wait_all();
+        const float graw = r < L ? decay_of(g, s.gpre[ch][r], h) : 0.f;
         const float gam = scan64(graw, s.wsum);
         s.gam[ch][r] = gam;
-        s.bet[ch][r] = r < L ? g.beta[tok * H + h] : 0.f;
+        s.bet[ch][r] = r < L ? s.bpre[ch][r] : 0.f;
         if (r < L) ws_gam[tok * H + h] = gam;
 
         bool ok = mbar_wait(&s.tma_bar, it & 1, g.spin_limit, g.status);
@@ -160,22 +172,24 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
 #pragma unroll
             for (int c = 0; c < 64; ++c) nrm = (c == r) ? kk[c] : nrm;
             const float rk = (r < L) ? (g.l2norm ? rsqrtf(nrm + 1e-6f) : 1.f) : 0.f;
-            s.rk[ch][r] = rk;
+            s.brk[ch][r] = s.bet[ch][r] * rk;
             tc_fence_before();
             __syncthreads();
             // K K^T is symmetric, so this row is also column r: thread r writes
             // A[i][r] = beta_i (k_i . k_r) e^(gamma_i - gamma_r) for i > r, i.e. row r of A^T
             const float gr = s.gam[ch][r];
             float4 *arow = reinterpret_cast<float4 *>(s.A[ch][r]);
+            const float4 *brk4 = reinterpret_cast<const float4 *>(s.brk[ch]);
+            const float4 *gam4 = reinterpret_cast<const float4 *>(s.gam[ch]);
 #pragma unroll
             for (int i4 = 0; i4 < 16; ++i4) {
+                const float4 b4 = brk4[i4], g4 = gam4[i4];
+                const float bb[4] = {b4.x, b4.y, b4.z, b4.w}, gg[4] = {g4.x, g4.y, g4.z, g4.w};
                 float x[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int i = 4 * i4 + e;
-                    x[e] = (i > r && i < L) ? s.bet[ch][i] * kk[i] * rk * s.rk[ch][i] *
-                                                  __expf(s.gam[ch][i] - gr)
-                                            : 0.f;
+                    x[e] = (i > r && i < L) ? bb[e] * kk[i] * rk * __expf(gg[e] - gr) : 0.f;
                 }
                 arow[i4] = make_float4(x[0], x[1], x[2], x[3]);
             }
@@ -229,12 +243,12 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             // and by beta_j (u).
             uint8_t *bw = stage;
             uint8_t *bu = bw + 2 * kTile;
-            const float bj = s.bet[ch][r], ej = __expf(s.gam[ch][r]), rkj = s.rk[ch][r];
+            const float bj = s.bet[ch][r], wj = __expf(s.gam[ch][r]) * s.brk[ch][r];
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
                 float x[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) x[i] = col[32 * q + i] * bj * ej * rkj;
+                for (int i = 0; i < 32; ++i) x[i] = col[32 * q + i] * wj;
                 st_row32(bw + ch * kTile, r, 32 * q, x);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) x[i] = col[32 * q + i] * bj;
@@ -269,7 +283,10 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             fence_proxy_async();
             load_kv(h_n, ra_n, rb_n);
         }
-        if (have_next) ++loads;
+        if (have_next) {
+            ++loads;
+            fetch_gb(h_n, ch ? rb_n : ra_n, !ch || has_b_n);
+        }
         tc_fence_after();
         // thread t = feature index (dk for W, dv for u): its 64 chunk rows form row t
         // of the W^T / u^T tile, staged swizzled in the dead A region (two tiles of
@@ -317,6 +334,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         if (mma_n > 0) mbar_drain(&s.mma_bar, (mma_n - 1) & 1);
     }
     if (tid == 0) bulk_wait_read();
+    cp_async_wait_all();                      // a prefetch still in flight after a bail
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tbase, 256);
