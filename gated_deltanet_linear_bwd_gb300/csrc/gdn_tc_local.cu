@@ -119,6 +119,47 @@ __device__ __forceinline__ float block_sum(float x, float *scratch8) {
     return s;
 }
 
+// 4 x 4 transpose inside each quad of lanes: lane 4j + f holds a[e] = M[f][e]
+// on entry and a[f'] = M[f'][f] on return (two exchange rounds).
+__device__ __forceinline__ void quad_transpose4(float *a) {
+    const int f = threadIdx.x & 3;
+    const bool up2 = (f & 2) != 0, up1 = (f & 1) != 0;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const float r = __shfl_xor_sync(0xffffffffu, up2 ? a[k] : a[k + 2], 2);
+        if (up2) a[k] = r; else a[k + 2] = r;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; k += 2) {
+        const float r = __shfl_xor_sync(0xffffffffu, up1 ? a[k] : a[k + 1], 1);
+        if (up1) a[k] = r; else a[k + 1] = r;
+    }
+}
+
+__device__ __forceinline__ void st4(float *p, const float *a) {
+    *reinterpret_cast<float4 *>(p) = make_float4(a[0], a[1], a[2], a[3]);
+}
+__device__ __forceinline__ void st4(__nv_bfloat16 *p, const float *a) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(a[0], a[1]), hi = __floats2bfloat162_rn(a[2], a[3]);
+    *reinterpret_cast<uint2 *>(p) = make_uint2(*reinterpret_cast<uint32_t *>(&lo),
+                                              *reinterpret_cast<uint32_t *>(&hi));
+}
+
+// Feature-major results to a row-major [rows][features] tensor: lane l holds
+// feature l of the warp's 32 at rows r0 .. r0+7 (x[e] is row r0 + e; `col`
+// points at row 0, feature l; rows are rs elements apart).  After a quad
+// transpose lane 4j + f writes features 4j .. 4j+3 of rows r0 + f and r0 + 4 + f
+// as one 16-byte (fp32) or 8-byte (bf16) store each; rows >= L are skipped.
+template <typename TG>
+__device__ __forceinline__ void store_rows8(TG *col, long long rs, float (&x)[8], int r0, int L) {
+    const int f = threadIdx.x & 3;
+    quad_transpose4(x);
+    quad_transpose4(x + 4);
+    TG *p = col - f + (long long)(r0 + f) * rs;
+    if (r0 + f < L) st4(p, x);
+    if (r0 + 4 + f < L) st4(p + 4 * rs, x + 4);
+}
+
 // 8 bf16 of a 128-byte swizzled row: columns 8 * chunk .. +7.
 __device__ __forceinline__ void ld_row8(const uint8_t *tile, int row, int chunk, float *x) {
     const uint4 raw = *reinterpret_cast<const uint4 *>(
@@ -367,10 +408,13 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
                            tmem_addr(t_dkh, warp, c0 + 8 * q), yw, yu, pz);
                 st_row8(dywT, v, cq + q, yw);
                 st_row8(dyuT, v, cq + q, yu);
+                float dvq[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) dvq[e] = s.bet[c0 + 8 * q + e] * yu[e];
+                store_rows8(dv, (long long)H * kD, dvq, c0 + 8 * q, L);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int c = c0 + 8 * q + e;
-                    if (c < L) from_f(dv + (long long)c * H * kD, s.bet[c] * yu[e]);
                     const float kv = c < L ? ld_bf16(krow, c, v & 63) : 0.f;
                     yw[e] *= kv;
                     yu[e] = c < L ? yu[e] * ld_bf16(vrow, c, v & 63) : 0.f;
@@ -530,22 +574,18 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
             TG *dk = (TG *)a.dk + (bos * H + h) * (long long)kD + v;
 #pragma unroll 1
             for (int q = 0; q < 4; ++q) {
-                float x[8], y[8], pw[8];
-                tmem_ld8x2(tmem_addr(t_q1, warp, c0 + 8 * q), tmem_addr(t_q2, warp, c0 + 8 * q),
-                           x, y);
+                float x[8], y[8], pw[8], x1[8], y1[8];
+                tmem_ld8x5(tmem_addr(t_q1, warp, c0 + 8 * q), tmem_addr(t_q2, warp, c0 + 8 * q),
+                           tmem_addr(t_dk, warp, c0 + 8 * q), tmem_addr(t_dkh, warp, c0 + 8 * q),
+                           tmem_addr(t_yw, warp, c0 + 8 * q), x1, y1, x, y, pw);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int c = c0 + 8 * q + e;
-                    if (c < L) from_f(dq + c * rs, scale * s.ee[c] * x[e] + y[e]);
+                    x1[e] = scale * s.ee[c] * x1[e] + y1[e];
+                    x[e] = x[e] + s.ff[c] * y[e] + s.bet[c] * s.ee[c] * pw[e];
                 }
-                tmem_ld8x3(tmem_addr(t_dk, warp, c0 + 8 * q), tmem_addr(t_dkh, warp, c0 + 8 * q),
-                           tmem_addr(t_yw, warp, c0 + 8 * q), x, y, pw);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int c = c0 + 8 * q + e;
-                    if (c < L)
-                        from_f(dk + c * rs, x[e] + s.ff[c] * y[e] + s.bet[c] * s.ee[c] * pw[e]);
-                }
+                store_rows8(dq, rs, x1, c0 + 8 * q, L);
+                store_rows8(dk, rs, x, c0 + 8 * q, L);
             }
         }
         {

@@ -247,6 +247,35 @@ __device__ __forceinline__ void tmem_ld8x3(uint32_t a0, uint32_t a1, uint32_t a2
     }
 }
 
+__device__ __forceinline__ void tmem_ld8x5(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                           uint32_t a4, float *v0, float *v1, float *v2,
+                                           float *v3, float *v4) {
+    uint32_t r[40];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%40];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8,%9,%10,%11,%12,%13,%14,%15}, [%41];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%16,%17,%18,%19,%20,%21,%22,%23}, [%42];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%24,%25,%26,%27,%28,%29,%30,%31}, [%43];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%32,%33,%34,%35,%36,%37,%38,%39}, [%44];\n"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+          "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+          "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]),
+          "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(a4)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        v0[i] = __uint_as_float(r[i]);
+        v1[i] = __uint_as_float(r[8 + i]);
+        v2[i] = __uint_as_float(r[16 + i]);
+        v3[i] = __uint_as_float(r[24 + i]);
+        v4[i] = __uint_as_float(r[32 + i]);
+    }
+}
+
 // Writes 8 bf16 values (columns 8 * chunk .. +7) of a 128-byte swizzled row.
 __device__ __forceinline__ void st_row8(uint8_t *tile, int row, int chunk, const float *x) {
     uint32_t w[4];
