@@ -291,7 +291,9 @@ walk_kernel(Geo g, WalkArgs a) {
 // d(final state) and end[j-1] = A'_j end[j] + B'_j.  The maps of the next
 // two steps are copied into shared memory (cp.async, three buffers, rows
 // padded by 4 floats against bank conflicts) while the current step
-// computes; thread t owns row t/2 and four of the kSB columns.
+// computes.  Thread t owns four of the kSB columns of rows r and r + 64
+// (r = (t % 128) / 2) over one half of the contraction index (t / 128); the
+// halves meet in shared memory, so each 16-byte read of A or S feeds more FMAs.
 constexpr int kSB = 8;
 constexpr int kScanStages = 3;
 
@@ -323,8 +325,9 @@ map_scan_kernel(Geo g, const float *maps, const float *init, const int32_t *warm
     float *Abuf = sm;                            // [kScanStages][K][ld]
     float *Bbuf = Abuf + kScanStages * K * ld;   // [kScanStages][K][kSB]
     float *S = Bbuf + kScanStages * K * kSB;     // [K][kSB]
-    const int t = threadIdx.x, i = t >> 1, jq = (t & 1) * 4;
-    const bool act = i < K;
+    float *X = S + K * kSB;                      // [K][kSB] upper-half partial sums
+    constexpr int R = K / 64;                    // rows per thread
+    const int t = threadIdx.x, kh = t >> 7, r2 = (t & 127) >> 1, jq = (t & 1) * 4;
     auto stage = [&](int step, int buf) {
         const int j = reverse ? nseg - 1 - step : step;
         const float *M = maps + ((long long)(sbase + j) * H + h) * K * (K + V);
@@ -361,36 +364,66 @@ map_scan_kernel(Geo g, const float *maps, const float *init, const int32_t *warm
         __syncthreads();
         const int j = reverse ? nseg - 1 - step : step;      // map applied
         const int jo = reverse ? j - 1 : j + 1;              // segment that receives the state
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (act) {
-            const float *A = Abuf + buf * K * ld + i * ld;
-            acc = *reinterpret_cast<const float4 *>(Bbuf + buf * K * kSB + i * kSB + jq);
+        float4 acc[R];
 #pragma unroll
-            for (int l4 = 0; l4 < K / 4; ++l4) {
-                const float4 a4 = *reinterpret_cast<const float4 *>(A + 4 * l4);
-                const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+        for (int m = 0; m < R; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+        {
+            const float *A = Abuf + buf * K * ld;
+            const int l0 = kh * (K / 2);
+#pragma unroll 4
+            for (int l4 = 0; l4 < K / 8; ++l4) {
+                const int l = l0 + 4 * l4;
+                float4 s4[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float4 s4 = *reinterpret_cast<const float4 *>(&S[(4 * l4 + e) * kSB + jq]);
-                    acc.x += av[e] * s4.x;
-                    acc.y += av[e] * s4.y;
-                    acc.z += av[e] * s4.z;
-                    acc.w += av[e] * s4.w;
+                for (int e = 0; e < 4; ++e)
+                    s4[e] = *reinterpret_cast<const float4 *>(&S[(l + e) * kSB + jq]);
+#pragma unroll
+                for (int m = 0; m < R; ++m) {
+                    const float4 a4 = *reinterpret_cast<const float4 *>(A + (r2 + 64 * m) * ld + l);
+                    const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        acc[m].x += av[e] * s4[e].x;
+                        acc[m].y += av[e] * s4[e].y;
+                        acc[m].z += av[e] * s4[e].z;
+                        acc[m].w += av[e] * s4[e].w;
+                    }
                 }
             }
         }
+        if (kh == 1) {
+#pragma unroll
+            for (int m = 0; m < R; ++m)
+                *reinterpret_cast<float4 *>(&X[(r2 + 64 * m) * kSB + jq]) = acc[m];
+        } else {
+            // B now: the next step's prefetch may refill this buffer once all
+            // threads are past the barrier below
+#pragma unroll
+            for (int m = 0; m < R; ++m) {
+                const float4 b = *reinterpret_cast<const float4 *>(Bbuf + buf * K * kSB +
+                                                                   (r2 + 64 * m) * kSB + jq);
+                acc[m] = make_float4(acc[m].x + b.x, acc[m].y + b.y, acc[m].z + b.z, acc[m].w + b.w);
+            }
+        }
         __syncthreads();
-        if (act) {
-            *reinterpret_cast<float4 *>(&S[i * kSB + jq]) = acc;
-            float *dst = out + (((long long)(sbase + jo) * H + h) * K + i) * V + col0 + jq;
-            *reinterpret_cast<float4 *>(dst) = acc;
+        if (kh == 0) {
+#pragma unroll
+            for (int m = 0; m < R; ++m) {
+                const int i = r2 + 64 * m;
+                const float4 x = *reinterpret_cast<const float4 *>(&X[i * kSB + jq]);
+                const float4 r = make_float4(acc[m].x + x.x, acc[m].y + x.y, acc[m].z + x.z,
+                                             acc[m].w + x.w);
+                *reinterpret_cast<float4 *>(&S[i * kSB + jq]) = r;
+                float *dst = out + (((long long)(sbase + jo) * H + h) * K + i) * V + col0 + jq;
+                *reinterpret_cast<float4 *>(dst) = r;
+            }
         }
     }
 }
 
 static size_t map_scan_smem(int K) {
     // K in {64, 128}; the kernel is instantiated for both
-    return sizeof(float) * (kScanStages * K * (K + 4) + kScanStages * K * kSB + K * kSB);
+    return sizeof(float) * (kScanStages * K * (K + 4) + kScanStages * K * kSB + 2 * K * kSB);
 }
 
 // Warmup shortcut decision per (sequence, head): every segment j > 0 must

@@ -331,12 +331,31 @@ tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
     seq_range(g, n, sbos, slen);
     const bool tma_thread = tid == 255;
 
+    auto issue_tma = [&](int st, int c) {
+        const int tok0 = (int)(sbos + (long long)c * kChunk);
+        const int trow = (int)(((long long)(cbase + c) * H + h) * kD);
+        mbar_arrive_expect_tx(&s.tma_bar[st], (use_do ? 10 : 4) * kTile);
+        tma_load_3d(s.k[st], &m.k, &s.tma_bar[st], 0, h, tok0);
+        tma_load_3d(s.k[st] + kTile, &m.k, &s.tma_bar[st], 64, h, tok0);
+        tma_load_2d(s.w[st], &m.w, &s.tma_bar[st], 0, trow);
+        if (use_do) {
+            tma_load_3d(s.dO[st], &m.dO, &s.tma_bar[st], 0, h, tok0);
+            tma_load_3d(s.dO[st] + kTile, &m.dO, &s.tma_bar[st], 64, h, tok0);
+            tma_load_2d(s.qs[st], &m.qs, &s.tma_bar[st], 0, trow);
+            tma_load_2d(s.qs[st] + kTile, &m.qs, &s.tma_bar[st], 0, trow + 64);
+            tma_load_2d(s.y[st], &m.y, &s.tma_bar[st], 0, trow);
+        }
+    };
+
+    // the first chunk's tiles are requested at once, so that their latency
+    // overlaps the start gradient's load
     if (tid == 0) {
         mbar_init(&s.tma_bar[0], 1);
         mbar_init(&s.tma_bar[1], 1);
         mbar_init(&s.bar_x, 1);
         mbar_init(&s.bar_z, 1);
         fence_barrier_init();
+        if (c1 > c0) issue_tma(0, c1 - 1);
     }
     if (warp == 0) {
         tmem_alloc(&s.tmem_base, 256);
@@ -369,30 +388,11 @@ tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
     const uint32_t tbase = s.tmem_base;
     const uint32_t t_x = tbase, t_z = tbase + 128;
 
-    auto issue_tma = [&](int st, int c) {
-        const int tok0 = (int)(sbos + (long long)c * kChunk);
-        const int trow = (int)(((long long)(cbase + c) * H + h) * kD);
-        mbar_arrive_expect_tx(&s.tma_bar[st], (use_do ? 10 : 4) * kTile);
-        tma_load_3d(s.k[st], &m.k, &s.tma_bar[st], 0, h, tok0);
-        tma_load_3d(s.k[st] + kTile, &m.k, &s.tma_bar[st], 64, h, tok0);
-        tma_load_2d(s.w[st], &m.w, &s.tma_bar[st], 0, trow);
-        if (use_do) {
-            tma_load_3d(s.dO[st], &m.dO, &s.tma_bar[st], 0, h, tok0);
-            tma_load_3d(s.dO[st] + kTile, &m.dO, &s.tma_bar[st], 64, h, tok0);
-            tma_load_2d(s.qs[st], &m.qs, &s.tma_bar[st], 0, trow);
-            tma_load_2d(s.qs[st] + kTile, &m.qs, &s.tma_bar[st], 0, trow + 64);
-            tma_load_2d(s.y[st], &m.y, &s.tma_bar[st], 0, trow);
-        }
-    };
-
     // one commit per barrier per chunk: every barrier's parity is the chunk
     // iteration's; `pend` marks groups committed in this iteration, not yet waited
     int it = 0, tma_pending = 0, pend = 0;
     bool bailed = false;
-    if (c1 > c0) {
-        if (tma_thread) issue_tma(0, c1 - 1);
-        tma_pending |= 1;
-    }
+    if (c1 > c0) tma_pending |= 1;            // issued above
     for (int c = c1 - 1; c >= c0; --c, ++it) {
         const int st = it & 1;
         const uint32_t par = it & 1;

@@ -415,11 +415,24 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         cstart = max(0, c0 - a.warm_chunks);
     }
 
+    auto issue_tma = [&](int st, int c) {
+        const int tok0 = (int)(sbos + (long long)c * kChunk);
+        mbar_arrive_expect_tx(&s.tma_bar[st], 6 * kTile);   // K (2 halves), W^T, u^T
+        tma_load_3d(s.k[st], &tm_k, &s.tma_bar[st], 0, h, tok0);
+        tma_load_3d(s.k[st] + kTile, &tm_k, &s.tma_bar[st], 64, h, tok0);
+        const int trow = (int)(((long long)(cbase + c) * H + h) * kD);
+        tma_load_2d(s.w[st], &tm_w, &s.tma_bar[st], 0, trow);
+        tma_load_2d(s.u[st], &tm_u, &s.tma_bar[st], 0, trow);
+    };
+
+    // the first chunks' tiles are requested at once, so that their latency
+    // overlaps the start state's load
     if (tid == 0) {
         for (int i = 0; i < kWalkStages; ++i) mbar_init(&s.tma_bar[i], 1);
         mbar_init(&s.bar_u, 1);
         mbar_init(&s.bar_dh, 1);
         fence_barrier_init();
+        for (int i = 0; i < kWalkStages - 1 && cstart + i < c1; ++i) issue_tma(i, cstart + i);
     }
     if (warp == 0) {
         tmem_alloc(&s.tmem_base, 256);
@@ -453,16 +466,6 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     const uint32_t tbase = s.tmem_base;
     const uint32_t t_u = tbase, t_dh = tbase + 128;
 
-    auto issue_tma = [&](int st, int c) {
-        const int tok0 = (int)(sbos + (long long)c * kChunk);
-        mbar_arrive_expect_tx(&s.tma_bar[st], 6 * kTile);   // K (2 halves), W^T, u^T
-        tma_load_3d(s.k[st], &tm_k, &s.tma_bar[st], 0, h, tok0);
-        tma_load_3d(s.k[st] + kTile, &tm_k, &s.tma_bar[st], 64, h, tok0);
-        const int trow = (int)(((long long)(cbase + c) * H + h) * kD);
-        tma_load_2d(s.w[st], &tm_w, &s.tma_bar[st], 0, trow);
-        tma_load_2d(s.u[st], &tm_u, &s.tma_bar[st], 0, trow);
-    };
-
     // one commit per barrier per chunk: every barrier's parity is the chunk
     // iteration's; `pend` marks groups committed in this iteration, not yet waited
     // uniform bookkeeping for the bail-out path: loads issued per stage, and
@@ -478,10 +481,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     // the last warp issues the loads, away from warp 0 (MMA issue) and the
     // threads that read gam
     const bool tma_thread = tid == 255;
-    for (int i = 0; i < kWalkStages - 1 && cstart + i < c1; ++i) {
-        if (tma_thread) issue_tma(i, cstart + i);
-        note_load(i);
-    }
+    for (int i = 0; i < kWalkStages - 1 && cstart + i < c1; ++i) note_load(i);   // issued above
     for (int c = cstart; c < c1; ++c, ++it) {
         const int st = it % kWalkStages, gb = it & 1;
         const uint32_t par = it & 1;

@@ -231,16 +231,21 @@ tc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         if (have_next) ++issued[2];
         tc_fence_after();
         {
-            // O rows r, feature v: a warp's lanes write 32 consecutive features per store
+            // O rows r, feature v; each group of 8 rows leaves as 8-byte row pieces
+            // (four features) after a quad transpose
             __nv_bfloat16 *dst = o + (bos * H + h) * (long long)kD + v;
             float oi[32], oa[32];
             tmem_ld32(tmem_addr(t_oi, warp, c0), oi);
             tmem_ld32(tmem_addr(t_oa, warp, c0), oa);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const int r = c0 + e;
-                if (r < L)
-                    dst[(long long)r * H * kD] = __float2bfloat16_rn(g.scale * (oi[e] * s.er[r] + oa[e]));
+            for (int q = 0; q < 4; ++q) {
+                float x[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int r = c0 + 8 * q + e;
+                    x[e] = g.scale * (oi[8 * q + e] * s.er[r] + oa[8 * q + e]);
+                }
+                store_rows8(dst, (long long)H * kD, x, c0 + 8 * q, L);
             }
         }
         item += (int)gridDim.x;

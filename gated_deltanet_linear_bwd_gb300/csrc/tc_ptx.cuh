@@ -346,6 +346,47 @@ __device__ __forceinline__ void st_row64(uint8_t *tile, int row, const float *x)
     st_row32(tile, row, 32, x + 32);
 }
 
+// 4 x 4 transpose inside each quad of lanes: lane 4j + f holds a[e] = M[f][e]
+// on entry and a[f'] = M[f'][f] on return (two exchange rounds).
+__device__ __forceinline__ void quad_transpose4(float *a) {
+    const int f = threadIdx.x & 3;
+    const bool up2 = (f & 2) != 0, up1 = (f & 1) != 0;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const float r = __shfl_xor_sync(0xffffffffu, up2 ? a[k] : a[k + 2], 2);
+        if (up2) a[k] = r; else a[k + 2] = r;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; k += 2) {
+        const float r = __shfl_xor_sync(0xffffffffu, up1 ? a[k] : a[k + 1], 1);
+        if (up1) a[k] = r; else a[k + 1] = r;
+    }
+}
+
+__device__ __forceinline__ void st4(float *p, const float *a) {
+    *reinterpret_cast<float4 *>(p) = make_float4(a[0], a[1], a[2], a[3]);
+}
+__device__ __forceinline__ void st4(__nv_bfloat16 *p, const float *a) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(a[0], a[1]), hi = __floats2bfloat162_rn(a[2], a[3]);
+    *reinterpret_cast<uint2 *>(p) = make_uint2(*reinterpret_cast<uint32_t *>(&lo),
+                                              *reinterpret_cast<uint32_t *>(&hi));
+}
+
+// Feature-major results to a row-major [rows][features] tensor: lane l holds
+// feature l of the warp's 32 at rows r0 .. r0+7 (x[e] is row r0 + e; `col`
+// points at row 0, feature l; rows are rs elements apart).  After a quad
+// transpose lane 4j + f writes features 4j .. 4j+3 of rows r0 + f and r0 + 4 + f
+// as one 16-byte (fp32) or 8-byte (bf16) store each; rows >= L are skipped.
+template <typename TG>
+__device__ __forceinline__ void store_rows8(TG *col, long long rs, float (&x)[8], int r0, int L) {
+    const int f = threadIdx.x & 3;
+    quad_transpose4(x);
+    quad_transpose4(x + 4);
+    TG *p = col - f + (long long)(r0 + f) * rs;
+    if (r0 + f < L) st4(p, x);
+    if (r0 + 4 + f < L) st4(p + 4 * rs, x + 4);
+}
+
 __device__ __forceinline__ float ld_bf16(const uint8_t *tile, int row, int col) {
     return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tile + sw128_off(row, col)));
 }
