@@ -275,7 +275,7 @@ struct DWalkSmem {
     uint8_t dhT[4 * kTile];        // dH^T: [k half][128 rows v][128 B]   K-major A
     uint8_t duT[2 * kTile];        // dU^T: [128 rows v][64 chunk rows]    K-major A
     float gam[2][64];
-    float fr[64];                  // exp(gam_L - gam_r) (x 1/|k_r|), 0 past L
+    alignas(16) float fr[64];      // exp(gam_L - gam_r) (x 1/|k_r|), 0 past L
     float rk[64];
     uint64_t tma_bar[2], bar_x, bar_z;
     uint32_t tmem_base;
@@ -469,10 +469,14 @@ tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
             if (use_do)
                 raw = *reinterpret_cast<const uint4 *>(s.y[st] + v * 128 + ((chunk ^ (v & 7)) << 4));
             const __nv_bfloat16 *bv = reinterpret_cast<const __nv_bfloat16 *>(&raw);
+            // f of rows 8 chunk .. +7 as two 16-byte broadcast reads
+            const float4 f0 = reinterpret_cast<const float4 *>(s.fr)[2 * chunk];
+            const float4 f1 = reinterpret_cast<const float4 *>(s.fr)[2 * chunk + 1];
+            const float fq[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const int r = 8 * chunk + e;
-                x[e] = r < L ? __bfloat162float(bv[e]) + s.fr[r] * x[e] : 0.f;
+                x[e] = r < L ? __bfloat162float(bv[e]) + fq[e] * x[e] : 0.f;
             }
             st_row8(s.duT, v, chunk, x);
         }

@@ -352,7 +352,7 @@ struct WalkSmem {
     uint8_t hT[4 * kTile];         // [dk half][128 state rows][128 B]  (A operand)
     uint8_t uTs[2 * kTile];        // U^T diag(f): [128 state rows][64 chunk rows] (A operand)
     float gam[2][64];
-    float fr[64];                  // exp(gam_L - gam_r) (x 1/|k_r|); 0 past L
+    alignas(16) float fr[64];      // exp(gam_L - gam_r) (x 1/|k_r|); 0 past L
     float rk[64];
     uint64_t tma_bar[kWalkStages], bar_u, bar_dh;
     uint32_t tmem_base;
@@ -559,10 +559,14 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             if (!a_cols)
                 raw = *reinterpret_cast<const uint4 *>(s.u[st] + v * 128 + ((chunk ^ (v & 7)) << 4));
             const __nv_bfloat16 *bv = reinterpret_cast<const __nv_bfloat16 *>(&raw);
+            // f of rows 8 chunk .. +7 as two 16-byte broadcast reads
+            const float4 f0 = reinterpret_cast<const float4 *>(s.fr)[2 * chunk];
+            const float4 f1 = reinterpret_cast<const float4 *>(s.fr)[2 * chunk + 1];
+            const float fq[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const int r = 8 * chunk + e;
-                uu[e] = r < L ? (__bfloat162float(bv[e]) - x[e]) * s.fr[r] : 0.f;
+                uu[e] = r < L ? (__bfloat162float(bv[e]) - x[e]) * fq[e] : 0.f;
             }
             st_row8(s.uTs, v, chunk, uu);
         }
