@@ -400,21 +400,9 @@ tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
         const int L = min(kChunk, slen - c * kChunk);
         const int trow = (int)(((long long)(cbase + c) * H + h) * kD);
         pend = 0;
-        if (c - 1 >= c0) {
-            if (tma_thread) {
-                fence_proxy_async();
-                issue_tma(st ^ 1, c - 1);
-            }
-            tma_pending |= 1 << (st ^ 1);
-            // gam of chunk c - 1 (a full chunk) into the other buffer, asynchronously
-            if (tid < 64) cp_async4(&s.gam[st ^ 1][tid], a.ws_gam + (bos - kChunk + tid) * H + h, true);
-        }
-        if (MODE == kDOut && tma_thread) {
-            // the gradient at this chunk's end: the bf16 dH^T tile, by TMA
-            tma_store_2d(&m.dhc, s.dhT, 0, 2 * trow);
-            tma_store_2d(&m.dhc, s.dhT + 2 * kTile, 0, 2 * trow + kD);
-            bulk_commit();
-        }
+        // gam of chunk c - 1 (a full chunk) into the other buffer, asynchronously
+        if (c - 1 >= c0 && tid < 64)
+            cp_async4(&s.gam[st ^ 1][tid], a.ws_gam + (bos - kChunk + tid) * H + h, true);
         bool ok = mbar_wait(&s.tma_bar[st], (it >> 1) & 1, g.spin_limit, g.status);
         if (__syncthreads_or(!ok)) { bailed = true; break; }
         tma_pending &= ~(1 << st);
@@ -437,6 +425,21 @@ tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
             }
         }
         pend = 1;
+        // while the products run, the last warp requests chunk c - 1 (into the
+        // stage the previous chunk used) and stores the gradient at this chunk's end
+        if (c - 1 >= c0) {
+            if (tma_thread) {
+                fence_proxy_async();
+                issue_tma(st ^ 1, c - 1);
+            }
+            tma_pending |= 1 << (st ^ 1);
+        }
+        if (MODE == kDOut && tma_thread) {
+            // the bf16 dH^T tile, by TMA
+            tma_store_2d(&m.dhc, s.dhT, 0, 2 * trow);
+            tma_store_2d(&m.dhc, s.dhT + 2 * kTile, 0, 2 * trow + kD);
+            bulk_commit();
+        }
         if (g.l2norm && tid >= 64 && tid < 128) {
             const int r = tid - 64;
             float ss = 0.f;

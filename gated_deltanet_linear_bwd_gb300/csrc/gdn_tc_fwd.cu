@@ -488,28 +488,12 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         const long long bos = sbos + (long long)c * kChunk;
         const int L = min(kChunk, slen - c * kChunk);
         pend = 0;
-        if (c + kWalkStages - 1 < c1) {
-            // the stage the previous chunk used takes the chunk two ahead
-            const int sn = (it + kWalkStages - 1) % kWalkStages;
-            if (tma_thread) {
-                fence_proxy_async();
-                issue_tma(sn, c + kWalkStages - 1);
-            }
-            note_load(sn);
-        }
         if (c + 1 < c1) {
             const int Ln = min(kChunk, slen - (c + 1) * kChunk);
             // gam of the next chunk into the other buffer, asynchronously
             if (tid < 64)
                 cp_async4(&s.gam[gb ^ 1][tid], a.ws_gam + (bos + kChunk + min(tid, Ln - 1)) * H + h,
                           tid < Ln);
-        }
-        if (states && c >= c0 && tma_thread) {
-            // the chunk's start state: the bf16 H^T tile in shared memory, by TMA
-            const int row = (int)(((long long)(cbase + c) * H + h) * 2 * kD);
-            tma_store_2d(&tm_hc, s.hT, 0, row);
-            tma_store_2d(&tm_hc, s.hT + 2 * kTile, 0, row + kD);
-            bulk_commit();
         }
         bool ok = mbar_wait(&s.tma_bar[st], (it / kWalkStages) & 1, g.spin_limit, g.status);
         if (__syncthreads_or(!ok)) { bailed = true; break; }
@@ -526,6 +510,23 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             mma_commit(&s.bar_u);
         }
         pend = 1;
+        // while the product runs, the last warp requests the chunk two ahead (into
+        // the stage the previous chunk used) and stores this chunk's start state
+        if (c + kWalkStages - 1 < c1) {
+            const int sn = (it + kWalkStages - 1) % kWalkStages;
+            if (tma_thread) {
+                fence_proxy_async();
+                issue_tma(sn, c + kWalkStages - 1);
+            }
+            note_load(sn);
+        }
+        if (states && c >= c0 && tma_thread) {
+            // the bf16 H^T tile in shared memory, by TMA
+            const int row = (int)(((long long)(cbase + c) * H + h) * 2 * kD);
+            tma_store_2d(&tm_hc, s.hT, 0, row);
+            tma_store_2d(&tm_hc, s.hT + 2 * kTile, 0, row + kD);
+            bulk_commit();
+        }
         if (g.l2norm && tid >= 64 && tid < 128) {
             // 1 / |k_r| from the K rows
             const int r = tid - 64;
