@@ -206,13 +206,14 @@ def workload_problem(name):
     return gdn_synth.make(name)
 
 
-def config_of(p, name):
+def config_of(p, name, graph=False):
     m = p.meta
     return {"workload": f"{name}: B={p.B} T={p.T} H={p.H} K={p.K} V={p.V} "
                         f"{m['dtype']} q/k/v, fp32 g/beta/state, cp={m['cp']}, "
                         f"fwd (keeping its context) + bwd",
             "global_batch": p.B, "seq_len": p.T, "heads": p.H, "parallelism": "replicas",
-            "l2_flush_between_steps": True}
+            "l2_flush_between_steps": True,
+            **({"launch": "one CUDA graph per step"} if graph else {})}
 
 
 def run_reference(args, rank, world):
@@ -314,18 +315,40 @@ def run_ours(args, rank, world, local):
         ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / steps
         return ms, prof
 
+    def graphed(fn):
+        # fn captured once as a CUDA graph: the library launches only on the current
+        # stream and neither allocates nor synchronises inside a call, so a whole
+        # step replays as one graph launch (same kernels, no per-launch host work)
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            for _ in range(2):
+                fn()
+        torch.cuda.current_stream(dev).wait_stream(side)
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            fn()
+        torch.cuda.synchronize(dev)
+        return graph.replay
+
     for _ in range(max(args.warmup, 3)):
         step(d)
     torch.cuda.synchronize(dev)
     if gdn.gdn_sync_status(stream.cuda_stream) != 0:
         raise RuntimeError("device status after warm-up: " + gdn.gdn_last_error())
+    step_g = graphed(lambda: step(d))
+    fwd_g = graphed(lambda: fwd_only(d))
+    for _ in range(max(args.warmup, 3)):
+        step_g()
+        fwd_g()
 
     gpu_index = torch.cuda.get_device_properties(dev)
     uuid = getattr(gpu_index, "uuid", None)
     clocks = ClockSampler(f"GPU-{uuid}" if uuid is not None and not str(uuid).startswith("GPU")
                           else uuid)
-    ms_step, _ = timed(lambda: step(d), args.steps)
-    ms_fwd, _ = timed(lambda: fwd_only(d), args.steps)
+    ms_step, _ = timed(step_g, args.steps)
+    ms_fwd, _ = timed(fwd_g, args.steps)
 
     # the same step with the gate formed inside the library from raw logits
     import gdn_synth
@@ -340,9 +363,10 @@ def run_ours(args, rank, world, local):
                                               initial_state=x.h0, cu_seqlens=x.cu_seqlens,
                                               cp=cp, ctx=saved, gate_scale=ga)
 
+    gated_g = graphed(lambda: gated_step(d))
     for _ in range(max(args.warmup, 3)):
-        gated_step(d)
-    ms_gated, _ = timed(lambda: gated_step(d), args.steps)
+        gated_g()
+    ms_gated, _ = timed(gated_g, args.steps)
 
     # decode: one token for each of 64 sequences x 32 heads from resident fp32 states
     dn, dh = 64, 32
@@ -382,7 +406,10 @@ def run_ours(args, rank, world, local):
         for h, r in zip(host_out, res):
             h.copy_(r, non_blocking=True)
 
-    ms_e2e, _ = timed(e2e_step, args.steps)
+    e2e_g = graphed(e2e_step)
+    for _ in range(max(args.warmup, 3)):
+        e2e_g()
+    ms_e2e, _ = timed(e2e_g, args.steps)
     clk = clocks.stop()
     status = gdn.gdn_sync_status(stream.cuda_stream)
     if status != 0:
@@ -443,7 +470,7 @@ def run_ours(args, rank, world, local):
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic (seeded; see gdn_synth.py)", "config": config_of(p, args.workload),
+            "data": "synthetic (seeded; see gdn_synth.py)", "config": config_of(p, args.workload, True),
             "fwd": {"value": world * tokens / (ms_fwd / 1e3), "unit": "tokens/s",
                     "ms_per_step": ms_fwd},
             "decode": {"value": world * dn / (ms_dec / 1e3), "unit": "tokens/s",
