@@ -183,21 +183,18 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             float4 *arow = reinterpret_cast<float4 *>(s.A[ch][r]);
             const float4 *brk4 = reinterpret_cast<const float4 *>(s.brk[ch]);
             const float4 *gam4 = reinterpret_cast<const float4 *>(s.gam[ch]);
-            // every value first (in place of kk), then the stores: a store between
-            // the reads would stop the compiler from overlapping their latencies
 #pragma unroll
             for (int i4 = 0; i4 < 16; ++i4) {
                 const float4 b4 = brk4[i4], g4 = gam4[i4];
                 const float bb[4] = {b4.x, b4.y, b4.z, b4.w}, gg[4] = {g4.x, g4.y, g4.z, g4.w};
+                float x[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int i = 4 * i4 + e;
-                    kk[i] = (i > r && i < L) ? bb[e] * kk[i] * rk * __expf(gg[e] - gr) : 0.f;
+                    x[e] = (i > r && i < L) ? bb[e] * kk[i] * rk * __expf(gg[e] - gr) : 0.f;
                 }
+                arow[i4] = make_float4(x[0], x[1], x[2], x[3]);
             }
-#pragma unroll
-            for (int i4 = 0; i4 < 16; ++i4)
-                arow[i4] = make_float4(kk[4 * i4], kk[4 * i4 + 1], kk[4 * i4 + 2], kk[4 * i4 + 3]);
         }
         __syncthreads();
         {
