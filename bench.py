@@ -95,8 +95,8 @@ def kernel_bytes_per_token_head(name, K, V, e=2, eg=4):
 # kernel's source file still hashes to `sha256` (otherwise reported as null).
 NCU_TRAFFIC = {
     ("tc_local_grad", "edge"): {
-        "file": "gdn_tc_local.cu", "bytes": 193574144 + 57177856,
-        "sha256": "7cc79012f6ac82b36e94f6b45cbd546359292fdc26a2b42087c725d87cae4dfd"},
+        "file": "gdn_tc_local.cu", "bytes": 193560320 + 57232896,
+        "sha256": "2b572b435ef3a0a0bf77e87a6e4a458a739daf337dfe2fd966497e9585d25cd2"},
 }
 
 
