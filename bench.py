@@ -434,6 +434,10 @@ def run_ours(args, rank, world, local):
     hbm = peaks.get("hbm_gbs", 6800.0)
     bf16 = peaks.get("bf16_tflops", 1900.0)
     t_roof = max(step_bytes / (hbm * 1e9), step_flops / (bf16 * 1e12))
+    # the forward alone: inputs, O and the states (h0 in, final state out)
+    fwd_bytes = th * bytes_per_token_head(p.K, p.V, e_in, "fwd") + p.N * p.H * p.K * p.V * 4 * 2
+    fwd_flops = th * flops_per_token_head(p.K, p.V, "fwd")
+    t_roof_fwd = max(fwd_bytes / (hbm * 1e9), fwd_flops / (bf16 * 1e12))
     total_launches = sum(s[1] for s in prof)
     dom = max(prof, key=lambda s: s[2])
     dom_name, dom_launches, dom_ms = dom
@@ -472,7 +476,10 @@ def run_ours(args, rank, world, local):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded; see gdn_synth.py)", "config": config_of(p, args.workload, True),
             "fwd": {"value": world * tokens / (ms_fwd / 1e3), "unit": "tokens/s",
-                    "ms_per_step": ms_fwd},
+                    "ms_per_step": ms_fwd,
+                    "step_roofline": {"t_roof_ms": t_roof_fwd * 1e3,
+                                      "frac": t_roof_fwd * 1e3 / ms_fwd,
+                                      "bytes": fwd_bytes, "flops": fwd_flops}},
             "decode": {"value": world * dn / (ms_dec / 1e3), "unit": "tokens/s",
                        "ms_per_step": ms_dec, "batch": f"{dn} sequences x {dh} heads",
                        "hbm_gbs": dec_bytes / (ms_dec / 1e3) / 1e9,
