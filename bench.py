@@ -81,6 +81,7 @@ def kernel_bytes_per_token_head(name, K, V, e=2, eg=4):
     table = {
         "tc_prep": e * (K + V) + 8 + 4 + 2 * (K + V) + t_mat,
         "tc_walk": e * K + 2 * (K + V) + 4 + state,
+        "tc_walk_fused": 2 * e * K + 2 * (K + V) + 4 + state + e * V,   # forms O as well
         "tc_out": 2 * e * K + 2 * (K + V) + state + 4 + e * V,
         "tc_bwd_intra": e * (2 * K + V) + 4 + 2 * K + 2 * V,
         "tc_dwalk_out": e * K + 2 * K + e * V + 2 * K + 2 * V + 4 + state + 2 * V,

@@ -343,20 +343,31 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
 }
 
 // ------------------------------------------------------------------ walk
-// The walk carries only the state recurrence; outputs come from the
-// chunk-parallel output kernel, which reads the chunk start states it stores.
-constexpr int kWalkStages = 3;    // chunks in flight: the current one and two prefetched
+// kWalkOut: the state walk (start states stored; O from the output pass).
+// kWalkMap: segment maps.  kWalkFused: the state walk that also forms each
+// chunk's O inside its loop -- the start state, U and the decay are at hand
+// there -- so that no output pass runs:
+//   P = Q K^T .* lower_incl .* D,   O^T = scale (H^T Q^T diag(e) + U^T P^T).
+// Its stages carry Q stacked over K ([Q rows | K rows] per dk half) and it
+// keeps one chunk in flight ahead of the current one; the others keep two.
+enum { kWalkOut = 0, kWalkMap = 1, kWalkFused = 2 };
 
+template <int MODE>
 struct WalkSmem {
-    uint8_t k[kWalkStages][2 * kTile];   // per stage: K, [dk half][64 chunk rows][128 B]
-    uint8_t w[kWalkStages][2 * kTile];   // per stage: W^T, [128 rows k][64 chunk rows]
-    uint8_t u[kWalkStages][2 * kTile];   // per stage: u^T, [128 rows v][64 chunk rows]
+    static constexpr int kStages = MODE == kWalkFused ? 2 : 3;
+    static constexpr int kKBytes = MODE == kWalkFused ? 4 * kTile : 2 * kTile;
+    uint8_t k[kStages][kKBytes];   // per stage: [dk half][(Q rows 0-63,) K rows][128 B]
+    uint8_t w[kStages][2 * kTile];   // per stage: W^T, [128 rows k][64 chunk rows]
+    uint8_t u[kStages][2 * kTile];   // per stage: u^T, [128 rows v][64 chunk rows]
     uint8_t hT[4 * kTile];         // [dk half][128 state rows][128 B]  (A operand)
     uint8_t uTs[2 * kTile];        // U^T diag(f): [128 state rows][64 chunk rows] (A operand)
+    uint8_t uT[MODE == kWalkFused ? 2 * kTile : 1024];   // U^T (fused walk)
+    uint8_t p[MODE == kWalkFused ? kTile : 1024];        // P rows r (fused walk)
     float gam[2][64];
     alignas(16) float fr[64];      // exp(gam_L - gam_r) (x 1/|k_r|); 0 past L
+    alignas(16) float er[2][64];   // exp(gam_r) per chunk parity (output walk); 0 past L
     float rk[64];
-    uint64_t tma_bar[kWalkStages], bar_u, bar_dh;
+    uint64_t tma_bar[kStages], bar_u, bar_q, bar_dh;
     uint32_t tmem_base;
 };
 
@@ -369,27 +380,31 @@ struct TcWalkArgs {
     float *final_state;       // nullable
     __nv_bfloat16 *hc;        // chunk start states as bf16 H^T tiles [chunk][H][k half][v][64], nullable
     float *maps;              // [segs, H, K, K+V] (kWalkMap)
+    __nv_bfloat16 *o;         // [tokens, H, V]: formed inside the output walk when set
     int cp;
 };
 
-enum { kWalkOut = 0, kWalkMap = 1 };
-
 constexpr uint32_t kIdescDH = idesc_bf16(128, 128, false, true);      // B MN-major
 constexpr uint32_t kIdescKM64 = idesc_bf16(128, 64, false, true);     // B MN-major, N = 64
+constexpr uint32_t kIdescKK64 = idesc_bf16(128, 64, false, false);    // both K-major, N = 64
 
 // 256 threads: thread t owns state row v = t % 128 (TMEM lane v) and the
 // column half hs = t / 128; warps w and w + 4 share a TMEM lane quarter and
 // split every epilogue's columns between them.  Per chunk: U = u - W H (one
 // MMA group), U^T diag(f) into shared memory, K^T diag(f) U (second group),
-// H <- exp(gam_L) H + that.
+// H <- exp(gam_L) H + that.  The output walk adds [Q; K] K^T and H^T Q^T to
+// the first group, P (rows r on lanes 0-63) and U^T to shared memory, U^T P^T
+// to the second group, and O after it.
 template <int MODE>
 __global__ void __launch_bounds__(256, 1)
-tc_walk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_w,
-               const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_hc,
-               Geo g, TcWalkArgs a) {
+tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_u,
+               const __grid_constant__ CUtensorMap tm_hc, Geo g, TcWalkArgs a) {
     pdl_enter();
+    typedef WalkSmem<MODE> S;
+    constexpr int kWalkStages = S::kStages;
     extern __shared__ uint8_t smem_raw[];
-    WalkSmem &s = *reinterpret_cast<WalkSmem *>(
+    S &s = *reinterpret_cast<S *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, h = blockIdx.y, cb = blockIdx.z, H = g.H;
     const int v = tid & 127, hs = tid >> 7;
@@ -403,7 +418,12 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     }
     if (MODE == kWalkMap && (j == nseg - 1 || (a.warm && a.warm[n * H + h]))) return;
     const bool a_cols = MODE == kWalkMap && cb == 0;   // A columns: start I, u = 0
-    const bool states = MODE == kWalkOut && a.hc != nullptr;
+    constexpr bool kState = MODE != kWalkMap;         // a state walk (start states, O)
+    constexpr bool fused = MODE == kWalkFused;        // O formed here
+    const bool states = kState && a.hc != nullptr;
+    // byte offset of K's dk half hh inside a stage, and the stride between the halves
+    constexpr int kKOff = fused ? kTile : 0;
+    constexpr uint32_t kKHalf = fused ? 2 * kTile : kTile;
     const int nc = seq_nchunks(g, n);
     const int c0 = min(nc, j * g.seg_chunks), c1 = min(nc, (j + 1) * g.seg_chunks);
     const int cbase = seq_chunk_base(g, n);
@@ -412,16 +432,21 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     seq_range(g, n, sbos, slen);
     bool warm = false;
     int cstart = c0;
-    if (MODE == kWalkOut && a.cp && j > 0 && a.warm && a.warm[n * H + h]) {
+    if (kState && a.cp && j > 0 && a.warm && a.warm[n * H + h]) {
         warm = true;
         cstart = max(0, c0 - a.warm_chunks);
     }
 
     auto issue_tma = [&](int st, int c) {
         const int tok0 = (int)(sbos + (long long)c * kChunk);
-        mbar_arrive_expect_tx(&s.tma_bar[st], 6 * kTile);   // K (2 halves), W^T, u^T
-        tma_load_3d(s.k[st], &tm_k, &s.tma_bar[st], 0, h, tok0);
-        tma_load_3d(s.k[st] + kTile, &tm_k, &s.tma_bar[st], 64, h, tok0);
+        // K (2 halves), W^T, u^T (and Q's 2 halves above K's in the output walk)
+        mbar_arrive_expect_tx(&s.tma_bar[st], (fused ? 8 : 6) * kTile);
+        tma_load_3d(s.k[st] + kKOff, &tm_k, &s.tma_bar[st], 0, h, tok0);
+        tma_load_3d(s.k[st] + kKOff + kKHalf, &tm_k, &s.tma_bar[st], 64, h, tok0);
+        if (fused) {
+            tma_load_3d(s.k[st], &tm_q, &s.tma_bar[st], 0, h, tok0);
+            tma_load_3d(s.k[st] + kKHalf, &tm_q, &s.tma_bar[st], 64, h, tok0);
+        }
         const int trow = (int)(((long long)(cbase + c) * H + h) * kD);
         tma_load_2d(s.w[st], &tm_w, &s.tma_bar[st], 0, trow);
         tma_load_2d(s.u[st], &tm_u, &s.tma_bar[st], 0, trow);
@@ -432,12 +457,14 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     if (tid == 0) {
         for (int i = 0; i < kWalkStages; ++i) mbar_init(&s.tma_bar[i], 1);
         mbar_init(&s.bar_u, 1);
+        mbar_init(&s.bar_q, 1);
         mbar_init(&s.bar_dh, 1);
         fence_barrier_init();
         for (int i = 0; i < kWalkStages - 1 && cstart + i < c1; ++i) issue_tma(i, cstart + i);
     }
+    constexpr uint32_t kTmemCols = fused ? 512 : 256;
     if (warp == 0) {
-        tmem_alloc(&s.tmem_base, 256);
+        tmem_alloc(&s.tmem_base, kTmemCols);
         tmem_relinquish();
         tc_fence_before();
     }
@@ -445,7 +472,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     float Hr[64];
     {
         const float *src = nullptr;
-        if (MODE == kWalkOut && !warm) {
+        if (kState && !warm) {
             if (a.cp && j > 0)
                 src = a.seg_start + ((long long)(seq_seg_base(g, n) + j) * H + h) * kD * kD;
             else if (a.h0)
@@ -467,6 +494,31 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     tc_fence_after();
     const uint32_t tbase = s.tmem_base;
     const uint32_t t_u = tbase, t_dh = tbase + 128;
+    // output walk: P, and H^T Q^T / U^T P^T per chunk parity (a chunk's O is formed
+    // while the next chunk's first products run)
+    const uint32_t t_p = tbase + 64;
+    auto t_qh = [&](int b) { return tbase + 256 + 128 * b; };
+    auto t_pu = [&](int b) { return tbase + 320 + 128 * b; };
+    long long pbos = 0;
+    int pL = 0, pc = -1;                       // the previous chunk (output walk)
+    // O rows c = 32 hs .. +31 of the chunk at token pbos (parity b), feature v:
+    // scale (e_c (H^T Q^T) + U^T P^T)
+    auto out_epilogue = [&](int b) {
+        float qh[32], pu[32];
+        tmem_ld32(tmem_addr(t_qh(b), warp, 32 * hs), qh);
+        tmem_ld32(tmem_addr(t_pu(b), warp, 32 * hs), pu);
+        __nv_bfloat16 *dst = a.o + (pbos * H + h) * (long long)kD + v;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 e0 = reinterpret_cast<const float4 *>(s.er[b])[8 * hs + 2 * q];
+            const float4 e1 = reinterpret_cast<const float4 *>(s.er[b])[8 * hs + 2 * q + 1];
+            const float eq[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = g.scale * (eq[e] * qh[8 * q + e] + pu[8 * q + e]);
+            store_rows8(dst, (long long)H * kD, x, 32 * hs + 8 * q, pL);
+        }
+    };
 
     // one commit per barrier per chunk: every barrier's parity is the chunk
     // iteration's; `pend` marks groups committed in this iteration, not yet waited
@@ -502,7 +554,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         tma_pending &= ~(1 << st);
         if (warp == 0) {
             tc_fence_after();
-            const uint32_t wt = smem_u32(s.w[st]), hT = smem_u32(s.hT);
+            const uint32_t wt = smem_u32(s.w[st]), hT = smem_u32(s.hT), qk = smem_u32(s.k[st]);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 const uint64_t ah = desc_sw128(hT + (kk >> 2) * 2 * kTile + (kk & 3) * 32, 16, 1024);
@@ -510,9 +562,22 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                 mma_bf16(t_u, ah, bw, kIdescKM64, kk > 0);
             }
             mma_commit(&s.bar_u);
+            if (fused) {
+                // behind U on their own barrier: the U epilogue need not wait for them
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (kk >> 2) * kKHalf + (kk & 3) * 32;
+                    const uint64_t ah = desc_sw128(hT + (kk >> 2) * 2 * kTile + (kk & 3) * 32, 16, 1024);
+                    const uint64_t aq = desc_sw128(qk + off, 16, 1024);           // [Q; K], K-major
+                    const uint64_t bk = desc_sw128(qk + kKOff + off, 16, 1024);   // K, K-major
+                    mma_bf16(t_p, aq, bk, kIdescKK64, kk > 0);       // rows 0-63: Q K^T
+                    mma_bf16(t_qh(gb), ah, aq, kIdescKK64, kk > 0);  // H^T Q^T (columns 0-63)
+                }
+                mma_commit(&s.bar_q);
+            }
         }
-        pend = 1;
-        // while the product runs, the last warp requests the chunk two ahead (into
+        pend = fused ? 5 : 1;
+        // while the product runs, the last warp requests the next chunk(s) (into
         // the stage the previous chunk used) and stores this chunk's start state
         if (c + kWalkStages - 1 < c1) {
             const int sn = (it + kWalkStages - 1) % kWalkStages;
@@ -529,6 +594,10 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             tma_store_2d(&tm_hc, s.hT + 2 * kTile, 0, row + kD);
             bulk_commit();
         }
+        if (fused && pc >= c0) {
+            tc_fence_after();
+            out_epilogue(gb ^ 1);                 // the previous chunk's O
+        }
         if (g.l2norm && tid >= 64 && tid < 128) {
             // 1 / |k_r| from the K rows
             const int r = tid - 64;
@@ -537,7 +606,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             for (int half = 0; half < 2; ++half)
 #pragma unroll 8
                 for (int col = 0; col < 64; ++col) {
-                    const float x = ld_bf16(s.k[st] + half * kTile, r, col);
+                    const float x = ld_bf16(s.k[st] + kKOff + half * kKHalf, r, col);
                     ss += x * x;
                 }
             s.rk[r] = rsqrtf(ss + 1e-6f);
@@ -546,10 +615,11 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         if (tid < 64) {
             const float gl = s.gam[gb][L - 1], gr = s.gam[gb][tid];
             s.fr[tid] = tid < L ? __expf(gl - gr) * (g.l2norm ? s.rk[tid] : 1.f) : 0.f;
+            if (fused) s.er[gb][tid] = tid < L ? __expf(gr) : 0.f;
         }
         ok = mbar_wait(&s.bar_u, par, g.spin_limit, g.status);
         if (__syncthreads_or(!ok)) { bailed = true; break; }
-        pend = 0;
+        pend &= ~1;
         tc_fence_after();
         // U^T diag(f) rows v, chunk rows 32*hs .. +31 (one TMEM load, groups of 8)
         float xu[32];
@@ -569,25 +639,58 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const int r = 8 * chunk + e;
-                uu[e] = r < L ? (__bfloat162float(bv[e]) - x[e]) * fq[e] : 0.f;
+                x[e] = r < L ? __bfloat162float(bv[e]) - x[e] : 0.f;   // U^T
+                uu[e] = x[e] * fq[e];
             }
             st_row8(s.uTs, v, chunk, uu);
+            if (fused) st_row8(s.uT, v, chunk, x);
+        }
+        if (fused) {
+            ok = mbar_wait(&s.bar_q, par, g.spin_limit, g.status);
+            if (__syncthreads_or(!ok)) { bailed = true; break; }
+            pend &= ~4;
+            tc_fence_after();
+        }
+        if (fused && v < 64) {
+            // row r = v of P: Q K^T on lanes 0-63, masked to c <= r < L, times D_rc
+            const int r = v;
+            const float gr = s.gam[gb][r];
+            float xp[32];
+            tmem_ld32(tmem_addr(t_p, warp, 32 * hs), xp);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float *x = xp + 8 * q;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int c = 32 * hs + 8 * q + e;
+                    x[e] = (c <= r && r < L) ? x[e] * __expf(gr - s.gam[gb][c]) : 0.f;
+                }
+                st_row8(s.p, r, 4 * hs + q, x);
+            }
         }
         tc_fence_before();
         fence_proxy_async();
         __syncthreads();
         if (warp == 0) {
             tc_fence_after();
-            const uint32_t uTs = smem_u32(s.uTs), kt = smem_u32(s.k[st]);
+            const uint32_t uTs = smem_u32(s.uTs), kt = smem_u32(s.k[st]) + kKOff;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
                 const uint64_t au = desc_sw128(uTs + kk * 32, 16, 1024);
-                const uint64_t bk = desc_sw128(kt + kk * 2048, kTile, 1024);   // K, MN-major
+                const uint64_t bk = desc_sw128(kt + kk * 2048, kKHalf, 1024);   // K, MN-major
                 mma_bf16(t_dh, au, bk, kIdescDH, kk > 0);
+            }
+            if (fused) {
+                // U^T P^T: both operands K-major over the chunk rows
+                const uint32_t ua = smem_u32(s.uT), pp = smem_u32(s.p);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(t_pu(gb), desc_sw128(ua + kk * 32, 16, 1024),
+                             desc_sw128(pp + kk * 32, 16, 1024), kIdescKK64, kk > 0);
             }
             mma_commit(&s.bar_dh);
         }
-        pend = 2;
+        pend |= 2;
         if (tma_thread) bulk_wait_read();     // the state store has read H^T
         ok = mbar_wait(&s.bar_dh, par, g.spin_limit, g.status);
         if (__syncthreads_or(!ok)) { bailed = true; break; }
@@ -604,10 +707,17 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             }
         }
         st_row64(s.hT + hs * 2 * kTile, v, Hr);
+        pbos = bos;
+        pL = L;
+        pc = c;
         if (tid < 64) cp_async_wait_all();
         tc_fence_before();
         fence_proxy_async();
         __syncthreads();
+    }
+    if (fused && !bailed && pc >= c0) {
+        tc_fence_after();
+        out_epilogue((it - 1) & 1);              // the last chunk's O
     }
 
     if (tma_thread) bulk_wait_read();
@@ -617,6 +727,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             for (int st = 0; st < kWalkStages; ++st)
                 if (tma_pending & (1 << st)) mbar_drain(&s.tma_bar[st], (ld_par >> st) & 1u);
             if (pend & 1) mbar_drain(&s.bar_u, it & 1);
+            if (pend & 4) mbar_drain(&s.bar_q, it & 1);
             if (pend & 2) mbar_drain(&s.bar_dh, it & 1);
         }
     } else if (MODE == kWalkMap) {
@@ -630,7 +741,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tbase, 256);
+    if (warp == 0) tmem_dealloc(tbase, kTmemCols);
 }
 
 // ------------------------------------------------------------------ host side
@@ -702,7 +813,8 @@ static cudaError_t run_forward(const Plan &p, cudaStream_t s, bool states_only, 
     if (e != cudaSuccess) return e;
     const Geo &g = p.g;
     const long long tokens = (long long)g.B * g.T;
-    CUtensorMap mk, mv, mw, mu;
+    CUtensorMap mq, mk, mv, mw, mu;
+    if ((e = make_map(&mq, g.q, tokens, g.H)) != cudaSuccess) return e;
     if ((e = make_map(&mk, g.k, tokens, g.H)) != cudaSuccess) return e;
     if ((e = make_map(&mv, g.v, tokens, g.H)) != cudaSuccess) return e;
     const long long tile_rows = (long long)p.max_chunks * g.H * kD;
@@ -711,10 +823,14 @@ static cudaError_t run_forward(const Plan &p, cudaStream_t s, bool states_only, 
     CUtensorMap mhc;
     if ((e = make_map_tiles(&mhc, p.ws.hc, 2 * tile_rows)) != cudaSuccess) return e;
 
-    const size_t prep_smem = sizeof(PrepSmem) + 1024, walk_smem = sizeof(WalkSmem) + 1024;
+    const size_t prep_smem = sizeof(PrepSmem) + 1024;
+    const size_t out_smem = sizeof(WalkSmem<kWalkOut>) + 1024;
+    const size_t fused_smem = sizeof(WalkSmem<kWalkFused>) + 1024;
+    const size_t map_smem = sizeof(WalkSmem<kWalkMap>) + 1024;
     if ((e = set_smem(tc_prep_kernel, prep_smem)) != cudaSuccess) return e;
-    if ((e = set_smem(tc_walk_kernel<kWalkOut>, walk_smem)) != cudaSuccess) return e;
-    if ((e = set_smem(tc_walk_kernel<kWalkMap>, walk_smem)) != cudaSuccess) return e;
+    if ((e = set_smem(tc_walk_kernel<kWalkOut>, out_smem)) != cudaSuccess) return e;
+    if ((e = set_smem(tc_walk_kernel<kWalkFused>, fused_smem)) != cudaSuccess) return e;
+    if ((e = set_smem(tc_walk_kernel<kWalkMap>, map_smem)) != cudaSuccess) return e;
 
     prof_before("tc_prep", s);
     const int prep_items = (p.max_chunks + 1) / 2 * g.H;
@@ -733,7 +849,17 @@ static cudaError_t run_forward(const Plan &p, cudaStream_t s, bool states_only, 
     a.h0 = p.h0;
     a.final_state = states_only ? nullptr : p.final_state;
     a.hc = (__nv_bfloat16 *)p.ws.hc;
-    const char *out_name = states_only ? "tc_walk_states" : "tc_walk";
+    // The walk forms O itself (q, k not L2-normalised inside the library) when
+    // its CTAs fill at least three quarters of the SMs: each chunk then costs
+    // the walk about 4.3K more cycles, against about 6.6K SM-cycles of the
+    // chunk-parallel output pass (GB300 measurements on the four workloads;
+    // with fewer walk CTAs the output pass, spread over every SM, is cheaper).
+    const int walk_ctas = (p.cp ? p.max_segs : g.N) * g.H;
+    const bool fuse_out = !states_only && !g.l2norm && 4 * walk_ctas >= 3 * std::max(p.sms, 1);
+    a.o = fuse_out ? (__nv_bfloat16 *)p.o : nullptr;
+    auto walk_kernel = fuse_out ? tc_walk_kernel<kWalkFused> : tc_walk_kernel<kWalkOut>;
+    const char *out_name = states_only ? "tc_walk_states" : fuse_out ? "tc_walk_fused" : "tc_walk";
+    const size_t walk_smem = fuse_out ? fused_smem : out_smem;
     if (p.cp) {
         a.cp = 1;
         a.maps = p.ws.maps;
@@ -744,26 +870,26 @@ static cudaError_t run_forward(const Plan &p, cudaStream_t s, bool states_only, 
             a.warm_chunks = p.warm_chunks;
         }
         prof_before("tc_walk_map", s);
-        if ((e = launch_pdl(tc_walk_kernel<kWalkMap>, dim3(p.max_segs, g.H, 2), dim3(256), walk_smem, s,
-                            mk, mw, mu, mhc, g, a)) != cudaSuccess)
+        if ((e = launch_pdl(tc_walk_kernel<kWalkMap>, dim3(p.max_segs, g.H, 2), dim3(256), map_smem, s,
+                            mq, mk, mw, mu, mhc, g, a)) != cudaSuccess)
             return e;
         prof_after(s);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if ((e = simt::cp_scan(p, a.warm, s)) != cudaSuccess) return e;
         prof_before(out_name, s);
-        if ((e = launch_pdl(tc_walk_kernel<kWalkOut>, dim3(p.max_segs, g.H, 1), dim3(256), walk_smem, s,
-                            mk, mw, mu, mhc, g, a)) != cudaSuccess)
+        if ((e = launch_pdl(walk_kernel, dim3(p.max_segs, g.H, 1), dim3(256), walk_smem, s,
+                            mq, mk, mw, mu, mhc, g, a)) != cudaSuccess)
             return e;
         prof_after(s);
     } else {
         prof_before(out_name, s);
-        if ((e = launch_pdl(tc_walk_kernel<kWalkOut>, dim3(g.N, g.H, 1), dim3(256), walk_smem, s,
-                            mk, mw, mu, mhc, g, a)) != cudaSuccess)
+        if ((e = launch_pdl(walk_kernel, dim3(g.N, g.H, 1), dim3(256), walk_smem, s,
+                            mq, mk, mw, mu, mhc, g, a)) != cudaSuccess)
             return e;
         prof_after(s);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    return states_only ? cudaSuccess : output(p, s);
+    return (states_only || fuse_out) ? cudaSuccess : output(p, s);
 }
 
 cudaError_t forward(const Plan &p, cudaStream_t s, bool save) {
