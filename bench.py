@@ -399,18 +399,49 @@ def run_ours(args, rank, world, local):
                 if o is not None]
     d2h = sum(o.numel() * o.element_size() for o in host_out)
 
+    copy_stream = torch.cuda.Stream(dev)
+    n_fwd_out = sum(1 for o in outs[:2] if o is not None)
+
     def e2e_step():
-        x = {k: v.to(dev, non_blocking=True) for k, v in host_in.items()}
-        xx = type(d)(p.name, x["q"], x["k"], x["v"], x["g"], x["beta"], x.get("h0"),
-                     d.cu_seqlens, x["do"], x.get("dht"), p.meta)
-        res = [o for o in step(xx) if o is not None]
-        for h, r in zip(host_out, res):
-            h.copy_(r, non_blocking=True)
+        # The forward's inputs go first; the backward's own inputs (dO, d final
+        # state) travel on a second stream while the forward runs, and O and the
+        # final state travel back while the backward runs.
+        main = torch.cuda.current_stream(dev)
+        x = {k: host_in[k].to(dev, non_blocking=True)
+             for k in ("q", "k", "v", "g", "beta", "h0") if k in host_in}
+        copy_stream.wait_stream(main)
+        inputs_in = torch.cuda.Event()
+        with torch.cuda.stream(copy_stream):
+            xb = {k: host_in[k].to(dev, non_blocking=True) for k in ("do", "dht") if k in host_in}
+            inputs_in.record(copy_stream)
+        for t in xb.values():
+            t.record_stream(main)
+        o, fs, saved = gdn.chunk_gated_delta_rule_fwd(
+            x["q"], x["k"], x["v"], x["g"], x["beta"], initial_state=x.get("h0"),
+            output_final_state=True, cu_seqlens=d.cu_seqlens, cp=cp, save_ctx=True)
+        fwd_out = [t for t in (o, fs) if t is not None]
+        copy_stream.wait_stream(main)
+        with torch.cuda.stream(copy_stream):
+            for hbuf, t in zip(host_out[:n_fwd_out], fwd_out):
+                hbuf.copy_(t, non_blocking=True)
+        for t in fwd_out:
+            t.record_stream(copy_stream)
+        main.wait_event(inputs_in)
+        grads = gdn.chunk_gated_delta_rule_bwd(
+            x["q"], x["k"], x["v"], x["g"], x["beta"], xb["do"], dht=xb.get("dht"),
+            initial_state=x.get("h0"), cu_seqlens=d.cu_seqlens, cp=cp, ctx=saved)
+        for hbuf, t in zip(host_out[n_fwd_out:], [t for t in grads if t is not None]):
+            hbuf.copy_(t, non_blocking=True)
+        main.wait_stream(copy_stream)
 
     e2e_g = graphed(e2e_step)
     for _ in range(max(args.warmup, 3)):
         e2e_g()
     ms_e2e, _ = timed(e2e_g, args.steps)
+    torch.cuda.synchronize(dev)
+    for hbuf, t in zip(host_out, [t for t in outs if t is not None]):
+        if not torch.equal(hbuf, t.cpu()):
+            raise RuntimeError("end-to-end results differ from the device-resident step")
     clk = clocks.stop()
     status = gdn.gdn_sync_status(stream.cuda_stream)
     if status != 0:
