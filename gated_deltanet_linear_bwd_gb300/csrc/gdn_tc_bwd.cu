@@ -51,6 +51,7 @@ struct IntraSmem {
     uint8_t yT[2 * kTile];         // Y^T, [128 rows v][64 chunk rows]
     uint8_t p[kTile];              // P rows r (scale included)
     float gam[64], rq[64], rk[64];
+    float gpre[64];            // the next item's gam, fetched during the current one
     uint64_t load_bar[2], mma_bar; // loads: {q, k}, {dO}
     uint32_t tmem_base;
 };
@@ -133,10 +134,18 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         if (tid == 0) bulk_wait_read();       // the previous item's stores have read Qs, Y^T
         tc_fence_before();
         __syncthreads();
-        if (tid < 64) s.gam[tid] = tid < L ? ws_gam[(bos + tid) * H + h] : 0.f;
+        if (tid < 64) {
+            // gam of this item: fetched during the previous one (cp.async), else now
+            if (it > 0) cp_async_wait_all();
+            s.gam[tid] = it > 0 ? s.gpre[tid] : (tid < L ? ws_gam[(bos + tid) * H + h] : 0.f);
+        }
         bool ok = mbar_wait(&s.load_bar[0], it & 1, g.spin_limit, g.status);
         if (__syncthreads_or(!ok)) { bailed = true; break; }
         ++mma_n;
+        // every thread is past the copy of gpre above: the next item's gam can come
+        if (tid < 64 && have_next)
+            cp_async4(&s.gpre[tid], ws_gam + (cr_n.bos + min(tid, cr_n.len - 1)) * H + h_n,
+                      tid < cr_n.len);
         if (warp == 0) {
             tc_fence_after();
             const uint32_t qk = smem_u32(s.qk);
@@ -258,6 +267,7 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             if (issued[grp] > 0) mbar_drain(&s.load_bar[grp], (issued[grp] - 1) & 1);
         if (mma_n > 0) mbar_drain(&s.mma_bar, (mma_n - 1) & 1);
     }
+    if (tid < 64) cp_async_wait_all();        // a prefetch still in flight after a bail
     if (tid == 0) bulk_wait_read();
     tc_fence_before();
     __syncthreads();

@@ -33,6 +33,7 @@ struct OutSmem {
     uint8_t h0T[4 * kTile];    // H0^T: [k half][128 rows v][64]; after wave 1: U^T
     uint8_t p[kTile];          // P rows r
     float gam[64], er[64], rq[64], rk[64];
+    float gpre[64];            // the next item's gam, fetched during the current one
     uint64_t load_bar[3], mma_bar;  // loads: {q, k, W^T}, {u^T}, {H0^T}
     uint32_t tmem_base;
 };
@@ -123,10 +124,18 @@ tc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const bool have_next = item_ref(item + (int)gridDim.x, ci_n, h_n, cr_n);
         tc_fence_before();
         __syncthreads();                      // the previous item's last reads are done
-        if (tid < 64) s.gam[tid] = tid < L ? ws_gam[(bos + tid) * H + h] : 0.f;
+        if (tid < 64) {
+            // gam of this item: fetched during the previous one (cp.async), else now
+            if (it > 0) cp_async_wait_all();
+            s.gam[tid] = it > 0 ? s.gpre[tid] : (tid < L ? ws_gam[(bos + tid) * H + h] : 0.f);
+        }
         bool ok = mbar_wait(&s.load_bar[0], it & 1, g.spin_limit, g.status);
         ok = mbar_wait(&s.load_bar[2], it & 1, g.spin_limit, g.status) && ok;
         if (__syncthreads_or(!ok)) { bailed = true; break; }
+        // every thread is past the copy of gpre above: the next item's gam can come
+        if (tid < 64 && have_next)
+            cp_async4(&s.gpre[tid], ws_gam + (cr_n.bos + min(tid, cr_n.len - 1)) * H + h_n,
+                      tid < cr_n.len);
         ++mma_n;
         if (warp == 0) {
             tc_fence_after();
@@ -260,6 +269,7 @@ tc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             if (issued[grp] > 0) mbar_drain(&s.load_bar[grp], (issued[grp] - 1) & 1);
         if (mma_n > 0) mbar_drain(&s.mma_bar, (mma_n - 1) & 1);
     }
+    if (tid < 64) cp_async_wait_all();        // a prefetch still in flight after a bail
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tb, 256);
