@@ -467,6 +467,9 @@ tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
             const float gl = s.gam[st][L - 1];
             s.fr[tid] = tid < L ? __expf(gl - s.gam[st][tid]) * (g.l2norm ? s.rk[tid] : 1.f) : 0.f;
         }
+        // the previous chunk's dU^T store has read its tile (this chunk's dH^T store,
+        // the newest group, may go on)
+        if (tma_thread) bulk_wait_read_but_newest();
         ok = mbar_wait(&s.bar_x, par, g.spin_limit, g.status);
         if (__syncthreads_or(!ok)) { bailed = true; break; }
         pend = 0;
@@ -511,7 +514,9 @@ tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
             mma_commit(&s.bar_z);
         }
         pend = 2;
-        if (tma_thread) bulk_wait_read();     // the dH^T and dU^T stores have read their tiles
+        // the dH^T store has read its tile (the dU^T store, the newest group, may
+        // go on until the next chunk's dU epilogue)
+        if (tma_thread) bulk_wait_read_but_newest();
         ok = mbar_wait(&s.bar_z, par, g.spin_limit, g.status);
         if (__syncthreads_or(!ok)) { bailed = true; break; }
         pend = 0;
