@@ -85,6 +85,7 @@ def kernel_bytes_per_token_head(name, K, V, e=2, eg=4):
         "tc_out": 2 * e * K + 2 * (K + V) + state + 4 + e * V,
         "tc_bwd_intra": e * (2 * K + V) + 4 + 2 * K + 2 * V,
         "tc_dwalk_out": e * K + 2 * K + e * V + 2 * K + 2 * V + 4 + state + 2 * V,
+        "tc_dwalk_fused": 2 * e * K + 2 * K + e * V + 4 + state + 2 * V,   # forms Qs, Y^T itself
         "tc_local_grad": (e * (2 * K + 2 * V) + 2 * (K + 2 * V) + 2 * state + t_mat + 8 +
                           eg * (2 * K + V) + 8),
     }

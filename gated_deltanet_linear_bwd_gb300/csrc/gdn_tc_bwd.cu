@@ -276,18 +276,27 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 
 // ------------------------------------------------------------------ reverse walk
 namespace {
+// kDOut: the reverse walk (gradient states, dU); kDMap: segment maps;
+// kDFused: the reverse walk that forms the chunk's P, Qs and Y^T = dO^T P
+// itself from q, k, dO instead of reading the intra kernel's tiles.
+enum { kDOut = 0, kDMap = 1, kDFused = 2 };
+
+template <int MODE>
 struct DWalkSmem {
-    uint8_t k[2][2 * kTile];       // per stage: K, [dk half][64 rows][128 B]
+    static constexpr bool kF = MODE == kDFused;
+    uint8_t k[2][kF ? 4 * kTile : 2 * kTile];   // per stage: K, [dk half][64 rows][128 B];
+                                                 // fused: [dk half][Q rows | K rows][128 B]
     uint8_t w[2][2 * kTile];       // per stage: W^T, [128 rows k][64 chunk rows]  K-major B
     uint8_t dO[2][2 * kTile];      // per stage: dO, [dv half][64 rows][128 B]
-    uint8_t qs[2][2 * kTile];      // per stage: Qs, [dk half][64 rows][128 B]
-    uint8_t y[2][2 * kTile];       // per stage: Y^T, [128 rows v][64 chunk rows]
+    uint8_t qs[kF ? 1 : 2][2 * kTile];           // per stage: Qs, [dk half][64 rows][128 B]
+    uint8_t y[kF ? 1 : 2][kF ? 1024 : 2 * kTile];   // per stage: Y^T, [128 rows v][64 chunk rows]
+    uint8_t p[kF ? kTile : 1024];   // P rows r (fused)
     uint8_t dhT[4 * kTile];        // dH^T: [k half][128 rows v][128 B]   K-major A
     uint8_t duT[2 * kTile];        // dU^T: [128 rows v][64 chunk rows]    K-major A
     float gam[2][64];
     alignas(16) float fr[64];      // exp(gam_L - gam_r) (x 1/|k_r|), 0 past L
     float rk[64];
-    uint64_t tma_bar[2], bar_x, bar_z;
+    uint64_t tma_bar[2], bar_x, bar_z, bar_q, bar_y;
     uint32_t tmem_base;
 };
 
@@ -301,10 +310,8 @@ struct TcDWalkArgs {
 };
 
 struct DWalkMaps {
-    CUtensorMap k, w, dO, qs, y, dhc, du;
+    CUtensorMap q, k, w, dO, qs, y, dhc, du;
 };
-
-enum { kDOut = 0, kDMap = 1 };
 }  // namespace
 
 // 256 threads: thread t owns row v = t % 128 of dH^T (TMEM lane v) and the
@@ -317,8 +324,13 @@ template <int MODE>
 __global__ void __launch_bounds__(256, 1)
 tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
     pdl_enter();
+    typedef DWalkSmem<MODE> S;
+    constexpr bool fused = MODE == kDFused;
+    constexpr bool kOut = MODE != kDMap;                 // a gradient-state walk
+    constexpr int kKOff = fused ? kTile : 0;             // K rows inside a dk half block
+    constexpr uint32_t kKHalf = fused ? 2 * kTile : kTile;
     extern __shared__ uint8_t smem_raw[];
-    DWalkSmem &s = *reinterpret_cast<DWalkSmem *>(
+    S &s = *reinterpret_cast<S *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, h = blockIdx.y, cb = blockIdx.z, H = g.H;
     const int v = tid & 127, hs = tid >> 7;
@@ -344,13 +356,18 @@ tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
     auto issue_tma = [&](int st, int c) {
         const int tok0 = (int)(sbos + (long long)c * kChunk);
         const int trow = (int)(((long long)(cbase + c) * H + h) * kD);
-        mbar_arrive_expect_tx(&s.tma_bar[st], (use_do ? 10 : 4) * kTile);
-        tma_load_3d(s.k[st], &m.k, &s.tma_bar[st], 0, h, tok0);
-        tma_load_3d(s.k[st] + kTile, &m.k, &s.tma_bar[st], 64, h, tok0);
+        mbar_arrive_expect_tx(&s.tma_bar[st], (fused ? 8 : use_do ? 10 : 4) * kTile);
+        tma_load_3d(s.k[st] + kKOff, &m.k, &s.tma_bar[st], 0, h, tok0);
+        tma_load_3d(s.k[st] + kKOff + kKHalf, &m.k, &s.tma_bar[st], 64, h, tok0);
         tma_load_2d(s.w[st], &m.w, &s.tma_bar[st], 0, trow);
         if (use_do) {
             tma_load_3d(s.dO[st], &m.dO, &s.tma_bar[st], 0, h, tok0);
             tma_load_3d(s.dO[st] + kTile, &m.dO, &s.tma_bar[st], 64, h, tok0);
+        }
+        if (fused) {
+            tma_load_3d(s.k[st], &m.q, &s.tma_bar[st], 0, h, tok0);
+            tma_load_3d(s.k[st] + kKHalf, &m.q, &s.tma_bar[st], 64, h, tok0);
+        } else if (use_do) {
             tma_load_2d(s.qs[st], &m.qs, &s.tma_bar[st], 0, trow);
             tma_load_2d(s.qs[st] + kTile, &m.qs, &s.tma_bar[st], 0, trow + 64);
             tma_load_2d(s.y[st], &m.y, &s.tma_bar[st], 0, trow);
@@ -364,18 +381,21 @@ tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
         mbar_init(&s.tma_bar[1], 1);
         mbar_init(&s.bar_x, 1);
         mbar_init(&s.bar_z, 1);
+        mbar_init(&s.bar_q, 1);
+        mbar_init(&s.bar_y, 1);
         fence_barrier_init();
         if (c1 > c0) issue_tma(0, c1 - 1);
     }
+    constexpr uint32_t kTmemCols = fused ? 512 : 256;
     if (warp == 0) {
-        tmem_alloc(&s.tmem_base, 256);
+        tmem_alloc(&s.tmem_base, kTmemCols);
         tmem_relinquish();
         tc_fence_before();
     }
     float dH[64];     // dk half hs of row v of dH^T (= column v of dH)
     {
         const float *src = nullptr;
-        if (MODE == kDOut) {
+        if (kOut) {
             if (a.cp && j < nseg - 1)
                 src = a.seg_end + ((long long)(seq_seg_base(g, n) + j) * H + h) * kD * kD;
             else if (a.dht)
@@ -397,6 +417,7 @@ tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
     tc_fence_after();
     const uint32_t tbase = s.tmem_base;
     const uint32_t t_x = tbase, t_z = tbase + 128;
+    const uint32_t t_p = tbase + 64, t_y = tbase + 256;      // fused: P, Y^T
 
     // one commit per barrier per chunk: every barrier's parity is the chunk
     // iteration's; `pend` marks groups committed in this iteration, not yet waited
@@ -423,10 +444,19 @@ tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
             for (int kk = 0; kk < 8; ++kk) {
                 const uint32_t half = kk >> 2, sub = (kk & 3) * 32;
                 mma_bf16(t_x, desc_sw128(dhT + half * 2 * kTile + sub, 16, 1024),
-                         desc_sw128(kt + half * kTile + sub, 16, 1024), kIdKK64, kk > 0);
+                         desc_sw128(kt + kKOff + half * kKHalf + sub, 16, 1024), kIdKK64, kk > 0);
             }
             mma_commit(&s.bar_x);
-            if (use_do) {
+            if (fused) {
+                // [Q; K] K^T, rows 0-63 = Q K^T, on its own barrier
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (kk >> 2) * kKHalf + (kk & 3) * 32;
+                    mma_bf16(t_p, desc_sw128(kt + off, 16, 1024),
+                             desc_sw128(kt + kKOff + off, 16, 1024), kIdKK64, kk > 0);
+                }
+                mma_commit(&s.bar_q);
+            } else if (use_do) {
                 const uint32_t dO = smem_u32(s.dO[st]), qs = smem_u32(s.qs[st]);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
@@ -434,7 +464,7 @@ tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
                              desc_sw128(qs + kk * 2048, kTile, 1024), kIdMM128, kk > 0);
             }
         }
-        pend = 1;
+        pend = fused ? 5 : 1;
         // while the products run, the last warp requests chunk c - 1 (into the
         // stage the previous chunk used) and stores the gradient at this chunk's end
         if (c - 1 >= c0) {
@@ -444,7 +474,7 @@ tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
             }
             tma_pending |= 1 << (st ^ 1);
         }
-        if (MODE == kDOut && tma_thread) {
+        if (kOut && tma_thread) {
             // the bf16 dH^T tile, by TMA
             tma_store_2d(&m.dhc, s.dhT, 0, 2 * trow);
             tma_store_2d(&m.dhc, s.dhT + 2 * kTile, 0, 2 * trow + kD);
@@ -457,7 +487,7 @@ tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
             for (int half = 0; half < 2; ++half)
 #pragma unroll 8
                 for (int col = 0; col < 64; ++col) {
-                    const float x = ld_bf16(s.k[st] + half * kTile, r, col);
+                    const float x = ld_bf16(s.k[st] + kKOff + half * kKHalf, r, col);
                     ss += x * x;
                 }
             s.rk[r] = rsqrtf(ss + 1e-6f);
@@ -467,22 +497,81 @@ tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
             const float gl = s.gam[st][L - 1];
             s.fr[tid] = tid < L ? __expf(gl - s.gam[st][tid]) * (g.l2norm ? s.rk[tid] : 1.f) : 0.f;
         }
+        if (fused) {
+            // Qs = diag(scale e^gam) Q (zero past L) from the Q rows of the stage:
+            // thread t scales four 16-byte pieces of row t % 64
+            {
+                const int r = tid & 63;
+                const float f = r < L ? g.scale * __expf(s.gam[st][r]) : 0.f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int pc = 4 * (tid >> 6) + i, half = pc >> 3, chunk = pc & 7;
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(
+                        s.k[st] + half * kKHalf + r * 128 + ((chunk ^ (r & 7)) << 4));
+                    const __nv_bfloat16 *bb = reinterpret_cast<const __nv_bfloat16 *>(&raw);
+                    float x[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) x[e] = f * __bfloat162float(bb[e]);
+                    st_row8(s.qs[0] + half * kTile, r, chunk, x);
+                }
+            }
+            ok = mbar_wait(&s.bar_q, par, g.spin_limit, g.status);
+            if (__syncthreads_or(!ok)) { bailed = true; break; }
+            pend &= ~4;
+            tc_fence_after();
+            if (v < 64) {
+                // P row r = v, columns 32 hs .. +31: scale Q K^T D, masked to c <= r < L
+                const int r = v;
+                const float gr = s.gam[st][r];
+                float xp[32];
+                tmem_ld32(tmem_addr(t_p, warp, 32 * hs), xp);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float *x = xp + 8 * q;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int c = 32 * hs + 8 * q + e;
+                        x[e] = (c <= r && r < L) ? g.scale * x[e] * __expf(gr - s.gam[st][c]) : 0.f;
+                    }
+                    st_row8(s.p, r, 4 * hs + q, x);
+                }
+            }
+            tc_fence_before();
+            fence_proxy_async();
+            __syncthreads();
+            if (warp == 0) {
+                // Y^T = dO^T P, and dO^T Qs into the update accumulator
+                tc_fence_after();
+                const uint32_t dO = smem_u32(s.dO[st]), pp = smem_u32(s.p), qs = smem_u32(s.qs[0]);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    mma_bf16(t_y, desc_sw128(dO + kk * 2048, kTile, 1024),    // dO^T, MN-major
+                             desc_sw128(pp + kk * 2048, kTile, 1024), kIdMM64, kk > 0);   // P, MN-major
+                    mma_bf16(t_z, desc_sw128(dO + kk * 2048, kTile, 1024),
+                             desc_sw128(qs + kk * 2048, kTile, 1024), kIdMM128, kk > 0);
+                }
+                mma_commit(&s.bar_y);
+            }
+            pend |= 8;
+        }
         // the previous chunk's dU^T store has read its tile (this chunk's dH^T store,
         // the newest group, may go on)
         if (tma_thread) bulk_wait_read_but_newest();
         ok = mbar_wait(&s.bar_x, par, g.spin_limit, g.status);
+        if (fused) ok = mbar_wait(&s.bar_y, par, g.spin_limit, g.status) && ok;
         if (__syncthreads_or(!ok)) { bailed = true; break; }
         pend = 0;
         tc_fence_after();
         // dU^T row v, chunk rows 32*hs .. +31 (one TMEM load, groups of 8): Y^T + X^T diag(f)
-        float xs[32];
+        float xs[32], ys[32];
         tmem_ld32(tmem_addr(t_x, warp, 32 * hs), xs);
+        if (fused) tmem_ld32(tmem_addr(t_y, warp, 32 * hs), ys);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             float *x = xs + 8 * q;
             const int chunk = 4 * hs + q;
             uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-            if (use_do)
+            if (use_do && !fused)
                 raw = *reinterpret_cast<const uint4 *>(s.y[st] + v * 128 + ((chunk ^ (v & 7)) << 4));
             const __nv_bfloat16 *bv = reinterpret_cast<const __nv_bfloat16 *>(&raw);
             // f of rows 8 chunk .. +7 as two 16-byte broadcast reads
@@ -492,14 +581,15 @@ tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const int r = 8 * chunk + e;
-                x[e] = r < L ? __bfloat162float(bv[e]) + fq[e] * x[e] : 0.f;
+                const float y = fused ? ys[8 * q + e] : __bfloat162float(bv[e]);
+                x[e] = r < L ? y + fq[e] * x[e] : 0.f;
             }
             st_row8(s.duT, v, chunk, x);
         }
         tc_fence_before();
         fence_proxy_async();
         __syncthreads();
-        if (MODE == kDOut && tma_thread) {
+        if (kOut && tma_thread) {
             tma_store_2d(&m.du, s.duT, 0, trow);
             bulk_commit();
         }
@@ -546,6 +636,8 @@ tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
                 if (tma_pending & (1 << st))
                     mbar_drain(&s.tma_bar[st], ((it + (st != (it & 1))) >> 1) & 1);
             if (pend & 1) mbar_drain(&s.bar_x, it & 1);
+            if (pend & 4) mbar_drain(&s.bar_q, it & 1);
+            if (pend & 8) mbar_drain(&s.bar_y, it & 1);
             if (pend & 2) mbar_drain(&s.bar_z, it & 1);
         }
     } else if (MODE == kDMap) {
@@ -559,7 +651,7 @@ tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tbase, 256);
+    if (warp == 0) tmem_dealloc(tbase, kTmemCols);
 }
 
 // ------------------------------------------------------------------ host side
@@ -572,8 +664,7 @@ cudaError_t backward(const Plan &p, cudaStream_t s, bool have_ctx) {
     const long long tokens = (long long)g.B * g.T;
     const long long tile_rows = (long long)p.max_chunks * g.H * kD;
     DWalkMaps m;
-    CUtensorMap mq;
-    if ((e = make_map(&mq, g.q, tokens, g.H)) != cudaSuccess) return e;
+    if ((e = make_map(&m.q, g.q, tokens, g.H)) != cudaSuccess) return e;
     if ((e = make_map(&m.k, g.k, tokens, g.H)) != cudaSuccess) return e;
     if ((e = make_map(&m.dO, p.d_o, tokens, g.H)) != cudaSuccess) return e;
     if ((e = make_map_tiles(&m.w, p.ws.w, tile_rows)) != cudaSuccess) return e;
@@ -582,20 +673,31 @@ cudaError_t backward(const Plan &p, cudaStream_t s, bool have_ctx) {
     if ((e = make_map_tiles(&m.dhc, p.ws.dhc, 2 * tile_rows)) != cudaSuccess) return e;
     if ((e = make_map_tiles(&m.du, p.ws.du, tile_rows)) != cudaSuccess) return e;
 
-    const size_t ismem = sizeof(IntraSmem) + 1024;
-    if ((e = set_smem(tc_bwd_intra_kernel, ismem)) != cudaSuccess) return e;
-    prof_before("tc_bwd_intra", s);
-    const int n_items = p.max_chunks * g.H;
-    if ((e = launch_pdl(tc_bwd_intra_kernel, dim3(std::min(n_items, 2 * std::max(p.sms, 1))),
-                        dim3(256), ismem, s, mq, m.k, m.dO, m.qs, m.y, g, p.ws.gam, n_items)) !=
-        cudaSuccess)
-        return e;
-    prof_after(s);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // Without CP, when the reverse walk's CTAs fill at least three quarters of
+    // the SMs (q, k not L2-normalised inside), the walk forms P, Qs and Y^T
+    // itself and the chunk-parallel intra kernel is skipped: its work then
+    // costs the walk less than the separate pass (the rule of the forward's
+    // fused output walk).
+    const bool fuse_intra = !p.cp && !g.l2norm && 4 * g.N * g.H >= 3 * std::max(p.sms, 1);
+    if (!fuse_intra) {
+        const size_t ismem = sizeof(IntraSmem) + 1024;
+        if ((e = set_smem(tc_bwd_intra_kernel, ismem)) != cudaSuccess) return e;
+        prof_before("tc_bwd_intra", s);
+        const int n_items = p.max_chunks * g.H;
+        if ((e = launch_pdl(tc_bwd_intra_kernel, dim3(std::min(n_items, 2 * std::max(p.sms, 1))),
+                            dim3(256), ismem, s, m.q, m.k, m.dO, m.qs, m.y, g, p.ws.gam,
+                            n_items)) != cudaSuccess)
+            return e;
+        prof_after(s);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
 
-    const size_t smem = sizeof(DWalkSmem) + 1024;
+    const size_t smem = sizeof(DWalkSmem<kDOut>) + 1024;
+    const size_t map_smem = sizeof(DWalkSmem<kDMap>) + 1024;
+    const size_t fused_smem = sizeof(DWalkSmem<kDFused>) + 1024;
     if ((e = set_smem(tc_dwalk_kernel<kDOut>, smem)) != cudaSuccess) return e;
-    if ((e = set_smem(tc_dwalk_kernel<kDMap>, smem)) != cudaSuccess) return e;
+    if ((e = set_smem(tc_dwalk_kernel<kDMap>, map_smem)) != cudaSuccess) return e;
+    if ((e = set_smem(tc_dwalk_kernel<kDFused>, fused_smem)) != cudaSuccess) return e;
     TcDWalkArgs a{};
     a.ws_gam = p.ws.gam;
     a.dht = p.dht;
@@ -605,7 +707,7 @@ cudaError_t backward(const Plan &p, cudaStream_t s, bool have_ctx) {
         a.maps = p.ws.maps;
         a.seg_end = p.ws.seg_state;
         prof_before("tc_dwalk_map", s);
-        if ((e = launch_pdl(tc_dwalk_kernel<kDMap>, dim3(p.max_segs, g.H, 2), dim3(256), smem, s,
+        if ((e = launch_pdl(tc_dwalk_kernel<kDMap>, dim3(p.max_segs, g.H, 2), dim3(256), map_smem, s,
                             m, g, a)) != cudaSuccess)
             return e;
         prof_after(s);
@@ -613,6 +715,12 @@ cudaError_t backward(const Plan &p, cudaStream_t s, bool have_ctx) {
         if ((e = simt::cp_rscan(p, s)) != cudaSuccess) return e;
         prof_before("tc_dwalk_out", s);
         if ((e = launch_pdl(tc_dwalk_kernel<kDOut>, dim3(p.max_segs, g.H, 1), dim3(256), smem, s,
+                            m, g, a)) != cudaSuccess)
+            return e;
+        prof_after(s);
+    } else if (fuse_intra) {
+        prof_before("tc_dwalk_fused", s);
+        if ((e = launch_pdl(tc_dwalk_kernel<kDFused>, dim3(g.N, g.H, 1), dim3(256), fused_smem, s,
                             m, g, a)) != cudaSuccess)
             return e;
         prof_after(s);

@@ -1,12 +1,13 @@
-"""The state walk that forms O inside its chunk loop (used when the walk's CTAs
-fill most of the SMs, q and k not L2-normalised): O and the final state match
-the oracle, with and without intra-card sequence parallelism, and the separate
-output pass does not run; with few walk CTAs the output pass does run."""
+"""The walks that absorb a chunk-parallel pass when their CTAs fill most of
+the SMs (q and k not L2-normalised): the state walk that forms O (with and
+without intra-card sequence parallelism) and the reverse walk that forms P, Qs
+and Y^T itself (without it).  Results match the oracle, the absorbed pass does
+not run, and with few walk CTAs it does."""
 import pytest
 import torch
 
 import gdn_synth
-from gpu_helpers import TOL, check, gpu_fwd, lib, oracle_fwd
+from gpu_helpers import TOL, check, gpu_bwd, gpu_fwd, lib, oracle_bwd, oracle_fwd
 
 pytestmark = pytest.mark.gpu
 
@@ -43,3 +44,31 @@ def test_few_walk_ctas_use_the_output_pass():
     assert "tc_out" in names and "tc_walk" in names, names
     ro, rfs = oracle_fwd(p)
     check("o", o, ro, TOL["bf16"])
+
+
+def _bwd_kernels(p, cp):
+    gdn = lib()
+    gdn.gdn_profile_begin()
+    g = gpu_bwd(p, cp=cp)
+    torch.cuda.synchronize()
+    names = {n for n, _, _ in gdn.gdn_profile_end()}
+    return g, names
+
+
+@pytest.mark.parametrize("kw", [
+    dict(B=2, T=200, H=64),                          # 128 reverse-walk CTAs, ragged last chunk
+    dict(lengths=[130, 0, 64, 257, 1], H=32),        # varlen, one sequence empty
+])
+def test_fused_reverse_walk_matches_oracle(kw):
+    p = gdn_synth.make("training", h0_std=0.1, dht_std=0.01, **kw)
+    g, names = _bwd_kernels(p, "off")
+    assert "tc_dwalk_fused" in names and "tc_bwd_intra" not in names, names
+    r = oracle_bwd(p)
+    for k in ("dq", "dk", "dv", "dg", "dbeta", "dh0"):
+        check(k, g[k], r[k], TOL["bf16"])
+
+
+def test_few_reverse_walk_ctas_use_the_intra_pass():
+    p = gdn_synth.make("training", B=1, T=300, H=2, h0_std=0.1, dht_std=0.01)
+    g, names = _bwd_kernels(p, "off")
+    assert "tc_bwd_intra" in names and "tc_dwalk_out" in names, names
