@@ -131,7 +131,7 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         int ci_n = 0, h_n = 0;
         ChunkRef cr_n;
         const bool have_next = item_ref(item + (int)gridDim.x, ci_n, h_n, cr_n);
-        if (tid == 0) bulk_wait_read();       // the previous item's stores have read Qs, Y^T
+        if (tid == 0) bulk_wait_read_but_newest();   // the previous item's Qs store has read Qs
         tc_fence_before();
         __syncthreads();
         if (tid < 64) {
@@ -235,6 +235,8 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                          desc_sw128(pp + kk * 2048, kTile, 1024), kIdMM64, kk > 0);   // P, MN-major
             mma_commit(&s.mma_bar);
         }
+        // the previous item's Y^T store (older than this item's Qs store) has read Y^T
+        if (tid == 0) bulk_wait_read_but_newest();
         ok = mbar_wait(&s.mma_bar, 1, g.spin_limit, g.status);
         if (__syncthreads_or(!ok)) { bailed = true; break; }
         if (tid == 0 && have_next) {
