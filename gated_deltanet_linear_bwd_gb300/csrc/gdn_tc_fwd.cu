@@ -40,7 +40,7 @@ struct PrepSmem {
     float A[2][64][68];            // A^T per chunk (row j = column j of strict-lower A); rows padded
                                    // to 272 bytes so that 32 threads writing their own rows hit
                                    // every bank; reused for bw/bu below
-    float gam[2][64], bet[2][64], brk[2][64], wsum[4];
+    alignas(16) float gam[2][64], bet[2][64], brk[2][64], eg[2][64], wsum[4];   // eg: e^(g_i)
     float gpre[2][64], bpre[2][64];  // g and beta of the item, fetched during the previous one
     uint64_t tma_bar, mma_bar;
     uint32_t tmem_base;
@@ -145,6 +145,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         const float graw = r < L ? decay_of(g, s.gpre[ch][r], h) : 0.f;
         const float gam = scan64(graw, s.wsum);
         s.gam[ch][r] = gam;
+        s.eg[ch][r] = r < L ? __expf(graw) : 0.f;
         s.bet[ch][r] = r < L ? s.bpre[ch][r] : 0.f;
         if (r < L) ws_gam[tok * H + h] = gam;
 
@@ -178,20 +179,23 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             tc_fence_before();
             __syncthreads();
             // K K^T is symmetric, so this row is also column r: thread r writes
-            // A[i][r] = beta_i (k_i . k_r) e^(gamma_i - gamma_r) for i > r, i.e. row r of A^T
-            const float gr = s.gam[ch][r];
+            // A[i][r] = beta_i (k_i . k_r) e^(gamma_i - gamma_r) for i > r, i.e. row r of A^T.
+            // The decay is a running product: e^(gamma_i - gamma_r) = prod_{r<j<=i} e^(g_j),
+            // one exponential per token for the whole chunk instead of one per entry.
             float4 *arow = reinterpret_cast<float4 *>(s.A[ch][r]);
             const float4 *brk4 = reinterpret_cast<const float4 *>(s.brk[ch]);
-            const float4 *gam4 = reinterpret_cast<const float4 *>(s.gam[ch]);
+            const float4 *eg4 = reinterpret_cast<const float4 *>(s.eg[ch]);
+            float dec = 1.f;
 #pragma unroll
             for (int i4 = 0; i4 < 16; ++i4) {
-                const float4 b4 = brk4[i4], g4 = gam4[i4];
-                const float bb[4] = {b4.x, b4.y, b4.z, b4.w}, gg[4] = {g4.x, g4.y, g4.z, g4.w};
+                const float4 b4 = brk4[i4], g4 = eg4[i4];
+                const float bb[4] = {b4.x, b4.y, b4.z, b4.w}, ge[4] = {g4.x, g4.y, g4.z, g4.w};
                 float x[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int i = 4 * i4 + e;
-                    x[e] = (i > r && i < L) ? bb[e] * kk[i] * rk * __expf(gg[e] - gr) : 0.f;
+                    dec = i > r ? dec * ge[e] : 1.f;
+                    x[e] = (i > r && i < L) ? bb[e] * kk[i] * rk * dec : 0.f;
                 }
                 arow[i4] = make_float4(x[0], x[1], x[2], x[3]);
             }
