@@ -52,6 +52,7 @@ struct IntraSmem {
     uint8_t p[kTile];              // P rows r (scale included)
     float gam[64], rq[64], rk[64];
     float gpre[64];            // the next item's gam, fetched during the current one
+    float eg[64];              // e^(gam_j - gam_{j-1})
     uint64_t load_bar[2], mma_bar; // loads: {q, k}, {dO}
     uint32_t tmem_base;
 };
@@ -142,6 +143,10 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         bool ok = mbar_wait(&s.load_bar[0], it & 1, g.spin_limit, g.status);
         if (__syncthreads_or(!ok)) { bailed = true; break; }
         ++mma_n;
+        if (tid >= 192) {
+            const int j = tid - 192;
+            s.eg[j] = j > 0 ? __expf(s.gam[j] - s.gam[j - 1]) : 1.f;
+        }
         // every thread is past the copy of gpre above: the next item's gam can come
         if (tid < 64 && have_next)
             cp_async4(&s.gpre[tid], ws_gam + (cr_n.bos + min(tid, cr_n.len - 1)) * H + h_n,
@@ -194,17 +199,17 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         if (v < 64) {
             // P row r = v, columns c0 .. c0+31, scale included
             const int r = v;
-            const float gr = s.gam[r];
             const float sr = g.l2norm ? s.rq[r] : 1.f;
-            float xs[32];
+            float xs[32], dd[32];
             tmem_ld32(tmem_addr(t_p, warp, c0), xs);
+            row_decays32(s.gam, s.eg, r, c0, dd);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 float *x = xs + 8 * q;
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int c = c0 + 8 * q + e;
-                    x[e] = (c <= r && r < L) ? g.scale * x[e] * __expf(gr - s.gam[c]) * sr *
+                    x[e] = (c <= r && r < L) ? g.scale * x[e] * dd[8 * q + e] * sr *
                                                    (g.l2norm ? s.rk[c] : 1.f)
                                              : 0.f;
                 }
@@ -298,6 +303,7 @@ struct DWalkSmem {
     float gam[2][64];
     alignas(16) float fr[64];      // exp(gam_L - gam_r) (x 1/|k_r|), 0 past L
     float rk[64];
+    float egd[64];                 // exp(gam_j - gam_{j-1}) of the current chunk (fused)
     uint64_t tma_bar[2], bar_x, bar_z, bar_q, bar_y;
     uint32_t tmem_base;
 };
@@ -498,6 +504,7 @@ tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
         if (tid < 64) {
             const float gl = s.gam[st][L - 1];
             s.fr[tid] = tid < L ? __expf(gl - s.gam[st][tid]) * (g.l2norm ? s.rk[tid] : 1.f) : 0.f;
+            if (fused) s.egd[tid] = tid > 0 ? __expf(s.gam[st][tid] - s.gam[st][tid - 1]) : 1.f;
         }
         if (fused) {
             // Qs = diag(scale e^gam) Q (zero past L) from the Q rows of the stage:
@@ -524,16 +531,16 @@ tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
             if (v < 64) {
                 // P row r = v, columns 32 hs .. +31: scale Q K^T D, masked to c <= r < L
                 const int r = v;
-                const float gr = s.gam[st][r];
-                float xp[32];
+                float xp[32], dd[32];
                 tmem_ld32(tmem_addr(t_p, warp, 32 * hs), xp);
+                row_decays32(s.gam[st], s.egd, r, 32 * hs, dd);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     float *x = xp + 8 * q;
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const int c = 32 * hs + 8 * q + e;
-                        x[e] = (c <= r && r < L) ? g.scale * x[e] * __expf(gr - s.gam[st][c]) : 0.f;
+                        x[e] = (c <= r && r < L) ? g.scale * x[e] * dd[8 * q + e] : 0.f;
                     }
                     st_row8(s.p, r, 4 * hs + q, x);
                 }

@@ -370,6 +370,7 @@ struct WalkSmem {
     float gam[2][64];
     alignas(16) float fr[64];      // exp(gam_L - gam_r) (x 1/|k_r|); 0 past L
     alignas(16) float er[2][64];   // exp(gam_r) per chunk parity (output walk); 0 past L
+    float egw[2][64];              // exp(gam_j - gam_{j-1}) per chunk parity (output walk)
     float rk[64];
     uint64_t tma_bar[kStages], bar_u, bar_q, bar_dh;
     uint32_t tmem_base;
@@ -619,7 +620,10 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (tid < 64) {
             const float gl = s.gam[gb][L - 1], gr = s.gam[gb][tid];
             s.fr[tid] = tid < L ? __expf(gl - gr) * (g.l2norm ? s.rk[tid] : 1.f) : 0.f;
-            if (fused) s.er[gb][tid] = tid < L ? __expf(gr) : 0.f;
+            if (fused) {
+                s.er[gb][tid] = tid < L ? __expf(gr) : 0.f;
+                s.egw[gb][tid] = tid > 0 ? __expf(gr - s.gam[gb][tid - 1]) : 1.f;
+            }
         }
         ok = mbar_wait(&s.bar_u, par, g.spin_limit, g.status);
         if (__syncthreads_or(!ok)) { bailed = true; break; }
@@ -658,16 +662,16 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (fused && v < 64) {
             // row r = v of P: Q K^T on lanes 0-63, masked to c <= r < L, times D_rc
             const int r = v;
-            const float gr = s.gam[gb][r];
-            float xp[32];
+            float xp[32], dd[32];
             tmem_ld32(tmem_addr(t_p, warp, 32 * hs), xp);
+            row_decays32(s.gam[gb], s.egw[gb], r, 32 * hs, dd);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 float *x = xp + 8 * q;
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int c = 32 * hs + 8 * q + e;
-                    x[e] = (c <= r && r < L) ? x[e] * __expf(gr - s.gam[gb][c]) : 0.f;
+                    x[e] = (c <= r && r < L) ? x[e] * dd[8 * q + e] : 0.f;
                 }
                 st_row8(s.p, r, 4 * hs + q, x);
             }

@@ -32,7 +32,7 @@ struct OutSmem {
     uint8_t u[2 * kTile];      // u^T: [128 rows v][64 chunk rows]
     uint8_t h0T[4 * kTile];    // H0^T: [k half][128 rows v][64]; after wave 1: U^T
     uint8_t p[kTile];          // P rows r
-    float gam[64], er[64], rq[64], rk[64];
+    float gam[64], er[64], rq[64], rk[64], eg[64];   // eg: e^(gam_j - gam_{j-1})
     float gpre[64];            // the next item's gam, fetched during the current one
     uint64_t load_bar[3], mma_bar;  // loads: {q, k, W^T}, {u^T}, {H0^T}
     uint32_t tmem_base;
@@ -167,7 +167,10 @@ tc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             (tid >= 64 ? s.rk : s.rq)[r] = rsqrtf(ss + 1e-6f);
         }
         if (g.l2norm) __syncthreads();
-        if (tid < 64) s.er[tid] = tid < L ? __expf(s.gam[tid]) * (g.l2norm ? s.rq[tid] : 1.f) : 0.f;
+        if (tid < 64) {
+            s.er[tid] = tid < L ? __expf(s.gam[tid]) * (g.l2norm ? s.rq[tid] : 1.f) : 0.f;
+            s.eg[tid] = tid > 0 ? __expf(s.gam[tid] - s.gam[tid - 1]) : 1.f;
+        }
         ok = mbar_wait(&s.mma_bar, 0, g.spin_limit, g.status);
         ok = mbar_wait(&s.load_bar[1], it & 1, g.spin_limit, g.status) && ok;
         if (__syncthreads_or(!ok)) { bailed = true; break; }
@@ -197,9 +200,10 @@ tc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             }
             if (v < 64) {
                 const int r = v;
-                const float gr = s.gam[r];
                 const float sr = g.l2norm ? s.rq[r] : 1.f;
+                float dd[32];
                 tmem_ld32(tmem_addr(t_p, warp, c0), xs);
+                row_decays32(s.gam, s.eg, r, c0, dd);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     float *x = xs + 8 * q;
@@ -207,7 +211,7 @@ tc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     for (int e = 0; e < 8; ++e) {
                         const int c = c0 + 8 * q + e;
                         x[e] = (c <= r && r < L)
-                                   ? x[e] * __expf(gr - s.gam[c]) * sr * (g.l2norm ? s.rk[c] : 1.f)
+                                   ? x[e] * dd[8 * q + e] * sr * (g.l2norm ? s.rk[c] : 1.f)
                                    : 0.f;
                     }
                     st_row8(s.p, r, cq + q, x);

@@ -392,6 +392,24 @@ __device__ __forceinline__ void store_rows8(TG *col, long long rs, float (&x)[8]
     if (r0 + 4 + f < L) st4(p + 4 * rs, x + 4);
 }
 
+// Decay factors D_rc = e^(gam_r - gam_c) of row r for the 32 columns c = c_lo ..
+// c_lo + 31, valid where c <= r (the caller masks the rest).  They are formed as
+// a running product downward from c = min(r, c_lo + 31), using
+// e^(gam_r - gam_c) = e^(gam_r - gam_{c+1}) e^(gam_{c+1} - gam_c) with
+// eg[j] = e^(gam_j - gam_{j-1}): every factor multiplied in is a decay of one
+// token, so at most one exponential per row (when r lies past the block).
+__device__ __forceinline__ void row_decays32(const float *gam, const float *eg, int r, int c_lo,
+                                             float (&d)[32]) {
+    const int top = c_lo + 31;
+    float x = r > top ? __expf(gam[r] - gam[top]) : 1.f;
+#pragma unroll
+    for (int k = 31; k >= 0; --k) {
+        const int c = c_lo + k;
+        if (k < 31) x = c < r ? x * eg[c + 1] : 1.f;
+        d[k] = x;
+    }
+}
+
 __device__ __forceinline__ float ld_bf16(const uint8_t *tile, int row, int col) {
     return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tile + sw128_off(row, col)));
 }
