@@ -184,6 +184,23 @@ def oracle_sample(p, heads, reps_min_s=0.0):
     return dt, threads, sub.B * sub.T * len(heads)
 
 
+# ------------------------------------------------------------------ ranks
+def max_over_ranks(values, dist=None, device=None):
+    """The slowest rank's figure for each entry (max over ranks, which every rank
+    receives); the figures themselves when running alone."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_rate(world, units, ms):
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
+    return world * units / (ms / 1e3)
+
+
 # ------------------------------------------------------------------ main
 def main():
     ap = argparse.ArgumentParser()
@@ -448,16 +465,14 @@ def run_ours(args, rank, world, local):
     if status != 0:
         raise RuntimeError("device status after the timed region: " + gdn.gdn_last_error())
 
-    if dist:
-        t = torch.tensor([ms_step, ms_fwd, ms_e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step, ms_fwd, ms_e2e = t.tolist()
+    ms_step, ms_fwd, ms_e2e, ms_gated, ms_dec = max_over_ranks(
+        [ms_step, ms_fwd, ms_e2e, ms_gated, ms_dec], dist, dev)
     if rank != 0:
         if dist:
             dist.destroy_process_group()
         return 0
 
-    value = world * tokens / (ms_step / 1e3)
+    value = job_rate(world, tokens, ms_step)
     th = tokens * p.H
     step_bytes = th * (bytes_per_token_head(p.K, p.V, e_in, "fwd") +
                        bytes_per_token_head(p.K, p.V, e_in, "bwd"))
@@ -508,17 +523,17 @@ def run_ours(args, rank, world, local):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded; see gdn_synth.py)", "config": config_of(p, args.workload, True),
-            "fwd": {"value": world * tokens / (ms_fwd / 1e3), "unit": "tokens/s",
+            "fwd": {"value": job_rate(world, tokens, ms_fwd), "unit": "tokens/s",
                     "ms_per_step": ms_fwd,
                     "step_roofline": {"t_roof_ms": t_roof_fwd * 1e3,
                                       "frac": t_roof_fwd * 1e3 / ms_fwd,
                                       "bytes": fwd_bytes, "flops": fwd_flops}},
-            "decode": {"value": world * dn / (ms_dec / 1e3), "unit": "tokens/s",
+            "decode": {"value": job_rate(world, dn, ms_dec), "unit": "tokens/s",
                        "ms_per_step": ms_dec, "batch": f"{dn} sequences x {dh} heads",
                        "hbm_gbs": dec_bytes / (ms_dec / 1e3) / 1e9,
                        "frac_of_hbm": dec_bytes / (ms_dec / 1e3) / 1e9 / hbm,
                        "what": "one gdn_recurrent_step: state read and written once"},
-            "gated": {"value": world * tokens / (ms_gated / 1e3), "unit": "tokens/s",
+            "gated": {"value": job_rate(world, tokens, ms_gated), "unit": "tokens/s",
                       "ms_per_step": ms_gated,
                       "what": "the same fwd+bwd step with the decay formed inside from gate "
                               "logits (gate_scale), d(logits) and d(gate_scale) returned"},
@@ -530,7 +545,7 @@ def run_ours(args, rank, world, local):
             "kernels": [kernel_entry(n, l, m, sum(s[2] for s in prof), p, th, e_in)
                         for n, l, m in prof],
             "gpu_launches": total_launches,
-            "e2e": {"value": world * tokens / (ms_e2e / 1e3), "unit": "tokens/s",
+            "e2e": {"value": job_rate(world, tokens, ms_e2e), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "clocks": clk, "cpu_baseline": cpu}
     print(json.dumps(line), flush=True)
