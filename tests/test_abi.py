@@ -124,3 +124,43 @@ def test_missing_outputs_are_rejected(abi):
     rc = abi.load().gdn_chunk_bwd(ctypes.byref(b), ctypes.c_void_p(4096), 1 << 30, None)
     assert rc == abi.GDN_ERR_INVALID_ARG
     assert "required" in abi.gdn_last_error()
+
+
+def _step_args(abi, **kw):
+    a = abi.gdn_step_args()
+    a.q = a.k = a.v = a.g = a.beta = a.state = a.o = 4096
+    a.N, a.H, a.K, a.V = 2, 3, 128, 128
+    a.dtype = abi.GDN_BF16
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("bad, rc_name, msg", [
+    (dict(K=96), "GDN_ERR_UNSUPPORTED", "K = 96"),
+    (dict(V=32), "GDN_ERR_UNSUPPORTED", "V = 32"),
+    (dict(dtype=5), "GDN_ERR_UNSUPPORTED", "dtype"),
+    (dict(state=None), "GDN_ERR_INVALID_ARG", "required"),
+    (dict(o=None), "GDN_ERR_INVALID_ARG", "required"),
+    (dict(beta=4100), "GDN_ERR_INVALID_ARG", "aligned"),
+    (dict(N=-1), "GDN_ERR_INVALID_ARG", ">= 0"),
+])
+def test_decode_step_rejects_bad_arguments_on_the_host(abi, bad, rc_name, msg):
+    rc = abi.load().gdn_recurrent_step(ctypes.byref(_step_args(abi, **bad)), None)
+    assert rc == getattr(abi, rc_name)
+    assert msg in abi.gdn_last_error()
+
+
+def test_decode_step_with_no_sequences_is_a_host_side_no_op(abi):
+    assert abi.load().gdn_recurrent_step(ctypes.byref(_step_args(abi, N=0)), None) == abi.GDN_OK
+
+
+def test_saved_context_exists_only_on_the_tensor_core_path(abi):
+    bf = _fwd_args(abi, dtype=abi.GDN_BF16, K=128, V=128, T=1000)
+    n = abi.gdn_fwd_ctx_size(bf)
+    assert n > 0
+    # bf16 T, W, u and chunk start states, about 2KV/C + 2(K+V) + 132 bytes per token-head
+    per = (2 * 128 * 128 / 64 + 2 * 256 + 132) * 1000 * 2
+    assert 0.5 * per < n < 2 * per
+    assert abi.gdn_fwd_ctx_size(_fwd_args(abi, dtype=abi.GDN_FP32, K=128, V=128)) == 0
+    assert abi.gdn_fwd_ctx_size(_fwd_args(abi, dtype=abi.GDN_BF16, K=64, V=64)) == 0
