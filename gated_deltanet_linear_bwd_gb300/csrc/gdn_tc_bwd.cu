@@ -8,7 +8,8 @@
 //   dU^T = Y^T + X^T diag(f),            f = exp(gam_L - gam)
 //   dH^T <- exp(gam_L) dH^T + dO^T Qs - dU^T W
 // where the parts that do not depend on dH come from the chunk-parallel
-// intra kernel run first:
+// intra kernel run first, or, without CP when the walk's CTAs fill the GPU,
+// are formed inside the walk's own loop (its fused variant):
 //   P    = scale (Q K^T .* lower_incl .* D),  Y^T = dO^T P
 //   Qs   = diag(scale e^gam) Q
 // The segment map of the walk ([A' | B'], A' the transpose of the forward

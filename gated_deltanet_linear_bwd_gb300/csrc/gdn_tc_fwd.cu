@@ -11,10 +11,12 @@
 //   [Ka; Kb] [Ka; Kb]^T                -> the two 64x64 K K^T blocks
 //   A = strict_lower(diag(beta) K K^T .* D),  T = (I + A)^-1 (CUDA cores)
 //   W^T = K^T (diag(beta e) T^T),  u^T = V^T (diag(beta) T^T)
-// Walk kernel (per sequence or segment, sequential over chunks; only the
-// state recurrence, every chunk's start state stored for the output kernel):
+// Walk kernel (per sequence or segment, sequential over chunks; the state
+// recurrence, every chunk's start state stored for the output kernel):
 //   U^T = u^T - H^T W^T                 (state product)
 //   dH^T = (U^T diag(f)) K              H <- exp(gam_L) H + dH,  f = exp(gam_L - gam)
+// Its fused variant also forms each chunk's O inside the loop, so that no
+// output pass runs, when the walk's CTAs fill the GPU (host side, below).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
