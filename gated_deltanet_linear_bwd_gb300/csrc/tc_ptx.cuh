@@ -106,10 +106,6 @@ __device__ __forceinline__ void bulk_wait_read() {
 __device__ __forceinline__ void bulk_wait_read_but_newest() {
     asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
-// Waits until the issuing thread's bulk stores are complete.
-__device__ __forceinline__ void bulk_wait_all() {
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
 // 4-byte asynchronous global -> shared copy (zero-filled when !valid; the
 // source address must still be a valid one).  Unlike a plain load it does not
 // hold up the thread at the next barrier; cp_async_wait_all completes it.
@@ -195,20 +191,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
         : "memory");
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// Same for 8 consecutive columns.
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float *v) {
-    uint32_t r[8];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
-        "tcgen05.wait::ld.sync.aligned;\n"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7])
-        : "r"(taddr)
-        : "memory");
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // Two or three 8-column loads from different TMEM addresses, one wait: the
