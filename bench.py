@@ -1,12 +1,17 @@
 #!/usr/bin/env python
-"""Throughput of GDN chunked prefill (forward + backward) on GB300.
+"""Throughput of GDN chunked prefill (forward; forward + backward) on GB300.
 
 One step = one pass of the whole path over one batch of seeded synthetic
-input: forward (prep, state walk with output, intra-card sequence-parallel
-maps and scan) and backward (recomputed states, reverse gradient walk,
-chunk-local gradients).  Default workload: the edge / TP8 prefill shape
-(B=1, T=8192, H=8, K=V=128, bf16 q/k/v, fp32 g/beta/state, sequence
-parallelism forced).  Prints one JSON line on rank 0.
+input: the forward (prep, state walk with output, and the intra-card
+sequence-parallel maps and scan where the workload uses them) keeping its
+per-chunk context, then the backward (reverse gradient walk, chunk-local
+gradients) reading that context.  q and k are L2-normalised inside the
+library (use_qk_l2norm) unless --no-l2norm is given.
+
+Headline workload: the packed varlen batch (16 sequences of 512-8192 tokens,
+H=32, K=V=128, bf16 q/k/v, fp32 g/beta/state), the largest configuration that
+fits one GPU.  The training, long-context and edge workloads are reported as
+extra entries.  Prints one JSON line on rank 0.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -15,6 +20,7 @@ has here) on a bounded sample of the same workload.
 """
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -26,9 +32,14 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "GDN chunked-prefill tokens/s (fwd; fwd+bwd) on 1 GB300 + % of roofline"
+HEADLINE = "varlen"
+EXTRA_WORKLOADS = ("training", "long", "edge")
+WARMUP_WORKLOADS = {"edge": [0, 5], "long": [3]}     # sampled heads for the oracle check
+WARMUP_CHUNKS, WARMUP_TAU = 8, 1e-3
 CHUNK = 64
 GRAD_BYTES = 4          # dq, dk, dv come back in fp32 (the library's default)
 L2_BYTES = 129 * 2 ** 20
+SUSTAINED_S = 1.2       # length of the sustained block the clocks are sampled over
 
 
 # ------------------------------------------------------------------ algorithmic work
@@ -41,78 +52,78 @@ def flops_per_token_head(K, V, part):
     return 12 * K * V + 6 * C * K + 4 * C * V + 2 * C * C / 3
 
 
-def bytes_per_token_head(K, V, e, part):
-    """Inputs read once, outputs written once.  fwd: q, k, v, g, beta, o.
-    bwd: q, k, v, g, beta, dO in; dq, dk, dv (fp32), dg, dbeta out."""
+def bytes_per_token_head(K, V, e, part, eg=GRAD_BYTES):
+    """Inputs read once, outputs written once.  fwd: q, k, v, g, beta in, o out.
+    bwd: q, k, v, g, beta, dO in; dq, dk, dv (eg bytes each), dg, dbeta out."""
     if part == "fwd":
         return e * (2 * K + V) + 8 + e * V
-    return e * (2 * K + V) + 8 + e * V + 4 * (2 * K + V) + 8
+    return e * (2 * K + V) + 8 + e * V + eg * (2 * K + V) + 8
 
 
-# Per-kernel algorithmic FLOPs per token-head processed (the kernel's share
-# of the chunk form) -- used for the roofline of the dominant kernel.
-def kernel_flops_per_token_head(name, K, V):
+# Per-kernel HBM bytes per token-head on the tensor-core path (bf16 inputs, K =
+# V = 128, C = 64, gradients of eg bytes), split into ALGORITHMIC bytes (the
+# method's own inputs the kernel reads and outputs it writes, each once) and
+# OVERHEAD bytes (intermediates of the split design: the within-chunk cumsum
+# gam, the bf16 W^T / u^T / dU^T / Qs / Y^T chunk tiles of 2 bytes per feature,
+# the bf16 (I + A)^-1 of 2C bytes per token, and bf16 chunk states of 2KV/C
+# bytes per token).  The roofline of a kernel counts the algorithmic bytes only.
+def kernel_bytes_per_token_head(name, K, V, e=2, eg=GRAD_BYTES):
     C = CHUNK
+    t_mat = 2 * C
+    state = 2 * K * V / C
     table = {
-        "simt_prep": 2 * C * K + C * V + C * C / 3,
-        "simt_walk_out": 6 * K * V + C * K + C * V,
-        "simt_walk_states": 4 * K * V,
-        "simt_walk_map": 4 * K * (K + V),
-        "simt_dwalk_out": 6 * K * V + C * K + C * V,
-        "simt_dwalk_map": 4 * K * (K + V) + C * K + C * V,
-        "simt_local_grad": 6 * K * V + 6 * C * K + 3 * C * V + 2 * C * C / 3,
+        "tc_prep": (e * (K + V) + 8, 4 + 2 * (K + V) + t_mat),
+        "tc_walk": (e * K, 2 * (K + V) + 4 + state),
+        "tc_walk_fused": (2 * e * K + e * V, 2 * (K + V) + 4 + state),
+        "tc_out": (2 * e * K + e * V, 2 * (K + V) + state + 4),
+        "tc_bwd_intra": (e * (2 * K + V), 4 + 2 * K + 2 * V),
+        "tc_dwalk_out": (e * K + e * V, 2 * K + 2 * K + 2 * V + 4 + state + 2 * V),
+        "tc_dwalk_fused": (2 * e * K + e * V, 2 * K + 4 + state + 2 * V),
+        "tc_local_grad": (e * (2 * K + 2 * V) + 8 + eg * (2 * K + V) + 8,
+                          2 * (K + 2 * V) + 2 * state + t_mat),
     }
     return table.get(name)
 
 
-FP32_LANES_PER_SM = 128
+# DRAM bytes per token-head (dram__bytes_read.sum + dram__bytes_write.sum of one
+# launch, divided by the token-heads it processed) from one ncu capture of the
+# named kernel on the named workload; valid while the kernel's source file
+# still hashes to `sha256` (otherwise reported as null).  The kernels' traffic
+# grows in proportion to the token-heads processed, so it is scaled to the
+# benchmarked launch.
+NCU_TRAFFIC = {}
 
 
-# Per-kernel algorithmic HBM bytes per token-head for the tensor-core path
-# (bf16 q/k/v/dO, K = V = 128, chunk C = 64; gradients of eg bytes): every
-# operand the kernel needs read once, every result written once.  W^T, u^T,
-# dU^T, Y^T = (dO^T P)^T and Qs are bf16 chunk tiles (2 bytes per feature per
-# token); T is the bf16 64 x 64 inverse (128 bytes per token); hc / dhc are
-# the bf16 chunk states (K V 2 / C bytes per token).
-def kernel_bytes_per_token_head(name, K, V, e=2, eg=4):
-    C = CHUNK
-    t_mat = C * 2
-    state = K * V * 2 / C
-    table = {
-        "tc_prep": e * (K + V) + 8 + 4 + 2 * (K + V) + t_mat,
-        "tc_walk": e * K + 2 * (K + V) + 4 + state,
-        "tc_walk_fused": 2 * e * K + 2 * (K + V) + 4 + state + e * V,   # forms O as well
-        "tc_out": 2 * e * K + 2 * (K + V) + state + 4 + e * V,
-        "tc_bwd_intra": e * (2 * K + V) + 4 + 2 * K + 2 * V,
-        "tc_dwalk_out": e * K + 2 * K + e * V + 2 * K + 2 * V + 4 + state + 2 * V,
-        "tc_dwalk_fused": 2 * e * K + 2 * K + e * V + 4 + state + 2 * V,   # forms Qs, Y^T itself
-        "tc_local_grad": (e * (2 * K + 2 * V) + 2 * (K + 2 * V) + 2 * state + t_mat + 8 +
-                          eg * (2 * K + V) + 8),
-    }
-    return table.get(name)
-
-
-# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
-# ncu capture of the named kernel on the named workload, valid while the
-# kernel's source file still hashes to `sha256` (otherwise reported as null).
-NCU_TRAFFIC = {
-    ("tc_local_grad", "edge"): {
-        "file": "gdn_tc_local.cu", "bytes": 193560320 + 57232896,
-        "sha256": "2b572b435ef3a0a0bf77e87a6e4a458a739daf337dfe2fd966497e9585d25cd2"},
-}
-
-
-def measured_traffic(name, workload):
+def measured_traffic_per_th(name):
     import hashlib
-    rec = NCU_TRAFFIC.get((name, workload))
+    rec = NCU_TRAFFIC.get(name)
     if not rec:
-        return None
+        return None, None
     src = os.path.join(ROOT, "gated_deltanet_linear_bwd_gb300", "csrc", rec["file"])
     try:
         digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
     except OSError:
+        return None, None
+    if digest != rec["sha256"]:
+        return None, None
+    return rec["bytes_per_token_head"], rec["workload"]
+
+
+# ------------------------------------------------------------------ statistics
+def pct(xs, q):
+    """q-th percentile (0..100) by linear interpolation."""
+    s = sorted(xs)
+    if not s:
         return None
-    return rec["bytes"] if digest == rec["sha256"] else None
+    pos = (len(s) - 1) * q / 100.0
+    lo, hi = int(math.floor(pos)), int(math.ceil(pos))
+    return s[lo] + (s[hi] - s[lo]) * (pos - lo)
+
+
+def summary(ms_list):
+    return {"median_ms": statistics.median(ms_list), "p5_ms": pct(ms_list, 5),
+            "p95_ms": pct(ms_list, 95), "mean_ms": statistics.mean(ms_list),
+            "n": len(ms_list)}
 
 
 # ------------------------------------------------------------------ clocks
@@ -154,19 +165,31 @@ class ClockSampler:
             self.proc.kill()
         if not self.rows:
             return None
-        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
-        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[0]) for r in self.rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in self.rows if num(r[1]) is not None]
+        pw = [num(r[2]) for r in self.rows if num(r[2]) is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({n for r in self.rows for n, v in zip(names, r[4:]) if v == "Active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None,
+        # samples under load: power well above the idle floor
+        floor = min(pw) if pw else 0.0
+        loaded = [num(r[0]) for r in self.rows
+                  if num(r[2]) is not None and num(r[2]) > floor + 100 and num(r[0]) is not None]
+        return {"sm_mhz": statistics.median(loaded or sm) if (loaded or sm) else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(self.rows)}
+                "samples": len(self.rows), "samples_under_load": len(loaded),
+                "power_w_max": max(pw) if pw else None}
 
 
 # ------------------------------------------------------------------ CPU oracle
 def oracle_sample(p, heads, reps_min_s=0.0):
-    """fp64 oracle forward + backward on the given heads of problem p.
-    Returns (seconds per pass, threads used, token-heads per pass)."""
+    """fp64 oracle forward + backward on the given heads of problem p (every
+    sequence).  Returns (seconds per pass, threads used, token-heads per pass)."""
     import oracle
     sub = p.heads(heads)
     threads = min(oracle.max_threads(), len(heads) * sub.N)
@@ -201,6 +224,27 @@ def job_rate(world, units, ms):
     return world * units / (ms / 1e3)
 
 
+# ------------------------------------------------------------------ the timed calls
+def training_step(gdn, x, cp, l2):
+    """The benchmarked step: the forward keeps its per-chunk context and the
+    backward reuses it.  Returns (o, final_state, dq, dk, dv, dg, dbeta, dh0)."""
+    o, fs, saved = gdn.chunk_gated_delta_rule_fwd(x.q, x.k, x.v, x.g, x.beta,
+                                                  initial_state=x.h0, output_final_state=True,
+                                                  cu_seqlens=x.cu_seqlens, use_qk_l2norm=l2,
+                                                  cp=cp, save_ctx=True)
+    grads = gdn.chunk_gated_delta_rule_bwd(x.q, x.k, x.v, x.g, x.beta, x.do, dht=x.dht,
+                                           initial_state=x.h0, cu_seqlens=x.cu_seqlens,
+                                           use_qk_l2norm=l2, cp=cp, ctx=saved)
+    return (o, fs) + tuple(grads)
+
+
+def forward_step(gdn, x, cp, l2, **kw):
+    """The benchmarked forward alone (no context kept)."""
+    return gdn.chunk_gated_delta_rule_fwd(x.q, x.k, x.v, x.g, x.beta, initial_state=x.h0,
+                                          output_final_state=True, cu_seqlens=x.cu_seqlens,
+                                          use_qk_l2norm=l2, cp=cp, **kw)
+
+
 # ------------------------------------------------------------------ main
 def main():
     ap = argparse.ArgumentParser()
@@ -208,8 +252,12 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="edge")
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--extra", default=",".join(EXTRA_WORKLOADS),
+                    help="comma-separated extra workloads ('' for none)")
+    ap.add_argument("--no-l2norm", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-warmup-check", action="store_true")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -225,51 +273,242 @@ def workload_problem(name):
     return gdn_synth.make(name)
 
 
-def config_of(p, name, graph=False):
+def config_of(p, name, l2, graph=False):
     m = p.meta
-    return {"workload": f"{name}: B={p.B} T={p.T} H={p.H} K={p.K} V={p.V} "
-                        f"{m['dtype']} q/k/v, fp32 g/beta/state, cp={m['cp']}, "
-                        f"fwd (keeping its context) + bwd",
-            "global_batch": p.B, "seq_len": p.T, "heads": p.H, "parallelism": "replicas",
+    shape = (f"N={p.N} packed sequences of {min(m['lengths'])}-{max(m['lengths'])} tokens "
+             f"({p.T} in all)" if p.cu_seqlens is not None else f"B={p.B} T={p.T}")
+    return {"workload": f"{name}: {shape} H={p.H} K={p.K} V={p.V} {m['dtype']} q/k/v, fp32 "
+                        f"g/beta/state, cp={m['cp']}, use_qk_l2norm={l2}; step = fwd (keeping "
+                        f"its context) + bwd",
+            "global_batch": p.N, "seq_len": p.T, "heads": p.H, "parallelism": "replicas",
             "l2_flush_between_steps": True,
             **({"launch": "one CUDA graph per step"} if graph else {})}
+
+
+def reference_heads(p):
+    return [0]
 
 
 def run_reference(args, rank, world):
     if rank != 0:
         return 0
     p = workload_problem(args.workload)
-    heads = list(range(p.H))
+    heads = reference_heads(p)
     for _ in range(args.warmup):
-        oracle_sample(p, heads[:1])
+        oracle_sample(p, heads)
     times = []
     threads = tokens_heads = None
     for _ in range(args.steps):
         dt, threads, tokens_heads = oracle_sample(p, heads)
         times.append(dt)
-    ms = 1e3 * statistics.mean(times)
-    tok = tokens_heads / p.H
-    value = tok / (ms / 1e3)
+    ms = 1e3 * statistics.median(times)
+    tok = tokens_heads / len(heads)              # tokens of the whole batch per sampled head
+    # the whole workload has p.H heads: its tokens/s is the sampled rate / H
+    value = tok / p.H / (ms / 1e3) * len(heads)
+    sample = (f"fp64 oracle fwd+bwd over head(s) {heads} of the {args.workload} workload "
+              f"(all {p.N} sequences, {p.T} tokens) per step; tokens/s scaled to all {p.H} heads")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": config_of(p, args.workload),
+            "data": "synthetic", "config": config_of(p, args.workload, not args.no_l2norm),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads,
-                             "kind": "oracle",
-                             "sample": f"fp64 oracle fwd+bwd over all {p.H} heads of the "
-                                       f"{args.workload} workload per step"},
+                             "host_cores": os.cpu_count(), "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
 
 
-def kernel_entry(name, launches, ms, total_ms, p, th, e_in):
-    ent = {"name": name, "launches": launches, "ms": ms, "share": ms / total_ms}
-    by_th = kernel_bytes_per_token_head(name, p.K, p.V, e_in, GRAD_BYTES)
-    if by_th is not None:
-        ent["gbs"] = by_th * th / (ms / launches / 1e3) / 1e9
-    return ent
+class Timer:
+    """Per-step CUDA events on the launching stream, the L2 flushed between steps
+    outside the events."""
+
+    def __init__(self, torch, dev, stream, dist):
+        self.torch, self.dev, self.stream, self.dist = torch, dev, stream, dist
+        self.flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def run(self, fn, steps, profile_gdn=None):
+        torch = self.torch
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        torch.cuda.synchronize(self.dev)
+        if self.dist:
+            self.dist.barrier()
+        torch.cuda.synchronize(self.dev)
+        if profile_gdn:
+            profile_gdn.gdn_profile_begin()
+        for i in range(steps):
+            self.flush.fill_(float(i))                 # evict the inputs from L2 (untimed)
+            starts[i].record(self.stream)
+            fn()
+            ends[i].record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        prof = profile_gdn.gdn_profile_end() if profile_gdn else None
+        if self.dist:
+            self.dist.barrier()
+        return [s.elapsed_time(e) for s, e in zip(starts, ends)], prof
+
+
+def graphed(torch, dev, fn):
+    """fn captured once as a CUDA graph: the library launches only on the current
+    stream and neither allocates nor synchronises inside a call, so a whole step
+    replays as one graph launch (same kernels, no per-launch host work)."""
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        for _ in range(2):
+            fn()
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        fn()
+    torch.cuda.synchronize(dev)
+    return graph.replay, graph
+
+
+def roofline_terms(p, e_in, peaks):
+    th = p.B * p.T * p.H
+    hbm = peaks.get("hbm_gbs", 6800.0)
+    bf16 = peaks.get("bf16_tflops", 1900.0)
+    states = p.N * p.H * p.K * p.V * 4
+    fwd_bytes = th * bytes_per_token_head(p.K, p.V, e_in, "fwd") + states * (2 if p.h0 is not None else 1)
+    fwd_flops = th * flops_per_token_head(p.K, p.V, "fwd")
+    bwd_bytes = th * bytes_per_token_head(p.K, p.V, e_in, "bwd")
+    bwd_bytes += states * ((1 if p.dht is not None else 0) + 1)       # dh_T in, dh0 out
+    step_bytes = fwd_bytes + bwd_bytes
+    step_flops = fwd_flops + th * flops_per_token_head(p.K, p.V, "bwd")
+    t_step = max(step_bytes / (hbm * 1e9), step_flops / (bf16 * 1e12))
+    t_fwd = max(fwd_bytes / (hbm * 1e9), fwd_flops / (bf16 * 1e12))
+    return dict(th=th, hbm=hbm, bf16=bf16, step_bytes=step_bytes, step_flops=step_flops,
+                fwd_bytes=fwd_bytes, fwd_flops=fwd_flops, t_step=t_step, t_fwd=t_fwd)
+
+
+def kernel_table(prof, steps, p, e_in):
+    th = p.B * p.T * p.H
+    total = sum(s[2] for s in prof)
+    out = []
+    for name, launches, ms in prof:
+        ent = {"name": name, "launches_per_step": launches / steps, "ms_per_step": ms / steps,
+               "share": ms / total}
+        b = kernel_bytes_per_token_head(name, p.K, p.V, e_in, GRAD_BYTES)
+        if b is not None:
+            per_launch_s = ms / launches / 1e3
+            ent["alg_gbs"] = b[0] * th / per_launch_s / 1e9
+            ent["all_gbs"] = (b[0] + b[1]) * th / per_launch_s / 1e9
+        out.append(ent)
+    return out
+
+
+def dominant_roofline(prof, p, e_in, rt, peaks_src):
+    dom = max(prof, key=lambda s: s[2])
+    name, launches, ms = dom
+    th = rt["th"]
+    avg_s = ms / launches / 1e3
+    b = kernel_bytes_per_token_head(name, p.K, p.V, e_in, GRAD_BYTES)
+    if b is None:
+        return {"kernel": name, "bound": "hbm", "unit": "GB/s", "achieved": None,
+                "peak": rt["hbm"], "frac": None, "traffic": None,
+                "avg_launch_ms": avg_s * 1e3}
+    alg, ovh = b[0] * th, b[1] * th
+    tr_th, tr_wl = measured_traffic_per_th(name)
+    traffic = None if tr_th is None else tr_th * th
+    achieved = alg / avg_s / 1e9
+    return {"kernel": name, "bound": "hbm", "unit": "GB/s", "achieved": achieved,
+            "peak": rt["hbm"], "frac": achieved / rt["hbm"],
+            "peak_source": f"{peaks_src} HBM copy bandwidth (MEASURED_PEAKS hbm_gbs)",
+            "bytes_per_launch": alg, "overhead_bytes": ovh,
+            "achieved_incl_overhead": (alg + ovh) / avg_s / 1e9,
+            "traffic": traffic,
+            "traffic_ratio": None if traffic is None else traffic / alg,
+            "traffic_source": None if tr_wl is None else
+            f"ncu DRAM read+write per token-head of one launch on the {tr_wl} workload, "
+            f"scaled to this launch's token-heads",
+            "avg_launch_ms": avg_s * 1e3, "launches_per_step": None}
+
+
+def measure_workload(torch, gdn, name, args, timer, dev, peaks, peaks_src, l2, headline=False):
+    """Times the fwd+bwd step and the forward of one workload (graph replays)."""
+    p = workload_problem(name)
+    cp = p.meta["cp"]
+    d = p.to(dev)
+    e_in = 2 if p.meta["dtype"] == "bf16" else 4
+    tokens = p.B * p.T
+    steps = args.steps
+    for _ in range(max(args.warmup, 3)):
+        training_step(gdn, d, cp, l2)
+    torch.cuda.synchronize(dev)
+    st = timer.stream
+    if gdn.gdn_sync_status(st.cuda_stream) != 0:
+        raise RuntimeError(f"{name}: device status after warm-up: " + gdn.gdn_last_error())
+    step_g, g1 = graphed(torch, dev, lambda: training_step(gdn, d, cp, l2))
+    fwd_g, g2 = graphed(torch, dev, lambda: forward_step(gdn, d, cp, l2))
+    for _ in range(max(args.warmup, 3)):
+        step_g()
+        fwd_g()
+    res = {"p": p, "d": d, "cp": cp, "e_in": e_in, "tokens": tokens, "graphs": (g1, g2)}
+    clocks = None
+    if headline:
+        props = torch.cuda.get_device_properties(dev)
+        uuid = getattr(props, "uuid", None)
+        clocks = ClockSampler(f"GPU-{uuid}" if uuid is not None and
+                              not str(uuid).startswith("GPU") else uuid)
+    ms_step, _ = timer.run(step_g, steps)
+    if headline:
+        # the same step repeated for >= SUSTAINED_S, so that the clock samples cover a
+        # sustained run; reported beside the K-step figures
+        n_s = max(steps, int(math.ceil(SUSTAINED_S * 1e3 / statistics.median(ms_step))))
+        ms_sus, _ = timer.run(step_g, n_s)
+        res["sustained"] = summary(ms_sus)
+        res["clocks"] = clocks.stop()
+    ms_fwd, _ = timer.run(fwd_g, steps)
+    # per-kernel times from the library's own CUDA events, in a separate eager pass:
+    # events between kernels stop them from overlapping, so they stay out of ms_step
+    _, prof = timer.run(lambda: training_step(gdn, d, cp, l2), steps, profile_gdn=gdn)
+    _, prof_fwd = timer.run(lambda: forward_step(gdn, d, cp, l2), steps, profile_gdn=gdn)
+    if gdn.gdn_sync_status(st.cuda_stream) != 0:
+        raise RuntimeError(f"{name}: device status after the timed region: " +
+                           gdn.gdn_last_error())
+    res.update(ms_step=ms_step, ms_fwd=ms_fwd, prof=prof, prof_fwd=prof_fwd)
+    return res
+
+
+def warmup_report(torch, gdn, name, heads, timer, dev, args, l2):
+    """The warmup shortcut (flag): its error against the oracle on sampled heads,
+    reported apart from the exact path, the fraction of heads that took it, and
+    the forward's time with and without it."""
+    import numpy as np
+    import oracle
+    p = workload_problem(name)
+    d = p.to(dev)
+    stats = torch.zeros(2, dtype=torch.int32, device=dev)
+    kw = dict(cp_warmup_chunks=WARMUP_CHUNKS, cp_warmup_tau=WARMUP_TAU)
+    o_w, fs_w = forward_step(gdn, d, "force", l2, cp_stats=stats, **kw)
+    o_x, fs_x = forward_step(gdn, d, "force", l2)
+    torch.cuda.synchronize(dev)
+    took, total = stats.tolist()
+    sub = p.heads(heads)
+    ro, rfs = oracle.fwd(sub.q, sub.k, sub.v, sub.g, sub.beta, h0=sub.h0,
+                         cu_seqlens=sub.cu_seqlens, use_l2norm=l2)
+
+    def err(a, b):
+        return float(np.abs(a.float().cpu().numpy().astype(np.float64) - b).max())
+    e_w = max(err(o_w[:, :, heads], ro), err(fs_w[:, heads], rfs))
+    e_x = max(err(o_x[:, :, heads], ro), err(fs_x[:, heads], rfs))
+    fw, _ = graphed(torch, dev, lambda: forward_step(gdn, d, "force", l2, **kw))
+    fx, _ = graphed(torch, dev, lambda: forward_step(gdn, d, "force", l2))
+    for _ in range(3):
+        fw()
+        fx()
+    t_w, _ = timer.run(fw, args.steps)
+    t_x, _ = timer.run(fx, args.steps)
+    return {"window_chunks": WARMUP_CHUNKS, "tau": WARMUP_TAU,
+            "heads_taking_shortcut": took, "heads_under_cp": total,
+            "fraction": took / total if total else None,
+            "pages_claim": "6-8 chunks enough for 60-80% of heads",
+            "max_abs_err_vs_oracle": e_w, "exact_path_max_abs_err_vs_oracle": e_x,
+            "sampled_heads": heads, "fwd_ms_median": statistics.median(t_w),
+            "exact_fwd_ms_median": statistics.median(t_x)}
 
 
 def run_ours(args, rank, world, local):
@@ -287,136 +526,25 @@ def run_ours(args, rank, world, local):
         peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
     except OSError:
         pass
-
-    p = workload_problem(args.workload)
-    cp = p.meta["cp"]
-    d = p.to(dev)
-    e_in = 2 if p.meta["dtype"] == "bf16" else 4
-    tokens = p.B * p.T
+    peaks_src = "measured" if "hbm_gbs" in peaks else "fallback"
+    l2 = not args.no_l2norm
     stream = torch.cuda.current_stream(dev)
+    timer = Timer(torch, dev, stream, dist)
 
-    def step(x):
-        # a training step: the forward keeps its per-chunk context, the backward reuses it
-        o, fs, saved = gdn.chunk_gated_delta_rule_fwd(x.q, x.k, x.v, x.g, x.beta,
-                                                      initial_state=x.h0, output_final_state=True,
-                                                      cu_seqlens=x.cu_seqlens, cp=cp,
-                                                      save_ctx=True)
-        grads = gdn.chunk_gated_delta_rule_bwd(x.q, x.k, x.v, x.g, x.beta, x.do, dht=x.dht,
-                                               initial_state=x.h0, cu_seqlens=x.cu_seqlens, cp=cp,
-                                               ctx=saved)
-        return (o, fs) + tuple(grads)
+    h = measure_workload(torch, gdn, args.workload, args, timer, dev, peaks, peaks_src, l2,
+                         headline=True)
+    p, d, cp, e_in, tokens = h["p"], h["d"], h["cp"], h["e_in"], h["tokens"]
 
-    def fwd_only(x):
-        return gdn.chunk_gated_delta_rule_fwd(x.q, x.k, x.v, x.g, x.beta, initial_state=x.h0,
-                                              output_final_state=True, cu_seqlens=x.cu_seqlens,
-                                              cp=cp)
-
-    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
-
-    def timed(fn, steps, profile=False):
-        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-        torch.cuda.synchronize(dev)
-        if dist:
-            dist.barrier()
-        torch.cuda.synchronize(dev)
-        if profile:
-            gdn.gdn_profile_begin()
-        for i in range(steps):
-            flush.fill_(float(i))                      # evict the inputs from L2 (untimed)
-            starts[i].record(stream)
-            fn()
-            ends[i].record(stream)
-        torch.cuda.synchronize(dev)
-        prof = gdn.gdn_profile_end() if profile else None
-        if dist:
-            dist.barrier()
-        ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / steps
-        return ms, prof
-
-    def graphed(fn):
-        # fn captured once as a CUDA graph: the library launches only on the current
-        # stream and neither allocates nor synchronises inside a call, so a whole
-        # step replays as one graph launch (same kernels, no per-launch host work)
-        side = torch.cuda.Stream(dev)
-        side.wait_stream(torch.cuda.current_stream(dev))
-        with torch.cuda.stream(side):
-            for _ in range(2):
-                fn()
-        torch.cuda.current_stream(dev).wait_stream(side)
-        torch.cuda.synchronize(dev)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            fn()
-        torch.cuda.synchronize(dev)
-        return graph.replay
-
-    for _ in range(max(args.warmup, 3)):
-        step(d)
-    torch.cuda.synchronize(dev)
-    if gdn.gdn_sync_status(stream.cuda_stream) != 0:
-        raise RuntimeError("device status after warm-up: " + gdn.gdn_last_error())
-    step_g = graphed(lambda: step(d))
-    fwd_g = graphed(lambda: fwd_only(d))
-    for _ in range(max(args.warmup, 3)):
-        step_g()
-        fwd_g()
-
-    gpu_index = torch.cuda.get_device_properties(dev)
-    uuid = getattr(gpu_index, "uuid", None)
-    clocks = ClockSampler(f"GPU-{uuid}" if uuid is not None and not str(uuid).startswith("GPU")
-                          else uuid)
-    ms_step, _ = timed(step_g, args.steps)
-    ms_fwd, _ = timed(fwd_g, args.steps)
-
-    # the same step with the gate formed inside the library from raw logits
-    import gdn_synth
-    gx, ga = (t.to(dev) for t in gdn_synth.gate_draws(p, seed=0))
-
-    def gated_step(x):
-        o, fs, saved = gdn.chunk_gated_delta_rule_fwd(x.q, x.k, x.v, gx, x.beta,
-                                                      initial_state=x.h0, output_final_state=True,
-                                                      cu_seqlens=x.cu_seqlens, cp=cp,
-                                                      save_ctx=True, gate_scale=ga)
-        return gdn.chunk_gated_delta_rule_bwd(x.q, x.k, x.v, gx, x.beta, x.do, dht=x.dht,
-                                              initial_state=x.h0, cu_seqlens=x.cu_seqlens,
-                                              cp=cp, ctx=saved, gate_scale=ga)
-
-    gated_g = graphed(lambda: gated_step(d))
-    for _ in range(max(args.warmup, 3)):
-        gated_g()
-    ms_gated, _ = timed(gated_g, args.steps)
-
-    # decode: one token for each of 64 sequences x 32 heads from resident fp32 states
-    dn, dh = 64, 32
-    dgen = torch.Generator(device="cpu").manual_seed(7)
-    dq_ = (torch.randn(dn, dh, p.K, generator=dgen) / p.K ** 0.5).to(dev, d.q.dtype)
-    dk_ = (torch.randn(dn, dh, p.K, generator=dgen) / p.K ** 0.5).to(dev, d.q.dtype)
-    dv_ = torch.randn(dn, dh, p.V, generator=dgen).to(dev, d.q.dtype)
-    dg_ = -torch.rand(dn, dh, generator=dgen).to(dev)
-    db_ = torch.rand(dn, dh, generator=dgen).to(dev)
-    dst = (0.1 * torch.randn(dn, dh, p.K, p.V, generator=dgen)).to(dev)
-
-    def decode_step():
-        gdn.recurrent_step(dq_, dk_, dv_, dg_, db_, dst)
-
-    for _ in range(max(args.warmup, 3)):
-        decode_step()
-    ms_dec, _ = timed(decode_step, args.steps)
-    dec_bytes = 2 * dst.numel() * 4 + dn * dh * (2 * p.K + 2 * p.V) * e_in + dn * dh * 8
-    # per-kernel times from the library's own CUDA events, in a separate pass: the
-    # events between kernels stop them from overlapping, so they stay out of ms_step
-    _, prof = timed(lambda: step(d), args.steps, profile=True)
-
-    # end to end through the public API: pinned host inputs in, results back out
-    host_in = {k: getattr(p, k) for k in ("q", "k", "v", "g", "beta", "h0", "do", "dht")}
+    # end to end through the public API, called eagerly every step: pinned host
+    # inputs in, every result back to pinned host memory
+    host_in = {k: getattr(p, k) for k in ("q", "k", "v", "g", "beta", "h0", "cu_seqlens",
+                                          "do", "dht")}
     host_in = {k: v.pin_memory() for k, v in host_in.items() if v is not None}
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
-    outs = step(d)
+    outs = training_step(gdn, d, cp, l2)
     host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs
                 if o is not None]
     d2h = sum(o.numel() * o.element_size() for o in host_out)
-
     copy_stream = torch.cuda.Stream(dev)
     n_fwd_out = sum(1 for o in outs[:2] if o is not None)
 
@@ -426,7 +554,7 @@ def run_ours(args, rank, world, local):
         # final state travel back while the backward runs.
         main = torch.cuda.current_stream(dev)
         x = {k: host_in[k].to(dev, non_blocking=True)
-             for k in ("q", "k", "v", "g", "beta", "h0") if k in host_in}
+             for k in ("q", "k", "v", "g", "beta", "h0", "cu_seqlens") if k in host_in}
         copy_stream.wait_stream(main)
         inputs_in = torch.cuda.Event()
         with torch.cuda.stream(copy_stream):
@@ -436,7 +564,8 @@ def run_ours(args, rank, world, local):
             t.record_stream(main)
         o, fs, saved = gdn.chunk_gated_delta_rule_fwd(
             x["q"], x["k"], x["v"], x["g"], x["beta"], initial_state=x.get("h0"),
-            output_final_state=True, cu_seqlens=d.cu_seqlens, cp=cp, save_ctx=True)
+            output_final_state=True, cu_seqlens=x.get("cu_seqlens"), use_qk_l2norm=l2, cp=cp,
+            save_ctx=True)
         fwd_out = [t for t in (o, fs) if t is not None]
         copy_stream.wait_stream(main)
         with torch.cuda.stream(copy_stream):
@@ -447,107 +576,121 @@ def run_ours(args, rank, world, local):
         main.wait_event(inputs_in)
         grads = gdn.chunk_gated_delta_rule_bwd(
             x["q"], x["k"], x["v"], x["g"], x["beta"], xb["do"], dht=xb.get("dht"),
-            initial_state=x.get("h0"), cu_seqlens=d.cu_seqlens, cp=cp, ctx=saved)
+            initial_state=x.get("h0"), cu_seqlens=x.get("cu_seqlens"), use_qk_l2norm=l2,
+            cp=cp, ctx=saved)
         for hbuf, t in zip(host_out[n_fwd_out:], [t for t in grads if t is not None]):
             hbuf.copy_(t, non_blocking=True)
         main.wait_stream(copy_stream)
 
-    e2e_g = graphed(e2e_step)
     for _ in range(max(args.warmup, 3)):
-        e2e_g()
-    ms_e2e, _ = timed(e2e_g, args.steps)
+        e2e_step()
+    ms_e2e, _ = timer.run(e2e_step, args.steps)
     torch.cuda.synchronize(dev)
     for hbuf, t in zip(host_out, [t for t in outs if t is not None]):
         if not torch.equal(hbuf, t.cpu()):
             raise RuntimeError("end-to-end results differ from the device-resident step")
-    clk = clocks.stop()
+    # the same end-to-end step captured once as a CUDA graph (no per-call host work)
+    e2e_g, e2e_graph_obj = graphed(torch, dev, e2e_step)
+    for _ in range(3):
+        e2e_g()
+    ms_e2e_graph, _ = timer.run(e2e_g, args.steps)
+    torch.cuda.synchronize(dev)
+
+    # everything the headline line needs, before its tensors are released
+    rt = roofline_terms(p, e_in, peaks)
+    head = {"ms_step": h["ms_step"], "ms_fwd": h["ms_fwd"], "prof": h["prof"],
+            "prof_fwd": h["prof_fwd"], "sustained": h["sustained"], "clocks": h["clocks"]}
+    del h, outs, host_out, e2e_g, e2e_graph_obj, d
+    torch.cuda.empty_cache()
+
+    extra = {}
+    for name in [w for w in args.extra.split(",") if w and w != args.workload]:
+        x = measure_workload(torch, gdn, name, args, timer, dev, peaks, peaks_src, l2)
+        xp = x["p"]
+        xrt = roofline_terms(xp, x["e_in"], peaks)
+        ms_s, ms_f = statistics.median(x["ms_step"]), statistics.median(x["ms_fwd"])
+        extra[name] = {
+            "config": config_of(xp, name, l2, True)["workload"],
+            "fwd_bwd": {"value": job_rate(world, x["tokens"], ms_s), "unit": "tokens/s",
+                        **summary(x["ms_step"]),
+                        "step_roofline_frac": xrt["t_step"] * 1e3 / ms_s,
+                        "t_roof_ms": xrt["t_step"] * 1e3},
+            "fwd": {"value": job_rate(world, x["tokens"], ms_f), "unit": "tokens/s",
+                    **summary(x["ms_fwd"]),
+                    "step_roofline_frac": xrt["t_fwd"] * 1e3 / ms_f,
+                    "t_roof_ms": xrt["t_fwd"] * 1e3},
+            "roofline": dominant_roofline(x["prof"], xp, x["e_in"], xrt, peaks_src),
+            "kernels": kernel_table(x["prof"], args.steps, xp, x["e_in"])}
+        del x
+        torch.cuda.empty_cache()
+
+    warm = {}
+    if not args.no_warmup_check and world == 1:
+        for name, heads in WARMUP_WORKLOADS.items():
+            warm[name] = warmup_report(torch, gdn, name, heads, timer, dev, args, l2)
+            torch.cuda.empty_cache()
+
     status = gdn.gdn_sync_status(stream.cuda_stream)
     if status != 0:
-        raise RuntimeError("device status after the timed region: " + gdn.gdn_last_error())
+        raise RuntimeError("device status after the timed regions: " + gdn.gdn_last_error())
 
-    ms_step, ms_fwd, ms_e2e, ms_gated, ms_dec = max_over_ranks(
-        [ms_step, ms_fwd, ms_e2e, ms_gated, ms_dec], dist, dev)
+    med_step = statistics.median(head["ms_step"])
+    med_fwd = statistics.median(head["ms_fwd"])
+    med_e2e = statistics.median(ms_e2e)
+    med_e2e_g = statistics.median(ms_e2e_graph)
+    med_step, med_fwd, med_e2e, med_e2e_g = max_over_ranks(
+        [med_step, med_fwd, med_e2e, med_e2e_g], dist, dev)
     if rank != 0:
         if dist:
             dist.destroy_process_group()
         return 0
 
-    value = job_rate(world, tokens, ms_step)
-    th = tokens * p.H
-    step_bytes = th * (bytes_per_token_head(p.K, p.V, e_in, "fwd") +
-                       bytes_per_token_head(p.K, p.V, e_in, "bwd"))
-    step_bytes += p.N * p.H * p.K * p.V * 4 * 5          # h0 (x2), hT, dhT, dh0
-    step_flops = th * (flops_per_token_head(p.K, p.V, "fwd") +
-                       flops_per_token_head(p.K, p.V, "bwd"))
-    hbm = peaks.get("hbm_gbs", 6800.0)
-    bf16 = peaks.get("bf16_tflops", 1900.0)
-    t_roof = max(step_bytes / (hbm * 1e9), step_flops / (bf16 * 1e12))
-    # the forward alone: inputs, O and the states (h0 in, final state out)
-    fwd_bytes = th * bytes_per_token_head(p.K, p.V, e_in, "fwd") + p.N * p.H * p.K * p.V * 4 * 2
-    fwd_flops = th * flops_per_token_head(p.K, p.V, "fwd")
-    t_roof_fwd = max(fwd_bytes / (hbm * 1e9), fwd_flops / (bf16 * 1e12))
-    total_launches = sum(s[1] for s in prof)
-    dom = max(prof, key=lambda s: s[2])
-    dom_name, dom_launches, dom_ms = dom
-    avg_s = dom_ms / dom_launches / 1e3
-    hbm_src = "measured" if "hbm_gbs" in peaks else "fallback"
-    by_th = kernel_bytes_per_token_head(dom_name, p.K, p.V, e_in, GRAD_BYTES)
-    if by_th is not None:
-        # the tensor-core kernels move more bytes than their few MMAs can hide: HBM roofline
-        roof = {"kernel": dom_name, "bound": "hbm", "unit": "GB/s",
-                "achieved": by_th * th / avg_s / 1e9, "peak": hbm,
-                "peak_source": f"{hbm_src} HBM copy bandwidth",
-                "bytes_per_launch": by_th * th,
-                "traffic": measured_traffic(dom_name, args.workload),
-                "avg_launch_ms": avg_s * 1e3, "launches_per_step": dom_launches / args.steps}
-    else:
-        per_th = kernel_flops_per_token_head(dom_name, p.K, p.V)
-        sm_max = (clk or {}).get("sm_max_mhz") or peaks.get("sm_max_mhz", 2070.0)
-        n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
-        alu_peak = n_sms * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
-        roof = {"kernel": dom_name, "bound": "alu", "unit": "TFLOP/s",
-                "achieved": None if per_th is None else per_th * th / avg_s / 1e12,
-                "peak": alu_peak, "peak_source": "fp32 FMA: SMs x 128 lanes x 2 x max SM clock",
-                "traffic": None, "avg_launch_ms": avg_s * 1e3,
-                "launches_per_step": dom_launches / args.steps}
-    roof["frac"] = None if roof["achieved"] is None else roof["achieved"] / roof["peak"]
-
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        dt, threads, th_s = oracle_sample(p, list(range(p.H)), reps_min_s=10.0)
-        cpu = {"value": th_s / p.H / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-               "sample": f"fp64 oracle fwd+bwd over all {p.H} heads of the {args.workload} "
-                         f"workload, repeated for >= 10 s"}
+        heads = reference_heads(p)
+        dt, threads, th_s = oracle_sample(p, heads, reps_min_s=10.0)
+        cpu = {"value": (th_s / p.H) / dt, "unit": "tokens/s", "cores": threads,
+               "host_cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"fp64 oracle fwd+bwd over head(s) {heads} of the {args.workload} "
+                         f"workload (all {p.N} sequences), repeated for >= 10 s; tokens/s "
+                         f"scaled to all {p.H} heads"}
 
-    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+    prof = head["prof"]
+    roof = dominant_roofline(prof, p, e_in, rt, peaks_src)
+    roof["launches_per_step"] = {n: l for n, l, _ in prof}[roof["kernel"]] / args.steps
+    launches_per_step = sum(s[1] for s in prof) / args.steps
+    line = {"metric": METRIC, "value": job_rate(world, tokens, med_step), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": med_step, "step_stats": summary(head["ms_step"]),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic (seeded; see gdn_synth.py)", "config": config_of(p, args.workload, True),
-            "fwd": {"value": job_rate(world, tokens, ms_fwd), "unit": "tokens/s",
-                    "ms_per_step": ms_fwd,
-                    "step_roofline": {"t_roof_ms": t_roof_fwd * 1e3,
-                                      "frac": t_roof_fwd * 1e3 / ms_fwd,
-                                      "bytes": fwd_bytes, "flops": fwd_flops}},
-            "decode": {"value": job_rate(world, dn, ms_dec), "unit": "tokens/s",
-                       "ms_per_step": ms_dec, "batch": f"{dn} sequences x {dh} heads",
-                       "hbm_gbs": dec_bytes / (ms_dec / 1e3) / 1e9,
-                       "frac_of_hbm": dec_bytes / (ms_dec / 1e3) / 1e9 / hbm,
-                       "what": "one gdn_recurrent_step: state read and written once"},
-            "gated": {"value": job_rate(world, tokens, ms_gated), "unit": "tokens/s",
-                      "ms_per_step": ms_gated,
-                      "what": "the same fwd+bwd step with the decay formed inside from gate "
-                              "logits (gate_scale), d(logits) and d(gate_scale) returned"},
-            "step_roofline": {"t_roof_ms": t_roof * 1e3, "frac": t_roof * 1e3 / ms_step,
-                              "bytes": step_bytes, "flops": step_flops,
-                              "peaks": {"hbm_gbs": hbm, "bf16_tflops": bf16,
-                                        "source": "measured" if peaks else "fallback"}},
+            "data": "synthetic (seeded; see gdn_synth.py)",
+            "config": config_of(p, args.workload, l2, True),
+            "fwd": {"value": job_rate(world, tokens, med_fwd), "unit": "tokens/s",
+                    "ms_per_step": med_fwd, "stats": summary(head["ms_fwd"]),
+                    "step_roofline": {"t_roof_ms": rt["t_fwd"] * 1e3,
+                                      "frac": rt["t_fwd"] * 1e3 / med_fwd,
+                                      "bytes": rt["fwd_bytes"], "flops": rt["fwd_flops"]},
+                    "kernels": kernel_table(head["prof_fwd"], args.steps, p, e_in)},
+            "sustained": head["sustained"],
+            "step_roofline": {"t_roof_ms": rt["t_step"] * 1e3,
+                              "frac": rt["t_step"] * 1e3 / med_step,
+                              "bytes": rt["step_bytes"], "flops": rt["step_flops"],
+                              "peaks": {"hbm_gbs": rt["hbm"], "bf16_tflops": rt["bf16"],
+                                        "source": peaks_src}},
             "roofline": roof,
-            "kernels": [kernel_entry(n, l, m, sum(s[2] for s in prof), p, th, e_in)
-                        for n, l, m in prof],
-            "gpu_launches": total_launches,
-            "e2e": {"value": job_rate(world, tokens, ms_e2e), "unit": "tokens/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "clocks": clk, "cpu_baseline": cpu}
+            "kernels": kernel_table(prof, args.steps, p, e_in),
+            "gpu_launches": int(round(launches_per_step * args.steps)),
+            "e2e": {"value": job_rate(world, tokens, med_e2e), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": med_e2e, "stats": summary(ms_e2e),
+                    "what": "eager public-API calls every step (fwd keeping its context, bwd), "
+                            "inputs from pinned host memory and every result back to it inside "
+                            "the timed region"},
+            "e2e_graph": {"value": job_rate(world, tokens, med_e2e_g), "unit": "tokens/s",
+                          "ms_per_step": med_e2e_g,
+                          "what": "the same end-to-end step captured once as a CUDA graph"},
+            "workloads": extra, "warmup_shortcut": warm,
+            "clocks": head["clocks"], "cpu_baseline": cpu}
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()

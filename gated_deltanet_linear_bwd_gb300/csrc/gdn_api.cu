@@ -203,7 +203,6 @@ static size_t layout(Plan &p, bool bwd, char *base) {
     const size_t th = (size_t)g.B * g.T * g.H;
     Ws &w = p.ws;
     w = Ws{};
-    w.counters = (int32_t *)take(64 * sizeof(int32_t));
     w.gam = (float *)take(th * sizeof(float));
     // CUDA cores keep fp32 token rows, tensor cores bf16 chunk tiles of 64 rows
     const size_t tiles = (size_t)p.max_chunks * g.H * 64 * 2;
@@ -233,7 +232,9 @@ static size_t layout(Plan &p, bool bwd, char *base) {
         w.scratch = (float *)take((size_t)p.scratch_ctas *
                                   simt::scratch_floats_per_cta(g.K, g.V) * sizeof(float));
     }
-    return off;
+    // never 0 for valid arguments (an empty problem included): the size
+    // queries return 0 only for invalid ones
+    return std::max(off, kAlign);
 }
 
 // Upper bound on segments under CP for any segment length: every segment
@@ -546,6 +547,13 @@ static std::mutex g_static_mu;
 
 extern "C" gdn_status gdn_chunk_fwd_static(const gdn_fwd_args *a, void *stream) {
     if (!a) return fail(GDN_ERR_INVALID_ARG, "null args");
+    // the same host-side checks, in the same order, as gdn_chunk_fwd's, so that
+    // both entry points return the same status for the same bad arguments
+    gdn_status st = validate(common_of(a));
+    if (st != GDN_OK) return st;
+    DeviceInfo *dev_info = nullptr;
+    st = device_info(&dev_info);          // sm_103a check before any symbol lookup
+    if (st != GDN_OK) return st;
     const size_t need = gdn_fwd_workspace_size(a);
     if (need == 0) return GDN_ERR_INVALID_ARG;     // gdn_last_error already says why
     if (need > GDN_STATIC_SCRATCH_BYTES)
@@ -556,7 +564,6 @@ extern "C" gdn_status gdn_chunk_fwd_static(const gdn_fwd_args *a, void *stream) 
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    if (dev < 0 || dev >= 64) return fail(GDN_ERR_UNSUPPORTED, "device index %d out of range", dev);
     void *scratch = nullptr;
     {
         std::lock_guard<std::mutex> lock(g_static_mu);

@@ -30,7 +30,6 @@ struct Ws {
     void *yt = nullptr;            // [chunk][H][V][64] bf16 (dO^T P) tiles (bwd, tensor cores)
     void *tmat = nullptr;          // [chunks, H, 64, 64] bf16 T = (I + A)^-1 by column (bwd, tensor cores)
     float *scratch = nullptr;      // per-CTA scratch (bwd, CUDA-core path)
-    int32_t *counters = nullptr;   // small zeroed counters
 };
 
 struct Plan {
@@ -115,7 +114,7 @@ cudaError_t recompute_states(const Plan &p, cudaStream_t s);
 cudaError_t output(const Plan &p, cudaStream_t s);
 // have_ctx: gam, W, u, T and the chunk start states are already in p.ws.
 cudaError_t backward(const Plan &p, cudaStream_t s, bool have_ctx);
-// Chunk-local gradients on tensor cores (no q/k L2 normalisation).
+// Chunk-local gradients on tensor cores (q, k normalised inside or not).
 cudaError_t local_grads(const Plan &p, cudaStream_t s);
 // TMA descriptors of [tokens, H, 128] bf16 tensors (64 x 1 x 64 boxes, 128B swizzle).
 cudaError_t encoder();

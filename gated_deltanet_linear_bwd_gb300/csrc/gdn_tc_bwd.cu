@@ -51,7 +51,8 @@ struct IntraSmem {
     uint8_t qs[2 * kTile];         // Qs, [dk half][64 rows][128 B]
     uint8_t yT[2 * kTile];         // Y^T, [128 rows v][64 chunk rows]
     uint8_t p[kTile];              // P rows r (scale included)
-    float gam[64], rq[64], rk[64];
+    float gam[64];
+    float rqk[128];            // q, k normalised here: 1 / |q_r| at r, 1 / |k_r| at 64 + r
     float gpre[64];            // the next item's gam, fetched during the current one
     float eg[64];              // e^(gam_j - gam_{j-1})
     uint64_t load_bar[2], mma_bar; // loads: {q, k}, {dO}
@@ -163,25 +164,15 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             }
             mma_commit(&s.mma_bar);
         }
-        if (g.l2norm && tid < 128) {
-            // 1 / |q_r| from the Q rows (threads 0-63), 1 / |k_r| from the K rows (64-127)
-            const int r = tid & 63;
-            const uint8_t *base = s.qk + (tid >= 64 ? kTile : 0);
-            float ss = 0.f;
-#pragma unroll
-            for (int half = 0; half < 2; ++half)
-#pragma unroll 8
-                for (int col = 0; col < 64; ++col) {
-                    const float x = ld_bf16(base + half * 2 * kTile, r, col);
-                    ss += x * x;
-                }
-            (tid >= 64 ? s.rk : s.rq)[r] = rsqrtf(ss + 1e-6f);
+        if (g.l2norm) {
+            // 1 / |q_r| (stacked rows 0-63) and 1 / |k_r| (rows 64-127)
+            row_inv_norms(s.qk, 2 * kTile, 128, s.rqk);
+            __syncthreads();
         }
-        if (g.l2norm) __syncthreads();
         if (tid >= 128 && tid < 192) {
             // row r of Qs = diag(scale e^gam (x 1/|q_r|)) Q, both dk halves
             const int r = tid - 128;
-            const float f = r < L ? g.scale * __expf(s.gam[r]) * (g.l2norm ? s.rq[r] : 1.f) : 0.f;
+            const float f = r < L ? g.scale * __expf(s.gam[r]) * (g.l2norm ? s.rqk[r] : 1.f) : 0.f;
 #pragma unroll 1
             for (int q = 0; q < 16; ++q) {
                 const int half = q >> 3, chunk = q & 7;
@@ -200,7 +191,7 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         if (v < 64) {
             // P row r = v, columns c0 .. c0+31, scale included
             const int r = v;
-            const float sr = g.l2norm ? s.rq[r] : 1.f;
+            const float sr = g.l2norm ? s.rqk[r] : 1.f;
             float xs[32], dd[32];
             tmem_ld32(tmem_addr(t_p, warp, c0), xs);
             row_decays32(s.gam, s.eg, r, c0, dd);
@@ -211,7 +202,7 @@ tc_bwd_intra_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 for (int e = 0; e < 8; ++e) {
                     const int c = c0 + 8 * q + e;
                     x[e] = (c <= r && r < L) ? g.scale * x[e] * dd[8 * q + e] * sr *
-                                                   (g.l2norm ? s.rk[c] : 1.f)
+                                                   (g.l2norm ? s.rqk[64 + c] : 1.f)
                                              : 0.f;
                 }
                 st_row8(s.p, r, cq + q, x);
@@ -303,7 +294,8 @@ struct DWalkSmem {
     uint8_t duT[2 * kTile];        // dU^T: [128 rows v][64 chunk rows]    K-major A
     float gam[2][64];
     alignas(16) float fr[64];      // exp(gam_L - gam_r) (x 1/|k_r|), 0 past L
-    float rk[64];
+    float rqk[128];                // q, k normalised here: 1 / |q_r| at r (fused walk),
+                                   // 1 / |k_r| at 64 + r
     float egd[64];                 // exp(gam_j - gam_{j-1}) of the current chunk (fused)
     uint64_t tma_bar[2], bar_x, bar_z, bar_q, bar_y;
     uint32_t tmem_base;
@@ -489,22 +481,18 @@ tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
             tma_store_2d(&m.dhc, s.dhT + 2 * kTile, 0, 2 * trow + kD);
             bulk_commit();
         }
-        if (g.l2norm && tid >= 64 && tid < 128) {
-            const int r = tid - 64;
-            float ss = 0.f;
-#pragma unroll
-            for (int half = 0; half < 2; ++half)
-#pragma unroll 8
-                for (int col = 0; col < 64; ++col) {
-                    const float x = ld_bf16(s.k[st] + kKOff + half * kKHalf, r, col);
-                    ss += x * x;
-                }
-            s.rk[r] = rsqrtf(ss + 1e-6f);
+        if (g.l2norm) {
+            // 1 / |k_r| (and, in the fused walk, whose stage stacks Q rows 0-63
+            // over K rows 64-127, 1 / |q_r|) from the stage's rows
+            if (fused)
+                row_inv_norms(s.k[st], kKHalf, 128, s.rqk);
+            else
+                row_inv_norms(s.k[st] + kKOff, kKHalf, 64, s.rqk + 64);
+            __syncthreads();
         }
-        if (g.l2norm) __syncthreads();
         if (tid < 64) {
             const float gl = s.gam[st][L - 1];
-            s.fr[tid] = tid < L ? __expf(gl - s.gam[st][tid]) * (g.l2norm ? s.rk[tid] : 1.f) : 0.f;
+            s.fr[tid] = tid < L ? __expf(gl - s.gam[st][tid]) * (g.l2norm ? s.rqk[64 + tid] : 1.f) : 0.f;
             if (fused) s.egd[tid] = tid > 0 ? __expf(s.gam[st][tid] - s.gam[st][tid - 1]) : 1.f;
         }
         if (fused) {
@@ -512,7 +500,8 @@ tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
             // thread t scales four 16-byte pieces of row t % 64
             {
                 const int r = tid & 63;
-                const float f = r < L ? g.scale * __expf(s.gam[st][r]) : 0.f;
+                const float f = r < L ? g.scale * __expf(s.gam[st][r]) * (g.l2norm ? s.rqk[r] : 1.f)
+                                      : 0.f;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int pc = 4 * (tid >> 6) + i, half = pc >> 3, chunk = pc & 7;
@@ -531,17 +520,20 @@ tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
             tc_fence_after();
             if (v < 64) {
                 // P row r = v, columns 32 hs .. +31: scale Q K^T D, masked to c <= r < L
+                // (and 1 / (|q_r| |k_c|) when q, k are normalised here)
                 const int r = v;
                 float xp[32], dd[32];
                 tmem_ld32(tmem_addr(t_p, warp, 32 * hs), xp);
                 row_decays32(s.gam[st], s.egd, r, 32 * hs, dd);
+                const float sr = g.scale * (g.l2norm ? s.rqk[r] : 1.f);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     float *x = xp + 8 * q;
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const int c = 32 * hs + 8 * q + e;
-                        x[e] = (c <= r && r < L) ? g.scale * x[e] * dd[8 * q + e] : 0.f;
+                        const float sc = g.l2norm ? sr * s.rqk[64 + c] : sr;
+                        x[e] = (c <= r && r < L) ? sc * x[e] * dd[8 * q + e] : 0.f;
                     }
                     st_row8(s.p, r, 4 * hs + q, x);
                 }
@@ -684,11 +676,10 @@ cudaError_t backward(const Plan &p, cudaStream_t s, bool have_ctx) {
     if ((e = make_map_tiles(&m.du, p.ws.du, tile_rows)) != cudaSuccess) return e;
 
     // Without CP, when the reverse walk's CTAs fill at least three quarters of
-    // the SMs (q, k not L2-normalised inside), the walk forms P, Qs and Y^T
-    // itself and the chunk-parallel intra kernel is skipped: its work then
-    // costs the walk less than the separate pass (the rule of the forward's
-    // fused output walk).
-    const bool fuse_intra = !p.cp && !g.l2norm && 4 * g.N * g.H >= 3 * std::max(p.sms, 1);
+    // the SMs, the walk forms P, Qs and Y^T itself and the chunk-parallel intra
+    // kernel is skipped: its work then costs the walk less than the separate
+    // pass (the rule of the forward's fused output walk).
+    const bool fuse_intra = !p.cp && 4 * g.N * g.H >= 3 * std::max(p.sms, 1);
     if (!fuse_intra) {
         const size_t ismem = sizeof(IntraSmem) + 1024;
         if ((e = set_smem(tc_bwd_intra_kernel, ismem)) != cudaSuccess) return e;
@@ -742,7 +733,7 @@ cudaError_t backward(const Plan &p, cudaStream_t s, bool have_ctx) {
         prof_after(s);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    return g.l2norm ? simt::local_grads(p, s, true) : local_grads(p, s);
+    return local_grads(p, s);
 }
 
 }  // namespace tc

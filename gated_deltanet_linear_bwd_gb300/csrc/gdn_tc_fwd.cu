@@ -373,7 +373,8 @@ struct WalkSmem {
     alignas(16) float fr[64];      // exp(gam_L - gam_r) (x 1/|k_r|); 0 past L
     alignas(16) float er[2][64];   // exp(gam_r) per chunk parity (output walk); 0 past L
     float egw[2][64];              // exp(gam_j - gam_{j-1}) per chunk parity (output walk)
-    float rk[64];
+    float rqk[128];                // q, k normalised here: 1 / |q_r| at r (output walk),
+                                   // 1 / |k_r| at 64 + r
     uint64_t tma_bar[kStages], bar_u, bar_q, bar_dh;
     uint32_t tmem_base;
 };
@@ -605,25 +606,20 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             tc_fence_after();
             out_epilogue(gb ^ 1);                 // the previous chunk's O
         }
-        if (g.l2norm && tid >= 64 && tid < 128) {
-            // 1 / |k_r| from the K rows
-            const int r = tid - 64;
-            float ss = 0.f;
-#pragma unroll
-            for (int half = 0; half < 2; ++half)
-#pragma unroll 8
-                for (int col = 0; col < 64; ++col) {
-                    const float x = ld_bf16(s.k[st] + kKOff + half * kKHalf, r, col);
-                    ss += x * x;
-                }
-            s.rk[r] = rsqrtf(ss + 1e-6f);
+        if (g.l2norm) {
+            // 1 / |k_r| (and, in the output walk, whose stage stacks Q rows 0-63
+            // over K rows 64-127, 1 / |q_r|) from the stage's rows
+            if (fused)
+                row_inv_norms(s.k[st], kKHalf, 128, s.rqk);
+            else
+                row_inv_norms(s.k[st] + kKOff, kKHalf, 64, s.rqk + 64);
+            __syncthreads();
         }
-        if (g.l2norm) __syncthreads();
         if (tid < 64) {
             const float gl = s.gam[gb][L - 1], gr = s.gam[gb][tid];
-            s.fr[tid] = tid < L ? __expf(gl - gr) * (g.l2norm ? s.rk[tid] : 1.f) : 0.f;
+            s.fr[tid] = tid < L ? __expf(gl - gr) * (g.l2norm ? s.rqk[64 + tid] : 1.f) : 0.f;
             if (fused) {
-                s.er[gb][tid] = tid < L ? __expf(gr) : 0.f;
+                s.er[gb][tid] = tid < L ? __expf(gr) * (g.l2norm ? s.rqk[tid] : 1.f) : 0.f;
                 s.egw[gb][tid] = tid > 0 ? __expf(gr - s.gam[gb][tid - 1]) : 1.f;
             }
         }
@@ -663,17 +659,20 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         if (fused && v < 64) {
             // row r = v of P: Q K^T on lanes 0-63, masked to c <= r < L, times D_rc
+            // (and 1 / (|q_r| |k_c|) when q, k are normalised here)
             const int r = v;
             float xp[32], dd[32];
             tmem_ld32(tmem_addr(t_p, warp, 32 * hs), xp);
             row_decays32(s.gam[gb], s.egw[gb], r, 32 * hs, dd);
+            const float sr = g.l2norm ? s.rqk[r] : 1.f;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 float *x = xp + 8 * q;
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int c = 32 * hs + 8 * q + e;
-                    x[e] = (c <= r && r < L) ? x[e] * dd[8 * q + e] : 0.f;
+                    const float sc = g.l2norm ? sr * s.rqk[64 + c] : 1.f;
+                    x[e] = (c <= r && r < L) ? x[e] * dd[8 * q + e] * sc : 0.f;
                 }
                 st_row8(s.p, r, 4 * hs + q, x);
             }
@@ -859,13 +858,13 @@ static cudaError_t run_forward(const Plan &p, cudaStream_t s, bool states_only, 
     a.h0 = p.h0;
     a.final_state = states_only ? nullptr : p.final_state;
     a.hc = (__nv_bfloat16 *)p.ws.hc;
-    // The walk forms O itself (q, k not L2-normalised inside the library) when
-    // its CTAs fill at least three quarters of the SMs: each chunk then costs
-    // the walk about 4.3K more cycles, against about 6.6K SM-cycles of the
-    // chunk-parallel output pass (GB300 measurements on the four workloads;
-    // with fewer walk CTAs the output pass, spread over every SM, is cheaper).
+    // The walk forms O itself when its CTAs fill at least three quarters of the
+    // SMs: each chunk then costs the walk about 4.3K more cycles, against about
+    // 6.6K SM-cycles of the chunk-parallel output pass (GB300 measurements on
+    // the four workloads; with fewer walk CTAs the output pass, spread over
+    // every SM, is cheaper).
     const int walk_ctas = (p.cp ? p.max_segs : g.N) * g.H;
-    const bool fuse_out = !states_only && !g.l2norm && 4 * walk_ctas >= 3 * std::max(p.sms, 1);
+    const bool fuse_out = !states_only && 4 * walk_ctas >= 3 * std::max(p.sms, 1);
     a.o = fuse_out ? (__nv_bfloat16 *)p.o : nullptr;
     auto walk_kernel = fuse_out ? tc_walk_kernel<kWalkFused> : tc_walk_kernel<kWalkOut>;
     const char *out_name = states_only ? "tc_walk_states" : fuse_out ? "tc_walk_fused" : "tc_walk";

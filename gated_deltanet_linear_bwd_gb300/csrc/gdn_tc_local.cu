@@ -1,5 +1,9 @@
 // gdn_tc_local.cu -- tensor-core chunk-local gradients for bf16 q/k/v with
-// K = V = 128 (no q/k L2 normalisation), one (chunk, head) per CTA.
+// K = V = 128, one (chunk, head) per CTA.  With q, k L2-normalised inside the
+// library, the q and k tiles are normalised in shared memory when they land,
+// every formula below is taken with q^, k^, and the norm's chain rule
+//   dq = (dq^ - q^ <q^, dq^>) / |q|  (per row; likewise dk)
+// finishes dq and dk inside the last products and epilogue.
 //
 // Inputs per chunk, all by TMA: q, k, v, dO and the workspace's bf16 chunk
 // tiles of dU^T, W^T, u^T, T, the chunk start state H0^T and the gradient at
@@ -53,22 +57,28 @@ struct LocalSmem {
     uint8_t ut[2 * kTile];     // u^T: [128 rows v][64 chunk rows]
     uint8_t h0T[4 * kTile];    // H0^T: [k half][128 rows v][64]; after wave 1: U^T, dW^T
     uint8_t dl[4 * kTile];     // dHL^T: [k half][128 rows v][64]; after wave 2: dYu^T, dYw^T
-    uint8_t tt[kTile];         // row r = column r of T
+    uint8_t tt[kTile];         // row r = column r of T; q, k normalised here: after wave 2,
+                               // diag(-<q^_r, dq^_r>) (the norm's chain rule for dq, wave 3)
     uint8_t ds[kTile];         // dS rows r
     uint8_t gs[kTile];         // G rows r
     float gam[64], bet[64], ee[64], ff[64];
-    float red[8][32], red2[8][32], red3[8][32], red4[8][32], red5[8][32];
-    float zrow[2][64], zprow[2][64], dbA[2][64];
+    float red[16][16], red2[16][16], red3[16][16], red4[16][16], red5[16][16];
+    float zrow[4][64], zprow[4][64], dbA[4][64];   // per column group
+    float scan[4][32];         // dg's reverse cumsum
     float zcol[64], rowA[64], yw[64], yu[64], zpp[64];
-    float hdot[16];            // [0..3]: per-warp parts of <dHL, H0>; [8..15]: block_sum scratch
-    uint64_t load_bar[3], mma_bar;  // load groups: {v, dO, dU^T, H0^T, T}, {W^T, u^T, dHL^T}, {q, k}
+    float hdot[4];             // per-warp parts of <dHL, H0>
+    float bsum[16];            // block_sum scratch
+    float rq[64], rk[64];      // 1 / |q_r|, 1 / |k_r| (q, k normalised here)
+    uint64_t load_bar[3], mma_bar;  // load groups: {v, dO, dU^T, H0^T (, T)}, {W^T, u^T, dHL^T},
+                                    // {q, k (, T when q, k are normalised here)}
     uint32_t tmem_base;
 };
 
-// Sums over the 256 threads of per-column values, for epilogues that walk 8
-// columns at a time: thread t holds 8 values of columns 32 * (t / 128) + 8q
-// .. +7.  warp_sum8 adds them over the warp's lanes into red[warp][8q .. +7];
-// red_combine then adds the four warps of each column half into dst[0..63].
+// Sums over the 512 threads of per-column values, for epilogues that walk 8
+// columns at a time: thread t holds 8 values of columns 16 * (t / 128) + 8q
+// .. +7 (q = 0, 1).  warp_sum8 adds them over the warp's lanes into
+// red[warp][8q .. +7]; quad_sum / red_combine then add the four warps of each
+// column group (warps 4 g .. 4 g + 3 cover the 128 TMEM lanes) into dst[0..63].
 __device__ __forceinline__ void warp_sum8(float (&x)[8], float *red_row) {
     const int lane = threadIdx.x & 31;
     bool up = (lane & 16) != 0;
@@ -94,12 +104,12 @@ __device__ __forceinline__ void warp_sum8(float (&x)[8], float *red_row) {
         red_row[((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1)] = x[0];
 }
 
-__device__ __forceinline__ float quad_sum(float (&red)[8][32], int i) {
-    const int w0 = 4 * (i >> 5), l = i & 31;
+__device__ __forceinline__ float quad_sum(float (&red)[16][16], int i) {
+    const int w0 = 4 * (i >> 4), l = i & 15;
     return red[w0][l] + red[w0 + 1][l] + red[w0 + 2][l] + red[w0 + 3][l];
 }
 
-__device__ __forceinline__ void red_combine(float *dst, float (&red)[8][32], bool accumulate) {
+__device__ __forceinline__ void red_combine(float *dst, float (&red)[16][16], bool accumulate) {
     __syncthreads();
     if (threadIdx.x < 64) {
         const float sum = quad_sum(red, threadIdx.x);
@@ -108,13 +118,13 @@ __device__ __forceinline__ void red_combine(float *dst, float (&red)[8][32], boo
     __syncthreads();
 }
 
-__device__ __forceinline__ float block_sum(float x, float *scratch8) {
+__device__ __forceinline__ float block_sum(float x, float *scratch16) {
     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    if ((threadIdx.x & 31) == 0) scratch8[threadIdx.x >> 5] = x;
+    if ((threadIdx.x & 31) == 0) scratch16[threadIdx.x >> 5] = x;
     __syncthreads();
     float s = 0.f;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) s += scratch8[w];
+    for (int w = 0; w < 16; ++w) s += scratch16[w];
     __syncthreads();
     return s;
 }
@@ -126,6 +136,43 @@ __device__ __forceinline__ void ld_row8(const uint8_t *tile, int row, int chunk,
     const __nv_bfloat16 *b = reinterpret_cast<const __nv_bfloat16 *>(&raw);
 #pragma unroll
     for (int e = 0; e < 8; ++e) x[e] = __bfloat162float(b[e]);
+}
+
+// q and k normalised in place (the library's use_qk_l2norm): row r of the
+// stacked [Q; K] tile of each dk half is scaled by (|x_r|^2 + 1e-6)^-1/2, the
+// two halves' sums of squares joined by a shuffle.  Thread t takes row t / 2,
+// dk half t % 2; it visits its row's 16-byte pieces starting at piece
+// r + 4 (t % 2), so that the 8 threads of each shared-memory phase hit 8
+// different bank groups.  Every element of a row gets the same factor, so the
+// 128-byte swizzle plays no part.  Writes 1 / |q_r| to rq, 1 / |k_r| to rk.
+__device__ __forceinline__ void normalise_qk_rows(uint8_t *qk, float *rq, float *rk) {
+    const int t = threadIdx.x, r = t >> 1, hh = t & 1;
+    uint4 *row = reinterpret_cast<uint4 *>(qk + hh * 2 * kTile + r * 128);
+    uint4 x[8];
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        x[i] = row[(i + r + 4 * hh) & 7];
+        const __nv_bfloat162 *b = reinterpret_cast<const __nv_bfloat162 *>(&x[i]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 f = __bfloat1622float2(b[j]);
+            ss += f.x * f.x + f.y * f.y;
+        }
+    }
+    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+    const float inv = rsqrtf(ss + 1e-6f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        __nv_bfloat162 *b = reinterpret_cast<__nv_bfloat162 *>(&x[i]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 f = __bfloat1622float2(b[j]);
+            b[j] = __floats2bfloat162_rn(f.x * inv, f.y * inv);
+        }
+        row[(i + r + 4 * hh) & 7] = x[i];
+    }
+    if (hh == 0) (r < 64 ? rq : rk)[r & 63] = inv;
 }
 
 struct TcLocalArgs {
@@ -151,22 +198,23 @@ cudaError_t set_smem(F kernel, size_t bytes) {
 // fills are dead: {v, dO, dU^T, H0^T, T} after the second epilogue, {W^T, u^T,
 // dHL^T} after the dA product, {q, k} after the last product.
 //
-// 256 threads.  Feature-major results: thread t reads TMEM lane v = t % 128
-// (feature v) and the chunk-row half hs = t / 128 (columns c0 = 32 hs ..
-// +31).  Row-major 64 x 64 results sit on lanes 0-63 (warps 0, 1, 4, 5: row
-// r = v); lanes 64-127 of the [Q; K] K^T product hold K K^T and those of the
-// dA product a second copy of dA (warps 2, 3, 6, 7: row r = v - 64).
+// 512 threads.  Feature-major results: thread t reads TMEM lane v = t % 128
+// (feature v) and the column group cg = t / 128 (chunk columns c0 = 16 cg ..
+// +15), so every epilogue is split four ways.  Row-major 64 x 64 results sit
+// on lanes 0-63 (warps with warp % 4 < 2: row r = v); lanes 64-127 of the
+// [Q; K] K^T product hold K K^T and those of the dA product a second copy of
+// dA (warps with warp % 4 >= 2: row r = v - 64).
 template <typename TG>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(512, 1)
 tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
     pdl_enter();
     extern __shared__ uint8_t smem_raw[];
     LocalSmem &s = *reinterpret_cast<LocalSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, H = g.H;
-    const int v = tid & 127, hs = tid >> 7, c0 = 32 * hs, cq = c0 >> 3;
+    const int v = tid & 127, cg = tid >> 7, c0 = 16 * cg, cq = c0 >> 3;
     const float scale = g.scale;
-    const bool tma_thread = tid == 255;
+    const bool tma_thread = tid == 511;
     uint8_t *uT = s.h0T, *dwT = s.h0T + 2 * kTile;    // after wave 1
     uint8_t *dyuT = s.dl, *dywT = s.dl + 2 * kTile;   // after wave 2
 
@@ -181,8 +229,11 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
         const int tok0 = (int)bos;
         const int trow = (int)(((long long)ci * H + hh) * kD);
         uint64_t *bar = &s.load_bar[grp];
+        // T travels with group 0, or with group 2 when q, k are normalised here (its
+        // region then holds a diagonal tile until wave 3 is done)
+        const bool t_late = g.l2norm != 0;
         if (grp == 0) {
-            mbar_arrive_expect_tx(bar, 11 * kTile);
+            mbar_arrive_expect_tx(bar, (t_late ? 10 : 11) * kTile);
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 tma_load_3d(s.v + half * kTile, &m.v, bar, half * 64, hh, tok0);
@@ -190,7 +241,7 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
                 tma_load_2d(s.h0T + half * 2 * kTile, &m.hc, bar, 0, 2 * trow + half * kD);
             }
             tma_load_2d(s.du, &m.du, bar, 0, trow);
-            tma_load_2d(s.tt, &m.t, bar, 0, trow / 2);
+            if (!t_late) tma_load_2d(s.tt, &m.t, bar, 0, trow / 2);
         } else if (grp == 1) {
             mbar_arrive_expect_tx(bar, 8 * kTile);
             tma_load_2d(s.w, &m.w, bar, 0, trow);
@@ -198,12 +249,13 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
             tma_load_2d(s.dl, &m.dhc, bar, 0, 2 * trow);
             tma_load_2d(s.dl + 2 * kTile, &m.dhc, bar, 0, 2 * trow + kD);
         } else {
-            mbar_arrive_expect_tx(bar, 4 * kTile);
+            mbar_arrive_expect_tx(bar, (t_late ? 5 : 4) * kTile);
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 tma_load_3d(s.qk + half * 2 * kTile, &m.q, bar, half * 64, hh, tok0);
                 tma_load_3d(s.qk + half * 2 * kTile + kTile, &m.k, bar, half * 64, hh, tok0);
             }
+            if (t_late) tma_load_2d(s.tt, &m.t, bar, 0, trow / 2);
         }
     };
 
@@ -264,6 +316,14 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
                 ok = mbar_wait(&s.load_bar[grp], it & 1, g.spin_limit, g.status) && ok;
             if (__syncthreads_or(!ok)) { bailed = true; break; }
         }
+        if (g.l2norm) {
+            // every product and epilogue below then sees q^ = q / |q| and k^ = k / |k|,
+            // giving the gradients with respect to q^ and k^; the norm's own chain
+            // rule is applied to dq and dk at the end
+            if (tid < 256) normalise_qk_rows(s.qk, s.rq, s.rk);
+            fence_proxy_async();
+            __syncthreads();
+        }
         bool ok;
 
         // ---------------- wave 1: W H0, [Q; K] K^T, H0^T Q^T, H0 dU^T, H0 dO^T, dHL^T H0
@@ -296,7 +356,7 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
             // U^T and dW^T = -(H0 dU^T) rows v into the dead H0^T tile; partial sums
             // of dO[r][v] (Q H0)[r][v] over v for rowA
 #pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < 2; ++q) {
                 float x[8], y[8], uu[8];
                 float dw[8];
                 tmem_ld8x3(tmem_addr(t_u, warp, c0 + 8 * q), tmem_addr(t_qh, warp, c0 + 8 * q),
@@ -314,7 +374,7 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
                 for (int e = 0; e < 8; ++e) dw[e] = (c0 + 8 * q + e) < L ? -dw[e] : 0.f;
                 st_row8(dwT, v, cq + q, dw);
             }
-            if (hs == 0) {
+            if (cg == 0) {
                 // lane v's diagonal entry of dHL^T H0 sits in column v of t_hd
                 float x[32];
                 tmem_ld32(tmem_addr(t_hd, warp, 32 * warp), x);
@@ -361,7 +421,7 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
             // dV = diag(beta) dYu leaves now; a warp's lanes write 32 consecutive features
             TG *dv = (TG *)a.dv + (bos * H + h) * (long long)kD + v;
 #pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < 2; ++q) {
                 float yw[8], yu[8], pz[8];
                 tmem_ld8x3(tmem_addr(t_yw, warp, c0 + 8 * q), tmem_addr(t_yu, warp, c0 + 8 * q),
                            tmem_addr(t_dkh, warp, c0 + 8 * q), yw, yu, pz);
@@ -425,7 +485,7 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
             const float gr = s.gam[r];
             float zr = 0.f;
 #pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < 2; ++q) {
                 float dp[8], qk[8], zc[8];
                 tmem_ld8x2(tmem_addr(t_dp, warp, c0 + 8 * q), tmem_addr(t_p, warp, c0 + 8 * q),
                            dp, qk);
@@ -442,12 +502,12 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
                 st_row8(s.ds, r, cq + q, dp);
                 warp_sum8(zc, s.red[warp] + 8 * q);
             }
-            s.zrow[hs][r] = zr;
-            s.red5[warp][lane] = 0.f;
+            s.zrow[cg][r] = zr;
+            if (lane < 16) s.red5[warp][lane] = 0.f;
         } else {
             // rows r = v - 64: G = dA .* D .* beta_r, z' = G .* K K^T and the dA part
             // of dbeta
-            s.red[warp][lane] = 0.f;
+            if (lane < 16) s.red[warp][lane] = 0.f;
             ok = mbar_wait(&s.mma_bar, 0, g.spin_limit, g.status);
             if (ok) {
                 tc_fence_after();
@@ -455,7 +515,7 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
                 const float gr = s.gam[r], br = s.bet[r];
                 float zpr = 0.f, dba = 0.f;
 #pragma unroll 1
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < 2; ++q) {
                     float da[8], kk[8], zc[8];
                     tmem_ld8x2(tmem_addr(t_da, warp, c0 + 8 * q), tmem_addr(t_p, warp, c0 + 8 * q),
                                da, kk);
@@ -475,8 +535,8 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
                     st_row8(s.gs, r, cq + q, da);
                     warp_sum8(zc, s.red5[warp] + 8 * q);
                 }
-                s.zprow[hs][r] = zpr;
-                s.dbA[hs][r] = dba;
+                s.zprow[cg][r] = zpr;
+                s.dbA[cg][r] = dba;
             }
         }
         tc_fence_before();
@@ -492,6 +552,34 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
             ++issued[1];
         }
         if (tid < 64) s.zcol[tid] = quad_sum(s.red, tid) + quad_sum(s.red5, tid);
+        if (g.l2norm) {
+            // The norm's chain rule, dx = (dx^ - x^ <x^, dx^>) / |x| per row, joins
+            // wave 3.  The row dots are sums already formed above for dgam:
+            //   <q^_r, dq^_r> = rows of dS .* Q K^T + scale e_r <dO_r, (Q H0)_r>
+            //   <k^_r, dk^_r> = columns of dS .* Q K^T + rows and columns of G .* K K^T
+            //                   + f_r <(U dHL^T)_r, k^_r> + beta_r e_r <dYw_r, k^_r>.
+            // -<q^, dq^> q^ comes from one more product, Q^T diag(-<q^, dq^>), onto
+            // dS K (the diagonal in the dead T tile); -<k^, dk^> k^ from G's diagonal
+            // (zero so far), set to -<k^, dk^> / 2, which G K and G^T K each pass on.
+            if (tid < 64) {
+                const int r = tid;
+                const float zr = s.zrow[0][r] + s.zrow[1][r] + s.zrow[2][r] + s.zrow[3][r];
+                const float zp = s.zprow[0][r] + s.zprow[1][r] + s.zprow[2][r] + s.zprow[3][r];
+                const float dq_dot = zr + scale * s.ee[r] * s.rowA[r];
+                const float dk_dot = -s.zcol[r] + s.zpp[r] + s.bet[r] * s.ee[r] * s.yw[r] + zp;
+#pragma unroll 1
+                for (int chunk = 0; chunk < 8; ++chunk) {
+                    float x[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) x[e] = (8 * chunk + e == r) ? -dq_dot : 0.f;
+                    st_row8(s.tt, r, chunk, x);
+                }
+                *reinterpret_cast<__nv_bfloat16 *>(s.gs + sw128_off(r, r)) =
+                    __float2bfloat16_rn(-0.5f * dk_dot);
+            }
+            fence_proxy_async();
+            __syncthreads();
+        }
 
         // ---------------- wave 3: dS K, dS^T Q + (G + G^T) K
         ++mma_n;
@@ -507,11 +595,18 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
                 mma_bf16(t_dk, aK, desc_sw128(gs + kk * 32, 16, 1024), kMK, 1);         // G K
                 mma_bf16(t_dk, aK, desc_sw128(gs + kk * 2048, kTile, 1024), kMM, 1);    // G^T K
             }
+            if (g.l2norm) {
+                const uint32_t dq = smem_u32(s.tt);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)      // Q^T diag(-<q^, dq^>)
+                    mma_bf16(t_q2, desc_sw128(qk + kk * 2048, 2 * kTile, 1024),
+                             desc_sw128(dq + kk * 2048, kTile, 1024), kMM, 1);
+            }
             mma_commit(&s.mma_bar);
         }
         ok = mbar_wait(&s.mma_bar, 1, g.spin_limit, g.status);
         if (__syncthreads_or(!ok)) { bailed = true; break; }
-        // q, k are dead (their last reader was wave 3): next item's group 2
+        // q, k (and the T region) are dead (their last reader was wave 3): next item's group 2
         if (have_next) {
             if (tma_thread) {
                 fence_proxy_async();
@@ -532,7 +627,7 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
             TG *dq = (TG *)a.dq + (bos * H + h) * (long long)kD + v;
             TG *dk = (TG *)a.dk + (bos * H + h) * (long long)kD + v;
 #pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < 2; ++q) {
                 float x[8], y[8], pw[8], x1[8], y1[8];
                 tmem_ld8x5(tmem_addr(t_q1, warp, c0 + 8 * q), tmem_addr(t_q2, warp, c0 + 8 * q),
                            tmem_addr(t_dk, warp, c0 + 8 * q), tmem_addr(t_dkh, warp, c0 + 8 * q),
@@ -540,45 +635,50 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int c = c0 + 8 * q + e;
-                    x1[e] = scale * s.ee[c] * x1[e] + y1[e];
-                    x[e] = x[e] + s.ff[c] * y[e] + s.bet[c] * s.ee[c] * pw[e];
+                    // with q, k normalised here the products above already hold
+                    // dx^ - x^ <x^, dx^>; what is left of the norm's chain rule is 1 / |x|
+                    const float sq = g.l2norm ? s.rq[c] : 1.f, sk = g.l2norm ? s.rk[c] : 1.f;
+                    x1[e] = sq * (scale * s.ee[c] * x1[e] + y1[e]);
+                    x[e] = sk * (x[e] + s.ff[c] * y[e] + s.bet[c] * s.ee[c] * pw[e]);
                 }
                 store_rows8(dq, rs, x1, c0 + 8 * q, L);
                 store_rows8(dk, rs, x, c0 + 8 * q, L);
             }
         }
         {
-            const float zsum = block_sum(tid < 64 ? s.zpp[tid] : 0.f, s.hdot + 8);
+            const float zsum = block_sum(tid < 64 ? s.zpp[tid] : 0.f, s.bsum);
             if (tid < 64) {
                 const int r = tid;
                 float dgam = 0.f;
                 if (r < L) {
-                    dgam = s.zrow[0][r] + s.zrow[1][r] + s.zprow[0][r] + s.zprow[1][r] + s.zcol[r] +
+                    dgam = s.zrow[0][r] + s.zrow[1][r] + s.zrow[2][r] + s.zrow[3][r] +
+                           s.zprow[0][r] + s.zprow[1][r] + s.zprow[2][r] + s.zprow[3][r] + s.zcol[r] +
                            s.bet[r] * s.ee[r] * s.yw[r] + scale * s.ee[r] * s.rowA[r] - s.zpp[r];
                     if (r == L - 1)
                         dgam += zsum + s.ee[r] * (s.hdot[0] + s.hdot[1] + s.hdot[2] + s.hdot[3]);
-                    a.dbeta[(bos + r) * H + h] = s.yu[r] + s.ee[r] * s.yw[r] + s.dbA[0][r] + s.dbA[1][r];
+                    a.dbeta[(bos + r) * H + h] = s.yu[r] + s.ee[r] * s.yw[r] + s.dbA[0][r] +
+                                                 s.dbA[1][r] + s.dbA[2][r] + s.dbA[3][r];
                 }
-                s.red[r >> 5][r & 31] = dgam;
+                s.scan[r >> 5][r & 31] = dgam;
             }
             __syncthreads();
             if (tid < 64) {
                 // dg = reverse cumsum of dgam within the chunk (warp scans over 2 x 32)
                 const int w = tid >> 5;
-                float x = s.red[1 - w][31 - lane];          // reversed order: position p = 63 - r
+                float x = s.scan[1 - w][31 - lane];         // reversed order: position p = 63 - r
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
                     const float yv = __shfl_up_sync(0xffffffffu, x, o);
                     if (lane >= o) x += yv;
                 }
-                s.red[2 + w][lane] = x;
+                s.scan[2 + w][lane] = x;
             }
             __syncthreads();
             if (tid < 64) {
                 const int pidx = tid;                        // position in reversed order
                 const int r = 63 - pidx;
-                float x = s.red[2 + (pidx >> 5)][pidx & 31];
-                if (pidx >= 32) x += s.red[2][31];
+                float x = s.scan[2 + (pidx >> 5)][pidx & 31];
+                if (pidx >= 32) x += s.scan[2][31];
                 if (r < L) a.dg[(bos + r) * H + h] = x;
             }
         }
@@ -628,15 +728,16 @@ cudaError_t local_grads(const Plan &p, cudaStream_t s) {
     a.n_items = p.max_chunks * g.H;
     const size_t smem = sizeof(LocalSmem) + 1024;
     const dim3 grid(std::min(a.n_items, std::max(p.sms, 1)));
+    const dim3 block(512);
     prof_before("tc_local_grad", s);
     if (p.grad_dtype == GDN_BF16) {
         if ((e = set_smem(tc_local_kernel<__nv_bfloat16>, smem)) != cudaSuccess) return e;
-        if ((e = launch_pdl(tc_local_kernel<__nv_bfloat16>, grid, dim3(256), smem, s,
+        if ((e = launch_pdl(tc_local_kernel<__nv_bfloat16>, grid, block, smem, s,
                             m, g, a)) != cudaSuccess)
             return e;
     } else {
         if ((e = set_smem(tc_local_kernel<float>, smem)) != cudaSuccess) return e;
-        if ((e = launch_pdl(tc_local_kernel<float>, grid, dim3(256), smem, s,
+        if ((e = launch_pdl(tc_local_kernel<float>, grid, block, smem, s,
                             m, g, a)) != cudaSuccess)
             return e;
     }

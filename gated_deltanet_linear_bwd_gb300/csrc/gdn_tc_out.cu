@@ -32,7 +32,8 @@ struct OutSmem {
     uint8_t u[2 * kTile];      // u^T: [128 rows v][64 chunk rows]
     uint8_t h0T[4 * kTile];    // H0^T: [k half][128 rows v][64]; after wave 1: U^T
     uint8_t p[kTile];          // P rows r
-    float gam[64], er[64], rq[64], rk[64], eg[64];   // eg: e^(gam_j - gam_{j-1})
+    float gam[64], er[64], eg[64];   // eg: e^(gam_j - gam_{j-1})
+    float rqk[128];            // q, k normalised here: 1 / |q_r| at r, 1 / |k_r| at 64 + r
     float gpre[64];            // the next item's gam, fetched during the current one
     uint64_t load_bar[3], mma_bar;  // loads: {q, k, W^T}, {u^T}, {H0^T}
     uint32_t tmem_base;
@@ -152,23 +153,13 @@ tc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             }
             mma_commit(&s.mma_bar);
         }
-        if (g.l2norm && tid < 128) {
-            // 1 / |q_r| from the Q rows (threads 0-63), 1 / |k_r| from the K rows (64-127)
-            const int r = tid & 63;
-            const uint8_t *base = s.qk + (tid >= 64 ? kTile : 0);
-            float ss = 0.f;
-#pragma unroll
-            for (int half = 0; half < 2; ++half)
-#pragma unroll 8
-                for (int col = 0; col < 64; ++col) {
-                    const float x = ld_bf16(base + half * 2 * kTile, r, col);
-                    ss += x * x;
-                }
-            (tid >= 64 ? s.rk : s.rq)[r] = rsqrtf(ss + 1e-6f);
+        if (g.l2norm) {
+            // 1 / |q_r| (stacked rows 0-63) and 1 / |k_r| (rows 64-127)
+            row_inv_norms(s.qk, 2 * kTile, 128, s.rqk);
+            __syncthreads();
         }
-        if (g.l2norm) __syncthreads();
         if (tid < 64) {
-            s.er[tid] = tid < L ? __expf(s.gam[tid]) * (g.l2norm ? s.rq[tid] : 1.f) : 0.f;
+            s.er[tid] = tid < L ? __expf(s.gam[tid]) * (g.l2norm ? s.rqk[tid] : 1.f) : 0.f;
             s.eg[tid] = tid > 0 ? __expf(s.gam[tid] - s.gam[tid - 1]) : 1.f;
         }
         ok = mbar_wait(&s.mma_bar, 0, g.spin_limit, g.status);
@@ -200,7 +191,7 @@ tc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             }
             if (v < 64) {
                 const int r = v;
-                const float sr = g.l2norm ? s.rq[r] : 1.f;
+                const float sr = g.l2norm ? s.rqk[r] : 1.f;
                 float dd[32];
                 tmem_ld32(tmem_addr(t_p, warp, c0), xs);
                 row_decays32(s.gam, s.eg, r, c0, dd);
@@ -211,7 +202,7 @@ tc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     for (int e = 0; e < 8; ++e) {
                         const int c = c0 + 8 * q + e;
                         x[e] = (c <= r && r < L)
-                                   ? x[e] * dd[8 * q + e] * sr * (g.l2norm ? s.rk[c] : 1.f)
+                                   ? x[e] * dd[8 * q + e] * sr * (g.l2norm ? s.rqk[64 + c] : 1.f)
                                    : 0.f;
                     }
                     st_row8(s.p, r, cq + q, x);

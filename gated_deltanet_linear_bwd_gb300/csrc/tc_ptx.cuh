@@ -392,6 +392,34 @@ __device__ __forceinline__ void row_decays32(const float *gam, const float *eg, 
     }
 }
 
+// 1 / |x_r| = (sum of squares + 1e-6)^-1/2 of rows r = 0 .. nrows-1 of a bf16
+// tile stored as two dk halves of 128-byte rows, the second half_stride bytes
+// after the first (the q / k normalisation inside the library).  Thread t <
+// 2 nrows reads row t / 2, half t % 2, as 16-byte pieces (starting at piece
+// r + 4 (t % 2), so the 8 threads of a shared-memory phase hit 8 different
+// bank groups; the swizzle does not matter for a sum over the row); the two
+// halves meet by a shuffle and the even thread writes out[r].  Threads
+// t >= 2 nrows do nothing; a warp is either wholly in or wholly out.
+__device__ __forceinline__ void row_inv_norms(const uint8_t *base, uint32_t half_stride,
+                                              int nrows, float *out) {
+    const int t = threadIdx.x, r = t >> 1, hh = t & 1;
+    if (r >= nrows) return;
+    const uint4 *row = reinterpret_cast<const uint4 *>(base + hh * half_stride + r * 128);
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint4 x = row[(i + r + 4 * hh) & 7];
+        const __nv_bfloat162 *b = reinterpret_cast<const __nv_bfloat162 *>(&x);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 f = __bfloat1622float2(b[j]);
+            ss += f.x * f.x + f.y * f.y;
+        }
+    }
+    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+    if (hh == 0) out[r] = rsqrtf(ss + 1e-6f);
+}
+
 __device__ __forceinline__ float ld_bf16(const uint8_t *tile, int row, int col) {
     return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tile + sw128_off(row, col)));
 }

@@ -141,8 +141,9 @@ typedef struct gdn_bwd_args {
 /* GDN_ABI_VERSION of the loaded library. */
 int32_t gdn_abi_version(void);
 
-/* Bytes of workspace gdn_chunk_fwd needs for these arguments (0 when the
- * arguments are invalid; gdn_last_error then says why). */
+/* Bytes of workspace gdn_chunk_fwd needs for these arguments: at least 256
+ * for any valid arguments (an empty problem included), 0 when the arguments
+ * are invalid (gdn_last_error then says why). */
 size_t gdn_fwd_workspace_size(const gdn_fwd_args *args);
 
 /* Forward: O and (optionally) the final state, in chunked form: per chunk a UT transform T = (I + strict_lower(diag(beta)
@@ -161,14 +162,17 @@ gdn_status gdn_chunk_fwd(const gdn_fwd_args *args, void *workspace, size_t works
  * inputs, sizes and flags; the library cannot check that. */
 size_t gdn_fwd_ctx_size(const gdn_fwd_args *args);
 
-/* Bytes of workspace gdn_chunk_bwd needs. */
+/* Bytes of workspace gdn_chunk_bwd needs (at least 256 for valid arguments,
+ * 0 for invalid ones, as gdn_fwd_workspace_size). */
 size_t gdn_bwd_workspace_size(const gdn_bwd_args *args);
 
 /* Backward (which the traeai.com page, announcement text, singles out as the
  * most difficult piece to make fast): given
  * dO and d(final_state), writes dq, dk, dv, dg, dbeta and d(initial_state).
- * The forward's per-chunk states are recomputed, not read from a saved
- * context; the result does not depend on cp_mode beyond rounding. */
+ * Without args->ctx the forward's per-chunk quantities (W, u, (I + A)^-1 and
+ * the chunk start states) are recomputed here; with a ctx that a gdn_chunk_fwd
+ * call on the same inputs filled, they are read from it instead.  The result
+ * depends on neither choice, nor on cp_mode, beyond rounding. */
 gdn_status gdn_chunk_bwd(const gdn_bwd_args *args, void *workspace, size_t workspace_bytes,
                          void *stream);
 
@@ -187,7 +191,12 @@ gdn_status gdn_chunk_bwd(const gdn_bwd_args *args, void *workspace, size_t works
  *   are rejected with GDN_ERR_WORKSPACE before any work is queued.
  * - The first call on a device looks up the scratch area's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture on the device.
+ *   before any stream capture on the device.  The address is kept for the
+ *   life of the process, one per device index: it belongs to the device's
+ *   primary context (the CUDA runtime's), so do not call this entry point
+ *   with another driver-API context current, nor after cudaDeviceReset on
+ *   that device.  The per-device status word every entry point reports
+ *   through (gdn_sync_status) is located and kept the same way.
  * - Every call on a device shares the one scratch area, which keeps the
  *   last call's contents; the forward writes every scratch byte it reads,
  *   so nothing needs clearing between calls.  Calls whose work overlaps on

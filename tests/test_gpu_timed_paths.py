@@ -1,0 +1,102 @@
+"""Parity of the exact calls bench.py times, at the full workload sizes.
+
+bench.py's step is a forward that keeps its per-chunk context followed by a
+backward that reads it (bench.training_step), with intra-card sequence
+parallelism forced on the edge and long-context workloads and chosen by the
+library elsewhere.  Here that same step runs on the whole workload on the GPU,
+and sampled (sequence, head) units of O, the final state and every gradient
+are compared element by element with the fp64 oracle at the bf16 tolerance.
+The kernels that ran are read from the library's tracing, so each test also
+pins which path it covered (the fused reverse walk on training and varlen,
+the sequence-parallel map walks on edge and long)."""
+import numpy as np
+import pytest
+import torch
+
+import bench
+import gdn_synth
+from gpu_helpers import TOL, check, lib, oracle_bwd, oracle_fwd, sub_problem, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.fail("these tests need a CUDA GPU")
+    lib()
+
+
+def timed_step(p, l2):
+    gdn = lib()
+    d = p.to("cuda")
+    gdn.gdn_profile_begin()
+    outs = bench.training_step(gdn, d, p.meta["cp"], l2)
+    torch.cuda.synchronize()
+    names = {n for n, _, _ in gdn.gdn_profile_end()}
+    assert gdn.gdn_sync_status(torch.cuda.current_stream().cuda_stream) == 0
+    o, fs, dq, dk, dv, dg, db, dh0 = (to_np(t) for t in outs)
+    return dict(o=o, final_state=fs, dq=dq, dk=dk, dv=dv, dg=dg, dbeta=db, dh0=dh0), names
+
+
+def compare_sampled(name, got, p, heads, batches, l2):
+    tol = TOL[p.meta["dtype"]]
+    sub = sub_problem(p, heads=heads, batches=batches)
+    ro, rfs = oracle_fwd(sub, l2=l2)
+    r = oracle_bwd(sub, l2=l2)
+    packed = p.cu_seqlens is not None
+
+    def tok(x):          # [B, T, H, ...] -> sampled rows and heads
+        x = x if batches is None else x[batches]
+        return x[:, :, heads]
+
+    def st(x):           # [N, H, K, V] -> sampled sequences and heads
+        x = x if batches is None or packed else x[batches]
+        return x[:, heads]
+    errs = {"o": check(f"{name} o", tok(got["o"]), ro, tol),
+            "final_state": check(f"{name} final_state", st(got["final_state"]), rfs, tol)}
+    for k in ("dq", "dk", "dv", "dg", "dbeta"):
+        errs[k] = check(f"{name} {k}", tok(got[k]), r[k], tol)
+    if got["dh0"] is not None and r["dh0"] is not None:
+        errs["dh0"] = check(f"{name} dh0", st(got["dh0"]), r["dh0"], tol)
+    print(name, {k: f"{v:.2e}" for k, v in errs.items()})
+    return errs
+
+
+@pytest.mark.parametrize("l2", [False, True])
+def test_edge_step_as_timed(l2):
+    """B=1 T=8192 H=8: forward keeping its context, sequence parallelism forced,
+    backward reading the context (the map walks and both segment scans run)."""
+    p = gdn_synth.make("edge")
+    got, names = timed_step(p, l2)
+    assert {"tc_walk_map", "map_scan", "tc_dwalk_map", "map_rscan"} <= names, names
+    compare_sampled("edge", got, p, heads=[0, 5], batches=None, l2=l2)
+
+
+@pytest.mark.parametrize("l2", [False, True])
+def test_training_step_as_timed(l2):
+    """B=4 T=4096 H=32: no sequence parallelism; both fused walks with the saved
+    context (the reverse walk forms P, Qs and Y^T itself)."""
+    p = gdn_synth.make("training")
+    got, names = timed_step(p, l2)
+    assert "tc_dwalk_fused" in names and "tc_bwd_intra" not in names, names
+    assert "tc_walk_fused" in names and "tc_out" not in names, names
+    compare_sampled("training", got, p, heads=[1, 20], batches=[2], l2=l2)
+
+
+@pytest.mark.parametrize("l2", [False, True])
+def test_varlen_step_as_timed(l2):
+    """16 packed sequences of 512-8192 tokens, H=32: the headline workload."""
+    p = gdn_synth.make("varlen")
+    got, names = timed_step(p, l2)
+    assert "tc_dwalk_fused" in names and "tc_walk_fused" in names, names
+    compare_sampled("varlen", got, p, heads=[7, 30], batches=None, l2=l2)
+
+
+def test_long_context_step_as_timed():
+    """B=1 T=65536 H=16 forward + backward with sequence parallelism (the extra
+    fwd+bwd row of the long-context workload), one sampled head."""
+    p = gdn_synth.make("long")
+    got, names = timed_step(p, True)
+    assert {"tc_walk_map", "tc_dwalk_map"} <= names, names
+    compare_sampled("long", got, p, heads=[3], batches=None, l2=True)
