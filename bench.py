@@ -596,6 +596,43 @@ def run_ours(args, rank, world, local):
     ms_e2e_graph, _ = timer.run(e2e_g, args.steps)
     torch.cuda.synchronize(dev)
 
+    # the same step with the decay formed inside the library from raw gate logits
+    import gdn_synth
+    gx, ga = (t.to(dev) for t in gdn_synth.gate_draws(p, seed=0))
+
+    def gated_step():
+        o, fs, saved = gdn.chunk_gated_delta_rule_fwd(
+            d.q, d.k, d.v, gx, d.beta, initial_state=d.h0, output_final_state=True,
+            cu_seqlens=d.cu_seqlens, use_qk_l2norm=l2, cp=cp, save_ctx=True, gate_scale=ga)
+        return gdn.chunk_gated_delta_rule_bwd(
+            d.q, d.k, d.v, gx, d.beta, d.do, dht=d.dht, initial_state=d.h0,
+            cu_seqlens=d.cu_seqlens, use_qk_l2norm=l2, cp=cp, ctx=saved, gate_scale=ga)
+
+    gated_g, gated_graph = graphed(torch, dev, gated_step)
+    for _ in range(3):
+        gated_g()
+    ms_gated, _ = timer.run(gated_g, args.steps)
+    del gated_g, gated_graph, gx, ga
+
+    # decode: one token for each of 64 sequences x 32 heads from resident fp32 states
+    dn, dh = 64, 32
+    dgen = torch.Generator(device="cpu").manual_seed(7)
+    dq_ = (torch.randn(dn, dh, p.K, generator=dgen) / p.K ** 0.5).to(dev, d.q.dtype)
+    dk_ = (torch.randn(dn, dh, p.K, generator=dgen) / p.K ** 0.5).to(dev, d.q.dtype)
+    dv_ = torch.randn(dn, dh, p.V, generator=dgen).to(dev, d.q.dtype)
+    dg_ = -torch.rand(dn, dh, generator=dgen).to(dev)
+    db_ = torch.rand(dn, dh, generator=dgen).to(dev)
+    dst = (0.1 * torch.randn(dn, dh, p.K, p.V, generator=dgen)).to(dev)
+
+    def decode_step():
+        gdn.recurrent_step(dq_, dk_, dv_, dg_, db_, dst)
+
+    for _ in range(3):
+        decode_step()
+    ms_dec, _ = timer.run(decode_step, args.steps)
+    dec_bytes = 2 * dst.numel() * 4 + dn * dh * (2 * p.K + 2 * p.V) * e_in + dn * dh * 8
+    del dq_, dk_, dv_, dg_, db_, dst
+
     # everything the headline line needs, before its tensors are released
     rt = roofline_terms(p, e_in, peaks)
     head = {"ms_step": h["ms_step"], "ms_fwd": h["ms_fwd"], "prof": h["prof"],
@@ -638,8 +675,9 @@ def run_ours(args, rank, world, local):
     med_fwd = statistics.median(head["ms_fwd"])
     med_e2e = statistics.median(ms_e2e)
     med_e2e_g = statistics.median(ms_e2e_graph)
-    med_step, med_fwd, med_e2e, med_e2e_g = max_over_ranks(
-        [med_step, med_fwd, med_e2e, med_e2e_g], dist, dev)
+    med_gated, med_dec = statistics.median(ms_gated), statistics.median(ms_dec)
+    med_step, med_fwd, med_e2e, med_e2e_g, med_gated, med_dec = max_over_ranks(
+        [med_step, med_fwd, med_e2e, med_e2e_g, med_gated, med_dec], dist, dev)
     if rank != 0:
         if dist:
             dist.destroy_process_group()
@@ -689,6 +727,15 @@ def run_ours(args, rank, world, local):
             "e2e_graph": {"value": job_rate(world, tokens, med_e2e_g), "unit": "tokens/s",
                           "ms_per_step": med_e2e_g,
                           "what": "the same end-to-end step captured once as a CUDA graph"},
+            "gated": {"value": job_rate(world, tokens, med_gated), "unit": "tokens/s",
+                      "ms_per_step": med_gated,
+                      "what": "the same fwd+bwd step with the decay formed inside from gate "
+                              "logits (gate_scale), d(logits) and d(gate_scale) returned"},
+            "decode": {"value": job_rate(world, dn, med_dec), "unit": "tokens/s",
+                       "ms_per_step": med_dec, "batch": f"{dn} sequences x {dh} heads",
+                       "hbm_gbs": dec_bytes / (med_dec / 1e3) / 1e9,
+                       "frac_of_hbm": dec_bytes / (med_dec / 1e3) / 1e9 / rt["hbm"],
+                       "what": "one gdn_recurrent_step: state read and written once"},
             "workloads": extra, "warmup_shortcut": warm,
             "clocks": head["clocks"], "cpu_baseline": cpu}
     print(json.dumps(line), flush=True)

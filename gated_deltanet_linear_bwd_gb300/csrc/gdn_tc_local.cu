@@ -62,15 +62,16 @@ struct LocalSmem {
     uint8_t ds[kTile];         // dS rows r
     uint8_t gs[kTile];         // G rows r
     float gam[64], bet[64], ee[64], ff[64];
-    float red[16][16], red2[16][16], red3[16][16], red4[16][16], red5[16][16];
+    float red[16][16], red4[16][16], red5[16][16];
     float zrow[4][64], zprow[4][64], dbA[4][64];   // per column group
     float scan[4][32];         // dg's reverse cumsum
     float zcol[64], rowA[64], yw[64], yu[64], zpp[64];
     float hdot[4];             // per-warp parts of <dHL, H0>
     float bsum[16];            // block_sum scratch
     float rq[64], rk[64];      // 1 / |q_r|, 1 / |k_r| (q, k normalised here)
-    uint64_t load_bar[3], mma_bar;  // load groups: {v, dO, dU^T, H0^T (, T)}, {W^T, u^T, dHL^T},
+    uint64_t load_bar[3], mma_bar;  // load groups: {dO, dU^T, H0^T (, T)}, {v, W^T, u^T, dHL^T},
                                     // {q, k (, T when q, k are normalised here)}
+    uint64_t diag_bar;         // wave 2.5's diagonal products (yw, yu), one phase per item
     uint32_t tmem_base;
 };
 
@@ -233,17 +234,19 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
         // region then holds a diagonal tile until wave 3 is done)
         const bool t_late = g.l2norm != 0;
         if (grp == 0) {
-            mbar_arrive_expect_tx(bar, (t_late ? 10 : 11) * kTile);
+            mbar_arrive_expect_tx(bar, (t_late ? 8 : 9) * kTile);
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-                tma_load_3d(s.v + half * kTile, &m.v, bar, half * 64, hh, tok0);
                 tma_load_3d(s.dO + half * kTile, &m.dO, bar, half * 64, hh, tok0);
                 tma_load_2d(s.h0T + half * 2 * kTile, &m.hc, bar, 0, 2 * trow + half * kD);
             }
             tma_load_2d(s.du, &m.du, bar, 0, trow);
             if (!t_late) tma_load_2d(s.tt, &m.t, bar, 0, trow / 2);
         } else if (grp == 1) {
-            mbar_arrive_expect_tx(bar, 8 * kTile);
+            mbar_arrive_expect_tx(bar, 10 * kTile);
+#pragma unroll
+            for (int half = 0; half < 2; ++half)
+                tma_load_3d(s.v + half * kTile, &m.v, bar, half * 64, hh, tok0);
             tma_load_2d(s.w, &m.w, bar, 0, trow);
             tma_load_2d(s.ut, &m.u, bar, 0, trow);
             tma_load_2d(s.dl, &m.dhc, bar, 0, 2 * trow);
@@ -262,6 +265,7 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
     if (tid == 0) {
         for (int i = 0; i < 3; ++i) mbar_init(&s.load_bar[i], 1);
         mbar_init(&s.mma_bar, 1);
+        mbar_init(&s.diag_bar, 1);
         fence_barrier_init();
     }
     if (warp == 0) {
@@ -278,6 +282,8 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
                    t_hd = tb + 384;
     const uint32_t t_dp = tb, t_dkh = tb + 128, t_yw = tb + 256, t_yu = tb + 320;
     const uint32_t t_da = tb + 384;
+    // diag(dYw K^T) and diag(dYu V^T): yw and yu (columns free from wave 2.5 to wave 3)
+    const uint32_t t_dyk = tb + 320, t_dyv = tb + 448;
     const uint32_t t_dk = tb, t_q2 = tb + 448;
 
     int item = blockIdx.x, ci = 0, h = 0;
@@ -289,7 +295,7 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
             for (int grp = 0; grp < 3; ++grp) load_group(grp, ci, h, cr.bos);
         issued[0] = issued[1] = issued[2] = 1;
     }
-    int it = 0, mma_n = 0;
+    int it = 0, mma_n = 0, diag_n = 0;
     bool bailed = false;
     float pre_g = 0.f, pre_b = 0.f;           // the next item's gam / beta (threads < 64), read early
     bool pre = false;
@@ -415,9 +421,8 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
         tc_fence_after();
         {
             // every feature f = v: dYw^T, dYu^T rows into the dead dHL^T tiles, and
-            // sums over f of dYw .* K (yw) and dYu .* V (yu)
+            // sums over k of (diag(f) U dHL^T) .* K (zpp); yw and yu come from wave 2.5
             const uint8_t *krow = s.qk + (v >> 6) * 2 * kTile + kTile;
-            const uint8_t *vrow = s.v + (v >> 6) * kTile;
             // dV = diag(beta) dYu leaves now; a warp's lanes write 32 consecutive features
             TG *dv = (TG *)a.dv + (bos * H + h) * (long long)kD + v;
 #pragma unroll 1
@@ -435,24 +440,16 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
                 for (int e = 0; e < 8; ++e) {
                     const int c = c0 + 8 * q + e;
                     const float kv = c < L ? ld_bf16(krow, c, v & 63) : 0.f;
-                    yw[e] *= kv;
-                    yu[e] = c < L ? yu[e] * ld_bf16(vrow, c, v & 63) : 0.f;
                     pz[e] *= s.ff[c] * kv;           // (diag(f) U dHL^T) .* K, summed over k below
                 }
-                warp_sum8(yw, s.red2[warp] + 8 * q);
-                warp_sum8(yu, s.red3[warp] + 8 * q);
                 warp_sum8(pz, s.red4[warp] + 8 * q);
             }
             tc_fence_before();
             fence_proxy_async();
             __syncthreads();
-            if (tid < 64) {
-                s.yw[tid] = quad_sum(s.red2, tid);
-                s.yu[tid] = quad_sum(s.red3, tid);
-                s.zpp[tid] = quad_sum(s.red4, tid);
-            }
+            if (tid < 64) s.zpp[tid] = quad_sum(s.red4, tid);
         }
-        // v, dO, dU^T, the H0^T / U^T / dW^T tile and T are dead: next item's group 0
+        // dO, dU^T, the H0^T / U^T / dW^T tile and T are dead: next item's group 0
         if (have_next) {
             if (tma_thread) {
                 fence_proxy_async();
@@ -461,12 +458,14 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
             ++issued[0];
         }
 
-        // ---------------- wave 2.5: dA = -(dYu u^T + dYw W^T), rows duplicated on lanes 64-127
+        // ---------------- wave 2.5: dA = -(dYu u^T + dYw W^T), rows duplicated on lanes 64-127;
+        // dYw K^T and dYu V^T, whose diagonals are yw_r = <dYw_r, k_r> and yu_r = <dYu_r, v_r>
         ++mma_n;
+        ++diag_n;
         if (warp == 0) {
             tc_fence_after();
             const uint32_t yu = smem_u32(dyuT), yw = smem_u32(dywT), ua = smem_u32(s.ut),
-                           wa = smem_u32(s.w);
+                           wa = smem_u32(s.w), qk = smem_u32(s.qk), va = smem_u32(s.v);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 mma_bf16(t_da, desc_sw128(yu + kk * 2048, 0, 1024),
@@ -475,6 +474,16 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
                          desc_sw128(wa + kk * 2048, kTile, 1024), kMM, 1);
             }
             mma_commit(&s.mma_bar);
+            // behind dA on their own barrier, so that the dA epilogue need not wait
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t hh = kk >> 2, sub = (kk & 3) * 32;
+                mma_bf16(t_dyk, desc_sw128(yw + kk * 2048, 0, 1024),
+                         desc_sw128(qk + hh * 2 * kTile + kTile + sub, 16, 1024), kMK, kk > 0);
+                mma_bf16(t_dyv, desc_sw128(yu + kk * 2048, 0, 1024),
+                         desc_sw128(va + hh * kTile + sub, 16, 1024), kMK, kk > 0);
+            }
+            mma_commit(&s.diag_bar);
         }
         // While the dA product runs, lanes 0-63 form dS; lanes 64-127 then take
         // the dA epilogue.  Each half reduces into its own array.
@@ -504,6 +513,24 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
             }
             s.zrow[cg][r] = zr;
             if (lane < 16) s.red5[warp][lane] = 0.f;
+            if (cg == 0) {
+                // yw_r, yu_r: lane r's diagonal entries (column r) of wave 2.5's products
+                ok = mbar_wait(&s.diag_bar, it & 1, g.spin_limit, g.status);
+                if (ok) {
+                    tc_fence_after();
+                    float xk[32], xv[32];
+                    tmem_ld32(tmem_addr(t_dyk, warp, 32 * warp), xk);
+                    tmem_ld32(tmem_addr(t_dyv, warp, 32 * warp), xv);
+                    float dk_ = 0.f, dv_ = 0.f;
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj) {
+                        dk_ = jj == lane ? xk[jj] : dk_;
+                        dv_ = jj == lane ? xv[jj] : dv_;
+                    }
+                    s.yw[r] = r < L ? dk_ : 0.f;
+                    s.yu[r] = r < L ? dv_ : 0.f;
+                }
+            }
         } else {
             // rows r = v - 64: G = dA .* D .* beta_r, z' = G .* K K^T and the dA part
             // of dbeta
@@ -542,8 +569,8 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
         tc_fence_before();
         fence_proxy_async();
         if (__syncthreads_or(!ok)) { bailed = true; break; }
-        // the dA product is done (lanes 64-127 saw it): W^T, u^T and the dHL^T /
-        // dYu^T / dYw^T tiles are dead, the next item's group 1 can come
+        // wave 2.5 is done (lanes 64-127 saw it): v, W^T, u^T and the dHL^T / dYu^T /
+        // dYw^T tiles are dead, the next item's group 1 can come
         if (have_next) {
             if (tma_thread) {
                 fence_proxy_async();
@@ -695,6 +722,7 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
         for (int grp = 0; grp < 3; ++grp)
             if (issued[grp] > 0) mbar_drain(&s.load_bar[grp], (issued[grp] - 1) & 1);
         if (mma_n > 0) mbar_drain(&s.mma_bar, (mma_n - 1) & 1);
+        if (diag_n > 0) mbar_drain(&s.diag_bar, (diag_n - 1) & 1);
     }
     tc_fence_before();
     __syncthreads();
