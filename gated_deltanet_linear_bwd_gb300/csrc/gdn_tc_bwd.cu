@@ -566,8 +566,10 @@ tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
         tc_fence_after();
         // dU^T row v, chunk rows 32*hs .. +31 (one TMEM load, groups of 8): Y^T + X^T diag(f)
         float xs[32], ys[32];
-        tmem_ld32(tmem_addr(t_x, warp, 32 * hs), xs);
-        if (fused) tmem_ld32(tmem_addr(t_y, warp, 32 * hs), ys);
+        if (fused)
+            tmem_ld32x2(tmem_addr(t_x, warp, 32 * hs), tmem_addr(t_y, warp, 32 * hs), xs, ys);
+        else
+            tmem_ld32(tmem_addr(t_x, warp, 32 * hs), xs);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             float *x = xs + 8 * q;
@@ -615,13 +617,11 @@ tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
         tc_fence_after();
         {
             const float el = __expf(s.gam[st][L - 1]);
+            float z[64];
+            tmem_ld32x2(tmem_addr(t_z, warp, 64 * hs), tmem_addr(t_z, warp, 64 * hs + 32), z,
+                        z + 32);
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                float z[32];
-                tmem_ld32(tmem_addr(t_z, warp, 64 * hs + 32 * q), z);
-#pragma unroll
-                for (int jj = 0; jj < 32; ++jj) dH[32 * q + jj] = el * dH[32 * q + jj] + z[jj];
-            }
+            for (int jj = 0; jj < 64; ++jj) dH[jj] = el * dH[jj] + z[jj];
         }
         st_row64(s.dhT + hs * 2 * kTile, v, dH);
         if (tid < 64) cp_async_wait_all();

@@ -171,8 +171,8 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         {
             // row r of this chunk's K K^T block
             float kk[64];
-            tmem_ld32(tmem_addr(tbase, warp, ch * 64), kk);
-            tmem_ld32(tmem_addr(tbase, warp, ch * 64 + 32), kk + 32);
+            tmem_ld32x2(tmem_addr(tbase, warp, ch * 64), tmem_addr(tbase, warp, ch * 64 + 32), kk,
+                        kk + 32);
             float nrm = 0.f;
 #pragma unroll
             for (int c = 0; c < 64; ++c) nrm = (c == r) ? kk[c] : nrm;
@@ -513,8 +513,7 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     // scale (e_c (H^T Q^T) + U^T P^T)
     auto out_epilogue = [&](int b) {
         float qh[32], pu[32];
-        tmem_ld32(tmem_addr(t_qh(b), warp, 32 * hs), qh);
-        tmem_ld32(tmem_addr(t_pu(b), warp, 32 * hs), pu);
+        tmem_ld32x2(tmem_addr(t_qh(b), warp, 32 * hs), tmem_addr(t_pu(b), warp, 32 * hs), qh, pu);
         __nv_bfloat16 *dst = a.o + (pbos * H + h) * (long long)kD + v;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -707,13 +706,11 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         tc_fence_after();
         {
             const float el = __expf(s.gam[gb][L - 1]);
+            float d[64];
+            tmem_ld32x2(tmem_addr(t_dh, warp, 64 * hs), tmem_addr(t_dh, warp, 64 * hs + 32), d,
+                        d + 32);
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                float d[32];
-                tmem_ld32(tmem_addr(t_dh, warp, 64 * hs + 32 * q), d);
-#pragma unroll
-                for (int jj = 0; jj < 32; ++jj) Hr[32 * q + jj] = el * Hr[32 * q + jj] + d[jj];
-            }
+            for (int jj = 0; jj < 64; ++jj) Hr[jj] = el * Hr[jj] + d[jj];
         }
         st_row64(s.hT + hs * 2 * kTile, v, Hr);
         pbos = bos;

@@ -239,8 +239,7 @@ tc_out_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             // (four features) after a quad transpose
             __nv_bfloat16 *dst = o + (bos * H + h) * (long long)kD + v;
             float oi[32], oa[32];
-            tmem_ld32(tmem_addr(t_oi, warp, c0), oi);
-            tmem_ld32(tmem_addr(t_oa, warp, c0), oa);
+            tmem_ld32x2(tmem_addr(t_oi, warp, c0), tmem_addr(t_oa, warp, c0), oi, oa);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 float x[8];
