@@ -111,7 +111,8 @@ static gdn_status validate(const Common &c) {
         (c.gate_scale && !aligned16(c.gate_scale)))
         return fail(GDN_ERR_INVALID_ARG, "every tensor must be 16-byte aligned");
     const long long tokens = (long long)c.B * c.T;
-    if (tokens * c.H * (long long)(c.K > c.V ? c.K : c.V) >= (1ll << 40))
+    if (tokens * c.H * (long long)(c.K > c.V ? c.K : c.V) >= (1ll << 40) ||
+        (long long)(c.cu ? c.N : c.B) * c.H >= (1ll << 31))
         return fail(GDN_ERR_INVALID_ARG, "problem too large");
     return GDN_OK;
 }
@@ -211,6 +212,7 @@ static size_t layout(Plan &p, bool bwd, char *base) {
     if (g.cu) {
         w.chunk_off = (int32_t *)take((g.N + 1) * sizeof(int32_t));
         w.seg_off = (int32_t *)take((g.N + 1) * sizeof(int32_t));
+        w.order = (int32_t *)take(g.N * sizeof(int32_t));
     }
     if (p.cp) {
         w.warm = (int32_t *)take((size_t)g.N * g.H * sizeof(int32_t));
@@ -341,6 +343,7 @@ static gdn_status prepare(const Common &c, bool bwd, void *ws, size_t ws_bytes, 
     layout(p, bwd, (char *)ws);
     p.g.chunk_off = p.ws.chunk_off;
     p.g.seg_off = p.ws.seg_off;
+    p.g.order = p.ws.order;
     return GDN_OK;
 }
 

@@ -36,6 +36,7 @@ struct Geo {
     const int32_t *cu;          // nullable: fixed-length rows
     const int32_t *chunk_off;   // [N+1] chunk offsets (varlen only)
     const int32_t *seg_off;     // [N+1] segment offsets (varlen + CP only)
+    const int32_t *order;       // [N] sequences by chunk count, longest first (varlen), or null
     int B, T, H, K, V, N;
     int nc_fixed;               // chunks per row when cu == nullptr
     int seg_chunks;             // chunks per segment (CP), else huge
@@ -130,6 +131,16 @@ __device__ __forceinline__ int seq_nsegs(const Geo &g, int n) {
 }
 __device__ __forceinline__ int seq_seg_base(const Geo &g, int n) {
     return g.cu ? g.seg_off[n] : n * g.nseg_fixed;
+}
+
+// Sequence and head walked by block b of a walk launched without sequence
+// parallelism as a 1-D grid of N x H blocks: the blocks go out in index
+// order, so rank-major numbering (every head of the longest sequence first)
+// lets the longest walks start first.
+__device__ __forceinline__ void walk_unit(const Geo &g, int b, int &n, int &h) {
+    const int rank = b / g.H;
+    h = b - rank * g.H;
+    n = g.order ? g.order[rank] : rank;
 }
 
 // Maps a global segment index to (sequence, segment-in-sequence).

@@ -19,6 +19,7 @@ struct Ws {
     void *u = nullptr;           // u: likewise ([tokens, H, V] or [chunk][H][V][64])
     int32_t *chunk_off = nullptr;  // [N+1] (varlen)
     int32_t *seg_off = nullptr;    // [N+1] (varlen + CP)
+    int32_t *order = nullptr;      // [N] sequences by chunk count, longest first (varlen)
     int32_t *warm = nullptr;       // [N, H] warmup decision
     float *maps = nullptr;         // [segs, H, K, K+V] affine maps
     float *seg_state = nullptr;    // [segs, H, K, V] segment start states / end gradients

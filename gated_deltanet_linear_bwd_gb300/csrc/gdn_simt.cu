@@ -930,6 +930,26 @@ __global__ void tables_kernel(const int32_t *cu, int N, int T, int seg_chunks,
     }
 }
 
+// Sequences ranked by chunk count, longest first (ties by index): thread n
+// counts the sequences that go before it and writes n at that rank.  O(N^2)
+// work, so beyond kOrderMax sequences the order is left as given.
+constexpr int kOrderMax = 8192;
+__global__ void order_kernel(const int32_t *chunk_off, int N, int32_t *order) {
+    const int n = blockIdx.x * blockDim.x + threadIdx.x;
+    if (n >= N) return;
+    if (N > kOrderMax) {
+        order[n] = n;
+        return;
+    }
+    const int mine = chunk_off[n + 1] - chunk_off[n];
+    int rank = 0;
+    for (int m = 0; m < N; ++m) {
+        const int other = chunk_off[m + 1] - chunk_off[m];
+        rank += (other > mine || (other == mine && m < n)) ? 1 : 0;
+    }
+    order[rank] = n;
+}
+
 }  // namespace simt
 
 // ---------------------------------------------------------------- launchers
@@ -985,6 +1005,8 @@ cudaError_t tables(const Plan &p, cudaStream_t s) {
     prof_before("tables", s);
     tables_kernel<<<1, 32, 0, s>>>(p.g.cu, p.g.N, p.g.T, p.cp ? p.g.seg_chunks : 0,
                                    p.ws.chunk_off, p.cp ? p.ws.seg_off : nullptr, p.g.status);
+    if (p.ws.order)
+        order_kernel<<<(p.g.N + 255) / 256, 256, 0, s>>>(p.ws.chunk_off, p.g.N, p.ws.order);
     prof_after(s);
     return cudaGetLastError();
 }

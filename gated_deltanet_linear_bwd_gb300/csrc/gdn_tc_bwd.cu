@@ -333,14 +333,15 @@ tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
     extern __shared__ uint8_t smem_raw[];
     S &s = *reinterpret_cast<S *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int tid = threadIdx.x, warp = tid >> 5, h = blockIdx.y, cb = blockIdx.z, H = g.H;
+    const int tid = threadIdx.x, warp = tid >> 5, cb = blockIdx.z, H = g.H;
+    int h = blockIdx.y;
     const int v = tid & 127, hs = tid >> 7;
     int n, j = 0, nseg = 1;
     if (a.cp) {
         if (!seg_ref(g, blockIdx.x, n, j)) return;
         nseg = seq_nsegs(g, n);
     } else {
-        n = blockIdx.x;
+        walk_unit(g, blockIdx.x, n, h);
         if (n >= g.N) return;
     }
     if (MODE == kDMap && j == 0) return;                 // segment 0 needs no map
@@ -721,13 +722,13 @@ cudaError_t backward(const Plan &p, cudaStream_t s, bool have_ctx) {
         prof_after(s);
     } else if (fuse_intra) {
         prof_before("tc_dwalk_fused", s);
-        if ((e = launch_pdl(tc_dwalk_kernel<kDFused>, dim3(g.N, g.H, 1), dim3(256), fused_smem, s,
+        if ((e = launch_pdl(tc_dwalk_kernel<kDFused>, dim3(g.N * g.H, 1, 1), dim3(256), fused_smem, s,
                             m, g, a)) != cudaSuccess)
             return e;
         prof_after(s);
     } else {
         prof_before("tc_dwalk_out", s);
-        if ((e = launch_pdl(tc_dwalk_kernel<kDOut>, dim3(g.N, g.H, 1), dim3(256), smem, s,
+        if ((e = launch_pdl(tc_dwalk_kernel<kDOut>, dim3(g.N * g.H, 1, 1), dim3(256), smem, s,
                             m, g, a)) != cudaSuccess)
             return e;
         prof_after(s);

@@ -414,14 +414,15 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     extern __shared__ uint8_t smem_raw[];
     S &s = *reinterpret_cast<S *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int tid = threadIdx.x, warp = tid >> 5, h = blockIdx.y, cb = blockIdx.z, H = g.H;
+    const int tid = threadIdx.x, warp = tid >> 5, cb = blockIdx.z, H = g.H;
+    int h = blockIdx.y;
     const int v = tid & 127, hs = tid >> 7;
     int n, j = 0, nseg = 1;
     if (a.cp) {
         if (!seg_ref(g, blockIdx.x, n, j)) return;
         nseg = seq_nsegs(g, n);
     } else {
-        n = blockIdx.x;
+        walk_unit(g, blockIdx.x, n, h);
         if (n >= g.N) return;
     }
     if (MODE == kWalkMap && (j == nseg - 1 || (a.warm && a.warm[n * H + h]))) return;
@@ -866,6 +867,7 @@ static cudaError_t run_forward(const Plan &p, cudaStream_t s, bool states_only, 
     auto walk_kernel = fuse_out ? tc_walk_kernel<kWalkFused> : tc_walk_kernel<kWalkOut>;
     const char *out_name = states_only ? "tc_walk_states" : fuse_out ? "tc_walk_fused" : "tc_walk";
     const size_t walk_smem = fuse_out ? fused_smem : out_smem;
+    const dim3 walk_block(256);
     if (p.cp) {
         a.cp = 1;
         a.maps = p.ws.maps;
@@ -883,13 +885,13 @@ static cudaError_t run_forward(const Plan &p, cudaStream_t s, bool states_only, 
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if ((e = simt::cp_scan(p, a.warm, s)) != cudaSuccess) return e;
         prof_before(out_name, s);
-        if ((e = launch_pdl(walk_kernel, dim3(p.max_segs, g.H, 1), dim3(256), walk_smem, s,
+        if ((e = launch_pdl(walk_kernel, dim3(p.max_segs, g.H, 1), walk_block, walk_smem, s,
                             mq, mk, mw, mu, mhc, g, a)) != cudaSuccess)
             return e;
         prof_after(s);
     } else {
         prof_before(out_name, s);
-        if ((e = launch_pdl(walk_kernel, dim3(g.N, g.H, 1), dim3(256), walk_smem, s,
+        if ((e = launch_pdl(walk_kernel, dim3(g.N * g.H, 1, 1), walk_block, walk_smem, s,
                             mq, mk, mw, mu, mhc, g, a)) != cudaSuccess)
             return e;
         prof_after(s);
