@@ -168,6 +168,8 @@ static gdn_status make_plan(const Common &c, bool bwd, int sms, Plan &p) {
     const int nc_avg = (int)((avg_len + kChunk - 1) / kChunk);
     p.cp = c.cp_mode == GDN_CP_FORCE || (c.cp_mode == GDN_CP_AUTO && sms > 0 &&
                                          cp_auto(units, avg_len, sms));
+    p.cp_forced = c.cp_mode == GDN_CP_FORCE;
+    p.seg_chunks_arg = c.seg_chunks;
     if (p.cp) {
         int G = c.seg_chunks;
         if (G <= 0) {
@@ -245,7 +247,13 @@ static int seg_capacity(const Common &c, int max_chunks) {
     return c.cu ? max_chunks + c.N : (max_chunks > c.B ? max_chunks : c.B);
 }
 
-// Saved forward context (tensor-core path): gam, W, u, T, chunk start states.
+// Saved forward context (tensor-core path): gam, W, u, T, chunk start states,
+// and, for fixed-length batches with sequence parallelism forced, the A parts
+// of the forward's segment maps (the backward's reverse maps are their
+// transposes, so it then walks only the other half).  Every size here follows
+// from the arguments alone, not from the device: the maps region is sized for
+// the most segments the forward can choose (64 per sequence, or the count
+// cp_segment_chunks fixes).
 static size_t ctx_layout(Plan &p, char *base) {
     size_t off = 0;
     auto take = [&](size_t bytes) -> char * {
@@ -261,7 +269,16 @@ static size_t ctx_layout(Plan &p, char *base) {
     void *u = take(tiles * g.V);
     void *tm = take((size_t)p.max_chunks * g.H * 64 * 64 * 2);
     float *hc = (float *)take((size_t)p.max_chunks * g.H * g.K * g.V * 2);   // bf16 tiles
+    float *fm = nullptr;
+    if (p.cp && p.cp_forced && !g.cu) {
+        const int nc = std::max(g.nc_fixed, 1);
+        const long long segs =
+            (long long)g.B * (p.seg_chunks_arg > 0 ? (nc + p.seg_chunks_arg - 1) / p.seg_chunks_arg
+                                                   : std::min(64, nc));
+        fm = (float *)take((size_t)segs * g.H * g.K * g.K * sizeof(float));
+    }
     if (base) {
+        p.ws.fwd_maps = fm;
         p.ws.gam = gam;
         p.ws.w = w;
         p.ws.u = u;

@@ -22,6 +22,8 @@ struct Ws {
     int32_t *order = nullptr;      // [N] sequences by chunk count, longest first (varlen)
     int32_t *warm = nullptr;       // [N, H] warmup decision
     float *maps = nullptr;         // [segs, H, K, K+V] affine maps
+    float *fwd_maps = nullptr;     // [segs, H, K, K] A parts of the forward's segment maps kept in
+                                   // a saved context (sequence parallelism forced, fixed length)
     float *seg_state = nullptr;    // [segs, H, K, V] segment start states / end gradients
     float *hc = nullptr;           // chunk start states (bwd): fp32 [chunks, H, K, V] (CUDA
                                    // cores) or bf16 H^T tiles [chunk][H][k half][v][64] (tensor cores)
@@ -41,6 +43,8 @@ struct Plan {
     int max_chunks = 0;         // chunk capacity (>= actual)
     int max_segs = 0;           // segment capacity under CP
     int cp = 0;
+    int cp_forced = 0;          // cp_mode == GDN_CP_FORCE (device independent)
+    int seg_chunks_arg = 0;     // cp_segment_chunks as given (0: chosen here)
     int warm_chunks = 0;
     float warm_tau = 0.f;
     int sms = 0;
@@ -96,7 +100,9 @@ cudaError_t forward(const Plan &p, cudaStream_t s);
 cudaError_t backward(const Plan &p, cudaStream_t s);
 cudaError_t warm_decide(const Plan &p, cudaStream_t s);
 cudaError_t cp_scan(const Plan &p, const int32_t *warm, cudaStream_t s);
-cudaError_t cp_rscan(const Plan &p, cudaStream_t s);
+// fwd_maps: NULL, or the A parts of the forward's segment maps ([segs, H, K,
+// K], from a saved context); their transposes are the reverse maps' A'.
+cudaError_t cp_rscan(const Plan &p, cudaStream_t s, const float *fwd_maps = nullptr);
 // Chunk-local gradients from p.ws.hc / p.ws.dhc; W and u read as bf16 when ws_bf16.
 cudaError_t local_grads(const Plan &p, cudaStream_t s, bool ws_bf16);
 // Gate backward: dg (with respect to the log decay) becomes the gradient with

@@ -311,10 +311,14 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-template <int K>
+// maps_a holds the A parts, K rows of lda floats per (segment, head) (maps
+// itself with lda = K + V, or a separate [segs, H, K, K] array with lda = K).
+// TA: apply the transpose of each A instead (the backward with a saved forward
+// context, whose forward A maps are the reverse ones transposed).
+template <int K, bool TA>
 __global__ void __launch_bounds__(256)
-map_scan_kernel(Geo g, const float *maps, const float *init, const int32_t *warm, float *out,
-                int reverse) {
+map_scan_kernel(Geo g, const float *maps, const float *maps_a, int lda, const float *init,
+                const int32_t *warm, float *out, int reverse) {
     pdl_enter();
     const int n = blockIdx.x, h = blockIdx.y, col0 = blockIdx.z * kSB, V = g.V, H = g.H;
     if (n >= g.N || col0 >= V) return;
@@ -330,13 +334,14 @@ map_scan_kernel(Geo g, const float *maps, const float *init, const int32_t *warm
     const int t = threadIdx.x, kh = t >> 7, r2 = (t & 127) >> 1, jq = (t & 1) * 4;
     auto stage = [&](int step, int buf) {
         const int j = reverse ? nseg - 1 - step : step;
-        const float *M = maps + ((long long)(sbase + j) * H + h) * K * (K + V);
+        const long long sh = (long long)(sbase + j) * H + h;
+        const float *M = maps + sh * K * (K + V), *MA = maps_a + sh * K * lda;
         float *A = Abuf + buf * K * ld, *Bm = Bbuf + buf * K * kSB;
         constexpr int per_row = K / 4;
 #pragma unroll
         for (int m = 0; m < K * per_row / 256; ++m) {
             const int idx = t + 256 * m, row = idx / per_row, c4 = idx % per_row;
-            cp_async16(A + row * ld + 4 * c4, M + (long long)row * (K + V) + 4 * c4);
+            cp_async16(A + row * ld + 4 * c4, MA + (long long)row * lda + 4 * c4);
         }
         if (t < K * (kSB / 4)) {
             const int row = t / (kSB / 4), c4 = t % (kSB / 4);
@@ -379,8 +384,14 @@ map_scan_kernel(Geo g, const float *maps, const float *init, const int32_t *warm
                     s4[e] = *reinterpret_cast<const float4 *>(&S[(l + e) * kSB + jq]);
 #pragma unroll
                 for (int m = 0; m < R; ++m) {
-                    const float4 a4 = *reinterpret_cast<const float4 *>(A + (r2 + 64 * m) * ld + l);
-                    const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+                    float av[4];
+                    if (TA) {            // A^T[row][l + e] = A[l + e][row]
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) av[e] = A[(l + e) * ld + r2 + 64 * m];
+                    } else {
+                        const float4 a4 = *reinterpret_cast<const float4 *>(A + (r2 + 64 * m) * ld + l);
+                        av[0] = a4.x; av[1] = a4.y; av[2] = a4.z; av[3] = a4.w;
+                    }
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         acc[m].x += av[e] * s4[e].x;
@@ -1041,8 +1052,8 @@ static cudaError_t forward_t(const Plan &p, cudaStream_t s, bool states_only) {
         }
         GDN_LAUNCH("simt_walk_map", (walk_kernel<TI, kMap>), dim3(p.max_segs, H, (K + V) / kBV), walk_smem(K), s,
                    g, a);
-        GDN_LAUNCH_PDL("map_scan", (K == 128 ? map_scan_kernel<128> : map_scan_kernel<64>), dim3(g.N, H, V / kSB), map_scan_smem(K), s, g,
-                   (const float *)p.ws.maps, p.h0, (const int32_t *)a.warm, p.ws.seg_state, 0);
+        GDN_LAUNCH_PDL("map_scan", (K == 128 ? map_scan_kernel<128, false> : map_scan_kernel<64, false>), dim3(g.N, H, V / kSB), map_scan_smem(K), s, g,
+                   (const float *)p.ws.maps, (const float *)p.ws.maps, K + V, p.h0, (const int32_t *)a.warm, p.ws.seg_state, 0);
         GDN_LAUNCH(states_only ? "simt_walk_states" : "simt_walk_out", (walk_kernel<TI, kOut>), dim3(p.max_segs, H, V / kBV), walk_smem(K), s, g, a);
     } else {
         GDN_LAUNCH(states_only ? "simt_walk_states" : "simt_walk_out", (walk_kernel<TI, kOut>), dim3(g.N, H, V / kBV), walk_smem(K), s, g, a);
@@ -1096,8 +1107,10 @@ cudaError_t warm_decide(const Plan &p, cudaStream_t s) {
 
 cudaError_t cp_scan(const Plan &p, const int32_t *warm, cudaStream_t s) {
     const Geo &g = p.g;
-    GDN_LAUNCH_PDL("map_scan", (g.K == 128 ? map_scan_kernel<128> : map_scan_kernel<64>), dim3(g.N, g.H, g.V / kSB), map_scan_smem(g.K), s, g,
-               (const float *)p.ws.maps, p.h0, warm, p.ws.seg_state, 0);
+    GDN_LAUNCH_PDL("map_scan", (g.K == 128 ? map_scan_kernel<128, false> : map_scan_kernel<64, false>), dim3(g.N, g.H, g.V / kSB), map_scan_smem(g.K), s, g,
+               (const float *)p.ws.maps,
+               (const float *)(p.ws.fwd_maps ? p.ws.fwd_maps : p.ws.maps),
+               p.ws.fwd_maps ? g.K : g.K + g.V, p.h0, warm, p.ws.seg_state, 0);
     return cudaSuccess;
 }
 
@@ -1150,8 +1163,8 @@ static cudaError_t backward_t(const Plan &p, cudaStream_t s) {
         d.cp = 1;
         GDN_LAUNCH("simt_dwalk_map", (dwalk_kernel<TI, kMap>), dim3(p.max_segs, H, (K + V) / kBV), dwalk_smem(K), s,
                    g, d);
-        GDN_LAUNCH_PDL("map_rscan", (K == 128 ? map_scan_kernel<128> : map_scan_kernel<64>), dim3(g.N, H, V / kSB), map_scan_smem(K), s, g,
-                   (const float *)p.ws.maps, p.dht, (const int32_t *)nullptr, p.ws.seg_state, 1);
+        GDN_LAUNCH_PDL("map_rscan", (K == 128 ? map_scan_kernel<128, false> : map_scan_kernel<64, false>), dim3(g.N, H, V / kSB), map_scan_smem(K), s, g,
+                   (const float *)p.ws.maps, (const float *)p.ws.maps, K + V, p.dht, (const int32_t *)nullptr, p.ws.seg_state, 1);
         GDN_LAUNCH("simt_dwalk_out", (dwalk_kernel<TI, kOut>), dim3(p.max_segs, H, V / kBV), dwalk_smem(K), s, g,
                    d);
     } else {
@@ -1174,10 +1187,17 @@ cudaError_t local_grads(const Plan &p, cudaStream_t s, bool ws_bf16) {
                                     : local_grads_t<float, float, float>(p, s);
 }
 
-cudaError_t cp_rscan(const Plan &p, cudaStream_t s) {
+cudaError_t cp_rscan(const Plan &p, cudaStream_t s, const float *fwd_maps) {
     const Geo &g = p.g;
-    GDN_LAUNCH_PDL("map_rscan", (g.K == 128 ? map_scan_kernel<128> : map_scan_kernel<64>), dim3(g.N, g.H, g.V / kSB), map_scan_smem(g.K), s, g,
-               (const float *)p.ws.maps, p.dht, (const int32_t *)nullptr, p.ws.seg_state, 1);
+    if (fwd_maps) {
+        // A'_j = A_j^T from the forward's A maps ([segs, H, K, K]); B'_j from this
+        // backward's walk
+        GDN_LAUNCH_PDL("map_rscan", (g.K == 128 ? map_scan_kernel<128, true> : map_scan_kernel<64, true>), dim3(g.N, g.H, g.V / kSB), map_scan_smem(g.K), s, g,
+                   (const float *)p.ws.maps, fwd_maps, g.K, p.dht, (const int32_t *)nullptr, p.ws.seg_state, 1);
+    } else {
+        GDN_LAUNCH_PDL("map_rscan", (g.K == 128 ? map_scan_kernel<128, false> : map_scan_kernel<64, false>), dim3(g.N, g.H, g.V / kSB), map_scan_smem(g.K), s, g,
+                   (const float *)p.ws.maps, (const float *)p.ws.maps, g.K + g.V, p.dht, (const int32_t *)nullptr, p.ws.seg_state, 1);
+    }
     return cudaSuccess;
 }
 

@@ -307,6 +307,7 @@ struct TcDWalkArgs {
     const float *seg_end;     // [segs, H, K, V] (CP): gradient at each segment's end
     float *dh0;               // [N, H, K, V] nullable
     float *maps;              // [segs, H, K, K+V] (kDMap)
+    int cb_base;              // kDMap: 1 = only the B' columns (A' comes from the forward's maps)
     int cp;
 };
 
@@ -333,7 +334,7 @@ tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
     extern __shared__ uint8_t smem_raw[];
     S &s = *reinterpret_cast<S *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int tid = threadIdx.x, warp = tid >> 5, cb = blockIdx.z, H = g.H;
+    const int tid = threadIdx.x, warp = tid >> 5, cb = blockIdx.z + a.cb_base, H = g.H;
     int h = blockIdx.y;
     const int v = tid & 127, hs = tid >> 7;
     int n, j = 0, nseg = 1;
@@ -708,13 +709,17 @@ cudaError_t backward(const Plan &p, cudaStream_t s, bool have_ctx) {
         a.cp = 1;
         a.maps = p.ws.maps;
         a.seg_end = p.ws.seg_state;
+        // with the forward's A maps saved, A'_j = A_j^T and only the B' half runs
+        const bool fwd_a = have_ctx && p.ws.fwd_maps != nullptr;
+        a.cb_base = fwd_a ? 1 : 0;
         prof_before("tc_dwalk_map", s);
-        if ((e = launch_pdl(tc_dwalk_kernel<kDMap>, dim3(p.max_segs, g.H, 2), dim3(256), map_smem, s,
-                            m, g, a)) != cudaSuccess)
+        if ((e = launch_pdl(tc_dwalk_kernel<kDMap>, dim3(p.max_segs, g.H, fwd_a ? 1 : 2), dim3(256),
+                            map_smem, s, m, g, a)) != cudaSuccess)
             return e;
         prof_after(s);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        if ((e = simt::cp_rscan(p, s)) != cudaSuccess) return e;
+        a.cb_base = 0;
+        if ((e = simt::cp_rscan(p, s, fwd_a ? p.ws.fwd_maps : nullptr)) != cudaSuccess) return e;
         prof_before("tc_dwalk_out", s);
         if ((e = launch_pdl(tc_dwalk_kernel<kDOut>, dim3(p.max_segs, g.H, 1), dim3(256), smem, s,
                             m, g, a)) != cudaSuccess)

@@ -388,6 +388,7 @@ struct TcWalkArgs {
     float *final_state;       // nullable
     __nv_bfloat16 *hc;        // chunk start states as bf16 H^T tiles [chunk][H][k half][v][64], nullable
     float *maps;              // [segs, H, K, K+V] (kWalkMap)
+    float *maps_a;            // nullable: A columns to [segs, H, K, K] here instead (a saved context)
     __nv_bfloat16 *o;         // [tokens, H, V]: formed inside the output walk when set
     int cp;
 };
@@ -425,8 +426,12 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         walk_unit(g, blockIdx.x, n, h);
         if (n >= g.N) return;
     }
-    if (MODE == kWalkMap && (j == nseg - 1 || (a.warm && a.warm[n * H + h]))) return;
     const bool a_cols = MODE == kWalkMap && cb == 0;   // A columns: start I, u = 0
+    // the forward scan needs no map of the last segment; the backward's reverse
+    // scan does need that segment's A part when it takes it from a saved context
+    if (MODE == kWalkMap &&
+        ((j == nseg - 1 && !(a_cols && a.maps_a)) || (a.warm && a.warm[n * H + h])))
+        return;
     constexpr bool kState = MODE != kWalkMap;         // a state walk (start states, O)
     constexpr bool fused = MODE == kWalkFused;        // O formed here
     const bool states = kState && a.hc != nullptr;
@@ -738,9 +743,16 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             if (pend & 2) mbar_drain(&s.bar_dh, it & 1);
         }
     } else if (MODE == kWalkMap) {
-        float *dst = a.maps + ((long long)(seq_seg_base(g, n) + j) * H + h) * kD * (2 * kD);
+        const long long sh = (long long)(seq_seg_base(g, n) + j) * H + h;
+        if (a_cols && a.maps_a) {
+            float *dst = a.maps_a + sh * kD * kD;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) dst[(64 * hs + i) * (2 * kD) + cb * kD + v] = Hr[i];
+            for (int i = 0; i < 64; ++i) dst[(64 * hs + i) * kD + v] = Hr[i];
+        } else {
+            float *dst = a.maps + sh * kD * (2 * kD);
+#pragma unroll
+            for (int i = 0; i < 64; ++i) dst[(64 * hs + i) * (2 * kD) + cb * kD + v] = Hr[i];
+        }
     } else if (a.final_state && j == nseg - 1) {
         float *dst = a.final_state + ((long long)n * H + h) * kD * kD;
 #pragma unroll
@@ -871,6 +883,7 @@ static cudaError_t run_forward(const Plan &p, cudaStream_t s, bool states_only, 
     if (p.cp) {
         a.cp = 1;
         a.maps = p.ws.maps;
+        a.maps_a = p.ws.fwd_maps;
         a.seg_start = p.ws.seg_state;
         if (p.warm_chunks > 0 && !states_only) {
             if ((e = simt::warm_decide(p, s)) != cudaSuccess) return e;

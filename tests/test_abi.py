@@ -164,3 +164,20 @@ def test_saved_context_exists_only_on_the_tensor_core_path(abi):
     assert 0.5 * per < n < 2 * per
     assert abi.gdn_fwd_ctx_size(_fwd_args(abi, dtype=abi.GDN_FP32, K=128, V=128)) == 0
     assert abi.gdn_fwd_ctx_size(_fwd_args(abi, dtype=abi.GDN_BF16, K=64, V=64)) == 0
+
+
+def test_saved_context_keeps_the_forward_maps_under_forced_sequence_parallelism(abi):
+    """Fixed-length batches with sequence parallelism forced also keep the A
+    parts of the forward's segment maps (fp32 K x K per segment and head), sized
+    for the most segments the forward can choose: 64 per sequence, or the count
+    cp_segment_chunks fixes.  The size depends on the arguments only."""
+    base = dict(dtype=abi.GDN_BF16, K=128, V=128, B=2, T=8192, H=4)
+    off = abi.gdn_fwd_ctx_size(_fwd_args(abi, cp_mode=abi.GDN_CP_OFF, **base))
+    auto = abi.gdn_fwd_ctx_size(_fwd_args(abi, cp_mode=abi.GDN_CP_AUTO, **base))
+    force = abi.gdn_fwd_ctx_size(_fwd_args(abi, cp_mode=abi.GDN_CP_FORCE, **base))
+    fixed = abi.gdn_fwd_ctx_size(_fwd_args(abi, cp_mode=abi.GDN_CP_FORCE, cp_segment_chunks=16,
+                                           **base))
+    maps = lambda segs: base["B"] * segs * base["H"] * 128 * 128 * 4
+    assert off == auto
+    assert force - off == maps(64)
+    assert fixed - off == maps(8192 // 64 // 16)
