@@ -62,6 +62,7 @@ struct LocalSmem {
     uint8_t ds[kTile];         // dS rows r
     uint8_t gs[kTile];         // G rows r
     float gam[64], bet[64], ee[64], ff[64];
+    float dbet[64], dee[64];   // beta and e of the item whose dgam / dbeta are still to come
     float red[16][16], red4[16][16], red5[16][16];
     float zrow[4][64], zprow[4][64], dbA[4][64];   // per column group
     float scan[4][32];         // dg's reverse cumsum
@@ -295,6 +296,48 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
             for (int grp = 0; grp < 3; ++grp) load_group(grp, ci, h, cr.bos);
         issued[0] = issued[1] = issued[2] = 1;
     }
+    // dgam (every exp factor's share) -> dbeta and dg = reverse cumsum of dgam, for
+    // the item at token pbos with pL rows and head ph.  Every thread takes part.
+    auto dg_tail = [&](long long pbos, int pL, int ph) {
+        const float zsum = block_sum(tid < 64 ? s.zpp[tid] : 0.f, s.bsum);
+        if (tid < 64) {
+            const int r = tid;
+            float dgam = 0.f;
+            if (r < pL) {
+                dgam = s.zrow[0][r] + s.zrow[1][r] + s.zrow[2][r] + s.zrow[3][r] +
+                       s.zprow[0][r] + s.zprow[1][r] + s.zprow[2][r] + s.zprow[3][r] + s.zcol[r] +
+                       s.dbet[r] * s.dee[r] * s.yw[r] + scale * s.dee[r] * s.rowA[r] - s.zpp[r];
+                if (r == pL - 1)
+                    dgam += zsum + s.dee[r] * (s.hdot[0] + s.hdot[1] + s.hdot[2] + s.hdot[3]);
+                a.dbeta[(pbos + r) * H + ph] = s.yu[r] + s.dee[r] * s.yw[r] + s.dbA[0][r] +
+                                             s.dbA[1][r] + s.dbA[2][r] + s.dbA[3][r];
+            }
+            s.scan[r >> 5][r & 31] = dgam;
+        }
+        __syncthreads();
+        if (tid < 64) {
+            // dg = reverse cumsum of dgam within the chunk (warp scans over 2 x 32)
+            const int w = tid >> 5;
+            float x = s.scan[1 - w][31 - lane];         // reversed order: position p = 63 - r
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float yv = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += yv;
+            }
+            s.scan[2 + w][lane] = x;
+        }
+        __syncthreads();
+        if (tid < 64) {
+            const int pidx = tid;                        // position in reversed order
+            const int r = 63 - pidx;
+            float x = s.scan[2 + (pidx >> 5)][pidx & 31];
+            if (pidx >= 32) x += s.scan[2][31];
+            if (r < pL) a.dg[(pbos + r) * H + ph] = x;
+        }
+    };
+    bool dg_pending = false;
+    long long dg_bos = 0;
+    int dg_L = 0, dg_h = 0;
     int it = 0, mma_n = 0, diag_n = 0;
     bool bailed = false;
     float pre_g = 0.f, pre_b = 0.f;           // the next item's gam / beta (threads < 64), read early
@@ -354,6 +397,10 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
                 mma_bf16(t_hd, desc_sw128(dl + hh * 2 * kTile + sub, 16, 1024), aH, kKK128, kk > 0);
             }
             mma_commit(&s.mma_bar);
+        }
+        if (dg_pending) {
+            dg_tail(dg_bos, dg_L, dg_h);          // the previous item's, under this wave
+            dg_pending = false;
         }
         ok = mbar_wait(&s.mma_bar, 0, g.spin_limit, g.status);
         if (__syncthreads_or(!ok)) { bailed = true; break; }
@@ -672,43 +719,16 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
                 store_rows8(dk, rs, x, c0 + 8 * q, L);
             }
         }
-        {
-            const float zsum = block_sum(tid < 64 ? s.zpp[tid] : 0.f, s.bsum);
-            if (tid < 64) {
-                const int r = tid;
-                float dgam = 0.f;
-                if (r < L) {
-                    dgam = s.zrow[0][r] + s.zrow[1][r] + s.zrow[2][r] + s.zrow[3][r] +
-                           s.zprow[0][r] + s.zprow[1][r] + s.zprow[2][r] + s.zprow[3][r] + s.zcol[r] +
-                           s.bet[r] * s.ee[r] * s.yw[r] + scale * s.ee[r] * s.rowA[r] - s.zpp[r];
-                    if (r == L - 1)
-                        dgam += zsum + s.ee[r] * (s.hdot[0] + s.hdot[1] + s.hdot[2] + s.hdot[3]);
-                    a.dbeta[(bos + r) * H + h] = s.yu[r] + s.ee[r] * s.yw[r] + s.dbA[0][r] +
-                                                 s.dbA[1][r] + s.dbA[2][r] + s.dbA[3][r];
-                }
-                s.scan[r >> 5][r & 31] = dgam;
-            }
-            __syncthreads();
-            if (tid < 64) {
-                // dg = reverse cumsum of dgam within the chunk (warp scans over 2 x 32)
-                const int w = tid >> 5;
-                float x = s.scan[1 - w][31 - lane];         // reversed order: position p = 63 - r
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const float yv = __shfl_up_sync(0xffffffffu, x, o);
-                    if (lane >= o) x += yv;
-                }
-                s.scan[2 + w][lane] = x;
-            }
-            __syncthreads();
-            if (tid < 64) {
-                const int pidx = tid;                        // position in reversed order
-                const int r = 63 - pidx;
-                float x = s.scan[2 + (pidx >> 5)][pidx & 31];
-                if (pidx >= 32) x += s.scan[2][31];
-                if (r < L) a.dg[(bos + r) * H + h] = x;
-            }
+        // dgam, dbeta and dg of this item come during the next item's first wave (they
+        // read only this item's row sums, kept until then, and copies of beta and e)
+        if (tid < 64) {
+            s.dbet[tid] = s.bet[tid];
+            s.dee[tid] = s.ee[tid];
         }
+        dg_pending = true;
+        dg_bos = bos;
+        dg_L = L;
+        dg_h = h;
         item += (int)gridDim.x;
         ci = ci_n;
         h = h_n;
@@ -717,6 +737,7 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
         ++it;
     }
 
+    if (!bailed && dg_pending) dg_tail(dg_bos, dg_L, dg_h);   // the last item's
     if (bailed && tid == 0) {
         // loads of this item (issued, not yet seen) or of the next one, and the last MMA phase
         for (int grp = 0; grp < 3; ++grp)
