@@ -87,21 +87,35 @@ def kernel_bytes_per_token_head(name, K, V, e=2, eg=GRAD_BYTES):
 
 # DRAM bytes per token-head (dram__bytes_read.sum + dram__bytes_write.sum of one
 # launch, divided by the token-heads it processed) from one ncu capture of the
-# named kernel on the named workload; valid while the kernel's source file
-# still hashes to `sha256` (otherwise reported as null).  The kernels' traffic
-# grows in proportion to the token-heads processed, so it is scaled to the
-# benchmarked launch.
-NCU_TRAFFIC = {}
+# named kernel on the named workload; valid while the sources it was built from
+# still hash to `sha256` (sha256 over the files in order; otherwise reported as
+# null).  The kernels' traffic grows in proportion to the token-heads processed,
+# so it is scaled to the benchmarked launch.
+NCU_TRAFFIC = {
+    # training workload (B=4 T=4096 H=32, 524,288 token-heads): 1,547,878,000 B
+    # read + 768,460,800 B written in the captured launch
+    "tc_local_grad": {"bytes_per_token_head": 2316338800 / 524288, "workload": "training",
+                      "K": 128, "V": 128,
+                      "files": ["gdn_tc_local.cu", "tc_ptx.cuh", "gdn_common.cuh"],
+                      "sha256": "35d7599eaca6fb04cbaf1768966baeaf669474d5e61e4c0511d2ea703aa8d155"},
+}
 
 
-def measured_traffic_per_th(name):
+def sources_digest(files):
     import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "gated_deltanet_linear_bwd_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic_per_th(name, K, V):
     rec = NCU_TRAFFIC.get(name)
-    if not rec:
+    if not rec or (rec["K"], rec["V"]) != (K, V):
         return None, None
-    src = os.path.join(ROOT, "gated_deltanet_linear_bwd_gb300", "csrc", rec["file"])
     try:
-        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        digest = sources_digest(rec["files"])
     except OSError:
         return None, None
     if digest != rec["sha256"]:
@@ -411,7 +425,7 @@ def dominant_roofline(prof, p, e_in, rt, peaks_src):
                 "peak": rt["hbm"], "frac": None, "traffic": None,
                 "avg_launch_ms": avg_s * 1e3}
     alg, ovh = b[0] * th, b[1] * th
-    tr_th, tr_wl = measured_traffic_per_th(name)
+    tr_th, tr_wl = measured_traffic_per_th(name, p.K, p.V)
     traffic = None if tr_th is None else tr_th * th
     achieved = alg / avg_s / 1e9
     return {"kernel": name, "bound": "hbm", "unit": "GB/s", "achieved": achieved,
