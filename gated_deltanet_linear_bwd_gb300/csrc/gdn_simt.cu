@@ -443,23 +443,28 @@ static size_t map_scan_smem(int K) {
 // segment is dominated by the last wc chunks (each step I - beta k k^T has
 // norm <= 1 for unit keys and beta in [0, 1]).  Sliding-window warmup as on
 // the ollai.cn page ("FlashQLA的技术原理", third item).
+// One CTA per (sequence, head); warp w sums the windows of segments
+// j = 1 + w, 1 + w + warps, ... and the CTA takes the AND over all of them.
 __global__ void warm_decide_kernel(Geo g, int wc, float tau, int32_t *warm, int32_t *stats) {
-    const int n = blockIdx.x;
+    const int n = blockIdx.x / g.H, h = blockIdx.x % g.H;
     if (n >= g.N) return;
     long long bos;
     int len;
     seq_range(g, n, bos, len);
     const int nseg = seq_nsegs(g, n);
     const float lt = logf(tau);
-    for (int h = threadIdx.x; h < g.H; h += blockDim.x) {
-        int ok = nseg > 1;
-        for (int j = 1; j < nseg && ok; ++j) {
-            const int t1 = min(len, j * g.seg_chunks * kChunk);
-            const int t0 = max(0, t1 - wc * kChunk);
-            float s = 0.f;
-            for (int t = t0; t < t1; ++t) s += decay_at(g, (bos + t) * g.H + h, h);
-            ok = s < lt;
-        }
+    const int lane = threadIdx.x & 31, warps = blockDim.x >> 5;
+    int ok = nseg > 1;
+    for (int j = 1 + (threadIdx.x >> 5); j < nseg && ok; j += warps) {
+        const int t1 = min(len, j * g.seg_chunks * kChunk);
+        const int t0 = max(0, t1 - wc * kChunk);
+        float s = 0.f;
+        for (int t = t0 + lane; t < t1; t += 32) s += decay_at(g, (bos + t) * g.H + h, h);
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        ok = s < lt;
+    }
+    ok = __syncthreads_and(ok);
+    if (threadIdx.x == 0) {
         warm[n * g.H + h] = ok;
         if (stats) {
             if (ok) atomicAdd(stats, 1);
@@ -1042,7 +1047,7 @@ static cudaError_t forward_t(const Plan &p, cudaStream_t s, bool states_only) {
         a.seg_start = p.ws.seg_state;
         if (p.warm_chunks > 0 && !states_only) {
             prof_before("warm_decide", s);
-            warm_decide_kernel<<<g.N, 128, 0, s>>>(g, p.warm_chunks, p.warm_tau, p.ws.warm,
+            warm_decide_kernel<<<g.N * g.H, 128, 0, s>>>(g, p.warm_chunks, p.warm_tau, p.ws.warm,
                                                  p.cp_stats);
             prof_after(s);
             cudaError_t e = cudaGetLastError();
@@ -1099,7 +1104,7 @@ cudaError_t gate_bwd(const Plan &p, const float *gate_scale, float *d_gate_scale
 
 cudaError_t warm_decide(const Plan &p, cudaStream_t s) {
     prof_before("warm_decide", s);
-    warm_decide_kernel<<<p.g.N, 128, 0, s>>>(p.g, p.warm_chunks, p.warm_tau, p.ws.warm,
+    warm_decide_kernel<<<p.g.N * p.g.H, 128, 0, s>>>(p.g, p.warm_chunks, p.warm_tau, p.ws.warm,
                                              p.cp_stats);
     prof_after(s);
     return cudaGetLastError();
