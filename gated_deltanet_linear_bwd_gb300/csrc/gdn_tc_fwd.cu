@@ -45,7 +45,7 @@ struct PrepSmem {
                                    // every bank; reused for bw/bu below
     alignas(16) float gam[2][64], bet[2][64], brk[2][64], eg[2][64], wsum[4];   // eg: e^(g_i)
     float gpre[2][64], bpre[2][64];  // g and beta of the item, fetched during the previous one
-    uint64_t tma_bar, mma_bar;
+    uint64_t k_bar, v_bar, mma_bar;
     uint32_t tmem_base;
 };
 
@@ -95,9 +95,9 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float *x) {
 }
 
 // Persistent over (chunk pair, head) items with a stride of the grid, two
-// CTAs per SM.  The next item's K and V tiles are fetched as soon as the W/u
-// products have read the current ones; W^T and u^T leave through the dead A
-// region in two TMA-stored passes.
+// CTAs per SM.  The next item's K tile is fetched as soon as the W/u products
+// have read the current one, its V tile at the start of its turn; W^T and u^T
+// leave by TMA store from the dead A region and the dead V tile.
 __global__ void __launch_bounds__(128, 2)
 tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_u,
@@ -120,14 +120,16 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         if (!hb) rb = ra;
         return true;
     };
-    auto load_kv = [&](int hh, const ChunkRef &ra, const ChunkRef &rb) {
-        mbar_arrive_expect_tx(&s.tma_bar, 8 * kTile);
+    // K and V of an item land on their own barriers: V's tile doubles as the u^T
+    // staging area of the previous item, so its load waits until those stores
+    // have read it
+    auto load_x = [&](const CUtensorMap *map, uint8_t *dst, uint64_t *bar, int hh,
+                      const ChunkRef &ra, const ChunkRef &rb) {
+        mbar_arrive_expect_tx(bar, 4 * kTile);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-            tma_load_3d(s.k + half * 2 * kTile, &tm_k, &s.tma_bar, half * 64, hh, (int)ra.bos);
-            tma_load_3d(s.k + half * 2 * kTile + kTile, &tm_k, &s.tma_bar, half * 64, hh, (int)rb.bos);
-            tma_load_3d(s.v + half * 2 * kTile, &tm_v, &s.tma_bar, half * 64, hh, (int)ra.bos);
-            tma_load_3d(s.v + half * 2 * kTile + kTile, &tm_v, &s.tma_bar, half * 64, hh, (int)rb.bos);
+            tma_load_3d(dst + half * 2 * kTile, map, bar, half * 64, hh, (int)ra.bos);
+            tma_load_3d(dst + half * 2 * kTile + kTile, map, bar, half * 64, hh, (int)rb.bos);
         }
     };
 
@@ -141,7 +143,8 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     };
 
     if (tid == 0) {
-        mbar_init(&s.tma_bar, 1);
+        mbar_init(&s.k_bar, 1);
+        mbar_init(&s.v_bar, 1);
         mbar_init(&s.mma_bar, 1);
         fence_barrier_init();
     }
@@ -158,9 +161,9 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     ChunkRef ra, rb;
     bool has_b = false;
     bool have = item_ref(item, pair, h, ra, rb, has_b);
-    if (have && tid == 0) load_kv(h, ra, rb);
+    if (have && tid == 0) load_x(&tm_k, s.k, &s.k_bar, h, ra, rb);
     if (have) fetch_gb(h, ch ? rb : ra, !ch || has_b);
-    int loads = have ? 1 : 0;                 // TMA loads issued (uniform bookkeeping)
+    int k_loads = have ? 1 : 0, v_loads = 0;  // TMA loads issued (uniform bookkeeping)
     int it = 0, mma_n = 0;
     bool bailed = false;
     while (have) {
@@ -170,7 +173,11 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         const bool have_next = item_ref(item + (int)gridDim.x, pair_n, h_n, ra_n, rb_n, has_b_n);
         const ChunkRef &mine = ch ? rb : ra;
         const int L = (ch && !has_b) ? 0 : mine.len;
-        if (tid == 0) bulk_wait_read();       // the previous item's u^T stores have read the A region
+        if (tid == 0) {
+            bulk_wait_read();                 // the previous item's W^T / u^T stores have read
+            load_x(&tm_v, s.v, &s.v_bar, h, ra, rb);   // the A region and the V tile
+        }
+        ++v_loads;
         tc_fence_before();
         __syncthreads();
         // gam = cumsum(g), beta (zero beyond the chunk)
@@ -183,7 +190,7 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         s.bet[ch][r] = r < L ? s.bpre[ch][r] : 0.f;
         if (r < L) ws_gam[tok * H + h] = gam;
 
-        bool ok = mbar_wait(&s.tma_bar, it & 1, g.spin_limit, g.status);
+        bool ok = mbar_wait(&s.k_bar, it & 1, g.spin_limit, g.status);
         if (__syncthreads_or(!ok)) { bailed = true; break; }
         ++mma_n;
         if (warp == 0) {
@@ -388,7 +395,8 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             }
         }
         fence_proxy_async();
-        __syncthreads();
+        ok = mbar_wait(&s.v_bar, it & 1, g.spin_limit, g.status);
+        if (__syncthreads_or(!ok)) { bailed = true; break; }
         ++mma_n;
         if (warp == 0) {
             tc_fence_after();
@@ -410,29 +418,27 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         }
         ok = mbar_wait(&s.mma_bar, 1, g.spin_limit, g.status);
         if (__syncthreads_or(!ok)) { bailed = true; break; }
-        // K and V are dead: the next item's
+        // K is dead: the next item's (its V follows once the u^T stores below have
+        // read the V tile)
         if (tid == 0 && have_next) {
             fence_proxy_async();
-            load_kv(h_n, ra_n, rb_n);
+            load_x(&tm_k, s.k, &s.k_bar, h_n, ra_n, rb_n);
         }
         if (have_next) {
-            ++loads;
+            ++k_loads;
             fetch_gb(h_n, ch ? rb_n : ra_n, !ch || has_b_n);
         }
         tc_fence_after();
         // thread t = feature index (dk for W, dv for u): its 64 chunk rows form row t
-        // of the W^T / u^T tile, staged swizzled in the dead A region (two tiles of
-        // [128 rows][128 B] per pass) and stored by TMA
+        // of the W^T / u^T tile, staged swizzled (two tiles of [128 rows][128 B] each)
+        // in the dead A region (W^T) and the dead V tile (u^T), and stored by TMA
 #pragma unroll 1
         for (int pass = 0; pass < 2; ++pass) {
-            if (pass == 1) {
-                if (tid == 0) bulk_wait_read();   // the W^T tiles have been read
-                __syncthreads();
-            }
+            uint8_t *base = pass ? s.v : stage;
 #pragma unroll 1
             for (int c = 0; c < 2; ++c) {
                 const int Lc = (c && !has_b) ? 0 : (c ? rb.len : ra.len);
-                uint8_t *tile = stage + c * 2 * kTile;
+                uint8_t *tile = base + c * 2 * kTile;
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     float x[32];
@@ -442,15 +448,16 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                     st_row32(tile, tid, 32 * half, x);
                 }
             }
-            fence_proxy_async();
-            __syncthreads();
-            if (tid == 0) {
+        }
+        fence_proxy_async();
+        __syncthreads();
+        if (tid == 0) {
+            for (int pass = 0; pass < 2; ++pass)
                 for (int c = 0; c < (has_b ? 2 : 1); ++c) {
                     const int row = (int)(((long long)(2 * pair + c) * H + h) * kD);
-                    tma_store_2d(pass ? &tm_u : &tm_w, stage + c * 2 * kTile, 0, row);
+                    tma_store_2d(pass ? &tm_u : &tm_w, (pass ? s.v : stage) + c * 2 * kTile, 0, row);
                 }
-                bulk_commit();
-            }
+            bulk_commit();
         }
         item += (int)gridDim.x;
         pair = pair_n;
@@ -462,7 +469,8 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         ++it;
     }
     if (bailed && tid == 0) {
-        if (loads > 0) mbar_drain(&s.tma_bar, (loads - 1) & 1);
+        if (k_loads > 0) mbar_drain(&s.k_bar, (k_loads - 1) & 1);
+        if (v_loads > 0) mbar_drain(&s.v_bar, (v_loads - 1) & 1);
         if (mma_n > 0) mbar_drain(&s.mma_bar, (mma_n - 1) & 1);
     }
     if (tid == 0) bulk_wait_read();
