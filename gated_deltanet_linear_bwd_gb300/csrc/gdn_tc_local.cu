@@ -466,36 +466,21 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
         ok = mbar_wait(&s.mma_bar, 1, g.spin_limit, g.status);
         if (__syncthreads_or(!ok)) { bailed = true; break; }
         tc_fence_after();
-        {
-            // every feature f = v: dYw^T, dYu^T rows into the dead dHL^T tiles, and
-            // sums over k of (diag(f) U dHL^T) .* K (zpp); yw and yu come from wave 2.5
-            const uint8_t *krow = s.qk + (v >> 6) * 2 * kTile + kTile;
-            // dV = diag(beta) dYu leaves now; a warp's lanes write 32 consecutive features
-            TG *dv = (TG *)a.dv + (bos * H + h) * (long long)kD + v;
-#pragma unroll 1
-            for (int q = 0; q < 2; ++q) {
-                float yw[8], yu[8], pz[8];
-                tmem_ld8x3(tmem_addr(t_yw, warp, c0 + 8 * q), tmem_addr(t_yu, warp, c0 + 8 * q),
-                           tmem_addr(t_dkh, warp, c0 + 8 * q), yw, yu, pz);
-                st_row8(dywT, v, cq + q, yw);
-                st_row8(dyuT, v, cq + q, yu);
-                float dvq[8];
+        // every feature f = v: dYw^T, dYu^T rows into the dead dHL^T tiles first, so
+        // that wave 2.5 can start; dV and the sums over k of (diag(f) U dHL^T) .* K
+        // (zpp) follow under it (yu is kept: wave 2.5 overwrites its columns)
+        float yuk[16];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) dvq[e] = s.bet[c0 + 8 * q + e] * yu[e];
-                store_rows8(dv, (long long)H * kD, dvq, c0 + 8 * q, L);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int c = c0 + 8 * q + e;
-                    const float kv = c < L ? ld_bf16(krow, c, v & 63) : 0.f;
-                    pz[e] *= s.ff[c] * kv;           // (diag(f) U dHL^T) .* K, summed over k below
-                }
-                warp_sum8(pz, s.red4[warp] + 8 * q);
-            }
-            tc_fence_before();
-            fence_proxy_async();
-            __syncthreads();
-            if (tid < 64) s.zpp[tid] = quad_sum(s.red4, tid);
+        for (int q = 0; q < 2; ++q) {
+            float yw[8];
+            tmem_ld8x2(tmem_addr(t_yw, warp, c0 + 8 * q), tmem_addr(t_yu, warp, c0 + 8 * q), yw,
+                       yuk + 8 * q);
+            st_row8(dywT, v, cq + q, yw);
+            st_row8(dyuT, v, cq + q, yuk + 8 * q);
         }
+        tc_fence_before();
+        fence_proxy_async();
+        __syncthreads();
         // dO, dU^T, the H0^T / U^T / dW^T tile and T are dead: next item's group 0
         if (have_next) {
             if (tma_thread) {
@@ -531,6 +516,28 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
                          desc_sw128(va + hh * kTile + sub, 16, 1024), kMK, kk > 0);
             }
             mma_commit(&s.diag_bar);
+        }
+        tc_fence_after();
+        {
+            const uint8_t *krow = s.qk + (v >> 6) * 2 * kTile + kTile;
+            // dV = diag(beta) dYu; a warp's lanes write 32 consecutive features
+            TG *dv = (TG *)a.dv + (bos * H + h) * (long long)kD + v;
+            float pz[16];
+            tmem_ld8x2(tmem_addr(t_dkh, warp, c0), tmem_addr(t_dkh, warp, c0 + 8), pz, pz + 8);
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                float dvq[8], pq[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) dvq[e] = s.bet[c0 + 8 * q + e] * yuk[8 * q + e];
+                store_rows8(dv, (long long)H * kD, dvq, c0 + 8 * q, L);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int c = c0 + 8 * q + e;
+                    const float kv = c < L ? ld_bf16(krow, c, v & 63) : 0.f;
+                    pq[e] = pz[8 * q + e] * s.ff[c] * kv;   // (diag(f) U dHL^T) .* K, summed over k
+                }
+                warp_sum8(pq, s.red4[warp] + 8 * q);
+            }
         }
         // While the dA product runs, lanes 0-63 form dS; lanes 64-127 then take
         // the dA epilogue.  Each half reduces into its own array.
@@ -625,7 +632,10 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
             }
             ++issued[1];
         }
-        if (tid < 64) s.zcol[tid] = quad_sum(s.red, tid) + quad_sum(s.red5, tid);
+        if (tid < 64) {
+            s.zcol[tid] = quad_sum(s.red, tid) + quad_sum(s.red5, tid);
+            s.zpp[tid] = quad_sum(s.red4, tid);
+        }
         if (g.l2norm) {
             // The norm's chain rule, dx = (dx^ - x^ <x^, dx^>) / |x| per row, joins
             // wave 3.  The row dots are sums already formed above for dgam:
