@@ -68,7 +68,7 @@ struct LocalSmem {
     float scan[4][32];         // dg's reverse cumsum
     float zcol[64], rowA[64], yw[64], yu[64], zpp[64];
     float hdot[4];             // per-warp parts of <dHL, H0>
-    float bsum[16];            // block_sum scratch
+    float bsum[2];             // the zpp sum's two warp parts
     float rq[64], rk[64];      // 1 / |q_r|, 1 / |k_r| (q, k normalised here)
     uint64_t load_bar[3], mma_bar;  // load groups: {dO, dU^T, H0^T (, T)}, {v, W^T, u^T, dHL^T},
                                     // {q, k (, T when q, k are normalised here)}
@@ -118,17 +118,6 @@ __device__ __forceinline__ void red_combine(float *dst, float (&red)[16][16], bo
         dst[threadIdx.x] = accumulate ? dst[threadIdx.x] + sum : sum;
     }
     __syncthreads();
-}
-
-__device__ __forceinline__ float block_sum(float x, float *scratch16) {
-    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    if ((threadIdx.x & 31) == 0) scratch16[threadIdx.x >> 5] = x;
-    __syncthreads();
-    float s = 0.f;
-#pragma unroll
-    for (int w = 0; w < 16; ++w) s += scratch16[w];
-    __syncthreads();
-    return s;
 }
 
 // 8 bf16 of a 128-byte swizzled row: columns 8 * chunk .. +7.
@@ -297,27 +286,30 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
         issued[0] = issued[1] = issued[2] = 1;
     }
     // dgam (every exp factor's share) -> dbeta and dg = reverse cumsum of dgam, for
-    // the item at token pbos with pL rows and head ph.  Every thread takes part.
+    // the item at token pbos with pL rows and head ph.  Warps 2 and 3 run it (row
+    // r = tid - 64), meeting on named barrier 1, while warp 0 issues the next
+    // item's first wave and the others wait for it.
     auto dg_tail = [&](long long pbos, int pL, int ph) {
-        const float zsum = block_sum(tid < 64 ? s.zpp[tid] : 0.f, s.bsum);
-        if (tid < 64) {
-            const int r = tid;
-            float dgam = 0.f;
-            if (r < pL) {
-                dgam = s.zrow[0][r] + s.zrow[1][r] + s.zrow[2][r] + s.zrow[3][r] +
-                       s.zprow[0][r] + s.zprow[1][r] + s.zprow[2][r] + s.zprow[3][r] + s.zcol[r] +
-                       s.dbet[r] * s.dee[r] * s.yw[r] + scale * s.dee[r] * s.rowA[r] - s.zpp[r];
-                if (r == pL - 1)
-                    dgam += zsum + s.dee[r] * (s.hdot[0] + s.hdot[1] + s.hdot[2] + s.hdot[3]);
-                a.dbeta[(pbos + r) * H + ph] = s.yu[r] + s.dee[r] * s.yw[r] + s.dbA[0][r] +
-                                             s.dbA[1][r] + s.dbA[2][r] + s.dbA[3][r];
-            }
-            s.scan[r >> 5][r & 31] = dgam;
+        const int r = tid - 64, w = r >> 5;
+        float zs = s.zpp[r];
+        for (int o = 16; o > 0; o >>= 1) zs += __shfl_xor_sync(0xffffffffu, zs, o);
+        if (lane == 0) s.bsum[w] = zs;
+        named_sync(1, 64);
+        const float zsum = s.bsum[0] + s.bsum[1];
+        float dgam = 0.f;
+        if (r < pL) {
+            dgam = s.zrow[0][r] + s.zrow[1][r] + s.zrow[2][r] + s.zrow[3][r] +
+                   s.zprow[0][r] + s.zprow[1][r] + s.zprow[2][r] + s.zprow[3][r] + s.zcol[r] +
+                   s.dbet[r] * s.dee[r] * s.yw[r] + scale * s.dee[r] * s.rowA[r] - s.zpp[r];
+            if (r == pL - 1)
+                dgam += zsum + s.dee[r] * (s.hdot[0] + s.hdot[1] + s.hdot[2] + s.hdot[3]);
+            a.dbeta[(pbos + r) * H + ph] = s.yu[r] + s.dee[r] * s.yw[r] + s.dbA[0][r] +
+                                         s.dbA[1][r] + s.dbA[2][r] + s.dbA[3][r];
         }
-        __syncthreads();
-        if (tid < 64) {
+        s.scan[w][lane] = dgam;
+        named_sync(1, 64);
+        {
             // dg = reverse cumsum of dgam within the chunk (warp scans over 2 x 32)
-            const int w = tid >> 5;
             float x = s.scan[1 - w][31 - lane];         // reversed order: position p = 63 - r
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -326,13 +318,13 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
             }
             s.scan[2 + w][lane] = x;
         }
-        __syncthreads();
-        if (tid < 64) {
-            const int pidx = tid;                        // position in reversed order
-            const int r = 63 - pidx;
+        named_sync(1, 64);
+        {
+            const int pidx = r;                          // position in reversed order
+            const int rr = 63 - pidx;
             float x = s.scan[2 + (pidx >> 5)][pidx & 31];
             if (pidx >= 32) x += s.scan[2][31];
-            if (r < pL) a.dg[(pbos + r) * H + ph] = x;
+            if (rr < pL) a.dg[(pbos + rr) * H + ph] = x;
         }
     };
     bool dg_pending = false;
@@ -399,7 +391,7 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
             mma_commit(&s.mma_bar);
         }
         if (dg_pending) {
-            dg_tail(dg_bos, dg_L, dg_h);          // the previous item's, under this wave
+            if (warp == 2 || warp == 3) dg_tail(dg_bos, dg_L, dg_h);   // the previous item's
             dg_pending = false;
         }
         ok = mbar_wait(&s.mma_bar, 0, g.spin_limit, g.status);
@@ -494,10 +486,13 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
         // dYw K^T and dYu V^T, whose diagonals are yw_r = <dYw_r, k_r> and yu_r = <dYu_r, v_r>
         ++mma_n;
         ++diag_n;
-        if (warp == 0) {
+        // issued by two warps of the dA half, which wait for the dA product anyway:
+        // warp 2 the dA product, warp 3 the diagonal products on their own barrier
+        // (so that the dA epilogue need not wait for them)
+        const uint32_t yu = smem_u32(dyuT), yw = smem_u32(dywT);
+        if (warp == 2) {
             tc_fence_after();
-            const uint32_t yu = smem_u32(dyuT), yw = smem_u32(dywT), ua = smem_u32(s.ut),
-                           wa = smem_u32(s.w), qk = smem_u32(s.qk), va = smem_u32(s.v);
+            const uint32_t ua = smem_u32(s.ut), wa = smem_u32(s.w);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 mma_bf16(t_da, desc_sw128(yu + kk * 2048, 0, 1024),
@@ -506,7 +501,9 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
                          desc_sw128(wa + kk * 2048, kTile, 1024), kMM, 1);
             }
             mma_commit(&s.mma_bar);
-            // behind dA on their own barrier, so that the dA epilogue need not wait
+        } else if (warp == 3) {
+            tc_fence_after();
+            const uint32_t qk = smem_u32(s.qk), va = smem_u32(s.v);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 const uint32_t hh = kk >> 2, sub = (kk & 3) * 32;
@@ -747,7 +744,7 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
         ++it;
     }
 
-    if (!bailed && dg_pending) dg_tail(dg_bos, dg_L, dg_h);   // the last item's
+    if (!bailed && dg_pending && (warp == 2 || warp == 3)) dg_tail(dg_bos, dg_L, dg_h);
     if (bailed && tid == 0) {
         // loads of this item (issued, not yet seen) or of the next one, and the last MMA phase
         for (int grp = 0; grp < 3; ++grp)
