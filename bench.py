@@ -75,6 +75,8 @@ def kernel_bytes_per_token_head(name, K, V, e=2, eg=GRAD_BYTES):
         "tc_prep": (e * (K + V) + 8, 4 + 2 * (K + V) + t_mat),
         "tc_walk": (e * K, 2 * (K + V) + 4 + state),
         "tc_walk_fused": (2 * e * K + e * V, 2 * (K + V) + 4 + state),
+        # the one-kernel forward: q, k, v, g, beta in, O out, nothing in between
+        "tc_full_fwd": (e * (2 * K + V) + 8 + e * V, 0),
         "tc_out": (2 * e * K + e * V, 2 * (K + V) + state + 4),
         "tc_bwd_intra": (e * (2 * K + V), 4 + 2 * K + 2 * V),
         "tc_dwalk_out": (e * K + e * V, 2 * K + 2 * K + 2 * V + 4 + state + 2 * V),
@@ -441,6 +443,18 @@ def dominant_roofline(prof, p, e_in, rt, peaks_src):
             "avg_launch_ms": avg_s * 1e3, "launches_per_step": None}
 
 
+def one_kernel_entry(world, tokens, ms, rt, prof, steps, p, e_in):
+    """The forward with fuse_prep set: one kernel (prep inside the walk) where it
+    applies, else the same two-kernel path as `fwd`."""
+    m = statistics.median(ms)
+    return {"value": job_rate(world, tokens, m), "unit": "tokens/s", "ms_per_step": m,
+            "step_roofline_frac": rt["t_fwd"] * 1e3 / m,
+            "kernels": kernel_table(prof, steps, p, e_in),
+            "what": "the forward with fuse_prep=1: W, u and gam made and used inside one "
+                    "kernel where no context is kept, sequence parallelism is off and the "
+                    "(sequence, head) pairs fill the GPU"}
+
+
 def measure_workload(torch, gdn, name, args, timer, dev, peaks, peaks_src, l2, headline=False):
     """Times the fwd+bwd step and the forward of one workload (graph replays)."""
     p = workload_problem(name)
@@ -457,10 +471,13 @@ def measure_workload(torch, gdn, name, args, timer, dev, peaks, peaks_src, l2, h
         raise RuntimeError(f"{name}: device status after warm-up: " + gdn.gdn_last_error())
     step_g, g1 = graphed(torch, dev, lambda: training_step(gdn, d, cp, l2))
     fwd_g, g2 = graphed(torch, dev, lambda: forward_step(gdn, d, cp, l2))
+    # the one-kernel forward (fuse_prep), where it applies; elsewhere the same as fwd_g
+    fwd1_g, g3 = graphed(torch, dev, lambda: forward_step(gdn, d, cp, l2, fuse_prep=True))
     for _ in range(max(args.warmup, 3)):
         step_g()
         fwd_g()
-    res = {"p": p, "d": d, "cp": cp, "e_in": e_in, "tokens": tokens, "graphs": (g1, g2)}
+        fwd1_g()
+    res = {"p": p, "d": d, "cp": cp, "e_in": e_in, "tokens": tokens, "graphs": (g1, g2, g3)}
     clocks = None
     if headline:
         props = torch.cuda.get_device_properties(dev)
@@ -476,14 +493,18 @@ def measure_workload(torch, gdn, name, args, timer, dev, peaks, peaks_src, l2, h
         res["sustained"] = summary(ms_sus)
         res["clocks"] = clocks.stop()
     ms_fwd, _ = timer.run(fwd_g, steps)
+    ms_fwd1, _ = timer.run(fwd1_g, steps)
     # per-kernel times from the library's own CUDA events, in a separate eager pass:
     # events between kernels stop them from overlapping, so they stay out of ms_step
     _, prof = timer.run(lambda: training_step(gdn, d, cp, l2), steps, profile_gdn=gdn)
     _, prof_fwd = timer.run(lambda: forward_step(gdn, d, cp, l2), steps, profile_gdn=gdn)
+    _, prof_fwd1 = timer.run(lambda: forward_step(gdn, d, cp, l2, fuse_prep=True), steps,
+                             profile_gdn=gdn)
     if gdn.gdn_sync_status(st.cuda_stream) != 0:
         raise RuntimeError(f"{name}: device status after the timed region: " +
                            gdn.gdn_last_error())
-    res.update(ms_step=ms_step, ms_fwd=ms_fwd, prof=prof, prof_fwd=prof_fwd)
+    res.update(ms_step=ms_step, ms_fwd=ms_fwd, prof=prof, prof_fwd=prof_fwd, ms_fwd1=ms_fwd1,
+               prof_fwd1=prof_fwd1)
     return res
 
 
@@ -650,7 +671,8 @@ def run_ours(args, rank, world, local):
     # everything the headline line needs, before its tensors are released
     rt = roofline_terms(p, e_in, peaks)
     head = {"ms_step": h["ms_step"], "ms_fwd": h["ms_fwd"], "prof": h["prof"],
-            "prof_fwd": h["prof_fwd"], "sustained": h["sustained"], "clocks": h["clocks"]}
+            "prof_fwd": h["prof_fwd"], "sustained": h["sustained"], "clocks": h["clocks"],
+            "ms_fwd1": h["ms_fwd1"], "prof_fwd1": h["prof_fwd1"]}
     del h, outs, host_out, e2e_g, e2e_graph_obj, d
     torch.cuda.empty_cache()
 
@@ -670,6 +692,8 @@ def run_ours(args, rank, world, local):
                     **summary(x["ms_fwd"]),
                     "step_roofline_frac": xrt["t_fwd"] * 1e3 / ms_f,
                     "t_roof_ms": xrt["t_fwd"] * 1e3},
+            "fwd_one_kernel": one_kernel_entry(world, x["tokens"], x["ms_fwd1"], xrt,
+                                               x["prof_fwd1"], args.steps, xp, x["e_in"]),
             "roofline": dominant_roofline(x["prof"], xp, x["e_in"], xrt, peaks_src),
             "kernels": kernel_table(x["prof"], args.steps, xp, x["e_in"])}
         del x
@@ -690,8 +714,9 @@ def run_ours(args, rank, world, local):
     med_e2e = statistics.median(ms_e2e)
     med_e2e_g = statistics.median(ms_e2e_graph)
     med_gated, med_dec = statistics.median(ms_gated), statistics.median(ms_dec)
-    med_step, med_fwd, med_e2e, med_e2e_g, med_gated, med_dec = max_over_ranks(
-        [med_step, med_fwd, med_e2e, med_e2e_g, med_gated, med_dec], dist, dev)
+    med_fwd1 = statistics.median(head["ms_fwd1"])
+    med_step, med_fwd, med_e2e, med_e2e_g, med_gated, med_dec, med_fwd1 = max_over_ranks(
+        [med_step, med_fwd, med_e2e, med_e2e_g, med_gated, med_dec, med_fwd1], dist, dev)
     if rank != 0:
         if dist:
             dist.destroy_process_group()
@@ -723,6 +748,8 @@ def run_ours(args, rank, world, local):
                                       "frac": rt["t_fwd"] * 1e3 / med_fwd,
                                       "bytes": rt["fwd_bytes"], "flops": rt["fwd_flops"]},
                     "kernels": kernel_table(head["prof_fwd"], args.steps, p, e_in)},
+            "fwd_one_kernel": one_kernel_entry(world, tokens, [med_fwd1], rt, head["prof_fwd1"],
+                                               args.steps, p, e_in),
             "sustained": head["sustained"],
             "step_roofline": {"t_roof_ms": rt["t_step"] * 1e3,
                               "frac": rt["t_step"] * 1e3 / med_step,

@@ -27,7 +27,7 @@ class gdn_fwd_args(ctypes.Structure):
                 ("dtype", _i32), ("scale", _f32), ("use_qk_l2norm", _i32), ("cp_mode", _i32),
                 ("cp_segment_chunks", _i32), ("cp_warmup_chunks", _i32), ("cp_warmup_tau", _f32),
                 ("o", _vp), ("final_state", _vp), ("cp_stats", _vp), ("ctx", _vp),
-                ("gate_scale", _vp)]
+                ("gate_scale", _vp), ("fuse_prep", _i32)]
 
 
 class gdn_bwd_args(ctypes.Structure):

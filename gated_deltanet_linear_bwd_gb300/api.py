@@ -70,12 +70,14 @@ def chunk_gated_delta_rule_fwd(q, k, v, g, beta, scale=None, initial_state=None,
                                output_final_state=True, cu_seqlens=None, use_qk_l2norm=False,
                                cp="auto", cp_segment_chunks=0, cp_warmup_chunks=0,
                                cp_warmup_tau=1e-3, cp_stats=None, save_ctx=False,
-                               gate_scale=None):
+                               gate_scale=None, fuse_prep=False):
     """Low-level forward: returns (o, final_state or None), or
     (o, final_state, ctx) with save_ctx=True, where ctx is the saved-context
     buffer for chunk_gated_delta_rule_bwd (None when the path keeps none).
     With `gate_scale` ([H] fp32, a_h > 0), g holds raw gate logits x and the
-    log decay is -a_h * softplus(x)."""
+    log decay is -a_h * softplus(x).  fuse_prep=True asks for the one-kernel
+    forward where it applies (no ctx kept, no sequence parallelism, enough
+    (sequence, head) pairs to fill the GPU)."""
     a = _abi.gdn_fwd_args()
     B, T, H, K, V, N, dev = _common(a, q, k, v, g, beta, initial_state, cu_seqlens, scale,
                                     use_qk_l2norm, cp, cp_segment_chunks, gate_scale)
@@ -85,6 +87,7 @@ def chunk_gated_delta_rule_fwd(q, k, v, g, beta, scale=None, initial_state=None,
     a.cp_warmup_chunks = int(cp_warmup_chunks)
     a.cp_warmup_tau = float(cp_warmup_tau)
     a.cp_stats = _ptr(cp_stats)
+    a.fuse_prep = int(bool(fuse_prep))
     ctx = None
     if save_ctx:
         nc = _abi.gdn_fwd_ctx_size(a)

@@ -371,6 +371,8 @@ gdn_status gdn_chunk_fwd(const gdn_fwd_args *a, void *ws, size_t ws_bytes, void 
         return fail(GDN_ERR_INVALID_ARG, "outputs must be 16-byte aligned");
     if (a->cp_warmup_chunks < 0 || (a->cp_warmup_chunks > 0 && !(a->cp_warmup_tau > 0.f)))
         return fail(GDN_ERR_INVALID_ARG, "cp_warmup_chunks < 0 or cp_warmup_tau <= 0");
+    if (a->fuse_prep != 0 && a->fuse_prep != 1)
+        return fail(GDN_ERR_INVALID_ARG, "fuse_prep must be 0 or 1");
     Plan p;
     gdn_status st = prepare(common_of(a), false, ws, ws_bytes, p);
     if (st != GDN_OK) return st;
@@ -379,6 +381,7 @@ gdn_status gdn_chunk_fwd(const gdn_fwd_args *a, void *ws, size_t ws_bytes, void 
     p.cp_stats = a->cp_stats;
     p.warm_chunks = p.cp ? a->cp_warmup_chunks : 0;
     p.warm_tau = a->cp_warmup_tau;
+    p.fuse_prep = a->fuse_prep == 1;
     const bool save = a->ctx && tc::supported(p);
     if (save && p.warm_chunks > 0)
         return fail(GDN_ERR_INVALID_ARG,

@@ -46,6 +46,7 @@ struct Plan {
     int cp_forced = 0;          // cp_mode == GDN_CP_FORCE (device independent)
     int seg_chunks_arg = 0;     // cp_segment_chunks as given (0: chosen here)
     int warm_chunks = 0;
+    bool fuse_prep = false;     // the one-kernel forward where it applies
     float warm_tau = 0.f;
     int sms = 0;
     int scratch_ctas = 0;
@@ -115,6 +116,10 @@ namespace tc {
 bool supported(const Plan &p);
 // save: also keep T (p.ws.tmat) and every chunk's start state (p.ws.hc).
 cudaError_t forward(const Plan &p, cudaStream_t s, bool save);
+// The whole forward in one kernel (gdn_tc_full.cu): no sequence parallelism,
+// no saved context, and enough (sequence, head) pairs to fill the GPU.
+bool full_forward_fits(const Plan &p);
+cudaError_t full_forward(const Plan &p, cudaStream_t s);
 // Backward pieces: prep + walk storing chunk start states (p.ws.hc).
 cudaError_t recompute_states(const Plan &p, cudaStream_t s);
 // Chunk-parallel outputs O from the stored chunk start states (after the walk).

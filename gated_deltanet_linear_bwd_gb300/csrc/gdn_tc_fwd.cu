@@ -27,6 +27,7 @@
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
 #include "tc_ptx.cuh"
+#include "gdn_tc_solve.cuh"
 
 namespace gdn {
 namespace tc {
@@ -61,37 +62,6 @@ __device__ __forceinline__ float scan64(float x, float *wsum) {
     __syncthreads();
     if (warp & 1) x += wsum[warp - 1];
     return x;
-}
-
-// Rows I0 .. I0 + N - 1 of Y = T2 X for one column of X (xr = that column): T2
-// is unit lower triangular with T2[i][m] = At[32 + m][32 + i].  I0, N multiples of 4.
-template <int I0, int N>
-__device__ __forceinline__ void t2_times_x(const float (*At)[68], const float *xr, float *y) {
-#pragma unroll
-    for (int i = 0; i < N; ++i) y[i] = xr[I0 + i];
-#pragma unroll
-    for (int m = 0; m < I0 + N - 1; ++m) {
-        const float xm = xr[m];
-        const float4 *tr = reinterpret_cast<const float4 *>(At[32 + m] + 32);
-#pragma unroll
-        for (int i4 = (m + 1 > I0 ? m + 1 : I0) / 4; i4 < (I0 + N) / 4; ++i4) {
-            const float4 a4 = tr[i4];
-            if (4 * i4 + 0 > m) y[4 * i4 + 0 - I0] += a4.x * xm;
-            if (4 * i4 + 1 > m) y[4 * i4 + 1 - I0] += a4.y * xm;
-            if (4 * i4 + 2 > m) y[4 * i4 + 2 - I0] += a4.z * xm;
-            if (4 * i4 + 3 > m) y[4 * i4 + 3 - I0] += a4.w * xm;
-        }
-    }
-}
-
-__device__ __forceinline__ uint4 pack_bf16x8(const float *x) {
-    uint32_t w[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        __nv_bfloat162 b2 = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
-        w[e] = *reinterpret_cast<uint32_t *>(&b2);
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // Persistent over (chunk pair, head) items with a stride of the grid, two
@@ -243,100 +213,13 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         }
         __syncthreads();
         {
-            // T = (I + A)^-1 in 32 x 32 blocks:
-            //   T = [T1 0; T21 T2],  T1 = (I + A11)^-1,  T2 = (I + A22)^-1,  T21 = -T2 A21 T1.
-            // Warp 0 of the chunk solves T1 and warp 1 T2, one column per lane, by
-            // right-looking forward substitution (column j of A = row j of A^T, read by
-            // broadcast); then both form X = A21 T1 (16 of its 32 rows each) and
-            // T21 = -T2 X, with the rows split so that both do the same number of
-            // products.  Each block goes where the A^T region has gone dead:
-            //   T1 column c -> At[c][0..31]       (A11 part of row c; only warp 0 read it)
-            //   T2 column m -> At[32 + m][32..63] (A22 part; only warp 1 read it)
-            //   X column c  -> At[32 + c][0..31]  (upper triangle of A: zero, never read)
+            // T = (I + A)^-1 by both warps of the chunk (32 x 32 blocks)
             float (*At)[68] = s.A[ch];
             const int lane = r & 31, hi = r >> 5, jb = 32 * hi;
-            float t[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) t[i] = (i == lane) ? 1.f : 0.f;
-#pragma unroll
-            for (int j = 0; j < 31; ++j) {
-                const float tj = t[j];
-                const float4 *ar = reinterpret_cast<const float4 *>(At[jb + j] + jb);
-#pragma unroll
-                for (int i4 = (j + 1) / 4; i4 < 8; ++i4) {
-                    const float4 a4 = ar[i4];
-                    if (4 * i4 + 0 > j) t[4 * i4 + 0] -= a4.x * tj;
-                    if (4 * i4 + 1 > j) t[4 * i4 + 1] -= a4.y * tj;
-                    if (4 * i4 + 2 > j) t[4 * i4 + 2] -= a4.z * tj;
-                    if (4 * i4 + 3 > j) t[4 * i4 + 3] -= a4.w * tj;
-                }
-            }
-            __syncwarp();
-            {
-                float4 *dst = reinterpret_cast<float4 *>(At[jb + lane] + jb);
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    dst[q] = make_float4(t[4 * q], t[4 * q + 1], t[4 * q + 2], t[4 * q + 3]);
-            }
-            __syncthreads();
-            {
-                // X = A21 T1: column `lane`, rows 16 hi .. +15  (A21[m][k] = At[k][32 + m],
-                // T1[k][lane] = At[lane][k])
-                float x[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) x[i] = 0.f;
-                const float4 *t1c = reinterpret_cast<const float4 *>(At[lane]);
-#pragma unroll 2
-                for (int k4 = 0; k4 < 8; ++k4) {
-                    const float4 tk = t1c[k4];
-                    const float tkv[4] = {tk.x, tk.y, tk.z, tk.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float4 *ar =
-                            reinterpret_cast<const float4 *>(At[4 * k4 + e] + 32 + 16 * hi);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const float4 a4 = ar[q];
-                            x[4 * q + 0] += a4.x * tkv[e];
-                            x[4 * q + 1] += a4.y * tkv[e];
-                            x[4 * q + 2] += a4.z * tkv[e];
-                            x[4 * q + 3] += a4.w * tkv[e];
-                        }
-                    }
-                }
-                float4 *dst = reinterpret_cast<float4 *>(At[32 + lane] + 16 * hi);
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    dst[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
-            }
-            __syncthreads();
-            // Y = T2 X for column `lane` (T21 = -Y): warp 0 rows 0-7 and 24-31, warp 1 rows 8-23
-            float y[16];
-            {
-                float xr[32];
-                const float4 *xc = reinterpret_cast<const float4 *>(At[32 + lane]);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const float4 x4 = xc[q];
-                    xr[4 * q] = x4.x;
-                    xr[4 * q + 1] = x4.y;
-                    xr[4 * q + 2] = x4.z;
-                    xr[4 * q + 3] = x4.w;
-                }
-                if (hi == 0) {
-                    t2_times_x<0, 8>(At, xr, y);
-                    t2_times_x<24, 8>(At, xr, y + 8);
-                } else {
-                    t2_times_x<8, 16>(At, xr, y);
-                }
-            }
-            // the pieces this thread holds, as (column of T, first row of T, values):
-            //   warp 0: (lane, 0, T1 column), (lane, 32, -y[0..7]), (lane, 56, -y[8..15])
-            //   warp 1: (32 + lane, 0, zeros), (32 + lane, 32, T2 column), (lane, 40, -y[0..15])
+            float t[32], y[16];
+            solve_unit_lower64(At, r, t, y, [] { __syncthreads(); });
             const int cown = jb + lane;               // column of t
             const bool own_ok = cown < L, low_ok = lane < L;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) y[i] = -y[i];
             if (ws_t && (!ch || has_b)) {
                 // the backward keeps T as bf16: row c of the tile [chunk][h][64][64] is
                 // column c of this chunk's T (zero past the chunk's end)
@@ -360,39 +243,9 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             __syncthreads();  // every block done: A's space becomes bw / bu
             // MN-major B operands: row j holds column j of T scaled by beta_j e_j rk_j (W)
             // and by beta_j (u); both scales are zero past the chunk's end.
-            uint8_t *bw = stage + ch * kTile;
-            uint8_t *bu = stage + 2 * kTile + ch * kTile;
-            const float bo = s.bet[ch][cown], wo = __expf(s.gam[ch][cown]) * s.brk[ch][cown];
-            const float bl = s.bet[ch][lane], wl = __expf(s.gam[ch][lane]) * s.brk[ch][lane];
-            float xs[8];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) xs[e] = t[8 * q + e] * wo;
-                st_row8(bw, cown, 4 * hi + q, xs);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) xs[e] = t[8 * q + e] * bo;
-                st_row8(bu, cown, 4 * hi + q, xs);
-            }
-            if (hi) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) xs[e] = 0.f;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    st_row8(bw, cown, q, xs);
-                    st_row8(bu, cown, q, xs);
-                }
-            }
-#pragma unroll
-            for (int p2 = 0; p2 < 2; ++p2) {
-                const int piece = hi ? 5 + p2 : 4 + 3 * p2;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) xs[e] = y[8 * p2 + e] * wl;
-                st_row8(bw, lane, piece, xs);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) xs[e] = y[8 * p2 + e] * bl;
-                st_row8(bu, lane, piece, xs);
-            }
+            store_wu_operands(stage + ch * kTile, stage + 2 * kTile + ch * kTile, r, t, y,
+                              __expf(s.gam[ch][cown]) * s.brk[ch][cown], s.bet[ch][cown],
+                              __expf(s.gam[ch][lane]) * s.brk[ch][lane], s.bet[ch][lane]);
         }
         fence_proxy_async();
         ok = mbar_wait(&s.v_bar, it & 1, g.spin_limit, g.status);
@@ -1048,6 +901,9 @@ static cudaError_t run_forward(const Plan &p, cudaStream_t s, bool states_only, 
 cudaError_t forward(const Plan &p, cudaStream_t s, bool save) {
     cudaError_t e = simt::tables(p, s);
     if (e != cudaSuccess) return e;
+    // asked for, and without a context to keep: the one-kernel forward (prep
+    // inside the walk) for pairs that fill the GPU
+    if (p.fuse_prep && !save && full_forward_fits(p)) return full_forward(p, s);
     return run_forward(p, s, false, save);
 }
 

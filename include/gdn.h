@@ -44,7 +44,7 @@
 extern "C" {
 #endif
 
-#define GDN_ABI_VERSION 3
+#define GDN_ABI_VERSION 4
 
 typedef int32_t gdn_status;
 enum {
@@ -104,6 +104,20 @@ typedef struct gdn_fwd_args {
     const float *gate_scale;    /* NULL: g is the log decay itself.  Else [H] fp32,
                                    a_h > 0, and g holds raw gate logits x: the log
                                    decay is -a_h * softplus(x), softplus(x) = log(1 + e^x) */
+    /* the one-kernel forward ("FlashQLA是什么", ollai.cn, "FlashQLA的核心优势", first
+       item: a fully fused kernel against the split one at large batch) */
+    int32_t fuse_prep;          /* 0 (default): the chunk-local preparation (gam, A,
+                                   T = (I + A)^-1, W, u) and the state walk run as two
+                                   kernels, W and u passing through the workspace.
+                                   1: where the forward keeps no ctx, runs without
+                                   sequence parallelism, and its (sequence, head)
+                                   pairs fill at least three quarters of the SMs
+                                   (bf16, K = V = 128), one kernel does both, so that
+                                   W, u and gam never reach HBM; elsewhere ignored.
+                                   Same results up to rounding; on GB300 the two-kernel
+                                   form is the faster one (the preparation then runs
+                                   beside another CTA's instead of in line with the
+                                   walk).  Other values: GDN_ERR_INVALID_ARG.       */
 } gdn_fwd_args;
 
 typedef struct gdn_bwd_args {

@@ -86,7 +86,7 @@ def _fwd_args(abi, **kw):
 
 
 def test_abi_version_and_workspace_query_need_no_gpu(abi):
-    assert abi.gdn_abi_version() == 3
+    assert abi.gdn_abi_version() == 4
     n_off = abi.gdn_fwd_workspace_size(_fwd_args(abi, cp_mode=abi.GDN_CP_OFF))
     n_cp = abi.gdn_fwd_workspace_size(_fwd_args(abi, cp_mode=abi.GDN_CP_FORCE))
     assert 0 < n_off < n_cp
@@ -113,6 +113,13 @@ def test_bad_arguments_are_rejected_on_the_host(abi, bad, msg):
     rc = abi.load().gdn_chunk_fwd(ctypes.byref(a), ctypes.c_void_p(4096), 1 << 30, None)
     assert rc in (abi.GDN_ERR_INVALID_ARG, abi.GDN_ERR_UNSUPPORTED)
     assert msg in abi.gdn_last_error()
+
+
+def test_bad_fuse_prep_is_rejected_on_the_host(abi):
+    a = _fwd_args(abi, fuse_prep=2)
+    rc = abi.load().gdn_chunk_fwd(ctypes.byref(a), ctypes.c_void_p(4096), 1 << 30, None)
+    assert rc == abi.GDN_ERR_INVALID_ARG
+    assert "fuse_prep" in abi.gdn_last_error()
 
 
 def test_missing_outputs_are_rejected(abi):

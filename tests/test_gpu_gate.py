@@ -4,7 +4,7 @@ aivizor, FLA-flow paragraph); the backward returns the gradient with respect
 to x in dg and the gradient with respect to a_h.  Compared element by element
 with the oracle's gate followed by its recurrence, on the CUDA-core path
 (fp32) and the tensor-core path (bf16, with and without sequence
-parallelism, with a saved forward context)."""
+parallelism, with a saved forward context, and the one-kernel forward)."""
 import numpy as np
 import pytest
 import torch
@@ -16,14 +16,16 @@ from gpu_helpers import TOL, check, lib, to_np
 pytestmark = pytest.mark.gpu
 
 CASES = [
-    ("tiny", dict(T=200, H=2), "off", False),
-    ("training", dict(B=2, T=700, H=2, h0_std=0.1), "off", False),
-    ("training", dict(B=1, T=1500, H=2, h0_std=0.1), "force", True),
+    ("tiny", dict(T=200, H=2), "off", False, False),
+    ("training", dict(B=2, T=700, H=2, h0_std=0.1), "off", False, False),
+    ("training", dict(B=1, T=1500, H=2, h0_std=0.1), "force", True, False),
+    # 128 (sequence, head) pairs, no context: the one-kernel forward
+    ("training", dict(B=2, T=300, H=64, h0_std=0.1), "off", False, True),
 ]
 
 
-@pytest.mark.parametrize("name,kw,cp,ctx", CASES)
-def test_gated_forward_and_backward_match_the_oracle(name, kw, cp, ctx):
+@pytest.mark.parametrize("name,kw,cp,ctx,fuse", CASES)
+def test_gated_forward_and_backward_match_the_oracle(name, kw, cp, ctx, fuse):
     if not torch.cuda.is_available():
         pytest.fail("needs a CUDA GPU")
     p = gdn_synth.make(name, **kw)
@@ -40,7 +42,7 @@ def test_gated_forward_and_backward_match_the_oracle(name, kw, cp, ctx):
     gdn = lib()
     res = gdn.chunk_gated_delta_rule_fwd(d.q, d.k, d.v, xg, d.beta, initial_state=d.h0,
                                          output_final_state=True, cp=cp, save_ctx=ctx,
-                                         gate_scale=ag)
+                                         gate_scale=ag, fuse_prep=fuse)
     o, fs = res[0], res[1]
     saved = res[2] if ctx else None
     dq, dk, dv, dx, db, dh0, da = gdn.chunk_gated_delta_rule_bwd(

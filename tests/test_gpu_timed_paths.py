@@ -100,3 +100,40 @@ def test_long_context_step_as_timed():
     got, names = timed_step(p, True)
     assert {"tc_walk_map", "tc_dwalk_map"} <= names, names
     compare_sampled("long", got, p, heads=[3], batches=None, l2=True)
+
+
+def timed_forward(p, l2, fuse):
+    gdn = lib()
+    d = p.to("cuda")
+    gdn.gdn_profile_begin()
+    o, fs = bench.forward_step(gdn, d, p.meta["cp"], l2, fuse_prep=fuse)
+    torch.cuda.synchronize()
+    names = {n for n, _, _ in gdn.gdn_profile_end()}
+    assert gdn.gdn_sync_status(torch.cuda.current_stream().cuda_stream) == 0
+    return to_np(o), to_np(fs), names
+
+
+@pytest.mark.parametrize("name,heads,batches", [
+    ("training", [1, 20], [2]),
+    ("varlen", [7, 30], None),
+])
+@pytest.mark.parametrize("l2", [False, True])
+@pytest.mark.parametrize("fuse", [False, True])
+def test_forward_as_timed(name, heads, batches, l2, fuse):
+    """The forward bench.py times on its own (no context kept): prep and the
+    walk that forms O, or (fuse_prep) the one-kernel forward."""
+    p = gdn_synth.make(name)
+    o, fs, names = timed_forward(p, l2, fuse)
+    if fuse:
+        assert "tc_full_fwd" in names and not ({"tc_prep", "tc_walk_fused"} & names), names
+    else:
+        assert {"tc_prep", "tc_walk_fused"} <= names and "tc_full_fwd" not in names, names
+    sub = sub_problem(p, heads=heads, batches=batches)
+    ro, rfs = oracle_fwd(sub, l2=l2)
+    x = o if batches is None else o[batches]
+    packed = p.cu_seqlens is not None
+    f = fs if batches is None or packed else fs[batches]
+    tol = TOL[p.meta["dtype"]]
+    e_o = check(f"{name} o", x[:, :, heads], ro, tol)
+    e_s = check(f"{name} final_state", f[:, heads], rfs, tol)
+    print(name, f"o {e_o:.2e} final_state {e_s:.2e}")
