@@ -70,12 +70,13 @@ struct FullArgs {
 // (64-127: Q K^T on lanes 0-63, K K^T on lanes 64-127), the state update
 // (128-255, which first holds W^T and u^T), H^T Q^T and U^T P^T per chunk
 // parity (256 + 128 b, 320 + 128 b).  Per chunk:
-//   1. [Q; K] K^T and H^T Q^T; gam; the norms; the previous chunk's O
+//   1. [Q; K] K^T; gam; the norms; the previous chunk's O
 //   2. A^T rows (lanes 64-127) and P (lanes 0-63)
 //   3. T by warps 0-1, then the W / u operands
 //   4. W^T = K^T (T diag(beta e / |k|))^T, u^T = V^T (T diag(beta))^T into TMEM,
 //      then into shared memory as bf16
-//   5. the walk step: U, U^T diag(f), K^T diag(f) U and U^T P^T, the state update
+//   5. the walk step: U, U^T diag(f), K^T diag(f) U, U^T P^T and H^T Q^T, the state
+//      update
 __global__ void __launch_bounds__(256, 1)
 tc_full_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, Geo g, FullArgs a) {
@@ -182,21 +183,15 @@ tc_full_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (__syncthreads_or(!ok)) { bailed = true; break; }
         tma_pending &= ~(1 << st);
 
-        // ---- 1. [Q; K] K^T and H^T Q^T
+        // ---- 1. [Q; K] K^T (H^T Q^T goes with the state update's group)
         if (warp == 0) {
             tc_fence_after();
-            const uint32_t qk = smem_u32(s.qk[st]), hT = smem_u32(s.hT);
+            const uint32_t qk = smem_u32(s.qk[st]);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 const uint32_t off = (kk >> 2) * 2 * kTile + (kk & 3) * 32;
                 const uint64_t aq = desc_sw128(qk + off, 16, 1024);              // [Q; K]
                 mma_bf16(t_p, aq, desc_sw128(qk + kTile + off, 16, 1024), kIdKK64, kk > 0);
-            }
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t off = (kk >> 2) * 2 * kTile + (kk & 3) * 32;
-                const uint64_t ah = desc_sw128(hT + off, 16, 1024);
-                mma_bf16(t_qh(gb), ah, desc_sw128(qk + off, 16, 1024), kIdKK64, kk > 0);
             }
             mma_commit(&s.bar_q);
         }
@@ -395,6 +390,15 @@ tc_full_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             for (int kk = 0; kk < 4; ++kk)
                 mma_bf16(t_pu(gb), desc_sw128(ua + kk * 32, 16, 1024),
                          desc_sw128(pp + kk * 32, 16, 1024), kIdKK64, kk > 0);
+            // H^T Q^T from this chunk's start state, which the update below overwrites
+            // only after this group completes
+            const uint32_t hT = smem_u32(s.hT), qk = smem_u32(s.qk[st]);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t off = (kk >> 2) * 2 * kTile + (kk & 3) * 32;
+                mma_bf16(t_qh(gb), desc_sw128(hT + off, 16, 1024), desc_sw128(qk + off, 16, 1024),
+                         kIdKK64, kk > 0);
+            }
             mma_commit(&s.bar_dh);
         }
         pend = 8;

@@ -562,14 +562,13 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             mma_commit(&s.bar_u);
             if (fused) {
                 // behind U on their own barrier: the U epilogue need not wait for them
+                // (H^T Q^T, read only by the next chunk's O, goes with the second group)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t off = (kk >> 2) * kKHalf + (kk & 3) * 32;
-                    const uint64_t ah = desc_sw128(hT + (kk >> 2) * 2 * kTile + (kk & 3) * 32, 16, 1024);
                     const uint64_t aq = desc_sw128(qk + off, 16, 1024);           // [Q; K], K-major
                     const uint64_t bk = desc_sw128(qk + kKOff + off, 16, 1024);   // K, K-major
                     mma_bf16(t_p, aq, bk, kIdescKK64, kk > 0);       // rows 0-63: Q K^T
-                    mma_bf16(t_qh(gb), ah, aq, kIdescKK64, kk > 0);  // H^T Q^T (columns 0-63)
                 }
                 mma_commit(&s.bar_q);
             }
@@ -680,12 +679,21 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 mma_bf16(t_dh, au, bk, kIdescDH, kk > 0);
             }
             if (fused) {
-                // U^T P^T: both operands K-major over the chunk rows
+                // U^T P^T: both operands K-major over the chunk rows; H^T Q^T (this
+                // chunk's start state, which the state update overwrites only after
+                // this group completes)
                 const uint32_t ua = smem_u32(s.uT), pp = smem_u32(s.p);
+                const uint32_t hT = smem_u32(s.hT), qk = smem_u32(s.k[st]);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     mma_bf16(t_pu(gb), desc_sw128(ua + kk * 32, 16, 1024),
                              desc_sw128(pp + kk * 32, 16, 1024), kIdescKK64, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (kk >> 2) * kKHalf + (kk & 3) * 32;
+                    mma_bf16(t_qh(gb), desc_sw128(hT + (kk >> 2) * 2 * kTile + (kk & 3) * 32, 16, 1024),
+                             desc_sw128(qk + off, 16, 1024), kIdescKK64, kk > 0);
+                }
             }
             mma_commit(&s.bar_dh);
         }
