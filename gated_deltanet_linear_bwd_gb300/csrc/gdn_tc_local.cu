@@ -70,6 +70,7 @@ struct LocalSmem {
     float hdot[4];             // per-warp parts of <dHL, H0>
     float bsum[2];             // the zpp sum's two warp parts
     float rq[64], rk[64];      // 1 / |q_r|, 1 / |k_r| (q, k normalised here)
+    float dqd[64];             // -<q^_r, dq^_r> (q, k normalised here)
     uint64_t load_bar[3], mma_bar;  // load groups: {dO, dU^T, H0^T (, T)}, {v, W^T, u^T, dHL^T},
                                     // {q, k (, T when q, k are normalised here)}
     uint64_t diag_bar;         // wave 2.5's diagonal products (yw, yu), one phase per item
@@ -130,20 +131,22 @@ __device__ __forceinline__ void ld_row8(const uint8_t *tile, int row, int chunk,
 }
 
 // q and k normalised in place (the library's use_qk_l2norm): row r of the
-// stacked [Q; K] tile of each dk half is scaled by (|x_r|^2 + 1e-6)^-1/2, the
-// two halves' sums of squares joined by a shuffle.  Thread t takes row t / 2,
-// dk half t % 2; it visits its row's 16-byte pieces starting at piece
-// r + 4 (t % 2), so that the 8 threads of each shared-memory phase hit 8
-// different bank groups.  Every element of a row gets the same factor, so the
+// stacked [Q; K] tile of each dk half is scaled by (|x_r|^2 + 1e-6)^-1/2.  All
+// 512 threads take part, four per row: thread t takes row t / 4, dk half
+// (t / 2) % 2 and every other 16-byte piece (odd or even: t % 2), the four
+// threads' sums of squares joined by shuffles.  At each of the four steps the 8
+// threads of a shared-memory phase (two rows, both halves, both parities) visit
+// 8 different bank groups.  Every element of a row gets the same factor, so the
 // 128-byte swizzle plays no part.  Writes 1 / |q_r| to rq, 1 / |k_r| to rk.
 __device__ __forceinline__ void normalise_qk_rows(uint8_t *qk, float *rq, float *rk) {
-    const int t = threadIdx.x, r = t >> 1, hh = t & 1;
+    const int t = threadIdx.x, r = t >> 2, hh = (t >> 1) & 1, sub = t & 1;
+    const int rot = 2 * (r & 1) + hh;
     uint4 *row = reinterpret_cast<uint4 *>(qk + hh * 2 * kTile + r * 128);
-    uint4 x[8];
+    uint4 x[4];
     float ss = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        x[i] = row[(i + r + 4 * hh) & 7];
+    for (int i = 0; i < 4; ++i) {
+        x[i] = row[(2 * (i + rot) + sub) & 7];
         const __nv_bfloat162 *b = reinterpret_cast<const __nv_bfloat162 *>(&x[i]);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -152,18 +155,19 @@ __device__ __forceinline__ void normalise_qk_rows(uint8_t *qk, float *rq, float 
         }
     }
     ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
     const float inv = rsqrtf(ss + 1e-6f);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < 4; ++i) {
         __nv_bfloat162 *b = reinterpret_cast<__nv_bfloat162 *>(&x[i]);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const float2 f = __bfloat1622float2(b[j]);
             b[j] = __floats2bfloat162_rn(f.x * inv, f.y * inv);
         }
-        row[(i + r + 4 * hh) & 7] = x[i];
+        row[(2 * (i + rot) + sub) & 7] = x[i];
     }
-    if (hh == 0) (r < 64 ? rq : rk)[r & 63] = inv;
+    if ((t & 3) == 0) (r < 64 ? rq : rk)[r & 63] = inv;
 }
 
 struct TcLocalArgs {
@@ -361,7 +365,7 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
             // every product and epilogue below then sees q^ = q / |q| and k^ = k / |k|,
             // giving the gradients with respect to q^ and k^; the norm's own chain
             // rule is applied to dq and dk at the end
-            if (tid < 256) normalise_qk_rows(s.qk, s.rq, s.rk);
+            normalise_qk_rows(s.qk, s.rq, s.rk);
             fence_proxy_async();
             __syncthreads();
         }
@@ -648,15 +652,19 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
                 const float zp = s.zprow[0][r] + s.zprow[1][r] + s.zprow[2][r] + s.zprow[3][r];
                 const float dq_dot = zr + scale * s.ee[r] * s.rowA[r];
                 const float dk_dot = -s.zcol[r] + s.zpp[r] + s.bet[r] * s.ee[r] * s.yw[r] + zp;
-#pragma unroll 1
-                for (int chunk = 0; chunk < 8; ++chunk) {
-                    float x[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) x[e] = (8 * chunk + e == r) ? -dq_dot : 0.f;
-                    st_row8(s.tt, r, chunk, x);
-                }
+                s.dqd[r] = -dq_dot;
                 *reinterpret_cast<__nv_bfloat16 *>(s.gs + sw128_off(r, r)) =
                     __float2bfloat16_rn(-0.5f * dk_dot);
+            }
+            __syncthreads();
+            {
+                // the diagonal tile, one 16-byte piece per thread (row tid / 8)
+                const int r = tid >> 3, chunk = tid & 7;
+                const float d = s.dqd[r];
+                float x[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] = (8 * chunk + e == r) ? d : 0.f;
+                st_row8(s.tt, r, chunk, x);
             }
             fence_proxy_async();
             __syncthreads();
@@ -744,6 +752,9 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
         ++it;
     }
 
+    // the last item's tail: after a barrier, since its copies of beta and e were
+    // written after the item's last one
+    __syncthreads();
     if (!bailed && dg_pending && (warp == 2 || warp == 3)) dg_tail(dg_bos, dg_L, dg_h);
     if (bailed && tid == 0) {
         // loads of this item (issued, not yet seen) or of the next one, and the last MMA phase
