@@ -61,3 +61,21 @@ def test_step_does_not_depend_on_buffer_contents(name, kw, l2):
         for i, (x, y) in enumerate(zip(a, b)):
             assert torch.isfinite(x.float()).all(), (step.__name__, i)
             assert torch.equal(x, y), (step.__name__, i, (x.float() - y.float()).abs().max())
+
+
+@pytest.mark.parametrize("l2", [False, True])
+def test_repeated_steps_are_bit_identical(l2):
+    """The same step, twenty times: any ordering race between the kernels' warps
+    shows as a difference (128 walks and 152 persistent local-gradient CTAs,
+    each ending on its own last item)."""
+    gdn = lib()
+    p = gdn_synth.make("training", B=1, T=1024, H=128)
+    d = p.to("cuda")
+    ref = [t.clone() for t in bench.training_step(gdn, d, p.meta["cp"], l2) if t is not None]
+    for rep in range(20):
+        if rep % 2:
+            bench.forward_step(gdn, d, p.meta["cp"], not l2)      # other kernels in between
+        out = [t for t in bench.training_step(gdn, d, p.meta["cp"], l2) if t is not None]
+        torch.cuda.synchronize()
+        for i, (x, y) in enumerate(zip(ref, out)):
+            assert torch.equal(x, y), (rep, i, (x.float() - y.float()).abs().max())
