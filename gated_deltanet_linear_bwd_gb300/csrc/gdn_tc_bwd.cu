@@ -498,24 +498,6 @@ tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
             if (fused) s.egd[tid] = tid > 0 ? __expf(s.gam[st][tid] - s.gam[st][tid - 1]) : 1.f;
         }
         if (fused) {
-            // Qs = diag(scale e^gam) Q (zero past L) from the Q rows of the stage:
-            // thread t scales four 16-byte pieces of row t % 64
-            {
-                const int r = tid & 63;
-                const float f = r < L ? g.scale * __expf(s.gam[st][r]) * (g.l2norm ? s.rqk[r] : 1.f)
-                                      : 0.f;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int pc = 4 * (tid >> 6) + i, half = pc >> 3, chunk = pc & 7;
-                    const uint4 raw = *reinterpret_cast<const uint4 *>(
-                        s.k[st] + half * kKHalf + r * 128 + ((chunk ^ (r & 7)) << 4));
-                    const __nv_bfloat16 *bb = reinterpret_cast<const __nv_bfloat16 *>(&raw);
-                    float x[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) x[e] = f * __bfloat162float(bb[e]);
-                    st_row8(s.qs[0] + half * kTile, r, chunk, x);
-                }
-            }
             ok = mbar_wait(&s.bar_q, par, g.spin_limit, g.status);
             if (__syncthreads_or(!ok)) { bailed = true; break; }
             pend &= ~4;
@@ -538,6 +520,24 @@ tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
                         x[e] = (c <= r && r < L) ? sc * x[e] * dd[8 * q + e] : 0.f;
                     }
                     st_row8(s.p, r, 4 * hs + q, x);
+                }
+            } else {
+                // meanwhile the other warps form Qs = diag(scale e^gam) Q (zero past L)
+                // from the Q rows of the stage: thread u = 0..127 scales eight 16-byte
+                // pieces of row u % 64
+                const int u = (tid & 63) + 64 * (tid >> 7), r = u & 63;
+                const float f = r < L ? g.scale * __expf(s.gam[st][r]) * (g.l2norm ? s.rqk[r] : 1.f)
+                                      : 0.f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int pc = 8 * (u >> 6) + i, half = pc >> 3, chunk = pc & 7;
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(
+                        s.k[st] + half * kKHalf + r * 128 + ((chunk ^ (r & 7)) << 4));
+                    const __nv_bfloat16 *bb = reinterpret_cast<const __nv_bfloat16 *>(&raw);
+                    float x[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) x[e] = f * __bfloat162float(bb[e]);
+                    st_row8(s.qs[0] + half * kTile, r, chunk, x);
                 }
             }
             tc_fence_before();
