@@ -334,6 +334,19 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
     bool dg_pending = false;
     long long dg_bos = 0;
     int dg_L = 0, dg_h = 0;
+    // an item's dq and dk (16 rows each per thread), stored during the next item's
+    // first and second waves, where the warps wait anyway: a warp's lanes write 32
+    // consecutive features of one row per store
+    float dqv[2][8], dkv[2][8];
+    bool st_pending = false;
+    long long st_bos = 0;
+    int st_L = 0, st_h = 0;
+    auto store_grad = [&](void *base, float (&x)[2][8]) {
+        const long long rs = (long long)H * kD;
+        TG *dst = (TG *)base + (st_bos * H + st_h) * (long long)kD + v;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) store_rows8(dst, rs, x[q], c0 + 8 * q, st_L);
+    };
     int it = 0, mma_n = 0, diag_n = 0;
     bool bailed = false;
     float pre_g = 0.f, pre_b = 0.f;           // the next item's gam / beta (threads < 64), read early
@@ -394,6 +407,7 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
             }
             mma_commit(&s.mma_bar);
         }
+        if (st_pending) store_grad(a.dq, dqv);   // the previous item's dq (its dk: under wave 2)
         if (dg_pending) {
             if (warp == 2 || warp == 3) dg_tail(dg_bos, dg_L, dg_h);   // the previous item's
             dg_pending = false;
@@ -458,6 +472,10 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
                 mma_bf16(t_yu, desc_sw128(du + kk * 32, 16, 1024), bT, kKK, kk > 0);
             }
             mma_commit(&s.mma_bar);
+        }
+        if (st_pending) {
+            store_grad(a.dk, dkv);                // the previous item's dk, under this wave
+            st_pending = false;
         }
         ok = mbar_wait(&s.mma_bar, 1, g.spin_limit, g.status);
         if (__syncthreads_or(!ok)) { bailed = true; break; }
@@ -709,31 +727,28 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
         }
         pre = have_next;
         tc_fence_after();
-        {
-            // feature v (= k), chunk rows c0 .. c0+31: a warp's lanes write 32
-            // consecutive features of one row per store
-            const long long rs = (long long)H * kD;
-            TG *dq = (TG *)a.dq + (bos * H + h) * (long long)kD + v;
-            TG *dk = (TG *)a.dk + (bos * H + h) * (long long)kD + v;
-#pragma unroll 1
-            for (int q = 0; q < 2; ++q) {
-                float x[8], y[8], pw[8], x1[8], y1[8];
-                tmem_ld8x5(tmem_addr(t_q1, warp, c0 + 8 * q), tmem_addr(t_q2, warp, c0 + 8 * q),
-                           tmem_addr(t_dk, warp, c0 + 8 * q), tmem_addr(t_dkh, warp, c0 + 8 * q),
-                           tmem_addr(t_yw, warp, c0 + 8 * q), x1, y1, x, y, pw);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int c = c0 + 8 * q + e;
-                    // with q, k normalised here the products above already hold
-                    // dx^ - x^ <x^, dx^>; what is left of the norm's chain rule is 1 / |x|
-                    const float sq = g.l2norm ? s.rq[c] : 1.f, sk = g.l2norm ? s.rk[c] : 1.f;
-                    x1[e] = sq * (scale * s.ee[c] * x1[e] + y1[e]);
-                    x[e] = sk * (x[e] + s.ff[c] * y[e] + s.bet[c] * s.ee[c] * pw[e]);
-                }
-                store_rows8(dq, rs, x1, c0 + 8 * q, L);
-                store_rows8(dk, rs, x, c0 + 8 * q, L);
+        for (int q = 0; q < 2; ++q) {
+            // feature v (= k), chunk rows c0 + 8 q .. +7; kept in registers and stored
+            // during the next item's first two waves
+            float x[8], y[8], pw[8], x1[8], y1[8];
+            tmem_ld8x5(tmem_addr(t_q1, warp, c0 + 8 * q), tmem_addr(t_q2, warp, c0 + 8 * q),
+                       tmem_addr(t_dk, warp, c0 + 8 * q), tmem_addr(t_dkh, warp, c0 + 8 * q),
+                       tmem_addr(t_yw, warp, c0 + 8 * q), x1, y1, x, y, pw);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int c = c0 + 8 * q + e;
+                // with q, k normalised here the products above already hold
+                // dx^ - x^ <x^, dx^>; what is left of the norm's chain rule is 1 / |x|
+                const float sq = g.l2norm ? s.rq[c] : 1.f, sk = g.l2norm ? s.rk[c] : 1.f;
+                dqv[q][e] = sq * (scale * s.ee[c] * x1[e] + y1[e]);
+                dkv[q][e] = sk * (x[e] + s.ff[c] * y[e] + s.bet[c] * s.ee[c] * pw[e]);
             }
         }
+        st_pending = true;
+        st_bos = bos;
+        st_L = L;
+        st_h = h;
         // dgam, dbeta and dg of this item come during the next item's first wave (they
         // read only this item's row sums, kept until then, and copies of beta and e)
         if (tid < 64) {
@@ -755,6 +770,10 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
     // the last item's tail: after a barrier, since its copies of beta and e were
     // written after the item's last one
     __syncthreads();
+    if (!bailed && st_pending) {
+        store_grad(a.dq, dqv);
+        store_grad(a.dk, dkv);
+    }
     if (!bailed && dg_pending && (warp == 2 || warp == 3)) dg_tail(dg_bos, dg_L, dg_h);
     if (bailed && tid == 0) {
         // loads of this item (issued, not yet seen) or of the next one, and the last MMA phase
