@@ -481,8 +481,8 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
         if (__syncthreads_or(!ok)) { bailed = true; break; }
         tc_fence_after();
         // every feature f = v: dYw^T, dYu^T rows into the dead dHL^T tiles first, so
-        // that wave 2.5 can start; dV and the sums over k of (diag(f) U dHL^T) .* K
-        // (zpp) follow under it (yu is kept: wave 2.5 overwrites its columns)
+        // that wave 2.5 can start; the sums over k of (diag(f) U dHL^T) .* K (zpp)
+        // follow under it, dV under wave 3 (yu is kept: wave 2.5 overwrites its columns)
         float yuk[16];
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
@@ -539,16 +539,11 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
         tc_fence_after();
         {
             const uint8_t *krow = s.qk + (v >> 6) * 2 * kTile + kTile;
-            // dV = diag(beta) dYu; a warp's lanes write 32 consecutive features
-            TG *dv = (TG *)a.dv + (bos * H + h) * (long long)kD + v;
             float pz[16];
             tmem_ld8x2(tmem_addr(t_dkh, warp, c0), tmem_addr(t_dkh, warp, c0 + 8), pz, pz + 8);
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
-                float dvq[8], pq[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) dvq[e] = s.bet[c0 + 8 * q + e] * yuk[8 * q + e];
-                store_rows8(dv, (long long)H * kD, dvq, c0 + 8 * q, L);
+                float pq[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int c = c0 + 8 * q + e;
@@ -710,6 +705,18 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
                              desc_sw128(dq + kk * 2048, kTile, 1024), kMM, 1);
             }
             mma_commit(&s.mma_bar);
+        }
+        {
+            // dV = diag(beta) dYu under this wave (yu kept since the second epilogue);
+            // a warp's lanes write 32 consecutive features
+            TG *dv = (TG *)a.dv + (bos * H + h) * (long long)kD + v;
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                float dvq[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) dvq[e] = s.bet[c0 + 8 * q + e] * yuk[8 * q + e];
+                store_rows8(dv, (long long)H * kD, dvq, c0 + 8 * q, L);
+            }
         }
         ok = mbar_wait(&s.mma_bar, 1, g.spin_limit, g.status);
         if (__syncthreads_or(!ok)) { bailed = true; break; }
