@@ -624,7 +624,58 @@ def run_ours(args, rank, world, local):
     for hbuf, t in zip(host_out, [t for t in outs if t is not None]):
         if not torch.equal(hbuf, t.cpu()):
             raise RuntimeError("end-to-end results differ from the device-resident step")
-    # the same end-to-end step captured once as a CUDA graph (no per-call host work)
+    # The same steps as a user's loop would run them: step k + 1's inputs travel up
+    # while step k computes and step k - 1's results travel down (three streams;
+    # inputs at most two steps ahead).  Every step's copies are inside the timed
+    # region, which spans the whole loop; the per-step figure is that time / steps.
+    h2d_stream, d2h_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    fwd_keys = [k for k in ("q", "k", "v", "g", "beta", "h0", "cu_seqlens", "do", "dht")
+                if k in host_in]
+
+    def e2e_pipeline(n):
+        main = torch.cuda.current_stream(dev)
+        h2d_stream.wait_stream(main)          # nothing moves before the timed region opens
+        computed = []
+        for step in range(n):
+            if step >= 2:
+                h2d_stream.wait_event(computed[step - 2])
+            with torch.cuda.stream(h2d_stream):
+                x = {k: host_in[k].to(dev, non_blocking=True) for k in fwd_keys}
+                arrived = torch.cuda.Event()
+                arrived.record(h2d_stream)
+            main.wait_event(arrived)
+            for t in x.values():
+                t.record_stream(main)
+            o, fs, saved = gdn.chunk_gated_delta_rule_fwd(
+                x["q"], x["k"], x["v"], x["g"], x["beta"], initial_state=x.get("h0"),
+                output_final_state=True, cu_seqlens=x.get("cu_seqlens"), use_qk_l2norm=l2,
+                cp=cp, save_ctx=True)
+            grads = gdn.chunk_gated_delta_rule_bwd(
+                x["q"], x["k"], x["v"], x["g"], x["beta"], x["do"], dht=x.get("dht"),
+                initial_state=x.get("h0"), cu_seqlens=x.get("cu_seqlens"), use_qk_l2norm=l2,
+                cp=cp, ctx=saved)
+            done = torch.cuda.Event()
+            done.record(main)
+            computed.append(done)
+            res = [t for t in (o, fs) + tuple(grads) if t is not None]
+            d2h_stream.wait_event(done)
+            with torch.cuda.stream(d2h_stream):
+                for hbuf, t in zip(host_out, res):
+                    hbuf.copy_(t, non_blocking=True)
+            for t in res:
+                t.record_stream(d2h_stream)
+        main.wait_stream(d2h_stream)
+
+    e2e_pipeline(max(args.warmup, 3))
+    ms_pipe = []
+    for _ in range(3):
+        ms, _ = timer.run(lambda: e2e_pipeline(args.steps), 1)
+        ms_pipe.append(ms[0] / args.steps)
+    torch.cuda.synchronize(dev)
+    for hbuf, t in zip(host_out, [t for t in outs if t is not None]):
+        if not torch.equal(hbuf, t.cpu()):
+            raise RuntimeError("pipelined end-to-end results differ from the device-resident step")
+    # the serial end-to-end step captured once as a CUDA graph (no per-call host work)
     e2e_g, e2e_graph_obj = graphed(torch, dev, e2e_step)
     for _ in range(3):
         e2e_g()
@@ -713,10 +764,11 @@ def run_ours(args, rank, world, local):
     med_fwd = statistics.median(head["ms_fwd"])
     med_e2e = statistics.median(ms_e2e)
     med_e2e_g = statistics.median(ms_e2e_graph)
+    med_pipe = statistics.median(ms_pipe)
     med_gated, med_dec = statistics.median(ms_gated), statistics.median(ms_dec)
     med_fwd1 = statistics.median(head["ms_fwd1"])
-    med_step, med_fwd, med_e2e, med_e2e_g, med_gated, med_dec, med_fwd1 = max_over_ranks(
-        [med_step, med_fwd, med_e2e, med_e2e_g, med_gated, med_dec, med_fwd1], dist, dev)
+    med_step, med_fwd, med_e2e, med_e2e_g, med_gated, med_dec, med_fwd1, med_pipe = max_over_ranks(
+        [med_step, med_fwd, med_e2e, med_e2e_g, med_gated, med_dec, med_fwd1, med_pipe], dist, dev)
     if rank != 0:
         if dist:
             dist.destroy_process_group()
@@ -759,15 +811,22 @@ def run_ours(args, rank, world, local):
             "roofline": roof,
             "kernels": kernel_table(prof, args.steps, p, e_in),
             "gpu_launches": int(round(launches_per_step * args.steps)),
-            "e2e": {"value": job_rate(world, tokens, med_e2e), "unit": "tokens/s",
+            "e2e": {"value": job_rate(world, tokens, med_pipe), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": med_e2e, "stats": summary(ms_e2e),
-                    "what": "eager public-API calls every step (fwd keeping its context, bwd), "
-                            "inputs from pinned host memory and every result back to it inside "
-                            "the timed region"},
+                    "ms_per_step": med_pipe, "stats": summary(ms_pipe),
+                    "what": f"{args.steps} steps of eager public-API calls (fwd keeping its "
+                            "context, bwd), every step's inputs from pinned host memory and every "
+                            "result back to it inside the timed region, consecutive steps "
+                            "overlapped as a training loop would (step k+1's inputs in while step "
+                            "k computes and step k-1's results go out); time of the whole loop / "
+                            "steps, three loops"},
+            "e2e_serial": {"value": job_rate(world, tokens, med_e2e), "unit": "tokens/s",
+                           "ms_per_step": med_e2e, "stats": summary(ms_e2e),
+                           "what": "the same step with nothing overlapped across steps: each "
+                                   "step timed alone"},
             "e2e_graph": {"value": job_rate(world, tokens, med_e2e_g), "unit": "tokens/s",
                           "ms_per_step": med_e2e_g,
-                          "what": "the same end-to-end step captured once as a CUDA graph"},
+                          "what": "the serial end-to-end step captured once as a CUDA graph"},
             "gated": {"value": job_rate(world, tokens, med_gated), "unit": "tokens/s",
                       "ms_per_step": med_gated,
                       "what": "the same fwd+bwd step with the decay formed inside from gate "
