@@ -104,8 +104,6 @@ cudaError_t cp_scan(const Plan &p, const int32_t *warm, cudaStream_t s);
 // fwd_maps: NULL, or the A parts of the forward's segment maps ([segs, H, K,
 // K], from a saved context); their transposes are the reverse maps' A'.
 cudaError_t cp_rscan(const Plan &p, cudaStream_t s, const float *fwd_maps = nullptr);
-// Chunk-local gradients from p.ws.hc / p.ws.dhc; W and u read as bf16 when ws_bf16.
-cudaError_t local_grads(const Plan &p, cudaStream_t s, bool ws_bf16);
 // Gate backward: dg (with respect to the log decay) becomes the gradient with
 // respect to the logits in place; d_gate_scale [H] (nullable) gets its sum.
 cudaError_t gate_bwd(const Plan &p, const float *gate_scale, float *d_gate_scale, cudaStream_t s);

@@ -1178,20 +1178,6 @@ static cudaError_t backward_t(const Plan &p, cudaStream_t s) {
     return local_grads_t<TI, TG, float>(p, s);
 }
 
-cudaError_t local_grads(const Plan &p, cudaStream_t s, bool ws_bf16) {
-    typedef __nv_bfloat16 bf;
-    if (ws_bf16) {   // only the tensor-core recompute (bf16 inputs) leaves W, u in bf16
-        if (p.dtype != GDN_BF16) return cudaErrorInvalidValue;
-        return p.grad_dtype == GDN_BF16 ? local_grads_t<bf, bf, bf>(p, s)
-                                        : local_grads_t<bf, float, bf>(p, s);
-    }
-    if (p.dtype == GDN_BF16)
-        return p.grad_dtype == GDN_BF16 ? local_grads_t<bf, bf, float>(p, s)
-                                        : local_grads_t<bf, float, float>(p, s);
-    return p.grad_dtype == GDN_BF16 ? local_grads_t<float, bf, float>(p, s)
-                                    : local_grads_t<float, float, float>(p, s);
-}
-
 cudaError_t cp_rscan(const Plan &p, cudaStream_t s, const float *fwd_maps) {
     const Geo &g = p.g;
     if (fwd_maps) {
