@@ -405,6 +405,14 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
                 // dHL^T H0 (128 x 128): its trace is <dHL, H0>
                 mma_bf16(t_hd, desc_sw128(dl + hh * 2 * kTile + sub, 16, 1024), aH, kKK128, kk > 0);
             }
+            {
+                // T^T dU needs only loaded tiles: with this wave, into columns it leaves free
+                const uint32_t tt = smem_u32(s.tt);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(t_yu, desc_sw128(du + kk * 32, 16, 1024), desc_sw128(tt + kk * 32, 16, 1024),
+                             kKK, kk > 0);
+            }
             mma_commit(&s.mma_bar);
         }
         if (st_pending) store_grad(a.dq, dqv);   // the previous item's dq (its dk: under wave 2)
@@ -452,7 +460,7 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
             red_combine(s.rowA, s.red, false);    // its barriers publish U^T, dW^T and hdot
         }
 
-        // ---------------- wave 2: dO U^T, dHL U^T, T^T dW, T^T dU
+        // ---------------- wave 2: dO U^T, dHL U^T, T^T dW (T^T dU went with wave 1)
         ++mma_n;
         if (warp == 0) {
             tc_fence_after();
@@ -469,7 +477,6 @@ tc_local_kernel(const __grid_constant__ LocalMaps m, Geo g, TcLocalArgs a) {
             for (int kk = 0; kk < 4; ++kk) {
                 const uint64_t bT = desc_sw128(tt + kk * 32, 16, 1024);
                 mma_bf16(t_yw, desc_sw128(dwa + kk * 32, 16, 1024), bT, kKK, kk > 0);
-                mma_bf16(t_yu, desc_sw128(du + kk * 32, 16, 1024), bT, kKK, kk > 0);
             }
             mma_commit(&s.mma_bar);
         }
