@@ -94,12 +94,12 @@ def kernel_bytes_per_token_head(name, K, V, e=2, eg=GRAD_BYTES):
 # null).  The kernels' traffic grows in proportion to the token-heads processed,
 # so it is scaled to the benchmarked launch.
 NCU_TRAFFIC = {
-    # training workload (B=4 T=4096 H=32, 524,288 token-heads): 1,547,936,000 B
-    # read + 766,516,992 B written in the captured launch
-    "tc_local_grad": {"bytes_per_token_head": 2314452992 / 524288, "workload": "training",
+    # training workload (B=4 T=4096 H=32, 524,288 token-heads): 1,547,845,888 B
+    # read + 766,588,928 B written in the captured launch
+    "tc_local_grad": {"bytes_per_token_head": 2314434816 / 524288, "workload": "training",
                       "K": 128, "V": 128,
                       "files": ["gdn_tc_local.cu", "tc_ptx.cuh", "gdn_common.cuh"],
-                      "sha256": "6fef7c0c7f4c0f8de122f6a293c4975aea9a3ce446dc786c752a1975a416888a"},
+                      "sha256": "ea2b22f9082ef2928da13b7f425dda6b30c164c759daf2e0e081a62701062792"},
 }
 
 

@@ -1,7 +1,7 @@
 // gdn_step.cu -- one decode step of the gated delta rule per (sequence, head),
 // the state updated in place.  It reads and writes the K x V fp32 state once,
-// so it is bound by HBM: each CTA streams one state through registers with
-// coalesced row accesses and needs no shared-memory tiles beyond the vectors.
+// so it is bound by HBM: each CTA streams one state through registers in
+// 16-byte, coalesced pieces and needs no shared-memory tiles beyond the vectors.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -42,15 +42,42 @@ __device__ __forceinline__ float cta_sum(float x, float *red) {
 }
 }  // namespace
 
-// One CTA per (sequence, head), 2V threads: thread t owns state column
-// v = t % V and the key rows kr = (t / V) * K/2 .. +K/2.  The partial sums of
-// the two row halves meet in shared memory.
+// One CTA per (sequence, head), 2V threads.  Thread t owns state columns
+// 4 (t % (V/4)) .. +3 and the key rows of row group t / (V/4) (8 groups of K/8
+// rows), so that every state access is a 16-byte, fully coalesced piece; the
+// groups' partial sums meet in shared memory.
+template <int V>
+__device__ __forceinline__ float4 sum_groups(const float (*part)[V], int c) {
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+        const float4 p = *reinterpret_cast<const float4 *>(&part[g][c]);
+        s.x += p.x;
+        s.y += p.y;
+        s.z += p.z;
+        s.w += p.w;
+    }
+    return s;
+}
+
+__device__ __forceinline__ void store4(float *p, float4 x) { *reinterpret_cast<float4 *>(p) = x; }
+__device__ __forceinline__ void store4(__nv_bfloat16 *p, float4 x) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(x.x, x.y), b = __floats2bfloat162_rn(x.z, x.w);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t *>(&a);
+    u.y = *reinterpret_cast<uint32_t *>(&b);
+    *reinterpret_cast<uint2 *>(p) = u;
+}
+
 template <typename T, int K, int V>
 __global__ void __launch_bounds__(2 * V)
 step_kernel(StepArgs a) {
-    constexpr int NT = 2 * V, KH = K / 2;
-    __shared__ float kv[K], qv[K], part[2][V], red[NT / 32];
-    const int u = blockIdx.x, h = u % a.H, t = threadIdx.x, v = t % V, half = t / V;
+    constexpr int NT = 2 * V, NCG = V / 4, RG = K / 8;   // column groups, rows per group
+    static_assert(NT / NCG == 8, "eight row groups");
+    __shared__ float kv[K], qv[K], red[NT / 32];
+    __shared__ __align__(16) float part[8][V];
+    const int u = blockIdx.x, h = u % a.H, t = threadIdx.x;
+    const int c = 4 * (t % NCG), r0 = (t / NCG) * RG;
     const long long qk0 = (long long)u * K, v0 = (long long)u * V;
     // inputs of the token: k, q (optionally L2-normalised), decay, beta
     float kk = 0.f, qq = 0.f;
@@ -72,30 +99,46 @@ step_kernel(StepArgs a) {
                               : x;
     const float alpha = expf(gl), beta = a.beta[u];
     __syncthreads();
-    // Hbar = alpha H (rows of this half), partial (Hbar^T k)_v
+    // Hbar = alpha H (this thread's rows and columns), partial (Hbar^T k)_c
     float *S = a.state + (long long)u * K * V;
-    float hr[KH];
-    float dot = 0.f;
+    float4 hr[RG];
+    float4 dot = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int i = 0; i < KH; ++i) {
-        hr[i] = alpha * S[(long long)(half * KH + i) * V + v];
-        dot += hr[i] * kv[half * KH + i];
+    for (int i = 0; i < RG; ++i) {
+        const float4 x4 = *reinterpret_cast<const float4 *>(S + (long long)(r0 + i) * V + c);
+        const float kr = kv[r0 + i];
+        hr[i] = make_float4(alpha * x4.x, alpha * x4.y, alpha * x4.z, alpha * x4.w);
+        dot.x += hr[i].x * kr;
+        dot.y += hr[i].y * kr;
+        dot.z += hr[i].z * kr;
+        dot.w += hr[i].w * kr;
     }
-    part[half][v] = dot;
+    *reinterpret_cast<float4 *>(&part[t / NCG][c]) = dot;
     __syncthreads();
-    const float r = ld<T>(a.v, v0 + v) - (part[0][v] + part[1][v]);
-    // H = Hbar + beta k r^T, written back; partial (H^T q)_v
-    float o = 0.f;
+    const float4 kh = sum_groups<V>(part, c);
+    const float4 rr = make_float4(ld<T>(a.v, v0 + c) - kh.x, ld<T>(a.v, v0 + c + 1) - kh.y,
+                                  ld<T>(a.v, v0 + c + 2) - kh.z, ld<T>(a.v, v0 + c + 3) - kh.w);
+    // H = Hbar + beta k r^T, written back; partial (H^T q)_c
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int i = 0; i < KH; ++i) {
-        const float hn = hr[i] + beta * kv[half * KH + i] * r;
-        S[(long long)(half * KH + i) * V + v] = hn;
-        o += hn * qv[half * KH + i];
+    for (int i = 0; i < RG; ++i) {
+        const float bk = beta * kv[r0 + i], qr = qv[r0 + i];
+        const float4 hn = make_float4(hr[i].x + bk * rr.x, hr[i].y + bk * rr.y,
+                                      hr[i].z + bk * rr.z, hr[i].w + bk * rr.w);
+        *reinterpret_cast<float4 *>(S + (long long)(r0 + i) * V + c) = hn;
+        o.x += hn.x * qr;
+        o.y += hn.y * qr;
+        o.z += hn.z * qr;
+        o.w += hn.w * qr;
     }
-    __syncthreads();                          // both halves have read part[] above
-    part[half][v] = o;
+    __syncthreads();                          // every group has read part[] above
+    *reinterpret_cast<float4 *>(&part[t / NCG][c]) = o;
     __syncthreads();
-    if (half == 0) from_f(reinterpret_cast<T *>(a.o) + v0 + v, a.scale * (part[0][v] + part[1][v]));
+    if (t < NCG) {
+        const float4 os = sum_groups<V>(part, c);
+        store4(reinterpret_cast<T *>(a.o) + v0 + c,
+               make_float4(a.scale * os.x, a.scale * os.y, a.scale * os.z, a.scale * os.w));
+    }
 }
 
 template <typename T>
