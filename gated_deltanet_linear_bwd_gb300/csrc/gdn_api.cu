@@ -414,7 +414,7 @@ gdn_status gdn_recurrent_step(const gdn_step_args *a, void *stream) {
     DeviceInfo *dev = nullptr;
     gdn_status st = device_info(&dev);
     if (st != GDN_OK) return st;
-    const cudaError_t e = step::run(a, (cudaStream_t)stream);
+    const cudaError_t e = step::run(a, dev->sms, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "recurrent step launch");
     return GDN_OK;
 }

@@ -89,8 +89,9 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 namespace step {
-// One decode step per (sequence, head), the state updated in place.
-cudaError_t run(const gdn_step_args *args, cudaStream_t s);
+// One decode step per (sequence, head), the state updated in place, on a
+// device with `sms` SMs.
+cudaError_t run(const gdn_step_args *args, int sms, cudaStream_t s);
 }  // namespace step
 
 namespace simt {

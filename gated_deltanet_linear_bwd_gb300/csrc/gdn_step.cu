@@ -1,7 +1,12 @@
 // gdn_step.cu -- one decode step of the gated delta rule per (sequence, head),
 // the state updated in place.  It reads and writes the K x V fp32 state once,
-// so it is bound by HBM: each CTA streams one state through registers in
-// 16-byte, coalesced pieces and needs no shared-memory tiles beyond the vectors.
+// so it is bound by HBM.  Every warp works alone, with no CTA barrier: it
+// takes (sequence, head, 16-column slice) items in turn, holds the slice's
+// K x 16 block in registers (16-byte pieces of 64-byte row runs), reduces the
+// column sums Hbar^T k and H^T q over its lanes by shuffles, and writes the
+// new block back in place.  The eight warps of a CTA take the eight slices of
+// one (sequence, head) together, so the state's rows are read whole; the warps
+// of the persistent grid share the items to within one.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -23,141 +28,170 @@ struct StepArgs {
     int l2norm;
 };
 
-template <typename T>
-__device__ __forceinline__ float ld(const void *p, long long i) {
-    return to_f(reinterpret_cast<const T *>(p)[i]);
-}
+constexpr int kWarps = 8;  // per CTA
+constexpr int kSlice = 16; // state columns per item
 
-// Sum over the CTA of one value per thread (KV threads in warps of 32).
-template <int NT>
-__device__ __forceinline__ float cta_sum(float x, float *red) {
-    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = x;
-    __syncthreads();
-    float s = 0.f;
-#pragma unroll
-    for (int w = 0; w < NT / 32; ++w) s += red[w];
-    __syncthreads();
-    return s;
-}
-}  // namespace
-
-// One CTA per (sequence, head), 2V threads.  Thread t owns state columns
-// 4 (t % (V/4)) .. +3 and the key rows of row group t / (V/4) (8 groups of K/8
-// rows), so that every state access is a 16-byte, fully coalesced piece; the
-// groups' partial sums meet in shared memory.
-template <int V>
-__device__ __forceinline__ float4 sum_groups(const float (*part)[V], int c) {
-    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int g = 0; g < 8; ++g) {
-        const float4 p = *reinterpret_cast<const float4 *>(&part[g][c]);
-        s.x += p.x;
-        s.y += p.y;
-        s.z += p.z;
-        s.w += p.w;
+// `n` consecutive elements from `p + i` (n = 2 or 4, 16-byte aligned for
+// fp32 and 8-byte for bf16 at the offsets used here).
+template <typename T, int n>
+__device__ __forceinline__ void ld_vec(const void *p, long long i, float *x) {
+    const T *s = reinterpret_cast<const T *>(p) + i;
+    if constexpr (sizeof(T) == 4) {
+        if constexpr (n == 4) {
+            const float4 a = *reinterpret_cast<const float4 *>(s);
+            x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w;
+        } else {
+            const float2 a = *reinterpret_cast<const float2 *>(s);
+            x[0] = a.x, x[1] = a.y;
+        }
+    } else {
+        if constexpr (n == 4) {
+            const uint2 a = *reinterpret_cast<const uint2 *>(s);
+            const __nv_bfloat162 b0 = *reinterpret_cast<const __nv_bfloat162 *>(&a.x);
+            const __nv_bfloat162 b1 = *reinterpret_cast<const __nv_bfloat162 *>(&a.y);
+            x[0] = __low2float(b0), x[1] = __high2float(b0);
+            x[2] = __low2float(b1), x[3] = __high2float(b1);
+        } else {
+            const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(s);
+            x[0] = __low2float(b), x[1] = __high2float(b);
+        }
     }
-    return s;
 }
 
 __device__ __forceinline__ void store4(float *p, float4 x) { *reinterpret_cast<float4 *>(p) = x; }
 __device__ __forceinline__ void store4(__nv_bfloat16 *p, float4 x) {
-    __nv_bfloat162 a = __floats2bfloat162_rn(x.x, x.y), b = __floats2bfloat162_rn(x.z, x.w);
-    uint2 u;
-    u.x = *reinterpret_cast<uint32_t *>(&a);
-    u.y = *reinterpret_cast<uint32_t *>(&b);
-    *reinterpret_cast<uint2 *>(p) = u;
+    __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y), hi = __floats2bfloat162_rn(x.z, x.w);
+    uint2 w;
+    w.x = *reinterpret_cast<uint32_t *>(&lo);
+    w.y = *reinterpret_cast<uint32_t *>(&hi);
+    *reinterpret_cast<uint2 *>(p) = w;
+}
+
+// Sum over the eight lanes that share lane % 4 (the row blocks of one column group).
+__device__ __forceinline__ float4 sum_row_blocks(float4 x) {
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+        x.x += __shfl_xor_sync(0xffffffffu, x.x, o);
+        x.y += __shfl_xor_sync(0xffffffffu, x.y, o);
+        x.z += __shfl_xor_sync(0xffffffffu, x.z, o);
+        x.w += __shfl_xor_sync(0xffffffffu, x.w, o);
+    }
+    return x;
+}
+}  // namespace
+
+// Item w covers state columns cb .. cb + 15 of unit u = w / (V / 16),
+// cb = 16 (w % (V / 16)).  Lane l owns columns cb + c .. cb + c + 3, c = 4 (l % 4),
+// of rows RL (l / 4) .. RL (l / 4) + RL - 1, RL = K / 8.
+template <typename T, int K, int V>
+__global__ void __launch_bounds__(32 * kWarps, 2)
+step_kernel(StepArgs a) {
+    constexpr int NSL = V / kSlice, RL = K / 8, KL = K / 32;
+    __shared__ __align__(16) float kq[kWarps][2][K];  // each warp's normalised k and q
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int c = 4 * (lane & 3), r0 = RL * (lane >> 2);
+    float *kb = kq[warp][0], *qb = kq[warp][1];
+    const long long n_items = (long long)a.N * a.H * NSL;
+    const long long stride = (long long)gridDim.x * kWarps;
+    for (long long w = (long long)blockIdx.x * kWarps + warp; w < n_items; w += stride) {
+        const long long u = w / NSL;
+        const int cb = kSlice * (int)(w % NSL), h = (int)(u % a.H);
+        float *S = a.state + u * K * V + cb + c;
+        float4 hr[RL];
+#pragma unroll
+        for (int i = 0; i < RL; ++i)
+            hr[i] = *reinterpret_cast<const float4 *>(S + (long long)(r0 + i) * V);
+        float kx[KL], qx[KL], vx[4];
+        ld_vec<T, KL>(a.k, u * K + KL * lane, kx);
+        ld_vec<T, KL>(a.q, u * K + KL * lane, qx);
+        ld_vec<T, 4>(a.v, u * V + cb + c, vx);
+        const float gx = a.g[u], beta = a.beta[u];
+        if (a.l2norm) {
+            float sk = 0.f, sq = 0.f;
+#pragma unroll
+            for (int i = 0; i < KL; ++i) sk += kx[i] * kx[i], sq += qx[i] * qx[i];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                sk += __shfl_xor_sync(0xffffffffu, sk, o);
+                sq += __shfl_xor_sync(0xffffffffu, sq, o);
+            }
+            const float ik = rsqrtf(sk + 1e-6f), iq = rsqrtf(sq + 1e-6f);
+#pragma unroll
+            for (int i = 0; i < KL; ++i) kx[i] *= ik, qx[i] *= iq;
+        }
+        __syncwarp();  // the previous item's reads of kb, qb are done
+#pragma unroll
+        for (int i = 0; i < KL; ++i) kb[KL * lane + i] = kx[i], qb[KL * lane + i] = qx[i];
+        __syncwarp();
+        const float gl = a.gate_a ? -a.gate_a[h] * (gx > 0.f ? gx + log1pf(expf(-gx))
+                                                           : log1pf(expf(gx)))
+                                  : gx;
+        const float alpha = expf(gl);
+
+        // Hbar = alpha H; (Hbar^T k) over the lane's rows, then over the warp
+        float4 dot = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < RL; ++i) {
+            const float kr = kb[r0 + i];
+            hr[i] = make_float4(alpha * hr[i].x, alpha * hr[i].y, alpha * hr[i].z, alpha * hr[i].w);
+            dot.x += hr[i].x * kr;
+            dot.y += hr[i].y * kr;
+            dot.z += hr[i].z * kr;
+            dot.w += hr[i].w * kr;
+        }
+        dot = sum_row_blocks(dot);
+        const float4 rr = make_float4(vx[0] - dot.x, vx[1] - dot.y, vx[2] - dot.z, vx[3] - dot.w);
+
+        // H = Hbar + beta k r^T, written back; H^T q likewise
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < RL; ++i) {
+            const float bk = beta * kb[r0 + i], qr = qb[r0 + i];
+            const float4 hn = make_float4(hr[i].x + bk * rr.x, hr[i].y + bk * rr.y,
+                                          hr[i].z + bk * rr.z, hr[i].w + bk * rr.w);
+            *reinterpret_cast<float4 *>(S + (long long)(r0 + i) * V) = hn;
+            o.x += hn.x * qr;
+            o.y += hn.y * qr;
+            o.z += hn.z * qr;
+            o.w += hn.w * qr;
+        }
+        o = sum_row_blocks(o);
+        if (lane < 4)
+            store4(reinterpret_cast<T *>(a.o) + u * V + cb + c,
+                   make_float4(a.scale * o.x, a.scale * o.y, a.scale * o.z, a.scale * o.w));
+    }
 }
 
 template <typename T, int K, int V>
-__global__ void __launch_bounds__(2 * V)
-step_kernel(StepArgs a) {
-    constexpr int NT = 2 * V, NCG = V / 4, RG = K / 8;   // column groups, rows per group
-    static_assert(NT / NCG == 8, "eight row groups");
-    __shared__ float kv[K], qv[K], red[NT / 32];
-    __shared__ __align__(16) float part[8][V];
-    const int u = blockIdx.x, h = u % a.H, t = threadIdx.x;
-    const int c = 4 * (t % NCG), r0 = (t / NCG) * RG;
-    const long long qk0 = (long long)u * K, v0 = (long long)u * V;
-    // inputs of the token: k, q (optionally L2-normalised), decay, beta
-    float kk = 0.f, qq = 0.f;
-    if (t < K) {
-        kk = ld<T>(a.k, qk0 + t);
-        qq = ld<T>(a.q, qk0 + t);
-    }
-    if (a.l2norm) {
-        const float sk = cta_sum<NT>(kk * kk, red), sq = cta_sum<NT>(qq * qq, red);
-        kk *= rsqrtf(sk + 1e-6f);
-        qq *= rsqrtf(sq + 1e-6f);
-    }
-    if (t < K) {
-        kv[t] = kk;
-        qv[t] = qq;
-    }
-    const float x = a.g[u];
-    const float gl = a.gate_a ? -a.gate_a[h] * (x > 0.f ? x + log1pf(expf(-x)) : log1pf(expf(x)))
-                              : x;
-    const float alpha = expf(gl), beta = a.beta[u];
-    __syncthreads();
-    // Hbar = alpha H (this thread's rows and columns), partial (Hbar^T k)_c
-    float *S = a.state + (long long)u * K * V;
-    float4 hr[RG];
-    float4 dot = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int i = 0; i < RG; ++i) {
-        const float4 x4 = *reinterpret_cast<const float4 *>(S + (long long)(r0 + i) * V + c);
-        const float kr = kv[r0 + i];
-        hr[i] = make_float4(alpha * x4.x, alpha * x4.y, alpha * x4.z, alpha * x4.w);
-        dot.x += hr[i].x * kr;
-        dot.y += hr[i].y * kr;
-        dot.z += hr[i].z * kr;
-        dot.w += hr[i].w * kr;
-    }
-    *reinterpret_cast<float4 *>(&part[t / NCG][c]) = dot;
-    __syncthreads();
-    const float4 kh = sum_groups<V>(part, c);
-    const float4 rr = make_float4(ld<T>(a.v, v0 + c) - kh.x, ld<T>(a.v, v0 + c + 1) - kh.y,
-                                  ld<T>(a.v, v0 + c + 2) - kh.z, ld<T>(a.v, v0 + c + 3) - kh.w);
-    // H = Hbar + beta k r^T, written back; partial (H^T q)_c
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int i = 0; i < RG; ++i) {
-        const float bk = beta * kv[r0 + i], qr = qv[r0 + i];
-        const float4 hn = make_float4(hr[i].x + bk * rr.x, hr[i].y + bk * rr.y,
-                                      hr[i].z + bk * rr.z, hr[i].w + bk * rr.w);
-        *reinterpret_cast<float4 *>(S + (long long)(r0 + i) * V + c) = hn;
-        o.x += hn.x * qr;
-        o.y += hn.y * qr;
-        o.z += hn.z * qr;
-        o.w += hn.w * qr;
-    }
-    __syncthreads();                          // every group has read part[] above
-    *reinterpret_cast<float4 *>(&part[t / NCG][c]) = o;
-    __syncthreads();
-    if (t < NCG) {
-        const float4 os = sum_groups<V>(part, c);
-        store4(reinterpret_cast<T *>(a.o) + v0 + c,
-               make_float4(a.scale * os.x, a.scale * os.y, a.scale * os.z, a.scale * os.w));
-    }
-}
-
-template <typename T>
-static cudaError_t launch(const StepArgs &a, int K, int V, cudaStream_t s) {
-    const int n = a.N * a.H;
-    prof_before("recurrent_step", s);
-    if (K == 128 && V == 128) step_kernel<T, 128, 128><<<n, 256, 0, s>>>(a);
-    else if (K == 128 && V == 64) step_kernel<T, 128, 64><<<n, 128, 0, s>>>(a);
-    else if (K == 64 && V == 128) step_kernel<T, 64, 128><<<n, 256, 0, s>>>(a);
-    else step_kernel<T, 64, 64><<<n, 128, 0, s>>>(a);
-    prof_after(s);
+static cudaError_t launch_kv(const StepArgs &a, int sms, cudaStream_t st) {
+    int per_sm = 0;  // resident CTAs per SM
+    const cudaError_t e =
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, step_kernel<T, K, V>, 32 * kWarps, 0);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    const long long ctas = ((long long)a.N * a.H * (V / kSlice) + kWarps - 1) / kWarps;
+    const int grid = (int)(ctas < (long long)sms * per_sm ? ctas : (long long)sms * per_sm);
+    step_kernel<T, K, V><<<grid, 32 * kWarps, 0, st>>>(a);
     return cudaGetLastError();
 }
 
-cudaError_t run(const gdn_step_args *p, cudaStream_t s) {
+template <typename T>
+static cudaError_t launch(const StepArgs &a, int K, int V, int sms, cudaStream_t s) {
+    prof_before("recurrent_step", s);
+    cudaError_t e;
+    if (K == 128 && V == 128) e = launch_kv<T, 128, 128>(a, sms, s);
+    else if (K == 128 && V == 64) e = launch_kv<T, 128, 64>(a, sms, s);
+    else if (K == 64 && V == 128) e = launch_kv<T, 64, 128>(a, sms, s);
+    else e = launch_kv<T, 64, 64>(a, sms, s);
+    prof_after(s);
+    return e;
+}
+
+cudaError_t run(const gdn_step_args *p, int sms, cudaStream_t s) {
     StepArgs a{p->q, p->k, p->v, p->g, p->beta, p->gate_scale, p->state, p->o, p->N, p->H,
                p->scale > 0.f ? p->scale : 1.0f / sqrtf((float)p->K), p->use_qk_l2norm ? 1 : 0};
-    return p->dtype == GDN_BF16 ? launch<__nv_bfloat16>(a, p->K, p->V, s)
-                                : launch<float>(a, p->K, p->V, s);
+    return p->dtype == GDN_BF16 ? launch<__nv_bfloat16>(a, p->K, p->V, sms, s)
+                                : launch<float>(a, p->K, p->V, sms, s);
 }
 
 }  // namespace step

@@ -1,8 +1,10 @@
 """The decode step (gdn_recurrent_step): token-by-token steps from an initial
 state must reproduce the oracle's sequential recurrence over the same tokens
 (outputs of every step and the state after the last one), on fp32 and bf16,
-K = V = 64 and 128, with and without q/k normalisation and the gate; and a
-chunked prefill followed by decode steps must continue the same recurrence."""
+K, V in {64, 128}, with and without q/k normalisation and the gate; one step
+over enough (sequence, head) pairs that every persistent CTA cycles its
+state stages several times; and a chunked prefill followed by decode steps
+must continue the same recurrence."""
 import numpy as np
 import pytest
 import torch
@@ -30,15 +32,17 @@ def _steps(p, l2=False, gate=None):
     return to_np(torch.stack(outs, 1)), to_np(state)
 
 
-@pytest.mark.parametrize("name,K,l2,gated", [
-    ("tiny", 64, False, False), ("tiny", 64, True, True),
-    ("training", 128, False, False), ("training", 128, True, False),
-    ("training", 128, False, True),
+@pytest.mark.parametrize("name,K,V,l2,gated", [
+    ("tiny", 64, 64, False, False), ("tiny", 64, 64, True, True),
+    ("tiny", 128, 64, False, False), ("tiny", 64, 128, True, False),
+    ("training", 128, 128, False, False), ("training", 128, 128, True, False),
+    ("training", 128, 128, False, True),
+    ("training", 128, 64, True, False), ("training", 64, 128, False, True),
 ])
-def test_steps_reproduce_the_recurrence(name, K, l2, gated):
+def test_steps_reproduce_the_recurrence(name, K, V, l2, gated):
     if not torch.cuda.is_available():
         pytest.fail("needs a CUDA GPU")
-    p = gdn_synth.make(name, B=3, T=7, H=2, K=K, V=K, h0_std=0.3, normalise=not l2)
+    p = gdn_synth.make(name, B=3, T=7, H=2, K=K, V=V, h0_std=0.3, normalise=not l2)
     gate = gdn_synth.gate_draws(p, seed=9) if gated else None
     g = oracle.gate(*gate) if gated else p.g
     o_ref, ht_ref = oracle.fwd(p.q, p.k, p.v, g, p.beta, h0=p.h0, use_l2norm=l2)
@@ -46,6 +50,25 @@ def test_steps_reproduce_the_recurrence(name, K, l2, gated):
     tol = TOL[gdn_synth.WORKLOADS[name]["dtype"]]
     check("o (every step)", o, o_ref, tol)
     check("state after the last step", st, ht_ref, tol)
+
+
+@pytest.mark.parametrize("name,K,V,l2", [
+    ("training", 128, 128, False),     # 4096 half-state items, 27 per CTA
+    ("training", 128, 128, True),
+    ("tiny", 128, 128, False),         # fp32 inputs
+    ("training", 64, 64, False),       # whole-state items of 16 KB
+])
+def test_one_step_over_many_units(name, K, V, l2):
+    """One step for 64 sequences x 32 heads (the bench's decode batch) against
+    the oracle's recurrence over one token from the same state."""
+    if not torch.cuda.is_available():
+        pytest.fail("needs a CUDA GPU")
+    p = gdn_synth.make(name, B=64, T=1, H=32, K=K, V=V, h0_std=0.3, normalise=not l2)
+    o_ref, ht_ref = oracle.fwd(p.q, p.k, p.v, p.g, p.beta, h0=p.h0, use_l2norm=l2)
+    o, st = _steps(p, l2)
+    tol = TOL[gdn_synth.WORKLOADS[name]["dtype"]]
+    check("o", o, o_ref, tol)
+    check("state", st, ht_ref, tol)
 
 
 def test_prefill_then_decode_continues_the_recurrence():
