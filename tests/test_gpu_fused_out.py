@@ -2,8 +2,8 @@
 the SMs: the state walk that forms O (with intra-card sequence parallelism, or
 with a context kept for the backward), the one-kernel forward that also does
 each chunk's preparation (without either), and the reverse walk that forms P,
-Qs and Y^T itself.  Results match the oracle, the absorbed passes do not run,
-and with few walk CTAs they do."""
+Qs and Y^T itself (without sequence parallelism).  Results match the oracle,
+the absorbed passes do not run, and with few walk CTAs they do."""
 import pytest
 import torch
 
@@ -82,29 +82,40 @@ def test_few_walk_ctas_use_the_output_pass():
     check("o", o, ro, TOL["bf16"])
 
 
-def _bwd_kernels(p, cp):
+def _bwd_kernels(p, cp, seg=0, l2=False):
     gdn = lib()
     gdn.gdn_profile_begin()
-    g = gpu_bwd(p, cp=cp)
+    g = gpu_bwd(p, cp=cp, seg=seg, l2=l2)
     torch.cuda.synchronize()
     names = {n for n, _, _ in gdn.gdn_profile_end()}
     return g, names
 
 
-@pytest.mark.parametrize("kw", [
-    dict(B=2, T=200, H=64),                          # 128 reverse-walk CTAs, ragged last chunk
-    dict(lengths=[130, 0, 64, 257, 1], H=32),        # varlen, one sequence empty
+@pytest.mark.parametrize("kw,cp,seg,l2", [
+    (dict(B=2, T=200, H=64), "off", 0, False),       # 128 reverse-walk CTAs, ragged last chunk
+    (dict(B=2, T=200, H=64), "off", 0, True),
+    (dict(lengths=[130, 0, 64, 257, 1], H=32), "off", 0, False),   # varlen, one sequence empty
 ])
-def test_fused_reverse_walk_matches_oracle(kw):
+def test_fused_reverse_walk_matches_oracle(kw, cp, seg, l2):
     p = gdn_synth.make("training", h0_std=0.1, dht_std=0.01, **kw)
-    g, names = _bwd_kernels(p, "off")
+    g, names = _bwd_kernels(p, cp, seg, l2)
     assert "tc_dwalk_fused" in names and "tc_bwd_intra" not in names, names
-    r = oracle_bwd(p)
+    r = oracle_bwd(p, l2=l2)
     for k in ("dq", "dk", "dv", "dg", "dbeta", "dh0"):
         check(k, g[k], r[k], TOL["bf16"])
 
 
-def test_few_reverse_walk_ctas_use_the_intra_pass():
-    p = gdn_synth.make("training", B=1, T=300, H=2, h0_std=0.1, dht_std=0.01)
-    g, names = _bwd_kernels(p, "off")
+@pytest.mark.parametrize("kw,cp,seg", [
+    (dict(B=1, T=300, H=2), "off", 0),
+    (dict(B=1, T=300, H=2), "force", 1),
+    # with sequence parallelism the segment-map walk reads the intra pass's Qs and
+    # Y^T, so the intra pass runs however many segment walks there are
+    (dict(B=1, T=630, H=12), "force", 1),
+])
+def test_few_reverse_walk_ctas_or_segments_use_the_intra_pass(kw, cp, seg):
+    p = gdn_synth.make("training", h0_std=0.1, dht_std=0.01, **kw)
+    g, names = _bwd_kernels(p, cp, seg)
     assert "tc_bwd_intra" in names and "tc_dwalk_out" in names, names
+    r = oracle_bwd(p)
+    for k in ("dq", "dk", "dv", "dg", "dbeta", "dh0"):
+        check(k, g[k], r[k], TOL["bf16"])
