@@ -88,6 +88,7 @@ def _bwd_kernels(p, cp, seg=0, l2=False):
     g = gpu_bwd(p, cp=cp, seg=seg, l2=l2)
     torch.cuda.synchronize()
     names = {n for n, _, _ in gdn.gdn_profile_end()}
+    assert gdn.gdn_sync_status(torch.cuda.current_stream().cuda_stream) == 0
     return g, names
 
 
