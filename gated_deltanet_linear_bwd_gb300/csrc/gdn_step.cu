@@ -4,9 +4,10 @@
 // takes (sequence, head, 16-column slice) items in turn, holds the slice's
 // K x 16 block in registers (16-byte pieces of 64-byte row runs), reduces the
 // column sums Hbar^T k and H^T q over its lanes by shuffles, and writes the
-// new block back in place.  The eight warps of a CTA take the eight slices of
-// one (sequence, head) together, so the state's rows are read whole; the warps
-// of the persistent grid share the items to within one.
+// new block back in place.  The eight warps of a CTA take adjacent slices (the
+// eight of one (sequence, head) when V = 128), so the state's rows are read
+// whole at about the same time; the warps of the persistent grid share the
+// items to within one.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -164,11 +165,16 @@ step_kernel(StepArgs a) {
 
 template <typename T, int K, int V>
 static cudaError_t launch_kv(const StepArgs &a, int sms, cudaStream_t st) {
-    int per_sm = 0;  // resident CTAs per SM
-    const cudaError_t e =
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, step_kernel<T, K, V>, 32 * kWarps, 0);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) per_sm = 1;
+    // resident CTAs per SM, asked once per instantiation (the library runs on
+    // sm_103a only, so the answer is the same on every device)
+    static int per_sm = 0;
+    if (per_sm == 0) {
+        int n = 0;
+        const cudaError_t e =
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, step_kernel<T, K, V>, 32 * kWarps, 0);
+        if (e != cudaSuccess) return e;
+        per_sm = n > 0 ? n : 1;
+    }
     const long long ctas = ((long long)a.N * a.H * (V / kSlice) + kWarps - 1) / kWarps;
     const int grid = (int)(ctas < (long long)sms * per_sm ? ctas : (long long)sms * per_sm);
     step_kernel<T, K, V><<<grid, 32 * kWarps, 0, st>>>(a);
