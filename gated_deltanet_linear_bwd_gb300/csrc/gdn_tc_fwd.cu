@@ -291,15 +291,12 @@ tc_prep_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
 #pragma unroll 1
             for (int c = 0; c < 2; ++c) {
                 const int Lc = (c && !has_b) ? 0 : (c ? rb.len : ra.len);
-                uint8_t *tile = base + c * 2 * kTile;
+                float x[64];    // both halves of the row with one wait
+                tmem_ld32x2(tmem_addr(tbase, warp, 128 * pass + c * 64),
+                            tmem_addr(tbase, warp, 128 * pass + c * 64 + 32), x, x + 32);
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    float x[32];
-                    tmem_ld32(tmem_addr(tbase, warp, 128 * pass + c * 64 + 32 * half), x);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) x[j] = 32 * half + j < Lc ? x[j] : 0.f;
-                    st_row32(tile, tid, 32 * half, x);
-                }
+                for (int j = 0; j < 64; ++j) x[j] = j < Lc ? x[j] : 0.f;
+                st_row64(base + c * 2 * kTile, tid, x);
             }
         }
         fence_proxy_async();
