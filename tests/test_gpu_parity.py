@@ -182,6 +182,32 @@ def test_bounded_wait_gives_up_and_reports_timeout():
     assert gdn.gdn_sync_status(stream) == 0
 
 
+@pytest.mark.parametrize("kw,cp", [
+    (dict(B=1, T=300, H=2), "off"),          # intra pass, reverse walk, local gradients
+    (dict(B=2, T=200, H=64), "off"),         # the reverse walk that forms the intra terms
+    (dict(B=1, T=640, H=2), "force"),        # segment-map walks and scans
+])
+def test_backward_bounded_waits_give_up_and_report_timeout(kw, cp):
+    """The same for every backward kernel: with spin limit 0 each gives up at its
+    first wait, the status word reports GDN_ERR_TIMEOUT, and a backward run
+    afterwards matches the oracle."""
+    gdn = lib()
+    p = gdn_synth.make("training", h0_std=0.1, dht_std=0.01, **kw)
+    stream = torch.cuda.current_stream().cuda_stream
+    assert gdn.gdn_sync_status(stream) == 0
+    gdn.gdn_set_spin_limit(0)
+    try:
+        gpu_bwd(p, cp=cp)
+        assert gdn.gdn_sync_status(stream) == 5
+    finally:
+        gdn.gdn_set_spin_limit(-1)
+    g = gpu_bwd(p, cp=cp)
+    assert gdn.gdn_sync_status(stream) == 0
+    r = oracle_bwd(p)
+    for k in ("dq", "dk", "dv", "dg", "dbeta", "dh0"):
+        check(k + " after timeout", g[k], r[k], TOL["bf16"])
+
+
 def test_autograd_wrapper_matches_low_level_backward():
     gdn = lib()
     p = gdn_synth.make("tiny", T=130, h0_std=0.1).to("cuda")
