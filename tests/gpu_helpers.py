@@ -20,12 +20,13 @@ def to_np(t):
     return None if t is None else t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def gpu_fwd(p, cp="off", l2=False, seg=0, warm=0, tau=1e-3, stats=None, h0=True):
+def gpu_fwd(p, cp="off", l2=False, seg=0, warm=0, tau=1e-3, stats=None, h0=True, fuse=False):
     d = p.to("cuda")
     o, fs = lib().chunk_gated_delta_rule_fwd(
         d.q, d.k, d.v, d.g, d.beta, initial_state=d.h0 if h0 else None,
         output_final_state=True, cu_seqlens=d.cu_seqlens, use_qk_l2norm=l2, cp=cp,
-        cp_segment_chunks=seg, cp_warmup_chunks=warm, cp_warmup_tau=tau, cp_stats=stats)
+        cp_segment_chunks=seg, cp_warmup_chunks=warm, cp_warmup_tau=tau, cp_stats=stats,
+        fuse_prep=fuse)
     torch.cuda.synchronize()
     return to_np(o), to_np(fs)
 

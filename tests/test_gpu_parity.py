@@ -162,20 +162,25 @@ def test_bad_cu_seqlens_sets_the_status_word():
     assert gdn.gdn_sync_status(torch.cuda.current_stream().cuda_stream) == 0  # cleared
 
 
-def test_bounded_wait_gives_up_and_reports_timeout():
+@pytest.mark.parametrize("kw,fuse", [
+    (dict(B=1, T=300, H=2), False),          # prep, state walk, output pass
+    (dict(B=2, T=200, H=64), False),         # the walk that forms O
+    (dict(B=2, T=200, H=64), True),          # the one-kernel forward
+])
+def test_bounded_wait_gives_up_and_reports_timeout(kw, fuse):
     """Spin limit 0: every bounded wait of the tensor-core kernels gives up at
     once; the status word reports GDN_ERR_TIMEOUT and the context stays usable."""
     gdn = lib()
-    p = gdn_synth.make("training", B=1, T=300, H=2, h0_std=0.1)
+    p = gdn_synth.make("training", h0_std=0.1, **kw)
     stream = torch.cuda.current_stream().cuda_stream
     assert gdn.gdn_sync_status(stream) == 0
     gdn.gdn_set_spin_limit(0)
     try:
-        gpu_fwd(p)
+        gpu_fwd(p, fuse=fuse)
         assert gdn.gdn_sync_status(stream) == 5
     finally:
         gdn.gdn_set_spin_limit(-1)
-    o, fs = gpu_fwd(p)
+    o, fs = gpu_fwd(p, fuse=fuse)
     ro, rfs = oracle_fwd(p)
     check("o after timeout", o, ro, TOL["bf16"])
     check("final_state after timeout", fs, rfs, TOL["bf16"])
