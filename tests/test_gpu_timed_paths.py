@@ -8,7 +8,9 @@ and sampled (sequence, head) units of O, the final state and every gradient
 are compared element by element with the fp64 oracle at the bf16 tolerance.
 The kernels that ran are read from the library's tracing, so each test also
 pins which path it covered (the fused reverse walk on training and varlen,
-the sequence-parallel map walks on edge and long)."""
+the sequence-parallel map walks on edge and long).  The gated varlen step
+(bench.py's `gated` figure) is checked the same way, d(gate logits) and
+d(gate_scale) included."""
 import numpy as np
 import pytest
 import torch
@@ -137,3 +139,49 @@ def test_forward_as_timed(name, heads, batches, l2, fuse):
     e_o = check(f"{name} o", x[:, :, heads], ro, tol)
     e_s = check(f"{name} final_state", f[:, heads], rfs, tol)
     print(name, f"o {e_o:.2e} final_state {e_s:.2e}")
+
+
+def test_gated_varlen_step_as_timed():
+    """The bench's `gated` measurement: the varlen step with the decay formed
+    inside the library from gate logits (gate_scale), forward keeping its
+    context, q/k normalised inside; sampled heads of O, the final state, every
+    gradient, d(logits) and d(gate_scale) against the oracle's gate followed by
+    its recurrence."""
+    import oracle
+    p = gdn_synth.make("varlen")
+    x, a = gdn_synth.gate_draws(p, seed=0)
+    d = p.to("cuda")
+    xg, ag = x.cuda(), a.cuda()
+    gdn = lib()
+    gdn.gdn_profile_begin()
+    o, fs, saved = gdn.chunk_gated_delta_rule_fwd(
+        d.q, d.k, d.v, xg, d.beta, initial_state=d.h0, output_final_state=True,
+        cu_seqlens=d.cu_seqlens, use_qk_l2norm=True, cp=p.meta["cp"], save_ctx=True,
+        gate_scale=ag)
+    dq, dk, dv, dx, db, dh0, da = gdn.chunk_gated_delta_rule_bwd(
+        d.q, d.k, d.v, xg, d.beta, d.do, dht=d.dht, initial_state=d.h0,
+        cu_seqlens=d.cu_seqlens, use_qk_l2norm=True, cp=p.meta["cp"], ctx=saved, gate_scale=ag)
+    torch.cuda.synchronize()
+    names = {n for n, _, _ in gdn.gdn_profile_end()}
+    assert gdn.gdn_sync_status(torch.cuda.current_stream().cuda_stream) == 0
+    assert {"tc_walk_fused", "tc_dwalk_fused", "tc_local_grad"} <= names, names
+    heads = [5, 22]
+    sub = sub_problem(p, heads=heads)
+    xs, as_ = x[:, :, heads].contiguous(), a[heads].contiguous()
+    g = oracle.gate(xs, as_)
+    ro, rfs = oracle.fwd(sub.q, sub.k, sub.v, g, sub.beta, h0=sub.h0, cu_seqlens=sub.cu_seqlens,
+                         use_l2norm=True)
+    r = oracle.bwd(sub.q, sub.k, sub.v, g, sub.beta, do=sub.do, h0=sub.h0, dht=sub.dht,
+                   cu_seqlens=sub.cu_seqlens, use_l2norm=True)
+    dx_ref, da_ref = oracle.gate_bwd(xs, as_, r["dg"])
+    tol = TOL["bf16"]
+    tok = lambda t: to_np(t)[:, :, heads]
+    check("gated o", tok(o), ro, tol)
+    check("gated final_state", to_np(fs)[:, heads], rfs, tol)
+    for nm, got in (("dq", dq), ("dk", dk), ("dv", dv), ("dbeta", db)):
+        check(f"gated {nm}", tok(got), r[nm], tol)
+    check("gated dh0", to_np(dh0)[:, heads], r["dh0"], tol)
+    check("gated d(logits)", tok(dx), dx_ref, tol)
+    # d a_h sums one head's per-token terms over n tokens: the per-element
+    # tolerance times sqrt(n)
+    check("gated d(gate_scale)", to_np(da)[heads], da_ref, tol * np.sqrt(x.shape[1]))
