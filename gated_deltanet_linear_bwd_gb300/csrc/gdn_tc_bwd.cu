@@ -443,15 +443,9 @@ tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
         if (warp == 0) {
             tc_fence_after();
             const uint32_t kt = smem_u32(s.k[st]), dhT = smem_u32(s.dhT);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t half = kk >> 2, sub = (kk & 3) * 32;
-                mma_bf16(t_x, desc_sw128(dhT + half * 2 * kTile + sub, 16, 1024),
-                         desc_sw128(kt + kKOff + half * kKHalf + sub, 16, 1024), kIdKK64, kk > 0);
-            }
-            mma_commit(&s.bar_x);
             if (fused) {
-                // [Q; K] K^T, rows 0-63 = Q K^T, on its own barrier
+                // [Q; K] K^T first, on its own barrier: the P epilogue that reads it
+                // comes before X^T's, which then completes under it
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t off = (kk >> 2) * kKHalf + (kk & 3) * 32;
@@ -459,7 +453,15 @@ tc_dwalk_kernel(const __grid_constant__ DWalkMaps m, Geo g, TcDWalkArgs a) {
                              desc_sw128(kt + kKOff + off, 16, 1024), kIdKK64, kk > 0);
                 }
                 mma_commit(&s.bar_q);
-            } else if (use_do) {
+            }
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t half = kk >> 2, sub = (kk & 3) * 32;
+                mma_bf16(t_x, desc_sw128(dhT + half * 2 * kTile + sub, 16, 1024),
+                         desc_sw128(kt + kKOff + half * kKHalf + sub, 16, 1024), kIdKK64, kk > 0);
+            }
+            mma_commit(&s.bar_x);
+            if (!fused && use_do) {
                 const uint32_t dO = smem_u32(s.dO[st]), qs = smem_u32(s.qs[st]);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
