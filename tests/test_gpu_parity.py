@@ -7,6 +7,7 @@ import pytest
 import torch
 
 import gdn_synth
+import oracle
 from gpu_helpers import (TOL, check, gpu_bwd, gpu_fwd, lib, oracle_bwd, oracle_fwd,
                          sub_problem, to_np)
 
@@ -279,3 +280,35 @@ def test_full_varlen_workload_sampled():
 
 def test_full_training_workload_sampled():
     sampled_units_check("training", heads=[1, 20], batches=[2], bwd=True)
+
+
+@pytest.mark.parametrize("name,kw,cp", [
+    ("tiny", dict(T=130, H=2), "off"),                   # CUDA-core path, fp32
+    ("training", dict(B=1, T=300, H=2), "off"),          # tensor cores: output and intra passes
+    ("training", dict(B=2, T=200, H=64), "off"),         # the fused walks
+    ("training", dict(B=1, T=640, H=2), "force"),        # sequence parallelism
+])
+def test_explicit_scale_matches_oracle(name, kw, cp):
+    """A caller's own `scale` (here 0.3 instead of K^-1/2) reaches every
+    product that carries it, forward and backward, with and without q/k
+    normalisation inside."""
+    gdn = lib()
+    p = gdn_synth.make(name, h0_std=0.1, dht_std=0.01, **kw)
+    d = p.to("cuda")
+    tol = TOL[gdn_synth.WORKLOADS[name]["dtype"]]
+    for l2 in (False, True):
+        o, fs = gdn.chunk_gated_delta_rule_fwd(d.q, d.k, d.v, d.g, d.beta, scale=0.3,
+                                               initial_state=d.h0, output_final_state=True,
+                                               use_qk_l2norm=l2, cp=cp)
+        dq, dk, dv, dg, db, dh0 = gdn.chunk_gated_delta_rule_bwd(
+            d.q, d.k, d.v, d.g, d.beta, d.do, dht=d.dht, scale=0.3, initial_state=d.h0,
+            use_qk_l2norm=l2, cp=cp)
+        torch.cuda.synchronize()
+        ro, rfs = oracle.fwd(p.q, p.k, p.v, p.g, p.beta, h0=p.h0, scale=0.3, use_l2norm=l2)
+        r = oracle.bwd(p.q, p.k, p.v, p.g, p.beta, do=p.do, h0=p.h0, dht=p.dht, scale=0.3,
+                       use_l2norm=l2)
+        check(f"o l2={l2}", to_np(o), ro, tol)
+        check(f"final_state l2={l2}", to_np(fs), rfs, tol)
+        for k, x in (("dq", dq), ("dk", dk), ("dv", dv), ("dg", dg), ("dbeta", db), ("dh0", dh0)):
+            check(f"{k} l2={l2}", to_np(x), r[k], tol)
+    assert gdn.gdn_sync_status(torch.cuda.current_stream().cuda_stream) == 0

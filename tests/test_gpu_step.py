@@ -16,7 +16,7 @@ from gpu_helpers import TOL, check, lib, to_np
 pytestmark = pytest.mark.gpu
 
 
-def _steps(p, l2=False, gate=None):
+def _steps(p, l2=False, gate=None, scale=None):
     d = p.to("cuda")
     state = (d.h0.clone() if d.h0 is not None
              else torch.zeros(p.B, p.H, p.K, p.V, device="cuda"))
@@ -26,7 +26,7 @@ def _steps(p, l2=False, gate=None):
         g = (xg if xg is not None else d.g)[:, t].contiguous()
         o = lib().recurrent_step(d.q[:, t].contiguous(), d.k[:, t].contiguous(),
                                  d.v[:, t].contiguous(), g, d.beta[:, t].contiguous(), state,
-                                 use_qk_l2norm=l2, gate_scale=ag)
+                                 use_qk_l2norm=l2, gate_scale=ag, scale=scale)
         outs.append(o)
     torch.cuda.synchronize()
     return to_np(torch.stack(outs, 1)), to_np(state)
@@ -103,3 +103,11 @@ def test_empty_batch_is_a_no_op():
     a.N, a.K = 2, 96
     assert _abi.load().gdn_recurrent_step(a, None) == _abi.GDN_ERR_UNSUPPORTED
     assert "96" in gdn.gdn_last_error()
+
+
+def test_steps_with_an_explicit_scale():
+    p = gdn_synth.make("training", B=3, T=5, H=4, h0_std=0.3)
+    o_ref, ht_ref = oracle.fwd(p.q, p.k, p.v, p.g, p.beta, h0=p.h0, scale=0.3, use_l2norm=True)
+    o, st = _steps(p, True, scale=0.3)
+    check("o (every step)", o, o_ref, TOL["bf16"])
+    check("state after the last step", st, ht_ref, TOL["bf16"])
