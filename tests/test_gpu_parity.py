@@ -312,3 +312,30 @@ def test_explicit_scale_matches_oracle(name, kw, cp):
         for k, x in (("dq", dq), ("dk", dk), ("dv", dv), ("dg", dg), ("dbeta", db), ("dh0", dh0)):
             check(f"{k} l2={l2}", to_np(x), r[k], tol)
     assert gdn.gdn_sync_status(torch.cuda.current_stream().cuda_stream) == 0
+
+
+@pytest.mark.parametrize("kw,cp", [
+    (dict(B=1, T=300, H=2), "off"),
+    (dict(B=2, T=200, H=64), "off"),         # fused walks
+    (dict(B=1, T=640, H=2), "force"),        # sequence parallelism
+])
+def test_optional_outputs_left_out(kw, cp):
+    """No final state asked of the forward, no d(initial state) of the backward,
+    no initial state and no d(final state) given: the outputs that are asked
+    for still match the oracle (which takes the missing states as zeros)."""
+    gdn = lib()
+    p = gdn_synth.make("training", **kw)
+    d = p.to("cuda")
+    o, fs = gdn.chunk_gated_delta_rule_fwd(d.q, d.k, d.v, d.g, d.beta, output_final_state=False,
+                                           cp=cp)
+    assert fs is None
+    dq, dk, dv, dg, db, dh0 = gdn.chunk_gated_delta_rule_bwd(
+        d.q, d.k, d.v, d.g, d.beta, d.do, cp=cp, want_dh0=False)
+    assert dh0 is None
+    torch.cuda.synchronize()
+    assert gdn.gdn_sync_status(torch.cuda.current_stream().cuda_stream) == 0
+    ro, _ = oracle.fwd(p.q, p.k, p.v, p.g, p.beta)
+    r = oracle.bwd(p.q, p.k, p.v, p.g, p.beta, do=p.do)
+    check("o", to_np(o), ro, TOL["bf16"])
+    for k, x in (("dq", dq), ("dk", dk), ("dv", dv), ("dg", dg), ("dbeta", db)):
+        check(k, to_np(x), r[k], TOL["bf16"])
