@@ -809,9 +809,10 @@ cudaError_t make_map_tiles(CUtensorMap *m, const void *base, long long rows_tota
 }
 
 bool supported(const Plan &p) {
-    // the chunk-tile TMA row coordinate (chunk * H + head) * 128 is a 32-bit int
+    // TMA row coordinates are 32-bit ints: the largest, of the chunk-state tiles
+    // (two 128-row halves per (chunk, head)), is 2 (chunk * H + head) * 128 + 128
     return p.dtype == GDN_BF16 && p.g.K == kD && p.g.V == kD && (long long)p.g.B * p.g.T > 0 &&
-           (long long)p.max_chunks * p.g.H * kD < (1ll << 31);
+           (long long)p.max_chunks * p.g.H * 2 * kD + kD < (1ll << 31);
 }
 
 // Prep, then the walk: with output (states_only = false) or storing every

@@ -188,3 +188,15 @@ def test_saved_context_keeps_the_forward_maps_under_forced_sequence_parallelism(
     assert off == auto
     assert force - off == maps(64)
     assert fixed - off == maps(8192 // 64 // 16)
+
+
+def test_tensor_core_path_only_where_its_tma_coordinates_fit(abi):
+    """The tensor-core path addresses the per-(chunk, head) state tiles with 32-bit
+    TMA row coordinates up to 2 (chunk * H + head) * 128 + 128; a problem whose
+    coordinates would not fit takes the CUDA-core path (which keeps no saved
+    context), one chunk-head below the limit still takes the tensor cores."""
+    limit = (2 ** 31 - 128) // 256          # chunk-heads the coordinates allow
+    below = _fwd_args(abi, dtype=abi.GDN_BF16, K=128, V=128, B=1, H=1, T=64 * (limit - 1))
+    above = _fwd_args(abi, dtype=abi.GDN_BF16, K=128, V=128, B=1, H=1, T=64 * (limit + 1))
+    assert abi.gdn_fwd_ctx_size(below) > 0
+    assert abi.gdn_fwd_ctx_size(above) == 0
