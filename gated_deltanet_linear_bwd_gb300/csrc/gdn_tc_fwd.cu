@@ -637,11 +637,33 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             st_row8(s.uTs, v, chunk, uu);
             if (fused) st_row8(s.uT, v, chunk, x);
         }
+        // The state update's product Uᵀdiag(f) K and (fused) H^T Q^T need only the U
+        // epilogue's tiles: in the output walk warp 2, which has no P rows, issues
+        // them at once, so that they run under the P epilogue, and U^T P^T after it,
+        // all on bar_dh; otherwise warp 0 issues the product after the barrier.
         if (fused) {
+            tc_fence_before();
+            fence_proxy_async();                  // the U epilogue's tiles, for the products
             ok = mbar_wait(&s.bar_q, par, g.spin_limit, g.status);
             if (__syncthreads_or(!ok)) { bailed = true; break; }
             pend &= ~4;
             tc_fence_after();
+            if (warp == 2) {
+                const uint32_t uTs = smem_u32(s.uTs), kt = smem_u32(s.k[st]) + kKOff;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(t_dh, desc_sw128(uTs + kk * 32, 16, 1024),
+                             desc_sw128(kt + kk * 2048, kKHalf, 1024), kIdescDH, kk > 0);
+                // H^T Q^T (this chunk's start state, which the state update
+                // overwrites only after bar_dh)
+                const uint32_t hT = smem_u32(s.hT), qk = smem_u32(s.k[st]);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (kk >> 2) * kKHalf + (kk & 3) * 32;
+                    mma_bf16(t_qh(gb), desc_sw128(hT + (kk >> 2) * 2 * kTile + (kk & 3) * 32, 16, 1024),
+                             desc_sw128(qk + off, 16, 1024), kIdescKK64, kk > 0);
+                }
+            }
         }
         if (fused && v < 64) {
             // row r = v of P: Q K^T on lanes 0-63, masked to c <= r < L, times D_rc
@@ -666,31 +688,21 @@ tc_walk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         tc_fence_before();
         fence_proxy_async();
         __syncthreads();
-        if (warp == 0) {
+        if (warp == (fused ? 2 : 0)) {
             tc_fence_after();
-            const uint32_t uTs = smem_u32(s.uTs), kt = smem_u32(s.k[st]) + kKOff;
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t au = desc_sw128(uTs + kk * 32, 16, 1024);
-                const uint64_t bk = desc_sw128(kt + kk * 2048, kKHalf, 1024);   // K, MN-major
-                mma_bf16(t_dh, au, bk, kIdescDH, kk > 0);
-            }
             if (fused) {
-                // U^T P^T: both operands K-major over the chunk rows; H^T Q^T (this
-                // chunk's start state, which the state update overwrites only after
-                // this group completes)
+                // U^T P^T: both operands K-major over the chunk rows
                 const uint32_t ua = smem_u32(s.uT), pp = smem_u32(s.p);
-                const uint32_t hT = smem_u32(s.hT), qk = smem_u32(s.k[st]);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     mma_bf16(t_pu(gb), desc_sw128(ua + kk * 32, 16, 1024),
                              desc_sw128(pp + kk * 32, 16, 1024), kIdescKK64, kk > 0);
+            } else {
+                const uint32_t uTs = smem_u32(s.uTs), kt = smem_u32(s.k[st]) + kKOff;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t off = (kk >> 2) * kKHalf + (kk & 3) * 32;
-                    mma_bf16(t_qh(gb), desc_sw128(hT + (kk >> 2) * 2 * kTile + (kk & 3) * 32, 16, 1024),
-                             desc_sw128(qk + off, 16, 1024), kIdescKK64, kk > 0);
-                }
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(t_dh, desc_sw128(uTs + kk * 32, 16, 1024),
+                             desc_sw128(kt + kk * 2048, kKHalf, 1024), kIdescDH, kk > 0);
             }
             mma_commit(&s.bar_dh);
         }
